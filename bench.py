@@ -1,0 +1,493 @@
+#!/usr/bin/env python3
+"""Throughput of the packed, padding-free (bi)LSTM forward + BPTT on GB300.
+
+One step = pack (x and the upstream gradient) -> forward of every layer ->
+BPTT of every layer -> unpack (y and dx), on one batch of synthetic
+sequences already resident in HBM.  The metric counts non-padded frames:
+N = sum of the sequence lengths per step (no padded frame is computed).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload k] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  With --gpus N > 1 (torchrun) every rank runs
+an independent replica of the workload (weak scaling, no collective on the
+data path); the time is the maximum over ranks.
+
+Timing: CUDA events on the stream the library launches on, one pair per
+step; L2 is flushed (a 512 MiB write) before every timed step, outside the
+events.  SM clocks and throttle reasons are sampled with nvidia-smi during
+the timed loop.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "non-padded frames/sec LSTM fwd+bwd (1 GB300); % of GEMM/SMEM roofline"
+UNIT = "frames/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0, "source": "fallback"}
+NUM_SMS = 152
+FP32_LANES_PER_SM = 128
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        p["source"] = "measured"
+        return p
+    except Exception:
+        return dict(FALLBACK_PEAKS)
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.25)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"error": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) == len(self.FIELDS):
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"error": "no samples"}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            for name, v in zip(names, r[4:]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def gpu_index(local_rank: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_rank < len(ids) and ids[local_rank].isdigit():
+            return int(ids[local_rank])
+    return local_rank
+
+
+# --------------------------------------------------------------------------- algorithmic work
+
+def kind_work(kind: str, spec, rows: int, D0: int, uses_tensor: dict):
+    """Algorithmic (flops, HBM bytes) of one step's launches of `kind`, summed over layers."""
+    H, nd, e = spec.hidden_size, spec.num_directions, (2 if spec.dtype == "bf16" else 4)
+    fl = by = 0.0
+    for l in range(spec.num_layers):
+        D = D0 if l == 0 else nd * H
+        ex = e if l == 0 or spec.dtype == "bf16" else 4
+        G4 = nd * 4 * H
+        if kind == "input_gemm":
+            fl += 2.0 * rows * D * G4
+            by += rows * D * ex + G4 * D * e + rows * G4 * 4
+        elif kind == "rec_fwd":
+            fl += 8.0 * rows * H * H * nd
+            by += 2 * rows * G4 * 4 + 2 * rows * nd * H * 4 + nd * 4 * H * H * e
+        elif kind == "rec_bwd":
+            fl += 8.0 * rows * H * H * nd
+            by += 2 * rows * G4 * 4 + 3 * rows * nd * H * 4 + nd * 4 * H * H * e
+        elif kind == "gemm_dx":
+            fl += 2.0 * rows * G4 * D
+            by += rows * G4 * 4 + G4 * D * e + rows * D * 4
+        elif kind == "gemm_dw":
+            fl += 2.0 * rows * G4 * D
+            by += rows * G4 * 4 + rows * D * ex + G4 * D * 4
+        elif kind == "gemm_dr":
+            fl += 2.0 * rows * 4 * H * H * nd
+            by += rows * G4 * 4 + rows * nd * H * 4 + nd * 4 * H * H * 4
+    if kind == "pack":
+        fl, by = 0.0, 2.0 * rows * (D0 * e + nd * H * 4)
+    elif kind == "unpack":
+        fl, by = 0.0, 2.0 * rows * (nd * H + D0) * 4
+    return fl, by
+
+
+def roofline_of(kind, ms_per_step, calls_per_step, spec, rows, D0, peaks, sustained):
+    fl, by = kind_work(kind, spec, rows, D0, {})
+    sec = ms_per_step / 1e3
+    clk = float(peaks.get("sm_max_mhz", 2070.0))
+    alu_peak = NUM_SMS * FP32_LANES_PER_SM * 2 * clk * 1e6 / 1e12          # TFLOP/s, CUDA-core FFMA
+    hbm_peak = float(peaks["hbm_gbs"])                                        # GB/s
+    t_alu = fl / (alu_peak * 1e12) if fl else 0.0
+    t_hbm = by / (hbm_peak * 1e9)
+    if t_alu >= t_hbm:
+        ach = fl / sec / 1e12 if sec > 0 else 0.0
+        return {"kernel": kind, "bound": "alu", "achieved": round(ach, 3), "peak": round(alu_peak, 1),
+                "unit": "TFLOP/s", "frac": round(ach / alu_peak, 4),
+                "per_launch": {"flops": fl / max(1, calls_per_step), "ms": ms_per_step / max(1, calls_per_step)}}
+    ach = by / sec / 1e9 if sec > 0 else 0.0
+    return {"kernel": kind, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(ach / hbm_peak, 4),
+            "per_launch": {"bytes": by / max(1, calls_per_step), "ms": ms_per_step / max(1, calls_per_step)}}
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "padding_free_variable_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kind: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    ent = rec.get(kind)
+    if not ent or ent.get("source_digest") != source_digest() or ent.get("workload") != workload:
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------------- CPU oracle arm
+
+def oracle_sample(w, seconds: float, nthreads: int):
+    """Sequences (caller order) forming a sample of about `seconds` of oracle work."""
+    import oracle
+    st = np.concatenate([[0], np.cumsum(w.lengths)])
+    # calibrate on the shortest non-empty sequence
+    cand = [int(i) for i in np.argsort(w.lengths, kind="stable") if w.lengths[i] > 0]
+    i0 = cand[0]
+    t0 = time.perf_counter()
+    oracle.lstm_stack(w.lengths[[i0]], w.x[st[i0]:st[i0 + 1]], w.layers, w.spec.num_directions,
+                      w.spec.hidden_size, G=w.G[st[i0]:st[i0 + 1]], nthreads=1)
+    per_frame = (time.perf_counter() - t0) / max(1, int(w.lengths[i0]))
+    budget_frames = seconds * nthreads / max(per_frame, 1e-9)
+    seqs, frames = [], 0
+    for i in range(len(w.lengths)):
+        if w.lengths[i] == 0:
+            continue
+        if seqs and frames + w.lengths[i] > budget_frames:
+            break
+        seqs.append(i)
+        frames += int(w.lengths[i])
+    return seqs, frames
+
+
+def run_oracle_on(w, seqs, nthreads):
+    import oracle
+    st = np.concatenate([[0], np.cumsum(w.lengths)])
+    x = np.concatenate([w.x[st[s]:st[s + 1]] for s in seqs])
+    G = np.concatenate([w.G[st[s]:st[s + 1]] for s in seqs])
+    t0 = time.perf_counter()
+    oracle.lstm_stack(w.lengths[seqs], x, w.layers, w.spec.num_directions, w.spec.hidden_size, G=G,
+                      nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, seconds=15.0):
+    import oracle
+    oracle.build()
+    nthreads = os.cpu_count() or 1
+    seqs, frames = oracle_sample(w, seconds, nthreads)
+    dt = run_oracle_on(w, seqs, nthreads)
+    return {"value": round(frames / dt, 2), "unit": UNIT, "cores": nthreads, "kind": "oracle",
+            "sample": f"{len(seqs)} of {len(w.lengths)} sequences ({frames} frames), fwd+BPTT of every layer, "
+                      f"fp64, OpenMP over sequences, {dt:.1f} s"}
+
+
+def reference_arm(args, w, config):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    nthreads = os.cpu_count() or 1
+    per_step = max(0.5, 150.0 / max(1, args.steps + args.warmup))
+    seqs, frames = oracle_sample(w, per_step, nthreads)
+    for _ in range(args.warmup):
+        run_oracle_on(w, seqs, nthreads)
+    times = [run_oracle_on(w, seqs, nthreads) for _ in range(args.steps)]
+    total = sum(times)
+    value = frames * args.steps / total
+    out = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+           "config": dict(config, sample_frames_per_step=frames),
+           "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": nthreads, "kind": "oracle",
+                            "sample": f"{len(seqs)} of {len(w.lengths)} sequences ({frames} frames) per step"},
+           "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+    return 0
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--no-comparators", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    from padding_free_variable_gb300 import synthetic
+    w = synthetic.workload(args.workload)
+    spec = w.spec
+    N, T, B = w.N, w.T, len(w.lengths)
+    config = {"workload": spec.name, "sequences": B, "frames_per_step": N, "max_length": T,
+              "input_size": spec.input_size, "hidden_size": spec.hidden_size, "layers": spec.num_layers,
+              "directions": spec.num_directions, "gemm_operands": spec.dtype, "state": "f32",
+              "lengths": str(spec.lengths), "seed": w.seed, "l2": "flushed (512 MiB write) before every timed step",
+              "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+    if args.impl == "reference":
+        return reference_arm(args, w, config)
+
+    import torch
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    from padding_free_variable_gb300 import build as native, ops
+    if rank == 0:
+        native.build()
+    if dist:
+        dist.barrier()
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from gpu_harness import device_layers
+
+    bf16 = spec.dtype == "bf16"
+    xdt = torch.bfloat16 if bf16 else torch.float32
+    plan = ops.Plan(w.lengths)
+    stack = ops.PackedLSTMStack(plan, device_layers(w), spec.input_size, spec.hidden_size,
+                                spec.num_directions, bf16)
+    x_dev = torch.from_numpy(w.x).to("cuda", dtype=xdt)
+    G_dev = torch.from_numpy(w.G).cuda()
+    y_cat = torch.empty((N, spec.num_directions * spec.hidden_size), device="cuda")
+    dx_cat = torch.empty((N, spec.input_size), device="cuda")
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        plan.pack(x_dev, stack.x_packed)
+        plan.pack(G_dev, stack.dy_packed)
+        stack.forward_packed()
+        stack.backward_packed()
+        plan.unpack(stack.y[-1], y_cat)
+        plan.unpack(stack.dx[0], dx_cat)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = plan.poll()
+    if st != 0:
+        raise RuntimeError(f"device status {st} during warm-up")
+
+    # ---- timed region: K steps, per-step events, L2 flushed before each
+    sampler = ClockSampler(gpu_index(local_rank))
+    sampler.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = plan.launch_count()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    launches = plan.launch_count() - launches0
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if plan.poll() != 0:
+        raise RuntimeError("device status set during the timed region")
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * N * args.steps / (total_ms / 1e3)
+
+    # ---- per-kernel times (separate traced pass) for the roofline
+    peaks = load_peaks()
+    plan.enable_timing(True)
+    traced = max(3, min(20, args.steps))
+    for _ in range(traced):
+        flush.fill_(0.0)
+        step()
+    tim = plan.read_timing()
+    plan.enable_timing(False)
+    kernels = {}
+    for kind, (ms, calls) in tim.items():
+        if calls:
+            r = roofline_of(kind, ms / traced, calls / traced, spec, plan.rows, spec.input_size, peaks, False)
+            r["ms_per_step"] = round(ms / traced, 4)
+            kernels[kind] = r
+    dom = max(kernels.values(), key=lambda r: r["ms_per_step"])
+    roof = {k: dom[k] for k in ("bound", "achieved", "peak", "unit", "frac")}
+    roof["kernel"] = dom["kernel"]
+    roof["peak_source"] = ("derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock"
+                           if dom["bound"] == "alu" else f"MEASURED_PEAKS.json ({peaks.get('source')})")
+    roof["traffic"] = recorded_traffic(dom["kernel"], spec.name)
+    recurrent = {}
+    # per-step phases of the recurrent kernels from in-kernel clock64 stamps (CTA 0, direction 0)
+    tsteps = min(T, 4096)
+    tbuf = torch.zeros(2 * spec.num_directions * tsteps * 8, dtype=torch.int64, device="cuda")
+    plan.trace_steps(tbuf, tsteps)
+    step()
+    torch.cuda.synchronize()
+    plan.trace_steps(None, 0)
+    stamps = tbuf.view(2, spec.num_directions, tsteps, 8).cpu().numpy().astype(np.float64)
+    mhz = (clocks.get("sm_mhz") if isinstance(clocks, dict) else None) or float(peaks.get("sm_max_mhz", 2070.0))
+    for kname, ki in (("fwd", 0), ("bwd", 1)):
+        d = stamps[ki, 0]
+        if not d[:, 0].any():
+            continue
+        us = lambda cyc: round(float(np.median(cyc)) / mhz, 3)
+        recurrent[f"phases_us_{kname}"] = {
+            "barrier_wait": us(d[1:, 1] - d[1:, 0]), "stage_exchange": us(d[:, 2] - d[:, 1]),
+            "compute_cell": us(d[:, 3] - d[:, 2]), "publish": us(d[:, 4] - d[:, 3]),
+            "step": us(d[1:, 0] - d[:-1, 0]), "clock_mhz": mhz, "cta": 0, "direction": 0}
+    if "rec_fwd" in kernels:
+        recurrent["us_per_step_fwd"] = round(1e3 * kernels["rec_fwd"]["ms_per_step"] / (T * spec.num_layers), 3)
+    if "rec_bwd" in kernels:
+        recurrent["us_per_step_bwd"] = round(1e3 * kernels["rec_bwd"]["ms_per_step"] / (T * spec.num_layers), 3)
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    x_host = torch.from_numpy(w.x).to(xdt).pin_memory()
+    G_host = torch.from_numpy(w.G).pin_memory()
+    y_host = torch.empty(tuple(y_cat.shape), dtype=torch.float32).pin_memory()
+    dx_host = torch.empty(tuple(dx_cat.shape), dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 30))
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        flush.fill_(float(i))
+        es[i].record(stream)
+        x_dev.copy_(x_host, non_blocking=True)
+        G_dev.copy_(G_host, non_blocking=True)
+        step()
+        y_host.copy_(y_cat, non_blocking=True)
+        dx_host.copy_(dx_cat, non_blocking=True)
+        ee[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(es, ee))
+    e2e = {"value": round(world * N * e2e_steps / (e2e_ms / 1e3), 2), "unit": UNIT,
+           "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size() + G_host.numel() * 4),
+           "d2h_bytes_per_step": int(y_host.numel() * 4 + dx_host.numel() * 4)}
+
+    # ---- comparator: the same kernels on the zero-padded batch (masked)
+    comparators = {}
+    if not args.no_comparators and rank == 0:
+        pplan = ops.Plan(w.lengths, padded=True)
+        pstack = ops.PackedLSTMStack(pplan, stack.layers, spec.input_size, spec.hidden_size,
+                                     spec.num_directions, bf16)
+        psteps = max(3, min(10, args.steps))
+
+        def pstep():
+            pplan.pack(x_dev, pstack.x_packed)
+            pplan.pack(G_dev, pstack.dy_packed)
+            pstack.forward_packed()
+            pstack.backward_packed()
+            pplan.unpack(pstack.y[-1], y_cat)
+            pplan.unpack(pstack.dx[0], dx_cat)
+        pstep()
+        torch.cuda.synchronize()
+        ps = [torch.cuda.Event(enable_timing=True) for _ in range(psteps)]
+        pe = [torch.cuda.Event(enable_timing=True) for _ in range(psteps)]
+        for i in range(psteps):
+            flush.fill_(float(i))
+            ps[i].record(stream)
+            pstep()
+            pe[i].record(stream)
+        torch.cuda.synchronize()
+        pms = sum(s.elapsed_time(e) for s, e in zip(ps, pe)) / psteps
+        comparators["zero_padded"] = {"frames_per_s": round(N / (pms / 1e3), 2), "ms_per_step": round(pms, 3),
+                                      "computed_frames": int(B * T),
+                                      "waste_fraction": round((B * T - N) / (B * T), 4),
+                                      "zero_padding_rate": round((B * T - N) / N, 4)}
+        del pstack, pplan
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        out = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+               "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "bf16-operands/f32" if bf16 else "f32",
+               "data": "synthetic", "config": config, "clocks": clocks, "e2e": e2e, "gpu_launches": int(launches),
+               "roofline": roof, "cpu_baseline": cpu, "kernels": kernels, "recurrent": recurrent,
+               "comparators": comparators, "wall_s_timed_region": round(wall, 3),
+               "step_ms": {"min": round(min(step_ms), 4), "median": round(statistics.median(step_ms), 4),
+                           "max": round(max(step_ms), 4)}}
+        print(json.dumps(out))
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,301 @@
+/*
+ * lstm_packed.h -- C ABI of the padding-free (bi)LSTM library for sm_103a.
+ *
+ * The library computes the forward pass and the BPTT backward pass of LSTM
+ * layers with forget gates and peephole connections over a batch of
+ * variable-length sequences without computing any padded frame.
+ *
+ * Sources for what is computed:
+ *  - "No Padding Please: Efficient Neural Handwriting Recognition", Sec. V
+ *    (example-packing) and Appendix B (Algorithm 1): a list of variable-size
+ *    examples is packed, the layer runs on the packed tensor, and unpacking
+ *    extracts each example's activations with the original example indices.
+ *    Here the packing is the one-dimensional form: sequences are sorted by
+ *    length (longest first, ties keep the caller's order) and laid out time
+ *    major, so the rows of time step t are the first bs[t] sorted sequences.
+ *  - "Single Stream Parallelization of Generalized LSTM-Like RNNs on a GPU",
+ *    Sec. 2-3 and Fig. 1: the LSTM with forget gates and peepholes built from
+ *    additive and multiplicative layers, its BPTT training equations, and the
+ *    split into a non-recurrent part computed in parallel over all frames and
+ *    a recurrent part computed step by step.
+ *  - RETURNN paper, Sec. 4.2: the non-recurrent part of the forward pass is
+ *    one matrix product over the whole batch of sequences, and so are the
+ *    weight and input gradients after the recurrent part has been
+ *    back-propagated; the gating runs in custom kernels.
+ *
+ * The cell (one direction; the page's equations were lost, this is the
+ * standard reading of its graph):
+ *     a_t = W x_t + R h_{t-1} + b          gate blocks (i, f, z, o) along 4H
+ *     i = sig(a_i + p_i c_{t-1}),  f = sig(a_f + p_f c_{t-1}),  z = tanh(a_z)
+ *     c_t = f c_{t-1} + i z,   o = sig(a_o + p_o c_t),   h_t = o tanh(c_t)
+ * with h_0 = c_0 = 0.  The reverse direction runs its own cell over
+ * x_L..x_1; its output at position t is its state after consuming x_t.
+ *
+ * Conventions shared by every entry point:
+ *  - All device buffers are allocated, owned and freed by the caller.  The
+ *    library owns only what lstm_plan_create allocates (small index tables,
+ *    step flags and a status word), freed by lstm_plan_destroy.
+ *  - Every call is asynchronous on the caller's CUDA stream, passed as
+ *    `void* stream` (a cudaStream_t; NULL = legacy default stream).  A plan
+ *    may be used by one stream at a time and must outlive its queued work.
+ *  - Arguments are validated on the host before anything is launched; a
+ *    rejected call launches nothing and returns LSTM_ERR_INVALID_ARG (bad
+ *    pointer, size or alignment) or LSTM_ERR_UNSUPPORTED (a shape or device
+ *    the kernels do not cover).  LSTM_ERR_CUDA reports a failed CUDA call.
+ *  - Device-side failures (a step barrier that waited longer than the
+ *    plan's limit, an index out of range) are recorded in the plan's device
+ *    status word; kernels then stop early instead of hanging or trapping.
+ *    lstm_status_poll reads and clears it.
+ *  - Row-major everywhere.  Packed tensors have N = sum of lengths rows in
+ *    the packed order; "cat" tensors have N rows in the caller's order
+ *    (sequence 0's frames, then sequence 1's, ...).
+ *  - Pointers to device arrays must be 16-byte aligned.
+ *  - Nothing throws across this boundary.
+ */
+#ifndef LSTM_PACKED_H
+#define LSTM_PACKED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LSTM_OK = 0,
+    LSTM_ERR_INVALID_ARG = 1,
+    LSTM_ERR_UNSUPPORTED = 2,
+    LSTM_ERR_CUDA = 3,
+    LSTM_ERR_TIMEOUT = 4,   /* a per-step barrier wait ran past the plan's limit */
+    LSTM_ERR_BOUNDS = 5     /* a kernel found an index outside its buffer */
+} lstm_status;
+
+/* Element type of the GEMM operands x, W and R.  Biases, peepholes, states,
+ * gates, outputs and all gradients are fp32 in both cases.  With LSTM_BF16
+ * the products W x, R h, and the gradient products take bf16 operands
+ * (h and the gate errors are rounded to bf16 before they enter a product)
+ * and accumulate in fp32. */
+typedef enum { LSTM_F32 = 0, LSTM_BF16 = 1 } lstm_dtype;
+
+typedef struct lstm_plan lstm_plan;
+
+typedef struct {
+    int32_t input_size;      /* D: width of one input frame, >= 1 */
+    int32_t hidden_size;     /* H: units per direction, multiple of 8, 8..2048 */
+    int32_t num_directions;  /* 1 (forward only) or 2 (forward and reverse) */
+    int32_t dtype;           /* lstm_dtype of x, W and R */
+} lstm_layer_shape;
+
+/* Parameters of one layer, device pointers, ndir = num_directions:
+ *   W    [ndir][4H][D]   dtype   input weights, gate blocks (i, f, z, o)
+ *   R    [ndir][4H][H]   dtype   recurrent weights, same blocks
+ *   b    [ndir][4H]      fp32    one bias per gate unit
+ *   peep [ndir][3][H]    fp32    diagonal peepholes p_i, p_f, p_o           */
+typedef struct {
+    const void*  W;
+    const void*  R;
+    const float* b;
+    const float* peep;
+} lstm_layer_params;
+
+/* Gradients of one layer, fp32, same shapes as lstm_layer_params.
+ * Each is overwritten (not accumulated). */
+typedef struct {
+    float* dW;
+    float* dR;
+    float* db;
+    float* dpeep;
+} lstm_layer_grads;
+
+/*
+ * Build the packing plan of one batch ("No Padding Please", Sec. V-A and
+ * Algorithm 1: bucket and order the examples, keep the original example
+ * indices; here a stable sort by decreasing length).
+ *   lengths_host[B]  frames per sequence, each >= 0 (host memory, read only
+ *                    during the call); B >= 1; sum <= 2^31 - 1.
+ *   out              receives the plan.
+ * Allocates the plan's device tables with cudaMalloc and uploads them
+ * synchronously on the current device.
+ */
+lstm_status lstm_plan_create(const int32_t* lengths_host, int32_t B, lstm_plan** out);
+
+/*
+ * The padded comparator's plan: the same batch laid out as a right-padded
+ * time x batch grid (RETURNN paper, Sec. 5: an index tensor marks which
+ * frames of the time x batch tensor belong to a sequence; "No Padding
+ * Please", Sec. V: a binary mask blocks state input from padding cells).
+ * Every one of the T_max steps runs all B sequences in the caller's order;
+ * frames past a sequence's end are computed and then masked: their state
+ * and output are set to zero, and they pass no gradient.  Packed buffers of
+ * this plan have B * T_max rows.
+ */
+lstm_status lstm_plan_create_padded(const int32_t* lengths_host, int32_t B, lstm_plan** out);
+
+/*
+ * Host-only form of the plan (no device, no allocation): the tables
+ * lstm_plan_create uploads.  lstm_plan_dims gives the sizes to allocate:
+ * steps T and rows (N packed, or B*T padded).  lstm_plan_compute_host fills
+ * every non-NULL output:
+ *   batch_sizes[T]  active rows of step t
+ *   offsets[T+1]    first row of step t
+ *   perm[B]         caller index of the sequence in slot j (longest first;
+ *                   equal lengths keep the caller's order)
+ *   slot_len[B]     its length
+ *   row_src[rows]   caller-order frame of each row (-1: padding row)
+ *   prev_fwd[rows]  row holding the forward direction's h_{t-1} (-1: none)
+ *   prev_rev[rows]  row holding the reverse direction's state of step t+1
+ *                   (-1: the sequence starts there)
+ * padded != 0 gives the padded comparator's tables.
+ */
+lstm_status lstm_plan_dims(const int32_t* lengths_host, int32_t B, int32_t padded, int32_t* steps,
+                           int64_t* rows);
+lstm_status lstm_plan_compute_host(const int32_t* lengths_host, int32_t B, int32_t padded,
+                                   int32_t* batch_sizes, int32_t* offsets, int32_t* perm,
+                                   int32_t* slot_len, int32_t* row_src, int32_t* prev_fwd,
+                                   int32_t* prev_rev);
+
+/* Free the plan and its device tables.  NULL is accepted. */
+lstm_status lstm_plan_destroy(lstm_plan* plan);
+
+/* Sizes of the plan: rows of a packed tensor (N, or B*T_max when padded),
+ * number of steps T (the longest length), batch B, sum of lengths. */
+lstm_status lstm_plan_info(const lstm_plan* plan, int64_t* rows, int32_t* steps, int32_t* batch,
+                           int64_t* frames);
+
+/* Host copies of the plan's tables, owned by the plan:
+ *   batch_sizes[T]  rows of step t (the active sequences)
+ *   offsets[T+1]    first packed row of step t
+ *   perm[B]         caller index of the sequence in sorted slot j
+ *   slot_len[B]     length of the sequence in slot j                         */
+lstm_status lstm_plan_tables(const lstm_plan* plan, const int32_t** batch_sizes,
+                             const int32_t** offsets, const int32_t** perm,
+                             const int32_t** slot_len);
+
+/* Set the barrier wait limit in nanoseconds (default 2 s).  A step whose
+ * barrier waits longer records LSTM_ERR_TIMEOUT and the kernel returns. */
+lstm_status lstm_plan_set_wait_limit(lstm_plan* plan, uint64_t nanoseconds);
+
+/*
+ * Bytes of the per-layer workspace that lstm_fwd fills and lstm_bwd reads
+ * (the saved activations of BPTT: gate activations [rows][ndir*4H] and cell
+ * states [rows][ndir*H], fp32).  lstm_bwd overwrites the gate part with the
+ * gate errors.  0 on a bad argument.
+ */
+size_t lstm_workspace_bytes(const lstm_plan* plan, const lstm_layer_shape* shape);
+
+/* Bytes of the transient scratch lstm_bwd needs: the recurrent kernel's
+ * exchange of partial products R^T da between CTAs, and (reusing the same
+ * bytes afterwards) the split-K partial sums of the weight-gradient
+ * products.  Depends on the plan's CTA count: size it after
+ * lstm_plan_set_ctas_per_direction.  0 on a bad argument. */
+size_t lstm_scratch_bytes(const lstm_plan* plan, const lstm_layer_shape* shape);
+
+/*
+ * Pack ("No Padding Please", Sec. V-A): x_packed[row] = x_cat[source(row)]
+ * for every packed row; rows of the padded plan past a sequence's end are
+ * zero-filled.
+ *   x_cat     [frames][width] elements of elem_bytes (2 or 4) in caller order
+ *   x_packed  [rows][width]
+ * width * elem_bytes must be a multiple of 16.
+ */
+lstm_status lstm_pack(const lstm_plan* plan, const void* x_cat, int32_t width, int32_t elem_bytes,
+                      void* x_packed, void* stream);
+
+/*
+ * Unpack ("No Padding Please", Sec. V-A: extract each example's activations
+ * using the original example indices): y_cat[source(row)] = y_packed[row];
+ * padding rows are dropped.  Exact inverse of lstm_pack (bitwise).
+ */
+lstm_status lstm_unpack(const lstm_plan* plan, const void* y_packed, int32_t width,
+                        int32_t elem_bytes, void* y_cat, void* stream);
+
+/*
+ * Forward pass of one layer ("Single Stream Parallelization...", Sec. 3:
+ * the non-recurrent part over all frames at once, then the recurrent part
+ * step by step; RETURNN, Sec. 4.2).
+ *   x_packed   [rows][D] dtype         layer input in packed order
+ *   y_packed   [rows][ndir*H] fp32     output [h_fwd | h_rev] per row
+ *   y_lo       [rows][ndir*H] bf16     optional bf16 copy of y (the next
+ *                                      bf16 layer's input); NULL to skip
+ *   h_n, c_n   [ndir][B][H] fp32       final states in caller order (zero
+ *                                      for empty sequences); NULL to skip
+ *   workspace  lstm_workspace_bytes    saved activations for lstm_bwd
+ */
+lstm_status lstm_fwd(const lstm_plan* plan, const lstm_layer_shape* shape,
+                     const lstm_layer_params* params, const void* x_packed, float* y_packed,
+                     void* y_lo, float* h_n, float* c_n, void* workspace, void* stream);
+
+/*
+ * BPTT of one layer ("Single Stream Parallelization...", Sec. 3; RETURNN,
+ * Sec. 4.2: the weight and input gradients as single products after the
+ * recurrent part is back-propagated through time).
+ *   x_packed, y_packed, workspace   as left by lstm_fwd of this layer
+ *   dy_packed  [rows][ndir*H] fp32  dL/dy of this layer (read only)
+ *   dx_packed  [rows][D] fp32       dL/dx, overwritten; NULL to skip
+ *   grads                           overwritten
+ *   scratch    lstm_scratch_bytes
+ */
+lstm_status lstm_bwd(const lstm_plan* plan, const lstm_layer_shape* shape,
+                     const lstm_layer_params* params, const void* x_packed,
+                     const float* y_packed, void* workspace, const float* dy_packed,
+                     float* dx_packed, const lstm_layer_grads* grads, void* scratch,
+                     void* stream);
+
+/* Synchronise the stream, then return and clear the plan's device status
+ * word (LSTM_OK, LSTM_ERR_TIMEOUT or LSTM_ERR_BOUNDS). */
+lstm_status lstm_status_poll(lstm_plan* plan, void* stream);
+
+/* Static description of a status code. */
+const char* lstm_status_string(lstm_status status);
+
+/* Number of CTAs per direction of the recurrent kernels (0 = automatic:
+ * one CTA while a step's product is small, otherwise one per SM).  Each
+ * CTA owns ceil(H / ctas) units; the count is capped at the SMs available. */
+lstm_status lstm_plan_set_ctas_per_direction(lstm_plan* plan, int32_t ctas);
+
+/* Kinds of launch the plan's tracer times. */
+typedef enum {
+    LSTM_KERNEL_PACK = 0,       /* lstm_pack gather */
+    LSTM_KERNEL_UNPACK = 1,     /* lstm_unpack scatter */
+    LSTM_KERNEL_INPUT_GEMM = 2, /* forward: X W^T + b for both directions */
+    LSTM_KERNEL_REC_FWD = 3,    /* forward: persistent recurrent kernel */
+    LSTM_KERNEL_REC_BWD = 4,    /* backward: persistent BPTT kernel */
+    LSTM_KERNEL_GEMM_DX = 5,    /* backward: dX = dA W */
+    LSTM_KERNEL_GEMM_DW = 6,    /* backward: dW = dA^T X (with its split-K sum) */
+    LSTM_KERNEL_GEMM_DR = 7,    /* backward: dR = dA^T H_prev (with its split-K sum) */
+    LSTM_KERNEL_KINDS = 8
+} lstm_kernel_kind;
+
+/* Tracing ("CUDA events around each launch"): with timing enabled every
+ * launch sequence of the plan is bracketed by two CUDA events on the
+ * caller's stream.  Enabling (or disabling) clears the sums.
+ * lstm_plan_read_timing waits for the recorded events and returns, per
+ * kind, the summed milliseconds and the number of timed calls (either
+ * array may be NULL; each has LSTM_KERNEL_KINDS entries). */
+lstm_status lstm_plan_enable_timing(lstm_plan* plan, int32_t enable);
+lstm_status lstm_plan_read_timing(lstm_plan* plan, double* ms, int64_t* calls);
+
+/* Kernels launched through this plan since it was created (traced or not);
+ * -1 for a NULL plan. */
+int64_t lstm_plan_launch_count(const lstm_plan* plan);
+
+/* Per-step phase stamps of the recurrent kernels (diagnostics).  With a
+ * device buffer of 2 * ndir * steps * 8 int64 set, CTA 0 of each direction
+ * writes clock64() stamps for its first `steps` steps at
+ * [kernel (0 fwd, 1 bwd)][direction][step][k]: k = 0 step start, 1 after the
+ * barrier, 2 after the exchanged operands are staged, 3 after the cell
+ * update (and, backward, the partial product), 4 after publishing.  The
+ * buffer is the caller's; steps = 0 turns the stamps off. */
+lstm_status lstm_debug_trace_steps(lstm_plan* plan, int64_t* device_buffer, int32_t steps);
+
+/* Test hook: CTA `cta` of the recurrent kernels never announces its steps
+ * (-1 = off), so the others' barrier waits run out and report
+ * LSTM_ERR_TIMEOUT.  Exercises the failure path without a GPU fault. */
+lstm_status lstm_debug_skip_arrival(lstm_plan* plan, int32_t cta);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LSTM_PACKED_H */

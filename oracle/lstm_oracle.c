@@ -46,6 +46,7 @@
  *   stored back to back in that order.  Gradients use the same layout.
  */
 #include <math.h>
+#include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
@@ -53,6 +54,29 @@
 #endif
 
 static double sigm(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/*
+ * Diagnostic mode (off by default; never the parity reference): round the
+ * state h and the gate errors to bfloat16 before they enter a product, as a
+ * bf16-operand implementation does.  Comparing against this mode separates
+ * a wrong bf16 kernel from the expected bf16 rounding.
+ */
+static int g_bf16_products = 0;
+
+void oracle_set_bf16_products(int on) { g_bf16_products = on ? 1 : 0; }
+
+static double to_bf16(double v)
+{
+    float f = (float)v;
+    uint32_t u;
+    memcpy(&u, &f, sizeof(u));
+    if ((u & 0x7f800000u) == 0x7f800000u) return v;
+    u = (u + (((u >> 16) & 1u) + 0x7fffu)) & 0xffff0000u;
+    memcpy(&f, &u, sizeof(f));
+    return (double)f;
+}
+
+static double rb(double v) { return g_bf16_products ? to_bf16(v) : v; }
 
 static size_t layer_param_count(int ndir, int D, int H)
 {
@@ -82,7 +106,7 @@ void oracle_dir_forward(int L, int D, int H, const double* x,
             double acc = b[r];
             for (int k = 0; k < D; ++k) acc += W[(size_t)r * D + k] * x[(size_t)t * D + k];
             if (hp)
-                for (int k = 0; k < H; ++k) acc += R[(size_t)r * H + k] * hp[k];
+                for (int k = 0; k < H; ++k) acc += R[(size_t)r * H + k] * rb(hp[k]);
             a[r] = acc;
         }
         for (int u = 0; u < H; ++u) {
@@ -130,7 +154,7 @@ void oracle_dir_backward(int L, int D, int H, const double* x,
         for (int u = 0; u < H; ++u) {
             double acc = dy[(size_t)t * H + u];
             if (have_next)
-                for (size_t r = 0; r < G4; ++r) acc += R[r * H + u] * da_next[r];
+                for (size_t r = 0; r < G4; ++r) acc += R[r * H + u] * rb(da_next[r]);
             dh[u] = acc;
         }
         for (int u = 0; u < H; ++u) {
@@ -156,13 +180,13 @@ void oracle_dir_backward(int L, int D, int H, const double* x,
         }
         for (size_t r = 0; r < G4; ++r) {
             db[r] += da[r];
-            for (int k = 0; k < D; ++k) dW[r * D + k] += da[r] * x[(size_t)t * D + k];
+            for (int k = 0; k < D; ++k) dW[r * D + k] += rb(da[r]) * x[(size_t)t * D + k];
             if (s > 0)
-                for (int k = 0; k < H; ++k) dR[r * H + k] += da[r] * h[(size_t)tp * H + k];
+                for (int k = 0; k < H; ++k) dR[r * H + k] += rb(da[r]) * rb(h[(size_t)tp * H + k]);
         }
         for (int k = 0; k < D; ++k) {
             double acc = 0.0;
-            for (size_t r = 0; r < G4; ++r) acc += W[r * D + k] * da[r];
+            for (size_t r = 0; r < G4; ++r) acc += W[r * D + k] * rb(da[r]);
             dx[(size_t)t * D + k] += acc;
         }
         memcpy(da_next, da, sizeof(double) * G4);
@@ -262,6 +286,12 @@ int oracle_lstm_stack(int B, const int* lengths, int num_layers, int ndir, int H
                 for (int t = 0; t < L; ++t)
                     memcpy(acts[l + 1] + (size_t)t * Hout + (size_t)d * H, h + (size_t)t * H,
                            sizeof(double) * H);
+                if (g_bf16_products && l + 1 < num_layers)   /* next layer's operand */
+                    for (int t = 0; t < L; ++t)
+                        for (int u = 0; u < H; ++u) {
+                            double* v = acts[l + 1] + (size_t)t * Hout + (size_t)d * H + u;
+                            *v = to_bf16(*v);
+                        }
                 const int tl = (d == 0) ? L - 1 : 0;      /* last position consumed */
                 const size_t o = (((size_t)l * ndir + d) * B + b) * H;
                 if (h_n) memcpy(h_n + o, h + (size_t)tl * H, sizeof(double) * H);

@@ -46,6 +46,8 @@ def _load():
             lib.oracle_lstm_padded_layer.argtypes = [
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, dp,
                 ctypes.POINTER(ctypes.c_ubyte), dp, dp, dp, dp, dp, dp, dp]
+            lib.oracle_set_bf16_products.restype = None
+            lib.oracle_set_bf16_products.argtypes = [ctypes.c_int]
             lib.oracle_layer_param_count.restype = ctypes.c_long
             lib.oracle_layer_param_count.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
             _lib = lib
@@ -79,12 +81,15 @@ def unpack_layer_grads(flat: np.ndarray, ndir: int, D: int, H: int) -> dict:
 
 
 def lstm_stack(lengths, x, layers, num_directions: int, hidden_size: int, G=None,
-               nthreads: int = 1) -> dict:
+               nthreads: int = 1, bf16_products: bool = False) -> dict:
     """Forward (and, if ``G`` is given, BPTT) of a layer stack, each sequence on its own.
 
     lengths[B]; x[N, D0] in caller order; layers: list of dicts W, R, b, peep;
     G[N, ndir*H] = dL/dy of the top layer.  Returns y, h_n, c_n [layers, ndir, B, H]
     and, with G, dx and grads (list of dicts).
+
+    bf16_products=True is a diagnostic (not the parity reference): h and the
+    gate errors are rounded to bf16 before each product.
     """
     lib = _load()
     lengths = np.ascontiguousarray(lengths, dtype=np.int32)
@@ -112,9 +117,11 @@ def lstm_stack(lengths, x, layers, num_directions: int, hidden_size: int, G=None
         dx = np.zeros((N, D0))
         grads = [np.zeros_like(p) for p in params]
         garr = (dp * nl)(*[_ptr(g) for g in grads])
+    lib.oracle_set_bf16_products(1 if bf16_products else 0)
     rc = lib.oracle_lstm_stack(B, lengths.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), nl, nd, H, D0,
                                _ptr(x), parr, _ptr(dy), _ptr(y), _ptr(h_n), _ptr(c_n), _ptr(dx),
                                garr, int(nthreads))
+    lib.oracle_set_bf16_products(0)
     if rc != 0:
         raise ValueError("oracle_lstm_stack rejected its arguments")
     if G is not None:

@@ -1,0 +1,223 @@
+// api.cu -- lstm_fwd / lstm_bwd: argument checks and the order of launches.
+//
+// Forward of one layer ("Single Stream Parallelization...", Sec. 3; RETURNN,
+// Sec. 4.2):  (1) one product for the non-recurrent part of every frame and
+// both directions at once, A_in = X [W_fwd; W_rev]^T + b ("No Padding
+// Please", Sec. IV-B: all gate projections of one input in one grouped
+// operation); (2) the persistent recurrent kernel over the steps.
+// Backward:  (1) the persistent BPTT kernel (gate errors, db, dpeep);
+// (2) one product each for dX, dW and dR over all frames.
+#include <algorithm>
+#include <cstring>
+
+#include "common.cuh"
+#include "gemm.cuh"
+#include "recurrent.cuh"
+
+namespace lstm {
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+lstm_status check_shape(const lstm_layer_shape* s)
+{
+    if (!s) return LSTM_ERR_INVALID_ARG;
+    if (s->input_size < 1 || s->hidden_size < 8 || s->hidden_size % 8 != 0) return LSTM_ERR_INVALID_ARG;
+    if (s->num_directions != 1 && s->num_directions != 2) return LSTM_ERR_INVALID_ARG;
+    if (s->dtype != LSTM_F32 && s->dtype != LSTM_BF16) return LSTM_ERR_INVALID_ARG;
+    if (s->hidden_size > 2048 || s->input_size > 65536) return LSTM_ERR_UNSUPPORTED;
+    return LSTM_OK;
+}
+
+struct Layout {
+    size_t ga_off, c_off, total;   // workspace
+};
+
+Layout workspace_layout(const Plan& p, const lstm_layer_shape& s)
+{
+    Layout l;
+    const size_t rows = (size_t)p.rows, H = (size_t)s.hidden_size, nd = (size_t)s.num_directions;
+    l.ga_off = 0;
+    l.c_off = align256(rows * nd * 4 * H * sizeof(float));
+    l.total = l.c_off + align256(rows * nd * H * sizeof(float));
+    return l;
+}
+
+// The three gradient products of lstm_bwd (shapes only).
+void bwd_gemm_shapes(const Plan& p, const lstm_layer_shape& s, GemmDesc* dW, GemmDesc* dR, GemmDesc* dX)
+{
+    const int H = s.hidden_size, nd = s.num_directions, D = s.input_size;
+    dW->M = nd * 4 * H; dW->N = D; dW->K = (int)p.rows; dW->k_splits = 32;
+    dR->M = 4 * H; dR->N = H; dR->K = (int)p.rows; dR->k_splits = 32;
+    dX->M = (int)p.rows; dX->N = D; dX->K = nd * 4 * H; dX->k_splits = 8;
+}
+
+// The backward kernel's partial-product exchange and the split-K partial
+// sums of the gradient products are never live at the same time: one region.
+size_t scratch_floats(const Plan& p, const lstm_layer_shape& s)
+{
+    GemmDesc dW, dR, dX;
+    bwd_gemm_shapes(p, s, &dW, &dR, &dX);
+    const size_t gemm = std::max(std::max(gemm_partial_floats(dW, p.num_sms), gemm_partial_floats(dR, p.num_sms)),
+                                 gemm_partial_floats(dX, p.num_sms));
+    const size_t part = rec_bwd_part_floats(p, s.hidden_size, s.num_directions, s.dtype == LSTM_BF16,
+                                            p.forced_ctas);
+    return std::max(gemm, part);
+}
+
+RecArgs base_args(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm, float* ga,
+                  float* cbuf)
+{
+    RecArgs a;
+    memset(&a, 0, sizeof(a));
+    a.T = p.T; a.B = p.B; a.H = s.hidden_size; a.ndir = s.num_directions;
+    a.bf16 = s.dtype == LSTM_BF16; a.padded = p.padded ? 1 : 0;
+    a.debug_skip_cta = p.debug_skip_cta;
+    a.wait_limit_ns = p.wait_limit_ns;
+    a.bs = p.d_bs; a.off = p.d_off; a.slot_len = p.d_len; a.perm = p.d_perm;
+    a.ga = ga; a.R = prm.R; a.peep = prm.peep; a.cbuf = cbuf;
+    a.flags = p.d_flags; a.status = p.d_status;
+    return a;
+}
+
+lstm_status check_params(const lstm_layer_params* prm)
+{
+    if (!prm || !prm->W || !prm->R || !prm->b || !prm->peep) return LSTM_ERR_INVALID_ARG;
+    if (!aligned16(prm->W) || !aligned16(prm->R) || !aligned16(prm->b) || !aligned16(prm->peep))
+        return LSTM_ERR_INVALID_ARG;
+    return LSTM_OK;
+}
+
+}  // namespace
+
+}  // namespace lstm
+
+using namespace lstm;
+
+extern "C" {
+
+size_t lstm_workspace_bytes(const lstm_plan* plan, const lstm_layer_shape* shape)
+{
+    if (!plan || check_shape(shape) != LSTM_OK) return 0;
+    return workspace_layout(plan->p, *shape).total;
+}
+
+size_t lstm_scratch_bytes(const lstm_plan* plan, const lstm_layer_shape* shape)
+{
+    if (!plan || check_shape(shape) != LSTM_OK) return 0;
+    return align256(std::max<size_t>(1, scratch_floats(plan->p, *shape)) * sizeof(float));
+}
+
+lstm_status lstm_fwd(const lstm_plan* plan, const lstm_layer_shape* shape,
+                     const lstm_layer_params* params, const void* x_packed, float* y_packed,
+                     void* y_lo, float* h_n, float* c_n, void* workspace, void* stream)
+{
+    if (!plan) return LSTM_ERR_INVALID_ARG;
+    lstm_status st = check_shape(shape);
+    if (st != LSTM_OK) return st;
+    if ((st = check_params(params)) != LSTM_OK) return st;
+    const Plan& p = plan->p;
+    const lstm_layer_shape& s = *shape;
+    const int H = s.hidden_size, nd = s.num_directions, D = s.input_size;
+    const bool bf16 = s.dtype == LSTM_BF16;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if ((h_n && !aligned16(h_n)) || (c_n && !aligned16(c_n))) return LSTM_ERR_INVALID_ARG;
+    if (p.rows == 0) {
+        if (h_n) LSTM_CUDA_TRY(cudaMemsetAsync(h_n, 0, sizeof(float) * nd * p.B * H, cs));
+        if (c_n) LSTM_CUDA_TRY(cudaMemsetAsync(c_n, 0, sizeof(float) * nd * p.B * H, cs));
+        return LSTM_OK;
+    }
+    if (!x_packed || !y_packed || !workspace) return LSTM_ERR_INVALID_ARG;
+    if (!aligned16(x_packed) || !aligned16(y_packed) || !aligned16(workspace) || (y_lo && !aligned16(y_lo)))
+        return LSTM_ERR_INVALID_ARG;
+    const Layout L = workspace_layout(p, s);
+    float* ga = (float*)((char*)workspace + L.ga_off);
+    float* cbuf = (float*)((char*)workspace + L.c_off);
+
+    RecConfig rc;
+    if ((st = rec_configure(p, H, nd, bf16, false, p.forced_ctas, &rc)) != LSTM_OK) return st;
+
+    GemmDesc g;
+    g.M = (int)p.rows; g.N = nd * 4 * H; g.K = D;
+    g.A = x_packed; g.sam = D; g.sak = 1; g.a_bf16 = bf16;
+    g.B = params->W; g.sbk = 1; g.sbn = D; g.b_bf16 = bf16;
+    g.C = ga; g.ldc = nd * 4 * H; g.bias = params->b;
+    if ((st = gemm_simt(g, p, K_GEMM_IN, cs)) != LSTM_OK) return st;
+
+    RecArgs a = base_args(p, s, *params, ga, cbuf);
+    a.y = y_packed; a.y_lo = (__nv_bfloat16*)y_lo; a.h_n = h_n; a.c_n = c_n;
+    return rec_launch(p, rc, a, false, cs);
+}
+
+lstm_status lstm_bwd(const lstm_plan* plan, const lstm_layer_shape* shape,
+                     const lstm_layer_params* params, const void* x_packed, const float* y_packed,
+                     void* workspace, const float* dy_packed, float* dx_packed,
+                     const lstm_layer_grads* grads, void* scratch, void* stream)
+{
+    if (!plan) return LSTM_ERR_INVALID_ARG;
+    lstm_status st = check_shape(shape);
+    if (st != LSTM_OK) return st;
+    if ((st = check_params(params)) != LSTM_OK) return st;
+    if (!grads || !grads->dW || !grads->dR || !grads->db || !grads->dpeep) return LSTM_ERR_INVALID_ARG;
+    if (!aligned16(grads->dW) || !aligned16(grads->dR) || !aligned16(grads->db) || !aligned16(grads->dpeep))
+        return LSTM_ERR_INVALID_ARG;
+    const Plan& p = plan->p;
+    const lstm_layer_shape& s = *shape;
+    const int H = s.hidden_size, nd = s.num_directions, D = s.input_size;
+    const bool bf16 = s.dtype == LSTM_BF16;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (p.rows == 0) {
+        LSTM_CUDA_TRY(cudaMemsetAsync(grads->dW, 0, sizeof(float) * nd * 4 * H * D, cs));
+        LSTM_CUDA_TRY(cudaMemsetAsync(grads->dR, 0, sizeof(float) * nd * 4 * H * H, cs));
+        LSTM_CUDA_TRY(cudaMemsetAsync(grads->db, 0, sizeof(float) * nd * 4 * H, cs));
+        LSTM_CUDA_TRY(cudaMemsetAsync(grads->dpeep, 0, sizeof(float) * nd * 3 * H, cs));
+        return LSTM_OK;
+    }
+    if (!x_packed || !y_packed || !workspace || !dy_packed) return LSTM_ERR_INVALID_ARG;
+    if (!aligned16(x_packed) || !aligned16(y_packed) || !aligned16(workspace) || !aligned16(dy_packed) ||
+        (dx_packed && !aligned16(dx_packed)))
+        return LSTM_ERR_INVALID_ARG;
+    const size_t need_scratch = scratch_floats(p, s);
+    if (need_scratch > 0 && (!scratch || !aligned16(scratch))) return LSTM_ERR_INVALID_ARG;
+    const Layout L = workspace_layout(p, s);
+    float* ga = (float*)((char*)workspace + L.ga_off);
+    float* cbuf = (float*)((char*)workspace + L.c_off);
+
+    RecConfig rc;
+    if ((st = rec_configure(p, H, nd, bf16, true, p.forced_ctas, &rc)) != LSTM_OK) return st;
+    RecArgs a = base_args(p, s, *params, ga, cbuf);
+    a.y = const_cast<float*>(y_packed); a.dy = dy_packed; a.db = grads->db; a.dpeep = grads->dpeep;
+    a.part = (float*)scratch;
+    if ((st = rec_launch(p, rc, a, true, cs)) != LSTM_OK) return st;
+
+    const int nd4H = nd * 4 * H;
+    GemmDesc gw, gr, gx;
+    bwd_gemm_shapes(p, s, &gw, &gr, &gx);
+    if (dx_packed) {
+        GemmDesc g = gx;
+        g.partial = (float*)scratch;
+        g.A = ga; g.sam = nd4H; g.sak = 1;
+        g.B = params->W; g.sbk = D; g.sbn = 1; g.b_bf16 = bf16;
+        g.C = dx_packed; g.ldc = D; g.round_bf16 = bf16;
+        if ((st = gemm_simt(g, p, K_GEMM_DX, cs)) != LSTM_OK) return st;
+    }
+    gw.A = ga; gw.sam = 1; gw.sak = nd4H;
+    gw.B = x_packed; gw.sbk = D; gw.sbn = 1; gw.b_bf16 = bf16;
+    gw.C = grads->dW; gw.ldc = D; gw.round_bf16 = bf16; gw.partial = (float*)scratch;
+    if ((st = gemm_simt(gw, p, K_GEMM_DW, cs)) != LSTM_OK) return st;
+    for (int d = 0; d < nd; ++d) {
+        GemmDesc g = gr;
+        g.A = ga + (size_t)d * 4 * H; g.sam = 1; g.sak = nd4H;
+        g.B = y_packed + (size_t)d * H; g.sbk = nd * H; g.sbn = 1;
+        g.b_rows = d == 0 ? p.d_prev_fwd : p.d_prev_rev;
+        g.C = grads->dR + (size_t)d * 4 * H * H; g.ldc = H; g.round_bf16 = bf16;
+        g.partial = (float*)scratch;
+        if ((st = gemm_simt(g, p, K_GEMM_DR, cs)) != LSTM_OK) return st;
+    }
+    return LSTM_OK;
+}
+
+}  // extern "C"

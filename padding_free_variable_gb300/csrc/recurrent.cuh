@@ -1,0 +1,52 @@
+// recurrent.cuh -- launch interface of the persistent recurrent kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace lstm {
+
+struct RecArgs {
+    int T, B, H, ndir, G, Umax, JC;
+    int bf16, padded, debug_skip_cta;
+    unsigned long long wait_limit_ns;
+    const int32_t* bs;        // [T] active rows per step
+    const int32_t* off;       // [T+1] first row of each step
+    const int32_t* slot_len;  // [B] length of the sequence in slot j
+    const int32_t* perm;      // [B] caller index of slot j
+    float* ga;                // [rows][ndir*4H] gate pre-activations -> gates -> gate errors
+    const void* R;            // [ndir][4H][H]
+    const float* peep;        // [ndir][3][H]
+    float* y;                 // [rows][ndir*H]
+    __nv_bfloat16* y_lo;      // optional bf16 copy of y
+    float* cbuf;              // [rows][ndir*H] cell states
+    float* h_n;               // [ndir][B][H] caller order, optional
+    float* c_n;
+    const float* dy;          // backward: [rows][ndir*H]
+    float* db;                // backward: [ndir][4H]
+    float* dpeep;             // backward: [ndir][3][H]
+    float* part;              // backward: [2][ndir][B][G][H] partial R^T da exchange
+    unsigned* flags;
+    DeviceStatus* status;
+    long long* trace;         // optional [ndir][trace_steps][8] clock64 stamps of each direction's CTA 0
+    int trace_steps;
+    int tables_in_smem;
+    // dynamic shared-memory layout (byte offsets)
+    int off_h, off_red, off_acc, off_state, off_contrib, off_sums, off_tab, off_peep;
+};
+
+struct RecConfig {
+    int G = 0;          // CTAs per direction
+    int Umax = 0;       // units per CTA
+    int JC = 0;         // rows per staged chunk
+    int tables = 0;     // step tables copied to shared memory
+    size_t smem = 0;    // dynamic shared memory bytes
+};
+
+lstm_status rec_configure(const Plan& p, int H, int ndir, bool bf16, bool bwd, int forced_G,
+                          RecConfig* out);
+lstm_status rec_launch(const Plan& p, const RecConfig& c, RecArgs a, bool bwd, cudaStream_t s);
+
+// Floats of the backward kernel's partial-product exchange buffer.
+size_t rec_bwd_part_floats(const Plan& p, int H, int ndir, bool bf16, int forced_G);
+
+}  // namespace lstm

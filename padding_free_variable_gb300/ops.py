@@ -1,0 +1,210 @@
+"""Python-side use of the C ABI: plans, per-layer calls and a layer stack.
+
+PyTorch is used for device memory and streams only; every step of the path
+(pack, products, recurrence, BPTT, unpack) runs in liblstm_packed.so.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import LayerGrads, LayerParams, LayerShape, check
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Plan:
+    """Packing plan of one batch of sequence lengths (optionally the padded layout)."""
+
+    def __init__(self, lengths, padded: bool = False):
+        lib = _lib.load()
+        lens = np.ascontiguousarray(np.asarray(lengths, dtype=np.int32))
+        self.lengths = lens
+        self.padded = padded
+        h = ctypes.c_void_p()
+        fn = lib.lstm_plan_create_padded if padded else lib.lstm_plan_create
+        check(fn(lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), int(lens.size), ctypes.byref(h)),
+              "lstm_plan_create")
+        self.handle = h
+        rows, frames = ctypes.c_int64(), ctypes.c_int64()
+        steps, batch = ctypes.c_int32(), ctypes.c_int32()
+        check(lib.lstm_plan_info(h, ctypes.byref(rows), ctypes.byref(steps), ctypes.byref(batch),
+                                 ctypes.byref(frames)), "lstm_plan_info")
+        self.rows, self.steps, self.batch, self.frames = rows.value, steps.value, batch.value, frames.value
+
+    def tables(self):
+        """(batch_sizes[T], offsets[T+1], perm[B], slot_len[B]) as numpy copies."""
+        lib = _lib.load()
+        p = [ctypes.POINTER(ctypes.c_int32)() for _ in range(4)]
+        check(lib.lstm_plan_tables(self.handle, *[ctypes.byref(q) for q in p]), "lstm_plan_tables")
+        T, B = self.steps, self.batch
+        return (np.ctypeslib.as_array(p[0], (T,)).copy() if T else np.zeros(0, np.int32),
+                np.ctypeslib.as_array(p[1], (T + 1,)).copy(),
+                np.ctypeslib.as_array(p[2], (B,)).copy(),
+                np.ctypeslib.as_array(p[3], (B,)).copy())
+
+    def set_wait_limit(self, ns: int):
+        check(_lib.load().lstm_plan_set_wait_limit(self.handle, int(ns)), "lstm_plan_set_wait_limit")
+
+    def set_ctas_per_direction(self, ctas: int):
+        check(_lib.load().lstm_plan_set_ctas_per_direction(self.handle, int(ctas)),
+              "lstm_plan_set_ctas_per_direction")
+
+    def enable_timing(self, on: bool = True):
+        check(_lib.load().lstm_plan_enable_timing(self.handle, int(bool(on))), "lstm_plan_enable_timing")
+
+    def read_timing(self) -> dict:
+        """{kind: (milliseconds, timed calls)} summed since timing was enabled."""
+        n = len(_lib.KERNEL_KINDS)
+        ms = (ctypes.c_double * n)()
+        calls = (ctypes.c_int64 * n)()
+        check(_lib.load().lstm_plan_read_timing(self.handle, ms, calls), "lstm_plan_read_timing")
+        return {k: (ms[i], calls[i]) for i, k in enumerate(_lib.KERNEL_KINDS)}
+
+    def launch_count(self) -> int:
+        return int(_lib.load().lstm_plan_launch_count(self.handle))
+
+    def trace_steps(self, buffer, steps: int):
+        """Phase stamps into `buffer` (int64 device tensor of 2*ndir*steps*8), or off with steps=0."""
+        check(_lib.load().lstm_debug_trace_steps(self.handle, _ptr(buffer), int(steps)), "lstm_debug_trace_steps")
+
+    def debug_skip_arrival(self, cta: int):
+        check(_lib.load().lstm_debug_skip_arrival(self.handle, int(cta)), "lstm_debug_skip_arrival")
+
+    def poll(self, stream=None) -> int:
+        """Synchronise and return (and clear) the device status code."""
+        return int(_lib.load().lstm_status_poll(self.handle, _stream(stream)))
+
+    def pack(self, x_cat: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        width = x_cat.shape[1]
+        if out is None:
+            out = torch.empty((self.rows, width), dtype=x_cat.dtype, device=x_cat.device)
+        check(_lib.load().lstm_pack(self.handle, _ptr(x_cat), width, x_cat.element_size(), _ptr(out),
+                                    _stream(stream)), "lstm_pack")
+        return out
+
+    def unpack(self, y_packed: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        width = y_packed.shape[1]
+        if out is None:
+            out = torch.empty((self.frames, width), dtype=y_packed.dtype, device=y_packed.device)
+        check(_lib.load().lstm_unpack(self.handle, _ptr(y_packed), width, y_packed.element_size(),
+                                      _ptr(out), _stream(stream)), "lstm_unpack")
+        return out
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            _lib.load().lstm_plan_destroy(self.handle)
+            self.handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def layer_shape(input_size, hidden_size, num_directions, bf16: bool) -> LayerShape:
+    return LayerShape(int(input_size), int(hidden_size), int(num_directions),
+                      _lib.LSTM_BF16 if bf16 else _lib.LSTM_F32)
+
+
+def workspace_bytes(plan: Plan, shape: LayerShape) -> int:
+    return int(_lib.load().lstm_workspace_bytes(plan.handle, ctypes.byref(shape)))
+
+
+def scratch_bytes(plan: Plan, shape: LayerShape) -> int:
+    return int(_lib.load().lstm_scratch_bytes(plan.handle, ctypes.byref(shape)))
+
+
+def _params(layer: dict) -> LayerParams:
+    return LayerParams(layer["W"].data_ptr(), layer["R"].data_ptr(), layer["b"].data_ptr(),
+                       layer["peep"].data_ptr())
+
+
+def layer_forward(plan: Plan, shape: LayerShape, layer: dict, x_packed, y_packed, y_lo, h_n, c_n,
+                  workspace, stream=None):
+    check(_lib.load().lstm_fwd(plan.handle, ctypes.byref(shape), ctypes.byref(_params(layer)),
+                               _ptr(x_packed), _ptr(y_packed), _ptr(y_lo), _ptr(h_n), _ptr(c_n),
+                               _ptr(workspace), _stream(stream)), "lstm_fwd")
+
+
+def layer_backward(plan: Plan, shape: LayerShape, layer: dict, x_packed, y_packed, workspace, dy_packed,
+                   dx_packed, grads: dict, scratch, stream=None):
+    g = LayerGrads(grads["W"].data_ptr(), grads["R"].data_ptr(), grads["b"].data_ptr(),
+                   grads["peep"].data_ptr())
+    check(_lib.load().lstm_bwd(plan.handle, ctypes.byref(shape), ctypes.byref(_params(layer)),
+                               _ptr(x_packed), _ptr(y_packed), _ptr(workspace), _ptr(dy_packed),
+                               _ptr(dx_packed), ctypes.byref(g), _ptr(scratch), _stream(stream)),
+          "lstm_bwd")
+
+
+class PackedLSTMStack:
+    """A stack of (bi)LSTM layers run through the C ABI on one packed batch.
+
+    ``layers``: per layer a dict of device tensors W, R (fp32, or bf16 when
+    ``bf16``), b and peep (fp32) in the header's layout.  Buffers for every
+    layer's activations, workspace and gradients are allocated once, so
+    ``forward``/``backward`` allocate nothing and may be replayed.
+    """
+
+    def __init__(self, plan: Plan, layers: list, input_size: int, hidden_size: int,
+                 num_directions: int, bf16: bool, device="cuda"):
+        self.plan, self.layers = plan, layers
+        self.D0, self.H, self.nd, self.bf16 = int(input_size), int(hidden_size), int(num_directions), bool(bf16)
+        dev = torch.device(device)
+        rows, H, nd = plan.rows, self.H, self.nd
+        xdt = torch.bfloat16 if self.bf16 else torch.float32
+        self.shapes = [layer_shape(self.D0 if l == 0 else nd * H, H, nd, self.bf16) for l in range(len(layers))]
+        self.x_packed = torch.empty((rows, self.D0), dtype=xdt, device=dev)
+        self.y = [torch.empty((rows, nd * H), dtype=torch.float32, device=dev) for _ in layers]
+        # bf16 copies of every layer output but the last feed the next layer's products
+        self.y_lo = [torch.empty((rows, nd * H), dtype=torch.bfloat16, device=dev)
+                     if (self.bf16 and l + 1 < len(layers)) else None for l in range(len(layers))]
+        self.h_n = torch.empty((len(layers), nd, plan.batch, H), dtype=torch.float32, device=dev)
+        self.c_n = torch.empty_like(self.h_n)
+        self.ws = [torch.empty(max(1, workspace_bytes(plan, s)), dtype=torch.uint8, device=dev)
+                   for s in self.shapes]
+        self.scratch = torch.empty(max(scratch_bytes(plan, s) for s in self.shapes), dtype=torch.uint8,
+                                   device=dev)
+        self.dy_packed = torch.empty((rows, nd * H), dtype=torch.float32, device=dev)
+        self.dx = [torch.empty((rows, s.input_size), dtype=torch.float32, device=dev) for s in self.shapes]
+        self.grads = [{"W": torch.empty(tuple(lay["W"].shape), dtype=torch.float32, device=dev),
+                       "R": torch.empty(tuple(lay["R"].shape), dtype=torch.float32, device=dev),
+                       "b": torch.empty(tuple(lay["b"].shape), dtype=torch.float32, device=dev),
+                       "peep": torch.empty(tuple(lay["peep"].shape), dtype=torch.float32, device=dev)}
+                      for lay in layers]
+
+    def layer_input(self, l):
+        return self.x_packed if l == 0 else (self.y_lo[l - 1] if self.bf16 else self.y[l - 1])
+
+    def forward_packed(self, stream=None):
+        for l, lay in enumerate(self.layers):
+            layer_forward(self.plan, self.shapes[l], lay, self.layer_input(l), self.y[l], self.y_lo[l],
+                          self.h_n[l], self.c_n[l], self.ws[l], stream)
+        return self.y[-1]
+
+    def backward_packed(self, stream=None):
+        dy = self.dy_packed
+        for l in range(len(self.layers) - 1, -1, -1):
+            layer_backward(self.plan, self.shapes[l], self.layers[l], self.layer_input(l), self.y[l],
+                           self.ws[l], dy, self.dx[l], self.grads[l], self.scratch, stream)
+            dy = self.dx[l]
+        return self.dx[0]
+
+    def step(self, x_cat, G_cat, stream=None):
+        """pack -> forward of every layer -> backward of every layer -> unpack."""
+        self.plan.pack(x_cat, self.x_packed, stream)
+        self.plan.pack(G_cat, self.dy_packed, stream)
+        self.forward_packed(stream)
+        self.backward_packed(stream)
+        return self.plan.unpack(self.y[-1], stream=stream), self.plan.unpack(self.dx[0], stream=stream)
