@@ -242,6 +242,34 @@ lstm_status lstm_bwd(const lstm_plan* plan, const lstm_layer_shape* shape,
                      float* dx_packed, const lstm_layer_grads* grads, void* scratch,
                      void* stream);
 
+/*
+ * lstm_bwd without device allocation.  (The pages have no counterpart: this
+ * serves callers that cannot call cudaMalloc -- a host framework whose
+ * memory pool owns the device memory and forbids allocations from outside
+ * it, or a real-time loop that must not allocate once it has started.)
+ *
+ * Same arguments and results as lstm_bwd, minus `scratch`: the scratch comes
+ * from one array of LSTM_NOALLOC_SCRATCH_BYTES (32 MiB) inside the library's
+ * own device memory, which every GPU that loads the library holds until the
+ * process exits.  The caller still passes all inputs and outputs.
+ *   - Returns LSTM_ERR_UNSUPPORTED, launching nothing, when
+ *     lstm_scratch_bytes(plan, shape) exceeds LSTM_NOALLOC_SCRATCH_BYTES.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture begins.  Later calls only read the cached
+ *     address.  Neither calls cudaMalloc, cudaFree or an allocating library
+ *     routine.
+ *   - Every call on a device shares the one array and it keeps the last
+ *     call's contents; nothing in it needs to start at zero.  Calls whose
+ *     work overlaps on the GPU (other streams, other host threads) race on
+ *     it: serialise them.
+ */
+#define LSTM_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+lstm_status lstm_bwd_noalloc(const lstm_plan* plan, const lstm_layer_shape* shape,
+                             const lstm_layer_params* params, const void* x_packed,
+                             const float* y_packed, void* workspace, const float* dy_packed,
+                             float* dx_packed, const lstm_layer_grads* grads, void* stream);
+
 /* Synchronise the stream, then return and clear the plan's device status
  * word (LSTM_OK, LSTM_ERR_TIMEOUT or LSTM_ERR_BOUNDS). */
 lstm_status lstm_status_poll(lstm_plan* plan, void* stream);
