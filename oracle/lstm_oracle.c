@@ -8,8 +8,8 @@
  * What it computes, and where that comes from:
  *
  *  - The cell.  "Single Stream Parallelization of Generalized LSTM-Like RNNs
- *    on a GPU", Sec. 2 and Fig. 1, builds an LSTM "with forget gates and
- *    peephole connections" from additive layers (sum of the incoming
+ *    on a GPU", Sec. 2 and Fig. 1, builds an LSTM that has forget gates and
+ *    peepholes out of additive layers (sum of the incoming
  *    connections, then an activation) and multiplicative layers (element-wise
  *    products).  The page's equations did not survive extraction, so this
  *    file uses the standard reading of that graph: for one direction,
@@ -26,8 +26,8 @@
  *    in reverse time, and each connection's gradient is the sum over frames
  *    of its back-propagated error times its source activation.
  *  - Padding-free evaluation ("No Padding Please", Sec. V): every sequence is
- *    computed on its own frames only, so the packed result must equal what is
- *    obtained "for each input tensor separately" (Sec. V-B).  This oracle
+ *    computed on its own frames only, so the packed result must equal the
+ *    result of running every example on its own (Sec. V-B).  This oracle
  *    therefore loops over each sequence alone.
  *  - The padded comparator (RETURNN paper, Sec. 5: an index tensor marks which
  *    time-batch frames belong to a sequence; "No Padding Please", Sec. V: a
