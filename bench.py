@@ -406,9 +406,11 @@ def main():
         if not d[:, 0].any():
             continue
         us = lambda cyc: round(float(np.median(cyc)) / mhz, 3)
+        # forward: 1 -> 2 stage h, 2 -> 5 product, 5 -> 3 cell; backward: 1 -> 2 cell (with the
+        # peers' partial sums), 2 -> 5 partial product, 5 -> 3 gradient sums
         recurrent[f"phases_us_{kname}"] = {
-            "barrier_wait": us(d[1:, 1] - d[1:, 0]), "stage_exchange": us(d[:, 2] - d[:, 1]),
-            "compute_cell": us(d[:, 3] - d[:, 2]), "publish": us(d[:, 4] - d[:, 3]),
+            "barrier_wait": us(d[1:, 1] - d[1:, 0]), "after_barrier_to_2": us(d[:, 2] - d[:, 1]),
+            "2_to_5": us(d[:, 5] - d[:, 2]), "5_to_3": us(d[:, 3] - d[:, 5]), "publish": us(d[:, 4] - d[:, 3]),
             "step": us(d[1:, 0] - d[:-1, 0]), "clock_mhz": mhz, "cta": 0, "direction": 0}
     if "rec_fwd" in kernels:
         recurrent["us_per_step_fwd"] = round(1e3 * kernels["rec_fwd"]["ms_per_step"] / (T * spec.num_layers), 3)

@@ -282,6 +282,21 @@ const char* lstm_status_string(lstm_status status);
  * CTA owns ceil(H / ctas) units; the count is capped at the SMs available. */
 lstm_status lstm_plan_set_ctas_per_direction(lstm_plan* plan, int32_t ctas);
 
+/* Engine of the matrix products.  0 (default): tensor cores -- the bf16
+ * input projection on tcgen05 (TMA-fed, fp32 accumulation in tensor memory)
+ * and the recurrent kernels' per-step products on warp-level MMA wherever a
+ * CTA's R fragments fit in registers (fp32 operands as three tf32 products,
+ * about 22 bits per product; bf16 as one product).  1: CUDA-core FFMA for
+ * every product (a comparator).  The fp32 path's other products use CUDA
+ * cores under both settings. */
+lstm_status lstm_plan_set_gemm_engine(lstm_plan* plan, int32_t engine);
+
+/* Test hook: only the forward input projection of lstm_fwd,
+ * out[rows][ndir*4H] = x_packed W^T + b (fp32), with the plan's engine. */
+lstm_status lstm_debug_input_projection(const lstm_plan* plan, const lstm_layer_shape* shape,
+                                        const lstm_layer_params* params, const void* x_packed, float* out,
+                                        void* stream);
+
 /* Kinds of launch the plan's tracer times. */
 typedef enum {
     LSTM_KERNEL_PACK = 0,       /* lstm_pack gather */

@@ -83,6 +83,23 @@ RecArgs base_args(const Plan& p, const lstm_layer_shape& s, const lstm_layer_par
     return a;
 }
 
+// A_in[rows][ndir*4H] = X W^T + b for both directions at once; tcgen05 for bf16 operands.
+lstm_status input_projection(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm,
+                             const void* x_packed, float* out, cudaStream_t cs)
+{
+    const int H = s.hidden_size, nd = s.num_directions, D = s.input_size;
+    const bool bf16 = s.dtype == LSTM_BF16;
+    if (bf16 && p.gemm_engine == 0 && gemm_tc_supported((int)p.rows, nd * 4 * H, D, x_packed, prm.W))
+        return gemm_tc_bf16_nt(p, K_GEMM_IN, x_packed, prm.W, out, (int64_t)nd * 4 * H, prm.b, (int)p.rows,
+                               nd * 4 * H, D, cs);
+    GemmDesc g;
+    g.M = (int)p.rows; g.N = nd * 4 * H; g.K = D;
+    g.A = x_packed; g.sam = D; g.sak = 1; g.a_bf16 = bf16;
+    g.B = prm.W; g.sbk = 1; g.sbn = D; g.b_bf16 = bf16;
+    g.C = out; g.ldc = nd * 4 * H; g.bias = prm.b;
+    return gemm_simt(g, p, K_GEMM_IN, cs);
+}
+
 lstm_status check_params(const lstm_layer_params* prm)
 {
     if (!prm || !prm->W || !prm->R || !prm->b || !prm->peep) return LSTM_ERR_INVALID_ARG;
@@ -121,7 +138,7 @@ lstm_status lstm_fwd(const lstm_plan* plan, const lstm_layer_shape* shape,
     if ((st = check_params(params)) != LSTM_OK) return st;
     const Plan& p = plan->p;
     const lstm_layer_shape& s = *shape;
-    const int H = s.hidden_size, nd = s.num_directions, D = s.input_size;
+    const int H = s.hidden_size, nd = s.num_directions;
     const bool bf16 = s.dtype == LSTM_BF16;
     cudaStream_t cs = (cudaStream_t)stream;
     if ((h_n && !aligned16(h_n)) || (c_n && !aligned16(c_n))) return LSTM_ERR_INVALID_ARG;
@@ -140,12 +157,7 @@ lstm_status lstm_fwd(const lstm_plan* plan, const lstm_layer_shape* shape,
     RecConfig rc;
     if ((st = rec_configure(p, H, nd, bf16, false, p.forced_ctas, &rc)) != LSTM_OK) return st;
 
-    GemmDesc g;
-    g.M = (int)p.rows; g.N = nd * 4 * H; g.K = D;
-    g.A = x_packed; g.sam = D; g.sak = 1; g.a_bf16 = bf16;
-    g.B = params->W; g.sbk = 1; g.sbn = D; g.b_bf16 = bf16;
-    g.C = ga; g.ldc = nd * 4 * H; g.bias = params->b;
-    if ((st = gemm_simt(g, p, K_GEMM_IN, cs)) != LSTM_OK) return st;
+    if ((st = input_projection(p, s, *params, x_packed, ga, cs)) != LSTM_OK) return st;
 
     RecArgs a = base_args(p, s, *params, ga, cbuf);
     a.y = y_packed; a.y_lo = (__nv_bfloat16*)y_lo; a.h_n = h_n; a.c_n = c_n;
@@ -218,6 +230,19 @@ lstm_status lstm_bwd(const lstm_plan* plan, const lstm_layer_shape* shape,
         if ((st = gemm_simt(g, p, K_GEMM_DR, cs)) != LSTM_OK) return st;
     }
     return LSTM_OK;
+}
+
+lstm_status lstm_debug_input_projection(const lstm_plan* plan, const lstm_layer_shape* shape,
+                                        const lstm_layer_params* params, const void* x_packed, float* out,
+                                        void* stream)
+{
+    if (!plan) return LSTM_ERR_INVALID_ARG;
+    lstm_status st = check_shape(shape);
+    if (st != LSTM_OK) return st;
+    if ((st = check_params(params)) != LSTM_OK) return st;
+    if (plan->p.rows == 0) return LSTM_OK;
+    if (!x_packed || !out || !aligned16(x_packed) || !aligned16(out)) return LSTM_ERR_INVALID_ARG;
+    return input_projection(plan->p, *shape, *params, x_packed, out, (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -44,6 +44,7 @@ struct Plan {
     uint64_t wait_limit_ns = 2000000000ull;
     int32_t debug_skip_cta = -1;
     int32_t forced_ctas = 0;        // 0 = automatic
+    int32_t gemm_engine = 0;        // 0 = tensor cores for bf16 operands, 1 = CUDA cores
     int device = 0;
     int num_sms = 0;
     // host tables

@@ -33,4 +33,9 @@ lstm_status gemm_simt_run(const GemmDesc& d, int num_sms, cudaStream_t s);
 // Same, traced under `kind` in the plan's tracer.
 lstm_status gemm_simt(const GemmDesc& d, const Plan& p, int kind, cudaStream_t s);
 
+// bf16 A[M][K] x B[N][K]^T (+ bias) on tcgen05 tensor cores, fp32 out.
+bool gemm_tc_supported(int M, int N, int K, const void* A, const void* B);
+lstm_status gemm_tc_bf16_nt(const Plan& p, int kind, const void* A, const void* B, float* C, int64_t ldc,
+                            const float* bias, int M, int N, int K, cudaStream_t s);
+
 }  // namespace lstm

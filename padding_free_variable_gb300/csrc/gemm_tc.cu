@@ -1,0 +1,224 @@
+// gemm_tc.cu -- bf16 products on the 5th-generation tensor cores.
+//
+// RETURNN paper, Sec. 4.2: the non-recurrent part of the forward pass is one
+// matrix product over all frames of the batch.  On GB300 that product runs as
+// C[M][N] = A[M][K] B[N][K]^T + bias[N] with A, B bf16 (both K-major, i.e.
+// row-major with K innermost) and fp32 accumulation in tensor memory:
+//
+//   warp 0      TMA producer: 128x64 tiles of A and 256x64 tiles of B into a
+//               4-stage ring of 128-byte-swizzled shared-memory slots
+//   warp 1      owns the 256 TMEM columns; one thread issues tcgen05.mma
+//               (M=128, N=256, K=16) and commits each stage back to the ring
+//   warps 2..5  epilogue: tcgen05.ld of their TMEM lane quarter, + bias, store
+//
+// Every mbarrier wait is bounded; a timeout is recorded in the plan's status
+// word and the CTA still frees its tensor memory before returning.
+#include <cudaTypedefs.h>
+
+#include "gemm.cuh"
+#include "tc_ptx.cuh"
+
+namespace lstm {
+
+namespace {
+
+constexpr int TBM = 128, TBN = 256, TBK = 64, TSTAGES = 4;
+constexpr int TC_THREADS = 192;
+constexpr uint32_t A_BYTES = TBM * TBK * 2;
+constexpr uint32_t B_BYTES = TBN * TBK * 2;
+constexpr uint32_t TMEM_COLS = 256;
+constexpr size_t TC_SMEM = 1024 + (size_t)TSTAGES * (A_BYTES + B_BYTES) + 256;
+
+struct TcArgs {
+    int M, N, K;
+    float* C;
+    int64_t ldc;
+    const float* bias;
+    DeviceStatus* status;
+    unsigned long long limit_ns;
+};
+
+__device__ __forceinline__ void fail(const TcArgs& a, int* s_abort, unsigned where)
+{
+    record_failure(a.status, LSTM_ERR_TIMEOUT, 0x80000u | where);
+    *(volatile int*)s_abort = 1;
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+gemm_tc_bf16_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, TcArgs a)
+{
+    extern __shared__ unsigned char smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sA = base;
+    uint8_t* sB = base + TSTAGES * A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(base + TSTAGES * (A_BYTES + B_BYTES));
+    uint64_t* empty = full + TSTAGES;
+    uint64_t* accf = empty + TSTAGES;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+    int* s_abort = reinterpret_cast<int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.y * TBM, n0 = blockIdx.x * TBN;
+    const int nk = (a.K + TBK - 1) / TBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < TSTAGES; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        tc::mbar_init(accf, 1);
+        *s_abort = 0;
+        tc::fence_mbar_init();
+        tc::prefetch_tensormap(&mapA);
+        tc::prefetch_tensormap(&mapB);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before_sync();
+    __syncthreads();
+    tc::tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---- producer
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % TSTAGES;
+            if (kb >= TSTAGES && !tc::mbar_wait(&empty[s], ((kb / TSTAGES) - 1) & 1, a.limit_ns)) {
+                fail(a, s_abort, 1);
+                break;
+            }
+            if (*(volatile int*)s_abort) break;
+            tc::mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
+            tc::tma_load_2d(sA + s * A_BYTES, &mapA, &full[s], kb * TBK, m0);
+            tc::tma_load_2d(sB + s * B_BYTES, &mapB, &full[s], kb * TBK, n0);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer
+        constexpr uint32_t idesc = tc::idesc_bf16_f32(TBM, TBN);
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % TSTAGES;
+            if (*(volatile int*)s_abort) break;
+            if (!tc::mbar_wait(&full[s], (kb / TSTAGES) & 1, a.limit_ns)) {
+                fail(a, s_abort, 2);
+                break;
+            }
+            tc::tc_fence_after_sync();
+            const uint32_t a0 = tc::smem_u32(sA + s * A_BYTES), b0 = tc::smem_u32(sB + s * B_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < TBK / 16; ++kk)
+                tc::mma_bf16_ss(tmem, tc::sdesc_sw128(a0 + kk * 32), tc::sdesc_sw128(b0 + kk * 32), idesc,
+                                (kb | kk) != 0 ? 1u : 0u);
+            tc::mma_commit(&empty[s]);
+        }
+        tc::mma_commit(accf);      // arrives once every MMA issued above has completed
+    } else if (warp >= 2) {
+        // ---- epilogue: this warp may read TMEM lanes 32*(warp%4) .. +31
+        const int q = warp & 3;
+        const int row = m0 + q * 32 + lane;
+        const bool ok = tc::mbar_wait(accf, 0, a.limit_ns);
+        if (!ok && lane == 0) fail(a, s_abort, 3);
+        tc::tc_fence_after_sync();
+        if (__all_sync(0xffffffffu, ok) && !*(volatile int*)s_abort) {
+            const bool vec = (a.ldc % 4) == 0 && (((uintptr_t)a.C) & 15u) == 0;
+            for (int c = 0; c < TBN; c += 16) {
+                if (n0 + c >= a.N) break;                      // uniform across the warp
+                uint32_t r[16];
+                tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c, r);
+                tc::tmem_wait_ld();
+                if (row < a.M) {
+                    const int n = n0 + c;
+                    float* out = a.C + (int64_t)row * a.ldc + n;
+                    float v[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
+                    if (n + 16 <= a.N && vec) {
+                        if (a.bias) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v[e] += __ldg(a.bias + n + e);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4)
+                            *reinterpret_cast<float4*>(out + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                    } else {
+                        for (int e = 0; e < 16 && n + e < a.N; ++e)
+                            out[e] = v[e] + (a.bias ? __ldg(a.bias + n + e) : 0.f);
+                    }
+                }
+            }
+        }
+    }
+    tc::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc::tc_fence_after_sync();
+        tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// Row-major bf16 [rows][cols] (cols = K innermost) as 128-byte-swizzled boxes of 64 x box_rows.
+bool make_map(CUtensorMap* map, const void* ptr, int rows, int cols, int box_rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)TBK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool gemm_tc_supported(int M, int N, int K, const void* A, const void* B)
+{
+    // TMA: 16-byte aligned bases and row pitches; x coordinates are multiples of 64 elements.
+    return M > 0 && N > 0 && K > 0 && K % 8 == 0 && ((uintptr_t)A & 15u) == 0 && ((uintptr_t)B & 15u) == 0 &&
+           encode_fn() != nullptr;
+}
+
+lstm_status gemm_tc_bf16_nt(const Plan& p, int kind, const void* A, const void* B, float* C, int64_t ldc,
+                            const float* bias, int M, int N, int K, cudaStream_t s)
+{
+    if (!gemm_tc_supported(M, N, K, A, B)) return LSTM_ERR_UNSUPPORTED;
+    CUtensorMap mapA, mapB;
+    if (!make_map(&mapA, A, M, K, TBM) || !make_map(&mapB, B, N, K, TBN)) return LSTM_ERR_UNSUPPORTED;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(gemm_tc_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM) !=
+            cudaSuccess)
+            return LSTM_ERR_CUDA;
+        attr_set = true;
+    }
+    TcArgs a;
+    a.M = M; a.N = N; a.K = K; a.C = C; a.ldc = ldc; a.bias = bias;
+    a.status = p.d_status; a.limit_ns = p.wait_limit_ns;
+    const dim3 grid((N + TBN - 1) / TBN, (M + TBM - 1) / TBM);
+    trace_begin(p, kind, s);
+    gemm_tc_bf16_kernel<<<grid, TC_THREADS, TC_SMEM, s>>>(mapA, mapB, a);
+    const cudaError_t e = cudaGetLastError();
+    trace_end(p, kind, s, e == cudaSuccess ? 1 : 0);
+    return e == cudaSuccess ? LSTM_OK : LSTM_ERR_CUDA;
+}
+
+}  // namespace lstm

@@ -332,6 +332,13 @@ lstm_status lstm_debug_trace_steps(lstm_plan* plan, int64_t* device_buffer, int3
     return LSTM_OK;
 }
 
+lstm_status lstm_plan_set_gemm_engine(lstm_plan* plan, int32_t engine)
+{
+    if (!plan || engine < 0 || engine > 1) return LSTM_ERR_INVALID_ARG;
+    plan->p.gemm_engine = engine;
+    return LSTM_OK;
+}
+
 lstm_status lstm_plan_set_ctas_per_direction(lstm_plan* plan, int32_t ctas)
 {
     if (!plan || ctas < 0) return LSTM_ERR_INVALID_ARG;

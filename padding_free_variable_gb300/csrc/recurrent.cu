@@ -43,7 +43,14 @@ namespace {
 constexpr int kMaxItems = 4;      // cell items per thread held in registers
 constexpr int kMaxJC = 32;        // rows per chunk
 
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+// Logistic and tanh from the hardware exp2 (relative error of __expf about
+// 2^-21; absolute error of both functions below 1e-6 over the whole line).
+__device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float tanhf_(float x)
+{
+    const float e = __expf(2.0f * fminf(fmaxf(x, -40.0f), 40.0f));
+    return 1.0f - __fdividef(2.0f, e + 1.0f);
+}
 
 // 8 consecutive matrix elements from shared memory as floats.
 __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
@@ -58,6 +65,100 @@ __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
     for (int i = 0; i < 4; ++i) {
         v[2 * i] = __uint_as_float(w[i] << 16);
         v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// ---------------------------------------------------------------- warp-level tensor-core MMA
+//
+// The per-step product is small (16-32 gate rows per CTA, <= 32 rows of the
+// batch per chunk) and on the critical path of every step, so it runs as
+// mma.sync with the CTA's R fragments held in registers for the whole launch.
+// fp32 operands use three tf32 products (hi*hi + hi*lo + lo*hi, with x = hi +
+// lo split at load), which keeps about 22 bits of each product; bf16
+// operands use one bf16 product.
+
+constexpr int kFwdMTW = 2, kFwdKTW = 4;    // m-tiles and k-steps per warp, forward
+constexpr int kBwdMTW = 4, kBwdKTW = 2;    // backward
+
+__device__ __forceinline__ uint32_t to_tf32(float x)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo)
+{
+    hi = to_tf32(x);
+    lo = to_tf32(x - __uint_as_float(hi));
+}
+
+// bf16 pair: `lo_k` (the smaller k index) in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo_k, float hi_k)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi_k), "f"(lo_k));
+    return r;
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// A fragments (m16 x k) of a matrix given element-wise by `at(row, col)`:
+// tf32 -> hi/lo of m16n8k8 fragments; bf16 -> m16n8k16 fragments in hi.
+template <bool BF16, typename F>
+__device__ __forceinline__ void load_a_frag(F at, int mt, int kt, uint32_t (&hi)[4], uint32_t (&lo)[4])
+{
+    const int lane = threadIdx.x & 31, grp = lane >> 2, tig = lane & 3;
+    const int r0 = mt * 16 + grp, r1 = r0 + 8;
+    if (!BF16) {
+        const int k0 = kt * 8 + tig, k1 = k0 + 4;
+        split_tf32(at(r0, k0), hi[0], lo[0]);
+        split_tf32(at(r1, k0), hi[1], lo[1]);
+        split_tf32(at(r0, k1), hi[2], lo[2]);
+        split_tf32(at(r1, k1), hi[3], lo[3]);
+    } else {
+        const int k0 = kt * 16 + 2 * tig;
+        hi[0] = pack_bf16x2(at(r0, k0), at(r0, k0 + 1));
+        hi[1] = pack_bf16x2(at(r1, k0), at(r1, k0 + 1));
+        hi[2] = pack_bf16x2(at(r0, k0 + 8), at(r0, k0 + 9));
+        hi[3] = pack_bf16x2(at(r1, k0 + 8), at(r1, k0 + 9));
+        lo[0] = lo[1] = lo[2] = lo[3] = 0u;
+    }
+}
+
+// One k-step of C(m16 x n8) += A * B where B(k, n) = V[n][k] (V rows of stride ldv floats).
+template <bool BF16>
+__device__ __forceinline__ void mma_step(float (&acc)[4], const uint32_t (&ahi)[4], const uint32_t (&alo)[4],
+                                         const float* __restrict__ V, int ldv, int nt, int kt)
+{
+    const int lane = threadIdx.x & 31, grp = lane >> 2, tig = lane & 3;
+    const float* row = V + (size_t)(nt * 8 + grp) * ldv;
+    if (!BF16) {
+        uint32_t bh0, bl0, bh1, bl1;
+        split_tf32(row[kt * 8 + tig], bh0, bl0);
+        split_tf32(row[kt * 8 + tig + 4], bh1, bl1);
+        mma_tf32(acc, alo, bh0, bh1);
+        mma_tf32(acc, ahi, bl0, bl1);
+        mma_tf32(acc, ahi, bh0, bh1);
+    } else {
+        const int k0 = kt * 16 + 2 * tig;
+        const float2 x0 = *reinterpret_cast<const float2*>(row + k0);
+        const float2 x1 = *reinterpret_cast<const float2*>(row + k0 + 8);
+        mma_bf16(acc, ahi, pack_bf16x2(x0.x, x0.y), pack_bf16x2(x1.x, x1.y));
     }
 }
 
@@ -191,9 +292,10 @@ __device__ __forceinline__ void stamp(const RecArgs& a, bool bwd, int dir, int c
 
 // ------------------------------------------------------------------------- forward
 
-template <typename RT>
+template <typename RT, bool MMA>
 __global__ void __launch_bounds__(kRecThreads, 1) lstm_rec_fwd_kernel(RecArgs a)
 {
+    constexpr bool BF16 = sizeof(RT) == 2;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int H = a.H, G = a.G, Umax = a.Umax, RP = 4 * Umax, JC = a.JC, T = a.T;
     const int dir = blockIdx.x / G;
@@ -227,6 +329,27 @@ __global__ void __launch_bounds__(kRecThreads, 1) lstm_rec_fwd_kernel(RecArgs a)
     }
     const Tables tb = load_tables(a, reinterpret_cast<int*>(smem_raw + a.off_tab));
     __syncthreads();
+    // tensor-core path: this warp's R fragments, resident in registers
+    const int warp = threadIdx.x >> 5;
+    const int mw = a.mma_mw, kw = a.mma_kw, MT = (RP + 15) / 16, KT = H / (BF16 ? 16 : 8);
+    const int ktw = (KT + kw - 1) / kw;
+    const int wm = warp / kw, wk = warp - (warp / kw) * kw;
+    const bool mma_warp = MMA && warp < mw * kw;
+    uint32_t fa_hi[kFwdMTW][kFwdKTW][4], fa_lo[kFwdMTW][kFwdKTW][4];
+    if (MMA) {
+        auto at = [&](int r, int k) -> float { return r < RP ? to_f32(Rs[(size_t)r * ldr + k]) : 0.f; };
+#pragma unroll
+        for (int i = 0; i < kFwdMTW; ++i)
+#pragma unroll
+            for (int q = 0; q < kFwdKTW; ++q) {
+                const int mt = wm + i * mw, kt = wk * ktw + q;
+                if (mma_warp && mt < MT && q < ktw && kt < KT) load_a_frag<BF16>(at, mt, kt, fa_hi[i][q], fa_lo[i][q]);
+                else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) fa_hi[i][q][e] = fa_lo[i][q][e] = 0u;
+                }
+            }
+    }
     // empty sequences have zero final state
     if (a.h_n) {
         for (int idx = threadIdx.x; idx < a.B * Uc; idx += kRecThreads) {
@@ -285,7 +408,57 @@ __global__ void __launch_bounds__(kRecThreads, 1) lstm_rec_fwd_kernel(RecArgs a)
             }
             __syncthreads();
             if (j0 == 0) stamp(a, false, dir, cta, s, 2);
-            smem_matmul<RT>(Rs, ldr, hs, ldh, RP, JC, H, jn, red, accs);
+            if (!MMA) {
+                smem_matmul<RT>(Rs, ldr, hs, ldh, RP, JC, H, jn, red, accs);
+            } else {
+                // accs[j][r] = sum over k-slices (warps wk) of the warps' m16 x n8 tiles
+                if (mma_warp) {
+                    const int lane = threadIdx.x & 31, grp = lane >> 2, tig = lane & 3;
+                    const int NT = (jn + 7) >> 3;
+                    float acc[kFwdMTW][4][4];
+#pragma unroll
+                    for (int i = 0; i < kFwdMTW; ++i)
+#pragma unroll
+                        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) acc[i][nt][e] = 0.f;
+#pragma unroll
+                    for (int q = 0; q < kFwdKTW; ++q) {
+                        const int kt = wk * ktw + q;
+                        if (q >= ktw || kt >= KT) continue;
+#pragma unroll
+                        for (int nt = 0; nt < 4; ++nt) {
+                            if (nt >= NT) continue;
+#pragma unroll
+                            for (int i = 0; i < kFwdMTW; ++i)
+                                if (wm + i * mw < MT) mma_step<BF16>(acc[i][nt], fa_hi[i][q], fa_lo[i][q], hs, ldh, nt, kt);
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < kFwdMTW; ++i) {
+                        const int mt = wm + i * mw;
+                        if (mt >= MT) continue;
+#pragma unroll
+                        for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int r = mt * 16 + grp + ((e & 2) ? 8 : 0);
+                                const int j = nt * 8 + 2 * tig + (e & 1);
+                                if (r < RP && j < jn) red[((size_t)wk * RP + r) * JC + j] = acc[i][nt][e];
+                            }
+                        }
+                    }
+                }
+                __syncthreads();
+                for (int o = threadIdx.x; o < RP * jn; o += kRecThreads) {
+                    const int j = o / RP, r = o - j * RP;
+                    float sacc = 0.f;
+                    for (int w2 = 0; w2 < kw; ++w2) sacc += red[((size_t)w2 * RP + r) * JC + j];
+                    accs[j * RP + r] = sacc;
+                }
+                __syncthreads();
+            }
+            if (j0 == 0) stamp(a, false, dir, cta, s, 5);
             // cell update, one (row, unit) per item
 #pragma unroll
             for (int k = 0; k < kMaxItems; ++k) {
@@ -298,10 +471,10 @@ __global__ void __launch_bounds__(kRecThreads, 1) lstm_rec_fwd_kernel(RecArgs a)
                     const float cp = j < n_prev ? cst[j * Umax + uu] : 0.f;
                     const float ig = sigmoidf_(pre[k][0] + ac[uu] + peep_s[uu] * cp);
                     const float fg = sigmoidf_(pre[k][1] + ac[Umax + uu] + peep_s[Umax + uu] * cp);
-                    const float zg = tanhf(pre[k][2] + ac[2 * Umax + uu]);
+                    const float zg = tanhf_(pre[k][2] + ac[2 * Umax + uu]);
                     float c = fg * cp + ig * zg;
                     const float og = sigmoidf_(pre[k][3] + ac[3 * Umax + uu] + peep_s[2 * Umax + uu] * c);
-                    float h = og * tanhf(c);
+                    float h = og * tanhf_(c);
                     const int len = tb.len[j];
                     if (a.padded && t >= len) { c = 0.f; h = 0.f; }
                     float* gr = a.ga + (size_t)row * nd4H + dir * 4 * H + u;
@@ -328,19 +501,22 @@ __global__ void __launch_bounds__(kRecThreads, 1) lstm_rec_fwd_kernel(RecArgs a)
 
 // ------------------------------------------------------------------------- backward
 
-template <typename RT>
+template <typename RT, bool MMA>
 __global__ void __launch_bounds__(kRecThreads, 1) lstm_rec_bwd_kernel(RecArgs a)
 {
+    constexpr bool BF16 = sizeof(RT) == 2;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int H = a.H, G = a.G, Umax = a.Umax, JC = a.JC, T = a.T, B = a.B;
-    const int RP8 = (4 * Umax + 7) & ~7;           // R rows padded to a multiple of 8
+    // R rows padded to a multiple of the MMA k-step (8 tf32, 16 bf16)
+    const int RP8 = BF16 ? ((4 * Umax + 15) & ~15) : ((4 * Umax + 7) & ~7);
+    const int ldd = RP8 + 4;                       // padded row stride of da_s
     const int dir = blockIdx.x / G;
     const int cta = blockIdx.x - dir * G;
     const int u0 = cta * Umax;
     const int Uc = max(0, min(Umax, H - u0));
     const int ldr = H + 16 / (int)sizeof(RT);
     RT* Rs = reinterpret_cast<RT*>(smem_raw);
-    float* da_s = reinterpret_cast<float*>(smem_raw + a.off_h);       // [JC][RP8]
+    float* da_s = reinterpret_cast<float*>(smem_raw + a.off_h);       // [JC][ldd]
     float* dcc = reinterpret_cast<float*>(smem_raw + a.off_state);    // [B][Umax]
     float* contrib = reinterpret_cast<float*>(smem_raw + a.off_contrib);   // [7][JC][Umax]
     float* sums = reinterpret_cast<float*>(smem_raw + a.off_sums);    // [7][Umax]
@@ -361,7 +537,7 @@ __global__ void __launch_bounds__(kRecThreads, 1) lstm_rec_bwd_kernel(RecArgs a)
         if (g < 4 && uu < Uc) v = Rg[(size_t)(g * H + u0 + uu) * H + k];
         Rs[(size_t)r * ldr + k] = v;
     }
-    for (int idx = threadIdx.x; idx < JC * RP8; idx += kRecThreads) da_s[idx] = 0.f;
+    for (int idx = threadIdx.x; idx < JC * ldd; idx += kRecThreads) da_s[idx] = 0.f;
     for (int idx = threadIdx.x; idx < 7 * Umax; idx += kRecThreads) sums[idx] = 0.f;
     for (int idx = threadIdx.x; idx < 3 * Umax; idx += kRecThreads) {
         const int q = idx / Umax, uu = idx - q * Umax;
@@ -369,6 +545,24 @@ __global__ void __launch_bounds__(kRecThreads, 1) lstm_rec_bwd_kernel(RecArgs a)
     }
     const Tables tb = load_tables(a, reinterpret_cast<int*>(smem_raw + a.off_tab));
     __syncthreads();
+    // tensor-core path: fragments of R^T (rows = units u', cols = this CTA's gate rows)
+    const int warp = threadIdx.x >> 5;
+    const int MTb = H / 16, KTb = RP8 / (BF16 ? 16 : 8);
+    uint32_t fb_hi[kBwdMTW][kBwdKTW][4], fb_lo[kBwdMTW][kBwdKTW][4];
+    if (MMA) {
+        auto at = [&](int up, int r) -> float { return to_f32(Rs[(size_t)r * ldr + up]); };
+#pragma unroll
+        for (int i = 0; i < kBwdMTW; ++i)
+#pragma unroll
+            for (int q = 0; q < kBwdKTW; ++q) {
+                const int mt = warp + i * (kRecThreads / 32);
+                if (mt < MTb && q < KTb) load_a_frag<BF16>(at, mt, q, fb_hi[i][q], fb_lo[i][q]);
+                else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) fb_hi[i][q][e] = fb_lo[i][q][e] = 0u;
+                }
+            }
+    }
 
     for (int s = 0; s < T; ++s) {
         const int t = dir == 0 ? T - 1 - s : s;
@@ -432,7 +626,7 @@ __global__ void __launch_bounds__(kRecThreads, 1) lstm_rec_bwd_kernel(RecArgs a)
                     if (real) {
                         const float dh = op[k][6] + dh_rec;
                         const float carry = has_next ? dcc[j * Umax + uu] : 0.f;
-                        const float tc = tanhf(c);
+                        const float tc = tanhf_(c);
                         dao = dh * tc * og * (1.f - og);
                         const float dc = dh * og * (1.f - tc * tc) + dao * peep_s[2 * Umax + uu] + carry;
                         dai = dc * zg * ig * (1.f - ig);
@@ -442,7 +636,7 @@ __global__ void __launch_bounds__(kRecThreads, 1) lstm_rec_bwd_kernel(RecArgs a)
                     }
                     float* gr = a.ga + (size_t)row * nd4H + dir * 4 * H + u;
                     gr[0] = dai; gr[H] = daf; gr[2 * H] = daz; gr[3 * H] = dao;
-                    float* dr = da_s + jj * RP8 + uu;
+                    float* dr = da_s + jj * ldd + uu;
                     if (a.bf16) {
                         dr[0] = bf16_round(dai); dr[Umax] = bf16_round(daf);
                         dr[2 * Umax] = bf16_round(daz); dr[3 * Umax] = bf16_round(dao);
@@ -459,7 +653,31 @@ __global__ void __launch_bounds__(kRecThreads, 1) lstm_rec_bwd_kernel(RecArgs a)
             __syncthreads();
             if (j0 == 0) stamp(a, true, dir, cta, s, 2);
             // this CTA's share of R^T da for every unit, read by all peers at the next step
-            if (s + 1 < T) {
+            if (s + 1 < T && MMA) {
+                // D(u', j) = sum_r R[r][u'] da[j][r]: m16 tiles of units, n8 tiles of rows
+                const int lane = threadIdx.x & 31, grp = lane >> 2, tig = lane & 3;
+                const int NT = (jn + 7) >> 3;
+#pragma unroll
+                for (int i = 0; i < kBwdMTW; ++i) {
+                    const int mt = warp + i * (kRecThreads / 32);
+                    if (mt >= MTb) continue;
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt) {
+                        if (nt >= NT) continue;
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int q = 0; q < kBwdKTW; ++q)
+                            if (q < KTb) mma_step<BF16>(acc, fb_hi[i][q], fb_lo[i][q], da_s, ldd, nt, q);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int up = mt * 16 + grp + ((e & 2) ? 8 : 0);
+                            const int jj = nt * 8 + 2 * tig + (e & 1);
+                            if (jj < jn) part_at(wr, j0 + jj, cta)[up] = acc[e];
+                        }
+                    }
+                }
+            }
+            if (s + 1 < T && !MMA) {
                 for (int up = threadIdx.x; up < H; up += kRecThreads) {
                     float acc[kMaxJC];
 #pragma unroll
@@ -472,7 +690,7 @@ __global__ void __launch_bounds__(kRecThreads, 1) lstm_rec_bwd_kernel(RecArgs a)
                         for (int jj = 0; jj < kMaxJC; ++jj) {
                             if (jj < jn) {
                                 float d[8];
-                                load8(da_s + jj * RP8 + r0, d);
+                                load8(da_s + jj * ldd + r0, d);
                                 float v = acc[jj];
 #pragma unroll
                                 for (int e = 0; e < 8; ++e) v = fmaf(rv[e], d[e], v);
@@ -485,6 +703,7 @@ __global__ void __launch_bounds__(kRecThreads, 1) lstm_rec_bwd_kernel(RecArgs a)
                         if (jj < jn) part_at(wr, j0 + jj, cta)[up] = acc[jj];
                 }
             }
+            if (j0 == 0) stamp(a, true, dir, cta, s, 5);
             for (int idx = threadIdx.x; idx < 7 * Uc; idx += kRecThreads) {
                 const int q = idx / Uc, uu = idx - q * Uc;
                 const float* cb = contrib + (size_t)q * JC * Umax + uu;
@@ -530,13 +749,14 @@ static size_t rec_layout(const RecConfig& c, int H, int B, int T, int relem, boo
         const int RP = 4 * Umax;
         off = align_up((size_t)RP * (H + 16 / relem) * relem, 16);
         o_h = off; off = align_up(off + (size_t)JC * (H + 4) * 4, 16);
-        o_red = off; off = align_up(off + (size_t)matmul_red_floats(RP, JC, H) * 4, 16);
+        o_red = off;
+        off = align_up(off + (size_t)std::max(matmul_red_floats(RP, JC, H), 8 * RP * JC) * 4, 16);
         o_acc = off; off = align_up(off + (size_t)JC * RP * 4, 16);
         o_state = off; off = align_up(off + (size_t)B * Umax * 4, 16);
     } else {
-        const int RP8 = (4 * Umax + 7) & ~7;
+        const int RP8 = relem == 2 ? ((4 * Umax + 15) & ~15) : ((4 * Umax + 7) & ~7);
         off = align_up((size_t)RP8 * (H + 16 / relem) * relem, 16);
-        o_h = off; off = align_up(off + (size_t)JC * RP8 * 4, 16);
+        o_h = off; off = align_up(off + (size_t)JC * (RP8 + 4) * 4, 16);
         o_state = off; off = align_up(off + (size_t)B * Umax * 4, 16);
         o_contrib = off; off = align_up(off + (size_t)7 * JC * Umax * 4, 16);
         o_sums = off; off = align_up(off + (size_t)7 * Umax * 4, 16);
@@ -574,6 +794,25 @@ lstm_status rec_configure(const Plan& p, int H, int ndir, bool bf16, bool bwd, i
     const int relem = bf16 ? 2 : 4;
     RecConfig c;
     c.G = G; c.Umax = Umax;
+    // tensor-core product when this CTA's fragments fit the per-warp register budget
+    const int ksz = bf16 ? 16 : 8;
+    if (p.gemm_engine == 1) {
+        // CUDA cores only
+    } else if (!bwd) {
+        const int MT = (4 * Umax + 15) / 16;
+        if (H % ksz == 0) {
+            const int KT = H / ksz;
+            for (int mw = 1; mw <= kRecThreads / 32 && !c.mma; ++mw)
+                for (int kw = kRecThreads / 32 / mw; kw >= 1; --kw)
+                    if (ceil_div(MT, mw) <= kFwdMTW && ceil_div(KT, kw) <= kFwdKTW) {
+                        c.mma = 1; c.mma_mw = mw; c.mma_kw = kw;
+                        break;
+                    }
+        }
+    } else {
+        const int RPK = bf16 ? ((4 * Umax + 15) & ~15) : ((4 * Umax + 7) & ~7);
+        if (H % 16 == 0 && ceil_div(H / 16, kRecThreads / 32) <= kBwdMTW && RPK / ksz <= kBwdKTW) c.mma = 1;
+    }
     c.JC = 0;
     for (int tables = 1; tables >= 0 && c.JC == 0; --tables) {
         for (int jc : {32, 16, 8, 4}) {
@@ -602,9 +841,15 @@ lstm_status rec_launch(const Plan& p, const RecConfig& c, RecArgs a, bool bwd, c
     a.G = c.G; a.Umax = c.Umax; a.JC = c.JC;
     a.trace = p.d_trace; a.trace_steps = p.trace_steps;
     rec_layout(c, a.H, p.B, p.T, a.bf16 ? 2 : 4, bwd, &a);
+    a.mma_mw = c.mma_mw; a.mma_kw = c.mma_kw;
     void* fn;
-    if (!bwd) fn = a.bf16 ? (void*)lstm_rec_fwd_kernel<__nv_bfloat16> : (void*)lstm_rec_fwd_kernel<float>;
-    else fn = a.bf16 ? (void*)lstm_rec_bwd_kernel<__nv_bfloat16> : (void*)lstm_rec_bwd_kernel<float>;
+    if (!bwd) {
+        if (c.mma) fn = a.bf16 ? (void*)lstm_rec_fwd_kernel<__nv_bfloat16, true> : (void*)lstm_rec_fwd_kernel<float, true>;
+        else fn = a.bf16 ? (void*)lstm_rec_fwd_kernel<__nv_bfloat16, false> : (void*)lstm_rec_fwd_kernel<float, false>;
+    } else {
+        if (c.mma) fn = a.bf16 ? (void*)lstm_rec_bwd_kernel<__nv_bfloat16, true> : (void*)lstm_rec_bwd_kernel<float, true>;
+        else fn = a.bf16 ? (void*)lstm_rec_bwd_kernel<__nv_bfloat16, false> : (void*)lstm_rec_bwd_kernel<float, false>;
+    }
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem) != cudaSuccess)
         return LSTM_ERR_CUDA;
     // fresh step counters for this launch

@@ -30,6 +30,7 @@ struct RecArgs {
     long long* trace;         // optional [ndir][trace_steps][8] clock64 stamps of each direction's CTA 0
     int trace_steps;
     int tables_in_smem;
+    int mma_mw, mma_kw;       // forward tensor-core product: warps along rows and along k
     // dynamic shared-memory layout (byte offsets)
     int off_h, off_red, off_acc, off_state, off_contrib, off_sums, off_tab, off_peep;
 };
@@ -39,9 +40,14 @@ struct RecConfig {
     int Umax = 0;       // units per CTA
     int JC = 0;         // rows per staged chunk
     int tables = 0;     // step tables copied to shared memory
+    int mma = 0;        // 1: warp-level tensor-core product (mma.sync), 0: CUDA cores
+    int mma_mw = 1, mma_kw = 1;
     size_t smem = 0;    // dynamic shared memory bytes
 };
 
+// Launch configuration of the recurrent kernels.  The per-step product runs
+// on warp-level tensor cores when the CTA's fragments fit and the plan's
+// engine allows it (gemm_engine 0), otherwise on CUDA cores.
 lstm_status rec_configure(const Plan& p, int H, int ndir, bool bf16, bool bwd, int forced_G,
                           RecConfig* out);
 lstm_status rec_launch(const Plan& p, const RecConfig& c, RecArgs a, bool bwd, cudaStream_t s);

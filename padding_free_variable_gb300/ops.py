@@ -78,6 +78,10 @@ class Plan:
         """Phase stamps into `buffer` (int64 device tensor of 2*ndir*steps*8), or off with steps=0."""
         check(_lib.load().lstm_debug_trace_steps(self.handle, _ptr(buffer), int(steps)), "lstm_debug_trace_steps")
 
+    def set_gemm_engine(self, engine: int):
+        """0 = tensor cores for bf16 operands (default), 1 = CUDA cores."""
+        check(_lib.load().lstm_plan_set_gemm_engine(self.handle, int(engine)), "lstm_plan_set_gemm_engine")
+
     def debug_skip_arrival(self, cta: int):
         check(_lib.load().lstm_debug_skip_arrival(self.handle, int(cta)), "lstm_debug_skip_arrival")
 
@@ -129,6 +133,12 @@ def scratch_bytes(plan: Plan, shape: LayerShape) -> int:
 def _params(layer: dict) -> LayerParams:
     return LayerParams(layer["W"].data_ptr(), layer["R"].data_ptr(), layer["b"].data_ptr(),
                        layer["peep"].data_ptr())
+
+
+def input_projection(plan: Plan, shape: LayerShape, layer: dict, x_packed, out, stream=None):
+    check(_lib.load().lstm_debug_input_projection(plan.handle, ctypes.byref(shape), ctypes.byref(_params(layer)),
+                                                  _ptr(x_packed), _ptr(out), _stream(stream)),
+          "lstm_debug_input_projection")
 
 
 def layer_forward(plan: Plan, shape: LayerShape, layer: dict, x_packed, y_packed, y_lo, h_n, c_n,

@@ -72,7 +72,7 @@ def device_layers(w, device="cuda"):
     return out
 
 
-def run_gpu(w, padded: bool = False, device="cuda", ctas: int = 0):
+def run_gpu(w, padded: bool = False, device="cuda", ctas: int = 0, engine: int = 0):
     """pack -> all layers forward -> all layers backward -> unpack, through the C ABI."""
     import torch
     from padding_free_variable_gb300 import ops
@@ -80,6 +80,8 @@ def run_gpu(w, padded: bool = False, device="cuda", ctas: int = 0):
     plan = ops.Plan(w.lengths, padded=padded)
     if ctas:
         plan.set_ctas_per_direction(ctas)
+    if engine:
+        plan.set_gemm_engine(engine)
     stack = ops.PackedLSTMStack(plan, device_layers(w, device), w.spec.input_size, w.spec.hidden_size,
                                 w.spec.num_directions, bf16, device)
     x = torch.from_numpy(w.x).to(device=device, dtype=torch.bfloat16 if bf16 else torch.float32)

@@ -98,6 +98,30 @@ def test_bf16_workloads_full_size_sampled(wid):
     assert all(v <= TOL_BF16 for v in errs.values()), errs
 
 
+ENGINE_CASES = [
+    (2, 1, 16, 64, [9, 0, 4, 13, 13, 2, 7], "f32", 4),
+    (2, 2, 24, 40, [17, 2, 9, 33, 1, 0, 12], "f32", 3),
+    (1, 2, 8, 32, [5, 40, 39, 1, 2, 3, 4, 30], "f32", 0),
+    (2, 2, 16, 48, [9, 0, 4, 21, 21, 2], "bf16", 7),
+    (2, 1, 32, 256, [60, 3, 44, 17, 60, 9], "bf16", 0),
+]
+
+
+@pytest.mark.parametrize("engine", [0, 1], ids=["tensor-cores", "cuda-cores"])
+@pytest.mark.parametrize("case", ENGINE_CASES, ids=[f"nd{c[0]}-L{c[1]}-H{c[3]}-{c[5]}-g{c[6]}" for c in ENGINE_CASES])
+def test_both_product_engines(case, engine):
+    """The tensor-core and the CUDA-core products of every kernel against the oracle."""
+    nd, nl, D, H, lengths, dtype, ctas = case
+    w = synthetic.custom(nd, nl, D, H, lengths, seed=11 + H, dtype=dtype,
+                         weight_range=0.1 if dtype == "bf16" else 0.3)
+    gpu = run_gpu(w, ctas=ctas, engine=engine)
+    ref = run_oracle(w)
+    compare_all(gpu, ref, TOL_BF16 if dtype == "bf16" else TOL_F32, label=f"{case} engine={engine}")
+    if dtype == "bf16":
+        emu = run_oracle(w, bf16_products=True)
+        compare_all(gpu, emu, TOL_BF16_EMULATED, label=f"{case} engine={engine}", against="oracle-bf16-products")
+
+
 def test_padded_comparator_matches_oracle():
     """Invariant I3 on the GPU: the padded, masked run gives the per-sequence results."""
     w = synthetic.custom(2, 2, 12, 24, [6, 0, 2, 9, 1, 6], seed=31, weight_range=0.4)
