@@ -307,7 +307,8 @@ typedef enum {
     LSTM_KERNEL_GEMM_DX = 5,    /* backward: dX = dA W */
     LSTM_KERNEL_GEMM_DW = 6,    /* backward: dW = dA^T X (with its split-K sum) */
     LSTM_KERNEL_GEMM_DR = 7,    /* backward: dR = dA^T H_prev (with its split-K sum) */
-    LSTM_KERNEL_KINDS = 8
+    LSTM_KERNEL_CONVERT = 8,    /* backward, bf16: transposed bf16 operands of dX, dW, dR */
+    LSTM_KERNEL_KINDS = 9
 } lstm_kernel_kind;
 
 /* Tracing ("CUDA events around each launch"): with timing enabled every

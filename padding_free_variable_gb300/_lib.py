@@ -31,7 +31,7 @@ EXPORTED = (
     "lstm_plan_set_gemm_engine", "lstm_debug_input_projection",
 )
 
-KERNEL_KINDS = ("pack", "unpack", "input_gemm", "rec_fwd", "rec_bwd", "gemm_dx", "gemm_dw", "gemm_dr")
+KERNEL_KINDS = ("pack", "unpack", "input_gemm", "rec_fwd", "rec_bwd", "gemm_dx", "gemm_dw", "gemm_dr", "convert")
 
 
 class LayerShape(ctypes.Structure):

@@ -55,17 +55,50 @@ void bwd_gemm_shapes(const Plan& p, const lstm_layer_shape& s, GemmDesc* dW, Gem
     dX->M = (int)p.rows; dX->N = D; dX->K = nd * 4 * H; dX->k_splits = 8;
 }
 
-// The backward kernel's partial-product exchange and the split-K partial
-// sums of the gradient products are never live at the same time: one region.
-size_t scratch_floats(const Plan& p, const lstm_layer_shape& s)
+constexpr int kMaxTcSplits = 16;
+
+// Scratch of lstm_bwd.  Region U holds the recurrent kernel's partial-product
+// exchange, later the split-K partial sums (never live at the same time).  The
+// bf16 path adds its tensor-core operands: dA (row-major and transposed), X^T,
+// H_prev^T and W^T, all bf16, the frame dimension padded to a multiple of 8.
+struct BwdScratch {
+    size_t u_bytes = 0, dA16 = 0, dAT16 = 0, XT16 = 0, HpT16 = 0, WT16 = 0, total = 0;
+    int64_t ldr = 0;   // padded frame count (row pitch of the transposes)
+};
+
+BwdScratch bwd_scratch(const Plan& p, const lstm_layer_shape& s)
 {
+    BwdScratch b;
     GemmDesc dW, dR, dX;
     bwd_gemm_shapes(p, s, &dW, &dR, &dX);
-    const size_t gemm = std::max(std::max(gemm_partial_floats(dW, p.num_sms), gemm_partial_floats(dR, p.num_sms)),
-                                 gemm_partial_floats(dX, p.num_sms));
-    const size_t part = rec_bwd_part_floats(p, s.hidden_size, s.num_directions, s.dtype == LSTM_BF16,
-                                            p.forced_ctas);
-    return std::max(gemm, part);
+    const int H = s.hidden_size, nd = s.num_directions, D = s.input_size;
+    size_t gemm = std::max(std::max(gemm_partial_floats(dW, p.num_sms), gemm_partial_floats(dR, p.num_sms)),
+                           gemm_partial_floats(dX, p.num_sms));
+    const size_t part = rec_bwd_part_floats(p, H, nd, s.dtype == LSTM_BF16, p.forced_ctas);
+    if (s.dtype == LSTM_BF16) {
+        const int rows = (int)p.rows;
+        const size_t tc = std::max((size_t)gemm_tc_splits(nd * 4 * H, D, rows, p.num_sms, kMaxTcSplits) * nd * 4 * H * D,
+                                   (size_t)gemm_tc_splits(4 * H, H, rows, p.num_sms, kMaxTcSplits) * 4 * H * H);
+        gemm = std::max(gemm, tc);
+    }
+    b.u_bytes = align256(std::max<size_t>(1, std::max(gemm, part)) * sizeof(float));
+    size_t off = b.u_bytes;
+    if (s.dtype == LSTM_BF16) {
+        const size_t rows = (size_t)p.rows, G4 = (size_t)nd * 4 * H;
+        b.ldr = (int64_t)((rows + 7) / 8 * 8);
+        b.dA16 = off; off += align256(rows * G4 * 2);
+        b.dAT16 = off; off += align256(G4 * (size_t)b.ldr * 2);
+        b.XT16 = off; off += align256((size_t)D * b.ldr * 2);
+        b.HpT16 = off; off += align256((size_t)nd * H * b.ldr * 2);
+        b.WT16 = off; off += align256((size_t)D * G4 * 2);
+    }
+    b.total = off;
+    return b;
+}
+
+size_t scratch_floats(const Plan& p, const lstm_layer_shape& s)
+{
+    return bwd_scratch(p, s).total / sizeof(float);
 }
 
 RecArgs base_args(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm, float* ga,
@@ -98,6 +131,56 @@ lstm_status input_projection(const Plan& p, const lstm_layer_shape& s, const lst
     g.B = prm.W; g.sbk = 1; g.sbn = D; g.b_bf16 = bf16;
     g.C = out; g.ldc = nd * 4 * H; g.bias = prm.b;
     return gemm_simt(g, p, K_GEMM_IN, cs);
+}
+
+bool encode_ready() { return gemm_tc_supported(1, 1, 8, nullptr, nullptr); }
+
+// dX, dW and dR of a bf16 layer on tcgen05, from the gate errors dA (fp32, in
+// the workspace) and bf16 transposes built in the scratch.
+lstm_status bwd_products_tc(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm,
+                            const void* x_packed, const float* y_packed, const float* ga, float* dx_packed,
+                            const lstm_layer_grads& g, void* scratch, cudaStream_t cs)
+{
+    const int H = s.hidden_size, nd = s.num_directions, D = s.input_size, rows = (int)p.rows;
+    const int G4 = nd * 4 * H;
+    const BwdScratch b = bwd_scratch(p, s);
+    char* base = (char*)scratch;
+    float* partial = (float*)base;
+    void* dA16 = base + b.dA16;
+    char* dAT16 = base + b.dAT16;
+    void* XT16 = base + b.XT16;
+    char* HpT16 = base + b.HpT16;
+    void* WT16 = base + b.WT16;
+    lstm_status st;
+    // operands: dA as bf16 rows and columns, X^T, H_prev^T per direction, W^T
+    if ((st = transpose_to_bf16(p, ga, false, G4, 0, nullptr, rows, G4, dAT16, b.ldr, dA16, G4, cs)) != LSTM_OK)
+        return st;
+    if ((st = transpose_to_bf16(p, x_packed, true, D, 0, nullptr, rows, D, XT16, b.ldr, nullptr, 0, cs)) != LSTM_OK)
+        return st;
+    for (int d = 0; d < nd; ++d)
+        if ((st = transpose_to_bf16(p, y_packed, false, (int64_t)nd * H, d * H, d == 0 ? p.d_prev_fwd : p.d_prev_rev,
+                                    rows, H, HpT16 + (size_t)d * H * b.ldr * 2, b.ldr, nullptr, 0, cs)) != LSTM_OK)
+            return st;
+    if ((st = transpose_to_bf16(p, prm.W, true, D, 0, nullptr, G4, D, WT16, G4, nullptr, 0, cs)) != LSTM_OK)
+        return st;
+    // dX[rows][D] = dA[rows][G4] W[G4][D]
+    if (dx_packed &&
+        (st = gemm_tc_bf16(p, K_GEMM_DX, dA16, G4, WT16, G4, rows, D, G4, dx_packed, D, nullptr, 1, nullptr, cs)) !=
+            LSTM_OK)
+        return st;
+    // dW[G4][D] = dA^T X, K = frames
+    int sp = gemm_tc_splits(G4, D, rows, p.num_sms, kMaxTcSplits);
+    if ((st = gemm_tc_bf16(p, K_GEMM_DW, dAT16, b.ldr, XT16, b.ldr, G4, D, rows, g.dW, D, nullptr, sp, partial,
+                           cs)) != LSTM_OK)
+        return st;
+    // dR_d[4H][H] = dA_d^T H_prev_d, K = frames
+    sp = gemm_tc_splits(4 * H, H, rows, p.num_sms, kMaxTcSplits);
+    for (int d = 0; d < nd; ++d)
+        if ((st = gemm_tc_bf16(p, K_GEMM_DR, dAT16 + (size_t)d * 4 * H * b.ldr * 2, b.ldr,
+                               HpT16 + (size_t)d * H * b.ldr * 2, b.ldr, 4 * H, H, rows, g.dR + (size_t)d * 4 * H * H,
+                               H, nullptr, sp, partial, cs)) != LSTM_OK)
+            return st;
+    return LSTM_OK;
 }
 
 lstm_status check_params(const lstm_layer_params* prm)
@@ -206,6 +289,8 @@ lstm_status lstm_bwd(const lstm_plan* plan, const lstm_layer_shape* shape,
     if ((st = rec_launch(p, rc, a, true, cs)) != LSTM_OK) return st;
 
     const int nd4H = nd * 4 * H;
+    if (bf16 && p.gemm_engine == 0 && D % 8 == 0 && encode_ready())
+        return bwd_products_tc(p, s, *params, x_packed, y_packed, ga, dx_packed, *grads, scratch, cs);
     GemmDesc gw, gr, gx;
     bwd_gemm_shapes(p, s, &gw, &gr, &gx);
     if (dx_packed) {

@@ -21,7 +21,7 @@ struct DeviceStatus {
 
 // Kinds of work the tracer times (matches lstm_kernel_kind in the header).
 enum KernelKind {
-    K_PACK = 0, K_UNPACK, K_GEMM_IN, K_REC_FWD, K_REC_BWD, K_GEMM_DX, K_GEMM_DW, K_GEMM_DR, K_NUM
+    K_PACK = 0, K_UNPACK, K_GEMM_IN, K_REC_FWD, K_REC_BWD, K_GEMM_DX, K_GEMM_DW, K_GEMM_DR, K_CONVERT, K_NUM
 };
 
 // Optional CUDA-event timing of every library launch, and a launch counter.

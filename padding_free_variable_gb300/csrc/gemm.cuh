@@ -34,7 +34,25 @@ lstm_status gemm_simt_run(const GemmDesc& d, int num_sms, cudaStream_t s);
 lstm_status gemm_simt(const GemmDesc& d, const Plan& p, int kind, cudaStream_t s);
 
 // bf16 A[M][K] x B[N][K]^T (+ bias) on tcgen05 tensor cores, fp32 out.
+// Row pitches lda, ldb in elements (multiples of 8); K may be any positive
+// size (the tail reads zeros).  splits > 1 cuts K into that many ranges whose
+// partial products go to `partial` ([splits][M][N]) and are then added in
+// split order, plus bias, into C.
 bool gemm_tc_supported(int M, int N, int K, const void* A, const void* B);
+int gemm_tc_splits(int M, int N, int K, int num_sms, int max_splits);
+lstm_status gemm_tc_bf16(const Plan& p, int kind, const void* A, int64_t lda, const void* B, int64_t ldb, int M,
+                         int N, int K, float* C, int64_t ldc, const float* bias, int splits, float* partial,
+                         cudaStream_t s);
+
+// dstT[c][r] = bf16(src[row(r)][col0 + c]) (row(r) = map ? map[r] : r, negative
+// map entries read 0), optionally also dst_rm[r][c]; src fp32 or bf16.
+lstm_status transpose_to_bf16(const Plan& p, const void* src, bool src_bf16, int64_t lds, int col0,
+                              const int32_t* map, int rows, int cols, void* dstT, int64_t ldt, void* dst_rm,
+                              int64_t ldm, cudaStream_t s);
+
+// C = sum over splits (in split order) of partial, + bias.
+cudaError_t splitk_reduce(const float* partial, int splits, int M, int N, float* C, int64_t ldc,
+                          const float* bias, int num_sms, cudaStream_t s);
 lstm_status gemm_tc_bf16_nt(const Plan& p, int kind, const void* A, const void* B, float* C, int64_t ldc,
                             const float* bias, int M, int N, int K, cudaStream_t s);
 

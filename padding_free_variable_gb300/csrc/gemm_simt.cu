@@ -6,6 +6,8 @@
 // gradients with respect to the weights and the inputs after the recurrent
 // part has been back-propagated.  The fp32 path keeps full fp32 products
 // (CUDA-core FFMA): tf32 tensor cores would not hold a 1e-4 relative error.
+#include <algorithm>
+
 #include "gemm.cuh"
 
 namespace lstm {
@@ -158,16 +160,22 @@ lstm_status launch_typed(const GemmDesc& desc, int splits, int k_chunk, int num_
     else if (!akc && bkc) gemm_simt_kernel<TA, TB, false, true><<<grid, THREADS, 0, s>>>(d, k_chunk);
     else gemm_simt_kernel<TA, TB, false, false><<<grid, THREADS, 0, s>>>(d, k_chunk);
     if (cudaGetLastError() != cudaSuccess) return LSTM_ERR_CUDA;
-    if (splits > 1) {
-        const int64_t total = (int64_t)d.M * d.N;
-        int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)num_sms * 8);
-        splitk_reduce_kernel<<<blocks, 256, 0, s>>>(d.partial, splits, d.M, d.N, d.C, d.ldc, d.bias);
-        if (cudaGetLastError() != cudaSuccess) return LSTM_ERR_CUDA;
-    }
+    if (splits > 1 && splitk_reduce(d.partial, splits, d.M, d.N, d.C, d.ldc, d.bias, num_sms, s) != cudaSuccess)
+        return LSTM_ERR_CUDA;
     return LSTM_OK;
 }
 
 }  // namespace
+
+cudaError_t splitk_reduce(const float* partial, int splits, int M, int N, float* C, int64_t ldc,
+                          const float* bias, int num_sms, cudaStream_t s)
+{
+    const int64_t total = (int64_t)M * N;
+    if (total == 0) return cudaSuccess;
+    const int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)num_sms * 8);
+    splitk_reduce_kernel<<<blocks, 256, 0, s>>>(partial, splits, M, N, C, ldc, bias);
+    return cudaGetLastError();
+}
 
 int gemm_choose_splits(const GemmDesc& d, int num_sms)
 {

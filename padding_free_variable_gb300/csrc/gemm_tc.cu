@@ -15,6 +15,8 @@
 // word and the CTA still frees its tensor memory before returning.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "gemm.cuh"
 #include "tc_ptx.cuh"
 
@@ -31,9 +33,11 @@ constexpr size_t TC_SMEM = 1024 + (size_t)TSTAGES * (A_BYTES + B_BYTES) + 256;
 
 struct TcArgs {
     int M, N, K;
+    int k_chunk;          // k range of split z: [z*k_chunk, min(K, (z+1)*k_chunk)), multiple of 64
     float* C;
     int64_t ldc;
-    const float* bias;
+    const float* bias;    // added only without split
+    float* partial;       // split > 1: [z][M][N]
     DeviceStatus* status;
     unsigned long long limit_ns;
 };
@@ -59,7 +63,13 @@ gemm_tc_bf16_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * TBM, n0 = blockIdx.x * TBN;
-    const int nk = (a.K + TBK - 1) / TBK;
+    const int kbeg = blockIdx.z * a.k_chunk;
+    const int kend = min(a.K, kbeg + a.k_chunk);
+    const int nk = kend > kbeg ? (kend - kbeg + TBK - 1) / TBK : 0;
+    const bool split = gridDim.z > 1;
+    float* const Cout = split ? a.partial + (int64_t)blockIdx.z * a.M * a.N : a.C;
+    const int64_t ldo = split ? (int64_t)a.N : a.ldc;
+    const float* const bias = split ? nullptr : a.bias;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < TSTAGES; ++s) {
@@ -91,8 +101,8 @@ gemm_tc_bf16_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
             }
             if (*(volatile int*)s_abort) break;
             tc::mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
-            tc::tma_load_2d(sA + s * A_BYTES, &mapA, &full[s], kb * TBK, m0);
-            tc::tma_load_2d(sB + s * B_BYTES, &mapB, &full[s], kb * TBK, n0);
+            tc::tma_load_2d(sA + s * A_BYTES, &mapA, &full[s], kbeg + kb * TBK, m0);
+            tc::tma_load_2d(sB + s * B_BYTES, &mapB, &full[s], kbeg + kb * TBK, n0);
         }
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
@@ -121,29 +131,35 @@ gemm_tc_bf16_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
         if (!ok && lane == 0) fail(a, s_abort, 3);
         tc::tc_fence_after_sync();
         if (__all_sync(0xffffffffu, ok) && !*(volatile int*)s_abort) {
-            const bool vec = (a.ldc % 4) == 0 && (((uintptr_t)a.C) & 15u) == 0;
+            const bool vec = (ldo % 4) == 0 && (((uintptr_t)Cout) & 15u) == 0;
             for (int c = 0; c < TBN; c += 16) {
                 if (n0 + c >= a.N) break;                      // uniform across the warp
                 uint32_t r[16];
-                tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c, r);
-                tc::tmem_wait_ld();
+                if (nk > 0) {
+                    tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c, r);
+                    tc::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r[e] = 0u;   // empty k range: a zero product
+                }
                 if (row < a.M) {
                     const int n = n0 + c;
-                    float* out = a.C + (int64_t)row * a.ldc + n;
+                    float* out = Cout + (int64_t)row * ldo + n;
                     float v[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
                     if (n + 16 <= a.N && vec) {
-                        if (a.bias) {
+                        if (bias) {
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) v[e] += __ldg(a.bias + n + e);
+                            for (int e = 0; e < 16; ++e) v[e] += __ldg(bias + n + e);
                         }
 #pragma unroll
                         for (int e = 0; e < 16; e += 4)
                             *reinterpret_cast<float4*>(out + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
                     } else {
-                        for (int e = 0; e < 16 && n + e < a.N; ++e)
-                            out[e] = v[e] + (a.bias ? __ldg(a.bias + n + e) : 0.f);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            if (n + e < a.N) out[e] = v[e] + (bias ? __ldg(bias + n + e) : 0.f);
                     }
                 }
             }
@@ -174,13 +190,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// Row-major bf16 [rows][cols] (cols = K innermost) as 128-byte-swizzled boxes of 64 x box_rows.
-bool make_map(CUtensorMap* map, const void* ptr, int rows, int cols, int box_rows)
+// Row-major bf16 [rows][cols] with row pitch ld elements (cols = K innermost)
+// as 128-byte-swizzled boxes of 64 x box_rows; out-of-range elements read 0.
+bool make_map(CUtensorMap* map, const void* ptr, int rows, int cols, int64_t ld, int box_rows)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
     cuuint32_t box[2] = {(cuuint32_t)TBK, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -197,12 +214,25 @@ bool gemm_tc_supported(int M, int N, int K, const void* A, const void* B)
            encode_fn() != nullptr;
 }
 
-lstm_status gemm_tc_bf16_nt(const Plan& p, int kind, const void* A, const void* B, float* C, int64_t ldc,
-                            const float* bias, int M, int N, int K, cudaStream_t s)
+int gemm_tc_splits(int M, int N, int K, int num_sms, int max_splits)
 {
-    if (!gemm_tc_supported(M, N, K, A, B)) return LSTM_ERR_UNSUPPORTED;
+    const int tiles = ((N + TBN - 1) / TBN) * ((M + TBM - 1) / TBM);
+    const int kblocks = (K + TBK - 1) / TBK;
+    int splits = std::max(1, num_sms / std::max(1, tiles));
+    splits = std::min(splits, std::min(max_splits, std::max(1, kblocks / 4)));
+    return std::max(1, splits);
+}
+
+lstm_status gemm_tc_bf16(const Plan& p, int kind, const void* A, int64_t lda, const void* B, int64_t ldb, int M,
+                         int N, int K, float* C, int64_t ldc, const float* bias, int splits, float* partial,
+                         cudaStream_t s)
+{
+    if (M <= 0 || N <= 0) return LSTM_OK;
+    if (K <= 0 || lda % 8 != 0 || ldb % 8 != 0 || ((uintptr_t)A & 15u) || ((uintptr_t)B & 15u) || !encode_fn())
+        return LSTM_ERR_UNSUPPORTED;
+    if (splits > 1 && !partial) return LSTM_ERR_INVALID_ARG;
     CUtensorMap mapA, mapB;
-    if (!make_map(&mapA, A, M, K, TBM) || !make_map(&mapB, B, N, K, TBN)) return LSTM_ERR_UNSUPPORTED;
+    if (!make_map(&mapA, A, M, K, lda, TBM) || !make_map(&mapB, B, N, K, ldb, TBN)) return LSTM_ERR_UNSUPPORTED;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(gemm_tc_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM) !=
@@ -210,15 +240,32 @@ lstm_status gemm_tc_bf16_nt(const Plan& p, int kind, const void* A, const void* 
             return LSTM_ERR_CUDA;
         attr_set = true;
     }
+    const int kblocks = (K + TBK - 1) / TBK;
+    if (splits < 1) splits = 1;
+    const int kb_per = (kblocks + splits - 1) / splits;
+    splits = (kblocks + kb_per - 1) / kb_per;          // every split gets at least one k-block
     TcArgs a;
-    a.M = M; a.N = N; a.K = K; a.C = C; a.ldc = ldc; a.bias = bias;
+    a.M = M; a.N = N; a.K = K; a.k_chunk = kb_per * TBK;
+    a.C = C; a.ldc = ldc; a.bias = bias; a.partial = partial;
     a.status = p.d_status; a.limit_ns = p.wait_limit_ns;
-    const dim3 grid((N + TBN - 1) / TBN, (M + TBM - 1) / TBM);
+    const dim3 grid((N + TBN - 1) / TBN, (M + TBM - 1) / TBM, splits);
     trace_begin(p, kind, s);
     gemm_tc_bf16_kernel<<<grid, TC_THREADS, TC_SMEM, s>>>(mapA, mapB, a);
-    const cudaError_t e = cudaGetLastError();
-    trace_end(p, kind, s, e == cudaSuccess ? 1 : 0);
+    cudaError_t e = cudaGetLastError();
+    int launched = e == cudaSuccess ? 1 : 0;
+    if (e == cudaSuccess && splits > 1) {
+        e = splitk_reduce(partial, splits, M, N, C, ldc, bias, p.num_sms, s);
+        launched += e == cudaSuccess ? 1 : 0;
+    }
+    trace_end(p, kind, s, launched);
     return e == cudaSuccess ? LSTM_OK : LSTM_ERR_CUDA;
+}
+
+lstm_status gemm_tc_bf16_nt(const Plan& p, int kind, const void* A, const void* B, float* C, int64_t ldc,
+                            const float* bias, int M, int N, int K, cudaStream_t s)
+{
+    if (!gemm_tc_supported(M, N, K, A, B)) return LSTM_ERR_UNSUPPORTED;
+    return gemm_tc_bf16(p, kind, A, K, B, K, M, N, K, C, ldc, bias, 1, nullptr, s);
 }
 
 }  // namespace lstm
