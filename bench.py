@@ -411,7 +411,8 @@ def main():
         recurrent[f"phases_us_{kname}"] = {
             "barrier_wait": us(d[1:, 1] - d[1:, 0]), "after_barrier_to_2": us(d[:, 2] - d[:, 1]),
             "2_to_5": us(d[:, 5] - d[:, 2]), "5_to_3": us(d[:, 3] - d[:, 5]), "publish": us(d[:, 4] - d[:, 3]),
-            "step": us(d[1:, 0] - d[:-1, 0]), "clock_mhz": mhz, "cta": 0, "direction": 0}
+            "step": us(d[1:, 0] - d[:-1, 0]), "clock_mhz": mhz, "cta": 0, "direction": 0,
+            "since_step_start": {str(k): us(d[:, k] - d[:, 0]) for k in range(1, 8) if d[:, k].any()}}
     if "rec_fwd" in kernels:
         recurrent["us_per_step_fwd"] = round(1e3 * kernels["rec_fwd"]["ms_per_step"] / (T * spec.num_layers), 3)
     if "rec_bwd" in kernels:

@@ -74,7 +74,8 @@ BwdScratch bwd_scratch(const Plan& p, const lstm_layer_shape& s)
     const int H = s.hidden_size, nd = s.num_directions, D = s.input_size;
     size_t gemm = std::max(std::max(gemm_partial_floats(dW, p.num_sms), gemm_partial_floats(dR, p.num_sms)),
                            gemm_partial_floats(dX, p.num_sms));
-    const size_t part = rec_bwd_part_floats(p, H, nd, s.dtype == LSTM_BF16, p.forced_ctas);
+    const size_t part = std::max(rec_bwd_part_floats(p, H, nd, s.dtype == LSTM_BF16, p.forced_ctas),
+                                 rec_cluster_bwd_sum_floats(H, nd));
     if (s.dtype == LSTM_BF16) {
         const int rows = (int)p.rows;
         const size_t tc = std::max((size_t)gemm_tc_splits(nd * 4 * H, D, rows, p.num_sms, kMaxTcSplits) * nd * 4 * H * D,
@@ -237,13 +238,22 @@ lstm_status lstm_fwd(const lstm_plan* plan, const lstm_layer_shape* shape,
     float* ga = (float*)((char*)workspace + L.ga_off);
     float* cbuf = (float*)((char*)workspace + L.c_off);
 
-    RecConfig rc;
-    if ((st = rec_configure(p, H, nd, bf16, false, p.forced_ctas, &rc)) != LSTM_OK) return st;
+    RecConfig rc, rcc;
+    RecArgs cl_layout;
+    memset(&cl_layout, 0, sizeof(cl_layout));
+    const bool cluster = rec_cluster_fwd_configure(p, H, nd, bf16, &rcc, &cl_layout);
+    if (!cluster && (st = rec_configure(p, H, nd, bf16, false, p.forced_ctas, &rc)) != LSTM_OK) return st;
 
     if ((st = input_projection(p, s, *params, x_packed, ga, cs)) != LSTM_OK) return st;
 
     RecArgs a = base_args(p, s, *params, ga, cbuf);
     a.y = y_packed; a.y_lo = (__nv_bfloat16*)y_lo; a.h_n = h_n; a.c_n = c_n;
+    if (cluster) {
+        a.off_h = cl_layout.off_h; a.off_red = cl_layout.off_red; a.off_contrib = cl_layout.off_contrib;
+        a.off_acc = cl_layout.off_acc; a.off_state = cl_layout.off_state; a.off_sums = cl_layout.off_sums;
+        a.off_peep = cl_layout.off_peep; a.off_tab = cl_layout.off_tab;
+        return rec_cluster_fwd_launch(p, rcc, a, cs);
+    }
     return rec_launch(p, rc, a, false, cs);
 }
 
@@ -281,12 +291,22 @@ lstm_status lstm_bwd(const lstm_plan* plan, const lstm_layer_shape* shape,
     float* ga = (float*)((char*)workspace + L.ga_off);
     float* cbuf = (float*)((char*)workspace + L.c_off);
 
-    RecConfig rc;
-    if ((st = rec_configure(p, H, nd, bf16, true, p.forced_ctas, &rc)) != LSTM_OK) return st;
+    RecConfig rc, rcc;
+    RecArgs cl_layout;
+    memset(&cl_layout, 0, sizeof(cl_layout));
+    const bool cluster = rec_cluster_bwd_configure(p, H, nd, bf16, &rcc, &cl_layout);
+    if (!cluster && (st = rec_configure(p, H, nd, bf16, true, p.forced_ctas, &rc)) != LSTM_OK) return st;
     RecArgs a = base_args(p, s, *params, ga, cbuf);
     a.y = const_cast<float*>(y_packed); a.dy = dy_packed; a.db = grads->db; a.dpeep = grads->dpeep;
     a.part = (float*)scratch;
-    if ((st = rec_launch(p, rc, a, true, cs)) != LSTM_OK) return st;
+    if (cluster) {
+        a.off_h = cl_layout.off_h; a.off_red = cl_layout.off_red; a.off_contrib = cl_layout.off_contrib;
+        a.off_acc = cl_layout.off_acc; a.off_state = cl_layout.off_state; a.off_sums = cl_layout.off_sums;
+        a.off_peep = cl_layout.off_peep; a.off_tab = cl_layout.off_tab;
+        if ((st = rec_cluster_bwd_launch(p, rcc, a, (float*)scratch, cs)) != LSTM_OK) return st;
+    } else if ((st = rec_launch(p, rc, a, true, cs)) != LSTM_OK) {
+        return st;
+    }
 
     const int nd4H = nd * 4 * H;
     if (bf16 && p.gemm_engine == 0 && D % 8 == 0 && encode_ready())

@@ -772,28 +772,15 @@ static size_t rec_layout(const RecConfig& c, int H, int B, int T, int relem, boo
     return off + 64;   // room for the barrier's static shared word
 }
 
-lstm_status rec_configure(const Plan& p, int H, int ndir, bool bf16, bool bwd, int forced_G,
-                          RecConfig* out)
+// Product engine, chunk size and shared-memory layout for c.G / c.Umax; c.JC
+// stays 0 when nothing fits.
+static void configure_for(const Plan& p, int H, bool bf16, bool bwd, RecConfig& c)
 {
     int smem_optin = 0;
     if (cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p.device) != cudaSuccess)
-        return LSTM_ERR_CUDA;
-    const int per_dir_max = std::min(kMaxCtasPerDir, p.num_sms / ndir);
-    if (per_dir_max < 1) return LSTM_ERR_UNSUPPORTED;
-    int bmax = 0;
-    for (int t = 0; t < p.T; ++t) bmax = std::max(bmax, p.h_bs[t]);
-    int G;
-    if (forced_G > 0) G = std::min(forced_G, per_dir_max);
-    else {
-        // one CTA per direction while a step's product is small; otherwise one per SM
-        const double fmas = 4.0 * H * (double)H * std::max(1, bmax);
-        G = (fmas <= 1.5e6 && H <= 256) ? 1 : per_dir_max;
-    }
-    const int Umax = ceil_div(H, G);
-    G = ceil_div(H, Umax);
+        return;
     const int relem = bf16 ? 2 : 4;
-    RecConfig c;
-    c.G = G; c.Umax = Umax;
+    const int Umax = c.Umax;
     // tensor-core product when this CTA's fragments fit the per-warp register budget
     const int ksz = bf16 ? 16 : 8;
     if (p.gemm_engine == 1) {
@@ -823,6 +810,33 @@ lstm_status rec_configure(const Plan& p, int H, int ndir, bool bf16, bool bwd, i
             const size_t bytes = rec_layout(t, H, p.B, p.T, relem, bwd, nullptr);
             if (bytes <= (size_t)smem_optin) { c = t; c.smem = bytes; break; }
         }
+    }
+}
+
+lstm_status rec_configure(const Plan& p, int H, int ndir, bool bf16, bool bwd, int forced_G,
+                          RecConfig* out)
+{
+    const int per_dir_max = std::min(kMaxCtasPerDir, p.num_sms / ndir);
+    if (per_dir_max < 1) return LSTM_ERR_UNSUPPORTED;
+    int bmax = 0;
+    for (int t = 0; t < p.T; ++t) bmax = std::max(bmax, p.h_bs[t]);
+    int G0;
+    if (forced_G > 0) G0 = std::min(forced_G, per_dir_max);
+    else {
+        // one CTA per direction while a step's product is small; otherwise one per SM
+        const double fmas = 4.0 * H * (double)H * std::max(1, bmax);
+        G0 = (fmas <= 1.5e6 && H <= 256) ? 1 : per_dir_max;
+    }
+    // automatic choice: fall back to one CTA per SM when the slice does not fit
+    const int tries[2] = {G0, per_dir_max};
+    RecConfig c;
+    for (int attempt = 0; attempt < (forced_G > 0 ? 1 : 2) && c.JC == 0; ++attempt) {
+        int G = tries[attempt];
+        const int Umax = ceil_div(H, G);
+        G = ceil_div(H, Umax);
+        c = RecConfig();
+        c.G = G; c.Umax = Umax;
+        configure_for(p, H, bf16, bwd, c);
     }
     if (c.JC == 0) return LSTM_ERR_UNSUPPORTED;
     *out = c;

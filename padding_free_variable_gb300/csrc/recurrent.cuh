@@ -42,6 +42,7 @@ struct RecConfig {
     int tables = 0;     // step tables copied to shared memory
     int mma = 0;        // 1: warp-level tensor-core product (mma.sync), 0: CUDA cores
     int mma_mw = 1, mma_kw = 1;
+    int cluster = 0;    // 1: one thread-block cluster per direction (recurrent_cluster.cu)
     size_t smem = 0;    // dynamic shared memory bytes
 };
 
@@ -51,6 +52,18 @@ struct RecConfig {
 lstm_status rec_configure(const Plan& p, int H, int ndir, bool bf16, bool bwd, int forced_G,
                           RecConfig* out);
 lstm_status rec_launch(const Plan& p, const RecConfig& c, RecArgs a, bool bwd, cudaStream_t s);
+
+// Cluster-resident forward kernel: configured when one direction's R fits a
+// cluster of H/32 CTAs (<= 16) with its operand buffers; false otherwise.
+bool rec_cluster_fwd_configure(const Plan& p, int H, int ndir, bool bf16, RecConfig* out, RecArgs* layout);
+lstm_status rec_cluster_fwd_launch(const Plan& p, const RecConfig& c, RecArgs a, cudaStream_t s);
+
+// Cluster-resident BPTT kernel (and the db / dpeep sums after it, which need
+// rec_cluster_bwd_sum_floats floats of scratch).
+bool rec_cluster_bwd_configure(const Plan& p, int H, int ndir, bool bf16, RecConfig* out, RecArgs* layout);
+size_t rec_cluster_bwd_sum_floats(int H, int ndir);
+lstm_status rec_cluster_bwd_launch(const Plan& p, const RecConfig& c, RecArgs a, float* sum_scratch,
+                                   cudaStream_t s);
 
 // Floats of the backward kernel's partial-product exchange buffer.
 size_t rec_bwd_part_floats(const Plan& p, int H, int ndir, bool bf16, int forced_G);
