@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
         }
         tc::tc_fence_before_sync();
         __syncthreads();
-        cstamp(a, false, dir, rank, s, 2, 5);
+        cstamp(a, false, dir, rank, s, 2, 2);
         // cell: row j, units u0 + q8*4 .. +4
         const int nxt = cur ^ 1;
         for (int it = 0; it * 32 < n; ++it) {
@@ -367,6 +367,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
                     if (a.c_n) a.c_n[o + e] = cv[e];
                 }
             }
+            if (it == 0) cstamp(a, false, dir, rank, s, 5, 5);
             // h_t into every peer's operand of the next step (row j, columns u0 + q8*4 ..)
             if (s + 1 < T) {
                 const uint32_t o = sw_off4(j, u0 + q8 * 4, NBM);
@@ -644,6 +645,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
 #pragma unroll
                         for (int e = 0; e < 16; ++e) v[e] += __uint_as_float(r[e]);
                     }
+                    // lanes are consecutive units: each store is one coalesced 128-byte row
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
                         if (c0 + e < n) dst_base[(size_t)(c0 + e) * kCU + lane] = v[e];
