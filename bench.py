@@ -156,23 +156,65 @@ def kind_work(kind: str, spec, rows: int, D0: int, uses_tensor: dict):
     return fl, by
 
 
-def roofline_of(kind, ms_per_step, calls_per_step, spec, rows, D0, peaks, sustained):
+SMEM_BYTES_PER_CLK = 128      # shared-memory bandwidth of one SM, bytes per clock
+GEMM_KINDS = ("input_gemm", "gemm_dx", "gemm_dw", "gemm_dr")
+
+
+def rec_smem_bytes(kind, spec, rows, T, ctas):
+    """Algorithmic on-chip bytes of one recurrent pass over all layers.
+
+    Per step and direction: every element of R_dir read once from on-chip storage
+    (4H*H elements at the weight precision) plus the step's vector operand staged
+    into each of the direction's CTAs (bs[t] rows of H values: h_{t-1} forward, the
+    partial sums of R^T*dA backward).  Summed over steps: T*|R_dir| + ctas*N*H*b_h.
+    """
+    H, nd = spec.hidden_size, spec.num_directions
+    e = 2 if spec.dtype == "bf16" else 4
+    return float(spec.num_layers * nd * (T * 4 * H * H * e + ctas * rows * H * e))
+
+
+def roofline_of(kind, ms_per_step, calls_per_step, spec, rows, T, D0, peaks, rec_cfg):
+    """Roofline entry of one kernel kind from its per-step time.
+
+    rec_fwd/rec_bwd: shared-memory bandwidth of the SMs holding R (152 SMs x 128 B/clk at
+    the maximum SM clock, scaled to the CTAs in use).  GEMMs with bf16 operands (tcgen05):
+    the sustained measured bf16 peak, or HBM when the bytes take longer.  The rest:
+    HBM (measured copy bandwidth) or CUDA-core FP32 (derived) whichever bounds it.
+    """
     fl, by = kind_work(kind, spec, rows, D0, {})
     sec = ms_per_step / 1e3
     clk = float(peaks.get("sm_max_mhz", 2070.0))
-    alu_peak = NUM_SMS * FP32_LANES_PER_SM * 2 * clk * 1e6 / 1e12          # TFLOP/s, CUDA-core FFMA
+    per = max(1.0, calls_per_step)
+    if kind in ("rec_fwd", "rec_bwd") and rec_cfg and rec_cfg.get("ctas_per_direction"):
+        ctas = rec_cfg["ctas_per_direction"]
+        sb = rec_smem_bytes(kind, spec, rows, T, ctas)
+        sms = ctas * spec.num_directions
+        peak = sms * SMEM_BYTES_PER_CLK * clk * 1e6 / 1e9                     # GB/s
+        ach = sb / sec / 1e9 if sec > 0 else 0.0
+        tensor_peak = float(peaks["bf16_tflops_sustained"]) * (1.0 if spec.dtype == "bf16" else 1.1 / 2.25)
+        return {"kernel": kind, "bound": "smem", "achieved": round(ach, 1), "peak": round(peak, 1), "unit": "GB/s",
+                "frac": round(ach / peak, 4), "recurrent_kernel": rec_cfg,
+                "peak_source": f"derived: {sms} SMs x {SMEM_BYTES_PER_CLK} B/clk x {clk:.0f} MHz",
+                "tensor_view": {"achieved_tflops": round(fl / sec / 1e12, 3) if sec > 0 else 0.0,
+                                "peak_tflops": round(tensor_peak, 1)},
+                "per_launch": {"smem_bytes": sb / per, "flops": fl / per, "ms": ms_per_step / per}}
     hbm_peak = float(peaks["hbm_gbs"])                                        # GB/s
-    t_alu = fl / (alu_peak * 1e12) if fl else 0.0
     t_hbm = by / (hbm_peak * 1e9)
-    if t_alu >= t_hbm:
+    if kind in GEMM_KINDS and spec.dtype == "bf16":
+        cpeak, bound, src = float(peaks["bf16_tflops_sustained"]), "tensor", "MEASURED_PEAKS.json sustained bf16"
+    else:
+        cpeak, bound = NUM_SMS * FP32_LANES_PER_SM * 2 * clk * 1e6 / 1e12, "alu"
+        src = "derived: 152 SMs x 128 FP32 lanes x 2 flop x max SM clock"
+    t_c = fl / (cpeak * 1e12) if fl else 0.0
+    if t_c >= t_hbm:
         ach = fl / sec / 1e12 if sec > 0 else 0.0
-        return {"kernel": kind, "bound": "alu", "achieved": round(ach, 3), "peak": round(alu_peak, 1),
-                "unit": "TFLOP/s", "frac": round(ach / alu_peak, 4),
-                "per_launch": {"flops": fl / max(1, calls_per_step), "ms": ms_per_step / max(1, calls_per_step)}}
+        return {"kernel": kind, "bound": bound, "achieved": round(ach, 3), "peak": round(cpeak, 1),
+                "unit": "TFLOP/s", "frac": round(ach / cpeak, 4), "peak_source": src,
+                "per_launch": {"flops": fl / per, "ms": ms_per_step / per}}
     ach = by / sec / 1e9 if sec > 0 else 0.0
     return {"kernel": kind, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
-            "frac": round(ach / hbm_peak, 4),
-            "per_launch": {"bytes": by / max(1, calls_per_step), "ms": ms_per_step / max(1, calls_per_step)}}
+            "frac": round(ach / hbm_peak, 4), "peak_source": f"MEASURED_PEAKS.json ({peaks.get('source')})",
+            "per_launch": {"bytes": by / per, "ms": ms_per_step / per}}
 
 
 def source_digest() -> str:
@@ -364,11 +406,8 @@ def main():
     total_ms = sum(step_ms)
     if plan.poll() != 0:
         raise RuntimeError("device status set during the timed region")
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * N * args.steps / (total_ms / 1e3)
+    from padding_free_variable_gb300.sharding import timing_over_ranks
+    value, total_ms = timing_over_ranks(total_ms, N, args.steps, dist)
 
     # ---- per-kernel times (separate traced pass) for the roofline
     peaks = load_peaks()
@@ -380,16 +419,15 @@ def main():
     tim = plan.read_timing()
     plan.enable_timing(False)
     kernels = {}
+    rec_cfg = {"rec_fwd": plan.recurrent_config(False), "rec_bwd": plan.recurrent_config(True)}
     for kind, (ms, calls) in tim.items():
         if calls:
-            r = roofline_of(kind, ms / traced, calls / traced, spec, plan.rows, spec.input_size, peaks, False)
+            r = roofline_of(kind, ms / traced, calls / traced, spec, plan.rows, T, spec.input_size, peaks,
+                            rec_cfg.get(kind))
             r["ms_per_step"] = round(ms / traced, 4)
             kernels[kind] = r
     dom = max(kernels.values(), key=lambda r: r["ms_per_step"])
-    roof = {k: dom[k] for k in ("bound", "achieved", "peak", "unit", "frac")}
-    roof["kernel"] = dom["kernel"]
-    roof["peak_source"] = ("derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock"
-                           if dom["bound"] == "alu" else f"MEASURED_PEAKS.json ({peaks.get('source')})")
+    roof = {k: dom[k] for k in ("bound", "achieved", "peak", "unit", "frac", "kernel", "peak_source")}
     roof["traffic"] = recorded_traffic(dom["kernel"], spec.name)
     recurrent = {}
     # per-step phases of the recurrent kernels from in-kernel clock64 stamps (CTA 0, direction 0)

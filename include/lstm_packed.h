@@ -324,6 +324,17 @@ lstm_status lstm_plan_read_timing(lstm_plan* plan, double* ms, int64_t* calls);
  * -1 for a NULL plan. */
 int64_t lstm_plan_launch_count(const lstm_plan* plan);
 
+/* Launch configuration of the last recurrent kernel run through this plan:
+ * `pass` 0 = forward (lstm_fwd), 1 = backward (lstm_bwd / lstm_bwd_noalloc).
+ * kind: 0 none yet, 1 grid-wide persistent kernel with flag barriers,
+ *       2 one thread-block cluster per direction;
+ * ctas_per_direction: CTAs that hold one direction's recurrent weights;
+ * product: 0 CUDA cores, 1 warp-level mma.sync, 2 tcgen05 with TMEM accumulators.
+ * Any output pointer may be NULL.  LSTM_ERR_INVALID_ARG for a NULL plan or a
+ * pass other than 0 or 1.  Host only; no device work. */
+lstm_status lstm_plan_recurrent_config(const lstm_plan* plan, int32_t pass, int32_t* kind,
+                                       int32_t* ctas_per_direction, int32_t* product);
+
 /* Per-step phase stamps of the recurrent kernels (diagnostics).  With a
  * device buffer of 2 * ndir * steps * 8 int64 set, CTA 0 of each direction
  * writes clock64() stamps for its first `steps` steps at
@@ -333,9 +344,13 @@ int64_t lstm_plan_launch_count(const lstm_plan* plan);
  * buffer is the caller's; steps = 0 turns the stamps off. */
 lstm_status lstm_debug_trace_steps(lstm_plan* plan, int64_t* device_buffer, int32_t steps);
 
-/* Test hook: CTA `cta` of the recurrent kernels never announces its steps
- * (-1 = off), so the others' barrier waits run out and report
- * LSTM_ERR_TIMEOUT.  Exercises the failure path without a GPU fault. */
+/* Test hook (-1 = off).  Grid recurrent kernels: CTA `cta` never announces
+ * its steps, so the others' barrier waits run out.  Cluster recurrent
+ * kernels: CTA `cta` of the first direction's cluster withholds the
+ * completion signal of its first tensor-core product, so its own bounded wait
+ * runs out (and, with the bulk exchange, its peers' waits for its operand).
+ * Either way the launch returns and LSTM_ERR_TIMEOUT is reported: the failure
+ * path runs without a GPU fault. */
 lstm_status lstm_debug_skip_arrival(lstm_plan* plan, int32_t cta);
 
 #ifdef __cplusplus

@@ -28,7 +28,7 @@ EXPORTED = (
     "lstm_debug_skip_arrival", "lstm_plan_dims", "lstm_plan_compute_host",
     "lstm_plan_set_ctas_per_direction", "lstm_plan_enable_timing", "lstm_plan_read_timing",
     "lstm_plan_launch_count", "lstm_debug_trace_steps", "lstm_bwd_noalloc",
-    "lstm_plan_set_gemm_engine", "lstm_debug_input_projection",
+    "lstm_plan_set_gemm_engine", "lstm_debug_input_projection", "lstm_plan_recurrent_config",
 )
 
 KERNEL_KINDS = ("pack", "unpack", "input_gemm", "rec_fwd", "rec_bwd", "gemm_dx", "gemm_dw", "gemm_dr", "convert")
@@ -85,6 +85,7 @@ def _declare(lib):
         "lstm_plan_enable_timing": (c, [vp, i32]),
         "lstm_plan_read_timing": (c, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]),
         "lstm_plan_launch_count": (i64, [vp]),
+        "lstm_plan_recurrent_config": (c, [vp, i32, pi32, pi32, pi32]),
         "lstm_debug_trace_steps": (c, [vp, vp, i32]),
         "lstm_plan_set_gemm_engine": (c, [vp, i32]),
         "lstm_debug_input_projection": (c, [vp, ctypes.POINTER(LayerShape), ctypes.POINTER(LayerParams), vp, vp,

@@ -252,8 +252,10 @@ lstm_status lstm_fwd(const lstm_plan* plan, const lstm_layer_shape* shape,
         a.off_h = cl_layout.off_h; a.off_red = cl_layout.off_red; a.off_contrib = cl_layout.off_contrib;
         a.off_acc = cl_layout.off_acc; a.off_state = cl_layout.off_state; a.off_sums = cl_layout.off_sums;
         a.off_peep = cl_layout.off_peep; a.off_tab = cl_layout.off_tab;
+        p.last_rec_kind[0] = 2; p.last_rec_ctas[0] = rcc.G; p.last_rec_mma[0] = 2;
         return rec_cluster_fwd_launch(p, rcc, a, cs);
     }
+    p.last_rec_kind[0] = 1; p.last_rec_ctas[0] = rc.G; p.last_rec_mma[0] = rc.mma;
     return rec_launch(p, rc, a, false, cs);
 }
 
@@ -303,9 +305,11 @@ lstm_status lstm_bwd(const lstm_plan* plan, const lstm_layer_shape* shape,
         a.off_h = cl_layout.off_h; a.off_red = cl_layout.off_red; a.off_contrib = cl_layout.off_contrib;
         a.off_acc = cl_layout.off_acc; a.off_state = cl_layout.off_state; a.off_sums = cl_layout.off_sums;
         a.off_peep = cl_layout.off_peep; a.off_tab = cl_layout.off_tab;
+        p.last_rec_kind[1] = 2; p.last_rec_ctas[1] = rcc.G; p.last_rec_mma[1] = 2;
         if ((st = rec_cluster_bwd_launch(p, rcc, a, (float*)scratch, cs)) != LSTM_OK) return st;
-    } else if ((st = rec_launch(p, rc, a, true, cs)) != LSTM_OK) {
-        return st;
+    } else {
+        p.last_rec_kind[1] = 1; p.last_rec_ctas[1] = rc.G; p.last_rec_mma[1] = rc.mma;
+        if ((st = rec_launch(p, rc, a, true, cs)) != LSTM_OK) return st;
     }
 
     const int nd4H = nd * 4 * H;

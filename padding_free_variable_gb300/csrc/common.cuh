@@ -66,6 +66,10 @@ struct Plan {
     Tracer* tracer = nullptr;       // owned; mutable through const plans
     long long* d_trace = nullptr;   // caller's phase-stamp buffer (not owned)
     int32_t trace_steps = 0;
+    // launch configuration of the last recurrent launch: [0] forward, [1] backward
+    mutable int32_t last_rec_kind[2] = {0, 0};   // 0 none, 1 grid kernel, 2 cluster kernel
+    mutable int32_t last_rec_ctas[2] = {0, 0};   // CTAs per direction
+    mutable int32_t last_rec_mma[2] = {0, 0};    // 0 CUDA cores, 1 mma.sync, 2 tcgen05
 };
 
 // Bracket a launch sequence of `kind`; `kernels` = launches it issued.

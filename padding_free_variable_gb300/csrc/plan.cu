@@ -324,6 +324,16 @@ int64_t lstm_plan_launch_count(const lstm_plan* plan)
     return (plan && plan->p.tracer) ? (int64_t)plan->p.tracer->launches : -1;
 }
 
+lstm_status lstm_plan_recurrent_config(const lstm_plan* plan, int32_t pass, int32_t* kind,
+                                       int32_t* ctas_per_direction, int32_t* product)
+{
+    if (!plan || pass < 0 || pass > 1) return LSTM_ERR_INVALID_ARG;
+    if (kind) *kind = plan->p.last_rec_kind[pass];
+    if (ctas_per_direction) *ctas_per_direction = plan->p.last_rec_ctas[pass];
+    if (product) *product = plan->p.last_rec_mma[pass];
+    return LSTM_OK;
+}
+
 lstm_status lstm_debug_trace_steps(lstm_plan* plan, int64_t* device_buffer, int32_t steps)
 {
     if (!plan || steps < 0 || (steps > 0 && !device_buffer)) return LSTM_ERR_INVALID_ARG;

@@ -31,6 +31,7 @@ struct RecArgs {
     int trace_steps;
     int tables_in_smem;
     int mma_mw, mma_kw;       // forward tensor-core product: warps along rows and along k
+    int tm_chains, tm_acol;   // cluster kernels: TMEM accumulator chains, first column of the R operand
     // dynamic shared-memory layout (byte offsets)
     int off_h, off_red, off_acc, off_state, off_contrib, off_sums, off_tab, off_peep;
 };
@@ -43,6 +44,9 @@ struct RecConfig {
     int mma = 0;        // 1: warp-level tensor-core product (mma.sync), 0: CUDA cores
     int mma_mw = 1, mma_kw = 1;
     int cluster = 0;    // 1: one thread-block cluster per direction (recurrent_cluster.cu)
+    int chains = 0;     // cluster kernels: accumulator chains (issuing warps per M tile)
+    int acol = 0;       // cluster kernels: TMEM column of the R operand
+    int bulk = 0;       // cluster forward kernel: 1 = bulk-copy exchange into a double-buffered operand
     size_t smem = 0;    // dynamic shared memory bytes
 };
 

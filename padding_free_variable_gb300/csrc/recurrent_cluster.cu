@@ -1,4 +1,4 @@
-// recurrent_cluster.cu -- cluster-resident recurrent forward kernel.
+// recurrent_cluster.cu -- cluster-resident recurrent kernels (forward and BPTT).
 //
 // The same recurrence as lstm_rec_fwd_kernel ("Single Stream Parallelization
 // of Generalized LSTM-Like RNNs on a GPU", Sec. 3: one sequential step per
@@ -6,15 +6,20 @@
 // thread-block cluster when one direction's R fits in the cluster:
 //
 //  * one cluster of G = H/32 CTAs per direction; CTA c owns units
-//    [32c, 32c+32) and their 128 gate rows of R, resident in shared memory
-//    in the tcgen05 128-byte-swizzled K-major layout (bf16; fp32 operands
-//    are stored as bf16 hi + lo and multiplied as lo*hi + hi*lo + hi*hi);
-//  * per step one thread issues tcgen05.mma: D[128 gate rows][n rows] in
-//    tensor memory = R_slice x h_{t-1}^T, h taken from a shared-memory
-//    operand buffer that the peers filled;
-//  * the cell runs on the accumulator, and each CTA writes its new h (split
-//    and swizzled) straight into every peer's next operand buffer through
-//    distributed shared memory;
+//    [32c, 32c+32) and their 128 gate rows of R, resident in TENSOR MEMORY
+//    as the MMA's A operand (bf16; fp32 weights are stored as bf16 hi + lo
+//    and multiplied as lo*hi + hi*lo + hi*hi).  With A in tensor memory an
+//    M=128, N=32, K=16 MMA reads only its 1 KB B tile from shared memory
+//    (measured on GB300: ~19 cycles per MMA with 4 issuing warps, against
+//    ~43 with A in shared memory, where the 4 KB A tile bounds it);
+//  * per step up to 4 warps each issue one chain of tcgen05.mma into their
+//    own accumulator: D[128 gate rows][n rows] = R_slice x h_{t-1}^T, h taken
+//    from a shared-memory operand buffer that the peers filled;
+//  * the cell runs on the summed chains, and each CTA writes its new h
+//    (split and swizzled) straight into every peer's operand buffer through
+//    distributed shared memory.  The buffer is single: a split cluster
+//    barrier (arrive once this CTA's MMAs have read it, wait before writing
+//    to the peers) orders the overwrite;
 //  * one hardware cluster barrier per step replaces the grid-wide flag
 //    barrier (measured on GB300: ~0.22 us for 16 CTAs against ~1.8 us for a
 //    64-CTA flag barrier).
@@ -39,7 +44,9 @@ constexpr int kCU = 32;        // units per CTA
 constexpr int kCM = 128;       // gate rows per CTA (MMA M)
 constexpr int kCT = 256;       // threads
 constexpr int kSumChunks = 64; // row chunks of the db / dpeep sums
-constexpr int kChains = 4;     // independent TMEM accumulators per product (summed at read-out)
+// bound on the teardown wait for a product still in flight after a timeout
+// (an MMA takes microseconds; TMEM is freed only after it has completed)
+constexpr unsigned long long kTeardownWaitNs = 1000000000ull;
 
 __device__ __forceinline__ float sigm_c(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 __device__ __forceinline__ float tanh_c(float x)
@@ -70,25 +77,6 @@ __device__ __forceinline__ uint32_t bf16x2(float lo_k, float hi_k)
     return r;
 }
 
-// 8 fp32 values -> bf16 hi (rounded) and lo (rounded remainder), packed 2 per word
-__device__ __forceinline__ void split8(const float (&v)[8], uint4& hi, uint4& lo, bool want_lo)
-{
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        h[i] = bf16x2(v[2 * i], v[2 * i + 1]);
-        if (want_lo) {
-            const float a = v[2 * i] - __uint_as_float(h[i] << 16);
-            const float b = v[2 * i + 1] - __uint_as_float(h[i] & 0xffff0000u);
-            l[i] = bf16x2(a, b);
-        } else {
-            l[i] = 0u;
-        }
-    }
-    hi = make_uint4(h[0], h[1], h[2], h[3]);
-    lo = make_uint4(l[0], l[1], l[2], l[3]);
-}
-
 __device__ __forceinline__ void prefetch_l2(const void* p)
 {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
@@ -114,7 +102,6 @@ __device__ __forceinline__ void split4(const float (&v)[4], uint2& hi, uint2& lo
     }
 }
 
-__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (uint64_t)(bytes >> 4); }
 
 __device__ __forceinline__ void fence_proxy_async_cta()
 {
@@ -139,12 +126,200 @@ __device__ __forceinline__ void cstamp(const RecArgs& a, bool bwd, int dir, int 
     }
 }
 
+// Split cluster barrier: arrive (release) now, wait (acquire) later; every
+// thread of every CTA runs both, in the same order, once per phase.
+__device__ __forceinline__ void cluster_arrive()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+// Arrival without memory ordering: for "this CTA has finished reading"
+// signals whose reads are already complete (an MMA observed through its
+// mbarrier, shared-memory loads whose values have been consumed); it does
+// not wait for this thread's outstanding global loads and stores.
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 32 consecutive fp32 (or bf16) weights -> 16 bf16x2 words (hi) and, for
+// fp32 weights, 16 words of the rounded remainder (lo).
+template <bool SPLIT>
+__device__ __forceinline__ void split32(const float (&v)[32], uint32_t (&hi)[16], uint32_t (&lo)[16])
+{
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        hi[e] = bf16x2(v[2 * e], v[2 * e + 1]);
+        lo[e] = SPLIT ? bf16x2(v[2 * e] - __uint_as_float(hi[e] << 16),
+                               v[2 * e + 1] - __uint_as_float(hi[e] & 0xffff0000u))
+                      : 0u;
+    }
+}
+
+// One chain of the forward product: k-steps i = 4J + ch + v*NCH (v < 4/NCH)
+// over the 64-column blocks J of the B operand.  A (R slice) in TMEM from
+// column a_hi (lo part at a_lo), B in shared memory (descriptors bh, bl),
+// `bstep` = descriptor units between B blocks.
+template <int NCH, bool SPLIT>
+__device__ __forceinline__ void issue_chain(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t bh, uint64_t bl,
+                                            uint32_t bstep, int nks, int ch, uint32_t idesc)
+{
+    uint32_t acc = 0u;
+    for (int J = 0; 4 * J < nks; ++J) {
+#pragma unroll
+        for (int v = 0; v < 4 / NCH; ++v) {
+            const int w = ch + v * NCH;
+            const int i = 4 * J + w;
+            if (i < nks) {
+                const uint64_t bo = (uint64_t)(J * bstep + 2 * w);      // 32 bytes per k-step of 16
+                const uint32_t ac = (uint32_t)(i * 8);                  // 8 columns per k-step of 16
+                if (SPLIT) {
+                    tc::mma_bf16_ts(d, a_lo + ac, bh + bo, idesc, acc);
+                    tc::mma_bf16_ts(d, a_hi + ac, bl + bo, idesc, 1u);
+                    tc::mma_bf16_ts(d, a_hi + ac, bh + bo, idesc, 1u);
+                } else {
+                    tc::mma_bf16_ts(d, a_hi + ac, bh + bo, idesc, acc);
+                }
+                acc = 1u;
+            }
+        }
+    }
+}
+
+// The same chain over a B operand in 32-column blocks (64-byte swizzle, two
+// k-steps of 16 per block).
+template <int NCH, bool SPLIT>
+__device__ __forceinline__ void issue_chain32(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t bh, uint64_t bl,
+                                              uint32_t bstep, int nks, int ch, uint32_t idesc)
+{
+    uint32_t acc = 0u;
+#pragma unroll 2
+    for (int i = ch; i < nks; i += NCH) {
+        const uint64_t bo = (uint64_t)((uint32_t)(i >> 1) * bstep + (uint32_t)(i & 1) * 2u);
+        const uint32_t ac = (uint32_t)(i * 8);
+        if (SPLIT) {
+            tc::mma_bf16_ts(d, a_lo + ac, bh + bo, idesc, acc);
+            tc::mma_bf16_ts(d, a_hi + ac, bl + bo, idesc, 1u);
+            tc::mma_bf16_ts(d, a_hi + ac, bh + bo, idesc, 1u);
+        } else {
+            tc::mma_bf16_ts(d, a_hi + ac, bh + bo, idesc, acc);
+        }
+        acc = 1u;
+    }
+}
+
+template <bool SPLIT>
+__device__ __forceinline__ void issue_chains32(int nch, uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t bh,
+                                               uint64_t bl, uint32_t bstep, int nks, int ch, uint32_t idesc)
+{
+    if (nch == 4) issue_chain32<4, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, nks, ch, idesc);
+    else if (nch == 2) issue_chain32<2, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, nks, ch, idesc);
+    else issue_chain32<1, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, nks, ch, idesc);
+}
+
+// Shared-memory descriptor of a K-major operand in the 64-byte swizzled
+// layout: rows of 64 bytes (32 bf16), groups of 8 rows 512 bytes apart, the
+// 16-byte chunk c of row r stored at chunk c ^ ((r >> 1) & 3).
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);          // start address
+    d |= (uint64_t)1 << 16;                           // leading byte offset (unused for this layout)
+    d |= (uint64_t)(512u >> 4) << 32;                 // stride byte offset: 8 rows x 64 B
+    d |= (uint64_t)1 << 46;                           // descriptor version
+    d |= (uint64_t)4 << 61;                           // 64-byte swizzle
+    return d;
+}
+
+// byte offset of units [4q, 4q + 4) (q < 8) of row j in one 32-unit block of
+// the 64-byte swizzled layout
+__device__ __forceinline__ uint32_t sw64_off4(int j, int q)
+{
+    return (uint32_t)j * 64u + (uint32_t)((((q >> 1) ^ ((j >> 1) & 3))) << 4) + (uint32_t)(q & 1) * 8u;
+}
+
+__device__ __forceinline__ uint32_t mapa_u32(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// Bulk copy of `bytes` from this CTA's shared memory into a peer's
+// (shared::cluster address), completing on the peer's mbarrier.
+__device__ __forceinline__ void bulk_to_peer(uint32_t dst_cluster, const void* src, uint32_t bytes,
+                                             uint32_t mbar_cluster)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst_cluster), "r"(tc::smem_u32(src)), "r"(bytes), "r"(mbar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// this thread's bulk copies except the newest group have finished reading their source
+__device__ __forceinline__ void bulk_wait_read_all_but_one()
+{
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// this thread's bulk copies have completed (destination written)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Sum of the accumulator chains at columns col0 + ch * stride (ch < nch <= 4)
+// for 16 consecutive columns of this warp's 32 lanes: the loads are issued
+// together and waited for once.
+__device__ __forceinline__ void tmem_sum_chains(uint32_t taddr0, uint32_t stride, int nch, float (&v)[16])
+{
+    uint32_t r[4][16];
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch)
+        if (ch < nch) tc::tmem_ld_32x32b_x16(taddr0 + (uint32_t)ch * stride, r[ch]);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[0][e]);
+#pragma unroll
+    for (int ch = 1; ch < 4; ++ch)
+        if (ch < nch) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] += __uint_as_float(r[ch][e]);
+        }
+}
+
+template <bool SPLIT>
+__device__ __forceinline__ void issue_chains(int nch, uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t bh,
+                                             uint64_t bl, uint32_t bstep, int nks, int ch, uint32_t idesc)
+{
+    if (nch == 4) issue_chain<4, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, nks, ch, idesc);
+    else if (nch == 2) issue_chain<2, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, nks, ch, idesc);
+    else issue_chain<1, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, nks, ch, idesc);
+}
+
 }  // namespace
 
-// RecArgs offsets reused: off_h = A_hi, off_red = A_lo, off_acc = accs,
-// off_state = cell states, off_contrib = B buffers, off_sums = mbarrier and
-// TMEM slot, off_tab = tables, off_peep = peepholes.
-template <bool SPLIT>
+// Shared memory (RecArgs offsets): off_acc = accs, off_state = cell states,
+// off_contrib = B operand (h_{t-1}, hi then lo), off_sums = mbarrier, TMEM
+// slot and failure flag, off_tab = tables, off_peep = peepholes.
+// Tensor memory: accumulator chains in columns [0, chains * NBM), the R slice
+// (hi, then lo for fp32 weights, H/2 columns each) from column tm_acol.
+//
+// Two exchanges of h_t between the CTAs of a cluster:
+//  * BULK: the operand is double-buffered per step parity, in 32-unit blocks
+//    of the 64-byte swizzled layout, so that one CTA's units of all rows are
+//    one contiguous block.  Each CTA stages its h_t there in its own shared
+//    memory and copies it with one cp.async.bulk per peer (hi and lo), which
+//    completes on the peer's mbarrier of that parity: the arrival of the
+//    data is the step's synchronisation, and no cluster barrier runs inside
+//    the step loop.  A peer can only send h_{t+1} into buffer (s & 1) after
+//    it received this CTA's h_t, which is sent after this CTA's product of
+//    step s has read that buffer; each mbarrier is re-armed for its next use
+//    before this CTA's copies of the step go out, so no byte can arrive at an
+//    unarmed barrier.
+//  * otherwise (the double buffer does not fit): one operand buffer, written
+//    by the peers with plain DSMEM stores between two halves of a split
+//    cluster barrier.
+template <bool SPLIT, bool BULK>
 __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -157,43 +332,39 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
     const int KB = (H + 63) / 64;
     const int u0 = rank * kCU;
     const int ndH = a.ndir * H, nd4H = a.ndir * 4 * H;
-    uint8_t* Ahi = base + a.off_h;
-    uint8_t* Alo = base + a.off_red;
+    const int nch = a.tm_chains;
     float* accs = reinterpret_cast<float*>(base + a.off_acc);        // [NBM][128]
     float* cst = reinterpret_cast<float*>(base + a.off_state);       // [B][32]
-    uint8_t* Bb = base + a.off_contrib;                              // [2 parity][2 hi/lo][KB][NBM][128 B]
+    // B operand: BULK [2 parity][2 hi/lo][G][NBM][64 B], else [2 hi/lo][KB][NBM][128 B]
+    uint8_t* Bb = base + a.off_contrib;
     uint64_t* mma_bar = reinterpret_cast<uint64_t*>(base + a.off_sums);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 1);
     int* s_fail = reinterpret_cast<int*>(tmem_slot + 1);
+    uint64_t* full_bar = mma_bar + 2;                                // BULK: [2] operand arrival per parity
     float* peep_s = reinterpret_cast<float*>(base + a.off_peep);     // [3][32]
     int* s_bs = reinterpret_cast<int*>(base + a.off_tab);
     int* s_off = s_bs + T;
     int* s_len = s_off + T + 1;
-    const size_t bsz = (size_t)KB * NBM * 128;                       // bytes of one B operand
-    auto Bop = [&](int parity, int lo) -> uint8_t* { return Bb + (size_t)(parity * 2 + lo) * bsz; };
+    uint8_t* stage = base + a.off_h;                                 // BULK: [2 parity][2 hi/lo][NBM][64 B]
+    const size_t bsz = BULK ? (size_t)G * NBM * 64 : (size_t)KB * NBM * 128;   // bytes of one B operand
+    const size_t ssz = (size_t)NBM * 64;                             // bytes of one staged h slice
+    auto Bop = [&](int parity, int lo) -> uint8_t* {
+        return Bb + (BULK ? (size_t)parity * (SPLIT ? 2 : 1) * bsz : 0) + (size_t)lo * bsz;
+    };
+    auto Stg = [&](int parity, int lo) -> uint8_t* { return stage + (size_t)(parity * 2 + lo) * ssz; };
+    // bytes a CTA receives for step s (h of step s - 1 from every CTA, rows rounded to 16)
+    auto step_bytes = [&](int s2) -> uint32_t {
+        const int tp = dir == 0 ? s2 - 1 : T - s2;
+        return (uint32_t)G * (SPLIT ? 2u : 1u) * (uint32_t)((s_bs[tp] + 15) & ~15) * 64u;
+    };
     const uint32_t tcols = (uint32_t)a.Umax;                         // Umax carries the TMEM columns
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- set-up: R slice, operands zeroed, tables, barrier, tensor memory
-    const __nv_bfloat16* Rb = reinterpret_cast<const __nv_bfloat16*>(a.R);
-    const float* Rf = reinterpret_cast<const float*>(a.R);
-    for (int idx = threadIdx.x; idx < kCM * KB * 8; idx += kCT) {
-        const int r = idx / (KB * 8), rem = idx - r * (KB * 8);
-        const int k0 = rem * 8;
-        const int g = r / kCU, uu = r - g * kCU;
-        const size_t grow = (size_t)dir * 4 * H * H + (size_t)(g * H + u0 + uu) * H;
-        float v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int k = k0 + e;
-            v[e] = k < H ? (SPLIT ? Rf[grow + k] : __bfloat162float(Rb[grow + k])) : 0.f;
-        }
-        uint4 hi, lo;
-        split8(v, hi, lo, SPLIT);
-        const uint32_t o = sw_off(r, k0, kCM);
-        *reinterpret_cast<uint4*>(Ahi + o) = hi;
-        if (SPLIT) *reinterpret_cast<uint4*>(Alo + o) = lo;
-    }
-    for (size_t i = threadIdx.x; i < 4 * bsz / 16; i += kCT) reinterpret_cast<uint4*>(Bb)[i] = make_uint4(0, 0, 0, 0);
+    // ---- set-up: operand zeroed, tables, barrier, tensor memory
+    for (size_t i = threadIdx.x; i < (BULK ? 2 : 1) * (SPLIT ? 2 : 1) * bsz / 16; i += kCT)
+        reinterpret_cast<uint4*>(Bb)[i] = make_uint4(0, 0, 0, 0);
+    if (BULK)
+        for (size_t i = threadIdx.x; i < 4 * ssz / 16; i += kCT) reinterpret_cast<uint4*>(stage)[i] = make_uint4(0, 0, 0, 0);
     for (int i = threadIdx.x; i < T; i += kCT) s_bs[i] = a.bs[i];
     for (int i = threadIdx.x; i <= T; i += kCT) s_off[i] = a.off[i];
     for (int i = threadIdx.x; i < a.B; i += kCT) s_len[i] = a.slot_len[i];
@@ -202,9 +373,16 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
         peep_s[i] = a.peep[(size_t)dir * 3 * H + q * H + u0 + uu];
     }
     if (threadIdx.x == 0) {
-        tc::mbar_init(mma_bar, kChains);
+        tc::mbar_init(mma_bar, (uint32_t)nch);
         *s_fail = 0;
+        if (BULK) {
+            tc::mbar_init(&full_bar[0], 1);
+            tc::mbar_init(&full_bar[1], 1);
+        }
         tc::fence_mbar_init();
+        // the operand of step 1 (parity 1) is armed before the cluster barrier below,
+        // i.e. before any peer can send
+        if (BULK && T > 1) tc::mbar_arrive_expect_tx(&full_bar[1], step_bytes(1));
     }
     if (threadIdx.x < 32) {
         tc::tmem_alloc(tmem_slot, tcols);
@@ -215,6 +393,35 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
     __syncthreads();
     tc::tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    const uint32_t a_hi = tmem + (uint32_t)a.tm_acol, a_lo = a_hi + (uint32_t)(H / 2);
+    // R slice -> tensor memory: lane 32g + uu holds gate row g of unit u0 + uu (the MMA's row
+    // order), column c of the slice holds k = 2c and 2c + 1; warps g and g + 4 share the lanes
+    // of gate g and take alternate 32-wide k chunks
+    {
+        const int g = warp & 3;
+        const size_t grow = (size_t)dir * 4 * H * H + (size_t)(g * H + u0 + lane) * H;
+        const uint32_t lanes = (uint32_t)(32 * g) << 16;
+        for (int cc = warp >> 2; cc < H / 32; cc += 2) {
+            float v[32];
+            if (SPLIT) {
+                const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.R) + grow + 32 * cc);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float4 x = __ldg(src + e);
+                    v[4 * e] = x.x; v[4 * e + 1] = x.y; v[4 * e + 2] = x.z; v[4 * e + 3] = x.w;
+                }
+            } else {
+                const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(a.R) + grow + 32 * cc;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = __bfloat162float(src[e]);
+            }
+            uint32_t hi[16], lo[16];
+            split32<SPLIT>(v, hi, lo);
+            tc::tmem_st_32x32b_x16(a_hi + lanes + (uint32_t)(16 * cc), hi);
+            if (SPLIT) tc::tmem_st_32x32b_x16(a_lo + lanes + (uint32_t)(16 * cc), lo);
+        }
+        tc::tmem_wait_st();
+    }
     if (a.h_n) {
         for (int idx = threadIdx.x; idx < a.B * kCU; idx += kCT) {
             const int j = idx / kCU, uu = idx - j * kCU;
@@ -225,45 +432,52 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
             }
         }
     }
+    tc::tc_fence_before_sync();
+    __syncthreads();
+    tc::tc_fence_after_sync();
     cl.sync();     // every CTA of the cluster is resident before any remote write
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int jq = threadIdx.x >> 3, q8 = threadIdx.x & 7;          // cell item: row jq (+32k), units q8*4..+4
     const int nks = (H + 15) / 16;                                   // MMA k-steps
-    const int nch = min(kChains, nks);
+    const uint32_t bstep = (uint32_t)(NBM * (BULK ? 64 : 128)) >> 4;  // descriptor units between B blocks
+    bool failed = false;                  // CTA-uniform: an MMA completion wait timed out
     for (int s = 0; s < T; ++s) {
         const int t = dir == 0 ? s : T - 1 - s;
         const int n = s_bs[t];
         const int rowbase = s_off[t];
         const int n_prev = dir == 0 ? (t >= 1 ? n : 0) : (t + 1 < T ? s_bs[t + 1] : 0);
         const int NBs = (n + 15) & ~15;
-        const int cur = s & 1;
-        cstamp(a, false, dir, rank, s, 0, 0);
-        // D[gate rows][rows] = R_slice x h_{t-1}^T: chain ch (k-steps ch, ch + kChains, ...) is
-        // issued by warp ch into its own accumulator, so the chains overlap
-        if (lane == 0 && warp < kChains && !*(volatile int*)s_fail) {
+        const int par = BULK ? (s & 1) : 0;
+        bool arrived = true;
+        if (BULK) {
+            cstamp(a, false, dir, rank, s, 0, 0);
+            // h_{t-1} of every peer has arrived in this step's operand
+            if (s > 0 && !failed)
+                arrived = tc::mbar_wait(&full_bar[par], (uint32_t)(((s - 1) >> 1) & 1), a.wait_limit_ns);
+        } else {
+            if (s > 0) {
+                cluster_wait();    // h_{t-1} of every peer is in this CTA's operand
+                cstamp(a, false, dir, rank, s - 1, 4, 4);
+            }
+            cstamp(a, false, dir, rank, s, 0, 0);
+        }
+        // D[gate rows][rows] = R_slice x h_{t-1}^T: chain ch is issued by warp ch into its own
+        // accumulator, so the chains overlap
+        if (lane == 0 && warp < nch && !failed) {
             fence_proxy_async_cta();
             tc::tc_fence_after_sync();
             cstamp(a, false, dir, rank, s, 1, 1);
             const uint32_t idesc = tc::idesc_bf16_f32(kCM, NBs);
-            const uint64_t dah = tc::sdesc_sw128(tc::smem_u32(Ahi)), dal = tc::sdesc_sw128(tc::smem_u32(Alo));
-            const uint64_t dbh = tc::sdesc_sw128(tc::smem_u32(Bop(cur, 0))), dbl = tc::sdesc_sw128(tc::smem_u32(Bop(cur, 1)));
-            const uint32_t d = tmem + (uint32_t)(warp * NBM);
-            for (int i = warp; i < nks; i += kChains) {
-                const uint32_t ao = (uint32_t)(i >> 2) * kCM * 128 + (uint32_t)(i & 3) * 32;
-                const uint32_t bo = (uint32_t)(i >> 2) * NBM * 128 + (uint32_t)(i & 3) * 32;
-                const uint32_t acc = i == warp ? 0u : 1u;
-                if (SPLIT) {
-                    tc::mma_bf16_ss(d, desc_add(dal, ao), desc_add(dbh, bo), idesc, acc);
-                    tc::mma_bf16_ss(d, desc_add(dah, ao), desc_add(dbl, bo), idesc, 1u);
-                    tc::mma_bf16_ss(d, desc_add(dah, ao), desc_add(dbh, bo), idesc, 1u);
-                } else {
-                    tc::mma_bf16_ss(d, desc_add(dah, ao), desc_add(dbh, bo), idesc, acc);
-                }
+            if (BULK) {
+                const uint64_t dbh = sdesc_sw64(tc::smem_u32(Bop(par, 0))), dbl = sdesc_sw64(tc::smem_u32(Bop(par, 1)));
+                issue_chains32<SPLIT>(nch, tmem + (uint32_t)(warp * NBM), a_hi, a_lo, dbh, dbl, bstep, nks, warp, idesc);
+            } else {
+                const uint64_t dbh = tc::sdesc_sw128(tc::smem_u32(Bop(0, 0))), dbl = tc::sdesc_sw128(tc::smem_u32(Bop(0, 1)));
+                issue_chains<SPLIT>(nch, tmem + (uint32_t)(warp * NBM), a_hi, a_lo, dbh, dbl, bstep, nks, warp, idesc);
             }
-            tc::mma_commit(mma_bar);
+            if (!(s == 0 && dir == 0 && rank == a.debug_skip_cta)) tc::mma_commit(mma_bar);   // test hook
         }
-        if (warp < kChains) __syncwarp();     // the issuing lane's warp does not poll while it issues
+        if (warp < nch) __syncwarp();     // the issuing lane's warp does not poll while it issues
         cstamp(a, false, dir, rank, s, 6, 6);
         // meanwhile: the cell items' own operands (gate pre-activations), rows jq and jq + 32
         float pre[2][4][4];
@@ -284,40 +498,67 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
             for (int g = 0; g < 4; ++g)
                 prefetch_rows(a.ga, nd4H, s_off[t2], s_bs[t2], dir * 4 * H + g * H + u0);
         }
-        const bool ok = *(volatile int*)s_fail ? false : tc::mbar_wait(mma_bar, (uint32_t)(s & 1), a.wait_limit_ns);
-        if (!ok && !*(volatile int*)s_fail) {
-            record_failure(a.status, LSTM_ERR_TIMEOUT, 0x40000u | (unsigned)s);
-            *(volatile int*)s_fail = 1;
+        // A timeout (of the product, or of the operand's arrival) becomes a CTA-uniform decision
+        // at the barrier after the read-out: from then on the CTA issues no product, waits for
+        // no operand, re-arms nothing and sends nothing (so no barrier is armed twice and
+        // unmatched bytes stay within two steps), and the teardown waits for the product in
+        // flight before freeing tensor memory.  The read-out of the failing step itself may see
+        // partial sums; the status word marks the results as invalid.
+        const bool ok = failed ? true : tc::mbar_wait(mma_bar, (uint32_t)(s & 1), a.wait_limit_ns);
+        if ((!ok || !arrived) && !failed) {
+            record_failure(a.status, LSTM_ERR_TIMEOUT, (ok ? 0x60000u : 0x40000u) | (unsigned)s);
+            *s_fail = 1 + s;
         }
         cstamp(a, false, dir, rank, s, 7, 7);
         tc::tc_fence_after_sync();
+        if (!BULK) cluster_arrive_relaxed();   // this CTA's product has read its operand: peers may overwrite it
         // accumulators -> shared: warp (quarter q = gate, half) reads lanes 32q.. in 16-column blocks
-        {
+        if (!failed) {
             const int q = warp & 3, half = warp >> 2;
             for (int c0 = half * 16; c0 < NBs; c0 += 32) {
                 float v[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] = 0.f;
-                for (int ch = 0; ch < nch; ++ch) {
-                    uint32_t r[16];
-                    tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(ch * NBM + c0), r);
-                    tc::tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) v[e] += __uint_as_float(r[e]);
-                }
+                tmem_sum_chains(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, (uint32_t)NBM, nch, v);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) accs[(size_t)(c0 + e) * kCM + q * 32 + lane] = v[e];
             }
         }
         tc::tc_fence_before_sync();
-        __syncthreads();
+        if (__syncthreads_or(!ok || !arrived)) failed = true;
+        // BULK: re-arm this parity for step s + 2 before this CTA's h_t goes out (a peer
+        // needs h_t before it can send h_{t+1})
+        if (BULK && threadIdx.x == 0 && !failed && s + 2 < T)
+            tc::mbar_arrive_expect_tx(&full_bar[par], step_bytes(s + 2));
         cstamp(a, false, dir, rank, s, 2, 2);
-        // cell: row j, units u0 + q8*4 .. +4
-        const int nxt = cur ^ 1;
-        for (int it = 0; it * 32 < n; ++it) {
+        // cell: row j, units u0 + q8*4 .. +4; h_t kept (split) for the exchange.  The global
+        // outputs of rows jq and jq + 32 are written after the exchange's barrier arrival, so
+        // that the arrival (a release) does not wait for them
+        uint2 xh[4], xl[4];
+        float og_[2][4][4], oc_[2][4], oh_[2][4];
+        auto store_outputs = [&](int j, const float (&gg)[4][4], const float (&cv)[4], const float (&hv)[4],
+                                 uint2 hi) {
+            const int row = rowbase + j;
+            const int len = s_len[j];
+            float* gr = a.ga + (size_t)row * nd4H + dir * 4 * H + u0 + q8 * 4;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+                *reinterpret_cast<float4*>(gr + g * H) = make_float4(gg[g][0], gg[g][1], gg[g][2], gg[g][3]);
+            const size_t yo = (size_t)row * ndH + dir * H + u0 + q8 * 4;
+            *reinterpret_cast<float4*>(a.cbuf + yo) = make_float4(cv[0], cv[1], cv[2], cv[3]);
+            *reinterpret_cast<float4*>(a.y + yo) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+            if (a.y_lo) *reinterpret_cast<uint2*>(a.y_lo + yo) = hi;
+            if (a.h_n && ((dir == 0 && t == len - 1) || (dir == 1 && t == 0 && len > 0))) {
+                const size_t o = ((size_t)dir * a.B + a.perm[j]) * H + u0 + q8 * 4;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    a.h_n[o + e] = hv[e];
+                    if (a.c_n) a.c_n[o + e] = cv[e];
+                }
+            }
+        };
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
             const int j = jq + it * 32;
             if (j >= n) continue;
-            const int row = rowbase + j;
             const int len = s_len[j];
             float pv[4][4];
             if (it < 2) {
@@ -326,7 +567,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) pv[g][e] = it == 0 ? pre[0][g][e] : pre[1][g][e];
             } else {
-                const float* gr = a.ga + (size_t)row * nd4H + dir * 4 * H + u0 + q8 * 4;
+                const float* gr = a.ga + (size_t)(rowbase + j) * nd4H + dir * 4 * H + u0 + q8 * 4;
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     const float4 x = *reinterpret_cast<const float4*>(gr + g * H);
@@ -349,45 +590,80 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
                 gg[0][e] = ig; gg[1][e] = fg; gg[2][e] = zg; gg[3][e] = og; cv[e] = c; hv[e] = h;
                 cst[j * kCU + uu] = c;
             }
-            float* gr = a.ga + (size_t)row * nd4H + dir * 4 * H + u0 + q8 * 4;
-#pragma unroll
-            for (int g = 0; g < 4; ++g)
-                *reinterpret_cast<float4*>(gr + g * H) = make_float4(gg[g][0], gg[g][1], gg[g][2], gg[g][3]);
-            const size_t yo = (size_t)row * ndH + dir * H + u0 + q8 * 4;
-            *reinterpret_cast<float4*>(a.cbuf + yo) = make_float4(cv[0], cv[1], cv[2], cv[3]);
-            *reinterpret_cast<float4*>(a.y + yo) = make_float4(hv[0], hv[1], hv[2], hv[3]);
-            uint2 hi, lo;
-            split4(hv, hi, lo, SPLIT);
-            if (a.y_lo) *reinterpret_cast<uint2*>(a.y_lo + yo) = hi;
-            if (a.h_n && ((dir == 0 && t == len - 1) || (dir == 1 && t == 0 && len > 0))) {
-                const size_t o = ((size_t)dir * a.B + a.perm[j]) * H + u0 + q8 * 4;
+            split4(hv, xh[it], xl[it], SPLIT);
+            if (it < 2) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    a.h_n[o + e] = hv[e];
-                    if (a.c_n) a.c_n[o + e] = cv[e];
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) og_[it][g][e] = gg[g][e];
+                    oc_[it][e] = cv[e];
+                    oh_[it][e] = hv[e];
                 }
-            }
-            if (it == 0) cstamp(a, false, dir, rank, s, 5, 5);
-            // h_t into every peer's operand of the next step (row j, columns u0 + q8*4 ..)
-            if (s + 1 < T) {
-                const uint32_t o = sw_off4(j, u0 + q8 * 4, NBM);
-                for (int p2 = 0; p2 < G; ++p2) {
-                    *reinterpret_cast<uint2*>(cl.map_shared_rank(Bop(nxt, 0) + o, p2)) = hi;
-                    if (SPLIT) *reinterpret_cast<uint2*>(cl.map_shared_rank(Bop(nxt, 1) + o, p2)) = lo;
-                }
+            } else {
+                store_outputs(j, gg, cv, hv, xh[it]);
             }
         }
-        fence_proxy_async_cluster();
+        cstamp(a, false, dir, rank, s, 5, 5);
+        if (BULK) {
+            // h_t (rows [0, NBs)) staged in this CTA's 32-unit block, then one bulk copy per peer
+            // and half into that peer's operand of step s + 1
+            if (s + 1 < T) {
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                    const int j = jq + it * 32;
+                    if (j >= n) continue;
+                    const uint32_t o = sw64_off4(j, q8);
+                    *reinterpret_cast<uint2*>(Stg(par, 0) + o) = xh[it];
+                    if (SPLIT) *reinterpret_cast<uint2*>(Stg(par, 1) + o) = xl[it];
+                }
+            }
+            fence_proxy_async_cta();
+            __syncthreads();
+            if (s + 1 < T && threadIdx.x < G && !failed) {
+                const uint32_t p2 = (uint32_t)threadIdx.x, nxt = (uint32_t)(par ^ 1);
+                const uint32_t bytes = (uint32_t)NBs * 64u;
+                const uint32_t bar = mapa_u32(tc::smem_u32(&full_bar[nxt]), p2);
+                bulk_to_peer(mapa_u32(tc::smem_u32(Bop(nxt, 0) + (size_t)rank * NBM * 64), p2), Stg(par, 0), bytes, bar);
+                if (SPLIT)
+                    bulk_to_peer(mapa_u32(tc::smem_u32(Bop(nxt, 1) + (size_t)rank * NBM * 64), p2), Stg(par, 1), bytes, bar);
+                bulk_commit();
+                bulk_wait_read_all_but_one();    // the copies of step s - 1 have read their staging
+            }
+        } else {
+            cluster_wait();        // every peer's product of this step is done with its operand
+            // h_t into every peer's operand of the next step (row j, columns u0 + q8*4 ..)
+            if (s + 1 < T) {
+#pragma unroll
+                for (int it = 0; it < 4; ++it) {
+                    const int j = jq + it * 32;
+                    if (j >= n) continue;
+                    const uint32_t o = sw_off4(j, u0 + q8 * 4, NBM);
+                    for (int p2 = 0; p2 < G; ++p2) {
+                        *reinterpret_cast<uint2*>(cl.map_shared_rank(Bop(0, 0) + o, p2)) = xh[it];
+                        if (SPLIT) *reinterpret_cast<uint2*>(cl.map_shared_rank(Bop(0, 1) + o, p2)) = xl[it];
+                    }
+                }
+            }
+            fence_proxy_async_cluster();
+            cluster_arrive();      // release: this CTA's h_t is in every peer's operand
+        }
+#pragma unroll
+        for (int it = 0; it < 2; ++it)
+            if (jq + it * 32 < n) store_outputs(jq + it * 32, og_[it], oc_[it], oh_[it], xh[it]);
         cstamp(a, false, dir, rank, s, 3, 3);
-        cl.sync();
-        cstamp(a, false, dir, rank, s, 4, 4);
+    }
+    if (BULK) {
+        if (threadIdx.x < G) bulk_wait_all();   // no copy of this CTA is still in flight
+        cl.sync();                              // nor one into it: every CTA has passed its last wait
+    } else {
+        cluster_wait();            // the last step's arrival
     }
     tc::tc_fence_before_sync();
     __syncthreads();
     if (threadIdx.x < 32) {
         __syncwarp();
         tc::tc_fence_after_sync();
-        if (*(volatile int*)s_fail) tc::mbar_wait(mma_bar, (uint32_t)((T - 1) & 1) ^ 1u, a.wait_limit_ns);
+        if (failed) tc::mbar_wait(mma_bar, (uint32_t)((*s_fail - 1) & 1), kTeardownWaitNs);
         tc::tmem_dealloc(tmem, tcols);
     }
 }
@@ -396,15 +672,19 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
 //
 // BPTT of the same recurrence ("Single Stream Parallelization...", Sec. 2) in
 // the same cluster layout.  The error reaching h_t through R is
-// R^T da_{t+1}; CTA c holds its 128 gate rows of R and the gate errors it
-// computes for them, so it forms the partial product P_c = R_c^T da_c for
-// every unit on the tensor cores, and pushes the part of P_c that belongs to
-// CTA c' (its 32 units) into c''s inbox through distributed shared memory.
-// At the next step each CTA adds the G partials of its units in CTA order.
-// db and dpeep are summed afterwards by lstm_param_sums_kernel.
-// RecArgs offsets: off_h = A_hi, off_red = A_lo, off_contrib = B (gate
-// errors), off_acc = inbox, off_state = dc carry, off_sums = mbarrier, TMEM
-// slot, failure flag, off_peep = peepholes, off_tab = tables.
+// R^T da_{t+1}; CTA c holds its 128 gate rows of R (as R^T, in tensor memory)
+// and the gate errors it computes for them, so it forms the partial product
+// P_c = R_c^T da_c for every unit on the tensor cores, and pushes the part of
+// P_c that belongs to CTA c' (its 32 units) into c''s inbox through
+// distributed shared memory.  At the next step each CTA adds the G partials
+// of its units in CTA order.  db and dpeep are summed afterwards by
+// lstm_param_sums_kernel.
+// Shared memory (RecArgs offsets): off_contrib = B (gate errors, hi then
+// lo), off_acc = inbox, off_state = dc carry, off_sums = mbarrier, TMEM slot,
+// failure flag, off_peep = peepholes, off_tab = tables.
+// Tensor memory: accumulators (tile m, chain ch) at columns
+// (m * chains + ch) * NBM; R^T tile m from column tm_acol + 64m (hi) and
+// tm_acol + 64 MT + 64m (lo).
 template <bool SPLIT>
 __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
 {
@@ -416,14 +696,12 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
     const int dir = blockIdx.x / G;
     const int H = a.H, T = a.T, NBM = a.JC;
     const int MT = (H + kCM - 1) / kCM;              // 128-unit tiles of the partial product
-    const int AR = MT * kCM;                         // rows of the R^T operand (zero padded)
     const int u0 = rank * kCU;
     const int ndH = a.ndir * H, nd4H = a.ndir * 4 * H;
-    uint8_t* Ahi = base + a.off_h;
-    uint8_t* Alo = base + a.off_red;
+    const int nch = a.tm_chains;                     // chains per tile; issuers = MT * nch
     uint8_t* Bhi = base + a.off_contrib;             // [2 k-blocks][NBM][128 B]
     uint8_t* Blo = Bhi + (size_t)2 * NBM * 128;
-    float* inbox = reinterpret_cast<float*>(base + a.off_acc);       // [2][G][NBM][32]
+    float* inbox = reinterpret_cast<float*>(base + a.off_acc);       // [G][NBM][32]
     float* dcc = reinterpret_cast<float*>(base + a.off_state);       // [B][32]
     uint64_t* mma_bar = reinterpret_cast<uint64_t*>(base + a.off_sums);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 1);
@@ -433,30 +711,12 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
     int* s_off = s_bs + T;
     int* s_len = s_off + T + 1;
     const uint32_t tcols = (uint32_t)a.Umax;
-    auto inbox_at = [&](int parity, int src, int j) -> float* {
-        return inbox + (((size_t)parity * G + src) * NBM + j) * kCU;
-    };
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto inbox_at = [&](int src, int j) -> float* { return inbox + ((size_t)src * NBM + j) * kCU; };
 
-    // R^T slice: row u' (any unit), column r = g*32 + uu (this CTA's gate rows)
-    const __nv_bfloat16* Rb = reinterpret_cast<const __nv_bfloat16*>(a.R);
-    const float* Rf = reinterpret_cast<const float*>(a.R);
-    for (int idx = threadIdx.x; idx < AR * 16; idx += kCT) {
-        const int up = idx >> 4, r0 = (idx & 15) * 8;
-        float v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int r = r0 + e, g = r / kCU, uu = r - g * kCU;
-            const size_t src = (size_t)dir * 4 * H * H + (size_t)(g * H + u0 + uu) * H + up;
-            v[e] = up < H ? (SPLIT ? Rf[src] : __bfloat162float(Rb[src])) : 0.f;
-        }
-        uint4 hi, lo;
-        split8(v, hi, lo, SPLIT);
-        const uint32_t o = sw_off(up, r0, AR);
-        *reinterpret_cast<uint4*>(Ahi + o) = hi;
-        if (SPLIT) *reinterpret_cast<uint4*>(Alo + o) = lo;
-    }
-    for (int i = threadIdx.x; i < 2 * 2 * NBM * 128 / 16; i += kCT) reinterpret_cast<uint4*>(Bhi)[i] = make_uint4(0, 0, 0, 0);
-    for (int i = threadIdx.x; i < 2 * G * NBM * kCU; i += kCT) inbox[i] = 0.f;
+    for (int i = threadIdx.x; i < (SPLIT ? 2 : 1) * 2 * NBM * 128 / 16; i += kCT)
+        reinterpret_cast<uint4*>(Bhi)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < G * NBM * kCU; i += kCT) inbox[i] = 0.f;
     for (int i = threadIdx.x; i < T; i += kCT) s_bs[i] = a.bs[i];
     for (int i = threadIdx.x; i <= T; i += kCT) s_off[i] = a.off[i];
     for (int i = threadIdx.x; i < a.B; i += kCT) s_len[i] = a.slot_len[i];
@@ -465,7 +725,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
         peep_s[i] = a.peep[(size_t)dir * 3 * H + q * H + u0 + uu];
     }
     if (threadIdx.x == 0) {
-        tc::mbar_init(mma_bar, kChains);
+        tc::mbar_init(mma_bar, (uint32_t)(MT * nch));
         *s_fail = 0;
         tc::fence_mbar_init();
     }
@@ -478,10 +738,39 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
     __syncthreads();
     tc::tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    const uint32_t a_hi = tmem + (uint32_t)a.tm_acol, a_lo = a_hi + (uint32_t)(64 * MT);
+    // R^T slice -> tensor memory: tile m, lane l = unit 128m + l (zero past H); column 64m + c
+    // holds this CTA's gate rows r = 2c, 2c + 1 (r = 32g + uu); warps q and q + 4 share the
+    // lanes 32q.. and take alternate gates
+    {
+        const int q = warp & 3;
+        const uint32_t lanes = (uint32_t)(32 * q) << 16;
+        for (int m = 0; m < MT; ++m) {
+            const int up = 128 * m + 32 * q + lane;
+            for (int g = warp >> 2; g < 4; g += 2) {
+                float v[32];
+#pragma unroll
+                for (int uu = 0; uu < 32; ++uu) {
+                    const size_t src = (size_t)dir * 4 * H * H + (size_t)(g * H + u0 + uu) * H + up;
+                    v[uu] = up < H ? (SPLIT ? __ldg(reinterpret_cast<const float*>(a.R) + src)
+                                            : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.R)[src]))
+                                   : 0.f;
+                }
+                uint32_t hi[16], lo[16];
+                split32<SPLIT>(v, hi, lo);
+                tc::tmem_st_32x32b_x16(a_hi + lanes + (uint32_t)(64 * m + 16 * g), hi);
+                if (SPLIT) tc::tmem_st_32x32b_x16(a_lo + lanes + (uint32_t)(64 * m + 16 * g), lo);
+            }
+        }
+        tc::tmem_wait_st();
+    }
+    tc::tc_fence_before_sync();
+    __syncthreads();
+    tc::tc_fence_after_sync();
     cl.sync();
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int jq = threadIdx.x >> 3, q8 = threadIdx.x & 7;          // cell item: row jq (+32k), units q8*4..+4
+    const uint32_t bstep = (uint32_t)(NBM * 128) >> 4;
     // own operands (gates, c_t, c_{t-1}, dy) of row jq of a step, loaded one step ahead
     float nx[7][4];
     auto load_own = [&](int s2) {
@@ -510,6 +799,8 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
         }
     };
     load_own(0);
+    bool failed = false;                  // CTA-uniform: an MMA completion wait timed out
+    bool step_ok = true;                  // this thread's wait of the last product
     for (int s = 0; s < T; ++s) {
         const int t = dir == 0 ? T - 1 - s : s;
         const int n = s_bs[t];
@@ -518,7 +809,6 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
         const int prev_base = dir == 0 ? (t >= 1 ? s_off[t - 1] : 0) : (t + 1 < T ? s_off[t + 1] : 0);
         const int n_prev = dir == 0 ? (t >= 1 ? n : 0) : (t + 1 < T ? s_bs[t + 1] : 0);
         const int NBs = (n + 15) & ~15;
-        const int cur = s & 1, nxt = cur ^ 1;
         cstamp(a, true, dir, rank, s, 0, 1);
         for (int it = 0; it * 32 < n; ++it) {
             const int j = jq + it * 32;
@@ -535,12 +825,11 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
                 }
             } else {
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const float4 x = *reinterpret_cast<const float4*>(gr + g * H);
-                gv[g][0] = x.x; gv[g][1] = x.y; gv[g][2] = x.z; gv[g][3] = x.w;
-            }
-            const size_t yo = (size_t)row * ndH + dir * H + u0 + uub;
-            {
+                for (int g = 0; g < 4; ++g) {
+                    const float4 x = *reinterpret_cast<const float4*>(gr + g * H);
+                    gv[g][0] = x.x; gv[g][1] = x.y; gv[g][2] = x.z; gv[g][3] = x.w;
+                }
+                const size_t yo = (size_t)row * ndH + dir * H + u0 + uub;
                 const float4 c0 = __ldg(reinterpret_cast<const float4*>(a.cbuf + yo));
                 cv[0] = c0.x; cv[1] = c0.y; cv[2] = c0.z; cv[3] = c0.w;
                 const float4 d0 = __ldg(reinterpret_cast<const float4*>(a.dy + yo));
@@ -553,7 +842,6 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
                     cpv[0] = cpv[1] = cpv[2] = cpv[3] = 0.f;
                 }
             }
-            }
             const bool has_next = j < n_next;
             const bool real = !a.padded || t < s_len[j];
             float da[4][4];
@@ -562,7 +850,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
                 const int uu = uub + e;
                 float dh_rec = 0.f;
                 if (has_next)
-                    for (int c2 = 0; c2 < G; ++c2) dh_rec += inbox_at(cur, c2, j)[uu];
+                    for (int c2 = 0; c2 < G; ++c2) dh_rec += inbox_at(c2, j)[uu];
                 float dai = 0.f, daf = 0.f, daz = 0.f, dao = 0.f, carry_out = 0.f;
                 if (real) {
                     const float ig = gv[0][e], fg = gv[1][e], zg = gv[2][e], og = gv[3][e];
@@ -590,61 +878,47 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
                 if (SPLIT) *reinterpret_cast<uint2*>(Blo + o) = lo;
             }
         }
+        cluster_arrive_relaxed();   // this CTA has read its inbox: peers may overwrite it
         fence_proxy_async_cta();
-        __syncthreads();
+        // a timeout of the previous step's product becomes a CTA-uniform decision here, before
+        // the next issue (that step's read-out may have seen partial sums; the status word
+        // marks the results as invalid)
+        if (__syncthreads_or(!step_ok)) failed = true;
         cstamp(a, true, dir, rank, s, 2, 2);
         if (s + 1 < T) {
-            // P[u'][j] = sum over this CTA's gate rows r of R[r][u'] da[j][r]; chain ch of the 8
-            // k-steps (k = ch, ch + kChains, ...) is issued by warp ch into accumulators (m, ch)
-            if (lane == 0 && warp < kChains && !*(volatile int*)s_fail) {
+            // P[u'][j] = sum over this CTA's gate rows r of R[r][u'] da[j][r]: warp w issues tile
+            // m = w / chains, chain ch = w % chains (k-steps ch, ch + chains, ... of the 8)
+            if (lane == 0 && warp < MT * nch && !failed) {
                 tc::tc_fence_after_sync();
+                const int m = warp / nch, ch = warp - m * nch;
                 const uint32_t idesc = tc::idesc_bf16_f32(kCM, NBs);
-                const uint64_t dah = tc::sdesc_sw128(tc::smem_u32(Ahi)), dal = tc::sdesc_sw128(tc::smem_u32(Alo));
                 const uint64_t dbh = tc::sdesc_sw128(tc::smem_u32(Bhi)), dbl = tc::sdesc_sw128(tc::smem_u32(Blo));
-                for (int i = warp; i < 8; i += kChains) {
-                    const uint32_t bo = (uint32_t)(i >> 2) * NBM * 128 + (uint32_t)(i & 3) * 32;
-                    const uint32_t acc = i == warp ? 0u : 1u;
-                    for (int m = 0; m < MT; ++m) {
-                        const uint32_t ao = (uint32_t)(i >> 2) * AR * 128 + (uint32_t)m * kCM * 128 + (uint32_t)(i & 3) * 32;
-                        const uint32_t d = tmem + (uint32_t)((m * kChains + warp) * NBM);
-                        if (SPLIT) {
-                            tc::mma_bf16_ss(d, desc_add(dal, ao), desc_add(dbh, bo), idesc, acc);
-                            tc::mma_bf16_ss(d, desc_add(dah, ao), desc_add(dbl, bo), idesc, 1u);
-                            tc::mma_bf16_ss(d, desc_add(dah, ao), desc_add(dbh, bo), idesc, 1u);
-                        } else {
-                            tc::mma_bf16_ss(d, desc_add(dah, ao), desc_add(dbh, bo), idesc, acc);
-                        }
-                    }
-                }
-                tc::mma_commit(mma_bar);
+                issue_chains<SPLIT>(nch, tmem + (uint32_t)(warp * NBM), a_hi + (uint32_t)(64 * m),
+                                    a_lo + (uint32_t)(64 * m), dbh, dbl, bstep, 8, ch, idesc);
+                if (!(s == 0 && dir == 0 && rank == a.debug_skip_cta)) tc::mma_commit(mma_bar);   // test hook
             }
-            if (warp < kChains) __syncwarp();
+            if (warp < MT * nch) __syncwarp();
             cstamp(a, true, dir, rank, s, 6, 6);
-            const bool ok = *(volatile int*)s_fail ? false : tc::mbar_wait(mma_bar, (uint32_t)(s & 1), a.wait_limit_ns);
-            if (!ok && !*(volatile int*)s_fail) {
+            step_ok = failed ? true : tc::mbar_wait(mma_bar, (uint32_t)(s & 1), a.wait_limit_ns);
+            if (!step_ok) {
                 record_failure(a.status, LSTM_ERR_TIMEOUT, 0x50000u | (unsigned)s);
-                *(volatile int*)s_fail = 1;
+                *s_fail = 1 + s;
             }
             tc::tc_fence_after_sync();
             cstamp(a, true, dir, rank, s, 5, 7);
+        }
+        cluster_wait();        // every peer has read its inbox of this step
+        if (s + 1 < T && !failed) {
             // tile m, lane quarter q: units u' = 128m + 32q + lane, owned by CTA 4m + q
             for (int pq = warp; pq < MT * 4; pq += kCT / 32) {
                 const int m = pq >> 2, q = pq & 3;
                 const int owner = 4 * m + q;
                 if (owner >= G) continue;
-                float* dst_base = cl.map_shared_rank(inbox_at(nxt, rank, 0), owner);
+                float* dst_base = cl.map_shared_rank(inbox_at(rank, 0), owner);
                 for (int c0 = 0; c0 < NBs; c0 += 16) {
                     float v[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) v[e] = 0.f;
-                    for (int ch = 0; ch < kChains; ++ch) {
-                        uint32_t r[16];
-                        tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)(q * 32) << 16) +
-                                                   (uint32_t)((m * kChains + ch) * NBM + c0), r);
-                        tc::tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) v[e] += __uint_as_float(r[e]);
-                    }
+                    tmem_sum_chains(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(m * nch * NBM + c0),
+                                    (uint32_t)NBM, nch, v);
                     // lanes are consecutive units: each store is one coalesced 128-byte row
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
@@ -653,9 +927,11 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
             }
             tc::tc_fence_before_sync();
         }
-        if (s + 1 < T) load_own(s + 1);       // the next step's own operands, in flight across the barrier
         cstamp(a, true, dir, rank, s, 3, 3);
-        cl.sync();
+        fence_proxy_async_cluster();
+        cluster_arrive();      // release: this CTA's partial sums are in their owners' inboxes
+        if (s + 1 < T) load_own(s + 1);       // the next step's own operands, in flight across the barrier
+        cluster_wait();
         cstamp(a, true, dir, rank, s, 4, 4);
     }
     tc::tc_fence_before_sync();
@@ -663,6 +939,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
     if (threadIdx.x < 32) {
         __syncwarp();
         tc::tc_fence_after_sync();
+        if (failed) tc::mbar_wait(mma_bar, (uint32_t)((*s_fail - 1) & 1), kTeardownWaitNs);
         tc::tmem_dealloc(tmem, tcols);
     }
 }
@@ -714,48 +991,121 @@ __global__ void lstm_param_sums_combine(const float* __restrict__ partial, int c
 
 static size_t al(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+static uint32_t pow2_cols(int need)
+{
+    uint32_t cols = 32;
+    while (cols < (uint32_t)need) cols <<= 1;
+    return cols;
+}
+
+// Dynamic shared memory for a cluster kernel that allocates `tcols` TMEM
+// columns per CTA: at least enough that no more CTAs fit on one SM than
+// their columns fit in its 512 (a CTA whose allocation waited for another
+// CTA of the same cluster would never see it leave).
+static size_t tmem_safe_smem(const Plan& p, size_t smem, uint32_t tcols)
+{
+    int per_sm = 0;
+    if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, p.device) != cudaSuccess)
+        return 0;
+    const int fit = 512 / (int)tcols;                 // CTAs whose columns fit together
+    if (fit >= 2048 / kCT) return smem;               // the thread limit already caps residency
+    const size_t reserved = 1024;                     // per-CTA shared memory reserved by the system
+    const size_t need = (size_t)per_sm / (size_t)(fit + 1) - reserved + 64;
+    return std::max(smem, need);
+}
+
+// True when at least one cluster of `G` CTAs with `smem` bytes can be resident.
+static bool cluster_schedulable(const Plan& p, const void* fn, int G, size_t smem)
+{
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p.device) != cudaSuccess) return false;
+    if (smem > (size_t)optin) return false;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (G > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(G);
+    cfg.blockDim = dim3(kCT);
+    cfg.dynamicSmemBytes = smem;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = G;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return clusters >= 1;
+}
+
+static int max_active_rows(const Plan& p)
+{
+    int bmax = 0;
+    for (int t = 0; t < p.T; ++t) bmax = std::max(bmax, p.h_bs[t]);
+    return bmax;
+}
+
+static const void* fwd_kernel(bool bf16, bool bulk)
+{
+    if (bulk) return bf16 ? (const void*)lstm_rec_fwd_cluster_kernel<false, true>
+                          : (const void*)lstm_rec_fwd_cluster_kernel<true, true>;
+    return bf16 ? (const void*)lstm_rec_fwd_cluster_kernel<false, false> : (const void*)lstm_rec_fwd_cluster_kernel<true, false>;
+}
+
 bool rec_cluster_fwd_configure(const Plan& p, int H, int ndir, bool bf16, RecConfig* out, RecArgs* lay)
 {
     if (p.gemm_engine != 0 || p.forced_ctas != 0) return false;
     if (H % kCU != 0) return false;
     const int G = H / kCU;
     if (G > 16 || G * ndir > p.num_sms) return false;
-    int bmax = 0;
-    for (int t = 0; t < p.T; ++t) bmax = std::max(bmax, p.h_bs[t]);
-    const int NBM = std::max(16, (bmax + 15) & ~15);
-    if (NBM > 128) return false;                   // cell items: 2 rows of 64 per thread
-    const int KB = (H + 63) / 64;
+    const int NBM = std::max(16, (max_active_rows(p) + 15) & ~15);
+    if (NBM > 128) return false;                   // cell items: 4 rows of 32 per thread
     const bool split = !bf16;
-    size_t off = 0;
-    const size_t abytes = (size_t)KB * kCM * 128;
-    const size_t o_ahi = off; off = al(off + abytes, 1024);
-    const size_t o_alo = off; if (split) off = al(off + abytes, 1024);
-    const size_t o_b = off; off = al(off + 4 * (size_t)KB * NBM * 128, 1024);
-    const size_t o_acc = off; off = al(off + (size_t)NBM * kCM * 4, 16);
-    const size_t o_cst = off; off = al(off + (size_t)p.B * kCU * 4, 16);
-    const size_t o_bar = off; off = al(off + 64, 16);
-    const size_t o_peep = off; off = al(off + 3 * kCU * 4, 16);
-    const size_t o_tab = off; off = al(off + (size_t)(2 * p.T + 1 + p.B) * 4, 16);
-    const size_t smem = off + 1024 + 64;          // 1024 for the base alignment, 64 static
-    int optin = 0;
-    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p.device) != cudaSuccess) return false;
-    if (smem > (size_t)optin) return false;
-    uint32_t cols = 32;
-    while (cols < (uint32_t)(kChains * NBM)) cols <<= 1;
-    if (cols > 512) return false;
-    RecConfig c;
-    c.G = G; c.Umax = (int)cols; c.JC = NBM; c.smem = smem; c.cluster = 1;
-    *out = c;
-    lay->off_h = (int)o_ahi; lay->off_red = (int)o_alo; lay->off_contrib = (int)o_b; lay->off_acc = (int)o_acc;
-    lay->off_state = (int)o_cst; lay->off_sums = (int)o_bar; lay->off_peep = (int)o_peep; lay->off_tab = (int)o_tab;
-    return true;
+    const int KB = (H + 63) / 64;
+    const int nks = (H + 15) / 16;
+    const int acols = (H / 2) * (split ? 2 : 1);   // R slice in TMEM, two bf16 per column
+    int nch = 4;
+    while (nch > 1 && (nch > nks || nch * NBM + acols > 512)) nch >>= 1;
+    if (nch * NBM + acols > 512) return false;
+    const uint32_t cols = pow2_cols(nch * NBM + acols);
+    // bulk exchange first (double-buffered operand + staging), else the single-buffered one
+    for (int bulk = 1; bulk >= 0; --bulk) {
+        const size_t bbytes = bulk ? 2 * (split ? 2 : 1) * (size_t)G * NBM * 64 : (split ? 2 : 1) * (size_t)KB * NBM * 128;
+        size_t off = 0;
+        const size_t o_b = off; off = al(off + bbytes, 1024);
+        const size_t o_stage = off; if (bulk) off = al(off + 4 * (size_t)NBM * 64, 1024);
+        const size_t o_acc = off; off = al(off + (size_t)NBM * kCM * 4, 16);
+        const size_t o_cst = off; off = al(off + (size_t)p.B * kCU * 4, 16);
+        const size_t o_bar = off; off = al(off + 64, 16);
+        const size_t o_peep = off; off = al(off + 3 * kCU * 4, 16);
+        const size_t o_tab = off; off = al(off + (size_t)(2 * p.T + 1 + p.B) * 4, 16);
+        size_t smem = off + 1024 + 64;            // 1024 for the base alignment, 64 static
+        smem = tmem_safe_smem(p, smem, cols);
+        if (smem == 0) return false;
+        if (!cluster_schedulable(p, fwd_kernel(bf16, bulk != 0), G, smem)) continue;
+        RecConfig c;
+        c.G = G; c.Umax = (int)cols; c.JC = NBM; c.smem = smem; c.cluster = 1;
+        c.chains = nch; c.acol = (int)cols - acols; c.bulk = bulk;
+        *out = c;
+        lay->off_contrib = (int)o_b; lay->off_h = (int)o_stage; lay->off_acc = (int)o_acc;
+        lay->off_state = (int)o_cst; lay->off_sums = (int)o_bar; lay->off_peep = (int)o_peep;
+        lay->off_tab = (int)o_tab;
+        return true;
+    }
+    return false;
 }
 
-lstm_status rec_cluster_fwd_launch(const Plan& p, const RecConfig& c, RecArgs a, cudaStream_t s)
+static lstm_status cluster_launch(const RecConfig& c, const void* fn, RecArgs& a, cudaStream_t s)
 {
-    a.G = c.G; a.Umax = c.Umax; a.JC = c.JC;
-    a.trace = p.d_trace; a.trace_steps = p.trace_steps;
-    void* fn = a.bf16 ? (void*)lstm_rec_fwd_cluster_kernel<false> : (void*)lstm_rec_fwd_cluster_kernel<true>;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem) != cudaSuccess)
         return LSTM_ERR_CUDA;
     if (c.G > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
@@ -772,12 +1122,21 @@ lstm_status rec_cluster_fwd_launch(const Plan& p, const RecConfig& c, RecArgs a,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    trace_begin(p, K_REC_FWD, s);
     void* args[] = {&a};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
-    trace_end(p, K_REC_FWD, s, e == cudaSuccess ? 1 : 0);
     if (e != cudaSuccess) { cudaGetLastError(); return LSTM_ERR_UNSUPPORTED; }
     return LSTM_OK;
+}
+
+lstm_status rec_cluster_fwd_launch(const Plan& p, const RecConfig& c, RecArgs a, cudaStream_t s)
+{
+    a.G = c.G; a.Umax = c.Umax; a.JC = c.JC; a.tm_chains = c.chains; a.tm_acol = c.acol;
+    a.trace = p.d_trace; a.trace_steps = p.trace_steps;
+    const void* fn = fwd_kernel(a.bf16 != 0, c.bulk != 0);
+    trace_begin(p, K_REC_FWD, s);
+    const lstm_status st = cluster_launch(c, fn, a, s);
+    trace_end(p, K_REC_FWD, s, st == LSTM_OK ? 1 : 0);
+    return st;
 }
 
 bool rec_cluster_bwd_configure(const Plan& p, int H, int ndir, bool bf16, RecConfig* out, RecArgs* lay)
@@ -786,34 +1145,33 @@ bool rec_cluster_bwd_configure(const Plan& p, int H, int ndir, bool bf16, RecCon
     if (H % kCU != 0) return false;
     const int G = H / kCU;
     if (G > 16 || G * ndir > p.num_sms) return false;
-    int bmax = 0;
-    for (int t = 0; t < p.T; ++t) bmax = std::max(bmax, p.h_bs[t]);
-    const int NBM = std::max(16, (bmax + 15) & ~15);
+    const int NBM = std::max(16, (max_active_rows(p) + 15) & ~15);
     if (NBM > 128) return false;
     const int MT = (H + kCM - 1) / kCM;
     const bool split = !bf16;
-    const size_t abytes = (size_t)MT * kCM * 2 * 128;
+    const int acols = MT * 64 * (split ? 2 : 1);   // R^T tiles in TMEM: 128 gate rows = 64 columns
+    int nch = 4;
+    while (nch > 1 && (MT * nch > 4 || MT * nch * NBM + acols > 512)) nch >>= 1;
+    if (MT * nch * NBM + acols > 512 || MT * nch > kCT / 32) return false;
+    const uint32_t cols = pow2_cols(MT * nch * NBM + acols);
     size_t off = 0;
-    const size_t o_ahi = off; off = al(off + abytes, 1024);
-    const size_t o_alo = off; if (split) off = al(off + abytes, 1024);
-    const size_t o_b = off; off = al(off + (size_t)2 * 2 * NBM * 128, 1024);
-    const size_t o_in = off; off = al(off + (size_t)2 * G * NBM * kCU * 4, 16);
+    const size_t o_b = off; off = al(off + (split ? 2 : 1) * (size_t)2 * NBM * 128, 1024);
+    const size_t o_in = off; off = al(off + (size_t)G * NBM * kCU * 4, 16);
     const size_t o_dcc = off; off = al(off + (size_t)p.B * kCU * 4, 16);
     const size_t o_bar = off; off = al(off + 64, 16);
     const size_t o_peep = off; off = al(off + 3 * kCU * 4, 16);
     const size_t o_tab = off; off = al(off + (size_t)(2 * p.T + 1 + p.B) * 4, 16);
-    const size_t smem = off + 1024 + 64;
-    int optin = 0;
-    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p.device) != cudaSuccess) return false;
-    if (smem > (size_t)optin) return false;
-    uint32_t cols = 32;
-    while (cols < (uint32_t)(MT * kChains * NBM)) cols <<= 1;
-    if (cols > 512) return false;
+    size_t smem = off + 1024 + 64;
+    smem = tmem_safe_smem(p, smem, cols);
+    if (smem == 0) return false;
+    const void* fn = bf16 ? (const void*)lstm_rec_bwd_cluster_kernel<false> : (const void*)lstm_rec_bwd_cluster_kernel<true>;
+    if (!cluster_schedulable(p, fn, G, smem)) return false;
     RecConfig c;
     c.G = G; c.Umax = (int)cols; c.JC = NBM; c.smem = smem; c.cluster = 1;
+    c.chains = nch; c.acol = (int)cols - acols;
     *out = c;
-    lay->off_h = (int)o_ahi; lay->off_red = (int)o_alo; lay->off_contrib = (int)o_b; lay->off_acc = (int)o_in;
-    lay->off_state = (int)o_dcc; lay->off_sums = (int)o_bar; lay->off_peep = (int)o_peep; lay->off_tab = (int)o_tab;
+    lay->off_contrib = (int)o_b; lay->off_acc = (int)o_in; lay->off_state = (int)o_dcc;
+    lay->off_sums = (int)o_bar; lay->off_peep = (int)o_peep; lay->off_tab = (int)o_tab;
     return true;
 }
 
@@ -821,30 +1179,13 @@ size_t rec_cluster_bwd_sum_floats(int H, int ndir) { return (size_t)kSumChunks *
 
 lstm_status rec_cluster_bwd_launch(const Plan& p, const RecConfig& c, RecArgs a, float* sum_scratch, cudaStream_t s)
 {
-    a.G = c.G; a.Umax = c.Umax; a.JC = c.JC;
+    a.G = c.G; a.Umax = c.Umax; a.JC = c.JC; a.tm_chains = c.chains; a.tm_acol = c.acol;
     a.trace = p.d_trace; a.trace_steps = p.trace_steps;
-    void* fn = a.bf16 ? (void*)lstm_rec_bwd_cluster_kernel<false> : (void*)lstm_rec_bwd_cluster_kernel<true>;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem) != cudaSuccess)
-        return LSTM_ERR_CUDA;
-    if (c.G > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-        return LSTM_ERR_UNSUPPORTED;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    cfg.gridDim = dim3(c.G * a.ndir);
-    cfg.blockDim = dim3(kCT);
-    cfg.dynamicSmemBytes = c.smem;
-    cfg.stream = s;
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = c.G;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    const void* fn = a.bf16 ? (const void*)lstm_rec_bwd_cluster_kernel<false> : (const void*)lstm_rec_bwd_cluster_kernel<true>;
     trace_begin(p, K_REC_BWD, s);
-    void* args[] = {&a};
-    cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
-    int launched = e == cudaSuccess ? 1 : 0;
-    if (e == cudaSuccess) {
+    lstm_status st = cluster_launch(c, fn, a, s);
+    int launched = st == LSTM_OK ? 1 : 0;
+    if (st == LSTM_OK) {
         const int ncols = a.ndir * 7 * a.H;
         const int rows = (int)p.rows;
         const int chunk = (rows + kSumChunks - 1) / kSumChunks;
@@ -852,12 +1193,12 @@ lstm_status rec_cluster_bwd_launch(const Plan& p, const RecConfig& c, RecArgs a,
             a.ga, a.cbuf, p.d_prev_fwd, p.d_prev_rev, rows, a.H, a.ndir, chunk, sum_scratch);
         lstm_param_sums_combine<<<(ncols + 255) / 256, 256, 0, s>>>(sum_scratch, kSumChunks, a.H, a.ndir, a.db,
                                                                     a.dpeep);
-        e = cudaGetLastError();
-        launched += e == cudaSuccess ? 2 : 0;
+        const cudaError_t e = cudaGetLastError();
+        if (e == cudaSuccess) launched += 2;
+        else st = LSTM_ERR_UNSUPPORTED;
     }
     trace_end(p, K_REC_BWD, s, launched);
-    if (e != cudaSuccess) { cudaGetLastError(); return LSTM_ERR_UNSUPPORTED; }
-    return LSTM_OK;
+    return st;
 }
 
 }  // namespace lstm

@@ -74,6 +74,15 @@ class Plan:
     def launch_count(self) -> int:
         return int(_lib.load().lstm_plan_launch_count(self.handle))
 
+    def recurrent_config(self, backward: bool = False) -> dict:
+        """Configuration of the last forward (or backward) recurrent launch."""
+        k, g, m = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        check(_lib.load().lstm_plan_recurrent_config(self.handle, int(bool(backward)), ctypes.byref(k),
+                                                     ctypes.byref(g), ctypes.byref(m)),
+              "lstm_plan_recurrent_config")
+        return {"kernel": ("none", "grid", "cluster")[k.value], "ctas_per_direction": g.value,
+                "product": ("cuda_cores", "mma_sync", "tcgen05")[m.value]}
+
     def trace_steps(self, buffer, steps: int):
         """Phase stamps into `buffer` (int64 device tensor of 2*ndir*steps*8), or off with steps=0."""
         check(_lib.load().lstm_debug_trace_steps(self.handle, _ptr(buffer), int(steps)), "lstm_debug_trace_steps")

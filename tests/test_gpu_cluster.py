@@ -29,6 +29,12 @@ CASES = [
     (2, 1, 40, 256, list(np.random.default_rng(9).integers(1, 80, 20)), "f32"),
     (2, 2, 16, 64, [9, 0, 4, 21, 21, 2], "bf16"),
     (2, 1, 32, 256, [60, 3, 44, 17, 60, 9], "bf16"),
+    # wide batches: 112 and 128 operand rows (fewer accumulator chains fit next to R in TMEM)
+    (2, 1, 16, 64, list(np.random.default_rng(3).integers(1, 20, 100)), "f32"),
+    (2, 1, 32, 256, list(np.random.default_rng(4).integers(1, 12, 128)), "f32"),
+    # H = 512: clusters of 16 CTAs per direction
+    (1, 1, 32, 512, [20, 7, 13, 1], "bf16"),
+    (2, 2, 24, 512, [30, 5, 17, 30, 2, 9], "bf16"),
 ]
 
 
@@ -38,6 +44,9 @@ def test_cluster_kernels_match_oracle(case):
     w = synthetic.custom(nd, nl, D, H, lengths, seed=5 + H, dtype=dtype,
                          weight_range=0.1 if dtype == "bf16" else 0.3)
     gpu = run_gpu(w)
+    for backward in (False, True):
+        cfg = gpu["plan"].recurrent_config(backward)
+        assert cfg == {"kernel": "cluster", "ctas_per_direction": H // 32, "product": "tcgen05"}, cfg
     ref = run_oracle(w)
     compare_all(gpu, ref, TOL_BF16 if dtype == "bf16" else TOL_F32, label=f"cluster {case}")
     if dtype == "bf16":

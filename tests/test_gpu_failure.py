@@ -39,3 +39,47 @@ def test_barrier_timeout_is_reported_and_context_survives():
     assert plan.poll() == _lib.LSTM_OK
     assert torch.equal(y1, y2)
     assert torch.isfinite(y1).all()
+
+
+def test_cluster_kernels_timeout_is_reported_and_context_survives():
+    """The cluster kernels' waits that can run out are the bounded waits on MMA completion
+    (and, with the bulk exchange, on the peers' operands).  With the test hook one CTA
+    withholds the completion signal of its first product: its wait runs out, it stops
+    issuing and sending, its peers' operand waits run out in turn, every CTA still runs all
+    its cluster barriers, frees its tensor memory only after its products are done, and
+    reports LSTM_ERR_TIMEOUT; the context stays usable (forward and backward)."""
+    from padding_free_variable_gb300 import _lib, ops, synthetic
+    from gpu_harness import device_layers
+    w = synthetic.custom(2, 1, 8, 64, [30, 20, 10, 5, 17], seed=4)
+    layers = device_layers(w)
+
+    def fresh():
+        plan = ops.Plan(w.lengths)
+        stack = ops.PackedLSTMStack(plan, layers, 8, 64, 2, False)
+        return plan, stack
+
+    x = torch.from_numpy(w.x).cuda()
+    G = torch.from_numpy(w.G).cuda()
+    ref_plan, ref_stack = fresh()
+    y_ref, dx_ref = (t.clone() for t in ref_stack.step(x, G))
+    assert ref_plan.poll() == _lib.LSTM_OK
+    assert ref_plan.recurrent_config(False)["kernel"] == "cluster"
+    assert ref_plan.recurrent_config(True)["kernel"] == "cluster"
+
+    plan, stack = fresh()
+    plan.set_wait_limit(50_000_000)          # 50 ms
+    plan.pack(x, stack.x_packed)
+    plan.pack(G, stack.dy_packed)
+    plan.debug_skip_arrival(1)
+    stack.forward_packed()
+    assert plan.poll() == _lib.LSTM_ERR_TIMEOUT
+    plan.debug_skip_arrival(-1)
+    stack.forward_packed()
+    assert plan.poll() == _lib.LSTM_OK
+    plan.debug_skip_arrival(1)
+    stack.backward_packed()
+    assert plan.poll() == _lib.LSTM_ERR_TIMEOUT
+    plan.debug_skip_arrival(-1)
+    y, dx = stack.step(x, G)
+    assert plan.poll() == _lib.LSTM_OK
+    assert torch.equal(y, y_ref) and torch.equal(dx, dx_ref)
