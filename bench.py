@@ -282,9 +282,13 @@ def cpu_baseline(w, seconds=15.0):
     nthreads = os.cpu_count() or 1
     seqs, frames = oracle_sample(w, seconds, nthreads)
     dt = run_oracle_on(w, seqs, nthreads)
+    seqs1, frames1 = oracle_sample(w, seconds / 3, 1)
+    dt1 = run_oracle_on(w, seqs1, 1)
     return {"value": round(frames / dt, 2), "unit": UNIT, "cores": nthreads, "kind": "oracle",
             "sample": f"{len(seqs)} of {len(w.lengths)} sequences ({frames} frames), fwd+BPTT of every layer, "
-                      f"fp64, OpenMP over sequences, {dt:.1f} s"}
+                      f"fp64, OpenMP over sequences, {dt:.1f} s",
+            "single_core": {"value": round(frames1 / dt1, 2), "unit": UNIT, "cores": 1,
+                            "sample": f"{len(seqs1)} sequences ({frames1} frames), {dt1:.1f} s"}}
 
 
 def reference_arm(args, w, config):
@@ -313,6 +317,77 @@ def reference_arm(args, w, config):
 
 
 # --------------------------------------------------------------------------- GPU arm
+
+def _time_steps(fn, steps, flush, stream):
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i, (a, b) in enumerate(ev):
+        flush.fill_(float(i))
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / steps
+
+
+def bucket_comparator(w, spec, bf16, layers, flush, stream, steps, width=100):
+    """Sorted-bucket batching ("On batching variable size inputs", Sec. 2): sequences grouped
+    by length into buckets of `width` frames, each bucket padded to its own longest sequence
+    and run as its own batch (a padded plan) with the same kernels; one step = every bucket."""
+    import torch
+    from padding_free_variable_gb300 import ops
+    from padding_free_variable_gb300.sharding import shard_rows
+    lengths = np.asarray(w.lengths)
+    lo = int(lengths.min()) // width * width
+    groups = {}
+    for i, L in enumerate(lengths):
+        groups.setdefault((int(L) - lo) // width, []).append(i)
+    xdt = torch.bfloat16 if bf16 else torch.float32
+    runs, computed = [], 0
+    for k in sorted(groups):
+        idx = np.array(groups[k], dtype=np.int64)
+        rows = shard_rows(lengths, idx)
+        plan = ops.Plan(lengths[idx], padded=True)
+        st = ops.PackedLSTMStack(plan, layers, spec.input_size, spec.hidden_size, spec.num_directions, bf16)
+        x = torch.from_numpy(w.x[rows]).to("cuda", dtype=xdt)
+        G = torch.from_numpy(w.G[rows]).cuda()
+        runs.append((plan, st, x, G))
+        computed += len(idx) * int(lengths[idx].max())
+
+    def step():
+        for plan, st, x, G in runs:
+            st.step(x, G)
+
+    ms = _time_steps(step, steps, flush, stream)
+    N = int(lengths.sum())
+    return {"frames_per_s": round(N / (ms / 1e3), 2), "ms_per_step": round(ms, 3), "bucket_width": width,
+            "buckets": len(runs), "computed_frames": int(computed),
+            "zero_padding_rate": round((computed - N) / N, 4), "waste_fraction": round((computed - N) / computed, 4)}
+
+
+def stepwise_comparator(w, spec, bf16, layers, x_dev, G_dev, y_cat, dx_cat, flush, stream, steps):
+    """The per-step-launch path (one product launch per direction and one cell launch per time
+    step, the RETURNN paper's Sec. 4.2 design) on the same packed batch."""
+    from padding_free_variable_gb300 import ops
+    plan = ops.Plan(w.lengths)
+    st = ops.PackedLSTMStack(plan, layers, spec.input_size, spec.hidden_size, spec.num_directions, bf16,
+                             stepwise=True)
+
+    def step():
+        plan.pack(x_dev, st.x_packed)
+        plan.pack(G_dev, st.dy_packed)
+        st.forward_packed()
+        st.backward_packed()
+        plan.unpack(st.y[-1], y_cat)
+        plan.unpack(st.dx[0], dx_cat)
+
+    l0 = plan.launch_count()
+    ms = _time_steps(step, steps, flush, stream)
+    per_step = (plan.launch_count() - l0) // (steps + 1)
+    return {"frames_per_s": round(w.N / (ms / 1e3), 2), "ms_per_step": round(ms, 3), "launches_per_step": per_step}
+
 
 def main():
     ap = argparse.ArgumentParser()
@@ -510,6 +585,9 @@ def main():
                                       "waste_fraction": round((B * T - N) / (B * T), 4),
                                       "zero_padding_rate": round((B * T - N) / N, 4)}
         del pstack, pplan
+        comparators["sorted_buckets"] = bucket_comparator(w, spec, bf16, stack.layers, flush, stream, psteps)
+        comparators["per_step_launch"] = stepwise_comparator(w, spec, bf16, stack.layers, x_dev, G_dev, y_cat,
+                                                             dx_cat, flush, stream, max(3, min(5, args.steps)))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

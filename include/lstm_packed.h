@@ -320,6 +320,26 @@ typedef enum {
 lstm_status lstm_plan_enable_timing(lstm_plan* plan, int32_t enable);
 lstm_status lstm_plan_read_timing(lstm_plan* plan, double* ms, int64_t* calls);
 
+/* Per-step-launch path (a comparator, not the fast path).  The design the
+ * RETURNN paper describes for its GPU LSTM (Sec. 4.2): after the one
+ * non-recurrent product, every time step is one product launch per direction
+ * (R h_{t-1} over the step's active rows, CUDA cores) and one cell launch for
+ * both directions; the backward pass mirrors it (one cell launch and one
+ * R^T da product per direction per step), then the same db/dpeep sums and
+ * dX/dW/dR products as lstm_bwd.  Same arguments, layouts, results (within
+ * the fp32 / bf16 tolerances) and errors as lstm_fwd / lstm_bwd, plus
+ * `scratch` (device, 16-byte aligned, lstm_stepwise_scratch_bytes, owned by
+ * the caller; the forward pass also needs it).  Padded plans are refused with
+ * LSTM_ERR_UNSUPPORTED.  2·T·ndir + T launches per layer and pass. */
+size_t lstm_stepwise_scratch_bytes(const lstm_plan* plan, const lstm_layer_shape* shape);
+lstm_status lstm_fwd_stepwise(const lstm_plan* plan, const lstm_layer_shape* shape,
+                              const lstm_layer_params* params, const void* x_packed, float* y_packed,
+                              void* y_lo, float* h_n, float* c_n, void* workspace, void* scratch, void* stream);
+lstm_status lstm_bwd_stepwise(const lstm_plan* plan, const lstm_layer_shape* shape,
+                              const lstm_layer_params* params, const void* x_packed, const float* y_packed,
+                              void* workspace, const float* dy_packed, float* dx_packed,
+                              const lstm_layer_grads* grads, void* scratch, void* stream);
+
 /* Kernels launched through this plan since it was created (traced or not);
  * -1 for a NULL plan. */
 int64_t lstm_plan_launch_count(const lstm_plan* plan);

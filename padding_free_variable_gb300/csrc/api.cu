@@ -13,6 +13,7 @@
 #include "common.cuh"
 #include "gemm.cuh"
 #include "recurrent.cuh"
+#include "stepwise.cuh"
 
 namespace lstm {
 
@@ -184,6 +185,78 @@ lstm_status bwd_products_tc(const Plan& p, const lstm_layer_shape& s, const lstm
     return LSTM_OK;
 }
 
+// dX, dW and dR of a layer from its gate errors (ga) after the recurrence.
+lstm_status bwd_products(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm,
+                         const void* x_packed, const float* y_packed, const float* ga, float* dx_packed,
+                         const lstm_layer_grads& grads, void* scratch, cudaStream_t cs)
+{
+    const int H = s.hidden_size, nd = s.num_directions, D = s.input_size;
+    const bool bf16 = s.dtype == LSTM_BF16;
+    lstm_status st;
+    const int nd4H = nd * 4 * H;
+    if (bf16 && p.gemm_engine == 0 && D % 8 == 0 && encode_ready())
+        return bwd_products_tc(p, s, prm, x_packed, y_packed, ga, dx_packed, grads, scratch, cs);
+    GemmDesc gw, gr, gx;
+    bwd_gemm_shapes(p, s, &gw, &gr, &gx);
+    if (dx_packed) {
+        GemmDesc g = gx;
+        g.partial = (float*)scratch;
+        g.A = ga; g.sam = nd4H; g.sak = 1;
+        g.B = prm.W; g.sbk = D; g.sbn = 1; g.b_bf16 = bf16;
+        g.C = dx_packed; g.ldc = D; g.round_bf16 = bf16;
+        if ((st = gemm_simt(g, p, K_GEMM_DX, cs)) != LSTM_OK) return st;
+    }
+    gw.A = ga; gw.sam = 1; gw.sak = nd4H;
+    gw.B = x_packed; gw.sbk = D; gw.sbn = 1; gw.b_bf16 = bf16;
+    gw.C = grads.dW; gw.ldc = D; gw.round_bf16 = bf16; gw.partial = (float*)scratch;
+    if ((st = gemm_simt(gw, p, K_GEMM_DW, cs)) != LSTM_OK) return st;
+    for (int d = 0; d < nd; ++d) {
+        GemmDesc g = gr;
+        g.A = ga + (size_t)d * 4 * H; g.sam = 1; g.sak = nd4H;
+        g.B = y_packed + (size_t)d * H; g.sbk = nd * H; g.sbn = 1;
+        g.b_rows = d == 0 ? p.d_prev_fwd : p.d_prev_rev;
+        g.C = grads.dR + (size_t)d * 4 * H * H; g.ldc = H; g.round_bf16 = bf16;
+        g.partial = (float*)scratch;
+        if ((st = gemm_simt(g, p, K_GEMM_DR, cs)) != LSTM_OK) return st;
+    }
+    return LSTM_OK;
+}
+
+// Scratch of the per-step path: the gradient products' scratch (whose first
+// region also holds the db / dpeep partials), then R h_{t-1} of a step
+// [ndir][B][4H], R^T da of a step [ndir][B][H] and the cell-state error carry
+// [ndir][B][H].
+struct StepScratch {
+    size_t rh = 0, dh = 0, dcc = 0, total = 0;
+};
+
+StepScratch step_scratch(const Plan& p, const lstm_layer_shape& s)
+{
+    StepScratch q;
+    const size_t B = (size_t)p.B, H = (size_t)s.hidden_size, nd = (size_t)s.num_directions;
+    size_t off = align256(bwd_scratch(p, s).total);
+    q.rh = off; off += align256(nd * B * 4 * H * sizeof(float));
+    q.dh = off; off += align256(nd * B * H * sizeof(float));
+    q.dcc = off; off += align256(nd * B * H * sizeof(float));
+    q.total = off;
+    return q;
+}
+
+StepArgs step_args(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm, float* ga,
+                   float* cbuf, void* scratch)
+{
+    const StepScratch q = step_scratch(p, s);
+    StepArgs a;
+    memset(&a, 0, sizeof(a));
+    a.T = p.T; a.B = p.B; a.H = s.hidden_size; a.ndir = s.num_directions;
+    a.bs = p.d_bs; a.off = p.d_off; a.slot_len = p.d_len; a.perm = p.d_perm;
+    a.ga = ga; a.cbuf = cbuf; a.peep = prm.peep;
+    a.rh = (const float*)((char*)scratch + q.rh);
+    a.dh_rec = (const float*)((char*)scratch + q.dh);
+    a.dcc = (float*)((char*)scratch + q.dcc);
+    return a;
+}
+
 lstm_status check_params(const lstm_layer_params* prm)
 {
     if (!prm || !prm->W || !prm->R || !prm->b || !prm->peep) return LSTM_ERR_INVALID_ARG;
@@ -312,33 +385,134 @@ lstm_status lstm_bwd(const lstm_plan* plan, const lstm_layer_shape* shape,
         if ((st = rec_launch(p, rc, a, true, cs)) != LSTM_OK) return st;
     }
 
+    return bwd_products(p, s, *params, x_packed, y_packed, ga, dx_packed, *grads, scratch, cs);
+}
+
+size_t lstm_stepwise_scratch_bytes(const lstm_plan* plan, const lstm_layer_shape* shape)
+{
+    if (!plan || check_shape(shape) != LSTM_OK) return 0;
+    return step_scratch(plan->p, *shape).total;
+}
+
+lstm_status lstm_fwd_stepwise(const lstm_plan* plan, const lstm_layer_shape* shape,
+                              const lstm_layer_params* params, const void* x_packed, float* y_packed,
+                              void* y_lo, float* h_n, float* c_n, void* workspace, void* scratch, void* stream)
+{
+    if (!plan) return LSTM_ERR_INVALID_ARG;
+    lstm_status st = check_shape(shape);
+    if (st != LSTM_OK) return st;
+    if ((st = check_params(params)) != LSTM_OK) return st;
+    const Plan& p = plan->p;
+    const lstm_layer_shape& s = *shape;
+    if (p.padded) return LSTM_ERR_UNSUPPORTED;
+    const int H = s.hidden_size, nd = s.num_directions;
+    const bool bf16 = s.dtype == LSTM_BF16;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if ((h_n && !aligned16(h_n)) || (c_n && !aligned16(c_n))) return LSTM_ERR_INVALID_ARG;
+    if (p.rows == 0) {
+        if (h_n) LSTM_CUDA_TRY(cudaMemsetAsync(h_n, 0, sizeof(float) * nd * p.B * H, cs));
+        if (c_n) LSTM_CUDA_TRY(cudaMemsetAsync(c_n, 0, sizeof(float) * nd * p.B * H, cs));
+        return LSTM_OK;
+    }
+    if (!x_packed || !y_packed || !workspace || !scratch) return LSTM_ERR_INVALID_ARG;
+    if (!aligned16(x_packed) || !aligned16(y_packed) || !aligned16(workspace) || !aligned16(scratch) ||
+        (y_lo && !aligned16(y_lo)))
+        return LSTM_ERR_INVALID_ARG;
+    const Layout L = workspace_layout(p, s);
+    float* ga = (float*)((char*)workspace + L.ga_off);
+    float* cbuf = (float*)((char*)workspace + L.c_off);
+    if ((st = input_projection(p, s, *params, x_packed, ga, cs)) != LSTM_OK) return st;
+    StepArgs a = step_args(p, s, *params, ga, cbuf, scratch);
+    a.y = y_packed; a.y_lo = (__nv_bfloat16*)y_lo; a.h_n = h_n; a.c_n = c_n;
+    const int ndH = nd * H;
+    const size_t esz = bf16 ? 2 : 4;
+    trace_begin(p, K_REC_FWD, cs);
+    int launches = 0;
+    for (int step = 0; step < p.T && st == LSTM_OK; ++step) {
+        for (int d = 0; d < nd && st == LSTM_OK; ++d) {
+            // R h_{t-1} of the step's rows that have a previous state (the first M rows)
+            const int t = d == 0 ? step : p.T - 1 - step;
+            const int M = d == 0 ? (t >= 1 ? p.h_bs[t] : 0) : (t + 1 < p.T ? p.h_bs[t + 1] : 0);
+            if (M == 0) continue;
+            const int prow0 = d == 0 ? p.h_off[t - 1] : p.h_off[t + 1];
+            GemmDesc g;
+            g.M = M; g.N = 4 * H; g.K = H;
+            g.A = y_packed + (size_t)prow0 * ndH + (size_t)d * H; g.sam = ndH; g.sak = 1;
+            g.B = (const char*)params->R + (size_t)d * 4 * H * H * esz; g.sbk = 1; g.sbn = H; g.b_bf16 = bf16;
+            g.C = const_cast<float*>(a.rh) + (size_t)d * p.B * 4 * H; g.ldc = 4 * H;
+            g.round_bf16 = bf16; g.k_splits = 1;
+            st = gemm_simt_run(g, p.num_sms, cs);
+            ++launches;
+        }
+        if (st == LSTM_OK) st = step_cell_launch(a, step, false, cs);
+        ++launches;
+    }
+    trace_end(p, K_REC_FWD, cs, launches);
+    return st;
+}
+
+lstm_status lstm_bwd_stepwise(const lstm_plan* plan, const lstm_layer_shape* shape,
+                              const lstm_layer_params* params, const void* x_packed, const float* y_packed,
+                              void* workspace, const float* dy_packed, float* dx_packed,
+                              const lstm_layer_grads* grads, void* scratch, void* stream)
+{
+    if (!plan) return LSTM_ERR_INVALID_ARG;
+    lstm_status st = check_shape(shape);
+    if (st != LSTM_OK) return st;
+    if ((st = check_params(params)) != LSTM_OK) return st;
+    if (!grads || !grads->dW || !grads->dR || !grads->db || !grads->dpeep) return LSTM_ERR_INVALID_ARG;
+    if (!aligned16(grads->dW) || !aligned16(grads->dR) || !aligned16(grads->db) || !aligned16(grads->dpeep))
+        return LSTM_ERR_INVALID_ARG;
+    const Plan& p = plan->p;
+    const lstm_layer_shape& s = *shape;
+    if (p.padded) return LSTM_ERR_UNSUPPORTED;
+    const int H = s.hidden_size, nd = s.num_directions, D = s.input_size;
+    const bool bf16 = s.dtype == LSTM_BF16;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (p.rows == 0) {
+        LSTM_CUDA_TRY(cudaMemsetAsync(grads->dW, 0, sizeof(float) * nd * 4 * H * D, cs));
+        LSTM_CUDA_TRY(cudaMemsetAsync(grads->dR, 0, sizeof(float) * nd * 4 * H * H, cs));
+        LSTM_CUDA_TRY(cudaMemsetAsync(grads->db, 0, sizeof(float) * nd * 4 * H, cs));
+        LSTM_CUDA_TRY(cudaMemsetAsync(grads->dpeep, 0, sizeof(float) * nd * 3 * H, cs));
+        return LSTM_OK;
+    }
+    if (!x_packed || !y_packed || !workspace || !dy_packed || !scratch) return LSTM_ERR_INVALID_ARG;
+    if (!aligned16(x_packed) || !aligned16(y_packed) || !aligned16(workspace) || !aligned16(dy_packed) ||
+        !aligned16(scratch) || (dx_packed && !aligned16(dx_packed)))
+        return LSTM_ERR_INVALID_ARG;
+    const Layout L = workspace_layout(p, s);
+    float* ga = (float*)((char*)workspace + L.ga_off);
+    float* cbuf = (float*)((char*)workspace + L.c_off);
+    StepArgs a = step_args(p, s, *params, ga, cbuf, scratch);
+    a.dy = dy_packed;
     const int nd4H = nd * 4 * H;
-    if (bf16 && p.gemm_engine == 0 && D % 8 == 0 && encode_ready())
-        return bwd_products_tc(p, s, *params, x_packed, y_packed, ga, dx_packed, *grads, scratch, cs);
-    GemmDesc gw, gr, gx;
-    bwd_gemm_shapes(p, s, &gw, &gr, &gx);
-    if (dx_packed) {
-        GemmDesc g = gx;
-        g.partial = (float*)scratch;
-        g.A = ga; g.sam = nd4H; g.sak = 1;
-        g.B = params->W; g.sbk = D; g.sbn = 1; g.b_bf16 = bf16;
-        g.C = dx_packed; g.ldc = D; g.round_bf16 = bf16;
-        if ((st = gemm_simt(g, p, K_GEMM_DX, cs)) != LSTM_OK) return st;
+    const size_t esz = bf16 ? 2 : 4;
+    trace_begin(p, K_REC_BWD, cs);
+    int launches = 0;
+    for (int step = 0; step < p.T && st == LSTM_OK; ++step) {
+        st = step_cell_launch(a, step, true, cs);
+        ++launches;
+        if (step + 1 == p.T) break;
+        for (int d = 0; d < nd && st == LSTM_OK; ++d) {
+            // R^T da of every row of the step, for the step after it in recurrence order
+            const int t = d == 0 ? p.T - 1 - step : step;
+            GemmDesc g;
+            g.M = p.h_bs[t]; g.N = H; g.K = 4 * H;
+            g.A = ga + (size_t)p.h_off[t] * nd4H + (size_t)d * 4 * H; g.sam = nd4H; g.sak = 1;
+            g.B = (const char*)params->R + (size_t)d * 4 * H * H * esz; g.sbk = H; g.sbn = 1; g.b_bf16 = bf16;
+            g.C = const_cast<float*>(a.dh_rec) + (size_t)d * p.B * H; g.ldc = H;
+            g.round_bf16 = bf16; g.k_splits = 1;
+            st = gemm_simt_run(g, p.num_sms, cs);
+            ++launches;
+        }
     }
-    gw.A = ga; gw.sam = 1; gw.sak = nd4H;
-    gw.B = x_packed; gw.sbk = D; gw.sbn = 1; gw.b_bf16 = bf16;
-    gw.C = grads->dW; gw.ldc = D; gw.round_bf16 = bf16; gw.partial = (float*)scratch;
-    if ((st = gemm_simt(gw, p, K_GEMM_DW, cs)) != LSTM_OK) return st;
-    for (int d = 0; d < nd; ++d) {
-        GemmDesc g = gr;
-        g.A = ga + (size_t)d * 4 * H; g.sam = 1; g.sak = nd4H;
-        g.B = y_packed + (size_t)d * H; g.sbk = nd * H; g.sbn = 1;
-        g.b_rows = d == 0 ? p.d_prev_fwd : p.d_prev_rev;
-        g.C = grads->dR + (size_t)d * 4 * H * H; g.ldc = H; g.round_bf16 = bf16;
-        g.partial = (float*)scratch;
-        if ((st = gemm_simt(g, p, K_GEMM_DR, cs)) != LSTM_OK) return st;
+    if (st == LSTM_OK) {
+        st = param_sums_launch(p, ga, cbuf, H, nd, grads->db, grads->dpeep, (float*)scratch, cs);
+        launches += 2;
     }
-    return LSTM_OK;
+    trace_end(p, K_REC_BWD, cs, launches);
+    if (st != LSTM_OK) return st;
+    return bwd_products(p, s, *params, x_packed, y_packed, ga, dx_packed, *grads, scratch, cs);
 }
 
 lstm_status lstm_debug_input_projection(const lstm_plan* plan, const lstm_layer_shape* shape,

@@ -72,4 +72,10 @@ lstm_status rec_cluster_bwd_launch(const Plan& p, const RecConfig& c, RecArgs a,
 // Floats of the backward kernel's partial-product exchange buffer.
 size_t rec_bwd_part_floats(const Plan& p, int H, int ndir, bool bf16, int forced_G);
 
+// db and dpeep of a layer from its gate errors (ga) and cell states, summed in
+// a fixed row-chunk order (bitwise repeatable); sum_scratch holds
+// rec_cluster_bwd_sum_floats(H, ndir) floats.
+lstm_status param_sums_launch(const Plan& p, const float* ga, const float* cbuf, int H, int ndir, float* db,
+                              float* dpeep, float* sum_scratch, cudaStream_t s);
+
 }  // namespace lstm

@@ -1186,19 +1186,23 @@ lstm_status rec_cluster_bwd_launch(const Plan& p, const RecConfig& c, RecArgs a,
     lstm_status st = cluster_launch(c, fn, a, s);
     int launched = st == LSTM_OK ? 1 : 0;
     if (st == LSTM_OK) {
-        const int ncols = a.ndir * 7 * a.H;
-        const int rows = (int)p.rows;
-        const int chunk = (rows + kSumChunks - 1) / kSumChunks;
-        lstm_param_sums_kernel<<<dim3((ncols + 255) / 256, kSumChunks), 256, 0, s>>>(
-            a.ga, a.cbuf, p.d_prev_fwd, p.d_prev_rev, rows, a.H, a.ndir, chunk, sum_scratch);
-        lstm_param_sums_combine<<<(ncols + 255) / 256, 256, 0, s>>>(sum_scratch, kSumChunks, a.H, a.ndir, a.db,
-                                                                    a.dpeep);
-        const cudaError_t e = cudaGetLastError();
-        if (e == cudaSuccess) launched += 2;
-        else st = LSTM_ERR_UNSUPPORTED;
+        st = param_sums_launch(p, a.ga, a.cbuf, a.H, a.ndir, a.db, a.dpeep, sum_scratch, s);
+        if (st == LSTM_OK) launched += 2;
     }
     trace_end(p, K_REC_BWD, s, launched);
     return st;
+}
+
+lstm_status param_sums_launch(const Plan& p, const float* ga, const float* cbuf, int H, int ndir, float* db,
+                              float* dpeep, float* sum_scratch, cudaStream_t s)
+{
+    const int ncols = ndir * 7 * H;
+    const int rows = (int)p.rows;
+    const int chunk = (rows + kSumChunks - 1) / kSumChunks;
+    lstm_param_sums_kernel<<<dim3((ncols + 255) / 256, kSumChunks), 256, 0, s>>>(
+        ga, cbuf, p.d_prev_fwd, p.d_prev_rev, rows, H, ndir, chunk, sum_scratch);
+    lstm_param_sums_combine<<<(ncols + 255) / 256, 256, 0, s>>>(sum_scratch, kSumChunks, H, ndir, db, dpeep);
+    return cudaGetLastError() == cudaSuccess ? LSTM_OK : LSTM_ERR_UNSUPPORTED;
 }
 
 }  // namespace lstm

@@ -1,0 +1,113 @@
+// stepwise.cu -- the per-step-launch recurrence (comparator path).
+//
+// The design the pages describe for their own GPU LSTM ("RETURNN", Sec. 4.2:
+// one matrix product for the non-recurrent part, then per time step a product
+// with the recurrent weights and a small kernel for the gating): here each
+// step of each direction is one SIMT product launch (R·h_{t-1} over the
+// step's active rows) and each step one cell launch for both directions.
+// It computes the same cell as the persistent kernels and exists to measure
+// what the persistent, on-chip design saves.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "stepwise.cuh"
+
+namespace lstm {
+
+namespace {
+
+__device__ __forceinline__ float sigm(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+}  // namespace
+
+// One thread per (row j, unit u) of one direction (blockIdx.y) at step s.
+__global__ void step_cell_fwd_kernel(StepArgs a, int s)
+{
+    const int dir = blockIdx.y, H = a.H, T = a.T;
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    const int j = idx / H, u = idx - j * H;
+    const int ndH = a.ndir * H, nd4H = a.ndir * 4 * H;
+    if (s == 0 && j < a.B && a.slot_len[j] == 0 && a.h_n) {      // empty sequences end in the zero state
+        const size_t o = ((size_t)dir * a.B + a.perm[j]) * H + u;
+        a.h_n[o] = 0.f;
+        if (a.c_n) a.c_n[o] = 0.f;
+    }
+    const int t = dir == 0 ? s : T - 1 - s;
+    const int n = a.bs[t];
+    if (j >= n) return;
+    const int row = a.off[t] + j;
+    const bool has_prev = dir == 0 ? t >= 1 : (t + 1 < T && j < a.bs[t + 1]);
+    const int prow = has_prev ? (dir == 0 ? a.off[t - 1] + j : a.off[t + 1] + j) : 0;
+    const float* pre = a.ga + (size_t)row * nd4H + (size_t)dir * 4 * H + u;
+    const float* rh = a.rh + ((size_t)dir * a.B + j) * 4 * H + u;
+    float av[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) av[g] = pre[g * H] + (has_prev ? rh[g * H] : 0.f);
+    const float cp = has_prev ? a.cbuf[(size_t)prow * ndH + dir * H + u] : 0.f;
+    const float* pp = a.peep + (size_t)dir * 3 * H + u;
+    const float ig = sigm(av[0] + pp[0] * cp);
+    const float fg = sigm(av[1] + pp[H] * cp);
+    const float zg = tanhf(av[2]);
+    const float c = fg * cp + ig * zg;
+    const float og = sigm(av[3] + pp[2 * H] * c);
+    const float h = og * tanhf(c);
+    float* gw = a.ga + (size_t)row * nd4H + (size_t)dir * 4 * H + u;
+    gw[0] = ig; gw[H] = fg; gw[2 * H] = zg; gw[3 * H] = og;
+    const size_t yo = (size_t)row * ndH + dir * H + u;
+    a.cbuf[yo] = c;
+    a.y[yo] = h;
+    if (a.y_lo) a.y_lo[yo] = __float2bfloat16_rn(h);
+    const int len = a.slot_len[j];
+    if (a.h_n && ((dir == 0 && t == len - 1) || (dir == 1 && t == 0))) {
+        const size_t o = ((size_t)dir * a.B + a.perm[j]) * H + u;
+        a.h_n[o] = h;
+        if (a.c_n) a.c_n[o] = c;
+    }
+}
+
+// BPTT of one step: gate errors of the step's rows from dy, the recurrent
+// error R^T da of the step after it (in recurrence order) and the cell-state
+// error carried from there.
+__global__ void step_cell_bwd_kernel(StepArgs a, int s)
+{
+    const int dir = blockIdx.y, H = a.H, T = a.T;
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    const int j = idx / H, u = idx - j * H;
+    const int ndH = a.ndir * H, nd4H = a.ndir * 4 * H;
+    const int t = dir == 0 ? T - 1 - s : s;
+    const int n = a.bs[t];
+    if (j >= n) return;
+    const int row = a.off[t] + j;
+    // the step after t in recurrence order, and the step before it (c_{t-1} of the peepholes)
+    const bool has_next = dir == 0 ? (t + 1 < T && j < a.bs[t + 1]) : t >= 1;
+    const bool has_prev = dir == 0 ? t >= 1 : (t + 1 < T && j < a.bs[t + 1]);
+    const int prow = has_prev ? (dir == 0 ? a.off[t - 1] + j : a.off[t + 1] + j) : 0;
+    float* gw = a.ga + (size_t)row * nd4H + (size_t)dir * 4 * H + u;
+    const float ig = gw[0], fg = gw[H], zg = gw[2 * H], og = gw[3 * H];
+    const size_t yo = (size_t)row * ndH + dir * H + u;
+    const float c = a.cbuf[yo];
+    const float cp = has_prev ? a.cbuf[(size_t)prow * ndH + dir * H + u] : 0.f;
+    const size_t so = ((size_t)dir * a.B + j) * H + u;
+    const float dh = a.dy[yo] + (has_next ? a.dh_rec[so] : 0.f);
+    const float carry = has_next ? a.dcc[so] : 0.f;
+    const float* pp = a.peep + (size_t)dir * 3 * H + u;
+    const float tc = tanhf(c);
+    const float dao = dh * tc * og * (1.f - og);
+    const float dc = dh * og * (1.f - tc * tc) + dao * pp[2 * H] + carry;
+    const float dai = dc * zg * ig * (1.f - ig);
+    const float daf = dc * cp * fg * (1.f - fg);
+    const float daz = dc * ig * (1.f - zg * zg);
+    gw[0] = dai; gw[H] = daf; gw[2 * H] = daz; gw[3 * H] = dao;
+    a.dcc[so] = dc * fg + dai * pp[0] + daf * pp[H];
+}
+
+lstm_status step_cell_launch(const StepArgs& a, int s, bool backward, cudaStream_t st)
+{
+    const int threads = 256;
+    const dim3 grid((unsigned)ceil_div(a.B * a.H, threads), (unsigned)a.ndir);
+    if (backward) step_cell_bwd_kernel<<<grid, threads, 0, st>>>(a, s);
+    else step_cell_fwd_kernel<<<grid, threads, 0, st>>>(a, s);
+    return cudaGetLastError() == cudaSuccess ? LSTM_OK : LSTM_ERR_CUDA;
+}
+
+}  // namespace lstm

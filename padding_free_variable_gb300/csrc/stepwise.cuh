@@ -1,0 +1,32 @@
+// stepwise.cuh -- per-step cell kernels of the per-step-launch comparator path.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace lstm {
+
+struct StepArgs {
+    int T, B, H, ndir;
+    const int32_t* bs;        // [T] active rows per step
+    const int32_t* off;       // [T+1] first row of each step
+    const int32_t* slot_len;  // [B]
+    const int32_t* perm;      // [B]
+    float* ga;                // [rows][ndir*4H] pre-activations -> gates -> gate errors
+    const float* rh;          // forward: [ndir][B][4H] the step's R h_{t-1}
+    const float* peep;        // [ndir][3][H]
+    float* y;                 // [rows][ndir*H]
+    __nv_bfloat16* y_lo;      // optional bf16 copy of y
+    float* cbuf;              // [rows][ndir*H]
+    float* h_n;               // [ndir][B][H] caller order, optional
+    float* c_n;
+    const float* dy;          // backward: [rows][ndir*H]
+    const float* dh_rec;      // backward: [ndir][B][H] R^T da of the step after (recurrence order)
+    float* dcc;               // backward: [ndir][B][H] cell-state error carry
+};
+
+// Cell of step s (forward, or BPTT in backward order) for both directions.
+lstm_status step_cell_launch(const StepArgs& a, int s, bool backward, cudaStream_t st);
+
+}  // namespace lstm

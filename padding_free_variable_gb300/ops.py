@@ -167,6 +167,27 @@ def layer_backward(plan: Plan, shape: LayerShape, layer: dict, x_packed, y_packe
           "lstm_bwd")
 
 
+def stepwise_scratch_bytes(plan: Plan, shape: LayerShape) -> int:
+    return int(_lib.load().lstm_stepwise_scratch_bytes(plan.handle, ctypes.byref(shape)))
+
+
+def layer_forward_stepwise(plan: Plan, shape: LayerShape, layer: dict, x_packed, y_packed, y_lo, h_n, c_n,
+                           workspace, scratch, stream=None):
+    check(_lib.load().lstm_fwd_stepwise(plan.handle, ctypes.byref(shape), ctypes.byref(_params(layer)),
+                                        _ptr(x_packed), _ptr(y_packed), _ptr(y_lo), _ptr(h_n), _ptr(c_n),
+                                        _ptr(workspace), _ptr(scratch), _stream(stream)), "lstm_fwd_stepwise")
+
+
+def layer_backward_stepwise(plan: Plan, shape: LayerShape, layer: dict, x_packed, y_packed, workspace,
+                            dy_packed, dx_packed, grads: dict, scratch, stream=None):
+    g = LayerGrads(grads["W"].data_ptr(), grads["R"].data_ptr(), grads["b"].data_ptr(),
+                   grads["peep"].data_ptr())
+    check(_lib.load().lstm_bwd_stepwise(plan.handle, ctypes.byref(shape), ctypes.byref(_params(layer)),
+                                        _ptr(x_packed), _ptr(y_packed), _ptr(workspace), _ptr(dy_packed),
+                                        _ptr(dx_packed), ctypes.byref(g), _ptr(scratch), _stream(stream)),
+          "lstm_bwd_stepwise")
+
+
 class PackedLSTMStack:
     """A stack of (bi)LSTM layers run through the C ABI on one packed batch.
 
@@ -174,11 +195,13 @@ class PackedLSTMStack:
     ``bf16``), b and peep (fp32) in the header's layout.  Buffers for every
     layer's activations, workspace and gradients are allocated once, so
     ``forward``/``backward`` allocate nothing and may be replayed.
+    ``stepwise=True`` runs the per-step-launch comparator path instead of the
+    persistent recurrent kernels.
     """
 
     def __init__(self, plan: Plan, layers: list, input_size: int, hidden_size: int,
-                 num_directions: int, bf16: bool, device="cuda"):
-        self.plan, self.layers = plan, layers
+                 num_directions: int, bf16: bool, device="cuda", stepwise: bool = False):
+        self.plan, self.layers, self.stepwise = plan, layers, bool(stepwise)
         self.D0, self.H, self.nd, self.bf16 = int(input_size), int(hidden_size), int(num_directions), bool(bf16)
         dev = torch.device(device)
         rows, H, nd = plan.rows, self.H, self.nd
@@ -193,8 +216,8 @@ class PackedLSTMStack:
         self.c_n = torch.empty_like(self.h_n)
         self.ws = [torch.empty(max(1, workspace_bytes(plan, s)), dtype=torch.uint8, device=dev)
                    for s in self.shapes]
-        self.scratch = torch.empty(max(scratch_bytes(plan, s) for s in self.shapes), dtype=torch.uint8,
-                                   device=dev)
+        need = max((stepwise_scratch_bytes if self.stepwise else scratch_bytes)(plan, s) for s in self.shapes)
+        self.scratch = torch.empty(max(1, need), dtype=torch.uint8, device=dev)
         self.dy_packed = torch.empty((rows, nd * H), dtype=torch.float32, device=dev)
         self.dx = [torch.empty((rows, s.input_size), dtype=torch.float32, device=dev) for s in self.shapes]
         self.grads = [{"W": torch.empty(tuple(lay["W"].shape), dtype=torch.float32, device=dev),
@@ -208,15 +231,20 @@ class PackedLSTMStack:
 
     def forward_packed(self, stream=None):
         for l, lay in enumerate(self.layers):
-            layer_forward(self.plan, self.shapes[l], lay, self.layer_input(l), self.y[l], self.y_lo[l],
-                          self.h_n[l], self.c_n[l], self.ws[l], stream)
+            if self.stepwise:
+                layer_forward_stepwise(self.plan, self.shapes[l], lay, self.layer_input(l), self.y[l],
+                                       self.y_lo[l], self.h_n[l], self.c_n[l], self.ws[l], self.scratch, stream)
+            else:
+                layer_forward(self.plan, self.shapes[l], lay, self.layer_input(l), self.y[l], self.y_lo[l],
+                              self.h_n[l], self.c_n[l], self.ws[l], stream)
         return self.y[-1]
 
     def backward_packed(self, stream=None):
         dy = self.dy_packed
+        back = layer_backward_stepwise if self.stepwise else layer_backward
         for l in range(len(self.layers) - 1, -1, -1):
-            layer_backward(self.plan, self.shapes[l], self.layers[l], self.layer_input(l), self.y[l],
-                           self.ws[l], dy, self.dx[l], self.grads[l], self.scratch, stream)
+            back(self.plan, self.shapes[l], self.layers[l], self.layer_input(l), self.y[l],
+                 self.ws[l], dy, self.dx[l], self.grads[l], self.scratch, stream)
             dy = self.dx[l]
         return self.dx[0]
 

@@ -72,7 +72,7 @@ def device_layers(w, device="cuda"):
     return out
 
 
-def run_gpu(w, padded: bool = False, device="cuda", ctas: int = 0, engine: int = 0):
+def run_gpu(w, padded: bool = False, device="cuda", ctas: int = 0, engine: int = 0, stepwise: bool = False):
     """pack -> all layers forward -> all layers backward -> unpack, through the C ABI."""
     import torch
     from padding_free_variable_gb300 import ops
@@ -83,7 +83,7 @@ def run_gpu(w, padded: bool = False, device="cuda", ctas: int = 0, engine: int =
     if engine:
         plan.set_gemm_engine(engine)
     stack = ops.PackedLSTMStack(plan, device_layers(w, device), w.spec.input_size, w.spec.hidden_size,
-                                w.spec.num_directions, bf16, device)
+                                w.spec.num_directions, bf16, device, stepwise=stepwise)
     x = torch.from_numpy(w.x).to(device=device, dtype=torch.bfloat16 if bf16 else torch.float32)
     G = torch.from_numpy(w.G).to(device)
     y_cat, dx_cat = stack.step(x, G)

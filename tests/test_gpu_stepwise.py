@@ -1,0 +1,45 @@
+"""The per-step-launch comparator path (one product launch per direction and
+one cell launch per time step, the RETURNN paper's Sec. 4.2 design) against
+the oracle, on the same seeded inputs and tolerances as the persistent path."""
+import numpy as np
+import pytest
+
+from padding_free_variable_gb300 import synthetic
+from gpu_harness import TOL_BF16, TOL_F32, compare_all, run_gpu, run_oracle
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _needs_cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from padding_free_variable_gb300 import build
+    build.build()
+
+
+CASES = [
+    # ndir, layers, D, H, lengths, dtype
+    (1, 1, 8, 32, [1], "f32"),
+    (1, 2, 8, 48, [5, 40, 39, 1, 2, 3, 4, 30], "f32"),
+    (2, 1, 16, 64, [9, 0, 4, 13, 13, 2, 7], "f32"),
+    (2, 2, 24, 136, [17, 2, 9, 33, 1, 0, 12, 33], "f32"),
+    (2, 2, 16, 64, [9, 0, 4, 21, 21, 2], "bf16"),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"nd{c[0]}-L{c[1]}-H{c[3]}-{c[5]}" for c in CASES])
+def test_stepwise_matches_oracle(case):
+    nd, nl, D, H, lengths, dtype = case
+    w = synthetic.custom(nd, nl, D, H, lengths, seed=11 + H, dtype=dtype,
+                         weight_range=0.1 if dtype == "bf16" else 0.3)
+    gpu = run_gpu(w, stepwise=True)
+    compare_all(gpu, run_oracle(w), TOL_BF16 if dtype == "bf16" else TOL_F32, label=f"stepwise {case}")
+
+
+@pytest.mark.parametrize("wid", [1, 2])
+def test_stepwise_full_workload(wid):
+    w = synthetic.workload(wid)
+    gpu = run_gpu(w, stepwise=True)
+    compare_all(gpu, run_oracle(w), TOL_F32, label=f"stepwise workload {wid}")
