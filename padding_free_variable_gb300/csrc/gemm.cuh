@@ -1,6 +1,8 @@
 // gemm.cuh -- launch interface of the library's matrix products.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace lstm {
@@ -49,6 +51,13 @@ lstm_status gemm_tc_bf16(const Plan& p, int kind, const void* A, int64_t lda, co
 lstm_status transpose_to_bf16(const Plan& p, const void* src, bool src_bf16, int64_t lds, int col0,
                               const int32_t* map, int rows, int cols, void* dstT, int64_t ldt, void* dst_rm,
                               int64_t ldm, cudaStream_t s);
+
+// TMA map of a row-major fp32 matrix [rows][cols] (row pitch ld elements) in
+// boxes of box_cols x box_rows without swizzle; out-of-range elements read 0.
+// False when the driver entry point is missing or the layout is not
+// TMA-addressable (16-byte aligned base, pitch and box row).
+bool make_map_f32(CUtensorMap* map, const float* ptr, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                  int box_rows);
 
 // C = sum over splits (in split order) of partial, + bias.
 cudaError_t splitk_reduce(const float* partial, int splits, int M, int N, float* C, int64_t ldc,

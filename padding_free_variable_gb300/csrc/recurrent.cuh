@@ -32,6 +32,7 @@ struct RecArgs {
     int tables_in_smem;
     int mma_mw, mma_kw;       // forward tensor-core product: warps along rows and along k
     int tm_chains, tm_acol;   // cluster kernels: TMEM accumulator chains, first column of the R operand
+    int tma_pre;              // cluster forward kernel: gate pre-activations arrive by TMA (tile at off_red)
     // dynamic shared-memory layout (byte offsets)
     int off_h, off_red, off_acc, off_state, off_contrib, off_sums, off_tab, off_peep;
 };
@@ -47,6 +48,7 @@ struct RecConfig {
     int chains = 0;     // cluster kernels: accumulator chains (issuing warps per M tile)
     int acol = 0;       // cluster kernels: TMEM column of the R operand
     int bulk = 0;       // cluster forward kernel: 1 = bulk-copy exchange into a double-buffered operand
+    int tma_pre = 0;    // cluster forward kernel: 1 = pre-activation tiles loaded by TMA
     size_t smem = 0;    // dynamic shared memory bytes
 };
 

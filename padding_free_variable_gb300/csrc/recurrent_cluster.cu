@@ -29,8 +29,10 @@
 #include <cooperative_groups.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "common.cuh"
+#include "gemm.cuh"
 #include "recurrent.cuh"
 #include "tc_ptx.cuh"
 
@@ -319,8 +321,14 @@ __device__ __forceinline__ void issue_chains(int nch, uint32_t d, uint32_t a_hi,
 //  * otherwise (the double buffer does not fit): one operand buffer, written
 //    by the peers with plain DSMEM stores between two halves of a split
 //    cluster barrier.
+//
+// With a.tma_pre the gate pre-activations of a step (4 gates x NBM rows x this
+// CTA's 32 units, fp32) arrive in shared memory by four TMA tile loads, issued
+// by one thread right after the previous step's cell has read the tile: the
+// product's window stays free of the 256 threads' global loads (measured to
+// delay the MMAs' completion by ~0.8 us).
 template <bool SPLIT, bool BULK>
-__global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
+__global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a, const __grid_constant__ CUtensorMap pre_map)
 {
     extern __shared__ unsigned char smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -341,6 +349,9 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 1);
     int* s_fail = reinterpret_cast<int*>(tmem_slot + 1);
     uint64_t* full_bar = mma_bar + 2;                                // BULK: [2] operand arrival per parity
+    uint64_t* pre_bar = mma_bar + 4;                                 // tma_pre: arrival of a step's tile
+    float* pre_tile = reinterpret_cast<float*>(base + a.off_red);    // tma_pre: [4 gates][NBM][32]
+    const bool tma_pre = a.tma_pre != 0;
     float* peep_s = reinterpret_cast<float*>(base + a.off_peep);     // [3][32]
     int* s_bs = reinterpret_cast<int*>(base + a.off_tab);
     int* s_off = s_bs + T;
@@ -379,6 +390,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
             tc::mbar_init(&full_bar[0], 1);
             tc::mbar_init(&full_bar[1], 1);
         }
+        if (tma_pre) tc::mbar_init(pre_bar, 1);
         tc::fence_mbar_init();
         // the operand of step 1 (parity 1) is armed before the cluster barrier below,
         // i.e. before any peer can send
@@ -435,12 +447,24 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
     tc::tc_fence_before_sync();
     __syncthreads();
     tc::tc_fence_after_sync();
+    // tma_pre: the four gate tiles of step s2 (rows from off[t2], NBM of them; rows past the
+    // packed rows read 0), one thread, completing on pre_bar
+    auto issue_pre = [&](int s2, bool fence) {
+        const int t2 = dir == 0 ? s2 : T - 1 - s2;
+        if (fence) fence_proxy_async_cta();
+        tc::mbar_arrive_expect_tx(pre_bar, (uint32_t)(4 * NBM * kCU * 4));
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+            tc::tma_load_2d(pre_tile + (size_t)g * NBM * kCU, &pre_map, pre_bar, dir * 4 * H + g * H + u0, s_off[t2]);
+    };
+    if (tma_pre && threadIdx.x == 0) issue_pre(0, true);
     cl.sync();     // every CTA of the cluster is resident before any remote write
 
     const int jq = threadIdx.x >> 3, q8 = threadIdx.x & 7;          // cell item: row jq (+32k), units q8*4..+4
     const int nks = (H + 15) / 16;                                   // MMA k-steps
     const uint32_t bstep = (uint32_t)(NBM * (BULK ? 64 : 128)) >> 4;  // descriptor units between B blocks
     bool failed = false;                  // CTA-uniform: an MMA completion wait timed out
+    bool pre_ok_prev = true;              // this thread's wait for the previous step's tile
     for (int s = 0; s < T; ++s) {
         const int t = dir == 0 ? s : T - 1 - s;
         const int n = s_bs[t];
@@ -448,7 +472,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
         const int n_prev = dir == 0 ? (t >= 1 ? n : 0) : (t + 1 < T ? s_bs[t + 1] : 0);
         const int NBs = (n + 15) & ~15;
         const int par = BULK ? (s & 1) : 0;
-        bool arrived = true;
+        bool arrived = true;          // this step's operand (and the previous step's tile) arrived
         if (BULK) {
             cstamp(a, false, dir, rank, s, 0, 0);
             // h_{t-1} of every peer has arrived in this step's operand
@@ -457,6 +481,8 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
         } else {
             if (s > 0) {
                 cluster_wait();    // h_{t-1} of every peer is in this CTA's operand
+                // every thread of this CTA arrived after its cell: the tile is free
+                if (tma_pre && threadIdx.x == 0) issue_pre(s, true);
                 cstamp(a, false, dir, rank, s - 1, 4, 4);
             }
             cstamp(a, false, dir, rank, s, 0, 0);
@@ -479,12 +505,13 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
         }
         if (warp < nch) __syncwarp();     // the issuing lane's warp does not poll while it issues
         cstamp(a, false, dir, rank, s, 6, 6);
-        // meanwhile: the cell items' own operands (gate pre-activations), rows jq and jq + 32
+        // meanwhile (without tma_pre): the cell items' own operands (gate pre-activations),
+        // rows jq and jq + 32
         float pre[2][4][4];
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
             const int j = jq + it * 32;
-            if (j < n) {
+            if (!tma_pre && j < n) {
                 const float* gr = a.ga + (size_t)(rowbase + j) * nd4H + dir * 4 * H + u0 + q8 * 4;
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
@@ -493,7 +520,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
                 }
             }
         }
-        if (s + 1 < T) {   // next step's own rows into L2 (4 gate blocks of this CTA's units)
+        if (!tma_pre && s + 1 < T) {   // next step's own rows into L2 (4 gate blocks of this CTA's units)
             const int t2 = dir == 0 ? s + 1 : T - 2 - s;
             for (int g = 0; g < 4; ++g)
                 prefetch_rows(a.ga, nd4H, s_off[t2], s_bs[t2], dir * 4 * H + g * H + u0);
@@ -505,6 +532,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
         // flight before freeing tensor memory.  The read-out of the failing step itself may see
         // partial sums; the status word marks the results as invalid.
         const bool ok = failed ? true : tc::mbar_wait(mma_bar, (uint32_t)(s & 1), a.wait_limit_ns);
+        arrived = arrived && pre_ok_prev;
         if ((!ok || !arrived) && !failed) {
             record_failure(a.status, LSTM_ERR_TIMEOUT, (ok ? 0x60000u : 0x40000u) | (unsigned)s);
             *s_fail = 1 + s;
@@ -529,9 +557,15 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
         if (BULK && threadIdx.x == 0 && !failed && s + 2 < T)
             tc::mbar_arrive_expect_tx(&full_bar[par], step_bytes(s + 2));
         cstamp(a, false, dir, rank, s, 2, 2);
-        // cell: row j, units u0 + q8*4 .. +4; h_t kept (split) for the exchange.  The global
-        // outputs of rows jq and jq + 32 are written after the exchange's barrier arrival, so
-        // that the arrival (a release) does not wait for them
+        // cell: row j, units u0 + q8*4 .. +4; h_t kept (split) for the exchange.  Without the bulk
+        // exchange the global outputs of rows jq and jq + 32 are written after the exchange's
+        // barrier arrival, so that the arrival (a release) does not wait for them
+        bool pre_ok = true;
+        if (tma_pre) pre_ok = tc::mbar_wait(pre_bar, (uint32_t)(s & 1), a.wait_limit_ns);
+        if (!pre_ok && !failed) {
+            record_failure(a.status, LSTM_ERR_TIMEOUT, 0x70000u | (unsigned)s);
+            *s_fail = 1 + s;
+        }
         uint2 xh[4], xl[4];
         float og_[2][4][4], oc_[2][4], oh_[2][4];
         auto store_outputs = [&](int j, const float (&gg)[4][4], const float (&cv)[4], const float (&hv)[4],
@@ -561,7 +595,13 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
             if (j >= n) continue;
             const int len = s_len[j];
             float pv[4][4];
-            if (it < 2) {
+            if (tma_pre) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const float4 x = *reinterpret_cast<const float4*>(pre_tile + ((size_t)g * NBM + j) * kCU + q8 * 4);
+                    pv[g][0] = x.x; pv[g][1] = x.y; pv[g][2] = x.z; pv[g][3] = x.w;
+                }
+            } else if (it < 2) {
 #pragma unroll
                 for (int g = 0; g < 4; ++g)
 #pragma unroll
@@ -591,7 +631,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
                 cst[j * kCU + uu] = c;
             }
             split4(hv, xh[it], xl[it], SPLIT);
-            if (it < 2) {
+            if (!BULK && it < 2) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
 #pragma unroll
@@ -619,16 +659,24 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
             }
             fence_proxy_async_cta();
             __syncthreads();
-            if (s + 1 < T && threadIdx.x < G && !failed) {
-                const uint32_t p2 = (uint32_t)threadIdx.x, nxt = (uint32_t)(par ^ 1);
+            // lane 0 of warp w sends to peers w, w + 8 (copies issued by one warp's lanes serialise)
+            const bool sender = lane == 0 && warp < G;
+            if (s + 1 < T && sender && !failed) {
+                const uint32_t nxt = (uint32_t)(par ^ 1);
                 const uint32_t bytes = (uint32_t)NBs * 64u;
-                const uint32_t bar = mapa_u32(tc::smem_u32(&full_bar[nxt]), p2);
-                bulk_to_peer(mapa_u32(tc::smem_u32(Bop(nxt, 0) + (size_t)rank * NBM * 64), p2), Stg(par, 0), bytes, bar);
-                if (SPLIT)
-                    bulk_to_peer(mapa_u32(tc::smem_u32(Bop(nxt, 1) + (size_t)rank * NBM * 64), p2), Stg(par, 1), bytes, bar);
+                for (int p2 = warp; p2 < G; p2 += kCT / 32) {
+                    const uint32_t bar = mapa_u32(tc::smem_u32(&full_bar[nxt]), (uint32_t)p2);
+                    bulk_to_peer(mapa_u32(tc::smem_u32(Bop(nxt, 0) + (size_t)rank * NBM * 64), (uint32_t)p2), Stg(par, 0),
+                                 bytes, bar);
+                    if (SPLIT)
+                        bulk_to_peer(mapa_u32(tc::smem_u32(Bop(nxt, 1) + (size_t)rank * NBM * 64), (uint32_t)p2),
+                                     Stg(par, 1), bytes, bar);
+                }
                 bulk_commit();
-                bulk_wait_read_all_but_one();    // the copies of step s - 1 have read their staging
             }
+            cstamp(a, false, dir, rank, s, 4, 4);
+            if (tma_pre && threadIdx.x == 0 && s + 1 < T) issue_pre(s + 1, false);   // the tile has been read
+            if (s + 1 < T && sender && !failed) bulk_wait_read_all_but_one();   // step s - 1's staging
         } else {
             cluster_wait();        // every peer's product of this step is done with its operand
             // h_t into every peer's operand of the next step (row j, columns u0 + q8*4 ..)
@@ -647,13 +695,18 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a)
             fence_proxy_async_cluster();
             cluster_arrive();      // release: this CTA's h_t is in every peer's operand
         }
+        if (!BULK) {
 #pragma unroll
-        for (int it = 0; it < 2; ++it)
-            if (jq + it * 32 < n) store_outputs(jq + it * 32, og_[it], oc_[it], oh_[it], xh[it]);
+            for (int it = 0; it < 2; ++it)
+                if (jq + it * 32 < n) store_outputs(jq + it * 32, og_[it], oc_[it], oh_[it], xh[it]);
+        }
+        pre_ok_prev = pre_ok;
         cstamp(a, false, dir, rank, s, 3, 3);
     }
+    // the last tile was waited for at its step; wait again (bounded) in case that wait ran out
+    if (tma_pre && threadIdx.x == 0) tc::mbar_wait(pre_bar, (uint32_t)((T - 1) & 1), kTeardownWaitNs);
     if (BULK) {
-        if (threadIdx.x < G) bulk_wait_all();   // no copy of this CTA is still in flight
+        if (lane == 0 && warp < G) bulk_wait_all();   // no copy of this CTA is still in flight
         cl.sync();                              // nor one into it: every CTA has passed its last wait
     } else {
         cluster_wait();            // the last step's arrival
@@ -1077,12 +1130,16 @@ bool rec_cluster_fwd_configure(const Plan& p, int H, int ndir, bool bf16, RecCon
     while (nch > 1 && (nch > nks || nch * NBM + acols > 512)) nch >>= 1;
     if (nch * NBM + acols > 512) return false;
     const uint32_t cols = pow2_cols(nch * NBM + acols);
-    // bulk exchange first (double-buffered operand + staging), else the single-buffered one
-    for (int bulk = 1; bulk >= 0; --bulk) {
+    // preference: TMA pre-activation tiles, then the bulk exchange (double-buffered operand +
+    // staging); the single-buffered exchange without tiles needs the least shared memory
+    const int order[4][2] = {{1, 1}, {0, 1}, {1, 0}, {0, 0}};
+    for (int oi = 0; oi < 4; ++oi) {
+        const int bulk = order[oi][0], pre = order[oi][1];
         const size_t bbytes = bulk ? 2 * (split ? 2 : 1) * (size_t)G * NBM * 64 : (split ? 2 : 1) * (size_t)KB * NBM * 128;
         size_t off = 0;
         const size_t o_b = off; off = al(off + bbytes, 1024);
         const size_t o_stage = off; if (bulk) off = al(off + 4 * (size_t)NBM * 64, 1024);
+        const size_t o_pre = off; if (pre) off = al(off + 4 * (size_t)NBM * kCU * 4, 1024);
         const size_t o_acc = off; off = al(off + (size_t)NBM * kCM * 4, 16);
         const size_t o_cst = off; off = al(off + (size_t)p.B * kCU * 4, 16);
         const size_t o_bar = off; off = al(off + 64, 16);
@@ -1094,9 +1151,9 @@ bool rec_cluster_fwd_configure(const Plan& p, int H, int ndir, bool bf16, RecCon
         if (!cluster_schedulable(p, fwd_kernel(bf16, bulk != 0), G, smem)) continue;
         RecConfig c;
         c.G = G; c.Umax = (int)cols; c.JC = NBM; c.smem = smem; c.cluster = 1;
-        c.chains = nch; c.acol = (int)cols - acols; c.bulk = bulk;
+        c.chains = nch; c.acol = (int)cols - acols; c.bulk = bulk; c.tma_pre = pre;
         *out = c;
-        lay->off_contrib = (int)o_b; lay->off_h = (int)o_stage; lay->off_acc = (int)o_acc;
+        lay->off_contrib = (int)o_b; lay->off_h = (int)o_stage; lay->off_red = (int)o_pre; lay->off_acc = (int)o_acc;
         lay->off_state = (int)o_cst; lay->off_sums = (int)o_bar; lay->off_peep = (int)o_peep;
         lay->off_tab = (int)o_tab;
         return true;
@@ -1104,7 +1161,7 @@ bool rec_cluster_fwd_configure(const Plan& p, int H, int ndir, bool bf16, RecCon
     return false;
 }
 
-static lstm_status cluster_launch(const RecConfig& c, const void* fn, RecArgs& a, cudaStream_t s)
+static lstm_status cluster_launch(const RecConfig& c, const void* fn, void** args, int ndir, cudaStream_t s)
 {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem) != cudaSuccess)
         return LSTM_ERR_CUDA;
@@ -1112,7 +1169,7 @@ static lstm_status cluster_launch(const RecConfig& c, const void* fn, RecArgs& a
         return LSTM_ERR_UNSUPPORTED;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    cfg.gridDim = dim3(c.G * a.ndir);
+    cfg.gridDim = dim3(c.G * ndir);
     cfg.blockDim = dim3(kCT);
     cfg.dynamicSmemBytes = c.smem;
     cfg.stream = s;
@@ -1122,7 +1179,6 @@ static lstm_status cluster_launch(const RecConfig& c, const void* fn, RecArgs& a
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    void* args[] = {&a};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
     if (e != cudaSuccess) { cudaGetLastError(); return LSTM_ERR_UNSUPPORTED; }
     return LSTM_OK;
@@ -1133,8 +1189,14 @@ lstm_status rec_cluster_fwd_launch(const Plan& p, const RecConfig& c, RecArgs a,
     a.G = c.G; a.Umax = c.Umax; a.JC = c.JC; a.tm_chains = c.chains; a.tm_acol = c.acol;
     a.trace = p.d_trace; a.trace_steps = p.trace_steps;
     const void* fn = fwd_kernel(a.bf16 != 0, c.bulk != 0);
+    // the pre-activation tiles' map: ga as [rows][ndir*4H] fp32, boxes of 32 units x NBM rows
+    CUtensorMap pre_map;
+    memset(&pre_map, 0, sizeof(pre_map));
+    const int nd4H = a.ndir * 4 * a.H;
+    a.tma_pre = c.tma_pre && make_map_f32(&pre_map, a.ga, p.rows, nd4H, nd4H, kCU, c.JC) ? 1 : 0;
+    void* args[] = {&a, &pre_map};
     trace_begin(p, K_REC_FWD, s);
-    const lstm_status st = cluster_launch(c, fn, a, s);
+    const lstm_status st = cluster_launch(c, fn, args, a.ndir, s);
     trace_end(p, K_REC_FWD, s, st == LSTM_OK ? 1 : 0);
     return st;
 }
@@ -1182,8 +1244,9 @@ lstm_status rec_cluster_bwd_launch(const Plan& p, const RecConfig& c, RecArgs a,
     a.G = c.G; a.Umax = c.Umax; a.JC = c.JC; a.tm_chains = c.chains; a.tm_acol = c.acol;
     a.trace = p.d_trace; a.trace_steps = p.trace_steps;
     const void* fn = a.bf16 ? (const void*)lstm_rec_bwd_cluster_kernel<false> : (const void*)lstm_rec_bwd_cluster_kernel<true>;
+    void* args[] = {&a};
     trace_begin(p, K_REC_BWD, s);
-    lstm_status st = cluster_launch(c, fn, a, s);
+    lstm_status st = cluster_launch(c, fn, args, a.ndir, s);
     int launched = st == LSTM_OK ? 1 : 0;
     if (st == LSTM_OK) {
         st = param_sums_launch(p, a.ga, a.cbuf, a.H, a.ndir, a.db, a.dpeep, sum_scratch, s);
