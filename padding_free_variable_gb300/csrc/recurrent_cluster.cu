@@ -266,6 +266,8 @@ __device__ __forceinline__ void bulk_wait_read_all_but_one()
 {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
+// this thread's bulk copies have all finished reading their source
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // this thread's bulk copies have completed (destination written)
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
@@ -457,11 +459,17 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
         for (int g = 0; g < 4; ++g)
             tc::tma_load_2d(pre_tile + (size_t)g * NBM * kCU, &pre_map, pre_bar, dir * 4 * H + g * H + u0, s_off[t2]);
     };
-    if (tma_pre && threadIdx.x == 0) issue_pre(0, true);
+    int last_tile = -1;                   // thread 0: the last step whose tile was issued
+    if (tma_pre && threadIdx.x == 0) { issue_pre(0, true); last_tile = 0; }
     cl.sync();     // every CTA of the cluster is resident before any remote write
 
     const int jq = threadIdx.x >> 3, q8 = threadIdx.x & 7;          // cell item: row jq (+32k), units q8*4..+4
     const int nks = (H + 15) / 16;                                   // MMA k-steps
+    float pk[3][4];                                                  // peepholes i, f, o of units q8*4..+4
+#pragma unroll
+    for (int q = 0; q < 3; ++q)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pk[q][e] = peep_s[q * kCU + q8 * 4 + e];
     const uint32_t bstep = (uint32_t)(NBM * (BULK ? 64 : 128)) >> 4;  // descriptor units between B blocks
     bool failed = false;                  // CTA-uniform: an MMA completion wait timed out
     bool pre_ok_prev = true;              // this thread's wait for the previous step's tile
@@ -482,7 +490,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
             if (s > 0) {
                 cluster_wait();    // h_{t-1} of every peer is in this CTA's operand
                 // every thread of this CTA arrived after its cell: the tile is free
-                if (tma_pre && threadIdx.x == 0) issue_pre(s, true);
+                if (tma_pre && threadIdx.x == 0 && !failed) { issue_pre(s, true); last_tile = s; }
                 cstamp(a, false, dir, rank, s - 1, 4, 4);
             }
             cstamp(a, false, dir, rank, s, 0, 0);
@@ -561,7 +569,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
         // exchange the global outputs of rows jq and jq + 32 are written after the exchange's
         // barrier arrival, so that the arrival (a release) does not wait for them
         bool pre_ok = true;
-        if (tma_pre) pre_ok = tc::mbar_wait(pre_bar, (uint32_t)(s & 1), a.wait_limit_ns);
+        if (tma_pre && !failed) pre_ok = tc::mbar_wait(pre_bar, (uint32_t)(s & 1), a.wait_limit_ns);
         if (!pre_ok && !failed) {
             record_failure(a.status, LSTM_ERR_TIMEOUT, 0x70000u | (unsigned)s);
             *s_fail = 1 + s;
@@ -615,21 +623,31 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
                 }
             }
             float hv[4], cv[4], gg[4][4];
+            // the row's products of the 4 gates and its previous cell states, 4 units at a time
+            float acv[4][4], cpv[4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const float4 x = *reinterpret_cast<const float4*>(accs + (size_t)j * kCM + g * kCU + q8 * 4);
+                acv[g][0] = x.x; acv[g][1] = x.y; acv[g][2] = x.z; acv[g][3] = x.w;
+            }
+            {
+                const float4 x = j < n_prev ? *reinterpret_cast<const float4*>(cst + j * kCU + q8 * 4)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                cpv[0] = x.x; cpv[1] = x.y; cpv[2] = x.z; cpv[3] = x.w;
+            }
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int uu = q8 * 4 + e;
-                const float* ac = accs + (size_t)j * kCM + uu;
-                const float cp = j < n_prev ? cst[j * kCU + uu] : 0.f;
-                const float ig = sigm_c(pv[0][e] + ac[0] + peep_s[uu] * cp);
-                const float fg = sigm_c(pv[1][e] + ac[32] + peep_s[32 + uu] * cp);
-                const float zg = tanh_c(pv[2][e] + ac[64]);
+                const float cp = cpv[e];
+                const float ig = sigm_c(pv[0][e] + acv[0][e] + pk[0][e] * cp);
+                const float fg = sigm_c(pv[1][e] + acv[1][e] + pk[1][e] * cp);
+                const float zg = tanh_c(pv[2][e] + acv[2][e]);
                 float c = fg * cp + ig * zg;
-                const float og = sigm_c(pv[3][e] + ac[96] + peep_s[64 + uu] * c);
+                const float og = sigm_c(pv[3][e] + acv[3][e] + pk[2][e] * c);
                 float h = og * tanh_c(c);
                 if (a.padded && t >= len) { c = 0.f; h = 0.f; }
                 gg[0][e] = ig; gg[1][e] = fg; gg[2][e] = zg; gg[3][e] = og; cv[e] = c; hv[e] = h;
-                cst[j * kCU + uu] = c;
             }
+            *reinterpret_cast<float4*>(cst + j * kCU + q8 * 4) = make_float4(cv[0], cv[1], cv[2], cv[3]);
             split4(hv, xh[it], xl[it], SPLIT);
             if (!BULK && it < 2) {
 #pragma unroll
@@ -675,7 +693,10 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
                 bulk_commit();
             }
             cstamp(a, false, dir, rank, s, 4, 4);
-            if (tma_pre && threadIdx.x == 0 && s + 1 < T) issue_pre(s + 1, false);   // the tile has been read
+            if (tma_pre && threadIdx.x == 0 && s + 1 < T && !failed) {   // the tile has been read
+                issue_pre(s + 1, false);
+                last_tile = s + 1;
+            }
             if (s + 1 < T && sender && !failed) bulk_wait_read_all_but_one();   // step s - 1's staging
         } else {
             cluster_wait();        // every peer's product of this step is done with its operand
@@ -703,8 +724,9 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
         pre_ok_prev = pre_ok;
         cstamp(a, false, dir, rank, s, 3, 3);
     }
-    // the last tile was waited for at its step; wait again (bounded) in case that wait ran out
-    if (tma_pre && threadIdx.x == 0) tc::mbar_wait(pre_bar, (uint32_t)((T - 1) & 1), kTeardownWaitNs);
+    // after a timeout the last tile issued may not have been waited for: no load may still be
+    // writing this CTA's shared memory when it exits (bounded wait)
+    if (tma_pre && threadIdx.x == 0 && last_tile >= 0) tc::mbar_wait(pre_bar, (uint32_t)(last_tile & 1), kTeardownWaitNs);
     if (BULK) {
         if (lane == 0 && warp < G) bulk_wait_all();   // no copy of this CTA is still in flight
         cl.sync();                              // nor one into it: every CTA has passed its last wait
@@ -727,19 +749,35 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
 // the same cluster layout.  The error reaching h_t through R is
 // R^T da_{t+1}; CTA c holds its 128 gate rows of R (as R^T, in tensor memory)
 // and the gate errors it computes for them, so it forms the partial product
-// P_c = R_c^T da_c for every unit on the tensor cores, and pushes the part of
-// P_c that belongs to CTA c' (its 32 units) into c''s inbox through
-// distributed shared memory.  At the next step each CTA adds the G partials
-// of its units in CTA order.  db and dpeep are summed afterwards by
-// lstm_param_sums_kernel.
+// P_c = R_c^T da_c for every unit on the tensor cores, and sends the part of
+// P_c that belongs to CTA c' (its 32 units) into c''s inbox.  At the next step
+// each CTA adds the G partials of its units in CTA order.  db and dpeep are
+// summed afterwards by lstm_param_sums_kernel.
 // Shared memory (RecArgs offsets): off_contrib = B (gate errors, hi then
-// lo), off_acc = inbox, off_state = dc carry, off_sums = mbarrier, TMEM slot,
-// failure flag, off_peep = peepholes, off_tab = tables.
+// lo), off_acc = inbox, off_state = dc carry, off_sums = mbarriers, TMEM
+// slot, failure flag, off_peep = peepholes, off_tab = tables; BULK also
+// off_h = staging of the outgoing partials [G][NBM][32], off_red = operand
+// tiles [7][NBM][32] (gates i f z o, c_t, c_{t-1}, dy).
 // Tensor memory: accumulators (tile m, chain ch) at columns
 // (m * chains + ch) * NBM; R^T tile m from column tm_acol + 64m (hi) and
 // tm_acol + 64 MT + 64m (lo).
-template <bool SPLIT>
-__global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
+//
+// Exchanges of the partials:
+//  * BULK: the inbox is double-buffered per step parity ([2][G][NBM][32]);
+//    the TMEM read-out lands in a staging buffer laid out per owner, and one
+//    cp.async.bulk per owner copies it into the owner's inbox, completing on
+//    the owner's mbarrier of that parity (re-armed before the CTA's own copies
+//    go out, as in the forward kernel).  A source can only write parity
+//    (s & 1) again for step s + 2 after it received this CTA's partials of
+//    step s + 1, which are formed after this CTA's cell of step s has read the
+//    inbox.  The cell's own operands arrive as TMA tiles (a.tma_pre).
+//  * otherwise: one inbox written with plain DSMEM stores between the two
+//    halves of a split cluster barrier.
+template <bool SPLIT, bool BULK>
+__global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
+                                                                     const __grid_constant__ CUtensorMap map_ga,
+                                                                     const __grid_constant__ CUtensorMap map_c,
+                                                                     const __grid_constant__ CUtensorMap map_dy)
 {
     extern __shared__ unsigned char smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -754,22 +792,35 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
     const int nch = a.tm_chains;                     // chains per tile; issuers = MT * nch
     uint8_t* Bhi = base + a.off_contrib;             // [2 k-blocks][NBM][128 B]
     uint8_t* Blo = Bhi + (size_t)2 * NBM * 128;
-    float* inbox = reinterpret_cast<float*>(base + a.off_acc);       // [G][NBM][32]
+    float* inbox = reinterpret_cast<float*>(base + a.off_acc);       // [BULK ? 2 : 1][G][NBM][32]
+    float* stage = reinterpret_cast<float*>(base + a.off_h);         // BULK: [G][NBM][32]
+    float* tiles = reinterpret_cast<float*>(base + a.off_red);       // BULK + tma_pre: [7][NBM][32]
     float* dcc = reinterpret_cast<float*>(base + a.off_state);       // [B][32]
     uint64_t* mma_bar = reinterpret_cast<uint64_t*>(base + a.off_sums);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 1);
     int* s_fail = reinterpret_cast<int*>(tmem_slot + 1);
+    uint64_t* full_bar = mma_bar + 2;                                // BULK: [2] inbox arrival per parity
+    uint64_t* opnd_bar = mma_bar + 4;                                // operand tiles' arrival
     float* peep_s = reinterpret_cast<float*>(base + a.off_peep);
     int* s_bs = reinterpret_cast<int*>(base + a.off_tab);
     int* s_off = s_bs + T;
     int* s_len = s_off + T + 1;
     const uint32_t tcols = (uint32_t)a.Umax;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    auto inbox_at = [&](int src, int j) -> float* { return inbox + ((size_t)src * NBM + j) * kCU; };
+    const bool tma_opnd = BULK && a.tma_pre != 0;
+    auto inbox_at = [&](int parity, int src, int j) -> float* {
+        return inbox + (((size_t)(BULK ? parity : 0) * G + src) * NBM + j) * kCU;
+    };
+    auto tile = [&](int k, int j) -> float* { return tiles + ((size_t)k * NBM + j) * kCU; };
+    // bytes a CTA receives for step s2 (partials of step s2 - 1 from every CTA, rows rounded to 16)
+    auto step_bytes = [&](int s2) -> uint32_t {
+        const int tp = dir == 0 ? T - s2 : s2 - 1;
+        return (uint32_t)G * (uint32_t)((s_bs[tp] + 15) & ~15) * (uint32_t)(kCU * 4);
+    };
 
     for (int i = threadIdx.x; i < (SPLIT ? 2 : 1) * 2 * NBM * 128 / 16; i += kCT)
         reinterpret_cast<uint4*>(Bhi)[i] = make_uint4(0, 0, 0, 0);
-    for (int i = threadIdx.x; i < G * NBM * kCU; i += kCT) inbox[i] = 0.f;
+    for (int i = threadIdx.x; i < (BULK ? 2 : 1) * G * NBM * kCU; i += kCT) inbox[i] = 0.f;
     for (int i = threadIdx.x; i < T; i += kCT) s_bs[i] = a.bs[i];
     for (int i = threadIdx.x; i <= T; i += kCT) s_off[i] = a.off[i];
     for (int i = threadIdx.x; i < a.B; i += kCT) s_len[i] = a.slot_len[i];
@@ -780,7 +831,14 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
     if (threadIdx.x == 0) {
         tc::mbar_init(mma_bar, (uint32_t)(MT * nch));
         *s_fail = 0;
+        if (BULK) {
+            tc::mbar_init(&full_bar[0], 1);
+            tc::mbar_init(&full_bar[1], 1);
+        }
+        if (tma_opnd) tc::mbar_init(opnd_bar, 1);
         tc::fence_mbar_init();
+        // the inbox of step 1 (parity 1) is armed before the cluster barrier below
+        if (BULK && T > 1) tc::mbar_arrive_expect_tx(&full_bar[1], step_bytes(1));
     }
     if (threadIdx.x < 32) {
         tc::tmem_alloc(tmem_slot, tcols);
@@ -820,11 +878,32 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
     tc::tc_fence_before_sync();
     __syncthreads();
     tc::tc_fence_after_sync();
+    // tma_opnd: the seven operand tiles of step s2 (NBM rows each; rows past the packed rows read
+    // 0), one thread, completing on opnd_bar
+    auto issue_opnd = [&](int s2) {
+        const int t2 = dir == 0 ? T - 1 - s2 : s2;
+        const int y0 = s_off[t2];
+        const int yp = dir == 0 ? (t2 >= 1 ? s_off[t2 - 1] : 0) : (t2 + 1 < T ? s_off[t2 + 1] : 0);
+        tc::mbar_arrive_expect_tx(opnd_bar, (uint32_t)(7 * NBM * kCU * 4));
+#pragma unroll
+        for (int g = 0; g < 4; ++g) tc::tma_load_2d(tile(g, 0), &map_ga, opnd_bar, dir * 4 * H + g * H + u0, y0);
+        tc::tma_load_2d(tile(4, 0), &map_c, opnd_bar, dir * H + u0, y0);
+        tc::tma_load_2d(tile(5, 0), &map_c, opnd_bar, dir * H + u0, yp);
+        tc::tma_load_2d(tile(6, 0), &map_dy, opnd_bar, dir * H + u0, y0);
+    };
+    int last_tile = -1;                   // thread 0: the last step whose tiles were issued
+    if (tma_opnd && threadIdx.x == 0) { issue_opnd(0); last_tile = 0; }
     cl.sync();
 
     const int jq = threadIdx.x >> 3, q8 = threadIdx.x & 7;          // cell item: row jq (+32k), units q8*4..+4
     const uint32_t bstep = (uint32_t)(NBM * 128) >> 4;
+    float pk[3][4];                                                  // peepholes i, f, o of units q8*4..+4
+#pragma unroll
+    for (int q = 0; q < 3; ++q)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) pk[q][e] = peep_s[q * kCU + q8 * 4 + e];
     // own operands (gates, c_t, c_{t-1}, dy) of row jq of a step, loaded one step ahead
+    // (without operand tiles)
     float nx[7][4];
     auto load_own = [&](int s2) {
         const int t2 = dir == 0 ? T - 1 - s2 : s2;
@@ -851,8 +930,8 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
             nx[5][0] = nx[5][1] = nx[5][2] = nx[5][3] = 0.f;
         }
     };
-    load_own(0);
-    bool failed = false;                  // CTA-uniform: an MMA completion wait timed out
+    if (!tma_opnd) load_own(0);
+    bool failed = false;                  // CTA-uniform: a bounded wait ran out
     bool step_ok = true;                  // this thread's wait of the last product
     for (int s = 0; s < T; ++s) {
         const int t = dir == 0 ? T - 1 - s : s;
@@ -862,7 +941,17 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
         const int prev_base = dir == 0 ? (t >= 1 ? s_off[t - 1] : 0) : (t + 1 < T ? s_off[t + 1] : 0);
         const int n_prev = dir == 0 ? (t >= 1 ? n : 0) : (t + 1 < T ? s_bs[t + 1] : 0);
         const int NBs = (n + 15) & ~15;
-        cstamp(a, true, dir, rank, s, 0, 1);
+        const int par = BULK ? (s & 1) : 0;
+        cstamp(a, true, dir, rank, s, 0, 0);
+        bool arrived = true;              // this step's inbox and operand tiles arrived
+        if (BULK && s > 0 && !failed)
+            arrived = tc::mbar_wait(&full_bar[par], (uint32_t)(((s - 1) >> 1) & 1), a.wait_limit_ns);
+        if (tma_opnd && !failed && !tc::mbar_wait(opnd_bar, (uint32_t)(s & 1), a.wait_limit_ns)) arrived = false;
+        if (!arrived && !failed) {
+            record_failure(a.status, LSTM_ERR_TIMEOUT, 0x60000u | (unsigned)s);
+            *s_fail = 1 + s;
+        }
+        cstamp(a, true, dir, rank, s, 1, 1);
         for (int it = 0; it * 32 < n; ++it) {
             const int j = jq + it * 32;
             if (j >= n) continue;
@@ -870,7 +959,20 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
             const int uub = q8 * 4;
             float* gr = a.ga + (size_t)row * nd4H + dir * 4 * H + u0 + uub;
             float gv[4][4], cv[4], cpv[4], dyv[4];
-            if (it == 0) {
+            if (tma_opnd) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const float4 x = *reinterpret_cast<const float4*>(tile(g, j) + uub);
+                    gv[g][0] = x.x; gv[g][1] = x.y; gv[g][2] = x.z; gv[g][3] = x.w;
+                }
+                const float4 c0 = *reinterpret_cast<const float4*>(tile(4, j) + uub);
+                const float4 p0 = *reinterpret_cast<const float4*>(tile(5, j) + uub);
+                const float4 d0 = *reinterpret_cast<const float4*>(tile(6, j) + uub);
+                cv[0] = c0.x; cv[1] = c0.y; cv[2] = c0.z; cv[3] = c0.w;
+                dyv[0] = d0.x; dyv[1] = d0.y; dyv[2] = d0.z; dyv[3] = d0.w;
+                const bool hp = j < n_prev;
+                cpv[0] = hp ? p0.x : 0.f; cpv[1] = hp ? p0.y : 0.f; cpv[2] = hp ? p0.z : 0.f; cpv[3] = hp ? p0.w : 0.f;
+            } else if (it == 0) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     gv[0][e] = nx[0][e]; gv[1][e] = nx[1][e]; gv[2][e] = nx[2][e]; gv[3][e] = nx[3][e];
@@ -897,30 +999,36 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
             }
             const bool has_next = j < n_next;
             const bool real = !a.padded || t < s_len[j];
-            float da[4][4];
+            // the G partial sums of R^T da of the step after, added in CTA order, and the carry
+            float dhr[4] = {0.f, 0.f, 0.f, 0.f}, car[4] = {0.f, 0.f, 0.f, 0.f};
+            if (has_next) {
+                for (int c2 = 0; c2 < G; ++c2) {
+                    const float4 x = *reinterpret_cast<const float4*>(inbox_at(par, c2, j) + uub);
+                    dhr[0] += x.x; dhr[1] += x.y; dhr[2] += x.z; dhr[3] += x.w;
+                }
+                const float4 x = *reinterpret_cast<const float4*>(dcc + j * kCU + uub);
+                car[0] = x.x; car[1] = x.y; car[2] = x.z; car[3] = x.w;
+            }
+            float da[4][4], cout[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int uu = uub + e;
-                float dh_rec = 0.f;
-                if (has_next)
-                    for (int c2 = 0; c2 < G; ++c2) dh_rec += inbox_at(c2, j)[uu];
                 float dai = 0.f, daf = 0.f, daz = 0.f, dao = 0.f, carry_out = 0.f;
                 if (real) {
                     const float ig = gv[0][e], fg = gv[1][e], zg = gv[2][e], og = gv[3][e];
                     const float c = cv[e], cp = cpv[e];
-                    const float dh = dyv[e] + dh_rec;
-                    const float carry = has_next ? dcc[j * kCU + uu] : 0.f;
+                    const float dh = dyv[e] + dhr[e];
                     const float tc = tanh_c(c);
                     dao = dh * tc * og * (1.f - og);
-                    const float dc = dh * og * (1.f - tc * tc) + dao * peep_s[64 + uu] + carry;
+                    const float dc = dh * og * (1.f - tc * tc) + dao * pk[2][e] + car[e];
                     dai = dc * zg * ig * (1.f - ig);
                     daf = dc * cp * fg * (1.f - fg);
                     daz = dc * ig * (1.f - zg * zg);
-                    carry_out = dc * fg + dai * peep_s[uu] + daf * peep_s[32 + uu];
+                    carry_out = dc * fg + dai * pk[0][e] + daf * pk[1][e];
                 }
                 da[0][e] = dai; da[1][e] = daf; da[2][e] = daz; da[3][e] = dao;
-                dcc[j * kCU + uu] = carry_out;
+                cout[e] = carry_out;
             }
+            *reinterpret_cast<float4*>(dcc + j * kCU + uub) = make_float4(cout[0], cout[1], cout[2], cout[3]);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 *reinterpret_cast<float4*>(gr + g * H) = make_float4(da[g][0], da[g][1], da[g][2], da[g][3]);
@@ -931,12 +1039,23 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
                 if (SPLIT) *reinterpret_cast<uint2*>(Blo + o) = lo;
             }
         }
-        cluster_arrive_relaxed();   // this CTA has read its inbox: peers may overwrite it
+        if (!BULK) cluster_arrive_relaxed();   // this CTA has read its inbox: peers may overwrite it
+        // the previous step's staging must have been read by its copies before this step's read-out
+        if (BULK && lane == 0 && warp < G) bulk_wait_read_all();
         fence_proxy_async_cta();
-        // a timeout of the previous step's product becomes a CTA-uniform decision here, before
-        // the next issue (that step's read-out may have seen partial sums; the status word
-        // marks the results as invalid)
-        if (__syncthreads_or(!step_ok)) failed = true;
+        // a timeout (of the previous step's product, or of this step's arrivals) becomes a
+        // CTA-uniform decision here, before the next issue: from then on the CTA issues, waits
+        // for, re-arms and sends nothing (that step's read-out may have seen partial sums; the
+        // status word marks the results as invalid)
+        if (__syncthreads_or(!step_ok || !arrived)) failed = true;
+        // the operand tiles and this parity's inbox have been read
+        if (tma_opnd && threadIdx.x == 0 && s + 1 < T && !failed) {
+            issue_opnd(s + 1);
+            last_tile = s + 1;
+        }
+        // BULK: re-arm this parity for step s + 2 before this CTA's partials of step s go out
+        if (BULK && threadIdx.x == 0 && !failed && s + 2 < T)
+            tc::mbar_arrive_expect_tx(&full_bar[par], step_bytes(s + 2));
         cstamp(a, true, dir, rank, s, 2, 2);
         if (s + 1 < T) {
             // P[u'][j] = sum over this CTA's gate rows r of R[r][u'] da[j][r]: warp w issues tile
@@ -960,32 +1079,74 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a)
             tc::tc_fence_after_sync();
             cstamp(a, true, dir, rank, s, 5, 7);
         }
-        cluster_wait();        // every peer has read its inbox of this step
-        if (s + 1 < T && !failed) {
-            // tile m, lane quarter q: units u' = 128m + 32q + lane, owned by CTA 4m + q
-            for (int pq = warp; pq < MT * 4; pq += kCT / 32) {
-                const int m = pq >> 2, q = pq & 3;
-                const int owner = 4 * m + q;
-                if (owner >= G) continue;
-                float* dst_base = cl.map_shared_rank(inbox_at(rank, 0), owner);
-                for (int c0 = 0; c0 < NBs; c0 += 16) {
-                    float v[16];
-                    tmem_sum_chains(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(m * nch * NBM + c0),
-                                    (uint32_t)NBM, nch, v);
-                    // lanes are consecutive units: each store is one coalesced 128-byte row
+        if (BULK) {
+            if (s + 1 < T && !failed) {
+                // read-out into the staging, per owner: tile m, lane quarter q -> owner 4m + q,
+                // units 32q + lane of the tile, rows [0, NBs)
+                for (int pq = warp; pq < MT * 4; pq += kCT / 32) {
+                    const int m = pq >> 2, q = pq & 3;
+                    const int owner = 4 * m + q;
+                    if (owner >= G) continue;
+                    float* dst = stage + (size_t)owner * NBM * kCU;
+                    for (int c0 = 0; c0 < NBs; c0 += 16) {
+                        float v[16];
+                        tmem_sum_chains(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(m * nch * NBM + c0),
+                                        (uint32_t)NBM, nch, v);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        if (c0 + e < n) dst_base[(size_t)(c0 + e) * kCU + lane] = v[e];
+                        for (int e = 0; e < 16; ++e) dst[(size_t)(c0 + e) * kCU + lane] = v[e];
+                    }
                 }
             }
             tc::tc_fence_before_sync();
+            fence_proxy_async_cta();
+            __syncthreads();
+            // lane 0 of warp w sends to owners w, w + 8 (copies issued by one warp's lanes serialise)
+            if (s + 1 < T && !failed && lane == 0 && warp < G) {
+                const uint32_t nxt = (uint32_t)(par ^ 1);
+                const uint32_t bytes = (uint32_t)NBs * (uint32_t)(kCU * 4);
+                for (int o = warp; o < G; o += kCT / 32) {
+                    const uint32_t bar = mapa_u32(tc::smem_u32(&full_bar[nxt]), (uint32_t)o);
+                    bulk_to_peer(mapa_u32(tc::smem_u32(inbox_at(nxt, rank, 0)), (uint32_t)o),
+                                 stage + (size_t)o * NBM * kCU, bytes, bar);
+                }
+                bulk_commit();
+            }
+            cstamp(a, true, dir, rank, s, 3, 4);
+        } else {
+            cluster_wait();        // every peer has read its inbox of this step
+            if (s + 1 < T && !failed) {
+                // tile m, lane quarter q: units u' = 128m + 32q + lane, owned by CTA 4m + q
+                for (int pq = warp; pq < MT * 4; pq += kCT / 32) {
+                    const int m = pq >> 2, q = pq & 3;
+                    const int owner = 4 * m + q;
+                    if (owner >= G) continue;
+                    float* dst_base = cl.map_shared_rank(inbox_at(0, rank, 0), owner);
+                    for (int c0 = 0; c0 < NBs; c0 += 16) {
+                        float v[16];
+                        tmem_sum_chains(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(m * nch * NBM + c0),
+                                        (uint32_t)NBM, nch, v);
+                        // lanes are consecutive units: each store is one coalesced 128-byte row
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            if (c0 + e < n) dst_base[(size_t)(c0 + e) * kCU + lane] = v[e];
+                    }
+                }
+                tc::tc_fence_before_sync();
+            }
+            cstamp(a, true, dir, rank, s, 3, 3);
+            fence_proxy_async_cluster();
+            cluster_arrive();      // release: this CTA's partial sums are in their owners' inboxes
+            if (s + 1 < T) load_own(s + 1);       // the next step's own operands, in flight across the barrier
+            cluster_wait();
+            cstamp(a, true, dir, rank, s, 4, 4);
         }
-        cstamp(a, true, dir, rank, s, 3, 3);
-        fence_proxy_async_cluster();
-        cluster_arrive();      // release: this CTA's partial sums are in their owners' inboxes
-        if (s + 1 < T) load_own(s + 1);       // the next step's own operands, in flight across the barrier
-        cluster_wait();
-        cstamp(a, true, dir, rank, s, 4, 4);
+    }
+    if (BULK) {
+        if (lane == 0 && warp < G) bulk_wait_all();   // no copy of this CTA is still in flight
+        // after a timeout the last tiles issued may not have been waited for (bounded wait)
+        if (tma_opnd && threadIdx.x == 0 && last_tile >= 0)
+            tc::mbar_wait(opnd_bar, (uint32_t)(last_tile & 1), kTeardownWaitNs);
+        cl.sync();                                    // nor one into it
     }
     tc::tc_fence_before_sync();
     __syncthreads();
@@ -1201,6 +1362,13 @@ lstm_status rec_cluster_fwd_launch(const Plan& p, const RecConfig& c, RecArgs a,
     return st;
 }
 
+static const void* bwd_kernel(bool bf16, bool bulk)
+{
+    if (bulk) return bf16 ? (const void*)lstm_rec_bwd_cluster_kernel<false, true>
+                          : (const void*)lstm_rec_bwd_cluster_kernel<true, true>;
+    return bf16 ? (const void*)lstm_rec_bwd_cluster_kernel<false, false> : (const void*)lstm_rec_bwd_cluster_kernel<true, false>;
+}
+
 bool rec_cluster_bwd_configure(const Plan& p, int H, int ndir, bool bf16, RecConfig* out, RecArgs* lay)
 {
     if (p.gemm_engine != 0 || p.forced_ctas != 0) return false;
@@ -1216,25 +1384,30 @@ bool rec_cluster_bwd_configure(const Plan& p, int H, int ndir, bool bf16, RecCon
     while (nch > 1 && (MT * nch > 4 || MT * nch * NBM + acols > 512)) nch >>= 1;
     if (MT * nch * NBM + acols > 512 || MT * nch > kCT / 32) return false;
     const uint32_t cols = pow2_cols(MT * nch * NBM + acols);
-    size_t off = 0;
-    const size_t o_b = off; off = al(off + (split ? 2 : 1) * (size_t)2 * NBM * 128, 1024);
-    const size_t o_in = off; off = al(off + (size_t)G * NBM * kCU * 4, 16);
-    const size_t o_dcc = off; off = al(off + (size_t)p.B * kCU * 4, 16);
-    const size_t o_bar = off; off = al(off + 64, 16);
-    const size_t o_peep = off; off = al(off + 3 * kCU * 4, 16);
-    const size_t o_tab = off; off = al(off + (size_t)(2 * p.T + 1 + p.B) * 4, 16);
-    size_t smem = off + 1024 + 64;
-    smem = tmem_safe_smem(p, smem, cols);
-    if (smem == 0) return false;
-    const void* fn = bf16 ? (const void*)lstm_rec_bwd_cluster_kernel<false> : (const void*)lstm_rec_bwd_cluster_kernel<true>;
-    if (!cluster_schedulable(p, fn, G, smem)) return false;
-    RecConfig c;
-    c.G = G; c.Umax = (int)cols; c.JC = NBM; c.smem = smem; c.cluster = 1;
-    c.chains = nch; c.acol = (int)cols - acols;
-    *out = c;
-    lay->off_contrib = (int)o_b; lay->off_acc = (int)o_in; lay->off_state = (int)o_dcc;
-    lay->off_sums = (int)o_bar; lay->off_peep = (int)o_peep; lay->off_tab = (int)o_tab;
-    return true;
+    // bulk exchange with operand tiles first; the single-buffered barrier exchange needs the least
+    for (int bulk = 1; bulk >= 0; --bulk) {
+        size_t off = 0;
+        const size_t o_b = off; off = al(off + (split ? 2 : 1) * (size_t)2 * NBM * 128, 1024);
+        const size_t o_in = off; off = al(off + (bulk ? 2 : 1) * (size_t)G * NBM * kCU * 4, 1024);
+        const size_t o_stage = off; if (bulk) off = al(off + (size_t)G * NBM * kCU * 4, 1024);
+        const size_t o_tiles = off; if (bulk) off = al(off + 7 * (size_t)NBM * kCU * 4, 1024);
+        const size_t o_dcc = off; off = al(off + (size_t)p.B * kCU * 4, 16);
+        const size_t o_bar = off; off = al(off + 64, 16);
+        const size_t o_peep = off; off = al(off + 3 * kCU * 4, 16);
+        const size_t o_tab = off; off = al(off + (size_t)(2 * p.T + 1 + p.B) * 4, 16);
+        size_t smem = off + 1024 + 64;
+        smem = tmem_safe_smem(p, smem, cols);
+        if (smem == 0) return false;
+        if (!cluster_schedulable(p, bwd_kernel(bf16, bulk != 0), G, smem)) continue;
+        RecConfig c;
+        c.G = G; c.Umax = (int)cols; c.JC = NBM; c.smem = smem; c.cluster = 1;
+        c.chains = nch; c.acol = (int)cols - acols; c.bulk = bulk; c.tma_pre = bulk;
+        *out = c;
+        lay->off_contrib = (int)o_b; lay->off_acc = (int)o_in; lay->off_h = (int)o_stage; lay->off_red = (int)o_tiles;
+        lay->off_state = (int)o_dcc; lay->off_sums = (int)o_bar; lay->off_peep = (int)o_peep; lay->off_tab = (int)o_tab;
+        return true;
+    }
+    return false;
 }
 
 size_t rec_cluster_bwd_sum_floats(int H, int ndir) { return (size_t)kSumChunks * ndir * 7 * H; }
@@ -1243,8 +1416,17 @@ lstm_status rec_cluster_bwd_launch(const Plan& p, const RecConfig& c, RecArgs a,
 {
     a.G = c.G; a.Umax = c.Umax; a.JC = c.JC; a.tm_chains = c.chains; a.tm_acol = c.acol;
     a.trace = p.d_trace; a.trace_steps = p.trace_steps;
-    const void* fn = a.bf16 ? (const void*)lstm_rec_bwd_cluster_kernel<false> : (const void*)lstm_rec_bwd_cluster_kernel<true>;
-    void* args[] = {&a};
+    const void* fn = bwd_kernel(a.bf16 != 0, c.bulk != 0);
+    // operand tiles: ga as [rows][ndir*4H], c and dy as [rows][ndir*H] fp32, boxes of 32 x NBM
+    CUtensorMap map_ga, map_c, map_dy;
+    memset(&map_ga, 0, sizeof(map_ga));
+    memset(&map_c, 0, sizeof(map_c));
+    memset(&map_dy, 0, sizeof(map_dy));
+    const int nd4H = a.ndir * 4 * a.H, ndH = a.ndir * a.H;
+    a.tma_pre = c.tma_pre && make_map_f32(&map_ga, a.ga, p.rows, nd4H, nd4H, kCU, c.JC) &&
+                make_map_f32(&map_c, a.cbuf, p.rows, ndH, ndH, kCU, c.JC) &&
+                make_map_f32(&map_dy, a.dy, p.rows, ndH, ndH, kCU, c.JC) ? 1 : 0;
+    void* args[] = {&a, &map_ga, &map_c, &map_dy};
     trace_begin(p, K_REC_BWD, s);
     lstm_status st = cluster_launch(c, fn, args, a.ndir, s);
     int launched = st == LSTM_OK ? 1 : 0;
