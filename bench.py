@@ -149,6 +149,15 @@ def kind_work(kind: str, spec, rows: int, D0: int, uses_tensor: dict):
         elif kind == "gemm_dr":
             fl += 2.0 * rows * 4 * H * H * nd
             by += rows * G4 * 4 + rows * nd * H * 4 + nd * 4 * H * H * 4
+        if kind == "convert":
+            # bf16 operands of the tensor-core products (one K segment for bf16 layers, three for
+            # fp32 layers): dA read once, written transposed and row-major; X, H_prev, W read and
+            # written transposed; fp32 layers also split X and W for the input projection
+            ns = 1 if spec.dtype == "bf16" else 3
+            by += rows * G4 * 4 + rows * D * ex + rows * nd * H * 4 + G4 * D * e
+            by += ns * 2 * (2 * rows * G4 + rows * D + rows * nd * H + G4 * D)
+            if ns == 3:
+                by += rows * D * 4 + G4 * D * 4 + ns * 2 * (rows * D + G4 * D)
     if kind == "pack":
         fl, by = 0.0, 2.0 * rows * (D0 * e + nd * H * 4)
     elif kind == "unpack":
@@ -202,6 +211,13 @@ def roofline_of(kind, ms_per_step, calls_per_step, spec, rows, T, D0, peaks, rec
     t_hbm = by / (hbm_peak * 1e9)
     if kind in GEMM_KINDS and spec.dtype == "bf16":
         cpeak, bound, src = float(peaks["bf16_tflops_sustained"]), "tensor", "MEASURED_PEAKS.json sustained bf16"
+    elif kind in GEMM_KINDS and spec.input_size % 8 == 0:
+        # fp32 products on tensor cores (three bf16 products): the fp32-input tensor rate, i.e. the
+        # measured bf16 peak x the nominal tf32 / bf16 ratio (1.1 / 2.25 PFLOP/s)
+        cpeak, bound = float(peaks["bf16_tflops_sustained"]) * 1.1 / 2.25, "tensor"
+        src = "MEASURED_PEAKS.json sustained bf16 x 1.1/2.25 (nominal tf32/bf16)"
+    elif kind == "convert":
+        cpeak, bound, src = float("inf"), "hbm", ""
     else:
         cpeak, bound = NUM_SMS * FP32_LANES_PER_SM * 2 * clk * 1e6 / 1e12, "alu"
         src = "derived: 152 SMs x 128 FP32 lanes x 2 flop x max SM clock"

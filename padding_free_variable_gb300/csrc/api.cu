@@ -33,17 +33,26 @@ lstm_status check_shape(const lstm_layer_shape* s)
     return LSTM_OK;
 }
 
+// fp32 layers whose products can run on tcgen05 as three bf16 products (hi/lo split
+// concatenated along K): the K extents (D, ndir*4H, frames) must be TMA-addressable.
+bool f32_split_shape(const lstm_layer_shape& s) { return s.dtype == LSTM_F32 && s.input_size % 8 == 0; }
+
 struct Layout {
-    size_t ga_off, c_off, total;   // workspace
+    size_t ga_off, c_off, xs_off, ws_off, total;   // workspace
 };
 
+// gates/errors, cell states, then (fp32 split shapes) the input projection's split operands:
+// X as [rows][3D] and W as [ndir*4H][3D] bf16
 Layout workspace_layout(const Plan& p, const lstm_layer_shape& s)
 {
     Layout l;
     const size_t rows = (size_t)p.rows, H = (size_t)s.hidden_size, nd = (size_t)s.num_directions;
+    const size_t D = (size_t)s.input_size;
     l.ga_off = 0;
     l.c_off = align256(rows * nd * 4 * H * sizeof(float));
-    l.total = l.c_off + align256(rows * nd * H * sizeof(float));
+    l.xs_off = l.c_off + align256(rows * nd * H * sizeof(float));
+    l.ws_off = l.xs_off + (f32_split_shape(s) ? align256(rows * 3 * D * 2) : 0);
+    l.total = l.ws_off + (f32_split_shape(s) ? align256(nd * 4 * H * 3 * D * 2) : 0);
     return l;
 }
 
@@ -77,22 +86,25 @@ BwdScratch bwd_scratch(const Plan& p, const lstm_layer_shape& s)
                            gemm_partial_floats(dX, p.num_sms));
     const size_t part = std::max(rec_bwd_part_floats(p, H, nd, s.dtype == LSTM_BF16, p.forced_ctas),
                                  rec_cluster_bwd_sum_floats(H, nd));
-    if (s.dtype == LSTM_BF16) {
-        const int rows = (int)p.rows;
-        const size_t tc = std::max((size_t)gemm_tc_splits(nd * 4 * H, D, rows, p.num_sms, kMaxTcSplits) * nd * 4 * H * D,
-                                   (size_t)gemm_tc_splits(4 * H, H, rows, p.num_sms, kMaxTcSplits) * 4 * H * H);
+    const bool tc_shape = s.dtype == LSTM_BF16 || f32_split_shape(s);
+    const int ns = s.dtype == LSTM_BF16 ? 1 : 3;     // K segments of the tensor-core operands
+    const int64_t ldr = (int64_t)(((size_t)p.rows + 7) / 8 * 8);
+    if (tc_shape) {
+        const int kr = ns == 1 ? (int)p.rows : (int)(3 * ldr);
+        const size_t tc = std::max((size_t)gemm_tc_splits(nd * 4 * H, D, kr, p.num_sms, kMaxTcSplits) * nd * 4 * H * D,
+                                   (size_t)gemm_tc_splits(4 * H, H, kr, p.num_sms, kMaxTcSplits) * 4 * H * H);
         gemm = std::max(gemm, tc);
     }
     b.u_bytes = align256(std::max<size_t>(1, std::max(gemm, part)) * sizeof(float));
     size_t off = b.u_bytes;
-    if (s.dtype == LSTM_BF16) {
+    if (tc_shape) {
         const size_t rows = (size_t)p.rows, G4 = (size_t)nd * 4 * H;
-        b.ldr = (int64_t)((rows + 7) / 8 * 8);
-        b.dA16 = off; off += align256(rows * G4 * 2);
-        b.dAT16 = off; off += align256(G4 * (size_t)b.ldr * 2);
-        b.XT16 = off; off += align256((size_t)D * b.ldr * 2);
-        b.HpT16 = off; off += align256((size_t)nd * H * b.ldr * 2);
-        b.WT16 = off; off += align256((size_t)D * G4 * 2);
+        b.ldr = ldr;
+        b.dA16 = off; off += align256(rows * ns * G4 * 2);
+        b.dAT16 = off; off += align256(G4 * ns * (size_t)b.ldr * 2);
+        b.XT16 = off; off += align256((size_t)D * ns * b.ldr * 2);
+        b.HpT16 = off; off += align256((size_t)nd * H * ns * b.ldr * 2);
+        b.WT16 = off; off += align256((size_t)D * ns * G4 * 2);
     }
     b.total = off;
     return b;
@@ -118,15 +130,32 @@ RecArgs base_args(const Plan& p, const lstm_layer_shape& s, const lstm_layer_par
     return a;
 }
 
-// A_in[rows][ndir*4H] = X W^T + b for both directions at once; tcgen05 for bf16 operands.
+bool encode_ready();
+
+// A_in[rows][ndir*4H] = X W^T + b for both directions at once; tcgen05 for bf16 operands, and
+// for fp32 operands as three bf16 products (X as [hi, hi, lo], W as [hi, lo, hi] along K, in
+// the workspace's split region `split_ws`, when given).
 lstm_status input_projection(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm,
-                             const void* x_packed, float* out, cudaStream_t cs)
+                             const void* x_packed, float* out, void* split_ws, cudaStream_t cs)
 {
     const int H = s.hidden_size, nd = s.num_directions, D = s.input_size;
     const bool bf16 = s.dtype == LSTM_BF16;
     if (bf16 && p.gemm_engine == 0 && gemm_tc_supported((int)p.rows, nd * 4 * H, D, x_packed, prm.W))
         return gemm_tc_bf16_nt(p, K_GEMM_IN, x_packed, prm.W, out, (int64_t)nd * 4 * H, prm.b, (int)p.rows,
                                nd * 4 * H, D, cs);
+    if (!bf16 && split_ws && p.gemm_engine == 0 && f32_split_shape(s) && encode_ready()) {
+        const int rows = (int)p.rows, G4 = nd * 4 * H;
+        char* xs = (char*)split_ws;
+        char* ws = xs + align256((size_t)rows * 3 * D * 2);
+        lstm_status st;
+        if ((st = transpose_to_bf16_split(p, x_packed, false, D, 0, nullptr, rows, rows, D, 1, nullptr, 0, 0, xs,
+                                          3 * D, D, cs)) != LSTM_OK)
+            return st;
+        if ((st = transpose_to_bf16_split(p, prm.W, false, D, 0, nullptr, G4, G4, D, 2, nullptr, 0, 0, ws, 3 * D, D,
+                                          cs)) != LSTM_OK)
+            return st;
+        return gemm_tc_bf16_nt(p, K_GEMM_IN, xs, ws, out, G4, prm.b, rows, G4, 3 * D, cs);
+    }
     GemmDesc g;
     g.M = (int)p.rows; g.N = nd * 4 * H; g.K = D;
     g.A = x_packed; g.sam = D; g.sak = 1; g.a_bf16 = bf16;
@@ -137,15 +166,23 @@ lstm_status input_projection(const Plan& p, const lstm_layer_shape& s, const lst
 
 bool encode_ready() { return gemm_tc_supported(1, 1, 8, nullptr, nullptr); }
 
-// dX, dW and dR of a bf16 layer on tcgen05, from the gate errors dA (fp32, in
-// the workspace) and bf16 transposes built in the scratch.
+// dX, dW and dR on tcgen05, from the gate errors dA (fp32, in the workspace) and bf16
+// operands built in the scratch: transposes (frames innermost, padded to a multiple of 8
+// with zeros) and a row-major copy of dA.  bf16 layers use one bf16 copy of each operand;
+// fp32 layers three K segments per operand (dA as [hi, hi, lo], X, H_prev and W as
+// [hi, lo, hi]), so that each product is hi*hi + hi*lo + lo*hi in one launch.
 lstm_status bwd_products_tc(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm,
                             const void* x_packed, const float* y_packed, const float* ga, float* dx_packed,
                             const lstm_layer_grads& g, void* scratch, cudaStream_t cs)
 {
     const int H = s.hidden_size, nd = s.num_directions, D = s.input_size, rows = (int)p.rows;
     const int G4 = nd * 4 * H;
+    const bool bf16 = s.dtype == LSTM_BF16;
+    const int ns = bf16 ? 1 : 3;
+    const int pa = bf16 ? 0 : 1, pb = bf16 ? 0 : 2;      // split patterns of the two operand sides
     const BwdScratch b = bwd_scratch(p, s);
+    const int64_t ldr = b.ldr, kt = (int64_t)ns * ldr;    // transposed operands: row pitch = K extent
+    const int kr = bf16 ? rows : (int)kt;                 // K of the frame-reduced products
     char* base = (char*)scratch;
     float* partial = (float*)base;
     void* dA16 = base + b.dA16;
@@ -154,33 +191,34 @@ lstm_status bwd_products_tc(const Plan& p, const lstm_layer_shape& s, const lstm
     char* HpT16 = base + b.HpT16;
     void* WT16 = base + b.WT16;
     lstm_status st;
-    // operands: dA as bf16 rows and columns, X^T, H_prev^T per direction, W^T
-    if ((st = transpose_to_bf16(p, ga, false, G4, 0, nullptr, rows, G4, dAT16, b.ldr, dA16, G4, cs)) != LSTM_OK)
+    // operands: dA as bf16 columns and rows, X^T, H_prev^T per direction, W^T
+    if ((st = transpose_to_bf16_split(p, ga, false, G4, 0, nullptr, rows, (int)ldr, G4, pa, dAT16, kt, ldr, dA16,
+                                      (int64_t)ns * G4, G4, cs)) != LSTM_OK)
         return st;
-    if ((st = transpose_to_bf16(p, x_packed, true, D, 0, nullptr, rows, D, XT16, b.ldr, nullptr, 0, cs)) != LSTM_OK)
+    if ((st = transpose_to_bf16_split(p, x_packed, bf16, D, 0, nullptr, rows, (int)ldr, D, pb, XT16, kt, ldr,
+                                      nullptr, 0, 0, cs)) != LSTM_OK)
         return st;
     for (int d = 0; d < nd; ++d)
-        if ((st = transpose_to_bf16(p, y_packed, false, (int64_t)nd * H, d * H, d == 0 ? p.d_prev_fwd : p.d_prev_rev,
-                                    rows, H, HpT16 + (size_t)d * H * b.ldr * 2, b.ldr, nullptr, 0, cs)) != LSTM_OK)
+        if ((st = transpose_to_bf16_split(p, y_packed, false, (int64_t)nd * H, d * H, d == 0 ? p.d_prev_fwd : p.d_prev_rev,
+                                          rows, (int)ldr, H, pb, HpT16 + (size_t)d * H * kt * 2, kt, ldr, nullptr, 0, 0,
+                                          cs)) != LSTM_OK)
             return st;
-    if ((st = transpose_to_bf16(p, prm.W, true, D, 0, nullptr, G4, D, WT16, G4, nullptr, 0, cs)) != LSTM_OK)
+    if ((st = transpose_to_bf16_split(p, prm.W, bf16, D, 0, nullptr, G4, G4, D, pb, WT16, (int64_t)ns * G4, G4,
+                                      nullptr, 0, 0, cs)) != LSTM_OK)
         return st;
     // dX[rows][D] = dA[rows][G4] W[G4][D]
-    if (dx_packed &&
-        (st = gemm_tc_bf16(p, K_GEMM_DX, dA16, G4, WT16, G4, rows, D, G4, dx_packed, D, nullptr, 1, nullptr, cs)) !=
-            LSTM_OK)
+    if (dx_packed && (st = gemm_tc_bf16(p, K_GEMM_DX, dA16, (int64_t)ns * G4, WT16, (int64_t)ns * G4, rows, D, ns * G4,
+                                        dx_packed, D, nullptr, 1, nullptr, cs)) != LSTM_OK)
         return st;
     // dW[G4][D] = dA^T X, K = frames
-    int sp = gemm_tc_splits(G4, D, rows, p.num_sms, kMaxTcSplits);
-    if ((st = gemm_tc_bf16(p, K_GEMM_DW, dAT16, b.ldr, XT16, b.ldr, G4, D, rows, g.dW, D, nullptr, sp, partial,
-                           cs)) != LSTM_OK)
+    int sp = gemm_tc_splits(G4, D, kr, p.num_sms, kMaxTcSplits);
+    if ((st = gemm_tc_bf16(p, K_GEMM_DW, dAT16, kt, XT16, kt, G4, D, kr, g.dW, D, nullptr, sp, partial, cs)) != LSTM_OK)
         return st;
     // dR_d[4H][H] = dA_d^T H_prev_d, K = frames
-    sp = gemm_tc_splits(4 * H, H, rows, p.num_sms, kMaxTcSplits);
+    sp = gemm_tc_splits(4 * H, H, kr, p.num_sms, kMaxTcSplits);
     for (int d = 0; d < nd; ++d)
-        if ((st = gemm_tc_bf16(p, K_GEMM_DR, dAT16 + (size_t)d * 4 * H * b.ldr * 2, b.ldr,
-                               HpT16 + (size_t)d * H * b.ldr * 2, b.ldr, 4 * H, H, rows, g.dR + (size_t)d * 4 * H * H,
-                               H, nullptr, sp, partial, cs)) != LSTM_OK)
+        if ((st = gemm_tc_bf16(p, K_GEMM_DR, dAT16 + (size_t)d * 4 * H * kt * 2, kt, HpT16 + (size_t)d * H * kt * 2, kt,
+                               4 * H, H, kr, g.dR + (size_t)d * 4 * H * H, H, nullptr, sp, partial, cs)) != LSTM_OK)
             return st;
     return LSTM_OK;
 }
@@ -194,7 +232,7 @@ lstm_status bwd_products(const Plan& p, const lstm_layer_shape& s, const lstm_la
     const bool bf16 = s.dtype == LSTM_BF16;
     lstm_status st;
     const int nd4H = nd * 4 * H;
-    if (bf16 && p.gemm_engine == 0 && D % 8 == 0 && encode_ready())
+    if ((bf16 || f32_split_shape(s)) && p.gemm_engine == 0 && D % 8 == 0 && encode_ready())
         return bwd_products_tc(p, s, prm, x_packed, y_packed, ga, dx_packed, grads, scratch, cs);
     GemmDesc gw, gr, gx;
     bwd_gemm_shapes(p, s, &gw, &gr, &gx);
@@ -317,7 +355,7 @@ lstm_status lstm_fwd(const lstm_plan* plan, const lstm_layer_shape* shape,
     const bool cluster = rec_cluster_fwd_configure(p, H, nd, bf16, &rcc, &cl_layout);
     if (!cluster && (st = rec_configure(p, H, nd, bf16, false, p.forced_ctas, &rc)) != LSTM_OK) return st;
 
-    if ((st = input_projection(p, s, *params, x_packed, ga, cs)) != LSTM_OK) return st;
+    if ((st = input_projection(p, s, *params, x_packed, ga, (char*)workspace + L.xs_off, cs)) != LSTM_OK) return st;
 
     RecArgs a = base_args(p, s, *params, ga, cbuf);
     a.y = y_packed; a.y_lo = (__nv_bfloat16*)y_lo; a.h_n = h_n; a.c_n = c_n;
@@ -421,7 +459,7 @@ lstm_status lstm_fwd_stepwise(const lstm_plan* plan, const lstm_layer_shape* sha
     const Layout L = workspace_layout(p, s);
     float* ga = (float*)((char*)workspace + L.ga_off);
     float* cbuf = (float*)((char*)workspace + L.c_off);
-    if ((st = input_projection(p, s, *params, x_packed, ga, cs)) != LSTM_OK) return st;
+    if ((st = input_projection(p, s, *params, x_packed, ga, (char*)workspace + L.xs_off, cs)) != LSTM_OK) return st;
     StepArgs a = step_args(p, s, *params, ga, cbuf, scratch);
     a.y = y_packed; a.y_lo = (__nv_bfloat16*)y_lo; a.h_n = h_n; a.c_n = c_n;
     const int ndH = nd * H;
@@ -525,7 +563,7 @@ lstm_status lstm_debug_input_projection(const lstm_plan* plan, const lstm_layer_
     if ((st = check_params(params)) != LSTM_OK) return st;
     if (plan->p.rows == 0) return LSTM_OK;
     if (!x_packed || !out || !aligned16(x_packed) || !aligned16(out)) return LSTM_ERR_INVALID_ARG;
-    return input_projection(plan->p, *shape, *params, x_packed, out, (cudaStream_t)stream);
+    return input_projection(plan->p, *shape, *params, x_packed, out, nullptr, (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -22,51 +22,85 @@ __device__ __forceinline__ float load_f<__nv_bfloat16>(const __nv_bfloat16* p) {
 
 // dstT[c][r] = bf16(src[row(r)][col0 + c]) and, if dst_rm, dst_rm[r][c] = the same value,
 // for r < rows, c < cols; row(r) = map ? map[r] : r, and a negative map entry reads 0.
+// Rows in [rows, rows_pad) are written as zeros into dstT only (the padded tail of a K
+// range); dst_rm has rows rows.
+// Split patterns, for fp32 products on bf16 tensor cores as three products
+// concatenated along K: each value v becomes hi = bf16(v) and lo = bf16(v - hi),
+// written into three K segments (kseg_t apart in dstT rows, kseg_m apart in
+// dst_rm rows): pattern 1 = [hi, hi, lo], pattern 2 = [hi, lo, hi], so that
+// the product of a pattern-1 and a pattern-2 operand is hi*hi + hi*lo + lo*hi.
+// Pattern 0 writes hi only.
 template <typename Tin>
 __global__ void __launch_bounds__(256) transpose_bf16_kernel(const Tin* __restrict__ src, int64_t lds, int col0,
-                                                             const int32_t* __restrict__ map, int rows, int cols,
+                                                             const int32_t* __restrict__ map, int rows,
+                                                             int rows_pad, int cols, int pattern,
                                                              __nv_bfloat16* __restrict__ dstT, int64_t ldt,
-                                                             __nv_bfloat16* __restrict__ dst_rm, int64_t ldm)
+                                                             int64_t kseg_t, __nv_bfloat16* __restrict__ dst_rm,
+                                                             int64_t ldm, int64_t kseg_m)
 {
-    __shared__ __nv_bfloat16 tile[32][34];
+    __shared__ __nv_bfloat16 thi[32][34], tlo[32][34];
     const int r0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int nseg = pattern == 0 ? 1 : 3;
     for (int i = ty; i < 32; i += 8) {
         const int r = r0 + i, c = c0 + tx;
-        __nv_bfloat16 v = __float2bfloat16_rn(0.f);
+        float f = 0.f;
         if (r < rows && c < cols) {
             const int64_t sr = map ? (int64_t)__ldg(map + r) : (int64_t)r;
-            if (sr >= 0) v = __float2bfloat16_rn(load_f<Tin>(src + sr * lds + col0 + c));
-            if (dst_rm) dst_rm[(int64_t)r * ldm + c] = v;
+            if (sr >= 0) f = load_f<Tin>(src + sr * lds + col0 + c);
         }
-        tile[i][tx] = v;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(f);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(f - __bfloat162float(hi));
+        if (dst_rm && r < rows && c < cols)           // the row-major copy has no padded rows
+            for (int sg = 0; sg < nseg; ++sg) {
+                const bool use_lo = (pattern == 1 && sg == 2) || (pattern == 2 && sg == 1);
+                dst_rm[(int64_t)r * ldm + sg * kseg_m + c] = use_lo ? lo : hi;
+            }
+        thi[i][tx] = hi;
+        tlo[i][tx] = lo;
     }
     __syncthreads();
+    if (!dstT) return;
     for (int i = ty; i < 32; i += 8) {
         const int c = c0 + i, r = r0 + tx;
-        if (c < cols && r < rows) dstT[(int64_t)c * ldt + r] = tile[tx][i];
+        if (c < cols && r < rows_pad)
+            for (int sg = 0; sg < nseg; ++sg) {
+                const bool use_lo = (pattern == 1 && sg == 2) || (pattern == 2 && sg == 1);
+                dstT[(int64_t)c * ldt + sg * kseg_t + r] = use_lo ? tlo[tx][i] : thi[tx][i];
+            }
     }
 }
 
 }  // namespace
 
+lstm_status transpose_to_bf16_split(const Plan& p, const void* src, bool src_bf16, int64_t lds, int col0,
+                                    const int32_t* map, int rows, int rows_pad, int cols, int pattern, void* dstT,
+                                    int64_t ldt, int64_t kseg_t, void* dst_rm, int64_t ldm, int64_t kseg_m,
+                                    cudaStream_t s)
+{
+    rows_pad = rows_pad < rows ? rows : rows_pad;
+    if (rows_pad <= 0 || cols <= 0) return LSTM_OK;
+    const dim3 grid((rows_pad + 31) / 32, (cols + 31) / 32);
+    trace_begin(p, K_CONVERT, s);
+    if (src_bf16)
+        transpose_bf16_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            (const __nv_bfloat16*)src, lds, col0, map, rows, rows_pad, cols, pattern, (__nv_bfloat16*)dstT, ldt,
+            kseg_t, (__nv_bfloat16*)dst_rm, ldm, kseg_m);
+    else
+        transpose_bf16_kernel<float><<<grid, 256, 0, s>>>((const float*)src, lds, col0, map, rows, rows_pad, cols,
+                                                          pattern, (__nv_bfloat16*)dstT, ldt, kseg_t,
+                                                          (__nv_bfloat16*)dst_rm, ldm, kseg_m);
+    const cudaError_t e = cudaGetLastError();
+    trace_end(p, K_CONVERT, s, e == cudaSuccess ? 1 : 0);
+    return e == cudaSuccess ? LSTM_OK : LSTM_ERR_CUDA;
+}
+
 lstm_status transpose_to_bf16(const Plan& p, const void* src, bool src_bf16, int64_t lds, int col0,
                               const int32_t* map, int rows, int cols, void* dstT, int64_t ldt, void* dst_rm,
                               int64_t ldm, cudaStream_t s)
 {
-    if (rows <= 0 || cols <= 0) return LSTM_OK;
-    const dim3 grid((rows + 31) / 32, (cols + 31) / 32);
-    trace_begin(p, K_CONVERT, s);
-    if (src_bf16)
-        transpose_bf16_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-            (const __nv_bfloat16*)src, lds, col0, map, rows, cols, (__nv_bfloat16*)dstT, ldt,
-            (__nv_bfloat16*)dst_rm, ldm);
-    else
-        transpose_bf16_kernel<float><<<grid, 256, 0, s>>>((const float*)src, lds, col0, map, rows, cols,
-                                                          (__nv_bfloat16*)dstT, ldt, (__nv_bfloat16*)dst_rm, ldm);
-    const cudaError_t e = cudaGetLastError();
-    trace_end(p, K_CONVERT, s, e == cudaSuccess ? 1 : 0);
-    return e == cudaSuccess ? LSTM_OK : LSTM_ERR_CUDA;
+    return transpose_to_bf16_split(p, src, src_bf16, lds, col0, map, rows, rows, cols, 0, dstT, ldt, 0, dst_rm, ldm,
+                                   0, s);
 }
 
 }  // namespace lstm

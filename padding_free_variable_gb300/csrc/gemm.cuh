@@ -59,6 +59,15 @@ lstm_status transpose_to_bf16(const Plan& p, const void* src, bool src_bf16, int
 bool make_map_f32(CUtensorMap* map, const float* ptr, int64_t rows, int64_t cols, int64_t ld, int box_cols,
                   int box_rows);
 
+// The same with a padded row range (rows in [rows, rows_pad) written as 0)
+// and an fp32 split into bf16 hi/lo written as three K segments: pattern 1 =
+// [hi, hi, lo], pattern 2 = [hi, lo, hi] (kseg_t / kseg_m elements apart in the
+// transposed / row-major output), pattern 0 = hi only.  dstT may be null.
+lstm_status transpose_to_bf16_split(const Plan& p, const void* src, bool src_bf16, int64_t lds, int col0,
+                                    const int32_t* map, int rows, int rows_pad, int cols, int pattern, void* dstT,
+                                    int64_t ldt, int64_t kseg_t, void* dst_rm, int64_t ldm, int64_t kseg_m,
+                                    cudaStream_t s);
+
 // C = sum over splits (in split order) of partial, + bias.
 cudaError_t splitk_reduce(const float* partial, int splits, int M, int N, float* C, int64_t ldc,
                           const float* bias, int num_sms, cudaStream_t s);

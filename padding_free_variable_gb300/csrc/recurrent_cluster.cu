@@ -213,11 +213,37 @@ __device__ __forceinline__ void issue_chain32(uint32_t d, uint32_t a_hi, uint32_
     }
 }
 
+// The same with a compile-time k-step count, fully unrolled (the issuing
+// thread's own instruction stream bounds the issue rate of small MMAs).
+template <int NCH, int NKS, int KPB, bool SPLIT>
+__device__ __forceinline__ void issue_chain_fixed(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t bh, uint64_t bl,
+                                                  uint32_t bstep, int ch, uint32_t idesc)
+{
+#pragma unroll
+    for (int jj = 0; jj < NKS / NCH; ++jj) {
+        const int i = ch + jj * NCH;
+        const uint64_t bo = (uint64_t)((uint32_t)(i / KPB) * bstep + (uint32_t)(i % KPB) * 2u);
+        const uint32_t ac = (uint32_t)(i * 8);
+        const uint32_t acc = jj == 0 ? 0u : 1u;
+        if (SPLIT) {
+            tc::mma_bf16_ts(d, a_lo + ac, bh + bo, idesc, acc);
+            tc::mma_bf16_ts(d, a_hi + ac, bl + bo, idesc, 1u);
+            tc::mma_bf16_ts(d, a_hi + ac, bh + bo, idesc, 1u);
+        } else {
+            tc::mma_bf16_ts(d, a_hi + ac, bh + bo, idesc, acc);
+        }
+    }
+}
+
 template <bool SPLIT>
 __device__ __forceinline__ void issue_chains32(int nch, uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t bh,
                                                uint64_t bl, uint32_t bstep, int nks, int ch, uint32_t idesc)
 {
-    if (nch == 4) issue_chain32<4, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, nks, ch, idesc);
+    if (nch == 4 && nks == 16) issue_chain_fixed<4, 16, 2, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, ch, idesc);
+    else if (nch == 4 && nks == 32) issue_chain_fixed<4, 32, 2, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, ch, idesc);
+    else if (nch == 4 && nks == 8) issue_chain_fixed<4, 8, 2, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, ch, idesc);
+    else if (nch == 2 && nks == 16) issue_chain_fixed<2, 16, 2, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, ch, idesc);
+    else if (nch == 4) issue_chain32<4, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, nks, ch, idesc);
     else if (nch == 2) issue_chain32<2, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, nks, ch, idesc);
     else issue_chain32<1, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, nks, ch, idesc);
 }
@@ -1065,8 +1091,11 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
                 const int m = warp / nch, ch = warp - m * nch;
                 const uint32_t idesc = tc::idesc_bf16_f32(kCM, NBs);
                 const uint64_t dbh = tc::sdesc_sw128(tc::smem_u32(Bhi)), dbl = tc::sdesc_sw128(tc::smem_u32(Blo));
-                issue_chains<SPLIT>(nch, tmem + (uint32_t)(warp * NBM), a_hi + (uint32_t)(64 * m),
-                                    a_lo + (uint32_t)(64 * m), dbh, dbl, bstep, 8, ch, idesc);
+                const uint32_t dm = tmem + (uint32_t)(warp * NBM), ahm = a_hi + (uint32_t)(64 * m),
+                               alm = a_lo + (uint32_t)(64 * m);
+                if (nch == 4) issue_chain_fixed<4, 8, 4, SPLIT>(dm, ahm, alm, dbh, dbl, bstep, ch, idesc);
+                else if (nch == 2) issue_chain_fixed<2, 8, 4, SPLIT>(dm, ahm, alm, dbh, dbl, bstep, ch, idesc);
+                else issue_chain_fixed<1, 8, 4, SPLIT>(dm, ahm, alm, dbh, dbl, bstep, ch, idesc);
                 if (!(s == 0 && dir == 0 && rank == a.debug_skip_cta)) tc::mma_commit(mma_bar);   // test hook
             }
             if (warp < MT * nch) __syncwarp();
