@@ -194,6 +194,14 @@ def roofline_of(kind, ms_per_step, calls_per_step, spec, rows, T, D0, peaks, rec
     sec = ms_per_step / 1e3
     clk = float(peaks.get("sm_max_mhz", 2070.0))
     per = max(1.0, calls_per_step)
+    if kind in ("rec_fwd", "rec_bwd") and rec_cfg and rec_cfg.get("kernel") == "step_launches":
+        # per-step tcgen05 products over the whole GPU (bf16 layers wider than one cluster)
+        cpeak = float(peaks["bf16_tflops_sustained"])
+        ach = fl / sec / 1e12 if sec > 0 else 0.0
+        return {"kernel": kind, "bound": "tensor", "achieved": round(ach, 3), "peak": round(cpeak, 1),
+                "unit": "TFLOP/s", "frac": round(ach / cpeak, 4), "recurrent_kernel": rec_cfg,
+                "peak_source": "MEASURED_PEAKS.json sustained bf16",
+                "per_launch": {"flops": fl / per, "ms": ms_per_step / per}}
     if kind in ("rec_fwd", "rec_bwd") and rec_cfg and rec_cfg.get("ctas_per_direction"):
         ctas = rec_cfg["ctas_per_direction"]
         sb = rec_smem_bytes(kind, spec, rows, T, ctas)

@@ -323,9 +323,10 @@ lstm_status lstm_plan_read_timing(lstm_plan* plan, double* ms, int64_t* calls);
 /* Per-step-launch path (a comparator, not the fast path).  The design the
  * RETURNN paper describes for its GPU LSTM (Sec. 4.2): after the one
  * non-recurrent product, every time step is one product launch per direction
- * (R h_{t-1} over the step's active rows, CUDA cores) and one cell launch for
- * both directions; the backward pass mirrors it (one cell launch and one
- * R^T da product per direction per step), then the same db/dpeep sums and
+ * (R h_{t-1} over the step's active rows: tcgen05 for bf16 layers, CUDA cores
+ * for fp32) and one cell launch for both directions; the backward pass
+ * mirrors it (one cell launch and one R^T da product per direction per
+ * step), then the same db/dpeep sums and
  * dX/dW/dR products as lstm_bwd.  Same arguments, layouts, results (within
  * the fp32 / bf16 tolerances) and errors as lstm_fwd / lstm_bwd, plus
  * `scratch` (device, 16-byte aligned, lstm_stepwise_scratch_bytes, owned by
@@ -347,7 +348,9 @@ int64_t lstm_plan_launch_count(const lstm_plan* plan);
 /* Launch configuration of the last recurrent kernel run through this plan:
  * `pass` 0 = forward (lstm_fwd), 1 = backward (lstm_bwd / lstm_bwd_noalloc).
  * kind: 0 none yet, 1 grid-wide persistent kernel with flag barriers,
- *       2 one thread-block cluster per direction;
+ *       2 one thread-block cluster per direction, 3 per-step launches of a
+ *       tcgen05 product over the whole GPU and a cell kernel (bf16 layers
+ *       whose R does not fit one cluster, H > 512);
  * ctas_per_direction: CTAs that hold one direction's recurrent weights;
  * product: 0 CUDA cores, 1 warp-level mma.sync, 2 tcgen05 with TMEM accumulators.
  * Any output pointer may be NULL.  LSTM_ERR_INVALID_ARG for a NULL plan or a

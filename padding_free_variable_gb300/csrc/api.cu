@@ -37,8 +37,12 @@ lstm_status check_shape(const lstm_layer_shape* s)
 // concatenated along K): the K extents (D, ndir*4H, frames) must be TMA-addressable.
 bool f32_split_shape(const lstm_layer_shape& s) { return s.dtype == LSTM_F32 && s.input_size % 8 == 0; }
 
+// bf16 layers wider than one thread-block cluster can hold (one direction's R of more than 16
+// CTAs x 32 units): the recurrence runs as per-step tcgen05 products over the whole GPU.
+bool wide_bf16(const lstm_layer_shape& s) { return s.dtype == LSTM_BF16 && s.hidden_size > 512; }
+
 struct Layout {
-    size_t ga_off, c_off, xs_off, ws_off, total;   // workspace
+    size_t ga_off, c_off, xs_off, ws_off, rh_off, hb_off, total;   // workspace
 };
 
 // gates/errors, cell states, then (fp32 split shapes) the input projection's split operands:
@@ -52,7 +56,11 @@ Layout workspace_layout(const Plan& p, const lstm_layer_shape& s)
     l.c_off = align256(rows * nd * 4 * H * sizeof(float));
     l.xs_off = l.c_off + align256(rows * nd * H * sizeof(float));
     l.ws_off = l.xs_off + (f32_split_shape(s) ? align256(rows * 3 * D * 2) : 0);
-    l.total = l.ws_off + (f32_split_shape(s) ? align256(nd * 4 * H * 3 * D * 2) : 0);
+    l.rh_off = l.ws_off + (f32_split_shape(s) ? align256(nd * 4 * H * 3 * D * 2) : 0);
+    // wide bf16 layers: a step's R h_{t-1} [ndir][B][4H] fp32 and bf16 h [ndir][B][H]
+    const size_t B = (size_t)p.B;
+    l.hb_off = l.rh_off + (wide_bf16(s) ? align256(nd * B * 4 * H * 4) : 0);
+    l.total = l.hb_off + (wide_bf16(s) ? align256(nd * B * H * 2) : 0);
     return l;
 }
 
@@ -110,9 +118,12 @@ BwdScratch bwd_scratch(const Plan& p, const lstm_layer_shape& s)
     return b;
 }
 
+struct StepScratch;
+size_t step_scratch_total(const Plan& p, const lstm_layer_shape& s);
+
 size_t scratch_floats(const Plan& p, const lstm_layer_shape& s)
 {
-    return bwd_scratch(p, s).total / sizeof(float);
+    return (wide_bf16(s) ? step_scratch_total(p, s) : bwd_scratch(p, s).total) / sizeof(float);
 }
 
 RecArgs base_args(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm, float* ga,
@@ -264,8 +275,10 @@ lstm_status bwd_products(const Plan& p, const lstm_layer_shape& s, const lstm_la
 // region also holds the db / dpeep partials), then R h_{t-1} of a step
 // [ndir][B][4H], R^T da of a step [ndir][B][H] and the cell-state error carry
 // [ndir][B][H].
+// bf16 layers, the per-step products on tcgen05: bf16 h of a step's rows [ndir][B][H], bf16
+// gate errors [ndir][B][4H] and R^T [ndir][H][4H] bf16.
 struct StepScratch {
-    size_t rh = 0, dh = 0, dcc = 0, total = 0;
+    size_t rh = 0, dh = 0, dcc = 0, hb = 0, dab = 0, rt = 0, total = 0;
 };
 
 StepScratch step_scratch(const Plan& p, const lstm_layer_shape& s)
@@ -276,23 +289,141 @@ StepScratch step_scratch(const Plan& p, const lstm_layer_shape& s)
     q.rh = off; off += align256(nd * B * 4 * H * sizeof(float));
     q.dh = off; off += align256(nd * B * H * sizeof(float));
     q.dcc = off; off += align256(nd * B * H * sizeof(float));
+    if (s.dtype == LSTM_BF16) {
+        q.hb = off; off += align256(nd * B * H * 2);
+        q.dab = off; off += align256(nd * B * 4 * H * 2);
+        q.rt = off; off += align256(nd * H * 4 * H * 2);
+    }
     q.total = off;
     return q;
 }
 
-StepArgs step_args(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm, float* ga,
-                   float* cbuf, void* scratch)
+size_t step_scratch_total(const Plan& p, const lstm_layer_shape& s) { return step_scratch(p, s).total; }
+
+bool step_tc(const Plan& p, const lstm_layer_shape& s);
+
+// Whether lstm_fwd / lstm_bwd run this layer's recurrence as per-step tcgen05 products.
+bool wide_step_path(const Plan& p, const lstm_layer_shape& s)
 {
-    const StepScratch q = step_scratch(p, s);
+    return wide_bf16(s) && !p.padded && p.forced_ctas == 0 && step_tc(p, s);
+}
+
+StepArgs step_args(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm, float* ga,
+                   float* cbuf)
+{
     StepArgs a;
     memset(&a, 0, sizeof(a));
     a.T = p.T; a.B = p.B; a.H = s.hidden_size; a.ndir = s.num_directions;
     a.bs = p.d_bs; a.off = p.d_off; a.slot_len = p.d_len; a.perm = p.d_perm;
     a.ga = ga; a.cbuf = cbuf; a.peep = prm.peep;
-    a.rh = (const float*)((char*)scratch + q.rh);
-    a.dh_rec = (const float*)((char*)scratch + q.dh);
-    a.dcc = (float*)((char*)scratch + q.dcc);
     return a;
+}
+
+// Per-step tensor-core products for this layer (bf16 operands, tcgen05 available).
+bool step_tc(const Plan& p, const lstm_layer_shape& s)
+{
+    return s.dtype == LSTM_BF16 && p.gemm_engine == 0 && encode_ready();
+}
+
+// The forward recurrence as per-step launches: per direction one product R h_{t-1} over the
+// step's rows with a previous state (tcgen05 from the bf16 copy hb16 when given, else CUDA
+// cores from y), then one cell launch for both directions.
+lstm_status stepwise_fwd_core(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm, float* y,
+                              void* y_lo, float* h_n, float* c_n, float* ga, float* cbuf, float* rh,
+                              __nv_bfloat16* hb16, cudaStream_t cs)
+{
+    const int H = s.hidden_size, nd = s.num_directions, ndH = nd * H;
+    const bool bf16 = s.dtype == LSTM_BF16;
+    const size_t esz = bf16 ? 2 : 4;
+    StepArgs a = step_args(p, s, prm, ga, cbuf);
+    a.rh = rh; a.hb16 = hb16;
+    a.y = y; a.y_lo = (__nv_bfloat16*)y_lo; a.h_n = h_n; a.c_n = c_n;
+    lstm_status st = LSTM_OK;
+    trace_begin(p, K_REC_FWD, cs);
+    int launches = 0;
+    for (int step = 0; step < p.T && st == LSTM_OK; ++step) {
+        for (int d = 0; d < nd && st == LSTM_OK; ++d) {
+            // R h_{t-1} of the step's rows that have a previous state (the first M rows)
+            const int t = d == 0 ? step : p.T - 1 - step;
+            const int M = d == 0 ? (t >= 1 ? p.h_bs[t] : 0) : (t + 1 < p.T ? p.h_bs[t + 1] : 0);
+            if (M == 0) continue;
+            const char* Rd = (const char*)prm.R + (size_t)d * 4 * H * H * esz;
+            float* C = rh + (size_t)d * p.B * 4 * H;
+            if (hb16) {
+                st = gemm_tc_bf16(p, -1, hb16 + (size_t)d * p.B * H, H, Rd, H, M, 4 * H, H, C, 4 * H, nullptr, 1,
+                                  nullptr, cs);
+            } else {
+                const int prow0 = d == 0 ? p.h_off[t - 1] : p.h_off[t + 1];
+                GemmDesc g;
+                g.M = M; g.N = 4 * H; g.K = H;
+                g.A = y + (size_t)prow0 * ndH + (size_t)d * H; g.sam = ndH; g.sak = 1;
+                g.B = Rd; g.sbk = 1; g.sbn = H; g.b_bf16 = bf16;
+                g.C = C; g.ldc = 4 * H;
+                g.round_bf16 = bf16; g.k_splits = 1;
+                st = gemm_simt_run(g, p.num_sms, cs);
+                ++launches;
+            }
+        }
+        if (st == LSTM_OK) st = step_cell_launch(a, step, false, cs);
+        ++launches;
+    }
+    trace_end(p, K_REC_FWD, cs, launches);
+    return st;
+}
+
+// The BPTT recurrence as per-step launches (one cell launch, then per direction one product
+// R^T da of the step's rows, tcgen05 when dab16 / rt16 are given), the db / dpeep sums, and
+// the dX / dW / dR products.
+lstm_status stepwise_bwd_core(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm,
+                              const void* x_packed, const float* y_packed, float* ga, float* cbuf,
+                              const float* dy_packed, float* dx_packed, const lstm_layer_grads& grads, void* scratch,
+                              float* dh_rec, float* dcc, __nv_bfloat16* dab16, __nv_bfloat16* rt16, cudaStream_t cs)
+{
+    const int H = s.hidden_size, nd = s.num_directions;
+    const bool bf16 = s.dtype == LSTM_BF16;
+    const int nd4H = nd * 4 * H;
+    const size_t esz = bf16 ? 2 : 4;
+    StepArgs a = step_args(p, s, prm, ga, cbuf);
+    a.dy = dy_packed; a.dh_rec = dh_rec; a.dcc = dcc; a.dab16 = dab16;
+    lstm_status st = LSTM_OK;
+    if (rt16)   // R_d^T [H][4H] bf16: the B operand (K-major) of the per-step R^T da products
+        for (int d = 0; d < nd && st == LSTM_OK; ++d)
+            st = transpose_to_bf16_split(p, (const char*)prm.R + (size_t)d * 4 * H * H * esz, bf16, H, 0, nullptr,
+                                         4 * H, 4 * H, H, 0, rt16 + (size_t)d * H * 4 * H, 4 * H, 0, nullptr, 0, 0,
+                                         cs);
+    if (st != LSTM_OK) return st;
+    trace_begin(p, K_REC_BWD, cs);     // (no traced call may nest inside this bracket)
+    int launches = 0;
+    for (int step = 0; step < p.T && st == LSTM_OK; ++step) {
+        st = step_cell_launch(a, step, true, cs);
+        ++launches;
+        if (step + 1 == p.T) break;
+        for (int d = 0; d < nd && st == LSTM_OK; ++d) {
+            // R^T da of every row of the step, for the step after it in recurrence order
+            const int t = d == 0 ? p.T - 1 - step : step;
+            float* C = dh_rec + (size_t)d * p.B * H;
+            if (rt16) {
+                st = gemm_tc_bf16(p, -1, dab16 + (size_t)d * p.B * 4 * H, 4 * H, rt16 + (size_t)d * H * 4 * H, 4 * H,
+                                  p.h_bs[t], H, 4 * H, C, H, nullptr, 1, nullptr, cs);
+            } else {
+                GemmDesc g;
+                g.M = p.h_bs[t]; g.N = H; g.K = 4 * H;
+                g.A = ga + (size_t)p.h_off[t] * nd4H + (size_t)d * 4 * H; g.sam = nd4H; g.sak = 1;
+                g.B = (const char*)prm.R + (size_t)d * 4 * H * H * esz; g.sbk = H; g.sbn = 1; g.b_bf16 = bf16;
+                g.C = C; g.ldc = H;
+                g.round_bf16 = bf16; g.k_splits = 1;
+                st = gemm_simt_run(g, p.num_sms, cs);
+                ++launches;
+            }
+        }
+    }
+    if (st == LSTM_OK) {
+        st = param_sums_launch(p, ga, cbuf, H, nd, grads.db, grads.dpeep, (float*)scratch, cs);
+        launches += 2;
+    }
+    trace_end(p, K_REC_BWD, cs, launches);
+    if (st != LSTM_OK) return st;
+    return bwd_products(p, s, prm, x_packed, y_packed, ga, dx_packed, grads, scratch, cs);
 }
 
 lstm_status check_params(const lstm_layer_params* prm)
@@ -349,6 +480,14 @@ lstm_status lstm_fwd(const lstm_plan* plan, const lstm_layer_shape* shape,
     float* ga = (float*)((char*)workspace + L.ga_off);
     float* cbuf = (float*)((char*)workspace + L.c_off);
 
+    if (wide_step_path(p, s)) {
+        if ((st = input_projection(p, s, *params, x_packed, ga, (char*)workspace + L.xs_off, cs)) != LSTM_OK)
+            return st;
+        p.last_rec_kind[0] = 3; p.last_rec_ctas[0] = 0; p.last_rec_mma[0] = 2;
+        return stepwise_fwd_core(p, s, *params, y_packed, y_lo, h_n, c_n, ga, cbuf,
+                                 (float*)((char*)workspace + L.rh_off), (__nv_bfloat16*)((char*)workspace + L.hb_off),
+                                 cs);
+    }
     RecConfig rc, rcc;
     RecArgs cl_layout;
     memset(&cl_layout, 0, sizeof(cl_layout));
@@ -404,6 +543,14 @@ lstm_status lstm_bwd(const lstm_plan* plan, const lstm_layer_shape* shape,
     float* ga = (float*)((char*)workspace + L.ga_off);
     float* cbuf = (float*)((char*)workspace + L.c_off);
 
+    if (wide_step_path(p, s)) {
+        const StepScratch q = step_scratch(p, s);
+        char* sc = (char*)scratch;
+        p.last_rec_kind[1] = 3; p.last_rec_ctas[1] = 0; p.last_rec_mma[1] = 2;
+        return stepwise_bwd_core(p, s, *params, x_packed, y_packed, ga, cbuf, dy_packed, dx_packed, *grads, scratch,
+                                 (float*)(sc + q.dh), (float*)(sc + q.dcc), (__nv_bfloat16*)(sc + q.dab),
+                                 (__nv_bfloat16*)(sc + q.rt), cs);
+    }
     RecConfig rc, rcc;
     RecArgs cl_layout;
     memset(&cl_layout, 0, sizeof(cl_layout));
@@ -444,7 +591,6 @@ lstm_status lstm_fwd_stepwise(const lstm_plan* plan, const lstm_layer_shape* sha
     const lstm_layer_shape& s = *shape;
     if (p.padded) return LSTM_ERR_UNSUPPORTED;
     const int H = s.hidden_size, nd = s.num_directions;
-    const bool bf16 = s.dtype == LSTM_BF16;
     cudaStream_t cs = (cudaStream_t)stream;
     if ((h_n && !aligned16(h_n)) || (c_n && !aligned16(c_n))) return LSTM_ERR_INVALID_ARG;
     if (p.rows == 0) {
@@ -460,33 +606,10 @@ lstm_status lstm_fwd_stepwise(const lstm_plan* plan, const lstm_layer_shape* sha
     float* ga = (float*)((char*)workspace + L.ga_off);
     float* cbuf = (float*)((char*)workspace + L.c_off);
     if ((st = input_projection(p, s, *params, x_packed, ga, (char*)workspace + L.xs_off, cs)) != LSTM_OK) return st;
-    StepArgs a = step_args(p, s, *params, ga, cbuf, scratch);
-    a.y = y_packed; a.y_lo = (__nv_bfloat16*)y_lo; a.h_n = h_n; a.c_n = c_n;
-    const int ndH = nd * H;
-    const size_t esz = bf16 ? 2 : 4;
-    trace_begin(p, K_REC_FWD, cs);
-    int launches = 0;
-    for (int step = 0; step < p.T && st == LSTM_OK; ++step) {
-        for (int d = 0; d < nd && st == LSTM_OK; ++d) {
-            // R h_{t-1} of the step's rows that have a previous state (the first M rows)
-            const int t = d == 0 ? step : p.T - 1 - step;
-            const int M = d == 0 ? (t >= 1 ? p.h_bs[t] : 0) : (t + 1 < p.T ? p.h_bs[t + 1] : 0);
-            if (M == 0) continue;
-            const int prow0 = d == 0 ? p.h_off[t - 1] : p.h_off[t + 1];
-            GemmDesc g;
-            g.M = M; g.N = 4 * H; g.K = H;
-            g.A = y_packed + (size_t)prow0 * ndH + (size_t)d * H; g.sam = ndH; g.sak = 1;
-            g.B = (const char*)params->R + (size_t)d * 4 * H * H * esz; g.sbk = 1; g.sbn = H; g.b_bf16 = bf16;
-            g.C = const_cast<float*>(a.rh) + (size_t)d * p.B * 4 * H; g.ldc = 4 * H;
-            g.round_bf16 = bf16; g.k_splits = 1;
-            st = gemm_simt_run(g, p.num_sms, cs);
-            ++launches;
-        }
-        if (st == LSTM_OK) st = step_cell_launch(a, step, false, cs);
-        ++launches;
-    }
-    trace_end(p, K_REC_FWD, cs, launches);
-    return st;
+    const StepScratch q = step_scratch(p, s);
+    char* sc = (char*)scratch;
+    return stepwise_fwd_core(p, s, *params, y_packed, y_lo, h_n, c_n, ga, cbuf, (float*)(sc + q.rh),
+                             step_tc(p, s) ? (__nv_bfloat16*)(sc + q.hb) : nullptr, cs);
 }
 
 lstm_status lstm_bwd_stepwise(const lstm_plan* plan, const lstm_layer_shape* shape,
@@ -505,7 +628,6 @@ lstm_status lstm_bwd_stepwise(const lstm_plan* plan, const lstm_layer_shape* sha
     const lstm_layer_shape& s = *shape;
     if (p.padded) return LSTM_ERR_UNSUPPORTED;
     const int H = s.hidden_size, nd = s.num_directions, D = s.input_size;
-    const bool bf16 = s.dtype == LSTM_BF16;
     cudaStream_t cs = (cudaStream_t)stream;
     if (p.rows == 0) {
         LSTM_CUDA_TRY(cudaMemsetAsync(grads->dW, 0, sizeof(float) * nd * 4 * H * D, cs));
@@ -521,36 +643,12 @@ lstm_status lstm_bwd_stepwise(const lstm_plan* plan, const lstm_layer_shape* sha
     const Layout L = workspace_layout(p, s);
     float* ga = (float*)((char*)workspace + L.ga_off);
     float* cbuf = (float*)((char*)workspace + L.c_off);
-    StepArgs a = step_args(p, s, *params, ga, cbuf, scratch);
-    a.dy = dy_packed;
-    const int nd4H = nd * 4 * H;
-    const size_t esz = bf16 ? 2 : 4;
-    trace_begin(p, K_REC_BWD, cs);
-    int launches = 0;
-    for (int step = 0; step < p.T && st == LSTM_OK; ++step) {
-        st = step_cell_launch(a, step, true, cs);
-        ++launches;
-        if (step + 1 == p.T) break;
-        for (int d = 0; d < nd && st == LSTM_OK; ++d) {
-            // R^T da of every row of the step, for the step after it in recurrence order
-            const int t = d == 0 ? p.T - 1 - step : step;
-            GemmDesc g;
-            g.M = p.h_bs[t]; g.N = H; g.K = 4 * H;
-            g.A = ga + (size_t)p.h_off[t] * nd4H + (size_t)d * 4 * H; g.sam = nd4H; g.sak = 1;
-            g.B = (const char*)params->R + (size_t)d * 4 * H * H * esz; g.sbk = H; g.sbn = 1; g.b_bf16 = bf16;
-            g.C = const_cast<float*>(a.dh_rec) + (size_t)d * p.B * H; g.ldc = H;
-            g.round_bf16 = bf16; g.k_splits = 1;
-            st = gemm_simt_run(g, p.num_sms, cs);
-            ++launches;
-        }
-    }
-    if (st == LSTM_OK) {
-        st = param_sums_launch(p, ga, cbuf, H, nd, grads->db, grads->dpeep, (float*)scratch, cs);
-        launches += 2;
-    }
-    trace_end(p, K_REC_BWD, cs, launches);
-    if (st != LSTM_OK) return st;
-    return bwd_products(p, s, *params, x_packed, y_packed, ga, dx_packed, *grads, scratch, cs);
+    const StepScratch q = step_scratch(p, s);
+    char* sc = (char*)scratch;
+    const bool tc = step_tc(p, s);
+    return stepwise_bwd_core(p, s, *params, x_packed, y_packed, ga, cbuf, dy_packed, dx_packed, *grads, scratch,
+                             (float*)(sc + q.dh), (float*)(sc + q.dcc), tc ? (__nv_bfloat16*)(sc + q.dab) : nullptr,
+                             tc ? (__nv_bfloat16*)(sc + q.rt) : nullptr, cs);
 }
 
 lstm_status lstm_debug_input_projection(const lstm_plan* plan, const lstm_layer_shape* shape,

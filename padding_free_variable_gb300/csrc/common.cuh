@@ -72,7 +72,9 @@ struct Plan {
     mutable int32_t last_rec_mma[2] = {0, 0};    // 0 CUDA cores, 1 mma.sync, 2 tcgen05
 };
 
-// Bracket a launch sequence of `kind`; `kernels` = launches it issued.
+// Bracket a launch sequence of `kind`; `kernels` = launches it issued.  A
+// negative kind counts the launches without timing them (a sequence inside
+// another kind's bracket).
 void trace_begin(const Plan& p, int kind, cudaStream_t s);
 void trace_end(const Plan& p, int kind, cudaStream_t s, int kernels);
 

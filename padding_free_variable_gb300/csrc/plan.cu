@@ -60,7 +60,7 @@ lstm_status launch_pack(const Plan& p, const void* src, int width, int elem_byte
 void trace_begin(const Plan& p, int kind, cudaStream_t s)
 {
     Tracer* t = p.tracer;
-    if (!t || !t->enabled) return;
+    if (!t || !t->enabled || kind < 0) return;     // kind < 0: counted, not timed (inside another kind)
     if (t->npending == t->cap) {
         int ncap = t->cap ? 2 * t->cap : 64;
         Tracer::Rec* n = (Tracer::Rec*)realloc(t->pending, sizeof(Tracer::Rec) * ncap);
@@ -81,7 +81,7 @@ void trace_end(const Plan& p, int kind, cudaStream_t s, int kernels)
     Tracer* t = p.tracer;
     if (!t) return;
     t->launches += kernels;
-    if (!t->enabled || t->npending == 0) return;
+    if (!t->enabled || t->npending == 0 || kind < 0) return;
     Tracer::Rec& r = t->pending[t->npending - 1];
     if (r.kind == kind) cudaEventRecord(r.b, s);
 }
@@ -94,6 +94,8 @@ static void tracer_flush(Tracer* t)
         if (cudaEventSynchronize(r.b) == cudaSuccess && cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
             t->ms[r.kind] += ms;
             t->calls[r.kind] += 1;
+        } else {
+            cudaGetLastError();   // an unmatched bracket: drop the record, leave no error behind
         }
         cudaEventDestroy(r.a);
         cudaEventDestroy(r.b);

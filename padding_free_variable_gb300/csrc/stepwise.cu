@@ -1,12 +1,14 @@
-// stepwise.cu -- the per-step-launch recurrence (comparator path).
+// stepwise.cu -- cell kernels of the per-step-launch recurrence.
 //
 // The design the pages describe for their own GPU LSTM ("RETURNN", Sec. 4.2:
 // one matrix product for the non-recurrent part, then per time step a product
-// with the recurrent weights and a small kernel for the gating): here each
-// step of each direction is one SIMT product launch (R·h_{t-1} over the
-// step's active rows) and each step one cell launch for both directions.
-// It computes the same cell as the persistent kernels and exists to measure
-// what the persistent, on-chip design saves.
+// with the recurrent weights and a small kernel for the gating): each step of
+// each direction is one product launch (R·h_{t-1} over the step's active
+// rows) and each step one cell launch for both directions.  With CUDA-core
+// products it is the comparator that measures what the persistent, on-chip
+// design saves; with tcgen05 products it is the path for bf16 layers whose R
+// does not fit one thread-block cluster (each step's product is then a GEMM
+// large enough to spread over the whole GPU).
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -57,6 +59,7 @@ __global__ void step_cell_fwd_kernel(StepArgs a, int s)
     a.cbuf[yo] = c;
     a.y[yo] = h;
     if (a.y_lo) a.y_lo[yo] = __float2bfloat16_rn(h);
+    if (a.hb16) a.hb16[((size_t)dir * a.B + j) * H + u] = __float2bfloat16_rn(h);
     const int len = a.slot_len[j];
     if (a.h_n && ((dir == 0 && t == len - 1) || (dir == 1 && t == 0))) {
         const size_t o = ((size_t)dir * a.B + a.perm[j]) * H + u;
@@ -99,6 +102,11 @@ __global__ void step_cell_bwd_kernel(StepArgs a, int s)
     const float daz = dc * ig * (1.f - zg * zg);
     gw[0] = dai; gw[H] = daf; gw[2 * H] = daz; gw[3 * H] = dao;
     a.dcc[so] = dc * fg + dai * pp[0] + daf * pp[H];
+    if (a.dab16) {
+        __nv_bfloat16* db = a.dab16 + ((size_t)dir * a.B + j) * 4 * H + u;
+        db[0] = __float2bfloat16_rn(dai); db[H] = __float2bfloat16_rn(daf);
+        db[2 * H] = __float2bfloat16_rn(daz); db[3 * H] = __float2bfloat16_rn(dao);
+    }
 }
 
 lstm_status step_cell_launch(const StepArgs& a, int s, bool backward, cudaStream_t st)

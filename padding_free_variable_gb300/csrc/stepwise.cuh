@@ -24,6 +24,8 @@ struct StepArgs {
     const float* dy;          // backward: [rows][ndir*H]
     const float* dh_rec;      // backward: [ndir][B][H] R^T da of the step after (recurrence order)
     float* dcc;               // backward: [ndir][B][H] cell-state error carry
+    __nv_bfloat16* hb16;      // optional, forward: [ndir][B][H] bf16 h of the step's rows (next product's A)
+    __nv_bfloat16* dab16;     // optional, backward: [ndir][B][4H] bf16 gate errors of the step's rows
 };
 
 // Cell of step s (forward, or BPTT in backward order) for both directions.

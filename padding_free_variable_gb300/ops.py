@@ -80,7 +80,7 @@ class Plan:
         check(_lib.load().lstm_plan_recurrent_config(self.handle, int(bool(backward)), ctypes.byref(k),
                                                      ctypes.byref(g), ctypes.byref(m)),
               "lstm_plan_recurrent_config")
-        return {"kernel": ("none", "grid", "cluster")[k.value], "ctas_per_direction": g.value,
+        return {"kernel": ("none", "grid", "cluster", "step_launches")[k.value], "ctas_per_direction": g.value,
                 "product": ("cuda_cores", "mma_sync", "tcgen05")[m.value]}
 
     def trace_steps(self, buffer, steps: int):

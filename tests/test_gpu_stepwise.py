@@ -43,3 +43,17 @@ def test_stepwise_full_workload(wid):
     w = synthetic.workload(wid)
     gpu = run_gpu(w, stepwise=True)
     compare_all(gpu, run_oracle(w), TOL_F32, label=f"stepwise workload {wid}")
+
+
+def test_wide_bf16_layers_run_per_step_tensor_core_products():
+    """bf16 layers whose R does not fit one cluster (H > 512) run their recurrence through
+    lstm_fwd / lstm_bwd as per-step tcgen05 products plus cell launches."""
+    from gpu_harness import TOL_BF16_EMULATED
+    w = synthetic.custom(2, 2, 24, 520, [7, 1, 12, 0, 12, 3], seed=77, dtype="bf16", weight_range=0.1)
+    gpu = run_gpu(w)
+    for backward in (False, True):
+        cfg = gpu["plan"].recurrent_config(backward)
+        assert cfg["kernel"] == "step_launches" and cfg["product"] == "tcgen05", cfg
+    compare_all(gpu, run_oracle(w), TOL_BF16, label="wide bf16 per-step")
+    compare_all(gpu, run_oracle(w, bf16_products=True), TOL_BF16_EMULATED, label="wide bf16 per-step",
+                against="oracle-bf16-products")
