@@ -241,10 +241,19 @@ def roofline_of(kind, ms_per_step, calls_per_step, spec, rows, T, D0, peaks, rec
             "per_launch": {"bytes": by / per, "ms": ms_per_step / per}}
 
 
-def source_digest() -> str:
+# the sources that define each kernel kind's device code (a recorded ncu capture stays valid
+# while these files are unchanged)
+KERNEL_SOURCES = {
+    "rec_fwd": ("recurrent_cluster.cu", "recurrent.cu", "recurrent.cuh", "tc_ptx.cuh", "common.cuh"),
+    "rec_bwd": ("recurrent_cluster.cu", "recurrent.cu", "recurrent.cuh", "tc_ptx.cuh", "common.cuh"),
+}
+
+
+def source_digest(kind: str = "") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "padding_free_variable_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    files = KERNEL_SOURCES.get(kind) or tuple(sorted(os.listdir(csrc)))
+    for f in sorted(files):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -259,7 +268,7 @@ def recorded_traffic(kind: str, workload: str):
     except Exception:
         return None
     ent = rec.get(kind)
-    if not ent or ent.get("source_digest") != source_digest() or ent.get("workload") != workload:
+    if not ent or ent.get("source_digest") != source_digest(kind) or ent.get("workload") != workload:
         return None
     return ent.get("dram_bytes_per_launch")
 
