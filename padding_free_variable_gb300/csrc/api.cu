@@ -339,13 +339,26 @@ lstm_status stepwise_fwd_core(const Plan& p, const lstm_layer_shape& s, const ls
     a.rh = rh; a.hb16 = hb16;
     a.y = y; a.y_lo = (__nv_bfloat16*)y_lo; a.h_n = h_n; a.c_n = c_n;
     lstm_status st = LSTM_OK;
+    // tcgen05: both directions' products of a step in one launch, tensor maps encoded once
+    TcOperands op[2];
+    bool pair = hb16 != nullptr;
+    for (int d = 0; d < nd && pair; ++d)
+        pair = gemm_tc_prepare(&op[d], hb16 + (size_t)d * p.B * H, H, p.B, (const char*)prm.R + (size_t)d * 4 * H * H * esz,
+                               H, 4 * H, H, rh + (size_t)d * p.B * 4 * H, 4 * H);
     trace_begin(p, K_REC_FWD, cs);
     int launches = 0;
     for (int step = 0; step < p.T && st == LSTM_OK; ++step) {
-        for (int d = 0; d < nd && st == LSTM_OK; ++d) {
+        int Md[2] = {0, 0};
+        for (int d = 0; d < nd; ++d) {
+            const int t = d == 0 ? step : p.T - 1 - step;
+            Md[d] = d == 0 ? (t >= 1 ? p.h_bs[t] : 0) : (t + 1 < p.T ? p.h_bs[t + 1] : 0);
+        }
+        if (pair && (Md[0] > 0 || Md[1] > 0))
+            st = gemm_tc_pair(p, -1, op[0], Md[0], nd == 2 ? &op[1] : nullptr, Md[1], cs);
+        for (int d = 0; d < nd && st == LSTM_OK && !pair; ++d) {
             // R h_{t-1} of the step's rows that have a previous state (the first M rows)
             const int t = d == 0 ? step : p.T - 1 - step;
-            const int M = d == 0 ? (t >= 1 ? p.h_bs[t] : 0) : (t + 1 < p.T ? p.h_bs[t + 1] : 0);
+            const int M = Md[d];
             if (M == 0) continue;
             const char* Rd = (const char*)prm.R + (size_t)d * 4 * H * H * esz;
             float* C = rh + (size_t)d * p.B * 4 * H;
@@ -392,12 +405,22 @@ lstm_status stepwise_bwd_core(const Plan& p, const lstm_layer_shape& s, const ls
                                          4 * H, 4 * H, H, 0, rt16 + (size_t)d * H * 4 * H, 4 * H, 0, nullptr, 0, 0,
                                          cs);
     if (st != LSTM_OK) return st;
+    TcOperands op[2];
+    bool pair = rt16 != nullptr;
+    for (int d = 0; d < nd && pair; ++d)
+        pair = gemm_tc_prepare(&op[d], dab16 + (size_t)d * p.B * 4 * H, 4 * H, p.B, rt16 + (size_t)d * H * 4 * H,
+                               4 * H, H, 4 * H, dh_rec + (size_t)d * p.B * H, H);
     trace_begin(p, K_REC_BWD, cs);     // (no traced call may nest inside this bracket)
     int launches = 0;
     for (int step = 0; step < p.T && st == LSTM_OK; ++step) {
         st = step_cell_launch(a, step, true, cs);
         ++launches;
         if (step + 1 == p.T) break;
+        if (pair && st == LSTM_OK) {
+            const int M0 = p.h_bs[p.T - 1 - step], M1 = nd == 2 ? p.h_bs[step] : 0;
+            st = gemm_tc_pair(p, -1, op[0], M0, nd == 2 ? &op[1] : nullptr, M1, cs);
+            continue;
+        }
         for (int d = 0; d < nd && st == LSTM_OK; ++d) {
             // R^T da of every row of the step, for the step after it in recurrence order
             const int t = d == 0 ? p.T - 1 - step : step;

@@ -52,6 +52,22 @@ lstm_status transpose_to_bf16(const Plan& p, const void* src, bool src_bf16, int
                               const int32_t* map, int rows, int cols, void* dstT, int64_t ldt, void* dst_rm,
                               int64_t ldm, cudaStream_t s);
 
+// One product C[M][N] = A[M][K] B[N][K]^T (bf16, K-major, fp32 out, no bias)
+// with its tensor maps encoded once, for launches that repeat with varying M
+// (M <= rows_max; rows past M are computed from whatever A holds there and
+// not stored).
+struct TcOperands {
+    CUtensorMap A, B;
+    int N = 0, K = 0;
+    float* C = nullptr;
+    int64_t ldc = 0;
+};
+bool gemm_tc_prepare(TcOperands* o, const void* A, int64_t lda, int rows_max, const void* B, int64_t ldb, int N,
+                     int K, float* C, int64_t ldc);
+// Two prepared products (o1 may be null) in one launch, with M0 and M1 rows.
+lstm_status gemm_tc_pair(const Plan& p, int kind, const TcOperands& o0, int M0, const TcOperands* o1, int M1,
+                         cudaStream_t s);
+
 // TMA map of a row-major fp32 matrix [rows][cols] (row pitch ld elements) in
 // boxes of box_cols x box_rows without swizzle; out-of-range elements read 0.
 // False when the driver entry point is missing or the layout is not

@@ -48,8 +48,9 @@ __device__ __forceinline__ void fail(const TcArgs& a, int* s_abort, unsigned whe
     *(volatile int*)s_abort = 1;
 }
 
-__global__ void __launch_bounds__(TC_THREADS, 1)
-gemm_tc_bf16_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, TcArgs a)
+// One 128 x 256 output tile (blockIdx.x, blockIdx.y) of split zs of nzs.
+__device__ __forceinline__ void tc_gemm_tile(const CUtensorMap* mapA, const CUtensorMap* mapB, const TcArgs& a,
+                                             int zs, int nzs)
 {
     extern __shared__ unsigned char smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -63,11 +64,11 @@ gemm_tc_bf16_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * TBM, n0 = blockIdx.x * TBN;
-    const int kbeg = blockIdx.z * a.k_chunk;
+    const int kbeg = zs * a.k_chunk;
     const int kend = min(a.K, kbeg + a.k_chunk);
     const int nk = kend > kbeg ? (kend - kbeg + TBK - 1) / TBK : 0;
-    const bool split = gridDim.z > 1;
-    float* const Cout = split ? a.partial + (int64_t)blockIdx.z * a.M * a.N : a.C;
+    const bool split = nzs > 1;
+    float* const Cout = split ? a.partial + (int64_t)zs * a.M * a.N : a.C;
     const int64_t ldo = split ? (int64_t)a.N : a.ldc;
     const float* const bias = split ? nullptr : a.bias;
 
@@ -79,8 +80,8 @@ gemm_tc_bf16_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
         tc::mbar_init(accf, 1);
         *s_abort = 0;
         tc::fence_mbar_init();
-        tc::prefetch_tensormap(&mapA);
-        tc::prefetch_tensormap(&mapB);
+        tc::prefetch_tensormap(mapA);
+        tc::prefetch_tensormap(mapB);
     }
     if (warp == 1) {
         tc::tmem_alloc(tmem_slot, TMEM_COLS);
@@ -101,8 +102,8 @@ gemm_tc_bf16_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
             }
             if (*(volatile int*)s_abort) break;
             tc::mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
-            tc::tma_load_2d(sA + s * A_BYTES, &mapA, &full[s], kbeg + kb * TBK, m0);
-            tc::tma_load_2d(sB + s * B_BYTES, &mapB, &full[s], kbeg + kb * TBK, n0);
+            tc::tma_load_2d(sA + s * A_BYTES, mapA, &full[s], kbeg + kb * TBK, m0);
+            tc::tma_load_2d(sB + s * B_BYTES, mapB, &full[s], kbeg + kb * TBK, n0);
         }
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
@@ -172,6 +173,26 @@ gemm_tc_bf16_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_const
         tc::tc_fence_after_sync();
         tc::tmem_dealloc(tmem, TMEM_COLS);
     }
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+gemm_tc_bf16_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, TcArgs a)
+{
+    tc_gemm_tile(&mapA, &mapB, a, (int)blockIdx.z, (int)gridDim.z);
+}
+
+// Two independent products in one launch (blockIdx.z selects one; no split-K): the grid
+// covers the larger of the two, and a CTA past its own product's extent returns before it
+// touches any barrier or tensor memory.
+__global__ void __launch_bounds__(TC_THREADS, 1)
+gemm_tc_bf16_pair_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapB0,
+                         const __grid_constant__ CUtensorMap mapA1, const __grid_constant__ CUtensorMap mapB1,
+                         TcArgs a0, TcArgs a1)
+{
+    const bool second = blockIdx.z == 1;
+    const TcArgs& a = second ? a1 : a0;
+    if ((int)blockIdx.y * TBM >= a.M || (int)blockIdx.x * TBN >= a.N) return;
+    tc_gemm_tile(second ? &mapA1 : &mapA0, second ? &mapB1 : &mapB0, a, 0, 1);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -272,6 +293,46 @@ lstm_status gemm_tc_bf16(const Plan& p, int kind, const void* A, int64_t lda, co
         launched += e == cudaSuccess ? 1 : 0;
     }
     trace_end(p, kind, s, launched);
+    return e == cudaSuccess ? LSTM_OK : LSTM_ERR_CUDA;
+}
+
+bool gemm_tc_prepare(TcOperands* o, const void* A, int64_t lda, int rows_max, const void* B, int64_t ldb, int N,
+                     int K, float* C, int64_t ldc)
+{
+    if (rows_max <= 0 || N <= 0 || K <= 0 || lda % 8 != 0 || ldb % 8 != 0 || ((uintptr_t)A & 15u) ||
+        ((uintptr_t)B & 15u) || !encode_fn())
+        return false;
+    if (!make_map(&o->A, A, rows_max, K, lda, TBM) || !make_map(&o->B, B, N, K, ldb, TBN)) return false;
+    o->N = N; o->K = K; o->C = C; o->ldc = ldc;
+    return true;
+}
+
+lstm_status gemm_tc_pair(const Plan& p, int kind, const TcOperands& o0, int M0, const TcOperands* o1, int M1,
+                         cudaStream_t s)
+{
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(gemm_tc_bf16_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)TC_SMEM) != cudaSuccess)
+            return LSTM_ERR_CUDA;
+        attr_set = true;
+    }
+    if (!o1) { o1 = &o0; M1 = 0; }
+    const int Mmax = std::max(M0, M1), Nmax = std::max(o0.N, o1->N);
+    if (Mmax <= 0) return LSTM_OK;
+    auto args = [&](const TcOperands& o, int M) {
+        TcArgs a;
+        a.M = M; a.N = o.N; a.K = o.K; a.k_chunk = (o.K + TBK - 1) / TBK * TBK;
+        a.C = o.C; a.ldc = o.ldc; a.bias = nullptr; a.partial = nullptr;
+        a.status = p.d_status; a.limit_ns = p.wait_limit_ns;
+        return a;
+    };
+    const TcArgs a0 = args(o0, M0), a1 = args(*o1, M1);
+    const dim3 grid((Nmax + TBN - 1) / TBN, (Mmax + TBM - 1) / TBM, 2);
+    trace_begin(p, kind, s);
+    gemm_tc_bf16_pair_kernel<<<grid, TC_THREADS, TC_SMEM, s>>>(o0.A, o0.B, o1->A, o1->B, a0, a1);
+    const cudaError_t e = cudaGetLastError();
+    trace_end(p, kind, s, e == cudaSuccess ? 1 : 0);
     return e == cudaSuccess ? LSTM_OK : LSTM_ERR_CUDA;
 }
 
