@@ -49,6 +49,9 @@ constexpr int kSumChunks = 64; // row chunks of the db / dpeep sums
 // bound on the teardown wait for a product still in flight after a timeout
 // (an MMA takes microseconds; TMEM is freed only after it has completed)
 constexpr unsigned long long kTeardownWaitNs = 1000000000ull;
+// the thread that issues the TMA operand tiles: lane 0 of the last warp, which never issues
+// MMAs (at most 4 issuing warps), so the tile loads do not delay the next product
+constexpr int kTileIssuer = kCT - 32;
 
 __device__ __forceinline__ float sigm_c(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 __device__ __forceinline__ float tanh_c(float x)
@@ -485,8 +488,8 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
         for (int g = 0; g < 4; ++g)
             tc::tma_load_2d(pre_tile + (size_t)g * NBM * kCU, &pre_map, pre_bar, dir * 4 * H + g * H + u0, s_off[t2]);
     };
-    int last_tile = -1;                   // thread 0: the last step whose tile was issued
-    if (tma_pre && threadIdx.x == 0) { issue_pre(0, true); last_tile = 0; }
+    int last_tile = -1;                   // tile issuer: the last step whose tile was issued
+    if (tma_pre && threadIdx.x == kTileIssuer) { issue_pre(0, true); last_tile = 0; }
     cl.sync();     // every CTA of the cluster is resident before any remote write
 
     const int jq = threadIdx.x >> 3, q8 = threadIdx.x & 7;          // cell item: row jq (+32k), units q8*4..+4
@@ -516,7 +519,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
             if (s > 0) {
                 cluster_wait();    // h_{t-1} of every peer is in this CTA's operand
                 // every thread of this CTA arrived after its cell: the tile is free
-                if (tma_pre && threadIdx.x == 0 && !failed) { issue_pre(s, true); last_tile = s; }
+                if (tma_pre && threadIdx.x == kTileIssuer && !failed) { issue_pre(s, true); last_tile = s; }
                 cstamp(a, false, dir, rank, s - 1, 4, 4);
             }
             cstamp(a, false, dir, rank, s, 0, 0);
@@ -719,7 +722,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
                 bulk_commit();
             }
             cstamp(a, false, dir, rank, s, 4, 4);
-            if (tma_pre && threadIdx.x == 0 && s + 1 < T && !failed) {   // the tile has been read
+            if (tma_pre && threadIdx.x == kTileIssuer && s + 1 < T && !failed) {   // the tile has been read
                 issue_pre(s + 1, false);
                 last_tile = s + 1;
             }
@@ -752,7 +755,8 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
     }
     // after a timeout the last tile issued may not have been waited for: no load may still be
     // writing this CTA's shared memory when it exits (bounded wait)
-    if (tma_pre && threadIdx.x == 0 && last_tile >= 0) tc::mbar_wait(pre_bar, (uint32_t)(last_tile & 1), kTeardownWaitNs);
+    if (tma_pre && threadIdx.x == kTileIssuer && last_tile >= 0)
+        tc::mbar_wait(pre_bar, (uint32_t)(last_tile & 1), kTeardownWaitNs);
     if (BULK) {
         if (lane == 0 && warp < G) bulk_wait_all();   // no copy of this CTA is still in flight
         cl.sync();                              // nor one into it: every CTA has passed its last wait
@@ -917,8 +921,8 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
         tc::tma_load_2d(tile(5, 0), &map_c, opnd_bar, dir * H + u0, yp);
         tc::tma_load_2d(tile(6, 0), &map_dy, opnd_bar, dir * H + u0, y0);
     };
-    int last_tile = -1;                   // thread 0: the last step whose tiles were issued
-    if (tma_opnd && threadIdx.x == 0) { issue_opnd(0); last_tile = 0; }
+    int last_tile = -1;                   // tile issuer: the last step whose tiles were issued
+    if (tma_opnd && threadIdx.x == kTileIssuer) { issue_opnd(0); last_tile = 0; }
     cl.sync();
 
     const int jq = threadIdx.x >> 3, q8 = threadIdx.x & 7;          // cell item: row jq (+32k), units q8*4..+4
@@ -1065,6 +1069,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
                 if (SPLIT) *reinterpret_cast<uint2*>(Blo + o) = lo;
             }
         }
+        if (BULK) cstamp(a, true, dir, rank, s, 4, 4);   // (BULK: stamp 4 = cell done)
         if (!BULK) cluster_arrive_relaxed();   // this CTA has read its inbox: peers may overwrite it
         // the previous step's staging must have been read by its copies before this step's read-out
         if (BULK && lane == 0 && warp < G) bulk_wait_read_all();
@@ -1075,7 +1080,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
         // status word marks the results as invalid)
         if (__syncthreads_or(!step_ok || !arrived)) failed = true;
         // the operand tiles and this parity's inbox have been read
-        if (tma_opnd && threadIdx.x == 0 && s + 1 < T && !failed) {
+        if (tma_opnd && threadIdx.x == kTileIssuer && s + 1 < T && !failed) {
             issue_opnd(s + 1);
             last_tile = s + 1;
         }
@@ -1140,7 +1145,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
                 }
                 bulk_commit();
             }
-            cstamp(a, true, dir, rank, s, 3, 4);
+            cstamp(a, true, dir, rank, s, 3, 3);
         } else {
             cluster_wait();        // every peer has read its inbox of this step
             if (s + 1 < T && !failed) {
@@ -1173,7 +1178,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
     if (BULK) {
         if (lane == 0 && warp < G) bulk_wait_all();   // no copy of this CTA is still in flight
         // after a timeout the last tiles issued may not have been waited for (bounded wait)
-        if (tma_opnd && threadIdx.x == 0 && last_tile >= 0)
+        if (tma_opnd && threadIdx.x == kTileIssuer && last_tile >= 0)
             tc::mbar_wait(opnd_bar, (uint32_t)(last_tile & 1), kTeardownWaitNs);
         cl.sync();                                    // nor one into it
     }
