@@ -786,8 +786,8 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
 // Shared memory (RecArgs offsets): off_contrib = B (gate errors, hi then
 // lo), off_acc = inbox, off_state = dc carry, off_sums = mbarriers, TMEM
 // slot, failure flag, off_peep = peepholes, off_tab = tables; BULK also
-// off_h = staging of the outgoing partials [G][NBM][32], off_red = operand
-// tiles [7][NBM][32] (gates i f z o, c_t, c_{t-1}, dy).
+// off_h = staging of the outgoing partials [G][NBM][32]; with a.tma_pre
+// off_red = operand tiles [7][NBM][32] (gates i f z o, c_t, c_{t-1}, dy).
 // Tensor memory: accumulators (tile m, chain ch) at columns
 // (m * chains + ch) * NBM; R^T tile m from column tm_acol + 64m (hi) and
 // tm_acol + 64 MT + 64m (lo).
@@ -800,7 +800,9 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
 //    go out, as in the forward kernel).  A source can only write parity
 //    (s & 1) again for step s + 2 after it received this CTA's partials of
 //    step s + 1, which are formed after this CTA's cell of step s has read the
-//    inbox.  The cell's own operands arrive as TMA tiles (a.tma_pre).
+//    inbox.
+// The cell's own operands arrive as TMA tiles when they fit (a.tma_pre),
+// issued after the barrier that follows the cell (every thread has read them).
 //  * otherwise: one inbox written with plain DSMEM stores between the two
 //    halves of a split cluster barrier.
 template <bool SPLIT, bool BULK>
@@ -837,7 +839,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
     int* s_len = s_off + T + 1;
     const uint32_t tcols = (uint32_t)a.Umax;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool tma_opnd = BULK && a.tma_pre != 0;
+    const bool tma_opnd = a.tma_pre != 0;
     auto inbox_at = [&](int parity, int src, int j) -> float* {
         return inbox + (((size_t)(BULK ? parity : 0) * G + src) * NBM + j) * kCU;
     };
@@ -1170,16 +1172,16 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
             cstamp(a, true, dir, rank, s, 3, 3);
             fence_proxy_async_cluster();
             cluster_arrive();      // release: this CTA's partial sums are in their owners' inboxes
-            if (s + 1 < T) load_own(s + 1);       // the next step's own operands, in flight across the barrier
+            if (!tma_opnd && s + 1 < T) load_own(s + 1);   // the next step's own operands, in flight across the barrier
             cluster_wait();
             cstamp(a, true, dir, rank, s, 4, 4);
         }
     }
+    // after a timeout the last tiles issued may not have been waited for (bounded wait)
+    if (tma_opnd && threadIdx.x == kTileIssuer && last_tile >= 0)
+        tc::mbar_wait(opnd_bar, (uint32_t)(last_tile & 1), kTeardownWaitNs);
     if (BULK) {
         if (lane == 0 && warp < G) bulk_wait_all();   // no copy of this CTA is still in flight
-        // after a timeout the last tiles issued may not have been waited for (bounded wait)
-        if (tma_opnd && threadIdx.x == kTileIssuer && last_tile >= 0)
-            tc::mbar_wait(opnd_bar, (uint32_t)(last_tile & 1), kTeardownWaitNs);
         cl.sync();                                    // nor one into it
     }
     tc::tc_fence_before_sync();
@@ -1418,13 +1420,16 @@ bool rec_cluster_bwd_configure(const Plan& p, int H, int ndir, bool bf16, RecCon
     while (nch > 1 && (MT * nch > 4 || MT * nch * NBM + acols > 512)) nch >>= 1;
     if (MT * nch * NBM + acols > 512 || MT * nch > kCT / 32) return false;
     const uint32_t cols = pow2_cols(MT * nch * NBM + acols);
-    // bulk exchange with operand tiles first; the single-buffered barrier exchange needs the least
-    for (int bulk = 1; bulk >= 0; --bulk) {
+    // bulk exchange with operand tiles first, then the single-buffered barrier exchange with
+    // and without tiles (the last needs the least shared memory)
+    const int order[3][2] = {{1, 1}, {0, 1}, {0, 0}};
+    for (int oi = 0; oi < 3; ++oi) {
+        const int bulk = order[oi][0], tiles = order[oi][1];
         size_t off = 0;
         const size_t o_b = off; off = al(off + (split ? 2 : 1) * (size_t)2 * NBM * 128, 1024);
         const size_t o_in = off; off = al(off + (bulk ? 2 : 1) * (size_t)G * NBM * kCU * 4, 1024);
         const size_t o_stage = off; if (bulk) off = al(off + (size_t)G * NBM * kCU * 4, 1024);
-        const size_t o_tiles = off; if (bulk) off = al(off + 7 * (size_t)NBM * kCU * 4, 1024);
+        const size_t o_tiles = off; if (tiles) off = al(off + 7 * (size_t)NBM * kCU * 4, 1024);
         const size_t o_dcc = off; off = al(off + (size_t)p.B * kCU * 4, 16);
         const size_t o_bar = off; off = al(off + 64, 16);
         const size_t o_peep = off; off = al(off + 3 * kCU * 4, 16);
@@ -1435,7 +1440,7 @@ bool rec_cluster_bwd_configure(const Plan& p, int H, int ndir, bool bf16, RecCon
         if (!cluster_schedulable(p, bwd_kernel(bf16, bulk != 0), G, smem)) continue;
         RecConfig c;
         c.G = G; c.Umax = (int)cols; c.JC = NBM; c.smem = smem; c.cluster = 1;
-        c.chains = nch; c.acol = (int)cols - acols; c.bulk = bulk; c.tma_pre = bulk;
+        c.chains = nch; c.acol = (int)cols - acols; c.bulk = bulk; c.tma_pre = tiles;
         *out = c;
         lay->off_contrib = (int)o_b; lay->off_acc = (int)o_in; lay->off_h = (int)o_stage; lay->off_red = (int)o_tiles;
         lay->off_state = (int)o_dcc; lay->off_sums = (int)o_bar; lay->off_peep = (int)o_peep; lay->off_tab = (int)o_tab;
