@@ -175,10 +175,174 @@ __device__ __forceinline__ void tc_gemm_tile(const CUtensorMap* mapA, const CUte
     }
 }
 
+// Persistent form: one CTA per SM walks the (split, m, n) tiles of the product with stride
+// gridDim.x (n fastest, so the CTAs in flight share A tiles and all of B through L2).  The
+// shared-memory ring continues across tiles, and the accumulator is double-buffered in
+// tensor memory (2 x 256 columns): the epilogue warps drain tile i from one buffer while the
+// MMA warp accumulates tile i + 1 into the other.  Barriers: full / empty per ring stage,
+// accf per buffer (MMA -> epilogue) and acce per buffer (the 4 epilogue warps -> MMA).
 __global__ void __launch_bounds__(TC_THREADS, 1)
-gemm_tc_bf16_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, TcArgs a)
+gemm_tc_bf16_persistent_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                               TcArgs a, int nM, int nN, int splits)
 {
-    tc_gemm_tile(&mapA, &mapB, a, (int)blockIdx.z, (int)gridDim.z);
+    extern __shared__ unsigned char smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sA = base;
+    uint8_t* sB = base + TSTAGES * A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(base + TSTAGES * (A_BYTES + B_BYTES));
+    uint64_t* empty = full + TSTAGES;
+    uint64_t* accf = empty + TSTAGES;        // [2]
+    uint64_t* acce = accf + 2;               // [2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
+    int* s_abort = reinterpret_cast<int*>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntiles = nM * nN * splits;
+    const bool split = splits > 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < TSTAGES; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&accf[b], 1);
+            tc::mbar_init(&acce[b], 4);
+        }
+        *s_abort = 0;
+        tc::fence_mbar_init();
+        tc::prefetch_tensormap(&mapA);
+        tc::prefetch_tensormap(&mapB);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 2 * TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before_sync();
+    __syncthreads();
+    tc::tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    auto decode = [&](int tile, int& z, int& m0, int& n0, int& kbeg, int& nk) {
+        z = tile / (nM * nN);
+        const int rem = tile - z * nM * nN;
+        m0 = (rem / nN) * TBM;
+        n0 = (rem % nN) * TBN;
+        kbeg = z * a.k_chunk;
+        const int kend = min(a.K, kbeg + a.k_chunk);
+        nk = kend > kbeg ? (kend - kbeg + TBK - 1) / TBK : 0;
+    };
+
+    if (warp == 0 && lane == 0) {
+        // ---- producer: the ring's k-blocks of every tile of this CTA, in order
+        int g = 0;
+        for (int tile = blockIdx.x; tile < ntiles && !*(volatile int*)s_abort; tile += gridDim.x) {
+            int z, m0, n0, kbeg, nk;
+            decode(tile, z, m0, n0, kbeg, nk);
+            for (int kb = 0; kb < nk; ++kb, ++g) {
+                const int s = g % TSTAGES;
+                if (g >= TSTAGES && !tc::mbar_wait(&empty[s], ((g / TSTAGES) - 1) & 1, a.limit_ns)) {
+                    fail(a, s_abort, 11);
+                    break;
+                }
+                if (*(volatile int*)s_abort) break;
+                tc::mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
+                tc::tma_load_2d(sA + s * A_BYTES, &mapA, &full[s], kbeg + kb * TBK, m0);
+                tc::tma_load_2d(sB + s * B_BYTES, &mapB, &full[s], kbeg + kb * TBK, n0);
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer: tile i into accumulator buffer i & 1
+        constexpr uint32_t idesc = tc::idesc_bf16_f32(TBM, TBN);
+        int g = 0, i = 0;
+        for (int tile = blockIdx.x; tile < ntiles && !*(volatile int*)s_abort; tile += gridDim.x, ++i) {
+            int z, m0, n0, kbeg, nk;
+            decode(tile, z, m0, n0, kbeg, nk);
+            const int b = i & 1;
+            if (i >= 2 && !tc::mbar_wait(&acce[b], ((i >> 1) - 1) & 1, a.limit_ns)) {
+                fail(a, s_abort, 12);
+                break;
+            }
+            tc::tc_fence_after_sync();
+            const uint32_t d = tmem + (uint32_t)(b * TMEM_COLS);
+            bool ok = true;
+            for (int kb = 0; kb < nk; ++kb, ++g) {
+                const int s = g % TSTAGES;
+                if (*(volatile int*)s_abort || !tc::mbar_wait(&full[s], (g / TSTAGES) & 1, a.limit_ns)) {
+                    if (!*(volatile int*)s_abort) fail(a, s_abort, 13);
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after_sync();
+                const uint32_t a0 = tc::smem_u32(sA + s * A_BYTES), b0 = tc::smem_u32(sB + s * B_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < TBK / 16; ++kk)
+                    tc::mma_bf16_ss(d, tc::sdesc_sw128(a0 + kk * 32), tc::sdesc_sw128(b0 + kk * 32), idesc,
+                                    (kb | kk) != 0 ? 1u : 0u);
+                tc::mma_commit(&empty[s]);
+            }
+            if (!ok) break;
+            tc::mma_commit(&accf[b]);    // arrives once every MMA of this tile has completed
+        }
+    } else if (warp >= 2) {
+        // ---- epilogue: this warp reads TMEM lanes 32*(warp%4) .. +31 of the tile's buffer
+        const int q = warp & 3;
+        int i = 0;
+        for (int tile = blockIdx.x; tile < ntiles && !*(volatile int*)s_abort; tile += gridDim.x, ++i) {
+            int z, m0, n0, kbeg, nk;
+            decode(tile, z, m0, n0, kbeg, nk);
+            const int b = i & 1;
+            const bool ok = tc::mbar_wait(&accf[b], (i >> 1) & 1, a.limit_ns);
+            if (!ok && lane == 0) fail(a, s_abort, 14);
+            tc::tc_fence_after_sync();
+            if (!__all_sync(0xffffffffu, ok) || *(volatile int*)s_abort) break;
+            float* const Cout = split ? a.partial + (int64_t)z * a.M * a.N : a.C;
+            const int64_t ldo = split ? (int64_t)a.N : a.ldc;
+            const float* const bias = split ? nullptr : a.bias;
+            const bool vec = (ldo % 4) == 0 && (((uintptr_t)Cout) & 15u) == 0;
+            const int row = m0 + q * 32 + lane;
+            for (int c = 0; c < TBN; c += 16) {
+                if (n0 + c >= a.N) break;                      // uniform across the warp
+                uint32_t r[16];
+                if (nk > 0) {
+                    tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * TMEM_COLS + c), r);
+                    tc::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r[e] = 0u;   // empty k range: a zero product
+                }
+                if (row < a.M) {
+                    const int n = n0 + c;
+                    float* out = Cout + (int64_t)row * ldo + n;
+                    float v[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
+                    if (n + 16 <= a.N && vec) {
+                        if (bias) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v[e] += __ldg(bias + n + e);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4)
+                            *reinterpret_cast<float4*>(out + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            if (n + e < a.N) out[e] = v[e] + (bias ? __ldg(bias + n + e) : 0.f);
+                    }
+                }
+            }
+            // this warp has read the buffer: one arrival per warp frees it for tile i + 2
+            tc::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&acce[b]);
+        }
+    }
+    tc::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc::tc_fence_after_sync();
+        tc::tmem_dealloc(tmem, 2 * TMEM_COLS);
+    }
 }
 
 // Two independent products in one launch (blockIdx.z selects one; no split-K): the grid
@@ -270,8 +434,8 @@ lstm_status gemm_tc_bf16(const Plan& p, int kind, const void* A, int64_t lda, co
     if (!make_map(&mapA, A, M, K, lda, TBM) || !make_map(&mapB, B, N, K, ldb, TBN)) return LSTM_ERR_UNSUPPORTED;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(gemm_tc_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(gemm_tc_bf16_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)TC_SMEM) != cudaSuccess)
             return LSTM_ERR_CUDA;
         attr_set = true;
     }
@@ -283,9 +447,11 @@ lstm_status gemm_tc_bf16(const Plan& p, int kind, const void* A, int64_t lda, co
     a.M = M; a.N = N; a.K = K; a.k_chunk = kb_per * TBK;
     a.C = C; a.ldc = ldc; a.bias = bias; a.partial = partial;
     a.status = p.d_status; a.limit_ns = p.wait_limit_ns;
-    const dim3 grid((N + TBN - 1) / TBN, (M + TBM - 1) / TBM, splits);
+    const int nM = (M + TBM - 1) / TBM, nN = (N + TBN - 1) / TBN;
+    const int ntiles = nM * nN * splits;
+    const dim3 grid((unsigned)std::min(ntiles, std::max(1, p.num_sms)));
     trace_begin(p, kind, s);
-    gemm_tc_bf16_kernel<<<grid, TC_THREADS, TC_SMEM, s>>>(mapA, mapB, a);
+    gemm_tc_bf16_persistent_kernel<<<grid, TC_THREADS, TC_SMEM, s>>>(mapA, mapB, a, nM, nN, splits);
     cudaError_t e = cudaGetLastError();
     int launched = e == cudaSuccess ? 1 : 0;
     if (e == cudaSuccess && splits > 1) {
