@@ -41,6 +41,16 @@ bool f32_split_shape(const lstm_layer_shape& s) { return s.dtype == LSTM_F32 && 
 // CTAs x 32 units): the recurrence runs as per-step tcgen05 products over the whole GPU.
 bool wide_bf16(const lstm_layer_shape& s) { return s.dtype == LSTM_BF16 && s.hidden_size > 512; }
 
+// K splits of a bf16 layer's per-step tensor-core products (a function of the shape only, so
+// that the buffers holding their slices have a fixed layout): forward R h, N = 4H, K = H;
+// backward R^T da, N = H, K = 4H; both directions in one launch.
+int step_splits(const Plan& p, const lstm_layer_shape& s, bool bwd)
+{
+    if (s.dtype != LSTM_BF16) return 1;
+    const int H = s.hidden_size;
+    return gemm_tc_pair_splits(p.B, bwd ? H : 4 * H, bwd ? 4 * H : H, s.num_directions, p.num_sms);
+}
+
 struct Layout {
     size_t ga_off, c_off, xs_off, ws_off, rh_off, hb_off, total;   // workspace
 };
@@ -59,7 +69,7 @@ Layout workspace_layout(const Plan& p, const lstm_layer_shape& s)
     l.rh_off = l.ws_off + (f32_split_shape(s) ? align256(nd * 4 * H * 3 * D * 2) : 0);
     // wide bf16 layers: a step's R h_{t-1} [ndir][B][4H] fp32 and bf16 h [ndir][B][H]
     const size_t B = (size_t)p.B;
-    l.hb_off = l.rh_off + (wide_bf16(s) ? align256(nd * B * 4 * H * 4) : 0);
+    l.hb_off = l.rh_off + (wide_bf16(s) ? align256(nd * (size_t)step_splits(p, s, false) * B * 4 * H * 4) : 0);
     l.total = l.hb_off + (wide_bf16(s) ? align256(nd * B * H * 2) : 0);
     return l;
 }
@@ -286,8 +296,8 @@ StepScratch step_scratch(const Plan& p, const lstm_layer_shape& s)
     StepScratch q;
     const size_t B = (size_t)p.B, H = (size_t)s.hidden_size, nd = (size_t)s.num_directions;
     size_t off = align256(bwd_scratch(p, s).total);
-    q.rh = off; off += align256(nd * B * 4 * H * sizeof(float));
-    q.dh = off; off += align256(nd * B * H * sizeof(float));
+    q.rh = off; off += align256(nd * (size_t)step_splits(p, s, false) * B * 4 * H * sizeof(float));
+    q.dh = off; off += align256(nd * (size_t)step_splits(p, s, true) * B * H * sizeof(float));
     q.dcc = off; off += align256(nd * B * H * sizeof(float));
     if (s.dtype == LSTM_BF16) {
         q.hb = off; off += align256(nd * B * H * 2);
@@ -339,12 +349,16 @@ lstm_status stepwise_fwd_core(const Plan& p, const lstm_layer_shape& s, const ls
     a.rh = rh; a.hb16 = hb16;
     a.y = y; a.y_lo = (__nv_bfloat16*)y_lo; a.h_n = h_n; a.c_n = c_n;
     lstm_status st = LSTM_OK;
-    // tcgen05: both directions' products of a step in one launch, tensor maps encoded once
+    // tcgen05: both directions' products of a step in one launch, tensor maps encoded once, K
+    // split into S slices of rh that the cell adds; the CUDA-core products write one slice
     TcOperands op[2];
     bool pair = hb16 != nullptr;
+    int S = pair ? step_splits(p, s, false) : 1;
     for (int d = 0; d < nd && pair; ++d)
         pair = gemm_tc_prepare(&op[d], hb16 + (size_t)d * p.B * H, H, p.B, (const char*)prm.R + (size_t)d * 4 * H * H * esz,
-                               H, 4 * H, H, rh + (size_t)d * p.B * 4 * H, 4 * H);
+                               H, 4 * H, H, rh + (size_t)d * S * p.B * 4 * H, 4 * H, S);
+    if (!pair) S = 1;
+    a.rh_splits = S;
     trace_begin(p, K_REC_FWD, cs);
     int launches = 0;
     for (int step = 0; step < p.T && st == LSTM_OK; ++step) {
@@ -361,7 +375,7 @@ lstm_status stepwise_fwd_core(const Plan& p, const lstm_layer_shape& s, const ls
             const int M = Md[d];
             if (M == 0) continue;
             const char* Rd = (const char*)prm.R + (size_t)d * 4 * H * H * esz;
-            float* C = rh + (size_t)d * p.B * 4 * H;
+            float* C = rh + (size_t)d * S * p.B * 4 * H;
             if (hb16) {
                 st = gemm_tc_bf16(p, -1, hb16 + (size_t)d * p.B * H, H, Rd, H, M, 4 * H, H, C, 4 * H, nullptr, 1,
                                   nullptr, cs);
@@ -407,9 +421,12 @@ lstm_status stepwise_bwd_core(const Plan& p, const lstm_layer_shape& s, const ls
     if (st != LSTM_OK) return st;
     TcOperands op[2];
     bool pair = rt16 != nullptr;
+    int S = pair ? step_splits(p, s, true) : 1;
     for (int d = 0; d < nd && pair; ++d)
         pair = gemm_tc_prepare(&op[d], dab16 + (size_t)d * p.B * 4 * H, 4 * H, p.B, rt16 + (size_t)d * H * 4 * H,
-                               4 * H, H, 4 * H, dh_rec + (size_t)d * p.B * H, H);
+                               4 * H, H, 4 * H, dh_rec + (size_t)d * S * p.B * H, H, S);
+    if (!pair) S = 1;
+    a.dh_splits = S;
     trace_begin(p, K_REC_BWD, cs);     // (no traced call may nest inside this bracket)
     int launches = 0;
     for (int step = 0; step < p.T && st == LSTM_OK; ++step) {
@@ -424,7 +441,7 @@ lstm_status stepwise_bwd_core(const Plan& p, const lstm_layer_shape& s, const ls
         for (int d = 0; d < nd && st == LSTM_OK; ++d) {
             // R^T da of every row of the step, for the step after it in recurrence order
             const int t = d == 0 ? p.T - 1 - step : step;
-            float* C = dh_rec + (size_t)d * p.B * H;
+            float* C = dh_rec + (size_t)d * S * p.B * H;
             if (rt16) {
                 st = gemm_tc_bf16(p, -1, dab16 + (size_t)d * p.B * 4 * H, 4 * H, rt16 + (size_t)d * H * 4 * H, 4 * H,
                                   p.h_bs[t], H, 4 * H, C, H, nullptr, 1, nullptr, cs);

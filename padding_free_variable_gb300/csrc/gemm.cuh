@@ -56,15 +56,22 @@ lstm_status transpose_to_bf16(const Plan& p, const void* src, bool src_bf16, int
 // with its tensor maps encoded once, for launches that repeat with varying M
 // (M <= rows_max; rows past M are computed from whatever A holds there and
 // not stored).
+// With splits > 1 the K range is cut into that many pieces and piece z writes its partial
+// product into slice z of C (slices rows_max * ldc floats apart); the reader adds the
+// slices in order.
 struct TcOperands {
     CUtensorMap A, B;
     int N = 0, K = 0;
     float* C = nullptr;
     int64_t ldc = 0;
+    int splits = 1;
+    int64_t split_stride = 0;
 };
 bool gemm_tc_prepare(TcOperands* o, const void* A, int64_t lda, int rows_max, const void* B, int64_t ldb, int N,
-                     int K, float* C, int64_t ldc);
-// Two prepared products (o1 may be null) in one launch, with M0 and M1 rows.
+                     int K, float* C, int64_t ldc, int splits);
+// K splits that fill the GPU with `products` products of up to rows_max x N.
+int gemm_tc_pair_splits(int rows_max, int N, int K, int products, int num_sms);
+// Two prepared products (o1 may be null; equal splits) in one launch, with M0 and M1 rows.
 lstm_status gemm_tc_pair(const Plan& p, int kind, const TcOperands& o0, int M0, const TcOperands* o1, int M1,
                          cudaStream_t s);
 

@@ -37,7 +37,8 @@ struct TcArgs {
     float* C;
     int64_t ldc;
     const float* bias;    // added only without split
-    float* partial;       // split > 1: [z][M][N]
+    float* partial;       // split > 1: [z][M][N], or [z] slices split_stride apart with row pitch ldc
+    int64_t split_stride; // 0: slices of M x N
     DeviceStatus* status;
     unsigned long long limit_ns;
 };
@@ -68,8 +69,8 @@ __device__ __forceinline__ void tc_gemm_tile(const CUtensorMap* mapA, const CUte
     const int kend = min(a.K, kbeg + a.k_chunk);
     const int nk = kend > kbeg ? (kend - kbeg + TBK - 1) / TBK : 0;
     const bool split = nzs > 1;
-    float* const Cout = split ? a.partial + (int64_t)zs * a.M * a.N : a.C;
-    const int64_t ldo = split ? (int64_t)a.N : a.ldc;
+    float* const Cout = split ? a.partial + (int64_t)zs * (a.split_stride ? a.split_stride : (int64_t)a.M * a.N) : a.C;
+    const int64_t ldo = split ? (a.split_stride ? a.ldc : (int64_t)a.N) : a.ldc;
     const float* const bias = split ? nullptr : a.bias;
 
     if (threadIdx.x == 0) {
@@ -345,18 +346,19 @@ gemm_tc_bf16_persistent_kernel(const __grid_constant__ CUtensorMap mapA, const _
     }
 }
 
-// Two independent products in one launch (blockIdx.z selects one; no split-K): the grid
+// Two independent products in one launch (blockIdx.z = product * splits + split): the grid
 // covers the larger of the two, and a CTA past its own product's extent returns before it
-// touches any barrier or tensor memory.
+// touches any barrier or tensor memory.  With splits > 1 each split writes its own slice.
 __global__ void __launch_bounds__(TC_THREADS, 1)
 gemm_tc_bf16_pair_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapB0,
                          const __grid_constant__ CUtensorMap mapA1, const __grid_constant__ CUtensorMap mapB1,
-                         TcArgs a0, TcArgs a1)
+                         TcArgs a0, TcArgs a1, int splits)
 {
-    const bool second = blockIdx.z == 1;
+    const bool second = (int)blockIdx.z >= splits;
+    const int zs = (int)blockIdx.z - (second ? splits : 0);
     const TcArgs& a = second ? a1 : a0;
     if ((int)blockIdx.y * TBM >= a.M || (int)blockIdx.x * TBN >= a.N) return;
-    tc_gemm_tile(second ? &mapA1 : &mapA0, second ? &mapB1 : &mapB0, a, 0, 1);
+    tc_gemm_tile(second ? &mapA1 : &mapA0, second ? &mapB1 : &mapB0, a, zs, splits);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -445,7 +447,7 @@ lstm_status gemm_tc_bf16(const Plan& p, int kind, const void* A, int64_t lda, co
     splits = (kblocks + kb_per - 1) / kb_per;          // every split gets at least one k-block
     TcArgs a;
     a.M = M; a.N = N; a.K = K; a.k_chunk = kb_per * TBK;
-    a.C = C; a.ldc = ldc; a.bias = bias; a.partial = partial;
+    a.C = C; a.ldc = ldc; a.bias = bias; a.partial = partial; a.split_stride = 0;
     a.status = p.d_status; a.limit_ns = p.wait_limit_ns;
     const int nM = (M + TBM - 1) / TBM, nN = (N + TBN - 1) / TBN;
     const int ntiles = nM * nN * splits;
@@ -463,14 +465,27 @@ lstm_status gemm_tc_bf16(const Plan& p, int kind, const void* A, int64_t lda, co
 }
 
 bool gemm_tc_prepare(TcOperands* o, const void* A, int64_t lda, int rows_max, const void* B, int64_t ldb, int N,
-                     int K, float* C, int64_t ldc)
+                     int K, float* C, int64_t ldc, int splits)
 {
-    if (rows_max <= 0 || N <= 0 || K <= 0 || lda % 8 != 0 || ldb % 8 != 0 || ((uintptr_t)A & 15u) ||
+    if (rows_max <= 0 || N <= 0 || K <= 0 || splits < 1 || lda % 8 != 0 || ldb % 8 != 0 || ((uintptr_t)A & 15u) ||
         ((uintptr_t)B & 15u) || !encode_fn())
         return false;
     if (!make_map(&o->A, A, rows_max, K, lda, TBM) || !make_map(&o->B, B, N, K, ldb, TBN)) return false;
     o->N = N; o->K = K; o->C = C; o->ldc = ldc;
+    o->splits = splits; o->split_stride = (int64_t)rows_max * ldc;
     return true;
+}
+
+int gemm_tc_pair_splits(int rows_max, int N, int K, int products, int num_sms)
+{
+    const int tiles = products * ((rows_max + TBM - 1) / TBM) * ((N + TBN - 1) / TBN);
+    const int kblocks = (K + TBK - 1) / TBK;
+    // splitting pays only when the tiles alone leave most of the GPU idle: each split adds a
+    // slice of partial sums to write and read back (measured: 64 tiles of 256 x 4096 x 1024
+    // products are faster unsplit)
+    if (4 * tiles >= num_sms) return 1;
+    int splits = std::max(1, num_sms / std::max(1, tiles));
+    return std::max(1, std::min(splits, kblocks / 4));
 }
 
 lstm_status gemm_tc_pair(const Plan& p, int kind, const TcOperands& o0, int M0, const TcOperands* o1, int M1,
@@ -486,17 +501,22 @@ lstm_status gemm_tc_pair(const Plan& p, int kind, const TcOperands& o0, int M0, 
     if (!o1) { o1 = &o0; M1 = 0; }
     const int Mmax = std::max(M0, M1), Nmax = std::max(o0.N, o1->N);
     if (Mmax <= 0) return LSTM_OK;
+    if (o1->splits != o0.splits) return LSTM_ERR_INVALID_ARG;
+    const int splits = o0.splits;
     auto args = [&](const TcOperands& o, int M) {
         TcArgs a;
-        a.M = M; a.N = o.N; a.K = o.K; a.k_chunk = (o.K + TBK - 1) / TBK * TBK;
-        a.C = o.C; a.ldc = o.ldc; a.bias = nullptr; a.partial = nullptr;
+        const int kblocks = (o.K + TBK - 1) / TBK;
+        a.M = M; a.N = o.N; a.K = o.K; a.k_chunk = (kblocks + splits - 1) / splits * TBK;
+        a.C = o.C; a.ldc = o.ldc; a.bias = nullptr;
+        a.partial = splits > 1 ? o.C : nullptr;           // split z writes slice z of C
+        a.split_stride = o.split_stride;
         a.status = p.d_status; a.limit_ns = p.wait_limit_ns;
         return a;
     };
     const TcArgs a0 = args(o0, M0), a1 = args(*o1, M1);
-    const dim3 grid((Nmax + TBN - 1) / TBN, (Mmax + TBM - 1) / TBM, 2);
+    const dim3 grid((Nmax + TBN - 1) / TBN, (Mmax + TBM - 1) / TBM, 2 * splits);
     trace_begin(p, kind, s);
-    gemm_tc_bf16_pair_kernel<<<grid, TC_THREADS, TC_SMEM, s>>>(o0.A, o0.B, o1->A, o1->B, a0, a1);
+    gemm_tc_bf16_pair_kernel<<<grid, TC_THREADS, TC_SMEM, s>>>(o0.A, o0.B, o1->A, o1->B, a0, a1, splits);
     const cudaError_t e = cudaGetLastError();
     trace_end(p, kind, s, e == cudaSuccess ? 1 : 0);
     return e == cudaSuccess ? LSTM_OK : LSTM_ERR_CUDA;

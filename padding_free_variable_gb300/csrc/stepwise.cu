@@ -41,10 +41,21 @@ __global__ void step_cell_fwd_kernel(StepArgs a, int s)
     const bool has_prev = dir == 0 ? t >= 1 : (t + 1 < T && j < a.bs[t + 1]);
     const int prow = has_prev ? (dir == 0 ? a.off[t - 1] + j : a.off[t + 1] + j) : 0;
     const float* pre = a.ga + (size_t)row * nd4H + (size_t)dir * 4 * H + u;
-    const float* rh = a.rh + ((size_t)dir * a.B + j) * 4 * H + u;
+    const float* rh = a.rh + ((size_t)dir * a.rh_splits * a.B + j) * 4 * H + u;
+    const size_t rstride = (size_t)a.B * 4 * H;
+    // R h_{t-1}: the slices added in order, the four gates' loads of a slice issued together
+    float r[4] = {0.f, 0.f, 0.f, 0.f};
+    if (has_prev) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) r[g] = rh[g * H];
+        for (int z = 1; z < a.rh_splits; ++z) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) r[g] += rh[z * rstride + g * H];
+        }
+    }
     float av[4];
 #pragma unroll
-    for (int g = 0; g < 4; ++g) av[g] = pre[g * H] + (has_prev ? rh[g * H] : 0.f);
+    for (int g = 0; g < 4; ++g) av[g] = pre[g * H] + r[g];
     const float cp = has_prev ? a.cbuf[(size_t)prow * ndH + dir * H + u] : 0.f;
     const float* pp = a.peep + (size_t)dir * 3 * H + u;
     const float ig = sigm(av[0] + pp[0] * cp);
@@ -91,7 +102,12 @@ __global__ void step_cell_bwd_kernel(StepArgs a, int s)
     const float c = a.cbuf[yo];
     const float cp = has_prev ? a.cbuf[(size_t)prow * ndH + dir * H + u] : 0.f;
     const size_t so = ((size_t)dir * a.B + j) * H + u;
-    const float dh = a.dy[yo] + (has_next ? a.dh_rec[so] : 0.f);
+    float dhr = 0.f;
+    if (has_next) {
+        const float* dr = a.dh_rec + ((size_t)dir * a.dh_splits * a.B + j) * H + u;
+        for (int z = 0; z < a.dh_splits; ++z) dhr += dr[(size_t)z * a.B * H];
+    }
+    const float dh = a.dy[yo] + dhr;
     const float carry = has_next ? a.dcc[so] : 0.f;
     const float* pp = a.peep + (size_t)dir * 3 * H + u;
     const float tc = tanhf(c);

@@ -14,7 +14,7 @@ struct StepArgs {
     const int32_t* slot_len;  // [B]
     const int32_t* perm;      // [B]
     float* ga;                // [rows][ndir*4H] pre-activations -> gates -> gate errors
-    const float* rh;          // forward: [ndir][B][4H] the step's R h_{t-1}
+    const float* rh;          // forward: [ndir][rh_splits][B][4H] the step's R h_{t-1} (slices added in order)
     const float* peep;        // [ndir][3][H]
     float* y;                 // [rows][ndir*H]
     __nv_bfloat16* y_lo;      // optional bf16 copy of y
@@ -22,10 +22,11 @@ struct StepArgs {
     float* h_n;               // [ndir][B][H] caller order, optional
     float* c_n;
     const float* dy;          // backward: [rows][ndir*H]
-    const float* dh_rec;      // backward: [ndir][B][H] R^T da of the step after (recurrence order)
+    const float* dh_rec;      // backward: [ndir][dh_splits][B][H] R^T da of the step after (recurrence order)
     float* dcc;               // backward: [ndir][B][H] cell-state error carry
     __nv_bfloat16* hb16;      // optional, forward: [ndir][B][H] bf16 h of the step's rows (next product's A)
     __nv_bfloat16* dab16;     // optional, backward: [ndir][B][4H] bf16 gate errors of the step's rows
+    int rh_splits, dh_splits; // K slices of the per-step products (1 without split)
 };
 
 // Cell of step s (forward, or BPTT in backward order) for both directions.
