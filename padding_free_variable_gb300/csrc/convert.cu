@@ -71,6 +71,89 @@ __global__ void __launch_bounds__(256) transpose_bf16_kernel(const Tin* __restri
     }
 }
 
+template <typename Tin>
+__device__ __forceinline__ void load4(const Tin* p, float (&v)[4]);
+template <>
+__device__ __forceinline__ void load4<float>(const float* p, float (&v)[4])
+{
+    const float4 x = __ldg(reinterpret_cast<const float4*>(p));
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+}
+template <>
+__device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[4])
+{
+    const uint2 x = *reinterpret_cast<const uint2*>(p);
+    v[0] = __uint_as_float(x.x << 16); v[1] = __uint_as_float(x.x & 0xffff0000u);
+    v[2] = __uint_as_float(x.y << 16); v[3] = __uint_as_float(x.y & 0xffff0000u);
+}
+
+// The same conversion in 64 x 64 tiles with 4-element loads, 8-byte row-major stores and
+// 16-byte transposed stores, for layouts where every piece is aligned (cols, col0, lds,
+// ldm and kseg_m multiples of 4; ldt and kseg_t multiples of 8; 16-byte aligned bases).
+template <typename Tin>
+__global__ void __launch_bounds__(256) transpose_bf16_v4_kernel(const Tin* __restrict__ src, int64_t lds, int col0,
+                                                                const int32_t* __restrict__ map, int rows,
+                                                                int rows_pad, int cols, int pattern,
+                                                                __nv_bfloat16* __restrict__ dstT, int64_t ldt,
+                                                                int64_t kseg_t, __nv_bfloat16* __restrict__ dst_rm,
+                                                                int64_t ldm, int64_t kseg_m)
+{
+    __shared__ __align__(16) __nv_bfloat16 thi[64][72], tlo[64][72];     // [column][row]
+    const int r0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
+    const int tid = threadIdx.x;
+    const int nseg = pattern == 0 ? 1 : 3;
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int rr = (tid >> 4) + 16 * it, q = tid & 15;
+        const int r = r0 + rr, c = c0 + 4 * q;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (r < rows && c < cols) {
+            const int64_t sr = map ? (int64_t)__ldg(map + r) : (int64_t)r;
+            if (sr >= 0) load4<Tin>(src + sr * lds + col0 + c, v);
+        }
+        __nv_bfloat16 hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            hi[e] = __float2bfloat16_rn(v[e]);
+            lo[e] = __float2bfloat16_rn(v[e] - __bfloat162float(hi[e]));
+        }
+        if (dst_rm && r < rows && c < cols) {
+            uint2 phi, plo;
+            phi.x = (uint32_t)__bfloat16_as_ushort(hi[0]) | ((uint32_t)__bfloat16_as_ushort(hi[1]) << 16);
+            phi.y = (uint32_t)__bfloat16_as_ushort(hi[2]) | ((uint32_t)__bfloat16_as_ushort(hi[3]) << 16);
+            plo.x = (uint32_t)__bfloat16_as_ushort(lo[0]) | ((uint32_t)__bfloat16_as_ushort(lo[1]) << 16);
+            plo.y = (uint32_t)__bfloat16_as_ushort(lo[2]) | ((uint32_t)__bfloat16_as_ushort(lo[3]) << 16);
+            for (int sg = 0; sg < nseg; ++sg) {
+                const bool use_lo = (pattern == 1 && sg == 2) || (pattern == 2 && sg == 1);
+                *reinterpret_cast<uint2*>(dst_rm + (int64_t)r * ldm + sg * kseg_m + c) = use_lo ? plo : phi;
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            thi[4 * q + e][rr] = hi[e];
+            tlo[4 * q + e][rr] = lo[e];
+        }
+    }
+    __syncthreads();
+    if (!dstT) return;
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int cc = (tid >> 3) + 32 * it, o = tid & 7;
+        const int c = c0 + cc, r = r0 + 8 * o;
+        if (c >= cols || r >= rows_pad) continue;
+        for (int sg = 0; sg < nseg; ++sg) {
+            const bool use_lo = (pattern == 1 && sg == 2) || (pattern == 2 && sg == 1);
+            const __nv_bfloat16* t = use_lo ? &tlo[cc][8 * o] : &thi[cc][8 * o];
+            __nv_bfloat16* d = dstT + (int64_t)c * ldt + sg * kseg_t + r;
+            if (r + 8 <= rows_pad) {
+                *reinterpret_cast<uint4*>(d) = *reinterpret_cast<const uint4*>(t);
+            } else {
+                for (int e = 0; e < 8 && r + e < rows_pad; ++e) d[e] = t[e];
+            }
+        }
+    }
+}
+
 }  // namespace
 
 lstm_status transpose_to_bf16_split(const Plan& p, const void* src, bool src_bf16, int64_t lds, int col0,
@@ -80,6 +163,24 @@ lstm_status transpose_to_bf16_split(const Plan& p, const void* src, bool src_bf1
 {
     rows_pad = rows_pad < rows ? rows : rows_pad;
     if (rows_pad <= 0 || cols <= 0) return LSTM_OK;
+    const bool v4 = cols % 4 == 0 && col0 % 4 == 0 && lds % 4 == 0 && ((uintptr_t)src & 15u) == 0 &&
+                    (!dst_rm || (ldm % 4 == 0 && kseg_m % 4 == 0 && ((uintptr_t)dst_rm & 15u) == 0)) &&
+                    (!dstT || (ldt % 8 == 0 && kseg_t % 8 == 0 && ((uintptr_t)dstT & 15u) == 0));
+    if (v4) {
+        const dim3 grid4((rows_pad + 63) / 64, (cols + 63) / 64);
+        trace_begin(p, K_CONVERT, s);
+        if (src_bf16)
+            transpose_bf16_v4_kernel<__nv_bfloat16><<<grid4, 256, 0, s>>>(
+                (const __nv_bfloat16*)src, lds, col0, map, rows, rows_pad, cols, pattern, (__nv_bfloat16*)dstT, ldt,
+                kseg_t, (__nv_bfloat16*)dst_rm, ldm, kseg_m);
+        else
+            transpose_bf16_v4_kernel<float><<<grid4, 256, 0, s>>>((const float*)src, lds, col0, map, rows, rows_pad,
+                                                                  cols, pattern, (__nv_bfloat16*)dstT, ldt, kseg_t,
+                                                                  (__nv_bfloat16*)dst_rm, ldm, kseg_m);
+        const cudaError_t e = cudaGetLastError();
+        trace_end(p, K_CONVERT, s, e == cudaSuccess ? 1 : 0);
+        return e == cudaSuccess ? LSTM_OK : LSTM_ERR_CUDA;
+    }
     const dim3 grid((rows_pad + 31) / 32, (cols + 31) / 32);
     trace_begin(p, K_CONVERT, s);
     if (src_bf16)
