@@ -123,7 +123,7 @@ def gpu_index(local_rank: int) -> int:
 
 # --------------------------------------------------------------------------- algorithmic work
 
-def kind_work(kind: str, spec, rows: int, D0: int, uses_tensor: dict):
+def kind_work(kind: str, spec, rows: int, D0: int):
     """Algorithmic (flops, HBM bytes) of one step's launches of `kind`, summed over layers."""
     H, nd, e = spec.hidden_size, spec.num_directions, (2 if spec.dtype == "bf16" else 4)
     fl = by = 0.0
@@ -190,7 +190,7 @@ def roofline_of(kind, ms_per_step, calls_per_step, spec, rows, T, D0, peaks, rec
     the sustained measured bf16 peak, or HBM when the bytes take longer.  The rest:
     HBM (measured copy bandwidth) or CUDA-core FP32 (derived) whichever bounds it.
     """
-    fl, by = kind_work(kind, spec, rows, D0, {})
+    fl, by = kind_work(kind, spec, rows, D0)
     sec = ms_per_step / 1e3
     clk = float(peaks.get("sm_max_mhz", 2070.0))
     per = max(1.0, calls_per_step)
