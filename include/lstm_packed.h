@@ -352,11 +352,14 @@ int64_t lstm_plan_launch_count(const lstm_plan* plan);
  *       tcgen05 product over the whole GPU and a cell kernel (bf16 layers
  *       whose R does not fit one cluster, H > 512);
  * ctas_per_direction: CTAs that hold one direction's recurrent weights;
- * product: 0 CUDA cores, 1 warp-level mma.sync, 2 tcgen05 with TMEM accumulators.
+ * product: 0 CUDA cores, 1 warp-level mma.sync, 2 tcgen05 with TMEM accumulators;
+ * variant (cluster kernels): bit 0 = operands exchanged by bulk copies into
+ * double buffers (else DSMEM stores between cluster-barrier halves), bit 1 =
+ * the cell's operands arrive as TMA tiles.
  * Any output pointer may be NULL.  LSTM_ERR_INVALID_ARG for a NULL plan or a
  * pass other than 0 or 1.  Host only; no device work. */
 lstm_status lstm_plan_recurrent_config(const lstm_plan* plan, int32_t pass, int32_t* kind,
-                                       int32_t* ctas_per_direction, int32_t* product);
+                                       int32_t* ctas_per_direction, int32_t* product, int32_t* variant);
 
 /* Per-step phase stamps of the recurrent kernels (diagnostics).  With a
  * device buffer of 2 * ndir * steps * 8 int64 set, CTA 0 of each direction
@@ -375,6 +378,14 @@ lstm_status lstm_debug_trace_steps(lstm_plan* plan, int64_t* device_buffer, int3
  * Either way the launch returns and LSTM_ERR_TIMEOUT is reported: the failure
  * path runs without a GPU fault. */
 lstm_status lstm_debug_skip_arrival(lstm_plan* plan, int32_t cta);
+
+/* Test hook: restricts the cluster recurrent kernels to one variant (-1 =
+ * automatic choice; else bit 0 = bulk-copy exchange, bit 1 = TMA operand
+ * tiles, as lstm_plan_recurrent_config reports them).  When the forced
+ * variant does not fit (shared memory, co-residency), the plan falls back to
+ * the grid kernel exactly as when no cluster variant fits.  Lets parity tests
+ * reach every variant at small sizes.  LSTM_ERR_INVALID_ARG outside -1..3. */
+lstm_status lstm_debug_cluster_variant(lstm_plan* plan, int32_t variant);
 
 #ifdef __cplusplus
 }

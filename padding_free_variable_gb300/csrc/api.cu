@@ -523,7 +523,7 @@ lstm_status lstm_fwd(const lstm_plan* plan, const lstm_layer_shape* shape,
     if (wide_step_path(p, s)) {
         if ((st = input_projection(p, s, *params, x_packed, ga, (char*)workspace + L.xs_off, cs)) != LSTM_OK)
             return st;
-        p.last_rec_kind[0] = 3; p.last_rec_ctas[0] = 0; p.last_rec_mma[0] = 2;
+        p.last_rec_kind[0] = 3; p.last_rec_ctas[0] = 0; p.last_rec_mma[0] = 2; p.last_rec_variant[0] = 0;
         return stepwise_fwd_core(p, s, *params, y_packed, y_lo, h_n, c_n, ga, cbuf,
                                  (float*)((char*)workspace + L.rh_off), (__nv_bfloat16*)((char*)workspace + L.hb_off),
                                  cs);
@@ -543,6 +543,7 @@ lstm_status lstm_fwd(const lstm_plan* plan, const lstm_layer_shape* shape,
         a.off_acc = cl_layout.off_acc; a.off_state = cl_layout.off_state; a.off_sums = cl_layout.off_sums;
         a.off_peep = cl_layout.off_peep; a.off_tab = cl_layout.off_tab;
         p.last_rec_kind[0] = 2; p.last_rec_ctas[0] = rcc.G; p.last_rec_mma[0] = 2;
+        p.last_rec_variant[0] = (rcc.bulk ? 1 : 0) | (rcc.tma_pre ? 2 : 0);
         return rec_cluster_fwd_launch(p, rcc, a, cs);
     }
     p.last_rec_kind[0] = 1; p.last_rec_ctas[0] = rc.G; p.last_rec_mma[0] = rc.mma;
@@ -586,7 +587,7 @@ lstm_status lstm_bwd(const lstm_plan* plan, const lstm_layer_shape* shape,
     if (wide_step_path(p, s)) {
         const StepScratch q = step_scratch(p, s);
         char* sc = (char*)scratch;
-        p.last_rec_kind[1] = 3; p.last_rec_ctas[1] = 0; p.last_rec_mma[1] = 2;
+        p.last_rec_kind[1] = 3; p.last_rec_ctas[1] = 0; p.last_rec_mma[1] = 2; p.last_rec_variant[1] = 0;
         return stepwise_bwd_core(p, s, *params, x_packed, y_packed, ga, cbuf, dy_packed, dx_packed, *grads, scratch,
                                  (float*)(sc + q.dh), (float*)(sc + q.dcc), (__nv_bfloat16*)(sc + q.dab),
                                  (__nv_bfloat16*)(sc + q.rt), cs);
@@ -604,9 +605,10 @@ lstm_status lstm_bwd(const lstm_plan* plan, const lstm_layer_shape* shape,
         a.off_acc = cl_layout.off_acc; a.off_state = cl_layout.off_state; a.off_sums = cl_layout.off_sums;
         a.off_peep = cl_layout.off_peep; a.off_tab = cl_layout.off_tab;
         p.last_rec_kind[1] = 2; p.last_rec_ctas[1] = rcc.G; p.last_rec_mma[1] = 2;
+        p.last_rec_variant[1] = (rcc.bulk ? 1 : 0) | (rcc.tma_pre ? 2 : 0);
         if ((st = rec_cluster_bwd_launch(p, rcc, a, (float*)scratch, cs)) != LSTM_OK) return st;
     } else {
-        p.last_rec_kind[1] = 1; p.last_rec_ctas[1] = rc.G; p.last_rec_mma[1] = rc.mma;
+        p.last_rec_kind[1] = 1; p.last_rec_ctas[1] = rc.G; p.last_rec_mma[1] = rc.mma; p.last_rec_variant[1] = 0;
         if ((st = rec_launch(p, rc, a, true, cs)) != LSTM_OK) return st;
     }
 

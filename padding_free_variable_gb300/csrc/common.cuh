@@ -44,6 +44,7 @@ struct Plan {
     uint64_t wait_limit_ns = 2000000000ull;
     int32_t debug_skip_cta = -1;
     int32_t forced_ctas = 0;        // 0 = automatic
+    int32_t forced_variant = -1;    // cluster kernels: -1 automatic, else bit 0 bulk exchange, bit 1 TMA tiles
     int32_t gemm_engine = 0;        // 0 = tensor cores for bf16 operands, 1 = CUDA cores
     int device = 0;
     int num_sms = 0;
@@ -70,6 +71,7 @@ struct Plan {
     mutable int32_t last_rec_kind[2] = {0, 0};   // 0 none, 1 grid kernel, 2 cluster kernel
     mutable int32_t last_rec_ctas[2] = {0, 0};   // CTAs per direction
     mutable int32_t last_rec_mma[2] = {0, 0};    // 0 CUDA cores, 1 mma.sync, 2 tcgen05
+    mutable int32_t last_rec_variant[2] = {0, 0}; // cluster kernels: bit 0 bulk exchange, bit 1 TMA tiles
 };
 
 // Bracket a launch sequence of `kind`; `kernels` = launches it issued.  A

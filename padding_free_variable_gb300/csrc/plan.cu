@@ -327,12 +327,13 @@ int64_t lstm_plan_launch_count(const lstm_plan* plan)
 }
 
 lstm_status lstm_plan_recurrent_config(const lstm_plan* plan, int32_t pass, int32_t* kind,
-                                       int32_t* ctas_per_direction, int32_t* product)
+                                       int32_t* ctas_per_direction, int32_t* product, int32_t* variant)
 {
     if (!plan || pass < 0 || pass > 1) return LSTM_ERR_INVALID_ARG;
     if (kind) *kind = plan->p.last_rec_kind[pass];
     if (ctas_per_direction) *ctas_per_direction = plan->p.last_rec_ctas[pass];
     if (product) *product = plan->p.last_rec_mma[pass];
+    if (variant) *variant = plan->p.last_rec_variant[pass];
     return LSTM_OK;
 }
 
@@ -362,6 +363,13 @@ lstm_status lstm_debug_skip_arrival(lstm_plan* plan, int32_t cta)
 {
     if (!plan || cta < -1) return LSTM_ERR_INVALID_ARG;
     plan->p.debug_skip_cta = cta;
+    return LSTM_OK;
+}
+
+lstm_status lstm_debug_cluster_variant(lstm_plan* plan, int32_t variant)
+{
+    if (!plan || variant < -1 || variant > 3) return LSTM_ERR_INVALID_ARG;
+    plan->p.forced_variant = variant;
     return LSTM_OK;
 }
 

@@ -1147,6 +1147,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
                 }
                 bulk_commit();
             }
+            if (!tma_opnd && s + 1 < T) load_own(s + 1);   // the next step's own operands
             cstamp(a, true, dir, rank, s, 3, 3);
         } else {
             cluster_wait();        // every peer has read its inbox of this step
@@ -1332,6 +1333,7 @@ bool rec_cluster_fwd_configure(const Plan& p, int H, int ndir, bool bf16, RecCon
     const int order[4][2] = {{1, 1}, {0, 1}, {1, 0}, {0, 0}};
     for (int oi = 0; oi < 4; ++oi) {
         const int bulk = order[oi][0], pre = order[oi][1];
+        if (p.forced_variant >= 0 && p.forced_variant != (bulk | pre << 1)) continue;
         const size_t bbytes = bulk ? 2 * (split ? 2 : 1) * (size_t)G * NBM * 64 : (split ? 2 : 1) * (size_t)KB * NBM * 128;
         size_t off = 0;
         const size_t o_b = off; off = al(off + bbytes, 1024);
@@ -1422,9 +1424,11 @@ bool rec_cluster_bwd_configure(const Plan& p, int H, int ndir, bool bf16, RecCon
     const uint32_t cols = pow2_cols(MT * nch * NBM + acols);
     // bulk exchange with operand tiles first, then the single-buffered barrier exchange with
     // and without tiles (the last needs the least shared memory)
-    const int order[3][2] = {{1, 1}, {0, 1}, {0, 0}};
-    for (int oi = 0; oi < 3; ++oi) {
+    const int order[4][2] = {{1, 1}, {0, 1}, {0, 0}, {1, 0}};
+    for (int oi = 0; oi < 4; ++oi) {
         const int bulk = order[oi][0], tiles = order[oi][1];
+        if (oi == 3 && p.forced_variant < 0) break;   // the bulk exchange without tiles only on request
+        if (p.forced_variant >= 0 && p.forced_variant != (bulk | tiles << 1)) continue;
         size_t off = 0;
         const size_t o_b = off; off = al(off + (split ? 2 : 1) * (size_t)2 * NBM * 128, 1024);
         const size_t o_in = off; off = al(off + (bulk ? 2 : 1) * (size_t)G * NBM * kCU * 4, 1024);

@@ -76,12 +76,13 @@ class Plan:
 
     def recurrent_config(self, backward: bool = False) -> dict:
         """Configuration of the last forward (or backward) recurrent launch."""
-        k, g, m = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        k, g, m, v = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
         check(_lib.load().lstm_plan_recurrent_config(self.handle, int(bool(backward)), ctypes.byref(k),
-                                                     ctypes.byref(g), ctypes.byref(m)),
+                                                     ctypes.byref(g), ctypes.byref(m), ctypes.byref(v)),
               "lstm_plan_recurrent_config")
         return {"kernel": ("none", "grid", "cluster", "step_launches")[k.value], "ctas_per_direction": g.value,
-                "product": ("cuda_cores", "mma_sync", "tcgen05")[m.value]}
+                "product": ("cuda_cores", "mma_sync", "tcgen05")[m.value],
+                "exchange": "bulk" if v.value & 1 else "barrier", "tma_tiles": bool(v.value & 2)}
 
     def trace_steps(self, buffer, steps: int):
         """Phase stamps into `buffer` (int64 device tensor of 2*ndir*steps*8), or off with steps=0."""
@@ -93,6 +94,10 @@ class Plan:
 
     def debug_skip_arrival(self, cta: int):
         check(_lib.load().lstm_debug_skip_arrival(self.handle, int(cta)), "lstm_debug_skip_arrival")
+
+    def debug_cluster_variant(self, variant: int):
+        """Restrict the cluster recurrent kernels to one variant (-1 automatic; bit 0 bulk, bit 1 TMA tiles)."""
+        check(_lib.load().lstm_debug_cluster_variant(self.handle, int(variant)), "lstm_debug_cluster_variant")
 
     def poll(self, stream=None) -> int:
         """Synchronise and return (and clear) the device status code."""

@@ -72,7 +72,8 @@ def device_layers(w, device="cuda"):
     return out
 
 
-def run_gpu(w, padded: bool = False, device="cuda", ctas: int = 0, engine: int = 0, stepwise: bool = False):
+def run_gpu(w, padded: bool = False, device="cuda", ctas: int = 0, engine: int = 0, stepwise: bool = False,
+            variant: int = -1):
     """pack -> all layers forward -> all layers backward -> unpack, through the C ABI."""
     import torch
     from padding_free_variable_gb300 import ops
@@ -80,6 +81,8 @@ def run_gpu(w, padded: bool = False, device="cuda", ctas: int = 0, engine: int =
     plan = ops.Plan(w.lengths, padded=padded)
     if ctas:
         plan.set_ctas_per_direction(ctas)
+    if variant >= 0:
+        plan.debug_cluster_variant(variant)
     if engine:
         plan.set_gemm_engine(engine)
     stack = ops.PackedLSTMStack(plan, device_layers(w, device), w.spec.input_size, w.spec.hidden_size,

@@ -46,7 +46,7 @@ def test_cluster_kernels_match_oracle(case):
     gpu = run_gpu(w)
     for backward in (False, True):
         cfg = gpu["plan"].recurrent_config(backward)
-        assert cfg == {"kernel": "cluster", "ctas_per_direction": H // 32, "product": "tcgen05"}, cfg
+        assert (cfg["kernel"], cfg["ctas_per_direction"], cfg["product"]) == ("cluster", H // 32, "tcgen05"), cfg
     ref = run_oracle(w)
     compare_all(gpu, ref, TOL_BF16 if dtype == "bf16" else TOL_F32, label=f"cluster {case}")
     if dtype == "bf16":
@@ -55,6 +55,32 @@ def test_cluster_kernels_match_oracle(case):
     grid = run_gpu(w, ctas=H // 32)          # an explicit CTA count selects the grid kernels
     for k in ("y", "dx", "h_n", "c_n"):
         assert rel_err(gpu[k], grid[k]) <= (TOL_BF16 if dtype == "bf16" else TOL_F32), k
+
+
+VARIANT_CASES = [
+    (2, 1, 16, 64, [9, 0, 4, 21, 21, 2, 7], "f32"),
+    (2, 2, 24, 128, [17, 2, 9, 33, 1, 0, 12, 33], "f32"),
+    (1, 1, 32, 256, list(np.random.default_rng(12).integers(1, 40, 40)), "f32"),
+    (2, 1, 32, 256, [60, 3, 44, 17, 60, 9], "bf16"),
+]
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2, 3], ids=["barrier", "bulk", "barrier-tiles", "bulk-tiles"])
+@pytest.mark.parametrize("case", VARIANT_CASES, ids=[f"nd{c[0]}-L{c[1]}-H{c[3]}-{c[5]}" for c in VARIANT_CASES])
+def test_every_cluster_variant_matches_oracle(case, variant):
+    """Each exchange (DSMEM stores between barrier halves, or bulk copies into double
+    buffers) with and without TMA operand tiles: the automatic choice picks by shared
+    memory, so small batches alone would reach only one of them."""
+    nd, nl, D, H, lengths, dtype = case
+    w = synthetic.custom(nd, nl, D, H, lengths, seed=40 + H + variant, dtype=dtype,
+                         weight_range=0.1 if dtype == "bf16" else 0.3)
+    gpu = run_gpu(w, variant=variant)
+    for backward in (False, True):
+        cfg = gpu["plan"].recurrent_config(backward)
+        assert cfg["kernel"] == "cluster", cfg
+        assert cfg["exchange"] == ("bulk" if variant & 1 else "barrier"), cfg
+        assert cfg["tma_tiles"] == bool(variant & 2), cfg
+    compare_all(gpu, run_oracle(w), TOL_BF16 if dtype == "bf16" else TOL_F32, label=f"variant {variant} {case}")
 
 
 def test_cluster_kernels_padded_plan():

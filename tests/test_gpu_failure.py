@@ -41,7 +41,8 @@ def test_barrier_timeout_is_reported_and_context_survives():
     assert torch.isfinite(y1).all()
 
 
-def test_cluster_kernels_timeout_is_reported_and_context_survives():
+@pytest.mark.parametrize("variant", [-1, 0, 2], ids=["auto", "barrier", "barrier-tiles"])
+def test_cluster_kernels_timeout_is_reported_and_context_survives(variant):
     """The cluster kernels' waits that can run out are the bounded waits on MMA completion
     (and, with the bulk exchange, on the peers' operands).  With the test hook one CTA
     withholds the completion signal of its first product: its wait runs out, it stops
@@ -55,6 +56,7 @@ def test_cluster_kernels_timeout_is_reported_and_context_survives():
 
     def fresh():
         plan = ops.Plan(w.lengths)
+        plan.debug_cluster_variant(variant)
         stack = ops.PackedLSTMStack(plan, layers, 8, 64, 2, False)
         return plan, stack
 
@@ -63,8 +65,11 @@ def test_cluster_kernels_timeout_is_reported_and_context_survives():
     ref_plan, ref_stack = fresh()
     y_ref, dx_ref = (t.clone() for t in ref_stack.step(x, G))
     assert ref_plan.poll() == _lib.LSTM_OK
-    assert ref_plan.recurrent_config(False)["kernel"] == "cluster"
-    assert ref_plan.recurrent_config(True)["kernel"] == "cluster"
+    for backward in (False, True):
+        cfg = ref_plan.recurrent_config(backward)
+        assert cfg["kernel"] == "cluster", cfg
+        if variant >= 0:
+            assert (cfg["exchange"] == "bulk") == bool(variant & 1) and cfg["tma_tiles"] == bool(variant & 2), cfg
 
     plan, stack = fresh()
     plan.set_wait_limit(50_000_000)          # 50 ms
