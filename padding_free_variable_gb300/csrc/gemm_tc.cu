@@ -9,13 +9,16 @@
 //               4-stage ring of 128-byte-swizzled shared-memory slots
 //   warp 1      owns the 256 TMEM columns; one thread issues tcgen05.mma
 //               (M=128, N=256, K=16) and commits each stage back to the ring
-//   warps 2..5  epilogue: tcgen05.ld of their TMEM lane quarter, + bias, store
+//   warps 2..5  epilogue: tcgen05.ld of their TMEM lane quarter, + bias, store (the
+//               persistent kernel stages 32 x 32 pieces in shared memory and writes them
+//               with TMA stores: whole 128-byte rows instead of 16-byte pieces of 32 rows)
 //
 // Every mbarrier wait is bounded; a timeout is recorded in the plan's status
 // word and the CTA still frees its tensor memory before returning.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "gemm.cuh"
 #include "tc_ptx.cuh"
@@ -30,6 +33,12 @@ constexpr uint32_t A_BYTES = TBM * TBK * 2;
 constexpr uint32_t B_BYTES = TBN * TBK * 2;
 constexpr uint32_t TMEM_COLS = 256;
 constexpr size_t TC_SMEM = 1024 + (size_t)TSTAGES * (A_BYTES + B_BYTES) + 256;
+// persistent kernel: the epilogue warps' output staging, two 32 x 32 fp32 boxes per warp
+constexpr int EPI_COLS = 32;
+constexpr uint32_t EPI_BOX_BYTES = 32 * EPI_COLS * 4;
+constexpr uint32_t EPI_BYTES = 4 * 2 * EPI_BOX_BYTES;
+constexpr size_t TC_SMEM_P = TC_SMEM + EPI_BYTES;
+static_assert(TC_SMEM_P <= 227 * 1024, "shared memory of the persistent kernel");
 
 struct TcArgs {
     int M, N, K;
@@ -184,13 +193,15 @@ __device__ __forceinline__ void tc_gemm_tile(const CUtensorMap* mapA, const CUte
 // accf per buffer (MMA -> epilogue) and acce per buffer (the 4 epilogue warps -> MMA).
 __global__ void __launch_bounds__(TC_THREADS, 1)
 gemm_tc_bf16_persistent_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-                               TcArgs a, int nM, int nN, int splits)
+                               const __grid_constant__ CUtensorMap mapC, TcArgs a, int nM, int nN, int splits,
+                               int tma_c)
 {
     extern __shared__ unsigned char smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = base;
     uint8_t* sB = base + TSTAGES * A_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(base + TSTAGES * (A_BYTES + B_BYTES));
+    uint8_t* stg = base + TSTAGES * (A_BYTES + B_BYTES);      // 1024-aligned output staging
+    uint64_t* full = reinterpret_cast<uint64_t*>(stg + EPI_BYTES);
     uint64_t* empty = full + TSTAGES;
     uint64_t* accf = empty + TSTAGES;        // [2]
     uint64_t* acce = accf + 2;               // [2]
@@ -213,6 +224,7 @@ gemm_tc_bf16_persistent_kernel(const __grid_constant__ CUtensorMap mapA, const _
         tc::fence_mbar_init();
         tc::prefetch_tensormap(&mapA);
         tc::prefetch_tensormap(&mapB);
+        if (tma_c) tc::prefetch_tensormap(&mapC);
     }
     if (warp == 1) {
         tc::tmem_alloc(tmem_slot, 2 * TMEM_COLS);
@@ -286,6 +298,11 @@ gemm_tc_bf16_persistent_kernel(const __grid_constant__ CUtensorMap mapA, const _
     } else if (warp >= 2) {
         // ---- epilogue: this warp reads TMEM lanes 32*(warp%4) .. +31 of the tile's buffer
         const int q = warp & 3;
+        // tma_c: 32-column pieces go through this warp's two staging boxes (128-byte swizzle:
+        // 16-byte chunk j of row r at chunk j ^ (r & 7), so each 8-lane phase of the v4 stores
+        // covers all banks) and leave as one TMA store each: whole 128-byte rows, clipped to C
+        float* const box0 = reinterpret_cast<float*>(stg + (size_t)q * 2 * EPI_BOX_BYTES);
+        int pieces = 0;                       // this warp's staged pieces so far (box = pieces & 1)
         int i = 0;
         for (int tile = blockIdx.x; tile < ntiles && !*(volatile int*)s_abort; tile += gridDim.x, ++i) {
             int z, m0, n0, kbeg, nk;
@@ -300,34 +317,77 @@ gemm_tc_bf16_persistent_kernel(const __grid_constant__ CUtensorMap mapA, const _
             const float* const bias = split ? nullptr : a.bias;
             const bool vec = (ldo % 4) == 0 && (((uintptr_t)Cout) & 15u) == 0;
             const int row = m0 + q * 32 + lane;
-            for (int c = 0; c < TBN; c += 16) {
-                if (n0 + c >= a.N) break;                      // uniform across the warp
-                uint32_t r[16];
-                if (nk > 0) {
-                    tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * TMEM_COLS + c), r);
-                    tc::tmem_wait_ld();
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) r[e] = 0u;   // empty k range: a zero product
-                }
-                if (row < a.M) {
-                    const int n = n0 + c;
-                    float* out = Cout + (int64_t)row * ldo + n;
-                    float v[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
-                    if (n + 16 <= a.N && vec) {
-                        if (bias) {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) v[e] += __ldg(bias + n + e);
-                        }
-#pragma unroll
-                        for (int e = 0; e < 16; e += 4)
-                            *reinterpret_cast<float4*>(out + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+            if (tma_c && !split) {
+                // a warp whose 32 rows all lie past M (last row block) has nothing to store
+                const int cend = m0 + q * 32 < a.M ? TBN : 0;
+                const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * TMEM_COLS);
+                for (int c = 0; c < cend; c += EPI_COLS) {
+                    if (n0 + c >= a.N) break;                  // uniform across the warp
+                    uint32_t r0[16], r1[16];
+                    if (nk > 0) {
+                        tc::tmem_ld_32x32b_x16(tq + (uint32_t)c, r0);
+                        tc::tmem_ld_32x32b_x16(tq + (uint32_t)(c + 16), r1);
+                        tc::tmem_wait_ld();
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            if (n + e < a.N) out[e] = v[e] + (bias ? __ldg(bias + n + e) : 0.f);
+                        for (int e = 0; e < 16; ++e) r0[e] = r1[e] = 0u;   // empty k range: a zero product
+                    }
+                    // bias of the piece's 32 columns: one coalesced load, then broadcast by shuffle
+                    const int nb = n0 + c + lane;
+                    const float bl = (bias && nb < a.N) ? __ldg(bias + nb) : 0.f;
+                    float* const box = box0 + (pieces & 1) * (EPI_BOX_BYTES / 4);
+                    if (lane == 0) tc::bulk_wait_group_read<1>();   // this box's previous store has read it
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        float v[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int col = 4 * j + e;
+                            const uint32_t raw = col < 16 ? r0[col] : r1[col - 16];
+                            v[e] = __uint_as_float(raw) + __shfl_sync(0xffffffffu, bl, col);
+                        }
+                        *reinterpret_cast<float4*>(box + lane * EPI_COLS + ((j ^ (lane & 7)) * 4)) =
+                            make_float4(v[0], v[1], v[2], v[3]);
+                    }
+                    tc::fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tc::tma_store_2d(&mapC, box, n0 + c, m0 + q * 32);
+                        tc::bulk_commit_group();
+                    }
+                    ++pieces;
+                }
+            } else {
+                for (int c = 0; c < TBN; c += 16) {
+                    if (n0 + c >= a.N) break;                      // uniform across the warp
+                    uint32_t r[16];
+                    if (nk > 0) {
+                        tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * TMEM_COLS + c), r);
+                        tc::tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) r[e] = 0u;   // empty k range: a zero product
+                    }
+                    if (row < a.M) {
+                        const int n = n0 + c;
+                        float* out = Cout + (int64_t)row * ldo + n;
+                        float v[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
+                        if (n + 16 <= a.N && vec) {
+                            if (bias) {
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) v[e] += __ldg(bias + n + e);
+                            }
+#pragma unroll
+                            for (int e = 0; e < 16; e += 4)
+                                *reinterpret_cast<float4*>(out + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                if (n + e < a.N) out[e] = v[e] + (bias ? __ldg(bias + n + e) : 0.f);
+                        }
                     }
                 }
             }
@@ -336,6 +396,8 @@ gemm_tc_bf16_persistent_kernel(const __grid_constant__ CUtensorMap mapA, const _
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&acce[b]);
         }
+        // the stores must be complete before the kernel ends
+        if (tma_c && lane == 0) tc::bulk_wait_group_all();
     }
     tc::tc_fence_before_sync();
     __syncthreads();
@@ -408,6 +470,21 @@ bool make_map_f32(CUtensorMap* map, const float* ptr, int64_t rows, int64_t cols
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// C[M][N] fp32 with row pitch ldc as the epilogue's store target: 32 x 32 boxes, 128-byte
+// swizzle (the staging layout of the persistent kernel's epilogue warps).
+static bool make_map_c(CUtensorMap* map, float* C, int M, int N, int64_t ldc)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc || ((uintptr_t)C & 15u) || (ldc * 4) % 16 != 0) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)ldc * 4};
+    cuuint32_t box[2] = {(cuuint32_t)EPI_COLS, 32u};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool gemm_tc_supported(int M, int N, int K, const void* A, const void* B)
 {
     // TMA: 16-byte aligned bases and row pitches; x coordinates are multiples of 64 elements.
@@ -437,7 +514,7 @@ lstm_status gemm_tc_bf16(const Plan& p, int kind, const void* A, int64_t lda, co
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(gemm_tc_bf16_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)TC_SMEM) != cudaSuccess)
+                                 (int)TC_SMEM_P) != cudaSuccess)
             return LSTM_ERR_CUDA;
         attr_set = true;
     }
@@ -452,8 +529,12 @@ lstm_status gemm_tc_bf16(const Plan& p, int kind, const void* A, int64_t lda, co
     const int nM = (M + TBM - 1) / TBM, nN = (N + TBN - 1) / TBN;
     const int ntiles = nM * nN * splits;
     const dim3 grid((unsigned)std::min(ntiles, std::max(1, p.num_sms)));
+    // unsplit products store their tiles by TMA when C allows a tensor map
+    CUtensorMap mapC;
+    memset(&mapC, 0, sizeof(mapC));
+    const int tma_c = splits == 1 && make_map_c(&mapC, C, M, N, ldc) ? 1 : 0;
     trace_begin(p, kind, s);
-    gemm_tc_bf16_persistent_kernel<<<grid, TC_THREADS, TC_SMEM, s>>>(mapA, mapB, a, nM, nN, splits);
+    gemm_tc_bf16_persistent_kernel<<<grid, TC_THREADS, TC_SMEM_P, s>>>(mapA, mapB, mapC, a, nM, nN, splits, tma_c);
     cudaError_t e = cudaGetLastError();
     int launched = e == cudaSuccess ? 1 : 0;
     if (e == cudaSuccess && splits > 1) {
