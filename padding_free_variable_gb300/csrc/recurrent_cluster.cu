@@ -394,10 +394,16 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
         return Bb + (BULK ? (size_t)parity * (SPLIT ? 2 : 1) * bsz : 0) + (size_t)lo * bsz;
     };
     auto Stg = [&](int parity, int lo) -> uint8_t* { return stage + (size_t)(parity * 2 + lo) * ssz; };
-    // bytes a CTA receives for step s (h of step s - 1 from every CTA, rows rounded to 16)
+    // rows of h of step s2 - 1 that step s2 reads: the rows continuing into step s2.  Rows past
+    // them are never read going forward (finished sequences) and were never written going
+    // backward (sequences not yet started: still zero from the set-up)
+    auto step_rows = [&](int s2) -> int {
+        const int tp = dir == 0 ? s2 - 1 : T - s2, tn = dir == 0 ? s2 : T - 1 - s2;
+        return min(s_bs[tp], s_bs[tn]);
+    };
+    // bytes a CTA receives for step s2: those rows from every other CTA (its own it writes itself)
     auto step_bytes = [&](int s2) -> uint32_t {
-        const int tp = dir == 0 ? s2 - 1 : T - s2;
-        return (uint32_t)G * (SPLIT ? 2u : 1u) * (uint32_t)((s_bs[tp] + 15) & ~15) * 64u;
+        return (uint32_t)(G - 1) * (SPLIT ? 2u : 1u) * (uint32_t)step_rows(s2) * 64u;
     };
     const uint32_t tcols = (uint32_t)a.Umax;                         // Umax carries the TMEM columns
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -702,6 +708,10 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
                     const uint32_t o = sw64_off4(j, q8);
                     *reinterpret_cast<uint2*>(Stg(par, 0) + o) = xh[it];
                     if (SPLIT) *reinterpret_cast<uint2*>(Stg(par, 1) + o) = xl[it];
+                    // this CTA's own block of the next step's operand, written in place
+                    const size_t ob = (size_t)rank * NBM * 64 + o;
+                    *reinterpret_cast<uint2*>(Bop(par ^ 1, 0) + ob) = xh[it];
+                    if (SPLIT) *reinterpret_cast<uint2*>(Bop(par ^ 1, 1) + ob) = xl[it];
                 }
             }
             fence_proxy_async_cta();
@@ -710,8 +720,9 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
             const bool sender = lane == 0 && warp < G;
             if (s + 1 < T && sender && !failed) {
                 const uint32_t nxt = (uint32_t)(par ^ 1);
-                const uint32_t bytes = (uint32_t)NBs * 64u;
+                const uint32_t bytes = (uint32_t)step_rows(s + 1) * 64u;
                 for (int p2 = warp; p2 < G; p2 += kCT / 32) {
+                    if (p2 == (int)rank || bytes == 0) continue;
                     const uint32_t bar = mapa_u32(tc::smem_u32(&full_bar[nxt]), (uint32_t)p2);
                     bulk_to_peer(mapa_u32(tc::smem_u32(Bop(nxt, 0) + (size_t)rank * NBM * 64), (uint32_t)p2), Stg(par, 0),
                                  bytes, bar);
@@ -844,10 +855,15 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
         return inbox + (((size_t)(BULK ? parity : 0) * G + src) * NBM + j) * kCU;
     };
     auto tile = [&](int k, int j) -> float* { return tiles + ((size_t)k * NBM + j) * kCU; };
-    // bytes a CTA receives for step s2 (partials of step s2 - 1 from every CTA, rows rounded to 16)
+    // rows of the partials of step s2 - 1 that step s2 reads: its rows with a step after them
+    // (in recurrence order); the cell reads no others
+    auto step_rows = [&](int s2) -> int {
+        const int tp = dir == 0 ? T - s2 : s2 - 1, tn = dir == 0 ? T - 1 - s2 : s2;
+        return min(s_bs[tp], s_bs[tn]);
+    };
+    // bytes a CTA receives for step s2: those rows from every other CTA (its own it writes itself)
     auto step_bytes = [&](int s2) -> uint32_t {
-        const int tp = dir == 0 ? T - s2 : s2 - 1;
-        return (uint32_t)G * (uint32_t)((s_bs[tp] + 15) & ~15) * (uint32_t)(kCU * 4);
+        return (uint32_t)(G - 1) * (uint32_t)step_rows(s2) * (uint32_t)(kCU * 4);
     };
 
     for (int i = threadIdx.x; i < (SPLIT ? 2 : 1) * 2 * NBM * 128 / 16; i += kCT)
@@ -1123,7 +1139,8 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
                     const int m = pq >> 2, q = pq & 3;
                     const int owner = 4 * m + q;
                     if (owner >= G) continue;
-                    float* dst = stage + (size_t)owner * NBM * kCU;
+                    // this CTA's own units go straight into its next inbox
+                    float* dst = owner == (int)rank ? inbox_at(par ^ 1, rank, 0) : stage + (size_t)owner * NBM * kCU;
                     for (int c0 = 0; c0 < NBs; c0 += 16) {
                         float v[16];
                         tmem_sum_chains(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(m * nch * NBM + c0),
@@ -1139,8 +1156,9 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
             // lane 0 of warp w sends to owners w, w + 8 (copies issued by one warp's lanes serialise)
             if (s + 1 < T && !failed && lane == 0 && warp < G) {
                 const uint32_t nxt = (uint32_t)(par ^ 1);
-                const uint32_t bytes = (uint32_t)NBs * (uint32_t)(kCU * 4);
+                const uint32_t bytes = (uint32_t)step_rows(s + 1) * (uint32_t)(kCU * 4);
                 for (int o = warp; o < G; o += kCT / 32) {
+                    if (o == (int)rank || bytes == 0) continue;
                     const uint32_t bar = mapa_u32(tc::smem_u32(&full_bar[nxt]), (uint32_t)o);
                     bulk_to_peer(mapa_u32(tc::smem_u32(inbox_at(nxt, rank, 0)), (uint32_t)o),
                                  stage + (size_t)o * NBM * kCU, bytes, bar);
