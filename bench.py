@@ -431,6 +431,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--no-comparators", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cluster-variant", type=int, default=-1,
+                    help="diagnostic: force the cluster recurrent kernels' variant (bit 0 bulk exchange, "
+                         "bit 1 TMA tiles); -1 = the library's own choice")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -443,6 +446,8 @@ def main():
               "directions": spec.num_directions, "gemm_operands": spec.dtype, "state": "f32",
               "lengths": str(spec.lengths), "seed": w.seed, "l2": "flushed (512 MiB write) before every timed step",
               "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+    if args.cluster_variant >= 0:
+        config["cluster_variant_forced"] = args.cluster_variant
     if args.impl == "reference":
         return reference_arm(args, w, config)
 
@@ -465,6 +470,8 @@ def main():
     bf16 = spec.dtype == "bf16"
     xdt = torch.bfloat16 if bf16 else torch.float32
     plan = ops.Plan(w.lengths)
+    if args.cluster_variant >= 0:
+        plan.debug_cluster_variant(args.cluster_variant)
     stack = ops.PackedLSTMStack(plan, device_layers(w), spec.input_size, spec.hidden_size,
                                 spec.num_directions, bf16)
     x_dev = torch.from_numpy(w.x).to("cuda", dtype=xdt)
