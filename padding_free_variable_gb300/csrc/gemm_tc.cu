@@ -18,6 +18,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "gemm.cuh"
@@ -472,6 +473,23 @@ bool make_map_f32(CUtensorMap* map, const float* ptr, int64_t rows, int64_t cols
 
 // C[M][N] fp32 with row pitch ldc as the epilogue's store target: 32 x 32 boxes, 128-byte
 // swizzle (the staging layout of the persistent kernel's epilogue warps).
+// The kernel's dynamic shared-memory limit, raised once per device (the attribute belongs
+// to the device's context, so a process driving several GPUs sets it on each).
+static bool smem_attr_ready(const void* fn, int bytes)
+{
+    constexpr int kMaxDevices = 64;
+    static std::atomic<uint64_t> done_persistent{0}, done_pair{0};
+    std::atomic<uint64_t>& done =
+        fn == (const void*)gemm_tc_bf16_persistent_kernel ? done_persistent : done_pair;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return false;
+    const uint64_t bit = dev < kMaxDevices ? (uint64_t)1 << dev : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return true;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+    if (bit) done.fetch_or(bit, std::memory_order_release);
+    return true;
+}
+
 static bool make_map_c(CUtensorMap* map, float* C, int M, int N, int64_t ldc)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
@@ -511,13 +529,7 @@ lstm_status gemm_tc_bf16(const Plan& p, int kind, const void* A, int64_t lda, co
     if (splits > 1 && !partial) return LSTM_ERR_INVALID_ARG;
     CUtensorMap mapA, mapB;
     if (!make_map(&mapA, A, M, K, lda, TBM) || !make_map(&mapB, B, N, K, ldb, TBN)) return LSTM_ERR_UNSUPPORTED;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(gemm_tc_bf16_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)TC_SMEM_P) != cudaSuccess)
-            return LSTM_ERR_CUDA;
-        attr_set = true;
-    }
+    if (!smem_attr_ready((const void*)gemm_tc_bf16_persistent_kernel, (int)TC_SMEM_P)) return LSTM_ERR_CUDA;
     const int kblocks = (K + TBK - 1) / TBK;
     if (splits < 1) splits = 1;
     const int kb_per = (kblocks + splits - 1) / splits;
@@ -572,13 +584,7 @@ int gemm_tc_pair_splits(int rows_max, int N, int K, int products, int num_sms)
 lstm_status gemm_tc_pair(const Plan& p, int kind, const TcOperands& o0, int M0, const TcOperands* o1, int M1,
                          cudaStream_t s)
 {
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(gemm_tc_bf16_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)TC_SMEM) != cudaSuccess)
-            return LSTM_ERR_CUDA;
-        attr_set = true;
-    }
+    if (!smem_attr_ready((const void*)gemm_tc_bf16_pair_kernel, (int)TC_SMEM)) return LSTM_ERR_CUDA;
     if (!o1) { o1 = &o0; M1 = 0; }
     const int Mmax = std::max(M0, M1), Nmax = std::max(o0.N, o1->N);
     if (Mmax <= 0) return LSTM_OK;
