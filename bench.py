@@ -427,7 +427,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--workload", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--no-comparators", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -464,15 +464,13 @@ def main():
         native.build()
     if dist:
         dist.barrier()
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from gpu_harness import device_layers
 
     bf16 = spec.dtype == "bf16"
     xdt = torch.bfloat16 if bf16 else torch.float32
     plan = ops.Plan(w.lengths)
     if args.cluster_variant >= 0:
         plan.debug_cluster_variant(args.cluster_variant)
-    stack = ops.PackedLSTMStack(plan, device_layers(w), spec.input_size, spec.hidden_size,
+    stack = ops.PackedLSTMStack(plan, ops.device_layers(w.layers, bf16), spec.input_size, spec.hidden_size,
                                 spec.num_directions, bf16)
     x_dev = torch.from_numpy(w.x).to("cuda", dtype=xdt)
     G_dev = torch.from_numpy(w.G).cuda()

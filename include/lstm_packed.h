@@ -254,11 +254,14 @@ lstm_status lstm_bwd(const lstm_plan* plan, const lstm_layer_shape* shape,
  * process exits.  The caller still passes all inputs and outputs.
  *   - Returns LSTM_ERR_UNSUPPORTED, launching nothing, when
  *     lstm_scratch_bytes(plan, shape) exceeds LSTM_NOALLOC_SCRATCH_BYTES.
+ *   - The plan's device must be the current device; otherwise
+ *     LSTM_ERR_INVALID_ARG and nothing is launched.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture begins.  Later calls only read the cached
  *     address.  Neither calls cudaMalloc, cudaFree or an allocating library
- *     routine.
+ *     routine.  The cached address does not survive cudaDeviceReset: after a
+ *     reset this entry point must not be called again in the process.
  *   - Every call on a device shares the one array and it keeps the last
  *     call's contents; nothing in it needs to start at zero.  Calls whose
  *     work overlaps on the GPU (other streams, other host threads) race on
@@ -330,8 +333,9 @@ lstm_status lstm_plan_read_timing(lstm_plan* plan, double* ms, int64_t* calls);
  * dX/dW/dR products as lstm_bwd.  Same arguments, layouts, results (within
  * the fp32 / bf16 tolerances) and errors as lstm_fwd / lstm_bwd, plus
  * `scratch` (device, 16-byte aligned, lstm_stepwise_scratch_bytes, owned by
- * the caller; the forward pass also needs it).  Padded plans are refused with
- * LSTM_ERR_UNSUPPORTED.  2·T·ndir + T launches per layer and pass. */
+ * the caller; the forward pass also needs it).  Padded plans run with the
+ * same masking as lstm_fwd / lstm_bwd.  2·T·ndir + T launches per layer and
+ * pass. */
 size_t lstm_stepwise_scratch_bytes(const lstm_plan* plan, const lstm_layer_shape* shape);
 lstm_status lstm_fwd_stepwise(const lstm_plan* plan, const lstm_layer_shape* shape,
                               const lstm_layer_params* params, const void* x_packed, float* y_packed,
@@ -360,6 +364,23 @@ int64_t lstm_plan_launch_count(const lstm_plan* plan);
  * pass other than 0 or 1.  Host only; no device work. */
 lstm_status lstm_plan_recurrent_config(const lstm_plan* plan, int32_t pass, int32_t* kind,
                                        int32_t* ctas_per_direction, int32_t* product, int32_t* variant);
+
+/* Sequence groups of the last cluster recurrent kernel run through this plan
+ * (`pass` as above): the sorted slots are cut into `groups` contiguous groups
+ * of `slots_per_group` slots (the last may be shorter), and each (direction,
+ * group) pair runs as its own thread-block cluster.  Sequences never interact
+ * in the recurrence, so the groups exchange nothing; each group runs only as
+ * many steps as its longest sequence.  Other recurrent kernels report one
+ * group of B slots; 0 before any recurrent launch.  Host only.
+ * LSTM_ERR_INVALID_ARG for a NULL plan or a pass other than 0 or 1. */
+lstm_status lstm_plan_recurrent_groups(const lstm_plan* plan, int32_t pass, int32_t* groups,
+                                       int32_t* slots_per_group);
+
+/* Test hook: slots per sequence group of the cluster recurrent kernels (0 =
+ * automatic: the smallest multiple of 8 that gives every cluster an SM of its
+ * own; 1..128 forces that many).  Results do not depend on it.
+ * LSTM_ERR_INVALID_ARG outside 0..128. */
+lstm_status lstm_debug_sequence_groups(lstm_plan* plan, int32_t slots);
 
 /* Per-step phase stamps of the recurrent kernels (diagnostics).  With a
  * device buffer of 2 * ndir * steps * 8 int64 set, CTA 0 of each direction

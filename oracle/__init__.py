@@ -13,6 +13,7 @@ from .oracle import (  # noqa: F401
     lstm_stack,
     lstm_padded_layer,
     pack_layer_params,
+    round_bf16,
     unpack_layer_grads,
 )
 from .padding import zero_padding_rate, waste_fraction, bucket_batches  # noqa: F401

@@ -78,6 +78,10 @@ static double to_bf16(double v)
 
 static double rb(double v) { return g_bf16_products ? to_bf16(v) : v; }
 
+/* The diagnostic mode's rounding, exported for its pin: v rounded to fp32,
+ * then to the nearest bfloat16 (ties to even); Inf and NaN pass through. */
+double oracle_round_bf16(double v) { return to_bf16(v); }
+
 static size_t layer_param_count(int ndir, int D, int H)
 {
     return (size_t)ndir * ((size_t)4 * H * D + (size_t)4 * H * H + (size_t)4 * H + (size_t)3 * H);
@@ -91,17 +95,19 @@ long oracle_layer_param_count(int ndir, int D, int H) { return (long)layer_param
  * x[L][D]; h, c [L][H] and g [L][4H] (post-activation i, f, z, o) are indexed
  * by frame position: h[t] is the state after consuming x[t].
  * reverse = 0 walks t = 0..L-1, reverse = 1 walks t = L-1..0.
+ * h0, c0 [H]: the state before the first step (NULL = zero; RETURNN paper,
+ * Sec. 3.2: one RNN's final state passed on as another's initial state).
  */
 void oracle_dir_forward(int L, int D, int H, const double* x,
                         const double* W, const double* R, const double* b, const double* p,
-                        int reverse, double* h, double* c, double* g)
+                        int reverse, const double* h0, const double* c0, double* h, double* c, double* g)
 {
     double* a = (double*)malloc(sizeof(double) * 4 * (size_t)H);
     for (int s = 0; s < L; ++s) {
         const int t = reverse ? L - 1 - s : s;
         const int tp = reverse ? t + 1 : t - 1;          /* previous step's position */
-        const double* hp = (s == 0) ? NULL : h + (size_t)tp * H;
-        const double* cp = (s == 0) ? NULL : c + (size_t)tp * H;
+        const double* hp = (s == 0) ? h0 : h + (size_t)tp * H;
+        const double* cp = (s == 0) ? c0 : c + (size_t)tp * H;
         for (int r = 0; r < 4 * H; ++r) {
             double acc = b[r];
             for (int k = 0; k < D; ++k) acc += W[(size_t)r * D + k] * x[(size_t)t * D + k];
@@ -131,12 +137,17 @@ void oracle_dir_forward(int L, int D, int H, const double* x,
 /*
  * BPTT for one direction over one sequence, given the forward results.
  * dy[L][H] is dL/dh_t from outside the recurrence (the layer above, or G).
- * Accumulates into dx[L][D], dW[4H][D], dR[4H][H], db[4H], dp[3][H].
+ * h0, c0 [H]: the initial state of the forward pass (NULL = zero).
+ * dhn, dcn [H]: dL/dh and dL/dc of the final state from outside (NULL = zero).
+ * Accumulates into dx[L][D], dW[4H][D], dR[4H][H], db[4H], dp[3][H]; writes
+ * dh0, dc0 [H] (dL/d of the initial state; either may be NULL).
  */
 void oracle_dir_backward(int L, int D, int H, const double* x,
                          const double* W, const double* R, const double* p, int reverse,
+                         const double* h0, const double* c0, const double* dhn, const double* dcn,
                          const double* h, const double* c, const double* g, const double* dy,
-                         double* dx, double* dW, double* dR, double* db, double* dp)
+                         double* dx, double* dW, double* dR, double* db, double* dp,
+                         double* dh0, double* dc0)
 {
     const size_t G4 = 4 * (size_t)H;
     double* da = (double*)malloc(sizeof(double) * G4);
@@ -150,22 +161,27 @@ void oracle_dir_backward(int L, int D, int H, const double* x,
         const int t = reverse ? L - 1 - s : s;
         const int tp = reverse ? t + 1 : t - 1;
         const double* gt = g + (size_t)t * G4;
-        /* error reaching h_t: from outside, and from every gate of the next step through R */
+        /* error reaching h_t: from outside, and from every gate of the next step through R
+         * (the last step: from the final state's own gradient instead) */
         for (int u = 0; u < H; ++u) {
             double acc = dy[(size_t)t * H + u];
             if (have_next)
                 for (size_t r = 0; r < G4; ++r) acc += R[r * H + u] * rb(da_next[r]);
+            else if (dhn)
+                acc += dhn[u];
             dh[u] = acc;
         }
         for (int u = 0; u < H; ++u) {
             const double ig = gt[u], fg = gt[H + u], zg = gt[2 * H + u], og = gt[3 * H + u];
             const double cn = c[(size_t)t * H + u];
-            const double cprev = (s > 0) ? c[(size_t)tp * H + u] : 0.0;
+            const double cprev = (s > 0) ? c[(size_t)tp * H + u] : (c0 ? c0[u] : 0.0);
             const double tc = tanh(cn);
             const double da_o = dh[u] * tc * og * (1.0 - og);
             double dc = dh[u] * og * (1.0 - tc * tc) + da_o * p[2 * H + u];
             if (have_next)
                 dc += dc_next[u] * f_next[u] + da_next[u] * p[u] + da_next[H + u] * p[H + u];
+            else if (dcn)
+                dc += dcn[u];
             const double da_i = dc * zg * ig * (1.0 - ig);
             const double da_f = dc * cprev * fg * (1.0 - fg);
             const double da_z = dc * ig * (1.0 - zg * zg);
@@ -183,6 +199,20 @@ void oracle_dir_backward(int L, int D, int H, const double* x,
             for (int k = 0; k < D; ++k) dW[r * D + k] += rb(da[r]) * x[(size_t)t * D + k];
             if (s > 0)
                 for (int k = 0; k < H; ++k) dR[r * H + k] += rb(da[r]) * rb(h[(size_t)tp * H + k]);
+            else if (h0)
+                for (int k = 0; k < H; ++k) dR[r * H + k] += rb(da[r]) * rb(h0[k]);
+        }
+        if (s == 0) {
+            /* the initial state: dh0 through R from the first step's gates, dc0 as the carry
+             * the first step passes back (forget gate and the i, f peepholes read c0) */
+            for (int u = 0; u < H; ++u) {
+                if (dh0) {
+                    double acc = 0.0;
+                    for (size_t r = 0; r < G4; ++r) acc += R[r * H + u] * rb(da[r]);
+                    dh0[u] = acc;
+                }
+                if (dc0) dc0[u] = dc_cur[u] * gt[H + u] + da[u] * p[u] + da[H + u] * p[H + u];
+            }
         }
         for (int k = 0; k < D; ++k) {
             double acc = 0.0;
@@ -229,10 +259,34 @@ static dir_view view_of(double* base, int ndir, int dir, int D, int H)
  * sums are then added in thread order.
  * Returns 0 on success, -1 on a bad argument or allocation failure.
  */
+int oracle_lstm_stack_state(int B, const int* lengths, int num_layers, int ndir, int H, int D0,
+                            const double* x_cat, double* const* layer_params, const double* dy_cat,
+                            const double* h0, const double* c0, const double* dh_n, const double* dc_n,
+                            double* y_cat, double* h_n, double* c_n, double* dx_cat,
+                            double* const* layer_grads, double* dh0, double* dc0, int nthreads);
+
 int oracle_lstm_stack(int B, const int* lengths, int num_layers, int ndir, int H, int D0,
                       const double* x_cat, double* const* layer_params, const double* dy_cat,
                       double* y_cat, double* h_n, double* c_n, double* dx_cat,
                       double* const* layer_grads, int nthreads)
+{
+    return oracle_lstm_stack_state(B, lengths, num_layers, ndir, H, D0, x_cat, layer_params, dy_cat, NULL, NULL,
+                                   NULL, NULL, y_cat, h_n, c_n, dx_cat, layer_grads, NULL, NULL, nthreads);
+}
+
+/*
+ * The same stack with initial states and final-state gradients (all
+ * [num_layers][ndir][B][H], caller order, NULL = zero):
+ *   h0, c0       state of every layer and direction before its first step
+ *   dh_n, dc_n   dL/dh_n, dL/dc_n from outside (a loss that reads the final states)
+ *   dh0, dc0     outputs: dL/dh0, dL/dc0 (NULL: not wanted)
+ * A sequence of length 0 consumes nothing: h_n = h0, c_n = c0, dh0 = dh_n, dc0 = dc_n.
+ */
+int oracle_lstm_stack_state(int B, const int* lengths, int num_layers, int ndir, int H, int D0,
+                            const double* x_cat, double* const* layer_params, const double* dy_cat,
+                            const double* h0, const double* c0, const double* dh_n, const double* dc_n,
+                            double* y_cat, double* h_n, double* c_n, double* dx_cat,
+                            double* const* layer_grads, double* dh0, double* dc0, int nthreads)
 {
     if (B < 0 || num_layers < 1 || (ndir != 1 && ndir != 2) || H < 1 || D0 < 1) return -1;
     long long* start = (long long*)malloc(sizeof(long long) * (size_t)(B + 1));
@@ -252,8 +306,11 @@ int oracle_lstm_stack(int B, const int* lengths, int num_layers, int ndir, int H
     }
     /* private gradient sums, one set per thread */
     double* gpriv = do_bwd ? (double*)calloc(gtotal * (size_t)nthreads, sizeof(double)) : NULL;
-    if (h_n) memset(h_n, 0, sizeof(double) * (size_t)num_layers * ndir * B * H);
-    if (c_n) memset(c_n, 0, sizeof(double) * (size_t)num_layers * ndir * B * H);
+    const size_t nst = (size_t)num_layers * ndir * B * H;
+    if (h_n) { if (h0) memcpy(h_n, h0, sizeof(double) * nst); else memset(h_n, 0, sizeof(double) * nst); }
+    if (c_n) { if (c0) memcpy(c_n, c0, sizeof(double) * nst); else memset(c_n, 0, sizeof(double) * nst); }
+    if (dh0) { if (dh_n) memcpy(dh0, dh_n, sizeof(double) * nst); else memset(dh0, 0, sizeof(double) * nst); }
+    if (dc0) { if (dc_n) memcpy(dc0, dc_n, sizeof(double) * nst); else memset(dc0, 0, sizeof(double) * nst); }
 
     int err = 0;
 #ifdef _OPENMP
@@ -282,7 +339,9 @@ int oracle_lstm_stack(int B, const int* lengths, int num_layers, int ndir, int H
                 double* h = hs[l * ndir + d] = (double*)malloc(sizeof(double) * (size_t)L * H);
                 double* c = cs[l * ndir + d] = (double*)malloc(sizeof(double) * (size_t)L * H);
                 double* g = gs[l * ndir + d] = (double*)malloc(sizeof(double) * (size_t)L * 4 * H);
-                oracle_dir_forward(L, D, H, acts[l], v.W, v.R, v.b, v.p, d == 1, h, c, g);
+                const size_t so = (((size_t)l * ndir + d) * B + b) * H;     /* this state's offset */
+                oracle_dir_forward(L, D, H, acts[l], v.W, v.R, v.b, v.p, d == 1, h0 ? h0 + so : NULL,
+                                   c0 ? c0 + so : NULL, h, c, g);
                 for (int t = 0; t < L; ++t)
                     memcpy(acts[l + 1] + (size_t)t * Hout + (size_t)d * H, h + (size_t)t * H,
                            sizeof(double) * H);
@@ -318,9 +377,12 @@ int oracle_lstm_stack(int B, const int* lengths, int num_layers, int ndir, int H
                     for (int t = 0; t < L; ++t)
                         memcpy(dyd + (size_t)t * H, dout + (size_t)t * Hout + (size_t)d * H,
                                sizeof(double) * H);
-                    oracle_dir_backward(L, D, H, acts[l], v.W, v.R, v.p, d == 1,
+                    const size_t so = (((size_t)l * ndir + d) * B + b) * H;
+                    oracle_dir_backward(L, D, H, acts[l], v.W, v.R, v.p, d == 1, h0 ? h0 + so : NULL,
+                                        c0 ? c0 + so : NULL, dh_n ? dh_n + so : NULL, dc_n ? dc_n + so : NULL,
                                         hs[l * ndir + d], cs[l * ndir + d], gs[l * ndir + d], dyd,
-                                        din, gv.W, gv.R, gv.b, gv.p);
+                                        din, gv.W, gv.R, gv.b, gv.p, dh0 ? dh0 + so : NULL,
+                                        dc0 ? dc0 + so : NULL);
                 }
                 double* tmp = dout; dout = din; din = tmp;   /* dout now holds dL/d(input of l) */
             }

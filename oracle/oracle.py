@@ -42,12 +42,19 @@ def _load():
                 ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, dp, ctypes.POINTER(dp), dp, dp, dp, dp, dp, ctypes.POINTER(dp),
                 ctypes.c_int]
+            lib.oracle_lstm_stack_state.restype = ctypes.c_int
+            lib.oracle_lstm_stack_state.argtypes = [
+                ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, dp, ctypes.POINTER(dp), dp, dp, dp, dp, dp, dp, dp, dp, dp,
+                ctypes.POINTER(dp), dp, dp, ctypes.c_int]
             lib.oracle_lstm_padded_layer.restype = ctypes.c_int
             lib.oracle_lstm_padded_layer.argtypes = [
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, dp,
                 ctypes.POINTER(ctypes.c_ubyte), dp, dp, dp, dp, dp, dp, dp]
             lib.oracle_set_bf16_products.restype = None
             lib.oracle_set_bf16_products.argtypes = [ctypes.c_int]
+            lib.oracle_round_bf16.restype = ctypes.c_double
+            lib.oracle_round_bf16.argtypes = [ctypes.c_double]
             lib.oracle_layer_param_count.restype = ctypes.c_long
             lib.oracle_layer_param_count.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
             _lib = lib
@@ -81,12 +88,17 @@ def unpack_layer_grads(flat: np.ndarray, ndir: int, D: int, H: int) -> dict:
 
 
 def lstm_stack(lengths, x, layers, num_directions: int, hidden_size: int, G=None,
-               nthreads: int = 1, bf16_products: bool = False) -> dict:
+               nthreads: int = 1, bf16_products: bool = False, h0=None, c0=None, dh_n=None,
+               dc_n=None) -> dict:
     """Forward (and, if ``G`` is given, BPTT) of a layer stack, each sequence on its own.
 
     lengths[B]; x[N, D0] in caller order; layers: list of dicts W, R, b, peep;
     G[N, ndir*H] = dL/dy of the top layer.  Returns y, h_n, c_n [layers, ndir, B, H]
     and, with G, dx and grads (list of dicts).
+
+    h0, c0 [layers, ndir, B, H]: initial states (None = zero); dh_n, dc_n: dL/d of
+    the final states from outside the stack (None = zero).  With G, the result also
+    holds dh0 and dc0 [layers, ndir, B, H].
 
     bf16_products=True is a diagnostic (not the parity reference): h and the
     gate errors are rounded to bf16 before each product.
@@ -117,10 +129,14 @@ def lstm_stack(lengths, x, layers, num_directions: int, hidden_size: int, G=None
         dx = np.zeros((N, D0))
         grads = [np.zeros_like(p) for p in params]
         garr = (dp * nl)(*[_ptr(g) for g in grads])
+    st_shape = (nl, nd, B, H)
+    states = [None if a is None else _f64(a).reshape(st_shape) for a in (h0, c0, dh_n, dc_n)]
+    dh0 = np.zeros(st_shape) if G is not None else None
+    dc0 = np.zeros(st_shape) if G is not None else None
     lib.oracle_set_bf16_products(1 if bf16_products else 0)
-    rc = lib.oracle_lstm_stack(B, lengths.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), nl, nd, H, D0,
-                               _ptr(x), parr, _ptr(dy), _ptr(y), _ptr(h_n), _ptr(c_n), _ptr(dx),
-                               garr, int(nthreads))
+    rc = lib.oracle_lstm_stack_state(B, lengths.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), nl, nd, H, D0,
+                                     _ptr(x), parr, _ptr(dy), *[_ptr(a) for a in states], _ptr(y), _ptr(h_n),
+                                     _ptr(c_n), _ptr(dx), garr, _ptr(dh0), _ptr(dc0), int(nthreads))
     lib.oracle_set_bf16_products(0)
     if rc != 0:
         raise ValueError("oracle_lstm_stack rejected its arguments")
@@ -128,7 +144,14 @@ def lstm_stack(lengths, x, layers, num_directions: int, hidden_size: int, G=None
         out["dx"] = dx
         out["grads"] = [unpack_layer_grads(g, nd, D0 if i == 0 else nd * H, H)
                         for i, g in enumerate(grads)]
+        out["dh0"] = dh0
+        out["dc0"] = dc0
     return out
+
+
+def round_bf16(v: float) -> float:
+    """The bf16-product mode's rounding of one value (fp32, then nearest bf16, ties to even)."""
+    return float(_load().oracle_round_bf16(float(v)))
 
 
 def lstm_padded_layer(x_pad, mask, layer: dict, num_directions: int, hidden_size: int,

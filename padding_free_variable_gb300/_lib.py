@@ -30,6 +30,7 @@ EXPORTED = (
     "lstm_plan_launch_count", "lstm_debug_trace_steps", "lstm_bwd_noalloc",
     "lstm_plan_set_gemm_engine", "lstm_debug_input_projection", "lstm_plan_recurrent_config",
     "lstm_stepwise_scratch_bytes", "lstm_fwd_stepwise", "lstm_bwd_stepwise", "lstm_debug_cluster_variant",
+    "lstm_plan_recurrent_groups", "lstm_debug_sequence_groups",
 )
 
 KERNEL_KINDS = ("pack", "unpack", "input_gemm", "rec_fwd", "rec_bwd", "gemm_dx", "gemm_dw", "gemm_dr", "convert")
@@ -88,6 +89,8 @@ def _declare(lib):
         "lstm_plan_read_timing": (c, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]),
         "lstm_plan_launch_count": (i64, [vp]),
         "lstm_plan_recurrent_config": (c, [vp, i32, pi32, pi32, pi32, pi32]),
+        "lstm_plan_recurrent_groups": (c, [vp, i32, pi32, pi32]),
+        "lstm_debug_sequence_groups": (c, [vp, i32]),
         "lstm_stepwise_scratch_bytes": (ctypes.c_size_t, [vp, ctypes.POINTER(LayerShape)]),
         "lstm_fwd_stepwise": (c, [vp, ctypes.POINTER(LayerShape), ctypes.POINTER(LayerParams), vp, vp, vp, vp, vp,
                                   vp, vp, vp]),

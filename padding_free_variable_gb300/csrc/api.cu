@@ -33,8 +33,8 @@ lstm_status check_shape(const lstm_layer_shape* s)
     return LSTM_OK;
 }
 
-// fp32 layers whose products can run on tcgen05 as three bf16 products (hi/lo split
-// concatenated along K): the K extents (D, ndir*4H, frames) must be TMA-addressable.
+// fp32 layers whose products can run on tcgen05 as six bf16 products of three-piece splits
+// concatenated along K: the K extents (D, ndir*4H, frames) must be TMA-addressable.
 bool f32_split_shape(const lstm_layer_shape& s) { return s.dtype == LSTM_F32 && s.input_size % 8 == 0; }
 
 // bf16 layers wider than one thread-block cluster can hold (one direction's R of more than 16
@@ -56,7 +56,7 @@ struct Layout {
 };
 
 // gates/errors, cell states, then (fp32 split shapes) the input projection's split operands:
-// X as [rows][3D] and W as [ndir*4H][3D] bf16
+// X as [rows][6D] and W as [ndir*4H][6D] bf16 (six K segments, kSplitSegments)
 Layout workspace_layout(const Plan& p, const lstm_layer_shape& s)
 {
     Layout l;
@@ -65,8 +65,9 @@ Layout workspace_layout(const Plan& p, const lstm_layer_shape& s)
     l.ga_off = 0;
     l.c_off = align256(rows * nd * 4 * H * sizeof(float));
     l.xs_off = l.c_off + align256(rows * nd * H * sizeof(float));
-    l.ws_off = l.xs_off + (f32_split_shape(s) ? align256(rows * 3 * D * 2) : 0);
-    l.rh_off = l.ws_off + (f32_split_shape(s) ? align256(nd * 4 * H * 3 * D * 2) : 0);
+    const size_t ns = kSplitSegments;
+    l.ws_off = l.xs_off + (f32_split_shape(s) ? align256(rows * ns * D * 2) : 0);
+    l.rh_off = l.ws_off + (f32_split_shape(s) ? align256(nd * 4 * H * ns * D * 2) : 0);
     // wide bf16 layers: a step's R h_{t-1} [ndir][B][4H] fp32 and bf16 h [ndir][B][H]
     const size_t B = (size_t)p.B;
     l.hb_off = l.rh_off + (wide_bf16(s) ? align256(nd * (size_t)step_splits(p, s, false) * B * 4 * H * 4) : 0);
@@ -84,6 +85,19 @@ void bwd_gemm_shapes(const Plan& p, const lstm_layer_shape& s, GemmDesc* dW, Gem
 }
 
 constexpr int kMaxTcSplits = 16;
+// fp32 layers: the longest K range one tensor-memory accumulator sums (64 MMAs of K = 16).
+// The accumulator's additions lose about 2^-23 of the running sum each (measured on the
+// frame-reduced products dW and dR: the element-wise error grows linearly with the MMAs
+// per accumulator), so long K ranges are cut into splits whose partial sums are added in
+// fp32 on the CUDA cores, in split order.
+constexpr int kF32SplitK = 1024;
+
+// K splits of a tensor-core product of the backward pass.
+int bwd_tc_splits(const Plan& p, int M, int N, int K, bool f32)
+{
+    const int sp = gemm_tc_splits(M, N, K, p.num_sms, kMaxTcSplits);
+    return f32 ? std::max(sp, (K + kF32SplitK - 1) / kF32SplitK) : sp;
+}
 
 // Scratch of lstm_bwd.  Region U holds the recurrent kernel's partial-product
 // exchange, later the split-K partial sums (never live at the same time).  The
@@ -105,12 +119,15 @@ BwdScratch bwd_scratch(const Plan& p, const lstm_layer_shape& s)
     const size_t part = std::max(rec_bwd_part_floats(p, H, nd, s.dtype == LSTM_BF16, p.forced_ctas),
                                  rec_cluster_bwd_sum_floats(H, nd));
     const bool tc_shape = s.dtype == LSTM_BF16 || f32_split_shape(s);
-    const int ns = s.dtype == LSTM_BF16 ? 1 : 3;     // K segments of the tensor-core operands
+    const int ns = s.dtype == LSTM_BF16 ? 1 : kSplitSegments;   // K segments of the tensor-core operands
     const int64_t ldr = (int64_t)(((size_t)p.rows + 7) / 8 * 8);
     if (tc_shape) {
-        const int kr = ns == 1 ? (int)p.rows : (int)(3 * ldr);
-        const size_t tc = std::max((size_t)gemm_tc_splits(nd * 4 * H, D, kr, p.num_sms, kMaxTcSplits) * nd * 4 * H * D,
-                                   (size_t)gemm_tc_splits(4 * H, H, kr, p.num_sms, kMaxTcSplits) * 4 * H * H);
+        const bool f32 = ns > 1;
+        const int kr = ns == 1 ? (int)p.rows : (int)(ns * ldr);
+        size_t tc = std::max((size_t)bwd_tc_splits(p, nd * 4 * H, D, kr, f32) * nd * 4 * H * D,
+                             (size_t)bwd_tc_splits(p, 4 * H, H, kr, f32) * 4 * H * H);
+        const int sx = f32 ? bwd_tc_splits(p, (int)p.rows, D, ns * nd * 4 * H, true) : 1;
+        if (sx > 1) tc = std::max(tc, (size_t)sx * (size_t)p.rows * D);
         gemm = std::max(gemm, tc);
     }
     b.u_bytes = align256(std::max<size_t>(1, std::max(gemm, part)) * sizeof(float));
@@ -154,8 +171,8 @@ RecArgs base_args(const Plan& p, const lstm_layer_shape& s, const lstm_layer_par
 bool encode_ready();
 
 // A_in[rows][ndir*4H] = X W^T + b for both directions at once; tcgen05 for bf16 operands, and
-// for fp32 operands as three bf16 products (X as [hi, hi, lo], W as [hi, lo, hi] along K, in
-// the workspace's split region `split_ws`, when given).
+// for fp32 operands as six bf16 products of three-piece splits (X in split pattern 1, W in
+// pattern 2, six K segments each, in the workspace's split region `split_ws`, when given).
 lstm_status input_projection(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm,
                              const void* x_packed, float* out, void* split_ws, cudaStream_t cs)
 {
@@ -167,15 +184,16 @@ lstm_status input_projection(const Plan& p, const lstm_layer_shape& s, const lst
     if (!bf16 && split_ws && p.gemm_engine == 0 && f32_split_shape(s) && encode_ready()) {
         const int rows = (int)p.rows, G4 = nd * 4 * H;
         char* xs = (char*)split_ws;
-        char* ws = xs + align256((size_t)rows * 3 * D * 2);
+        const int ns = kSplitSegments;
+        char* ws = xs + align256((size_t)rows * ns * D * 2);
         lstm_status st;
         if ((st = transpose_to_bf16_split(p, x_packed, false, D, 0, nullptr, rows, rows, D, 1, nullptr, 0, 0, xs,
-                                          3 * D, D, cs)) != LSTM_OK)
+                                          (int64_t)ns * D, D, cs)) != LSTM_OK)
             return st;
-        if ((st = transpose_to_bf16_split(p, prm.W, false, D, 0, nullptr, G4, G4, D, 2, nullptr, 0, 0, ws, 3 * D, D,
-                                          cs)) != LSTM_OK)
+        if ((st = transpose_to_bf16_split(p, prm.W, false, D, 0, nullptr, G4, G4, D, 2, nullptr, 0, 0, ws,
+                                          (int64_t)ns * D, D, cs)) != LSTM_OK)
             return st;
-        return gemm_tc_bf16_nt(p, K_GEMM_IN, xs, ws, out, G4, prm.b, rows, G4, 3 * D, cs);
+        return gemm_tc_bf16_nt(p, K_GEMM_IN, xs, ws, out, G4, prm.b, rows, G4, ns * D, cs);
     }
     GemmDesc g;
     g.M = (int)p.rows; g.N = nd * 4 * H; g.K = D;
@@ -190,8 +208,8 @@ bool encode_ready() { return gemm_tc_supported(1, 1, 8, nullptr, nullptr); }
 // dX, dW and dR on tcgen05, from the gate errors dA (fp32, in the workspace) and bf16
 // operands built in the scratch: transposes (frames innermost, padded to a multiple of 8
 // with zeros) and a row-major copy of dA.  bf16 layers use one bf16 copy of each operand;
-// fp32 layers three K segments per operand (dA as [hi, hi, lo], X, H_prev and W as
-// [hi, lo, hi]), so that each product is hi*hi + hi*lo + lo*hi in one launch.
+// fp32 layers six K segments per operand (dA in split pattern 1; X, H_prev and W in pattern
+// 2), so that each product is the sum of the six piece products in one launch.
 lstm_status bwd_products_tc(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm,
                             const void* x_packed, const float* y_packed, const float* ga, float* dx_packed,
                             const lstm_layer_grads& g, void* scratch, cudaStream_t cs)
@@ -199,7 +217,7 @@ lstm_status bwd_products_tc(const Plan& p, const lstm_layer_shape& s, const lstm
     const int H = s.hidden_size, nd = s.num_directions, D = s.input_size, rows = (int)p.rows;
     const int G4 = nd * 4 * H;
     const bool bf16 = s.dtype == LSTM_BF16;
-    const int ns = bf16 ? 1 : 3;
+    const int ns = bf16 ? 1 : kSplitSegments;
     const int pa = bf16 ? 0 : 1, pb = bf16 ? 0 : 2;      // split patterns of the two operand sides
     const BwdScratch b = bwd_scratch(p, s);
     const int64_t ldr = b.ldr, kt = (int64_t)ns * ldr;    // transposed operands: row pitch = K extent
@@ -228,15 +246,16 @@ lstm_status bwd_products_tc(const Plan& p, const lstm_layer_shape& s, const lstm
                                       nullptr, 0, 0, cs)) != LSTM_OK)
         return st;
     // dX[rows][D] = dA[rows][G4] W[G4][D]
+    const int sx = bf16 ? 1 : bwd_tc_splits(p, rows, D, ns * G4, true);
     if (dx_packed && (st = gemm_tc_bf16(p, K_GEMM_DX, dA16, (int64_t)ns * G4, WT16, (int64_t)ns * G4, rows, D, ns * G4,
-                                        dx_packed, D, nullptr, 1, nullptr, cs)) != LSTM_OK)
+                                        dx_packed, D, nullptr, sx, partial, cs)) != LSTM_OK)
         return st;
     // dW[G4][D] = dA^T X, K = frames
-    int sp = gemm_tc_splits(G4, D, kr, p.num_sms, kMaxTcSplits);
+    int sp = bwd_tc_splits(p, G4, D, kr, !bf16);
     if ((st = gemm_tc_bf16(p, K_GEMM_DW, dAT16, kt, XT16, kt, G4, D, kr, g.dW, D, nullptr, sp, partial, cs)) != LSTM_OK)
         return st;
     // dR_d[4H][H] = dA_d^T H_prev_d, K = frames
-    sp = gemm_tc_splits(4 * H, H, kr, p.num_sms, kMaxTcSplits);
+    sp = bwd_tc_splits(p, 4 * H, H, kr, !bf16);
     for (int d = 0; d < nd; ++d)
         if ((st = gemm_tc_bf16(p, K_GEMM_DR, dAT16 + (size_t)d * 4 * H * kt * 2, kt, HpT16 + (size_t)d * H * kt * 2, kt,
                                4 * H, H, kr, g.dR + (size_t)d * 4 * H * H, H, nullptr, sp, partial, cs)) != LSTM_OK)
@@ -315,7 +334,7 @@ bool step_tc(const Plan& p, const lstm_layer_shape& s);
 // Whether lstm_fwd / lstm_bwd run this layer's recurrence as per-step tcgen05 products.
 bool wide_step_path(const Plan& p, const lstm_layer_shape& s)
 {
-    return wide_bf16(s) && !p.padded && p.forced_ctas == 0 && step_tc(p, s);
+    return wide_bf16(s) && p.forced_ctas == 0 && step_tc(p, s);
 }
 
 StepArgs step_args(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm, float* ga,
@@ -326,6 +345,7 @@ StepArgs step_args(const Plan& p, const lstm_layer_shape& s, const lstm_layer_pa
     a.T = p.T; a.B = p.B; a.H = s.hidden_size; a.ndir = s.num_directions;
     a.bs = p.d_bs; a.off = p.d_off; a.slot_len = p.d_len; a.perm = p.d_perm;
     a.ga = ga; a.cbuf = cbuf; a.peep = prm.peep;
+    a.padded = p.padded ? 1 : 0;
     return a;
 }
 
@@ -524,6 +544,7 @@ lstm_status lstm_fwd(const lstm_plan* plan, const lstm_layer_shape* shape,
         if ((st = input_projection(p, s, *params, x_packed, ga, (char*)workspace + L.xs_off, cs)) != LSTM_OK)
             return st;
         p.last_rec_kind[0] = 3; p.last_rec_ctas[0] = 0; p.last_rec_mma[0] = 2; p.last_rec_variant[0] = 0;
+        p.last_rec_groups[0] = 1; p.last_rec_grp_rows[0] = p.B;
         return stepwise_fwd_core(p, s, *params, y_packed, y_lo, h_n, c_n, ga, cbuf,
                                  (float*)((char*)workspace + L.rh_off), (__nv_bfloat16*)((char*)workspace + L.hb_off),
                                  cs);
@@ -544,9 +565,11 @@ lstm_status lstm_fwd(const lstm_plan* plan, const lstm_layer_shape* shape,
         a.off_peep = cl_layout.off_peep; a.off_tab = cl_layout.off_tab;
         p.last_rec_kind[0] = 2; p.last_rec_ctas[0] = rcc.G; p.last_rec_mma[0] = 2;
         p.last_rec_variant[0] = (rcc.bulk ? 1 : 0) | (rcc.tma_pre ? 2 : 0);
+        p.last_rec_groups[0] = rcc.ngroups; p.last_rec_grp_rows[0] = rcc.grp_rows;
         return rec_cluster_fwd_launch(p, rcc, a, cs);
     }
     p.last_rec_kind[0] = 1; p.last_rec_ctas[0] = rc.G; p.last_rec_mma[0] = rc.mma;
+    p.last_rec_groups[0] = 1; p.last_rec_grp_rows[0] = p.B;
     return rec_launch(p, rc, a, false, cs);
 }
 
@@ -588,6 +611,7 @@ lstm_status lstm_bwd(const lstm_plan* plan, const lstm_layer_shape* shape,
         const StepScratch q = step_scratch(p, s);
         char* sc = (char*)scratch;
         p.last_rec_kind[1] = 3; p.last_rec_ctas[1] = 0; p.last_rec_mma[1] = 2; p.last_rec_variant[1] = 0;
+        p.last_rec_groups[1] = 1; p.last_rec_grp_rows[1] = p.B;
         return stepwise_bwd_core(p, s, *params, x_packed, y_packed, ga, cbuf, dy_packed, dx_packed, *grads, scratch,
                                  (float*)(sc + q.dh), (float*)(sc + q.dcc), (__nv_bfloat16*)(sc + q.dab),
                                  (__nv_bfloat16*)(sc + q.rt), cs);
@@ -606,9 +630,11 @@ lstm_status lstm_bwd(const lstm_plan* plan, const lstm_layer_shape* shape,
         a.off_peep = cl_layout.off_peep; a.off_tab = cl_layout.off_tab;
         p.last_rec_kind[1] = 2; p.last_rec_ctas[1] = rcc.G; p.last_rec_mma[1] = 2;
         p.last_rec_variant[1] = (rcc.bulk ? 1 : 0) | (rcc.tma_pre ? 2 : 0);
+        p.last_rec_groups[1] = rcc.ngroups; p.last_rec_grp_rows[1] = rcc.grp_rows;
         if ((st = rec_cluster_bwd_launch(p, rcc, a, (float*)scratch, cs)) != LSTM_OK) return st;
     } else {
         p.last_rec_kind[1] = 1; p.last_rec_ctas[1] = rc.G; p.last_rec_mma[1] = rc.mma; p.last_rec_variant[1] = 0;
+        p.last_rec_groups[1] = 1; p.last_rec_grp_rows[1] = p.B;
         if ((st = rec_launch(p, rc, a, true, cs)) != LSTM_OK) return st;
     }
 
@@ -631,7 +657,6 @@ lstm_status lstm_fwd_stepwise(const lstm_plan* plan, const lstm_layer_shape* sha
     if ((st = check_params(params)) != LSTM_OK) return st;
     const Plan& p = plan->p;
     const lstm_layer_shape& s = *shape;
-    if (p.padded) return LSTM_ERR_UNSUPPORTED;
     const int H = s.hidden_size, nd = s.num_directions;
     cudaStream_t cs = (cudaStream_t)stream;
     if ((h_n && !aligned16(h_n)) || (c_n && !aligned16(c_n))) return LSTM_ERR_INVALID_ARG;
@@ -668,7 +693,6 @@ lstm_status lstm_bwd_stepwise(const lstm_plan* plan, const lstm_layer_shape* sha
         return LSTM_ERR_INVALID_ARG;
     const Plan& p = plan->p;
     const lstm_layer_shape& s = *shape;
-    if (p.padded) return LSTM_ERR_UNSUPPORTED;
     const int H = s.hidden_size, nd = s.num_directions, D = s.input_size;
     cudaStream_t cs = (cudaStream_t)stream;
     if (p.rows == 0) {

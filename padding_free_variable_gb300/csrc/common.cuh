@@ -45,6 +45,7 @@ struct Plan {
     int32_t debug_skip_cta = -1;
     int32_t forced_ctas = 0;        // 0 = automatic
     int32_t forced_variant = -1;    // cluster kernels: -1 automatic, else bit 0 bulk exchange, bit 1 TMA tiles
+    int32_t forced_group_rows = 0;  // cluster kernels: sorted slots per sequence group (0 = automatic)
     int32_t gemm_engine = 0;        // 0 = tensor cores for bf16 operands, 1 = CUDA cores
     int device = 0;
     int num_sms = 0;
@@ -62,6 +63,7 @@ struct Plan {
     int32_t* d_row_src = nullptr;   // [rows] caller-order frame of packed row (-1 = padding)
     int32_t* d_prev_fwd = nullptr;  // [rows] row holding h_{t-1} for the forward direction (-1 none)
     int32_t* d_prev_rev = nullptr;  // [rows] row holding the reverse direction's previous state
+    int32_t* d_row_slot = nullptr;  // [rows] sorted slot j of packed row (row off[t] + j)
     unsigned* d_flags = nullptr;    // [2 * kMaxCtasPerDir] step counters
     DeviceStatus* d_status = nullptr;
     Tracer* tracer = nullptr;       // owned; mutable through const plans
@@ -72,6 +74,8 @@ struct Plan {
     mutable int32_t last_rec_ctas[2] = {0, 0};   // CTAs per direction
     mutable int32_t last_rec_mma[2] = {0, 0};    // 0 CUDA cores, 1 mma.sync, 2 tcgen05
     mutable int32_t last_rec_variant[2] = {0, 0}; // cluster kernels: bit 0 bulk exchange, bit 1 TMA tiles
+    mutable int32_t last_rec_groups[2] = {0, 0};  // cluster kernels: sequence groups
+    mutable int32_t last_rec_grp_rows[2] = {0, 0}; // cluster kernels: sorted slots per group
 };
 
 // Bracket a launch sequence of `kind`; `kernels` = launches it issued.  A

@@ -13,6 +13,24 @@ namespace lstm {
 
 namespace {
 
+constexpr int kSplitSegs = 6;
+
+// piece of segment sg under `pattern` (0 = the leading piece only)
+__device__ __forceinline__ int seg_piece(int pattern, int sg)
+{
+    if (pattern == 1) return (0x001021 >> (4 * sg)) & 15;    // [1, 2, 0, 1, 0, 0]
+    if (pattern == 2) return (0x010201 >> (4 * sg)) & 15;    // [1, 0, 2, 0, 1, 0]
+    return 0;
+}
+
+__device__ __forceinline__ void split3(float v, __nv_bfloat16 (&p)[3])
+{
+    p[0] = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(p[0]);
+    p[1] = __float2bfloat16_rn(r1);
+    p[2] = __float2bfloat16_rn(r1 - __bfloat162float(p[1]));
+}
+
 template <typename Tin>
 __device__ __forceinline__ float load_f(const Tin* p);
 template <>
@@ -24,12 +42,16 @@ __device__ __forceinline__ float load_f<__nv_bfloat16>(const __nv_bfloat16* p) {
 // for r < rows, c < cols; row(r) = map ? map[r] : r, and a negative map entry reads 0.
 // Rows in [rows, rows_pad) are written as zeros into dstT only (the padded tail of a K
 // range); dst_rm has rows rows.
-// Split patterns, for fp32 products on bf16 tensor cores as three products
-// concatenated along K: each value v becomes hi = bf16(v) and lo = bf16(v - hi),
-// written into three K segments (kseg_t apart in dstT rows, kseg_m apart in
-// dst_rm rows): pattern 1 = [hi, hi, lo], pattern 2 = [hi, lo, hi], so that
-// the product of a pattern-1 and a pattern-2 operand is hi*hi + hi*lo + lo*hi.
-// Pattern 0 writes hi only.
+// Split patterns, for fp32 products on bf16 tensor cores as six products
+// concatenated along K: each value v becomes three bf16 pieces v0 = bf16(v),
+// v1 = bf16(v - v0), v2 = bf16(v - v0 - v1) (the two differences are exact in
+// fp32, and v0 + v1 + v2 is v to within 2^-24 of |v|), written into six K
+// segments (kseg_t apart in dstT rows, kseg_m apart in dst_rm rows).  Pattern 1
+// (the A side, x) writes pieces [1, 2, 0, 1, 0, 0] and pattern 2 (the B side,
+// y) pieces [1, 0, 2, 0, 1, 0], so that the product of a pattern-1 and a
+// pattern-2 operand is x1 y1 + x2 y0 + x0 y2 + x1 y0 + x0 y1 + x0 y0: every
+// piece product above 2^-24 of x0 y0 (the other three are below 2^-26).
+// Pattern 0 writes v0 only.
 template <typename Tin>
 __global__ void __launch_bounds__(256) transpose_bf16_kernel(const Tin* __restrict__ src, int64_t lds, int col0,
                                                              const int32_t* __restrict__ map, int rows,
@@ -38,10 +60,11 @@ __global__ void __launch_bounds__(256) transpose_bf16_kernel(const Tin* __restri
                                                              int64_t kseg_t, __nv_bfloat16* __restrict__ dst_rm,
                                                              int64_t ldm, int64_t kseg_m)
 {
-    __shared__ __nv_bfloat16 thi[32][34], tlo[32][34];
+    __shared__ __nv_bfloat16 tp[3][32][34];
     const int r0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    const int nseg = pattern == 0 ? 1 : 3;
+    const int nseg = pattern == 0 ? 1 : kSplitSegs;
+    const int npc = pattern == 0 ? 1 : 3;
     for (int i = ty; i < 32; i += 8) {
         const int r = r0 + i, c = c0 + tx;
         float f = 0.f;
@@ -49,25 +72,18 @@ __global__ void __launch_bounds__(256) transpose_bf16_kernel(const Tin* __restri
             const int64_t sr = map ? (int64_t)__ldg(map + r) : (int64_t)r;
             if (sr >= 0) f = load_f<Tin>(src + sr * lds + col0 + c);
         }
-        const __nv_bfloat16 hi = __float2bfloat16_rn(f);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(f - __bfloat162float(hi));
+        __nv_bfloat16 pc[3];
+        split3(f, pc);
         if (dst_rm && r < rows && c < cols)           // the row-major copy has no padded rows
-            for (int sg = 0; sg < nseg; ++sg) {
-                const bool use_lo = (pattern == 1 && sg == 2) || (pattern == 2 && sg == 1);
-                dst_rm[(int64_t)r * ldm + sg * kseg_m + c] = use_lo ? lo : hi;
-            }
-        thi[i][tx] = hi;
-        tlo[i][tx] = lo;
+            for (int sg = 0; sg < nseg; ++sg) dst_rm[(int64_t)r * ldm + sg * kseg_m + c] = pc[seg_piece(pattern, sg)];
+        for (int q = 0; q < npc; ++q) tp[q][i][tx] = pc[q];
     }
     __syncthreads();
     if (!dstT) return;
     for (int i = ty; i < 32; i += 8) {
         const int c = c0 + i, r = r0 + tx;
         if (c < cols && r < rows_pad)
-            for (int sg = 0; sg < nseg; ++sg) {
-                const bool use_lo = (pattern == 1 && sg == 2) || (pattern == 2 && sg == 1);
-                dstT[(int64_t)c * ldt + sg * kseg_t + r] = use_lo ? tlo[tx][i] : thi[tx][i];
-            }
+            for (int sg = 0; sg < nseg; ++sg) dstT[(int64_t)c * ldt + sg * kseg_t + r] = tp[seg_piece(pattern, sg)][tx][i];
     }
 }
 
@@ -98,10 +114,11 @@ __global__ void __launch_bounds__(256) transpose_bf16_v4_kernel(const Tin* __res
                                                                 int64_t kseg_t, __nv_bfloat16* __restrict__ dst_rm,
                                                                 int64_t ldm, int64_t kseg_m)
 {
-    __shared__ __align__(16) __nv_bfloat16 thi[64][72], tlo[64][72];     // [column][row]
+    __shared__ __align__(16) __nv_bfloat16 tp[3][64][72];     // [piece][column][row]
     const int r0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
     const int tid = threadIdx.x;
-    const int nseg = pattern == 0 ? 1 : 3;
+    const int nseg = pattern == 0 ? 1 : kSplitSegs;
+    const int npc = pattern == 0 ? 1 : 3;
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
         const int rr = (tid >> 4) + 16 * it, q = tid & 15;
@@ -111,28 +128,24 @@ __global__ void __launch_bounds__(256) transpose_bf16_v4_kernel(const Tin* __res
             const int64_t sr = map ? (int64_t)__ldg(map + r) : (int64_t)r;
             if (sr >= 0) load4<Tin>(src + sr * lds + col0 + c, v);
         }
-        __nv_bfloat16 hi[4], lo[4];
+        __nv_bfloat16 pc[4][3];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            hi[e] = __float2bfloat16_rn(v[e]);
-            lo[e] = __float2bfloat16_rn(v[e] - __bfloat162float(hi[e]));
-        }
+        for (int e = 0; e < 4; ++e) split3(v[e], pc[e]);
         if (dst_rm && r < rows && c < cols) {
-            uint2 phi, plo;
-            phi.x = (uint32_t)__bfloat16_as_ushort(hi[0]) | ((uint32_t)__bfloat16_as_ushort(hi[1]) << 16);
-            phi.y = (uint32_t)__bfloat16_as_ushort(hi[2]) | ((uint32_t)__bfloat16_as_ushort(hi[3]) << 16);
-            plo.x = (uint32_t)__bfloat16_as_ushort(lo[0]) | ((uint32_t)__bfloat16_as_ushort(lo[1]) << 16);
-            plo.y = (uint32_t)__bfloat16_as_ushort(lo[2]) | ((uint32_t)__bfloat16_as_ushort(lo[3]) << 16);
-            for (int sg = 0; sg < nseg; ++sg) {
-                const bool use_lo = (pattern == 1 && sg == 2) || (pattern == 2 && sg == 1);
-                *reinterpret_cast<uint2*>(dst_rm + (int64_t)r * ldm + sg * kseg_m + c) = use_lo ? plo : phi;
+            uint2 pw[3];
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                pw[k].x = (uint32_t)__bfloat16_as_ushort(pc[0][k]) | ((uint32_t)__bfloat16_as_ushort(pc[1][k]) << 16);
+                pw[k].y = (uint32_t)__bfloat16_as_ushort(pc[2][k]) | ((uint32_t)__bfloat16_as_ushort(pc[3][k]) << 16);
             }
+            for (int sg = 0; sg < nseg; ++sg)
+                *reinterpret_cast<uint2*>(dst_rm + (int64_t)r * ldm + sg * kseg_m + c) = pw[seg_piece(pattern, sg)];
         }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            thi[4 * q + e][rr] = hi[e];
-            tlo[4 * q + e][rr] = lo[e];
-        }
+        for (int e = 0; e < 4; ++e)
+#pragma unroll
+            for (int k = 0; k < 3; ++k)
+                if (k < npc) tp[k][4 * q + e][rr] = pc[e][k];
     }
     __syncthreads();
     if (!dstT) return;
@@ -142,8 +155,7 @@ __global__ void __launch_bounds__(256) transpose_bf16_v4_kernel(const Tin* __res
         const int c = c0 + cc, r = r0 + 8 * o;
         if (c >= cols || r >= rows_pad) continue;
         for (int sg = 0; sg < nseg; ++sg) {
-            const bool use_lo = (pattern == 1 && sg == 2) || (pattern == 2 && sg == 1);
-            const __nv_bfloat16* t = use_lo ? &tlo[cc][8 * o] : &thi[cc][8 * o];
+            const __nv_bfloat16* t = &tp[seg_piece(pattern, sg)][cc][8 * o];
             __nv_bfloat16* d = dstT + (int64_t)c * ldt + sg * kseg_t + r;
             if (r + 8 <= rows_pad) {
                 *reinterpret_cast<uint4*>(d) = *reinterpret_cast<const uint4*>(t);

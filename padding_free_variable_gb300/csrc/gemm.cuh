@@ -83,9 +83,13 @@ bool make_map_f32(CUtensorMap* map, const float* ptr, int64_t rows, int64_t cols
                   int box_rows);
 
 // The same with a padded row range (rows in [rows, rows_pad) written as 0)
-// and an fp32 split into bf16 hi/lo written as three K segments: pattern 1 =
-// [hi, hi, lo], pattern 2 = [hi, lo, hi] (kseg_t / kseg_m elements apart in the
-// transposed / row-major output), pattern 0 = hi only.  dstT may be null.
+// and an fp32 split into three bf16 pieces v0 + v1 + v2 written as six K
+// segments (kSplitSegments, kseg_t / kseg_m elements apart in the transposed /
+// row-major output): pattern 1 = pieces [1, 2, 0, 1, 0, 0], pattern 2 =
+// [1, 0, 2, 0, 1, 0], so that a pattern-1 operand times a pattern-2 operand is
+// the sum of the six piece products above 2^-24 of the leading one; pattern 0
+// = v0 only.  dstT may be null.
+constexpr int kSplitSegments = 6;
 lstm_status transpose_to_bf16_split(const Plan& p, const void* src, bool src_bf16, int64_t lds, int col0,
                                     const int32_t* map, int rows, int rows_pad, int cols, int pattern, void* dstT,
                                     int64_t ldt, int64_t kseg_t, void* dst_rm, int64_t ldm, int64_t kseg_m,

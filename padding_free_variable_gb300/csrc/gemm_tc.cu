@@ -471,8 +471,6 @@ bool make_map_f32(CUtensorMap* map, const float* ptr, int64_t rows, int64_t cols
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// C[M][N] fp32 with row pitch ldc as the epilogue's store target: 32 x 32 boxes, 128-byte
-// swizzle (the staging layout of the persistent kernel's epilogue warps).
 // The kernel's dynamic shared-memory limit, raised once per device (the attribute belongs
 // to the device's context, so a process driving several GPUs sets it on each).
 static bool smem_attr_ready(const void* fn, int bytes)
@@ -490,6 +488,8 @@ static bool smem_attr_ready(const void* fn, int bytes)
     return true;
 }
 
+// C[M][N] fp32 with row pitch ldc as the epilogue's store target: 32 x 32 boxes, 128-byte
+// swizzle (the staging layout of the persistent kernel's epilogue warps).
 static bool make_map_c(CUtensorMap* map, float* C, int M, int N, int64_t ldc)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();

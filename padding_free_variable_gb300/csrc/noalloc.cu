@@ -13,7 +13,10 @@
 // library holds LSTM_NOALLOC_SCRATCH_BYTES for it until the process exits.
 // Host code cannot use the array's name as a device address, so the first
 // call on each device looks the address up with cudaGetSymbolAddress (with
-// that device current) and keeps it for later calls on that device.
+// that device current) and keeps it for later calls on that device.  The
+// plan's device must be the current device.  A cudaDeviceReset destroys the
+// array together with the context; the kept address is then stale, so no call
+// may follow a reset in the same process.
 #include <mutex>
 
 #include "common.cuh"
@@ -26,11 +29,13 @@ constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 void* g_noalloc_ptr[kMaxDevices] = {};
 
-// Device address of the array on the current device (looked up once per device).
-lstm_status noalloc_scratch(void** out)
+// Device address of the array on device `dev`, which must be the current device (looked up
+// once per device).
+lstm_status noalloc_scratch(int dev, void** out)
 {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return LSTM_ERR_CUDA;
+    int cur = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess) return LSTM_ERR_CUDA;
+    if (cur != dev) return LSTM_ERR_INVALID_ARG;     // the plan's tables live on another device
     if (dev < 0 || dev >= kMaxDevices) return LSTM_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
     if (!g_noalloc_ptr[dev]) {
@@ -54,7 +59,7 @@ extern "C" lstm_status lstm_bwd_noalloc(const lstm_plan* plan, const lstm_layer_
     if (need == 0) return LSTM_ERR_INVALID_ARG;
     if (need > (size_t)LSTM_NOALLOC_SCRATCH_BYTES) return LSTM_ERR_UNSUPPORTED;
     void* scratch = nullptr;
-    lstm_status st = noalloc_scratch(&scratch);
+    lstm_status st = noalloc_scratch(plan->p.device, &scratch);
     if (st != LSTM_OK) return st;
     // Nothing in the array has to start at zero: every scratch byte lstm_bwd
     // reads was written earlier in the same call.

@@ -112,7 +112,7 @@ static void free_plan(Plan& p)
     }
     free(p.h_bs); free(p.h_off); free(p.h_perm); free(p.h_len); free(p.h_cstart);
     cudaFree(p.d_bs); cudaFree(p.d_off); cudaFree(p.d_perm); cudaFree(p.d_len);
-    cudaFree(p.d_row_src); cudaFree(p.d_prev_fwd); cudaFree(p.d_prev_rev);
+    cudaFree(p.d_row_src); cudaFree(p.d_prev_fwd); cudaFree(p.d_prev_rev); cudaFree(p.d_row_slot);
     cudaFree(p.d_flags); cudaFree(p.d_status);
     p = Plan();
 }
@@ -217,6 +217,12 @@ static lstm_status create_plan(const int32_t* lengths, int32_t B, bool padded, l
     if (e == cudaSuccess) e = upload(&p.d_row_src, row_src.data(), (size_t)rows);
     if (e == cudaSuccess) e = upload(&p.d_prev_fwd, prev_fwd.data(), (size_t)rows);
     if (e == cudaSuccess) e = upload(&p.d_prev_rev, prev_rev.data(), (size_t)rows);
+    {   // sorted slot of each packed row (row off[t] + j holds slot j)
+        std::vector<int32_t> row_slot(rows);
+        for (int t = 0; t < T; ++t)
+            for (int j = 0; j < p.h_bs[t]; ++j) row_slot[(size_t)p.h_off[t] + j] = j;
+        if (e == cudaSuccess) e = upload(&p.d_row_slot, row_slot.data(), (size_t)rows);
+    }
     if (e == cudaSuccess) e = cudaMalloc((void**)&p.d_flags, sizeof(unsigned) * 2 * kMaxCtasPerDir);
     if (e == cudaSuccess) e = cudaMemset(p.d_flags, 0, sizeof(unsigned) * 2 * kMaxCtasPerDir);
     if (e == cudaSuccess) e = cudaMalloc((void**)&p.d_status, sizeof(DeviceStatus));
@@ -334,6 +340,21 @@ lstm_status lstm_plan_recurrent_config(const lstm_plan* plan, int32_t pass, int3
     if (ctas_per_direction) *ctas_per_direction = plan->p.last_rec_ctas[pass];
     if (product) *product = plan->p.last_rec_mma[pass];
     if (variant) *variant = plan->p.last_rec_variant[pass];
+    return LSTM_OK;
+}
+
+lstm_status lstm_plan_recurrent_groups(const lstm_plan* plan, int32_t pass, int32_t* groups, int32_t* slots_per_group)
+{
+    if (!plan || pass < 0 || pass > 1) return LSTM_ERR_INVALID_ARG;
+    if (groups) *groups = plan->p.last_rec_groups[pass];
+    if (slots_per_group) *slots_per_group = plan->p.last_rec_grp_rows[pass];
+    return LSTM_OK;
+}
+
+lstm_status lstm_debug_sequence_groups(lstm_plan* plan, int32_t slots)
+{
+    if (!plan || slots < 0 || slots > 128) return LSTM_ERR_INVALID_ARG;
+    plan->p.forced_group_rows = slots;
     return LSTM_OK;
 }
 

@@ -350,14 +350,14 @@ __global__ void __launch_bounds__(kRecThreads, 1) lstm_rec_fwd_kernel(RecArgs a)
                 }
             }
     }
-    // empty sequences have zero final state
+    // empty sequences end in their initial state (zero without one)
     if (a.h_n) {
         for (int idx = threadIdx.x; idx < a.B * Uc; idx += kRecThreads) {
             const int j = idx / Uc, uu = idx - j * Uc;
             if (tb.len[j] == 0) {
                 const size_t o = ((size_t)dir * a.B + a.perm[j]) * H + u0 + uu;
-                a.h_n[o] = 0.f;
-                if (a.c_n) a.c_n[o] = 0.f;
+                a.h_n[o] = a.h0 ? a.h0[o] : 0.f;
+                if (a.c_n) a.c_n[o] = a.c0 ? a.c0[o] : 0.f;
             }
         }
     }
@@ -468,7 +468,8 @@ __global__ void __launch_bounds__(kRecThreads, 1) lstm_rec_fwd_kernel(RecArgs a)
                     const int j = j0 + jj, u = u0 + uu;
                     const int row = rowbase + j;
                     const float* ac = accs + jj * RP;
-                    const float cp = j < n_prev ? cst[j * Umax + uu] : 0.f;
+                    const float cp = j < n_prev ? cst[j * Umax + uu]
+                                                : (a.c0 ? a.c0[((size_t)dir * a.B + a.perm[j]) * H + u] : 0.f);
                     const float ig = sigmoidf_(pre[k][0] + ac[uu] + peep_s[uu] * cp);
                     const float fg = sigmoidf_(pre[k][1] + ac[Umax + uu] + peep_s[Umax + uu] * cp);
                     const float zg = tanhf_(pre[k][2] + ac[2 * Umax + uu]);
@@ -591,7 +592,8 @@ __global__ void __launch_bounds__(kRecThreads, 1) lstm_rec_bwd_kernel(RecArgs a)
                     for (int g = 0; g < 4; ++g) op[k][g] = gr[g * H];
                     const size_t yo = (size_t)row * ndH + dir * H + u;
                     op[k][4] = __ldg(a.cbuf + yo);
-                    op[k][5] = j < n_prev ? __ldg(a.cbuf + (size_t)(prev_base + j) * ndH + dir * H + u) : 0.f;
+                    op[k][5] = j < n_prev ? __ldg(a.cbuf + (size_t)(prev_base + j) * ndH + dir * H + u)
+                                          : (a.c0 ? __ldg(a.c0 + ((size_t)dir * a.B + a.perm[j]) * H + u) : 0.f);
                     op[k][6] = __ldg(a.dy + yo);
                 }
             }
@@ -617,15 +619,18 @@ __global__ void __launch_bounds__(kRecThreads, 1) lstm_rec_bwd_kernel(RecArgs a)
                     const bool has_next = j < n_next;
                     // error reaching h_t through R: the peers' partials, in CTA order
                     float dh_rec = 0.f;
+                    const size_t so = ((size_t)dir * a.B + a.perm[j]) * H + u;   // caller-order state
                     if (has_next) {
                         const float* pp = part_at(rd, j, 0) + u;
                         for (int c2 = 0; c2 < G; ++c2) dh_rec += __ldcg(pp + (size_t)c2 * H);
+                    } else if (a.dh_n) {
+                        dh_rec = __ldg(a.dh_n + so);          // the sequence's last step: the final state's error
                     }
                     float dai = 0.f, daf = 0.f, daz = 0.f, dao = 0.f, carry_out = 0.f;
                     const bool real = !a.padded || t < tb.len[j];
                     if (real) {
                         const float dh = op[k][6] + dh_rec;
-                        const float carry = has_next ? dcc[j * Umax + uu] : 0.f;
+                        const float carry = has_next ? dcc[j * Umax + uu] : (a.dc_n ? __ldg(a.dc_n + so) : 0.f);
                         const float tc = tanhf_(c);
                         dao = dh * tc * og * (1.f - og);
                         const float dc = dh * og * (1.f - tc * tc) + dao * peep_s[2 * Umax + uu] + carry;
@@ -633,6 +638,7 @@ __global__ void __launch_bounds__(kRecThreads, 1) lstm_rec_bwd_kernel(RecArgs a)
                         daf = dc * cp * fg * (1.f - fg);
                         daz = dc * ig * (1.f - zg * zg);
                         carry_out = dc * fg + dai * peep_s[uu] + daf * peep_s[Umax + uu];
+                        if (j >= n_prev && a.dc0) a.dc0[so] = carry_out;   // the sequence's first step
                     }
                     float* gr = a.ga + (size_t)row * nd4H + dir * 4 * H + u;
                     gr[0] = dai; gr[H] = daf; gr[2 * H] = daz; gr[3 * H] = dao;

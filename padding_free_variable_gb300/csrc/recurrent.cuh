@@ -22,6 +22,14 @@ struct RecArgs {
     float* h_n;               // [ndir][B][H] caller order, optional
     float* c_n;
     const float* dy;          // backward: [rows][ndir*H]
+    // initial states ([ndir][B][H] fp32, caller order; NULL = zero).  The product R h0 is
+    // folded into the first step's pre-activations before the recurrent kernels run, so
+    // they read h0 only as the final state of an empty sequence.
+    const float* h0;
+    const float* c0;
+    const float* dh_n;        // backward: dL/dh_n from outside (NULL = zero)
+    const float* dc_n;        // backward: dL/dc_n from outside (NULL = zero)
+    float* dc0;               // backward: dL/dc0, written at each sequence's first step (NULL: not wanted)
     float* db;                // backward: [ndir][4H]
     float* dpeep;             // backward: [ndir][3][H]
     float* part;              // backward: [2][ndir][B][G][H] partial R^T da exchange
@@ -32,7 +40,8 @@ struct RecArgs {
     int tables_in_smem;
     int mma_mw, mma_kw;       // forward tensor-core product: warps along rows and along k
     int tm_chains, tm_acol;   // cluster kernels: TMEM accumulator chains, first column of the R operand
-    int tma_pre;              // cluster forward kernel: gate pre-activations arrive by TMA (tile at off_red)
+    int tma_pre;              // cluster kernels: the cell's operands arrive as TMA tiles (at off_red)
+    int grp_rows, ngroups;    // cluster kernels: sorted slots per sequence group, groups (one cluster each per direction)
     // dynamic shared-memory layout (byte offsets)
     int off_h, off_red, off_acc, off_state, off_contrib, off_sums, off_tab, off_peep;
 };
@@ -49,6 +58,8 @@ struct RecConfig {
     int acol = 0;       // cluster kernels: TMEM column of the R operand
     int bulk = 0;       // cluster forward kernel: 1 = bulk-copy exchange into a double-buffered operand
     int tma_pre = 0;    // cluster forward kernel: 1 = pre-activation tiles loaded by TMA
+    int grp_rows = 0;   // cluster kernels: sorted slots per sequence group
+    int ngroups = 1;    // cluster kernels: sequence groups (one cluster per direction each)
     size_t smem = 0;    // dynamic shared memory bytes
 };
 
@@ -61,6 +72,8 @@ lstm_status rec_launch(const Plan& p, const RecConfig& c, RecArgs a, bool bwd, c
 
 // Cluster-resident forward kernel: configured when one direction's R fits a
 // cluster of H/32 CTAs (<= 16) with its operand buffers; false otherwise.
+// The batch's sorted slots are cut into sequence groups, one cluster per
+// (direction, group).
 bool rec_cluster_fwd_configure(const Plan& p, int H, int ndir, bool bf16, RecConfig* out, RecArgs* layout);
 lstm_status rec_cluster_fwd_launch(const Plan& p, const RecConfig& c, RecArgs a, cudaStream_t s);
 

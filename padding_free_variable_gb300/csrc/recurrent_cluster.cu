@@ -2,30 +2,39 @@
 //
 // The same recurrence as lstm_rec_fwd_kernel ("Single Stream Parallelization
 // of Generalized LSTM-Like RNNs on a GPU", Sec. 3: one sequential step per
-// frame, the delayed connection R h_{t-1} then the cell), laid out for a
-// thread-block cluster when one direction's R fits in the cluster:
+// frame, the delayed connection R h_{t-1} then the cell), laid out for
+// thread-block clusters when one direction's R fits in a cluster:
 //
-//  * one cluster of G = H/32 CTAs per direction; CTA c owns units
-//    [32c, 32c+32) and their 128 gate rows of R, resident in TENSOR MEMORY
-//    as the MMA's A operand (bf16; fp32 weights are stored as bf16 hi + lo
-//    and multiplied as lo*hi + hi*lo + hi*hi).  With A in tensor memory an
-//    M=128, N=32, K=16 MMA reads only its 1 KB B tile from shared memory
-//    (measured on GB300: ~19 cycles per MMA with 4 issuing warps, against
-//    ~43 with A in shared memory, where the 4 KB A tile bounds it);
+//  * sequence groups: the sorted slots are cut into contiguous groups of S
+//    slots, and every (direction, group) pair is one cluster of G = H/32
+//    CTAs.  Sequences are independent, so the clusters never communicate;
+//    a group runs only as many steps as its longest sequence, and each
+//    cluster moves only its own rows between its CTAs every step;
+//  * CTA c of a cluster owns units [32c, 32c+32) and their 128 gate rows of
+//    R, resident in TENSOR MEMORY as the MMA's A operand.  bf16 weights are
+//    one bf16 piece; fp32 weights (and the fp32 B operands h_{t-1} or the
+//    gate errors) are three bf16 pieces v0 + v1 + v2 (v0 = bf16(v), each
+//    further piece the bf16 rounding of what the earlier ones leave), and
+//    each K = 16 step issues the six piece products above 2^-24 of the
+//    leading one, so the product keeps fp32 accuracy.  With A in tensor
+//    memory an M=128, N<=32, K=16 MMA reads only its B tile from shared
+//    memory (measured on GB300: ~19 cycles per MMA with 4 issuing warps,
+//    against ~43 with A in shared memory);
 //  * per step up to 4 warps each issue one chain of tcgen05.mma into their
-//    own accumulator: D[128 gate rows][n rows] = R_slice x h_{t-1}^T, h taken
-//    from a shared-memory operand buffer that the peers filled;
-//  * the cell runs on the summed chains, and each CTA writes its new h
-//    (split and swizzled) straight into every peer's operand buffer through
-//    distributed shared memory.  The buffer is single: a split cluster
-//    barrier (arrive once this CTA's MMAs have read it, wait before writing
-//    to the peers) orders the overwrite;
-//  * one hardware cluster barrier per step replaces the grid-wide flag
-//    barrier (measured on GB300: ~0.22 us for 16 CTAs against ~1.8 us for a
-//    64-CTA flag barrier).
-// Every CTA of a cluster runs exactly the same sequence of cluster barriers,
-// so none can leave early; the only other wait (MMA completion) is bounded
-// and a timeout is recorded in the plan's status word.
+//    own accumulator columns (chains summed at read-out); N is the group's
+//    active rows rounded up to 16;
+//  * the cell runs on the summed chains, and each CTA sends its h_t (bf16
+//    pieces, swizzled) to every peer of its cluster.  Two exchanges:
+//    BULK -- the operand is double-buffered per step parity; each CTA stages
+//    its h_t and pushes it with one cp.async.bulk per peer and piece into the
+//    peer's buffer of the other parity, completing on the peer's mbarrier of
+//    that parity.  The data's arrival is the step's synchronisation: no
+//    cluster barrier runs in the step loop.  Otherwise (the double buffers do
+//    not fit): one operand buffer written with DSMEM stores between the two
+//    halves of a split cluster barrier.
+// Every wait but the hardware cluster barrier (which every CTA of a cluster
+// reaches by construction) is bounded, and a timeout is recorded in the
+// plan's status word.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -94,16 +103,20 @@ __device__ __forceinline__ void prefetch_rows(const float* m, int64_t ld, int ro
     for (int j = threadIdx.x; j < n; j += kCT) prefetch_l2(m + (int64_t)(row0 + j) * ld + col0);
 }
 
-// 4 fp32 values -> bf16 hi and lo remainder, 2 per word
-__device__ __forceinline__ void split4(const float (&v)[4], uint2& hi, uint2& lo, bool want_lo)
+// 4 fp32 values -> NP bf16 pieces, 2 per word: piece 0 = bf16(v), piece k = bf16 of what
+// pieces 0..k-1 leave of v (each difference is exact in fp32)
+template <int NP>
+__device__ __forceinline__ void split4(const float (&v)[4], uint2 (&pc)[NP])
 {
-    const uint32_t h0 = bf16x2(v[0], v[1]), h1 = bf16x2(v[2], v[3]);
-    hi = make_uint2(h0, h1);
-    if (want_lo) {
-        lo = make_uint2(bf16x2(v[0] - __uint_as_float(h0 << 16), v[1] - __uint_as_float(h0 & 0xffff0000u)),
-                        bf16x2(v[2] - __uint_as_float(h1 << 16), v[3] - __uint_as_float(h1 & 0xffff0000u)));
-    } else {
-        lo = make_uint2(0u, 0u);
+    float r[4] = {v[0], v[1], v[2], v[3]};
+#pragma unroll
+    for (int k = 0; k < NP; ++k) {
+        const uint32_t w0 = bf16x2(r[0], r[1]), w1 = bf16x2(r[2], r[3]);
+        pc[k] = make_uint2(w0, w1);
+        r[0] -= __uint_as_float(w0 << 16);
+        r[1] -= __uint_as_float(w0 & 0xffff0000u);
+        r[2] -= __uint_as_float(w1 << 16);
+        r[3] -= __uint_as_float(w1 & 0xffff0000u);
     }
 }
 
@@ -150,26 +163,48 @@ __device__ __forceinline__ void cluster_wait()
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// 32 consecutive fp32 (or bf16) weights -> 16 bf16x2 words (hi) and, for
-// fp32 weights, 16 words of the rounded remainder (lo).
-template <bool SPLIT>
-__device__ __forceinline__ void split32(const float (&v)[32], uint32_t (&hi)[16], uint32_t (&lo)[16])
+// 32 consecutive fp32 (or bf16) weights -> NP pieces of 16 bf16x2 words (as split4)
+template <int NP>
+__device__ __forceinline__ void split32(const float (&v)[32], uint32_t (&pc)[NP][16])
 {
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-        hi[e] = bf16x2(v[2 * e], v[2 * e + 1]);
-        lo[e] = SPLIT ? bf16x2(v[2 * e] - __uint_as_float(hi[e] << 16),
-                               v[2 * e + 1] - __uint_as_float(hi[e] & 0xffff0000u))
-                      : 0u;
+        float r0 = v[2 * e], r1 = v[2 * e + 1];
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+            const uint32_t w = bf16x2(r0, r1);
+            pc[k][e] = w;
+            r0 -= __uint_as_float(w << 16);
+            r1 -= __uint_as_float(w & 0xffff0000u);
+        }
+    }
+}
+
+// One K = 16 step of D += A B^T with both operands in NP bf16 pieces: A piece k at TMEM
+// column a + k * ap, B piece k at descriptor b + k * bp.  NP = 3: the six piece products
+// x_i y_j with i + j <= 2 (each of the others is below 2^-26 of x0 y0), smallest first.
+template <int NP>
+__device__ __forceinline__ void mma_k16(uint32_t d, uint32_t a, uint32_t ap, uint64_t b, uint64_t bp, uint32_t idesc,
+                                        uint32_t acc)
+{
+    if (NP == 1) {
+        tc::mma_bf16_ts(d, a, b, idesc, acc);
+    } else {
+        tc::mma_bf16_ts(d, a + ap, b + bp, idesc, acc);          // x1 y1
+        tc::mma_bf16_ts(d, a + 2u * ap, b, idesc, 1u);            // x2 y0
+        tc::mma_bf16_ts(d, a, b + 2u * bp, idesc, 1u);            // x0 y2
+        tc::mma_bf16_ts(d, a + ap, b, idesc, 1u);                 // x1 y0
+        tc::mma_bf16_ts(d, a, b + bp, idesc, 1u);                 // x0 y1
+        tc::mma_bf16_ts(d, a, b, idesc, 1u);                      // x0 y0
     }
 }
 
 // One chain of the forward product: k-steps i = 4J + ch + v*NCH (v < 4/NCH)
 // over the 64-column blocks J of the B operand.  A (R slice) in TMEM from
-// column a_hi (lo part at a_lo), B in shared memory (descriptors bh, bl),
-// `bstep` = descriptor units between B blocks.
-template <int NCH, bool SPLIT>
-__device__ __forceinline__ void issue_chain(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t bh, uint64_t bl,
+// column a0 (pieces ap apart), B in shared memory from descriptor b0 (pieces
+// bp apart), `bstep` = descriptor units between B blocks.
+template <int NCH, int NP>
+__device__ __forceinline__ void issue_chain(uint32_t d, uint32_t a0, uint32_t ap, uint64_t b0, uint64_t bp,
                                             uint32_t bstep, int nks, int ch, uint32_t idesc)
 {
     uint32_t acc = 0u;
@@ -181,13 +216,7 @@ __device__ __forceinline__ void issue_chain(uint32_t d, uint32_t a_hi, uint32_t 
             if (i < nks) {
                 const uint64_t bo = (uint64_t)(J * bstep + 2 * w);      // 32 bytes per k-step of 16
                 const uint32_t ac = (uint32_t)(i * 8);                  // 8 columns per k-step of 16
-                if (SPLIT) {
-                    tc::mma_bf16_ts(d, a_lo + ac, bh + bo, idesc, acc);
-                    tc::mma_bf16_ts(d, a_hi + ac, bl + bo, idesc, 1u);
-                    tc::mma_bf16_ts(d, a_hi + ac, bh + bo, idesc, 1u);
-                } else {
-                    tc::mma_bf16_ts(d, a_hi + ac, bh + bo, idesc, acc);
-                }
+                mma_k16<NP>(d, a0 + ac, ap, b0 + bo, bp, idesc, acc);
                 acc = 1u;
             }
         }
@@ -196,8 +225,8 @@ __device__ __forceinline__ void issue_chain(uint32_t d, uint32_t a_hi, uint32_t 
 
 // The same chain over a B operand in 32-column blocks (64-byte swizzle, two
 // k-steps of 16 per block).
-template <int NCH, bool SPLIT>
-__device__ __forceinline__ void issue_chain32(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t bh, uint64_t bl,
+template <int NCH, int NP>
+__device__ __forceinline__ void issue_chain32(uint32_t d, uint32_t a0, uint32_t ap, uint64_t b0, uint64_t bp,
                                               uint32_t bstep, int nks, int ch, uint32_t idesc)
 {
     uint32_t acc = 0u;
@@ -205,21 +234,15 @@ __device__ __forceinline__ void issue_chain32(uint32_t d, uint32_t a_hi, uint32_
     for (int i = ch; i < nks; i += NCH) {
         const uint64_t bo = (uint64_t)((uint32_t)(i >> 1) * bstep + (uint32_t)(i & 1) * 2u);
         const uint32_t ac = (uint32_t)(i * 8);
-        if (SPLIT) {
-            tc::mma_bf16_ts(d, a_lo + ac, bh + bo, idesc, acc);
-            tc::mma_bf16_ts(d, a_hi + ac, bl + bo, idesc, 1u);
-            tc::mma_bf16_ts(d, a_hi + ac, bh + bo, idesc, 1u);
-        } else {
-            tc::mma_bf16_ts(d, a_hi + ac, bh + bo, idesc, acc);
-        }
+        mma_k16<NP>(d, a0 + ac, ap, b0 + bo, bp, idesc, acc);
         acc = 1u;
     }
 }
 
 // The same with a compile-time k-step count, fully unrolled (the issuing
 // thread's own instruction stream bounds the issue rate of small MMAs).
-template <int NCH, int NKS, int KPB, bool SPLIT>
-__device__ __forceinline__ void issue_chain_fixed(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t bh, uint64_t bl,
+template <int NCH, int NKS, int KPB, int NP>
+__device__ __forceinline__ void issue_chain_fixed(uint32_t d, uint32_t a0, uint32_t ap, uint64_t b0, uint64_t bp,
                                                   uint32_t bstep, int ch, uint32_t idesc)
 {
 #pragma unroll
@@ -227,28 +250,21 @@ __device__ __forceinline__ void issue_chain_fixed(uint32_t d, uint32_t a_hi, uin
         const int i = ch + jj * NCH;
         const uint64_t bo = (uint64_t)((uint32_t)(i / KPB) * bstep + (uint32_t)(i % KPB) * 2u);
         const uint32_t ac = (uint32_t)(i * 8);
-        const uint32_t acc = jj == 0 ? 0u : 1u;
-        if (SPLIT) {
-            tc::mma_bf16_ts(d, a_lo + ac, bh + bo, idesc, acc);
-            tc::mma_bf16_ts(d, a_hi + ac, bl + bo, idesc, 1u);
-            tc::mma_bf16_ts(d, a_hi + ac, bh + bo, idesc, 1u);
-        } else {
-            tc::mma_bf16_ts(d, a_hi + ac, bh + bo, idesc, acc);
-        }
+        mma_k16<NP>(d, a0 + ac, ap, b0 + bo, bp, idesc, jj == 0 ? 0u : 1u);
     }
 }
 
-template <bool SPLIT>
-__device__ __forceinline__ void issue_chains32(int nch, uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t bh,
-                                               uint64_t bl, uint32_t bstep, int nks, int ch, uint32_t idesc)
+template <int NP>
+__device__ __forceinline__ void issue_chains32(int nch, uint32_t d, uint32_t a0, uint32_t ap, uint64_t b0,
+                                               uint64_t bp, uint32_t bstep, int nks, int ch, uint32_t idesc)
 {
-    if (nch == 4 && nks == 16) issue_chain_fixed<4, 16, 2, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, ch, idesc);
-    else if (nch == 4 && nks == 32) issue_chain_fixed<4, 32, 2, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, ch, idesc);
-    else if (nch == 4 && nks == 8) issue_chain_fixed<4, 8, 2, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, ch, idesc);
-    else if (nch == 2 && nks == 16) issue_chain_fixed<2, 16, 2, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, ch, idesc);
-    else if (nch == 4) issue_chain32<4, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, nks, ch, idesc);
-    else if (nch == 2) issue_chain32<2, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, nks, ch, idesc);
-    else issue_chain32<1, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, nks, ch, idesc);
+    if (nch == 4 && nks == 16) issue_chain_fixed<4, 16, 2, NP>(d, a0, ap, b0, bp, bstep, ch, idesc);
+    else if (nch == 4 && nks == 32) issue_chain_fixed<4, 32, 2, NP>(d, a0, ap, b0, bp, bstep, ch, idesc);
+    else if (nch == 4 && nks == 8) issue_chain_fixed<4, 8, 2, NP>(d, a0, ap, b0, bp, bstep, ch, idesc);
+    else if (nch == 2 && nks == 16) issue_chain_fixed<2, 16, 2, NP>(d, a0, ap, b0, bp, bstep, ch, idesc);
+    else if (nch == 4) issue_chain32<4, NP>(d, a0, ap, b0, bp, bstep, nks, ch, idesc);
+    else if (nch == 2) issue_chain32<2, NP>(d, a0, ap, b0, bp, bstep, nks, ch, idesc);
+    else issue_chain32<1, NP>(d, a0, ap, b0, bp, bstep, nks, ch, idesc);
 }
 
 // Shared-memory descriptor of a K-major operand in the 64-byte swizzled
@@ -320,28 +336,32 @@ __device__ __forceinline__ void tmem_sum_chains(uint32_t taddr0, uint32_t stride
         }
 }
 
-template <bool SPLIT>
-__device__ __forceinline__ void issue_chains(int nch, uint32_t d, uint32_t a_hi, uint32_t a_lo, uint64_t bh,
-                                             uint64_t bl, uint32_t bstep, int nks, int ch, uint32_t idesc)
+template <int NP>
+__device__ __forceinline__ void issue_chains(int nch, uint32_t d, uint32_t a0, uint32_t ap, uint64_t b0,
+                                             uint64_t bp, uint32_t bstep, int nks, int ch, uint32_t idesc)
 {
-    if (nch == 4) issue_chain<4, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, nks, ch, idesc);
-    else if (nch == 2) issue_chain<2, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, nks, ch, idesc);
-    else issue_chain<1, SPLIT>(d, a_hi, a_lo, bh, bl, bstep, nks, ch, idesc);
+    if (nch == 4) issue_chain<4, NP>(d, a0, ap, b0, bp, bstep, nks, ch, idesc);
+    else if (nch == 2) issue_chain<2, NP>(d, a0, ap, b0, bp, bstep, nks, ch, idesc);
+    else issue_chain<1, NP>(d, a0, ap, b0, bp, bstep, nks, ch, idesc);
 }
 
 }  // namespace
 
 // Shared memory (RecArgs offsets): off_acc = accs, off_state = cell states,
-// off_contrib = B operand (h_{t-1}, hi then lo), off_sums = mbarrier, TMEM
-// slot and failure flag, off_tab = tables, off_peep = peepholes.
-// Tensor memory: accumulator chains in columns [0, chains * NBM), the R slice
-// (hi, then lo for fp32 weights, H/2 columns each) from column tm_acol.
+// off_contrib = B operand (h_{t-1}, its NP pieces), off_sums = mbarriers, TMEM
+// slot, failure flag and the group's step count, off_tab = tables, off_peep =
+// peepholes.  Tensor memory: accumulator chains in columns [0, chains * NBM),
+// the R slice (NP pieces of H/2 columns each) from column tm_acol.
+//
+// The cluster serves sorted slots [j0, j0 + S) of direction `dir`: its step t
+// has rows off[t] + j0 .. + n - 1, n = min(max(bs[t] - j0, 0), S), and it runs
+// the Tg steps with n > 0 (Tg = the group's longest length).
 //
 // Two exchanges of h_t between the CTAs of a cluster:
 //  * BULK: the operand is double-buffered per step parity, in 32-unit blocks
 //    of the 64-byte swizzled layout, so that one CTA's units of all rows are
 //    one contiguous block.  Each CTA stages its h_t there in its own shared
-//    memory and copies it with one cp.async.bulk per peer (hi and lo), which
+//    memory and copies it with one cp.async.bulk per peer and piece, which
 //    completes on the peer's mbarrier of that parity: the arrival of the
 //    data is the step's synchronisation, and no cluster barrier runs inside
 //    the step loop.  A peer can only send h_{t+1} into buffer (s & 1) after
@@ -358,7 +378,7 @@ __device__ __forceinline__ void issue_chains(int nch, uint32_t d, uint32_t a_hi,
 // by one thread right after the previous step's cell has read the tile: the
 // product's window stays free of the 256 threads' global loads (measured to
 // delay the MMAs' completion by ~0.8 us).
-template <bool SPLIT, bool BULK>
+template <int NP, bool BULK>
 __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a, const __grid_constant__ CUtensorMap pre_map)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -366,60 +386,75 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
     cg::cluster_group cl = cg::this_cluster();
     const int G = a.G;
     const int rank = (int)cl.block_rank();
-    const int dir = blockIdx.x / G;
+    const int ng = a.ngroups;
+    const int dir = (int)(blockIdx.x / G) / ng, grp = (int)(blockIdx.x / G) % ng;
+    const int S = a.grp_rows, j0 = grp * S;           // this cluster's sorted slots [j0, j0 + S)
+    const int srank = grp == 0 ? rank : -1;           // the phase stamps come from group 0
     const int H = a.H, T = a.T, NBM = a.JC;          // JC carries the operand buffer rows (multiple of 16)
     const int KB = (H + 63) / 64;
     const int u0 = rank * kCU;
     const int ndH = a.ndir * H, nd4H = a.ndir * 4 * H;
     const int nch = a.tm_chains;
     float* accs = reinterpret_cast<float*>(base + a.off_acc);        // [NBM][128]
-    float* cst = reinterpret_cast<float*>(base + a.off_state);       // [B][32]
-    // B operand: BULK [2 parity][2 hi/lo][G][NBM][64 B], else [2 hi/lo][KB][NBM][128 B]
+    float* cst = reinterpret_cast<float*>(base + a.off_state);       // [S][32]
+    // B operand: BULK [2 parity][NP][G][NBM][64 B], else [NP][KB][NBM][128 B]
     uint8_t* Bb = base + a.off_contrib;
     uint64_t* mma_bar = reinterpret_cast<uint64_t*>(base + a.off_sums);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 1);
     int* s_fail = reinterpret_cast<int*>(tmem_slot + 1);
     uint64_t* full_bar = mma_bar + 2;                                // BULK: [2] operand arrival per parity
     uint64_t* pre_bar = mma_bar + 4;                                 // tma_pre: arrival of a step's tile
+    int* s_tg = reinterpret_cast<int*>(mma_bar + 6);                 // the group's step count
     float* pre_tile = reinterpret_cast<float*>(base + a.off_red);    // tma_pre: [4 gates][NBM][32]
     const bool tma_pre = a.tma_pre != 0;
     float* peep_s = reinterpret_cast<float*>(base + a.off_peep);     // [3][32]
-    int* s_bs = reinterpret_cast<int*>(base + a.off_tab);
-    int* s_off = s_bs + T;
-    int* s_len = s_off + T + 1;
-    uint8_t* stage = base + a.off_h;                                 // BULK: [2 parity][2 hi/lo][NBM][64 B]
-    const size_t bsz = BULK ? (size_t)G * NBM * 64 : (size_t)KB * NBM * 128;   // bytes of one B operand
-    const size_t ssz = (size_t)NBM * 64;                             // bytes of one staged h slice
-    auto Bop = [&](int parity, int lo) -> uint8_t* {
-        return Bb + (BULK ? (size_t)parity * (SPLIT ? 2 : 1) * bsz : 0) + (size_t)lo * bsz;
+    int* s_bs = reinterpret_cast<int*>(base + a.off_tab);            // [T] the group's active rows
+    int* s_off = s_bs + T;                                           // [T+1] the group's first row
+    int* s_len = s_off + T + 1;                                      // [S] lengths of the group's slots
+    uint8_t* stage = base + a.off_h;                                 // BULK: [2 parity][NP][NBM][64 B]
+    const size_t bsz = BULK ? (size_t)G * NBM * 64 : (size_t)KB * NBM * 128;   // bytes of one B piece
+    const size_t ssz = (size_t)NBM * 64;                             // bytes of one staged h piece
+    auto Bop = [&](int parity, int piece) -> uint8_t* {
+        return Bb + (BULK ? (size_t)parity * NP * bsz : 0) + (size_t)piece * bsz;
     };
-    auto Stg = [&](int parity, int lo) -> uint8_t* { return stage + (size_t)(parity * 2 + lo) * ssz; };
+    auto Stg = [&](int parity, int piece) -> uint8_t* { return stage + (size_t)(parity * NP + piece) * ssz; };
+    int Tg = 0;
     // rows of h of step s2 - 1 that step s2 reads: the rows continuing into step s2.  Rows past
     // them are never read going forward (finished sequences) and were never written going
     // backward (sequences not yet started: still zero from the set-up)
     auto step_rows = [&](int s2) -> int {
-        const int tp = dir == 0 ? s2 - 1 : T - s2, tn = dir == 0 ? s2 : T - 1 - s2;
+        const int tp = dir == 0 ? s2 - 1 : Tg - s2, tn = dir == 0 ? s2 : Tg - 1 - s2;
         return min(s_bs[tp], s_bs[tn]);
     };
     // bytes a CTA receives for step s2: those rows from every other CTA (its own it writes itself)
     auto step_bytes = [&](int s2) -> uint32_t {
-        return (uint32_t)(G - 1) * (SPLIT ? 2u : 1u) * (uint32_t)step_rows(s2) * 64u;
+        return (uint32_t)(G - 1) * (uint32_t)NP * (uint32_t)step_rows(s2) * 64u;
     };
     const uint32_t tcols = (uint32_t)a.Umax;                         // Umax carries the TMEM columns
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- set-up: operand zeroed, tables, barrier, tensor memory
-    for (size_t i = threadIdx.x; i < (BULK ? 2 : 1) * (SPLIT ? 2 : 1) * bsz / 16; i += kCT)
+    // ---- set-up: operand zeroed, the group's tables, barriers, tensor memory
+    for (size_t i = threadIdx.x; i < (BULK ? 2 : 1) * NP * bsz / 16; i += kCT)
         reinterpret_cast<uint4*>(Bb)[i] = make_uint4(0, 0, 0, 0);
     if (BULK)
-        for (size_t i = threadIdx.x; i < 4 * ssz / 16; i += kCT) reinterpret_cast<uint4*>(stage)[i] = make_uint4(0, 0, 0, 0);
-    for (int i = threadIdx.x; i < T; i += kCT) s_bs[i] = a.bs[i];
-    for (int i = threadIdx.x; i <= T; i += kCT) s_off[i] = a.off[i];
-    for (int i = threadIdx.x; i < a.B; i += kCT) s_len[i] = a.slot_len[i];
+        for (size_t i = threadIdx.x; i < 2 * NP * ssz / 16; i += kCT) reinterpret_cast<uint4*>(stage)[i] = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x == 0) *s_tg = 0;
+    __syncthreads();
+    // bs is non-increasing in t, so the group's steps are t < Tg, Tg = the one t whose
+    // successor has no row of the group
+    for (int i = threadIdx.x; i < T; i += kCT) {
+        const int n = min(max(a.bs[i] - j0, 0), S);
+        s_bs[i] = n;
+        if (n > 0 && (i + 1 == T || a.bs[i + 1] <= j0)) *s_tg = i + 1;
+    }
+    for (int i = threadIdx.x; i <= T; i += kCT) s_off[i] = a.off[i] + j0;
+    for (int i = threadIdx.x; i < S; i += kCT) s_len[i] = j0 + i < a.B ? a.slot_len[j0 + i] : 0;
     for (int i = threadIdx.x; i < 3 * kCU; i += kCT) {
         const int q = i / kCU, uu = i - q * kCU;
         peep_s[i] = a.peep[(size_t)dir * 3 * H + q * H + u0 + uu];
     }
+    __syncthreads();
+    Tg = *s_tg;
     if (threadIdx.x == 0) {
         tc::mbar_init(mma_bar, (uint32_t)nch);
         *s_fail = 0;
@@ -431,7 +466,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
         tc::fence_mbar_init();
         // the operand of step 1 (parity 1) is armed before the cluster barrier below,
         // i.e. before any peer can send
-        if (BULK && T > 1) tc::mbar_arrive_expect_tx(&full_bar[1], step_bytes(1));
+        if (BULK && Tg > 1) tc::mbar_arrive_expect_tx(&full_bar[1], step_bytes(1));
     }
     if (threadIdx.x < 32) {
         tc::tmem_alloc(tmem_slot, tcols);
@@ -442,7 +477,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
     __syncthreads();
     tc::tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t a_hi = tmem + (uint32_t)a.tm_acol, a_lo = a_hi + (uint32_t)(H / 2);
+    const uint32_t a0 = tmem + (uint32_t)a.tm_acol, ap = (uint32_t)(H / 2);
     // R slice -> tensor memory: lane 32g + uu holds gate row g of unit u0 + uu (the MMA's row
     // order), column c of the slice holds k = 2c and 2c + 1; warps g and g + 4 share the lanes
     // of gate g and take alternate 32-wide k chunks
@@ -452,7 +487,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
         const uint32_t lanes = (uint32_t)(32 * g) << 16;
         for (int cc = warp >> 2; cc < H / 32; cc += 2) {
             float v[32];
-            if (SPLIT) {
+            if (NP > 1) {
                 const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.R) + grow + 32 * cc);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -464,20 +499,20 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
 #pragma unroll
                 for (int e = 0; e < 32; ++e) v[e] = __bfloat162float(src[e]);
             }
-            uint32_t hi[16], lo[16];
-            split32<SPLIT>(v, hi, lo);
-            tc::tmem_st_32x32b_x16(a_hi + lanes + (uint32_t)(16 * cc), hi);
-            if (SPLIT) tc::tmem_st_32x32b_x16(a_lo + lanes + (uint32_t)(16 * cc), lo);
+            uint32_t pc[NP][16];
+            split32<NP>(v, pc);
+#pragma unroll
+            for (int k = 0; k < NP; ++k) tc::tmem_st_32x32b_x16(a0 + (uint32_t)k * ap + lanes + (uint32_t)(16 * cc), pc[k]);
         }
         tc::tmem_wait_st();
     }
     if (a.h_n) {
-        for (int idx = threadIdx.x; idx < a.B * kCU; idx += kCT) {
+        for (int idx = threadIdx.x; idx < S * kCU; idx += kCT) {
             const int j = idx / kCU, uu = idx - j * kCU;
-            if (s_len[j] == 0) {
-                const size_t o = ((size_t)dir * a.B + a.perm[j]) * H + u0 + uu;
-                a.h_n[o] = 0.f;
-                if (a.c_n) a.c_n[o] = 0.f;
+            if (j0 + j < a.B && s_len[j] == 0) {        // an empty sequence ends in its initial state
+                const size_t o = ((size_t)dir * a.B + a.perm[j0 + j]) * H + u0 + uu;
+                a.h_n[o] = a.h0 ? a.h0[o] : 0.f;
+                if (a.c_n) a.c_n[o] = a.c0 ? a.c0[o] : 0.f;
             }
         }
     }
@@ -487,7 +522,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
     // tma_pre: the four gate tiles of step s2 (rows from off[t2], NBM of them; rows past the
     // packed rows read 0), one thread, completing on pre_bar
     auto issue_pre = [&](int s2, bool fence) {
-        const int t2 = dir == 0 ? s2 : T - 1 - s2;
+        const int t2 = dir == 0 ? s2 : Tg - 1 - s2;
         if (fence) fence_proxy_async_cta();
         tc::mbar_arrive_expect_tx(pre_bar, (uint32_t)(4 * NBM * kCU * 4));
 #pragma unroll
@@ -495,7 +530,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
             tc::tma_load_2d(pre_tile + (size_t)g * NBM * kCU, &pre_map, pre_bar, dir * 4 * H + g * H + u0, s_off[t2]);
     };
     int last_tile = -1;                   // tile issuer: the last step whose tile was issued
-    if (tma_pre && threadIdx.x == kTileIssuer) { issue_pre(0, true); last_tile = 0; }
+    if (tma_pre && threadIdx.x == kTileIssuer && Tg > 0) { issue_pre(0, true); last_tile = 0; }
     cl.sync();     // every CTA of the cluster is resident before any remote write
 
     const int jq = threadIdx.x >> 3, q8 = threadIdx.x & 7;          // cell item: row jq (+32k), units q8*4..+4
@@ -508,16 +543,16 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
     const uint32_t bstep = (uint32_t)(NBM * (BULK ? 64 : 128)) >> 4;  // descriptor units between B blocks
     bool failed = false;                  // CTA-uniform: an MMA completion wait timed out
     bool pre_ok_prev = true;              // this thread's wait for the previous step's tile
-    for (int s = 0; s < T; ++s) {
-        const int t = dir == 0 ? s : T - 1 - s;
+    for (int s = 0; s < Tg; ++s) {
+        const int t = dir == 0 ? s : Tg - 1 - s;
         const int n = s_bs[t];
         const int rowbase = s_off[t];
-        const int n_prev = dir == 0 ? (t >= 1 ? n : 0) : (t + 1 < T ? s_bs[t + 1] : 0);
+        const int n_prev = dir == 0 ? (t >= 1 ? n : 0) : (t + 1 < Tg ? s_bs[t + 1] : 0);
         const int NBs = (n + 15) & ~15;
         const int par = BULK ? (s & 1) : 0;
         bool arrived = true;          // this step's operand (and the previous step's tile) arrived
         if (BULK) {
-            cstamp(a, false, dir, rank, s, 0, 0);
+            cstamp(a, false, dir, srank, s, 0, 0);
             // h_{t-1} of every peer has arrived in this step's operand
             if (s > 0 && !failed)
                 arrived = tc::mbar_wait(&full_bar[par], (uint32_t)(((s - 1) >> 1) & 1), a.wait_limit_ns);
@@ -526,28 +561,29 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
                 cluster_wait();    // h_{t-1} of every peer is in this CTA's operand
                 // every thread of this CTA arrived after its cell: the tile is free
                 if (tma_pre && threadIdx.x == kTileIssuer && !failed) { issue_pre(s, true); last_tile = s; }
-                cstamp(a, false, dir, rank, s - 1, 4, 4);
+                cstamp(a, false, dir, srank, s - 1, 4, 4);
             }
-            cstamp(a, false, dir, rank, s, 0, 0);
+            cstamp(a, false, dir, srank, s, 0, 0);
         }
         // D[gate rows][rows] = R_slice x h_{t-1}^T: chain ch is issued by warp ch into its own
         // accumulator, so the chains overlap
         if (lane == 0 && warp < nch && !failed) {
             fence_proxy_async_cta();
             tc::tc_fence_after_sync();
-            cstamp(a, false, dir, rank, s, 1, 1);
+            cstamp(a, false, dir, srank, s, 1, 1);
             const uint32_t idesc = tc::idesc_bf16_f32(kCM, NBs);
+            const uint64_t bp = (uint64_t)(bsz >> 4);                  // descriptor units between B pieces
             if (BULK) {
-                const uint64_t dbh = sdesc_sw64(tc::smem_u32(Bop(par, 0))), dbl = sdesc_sw64(tc::smem_u32(Bop(par, 1)));
-                issue_chains32<SPLIT>(nch, tmem + (uint32_t)(warp * NBM), a_hi, a_lo, dbh, dbl, bstep, nks, warp, idesc);
+                const uint64_t db0 = sdesc_sw64(tc::smem_u32(Bop(par, 0)));
+                issue_chains32<NP>(nch, tmem + (uint32_t)(warp * NBM), a0, ap, db0, bp, bstep, nks, warp, idesc);
             } else {
-                const uint64_t dbh = tc::sdesc_sw128(tc::smem_u32(Bop(0, 0))), dbl = tc::sdesc_sw128(tc::smem_u32(Bop(0, 1)));
-                issue_chains<SPLIT>(nch, tmem + (uint32_t)(warp * NBM), a_hi, a_lo, dbh, dbl, bstep, nks, warp, idesc);
+                const uint64_t db0 = tc::sdesc_sw128(tc::smem_u32(Bop(0, 0)));
+                issue_chains<NP>(nch, tmem + (uint32_t)(warp * NBM), a0, ap, db0, bp, bstep, nks, warp, idesc);
             }
-            if (!(s == 0 && dir == 0 && rank == a.debug_skip_cta)) tc::mma_commit(mma_bar);   // test hook
+            if (!(s == 0 && dir == 0 && grp == 0 && rank == a.debug_skip_cta)) tc::mma_commit(mma_bar);   // test hook
         }
         if (warp < nch) __syncwarp();     // the issuing lane's warp does not poll while it issues
-        cstamp(a, false, dir, rank, s, 6, 6);
+        cstamp(a, false, dir, srank, s, 6, 6);
         // meanwhile (without tma_pre): the cell items' own operands (gate pre-activations),
         // rows jq and jq + 32
         float pre[2][4][4];
@@ -563,8 +599,8 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
                 }
             }
         }
-        if (!tma_pre && s + 1 < T) {   // next step's own rows into L2 (4 gate blocks of this CTA's units)
-            const int t2 = dir == 0 ? s + 1 : T - 2 - s;
+        if (!tma_pre && s + 1 < Tg) {   // next step's own rows into L2 (4 gate blocks of this CTA's units)
+            const int t2 = dir == 0 ? s + 1 : Tg - 2 - s;
             for (int g = 0; g < 4; ++g)
                 prefetch_rows(a.ga, nd4H, s_off[t2], s_bs[t2], dir * 4 * H + g * H + u0);
         }
@@ -580,7 +616,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
             record_failure(a.status, LSTM_ERR_TIMEOUT, (ok ? 0x60000u : 0x40000u) | (unsigned)s);
             *s_fail = 1 + s;
         }
-        cstamp(a, false, dir, rank, s, 7, 7);
+        cstamp(a, false, dir, srank, s, 7, 7);
         tc::tc_fence_after_sync();
         if (!BULK) cluster_arrive_relaxed();   // this CTA's product has read its operand: peers may overwrite it
         // accumulators -> shared: warp (quarter q = gate, half) reads lanes 32q.. in 16-column blocks
@@ -597,9 +633,9 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
         if (__syncthreads_or(!ok || !arrived)) failed = true;
         // BULK: re-arm this parity for step s + 2 before this CTA's h_t goes out (a peer
         // needs h_t before it can send h_{t+1})
-        if (BULK && threadIdx.x == 0 && !failed && s + 2 < T)
+        if (BULK && threadIdx.x == 0 && !failed && s + 2 < Tg)
             tc::mbar_arrive_expect_tx(&full_bar[par], step_bytes(s + 2));
-        cstamp(a, false, dir, rank, s, 2, 2);
+        cstamp(a, false, dir, srank, s, 2, 2);
         // cell: row j, units u0 + q8*4 .. +4; h_t kept (split) for the exchange.  Without the bulk
         // exchange the global outputs of rows jq and jq + 32 are written after the exchange's
         // barrier arrival, so that the arrival (a release) does not wait for them
@@ -609,7 +645,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
             record_failure(a.status, LSTM_ERR_TIMEOUT, 0x70000u | (unsigned)s);
             *s_fail = 1 + s;
         }
-        uint2 xh[4], xl[4];
+        uint2 xp[4][NP];
         float og_[2][4][4], oc_[2][4], oh_[2][4];
         auto store_outputs = [&](int j, const float (&gg)[4][4], const float (&cv)[4], const float (&hv)[4],
                                  uint2 hi) {
@@ -624,7 +660,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
             *reinterpret_cast<float4*>(a.y + yo) = make_float4(hv[0], hv[1], hv[2], hv[3]);
             if (a.y_lo) *reinterpret_cast<uint2*>(a.y_lo + yo) = hi;
             if (a.h_n && ((dir == 0 && t == len - 1) || (dir == 1 && t == 0 && len > 0))) {
-                const size_t o = ((size_t)dir * a.B + a.perm[j]) * H + u0 + q8 * 4;
+                const size_t o = ((size_t)dir * a.B + a.perm[j0 + j]) * H + u0 + q8 * 4;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     a.h_n[o + e] = hv[e];
@@ -667,7 +703,9 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
             }
             {
                 const float4 x = j < n_prev ? *reinterpret_cast<const float4*>(cst + j * kCU + q8 * 4)
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                                 : a.c0 ? __ldg(reinterpret_cast<const float4*>(
+                                              a.c0 + ((size_t)dir * a.B + a.perm[j0 + j]) * H + u0 + q8 * 4))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
                 cpv[0] = x.x; cpv[1] = x.y; cpv[2] = x.z; cpv[3] = x.w;
             }
 #pragma unroll
@@ -683,7 +721,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
                 gg[0][e] = ig; gg[1][e] = fg; gg[2][e] = zg; gg[3][e] = og; cv[e] = c; hv[e] = h;
             }
             *reinterpret_cast<float4*>(cst + j * kCU + q8 * 4) = make_float4(cv[0], cv[1], cv[2], cv[3]);
-            split4(hv, xh[it], xl[it], SPLIT);
+            split4<NP>(hv, xp[it]);
             if (!BULK && it < 2) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -693,64 +731,64 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
                     oh_[it][e] = hv[e];
                 }
             } else {
-                store_outputs(j, gg, cv, hv, xh[it]);
+                store_outputs(j, gg, cv, hv, xp[it][0]);
             }
         }
-        cstamp(a, false, dir, rank, s, 5, 5);
+        cstamp(a, false, dir, srank, s, 5, 5);
         if (BULK) {
             // h_t (rows [0, NBs)) staged in this CTA's 32-unit block, then one bulk copy per peer
             // and half into that peer's operand of step s + 1
-            if (s + 1 < T) {
+            if (s + 1 < Tg) {
 #pragma unroll
                 for (int it = 0; it < 4; ++it) {
                     const int j = jq + it * 32;
                     if (j >= n) continue;
                     const uint32_t o = sw64_off4(j, q8);
-                    *reinterpret_cast<uint2*>(Stg(par, 0) + o) = xh[it];
-                    if (SPLIT) *reinterpret_cast<uint2*>(Stg(par, 1) + o) = xl[it];
-                    // this CTA's own block of the next step's operand, written in place
+                    // this CTA's own block of the next step's operand is written in place
                     const size_t ob = (size_t)rank * NBM * 64 + o;
-                    *reinterpret_cast<uint2*>(Bop(par ^ 1, 0) + ob) = xh[it];
-                    if (SPLIT) *reinterpret_cast<uint2*>(Bop(par ^ 1, 1) + ob) = xl[it];
+#pragma unroll
+                    for (int k = 0; k < NP; ++k) {
+                        *reinterpret_cast<uint2*>(Stg(par, k) + o) = xp[it][k];
+                        *reinterpret_cast<uint2*>(Bop(par ^ 1, k) + ob) = xp[it][k];
+                    }
                 }
             }
             fence_proxy_async_cta();
             __syncthreads();
             // lane 0 of warp w sends to peers w, w + 8 (copies issued by one warp's lanes serialise)
             const bool sender = lane == 0 && warp < G;
-            if (s + 1 < T && sender && !failed) {
+            if (s + 1 < Tg && sender && !failed) {
                 const uint32_t nxt = (uint32_t)(par ^ 1);
                 const uint32_t bytes = (uint32_t)step_rows(s + 1) * 64u;
                 for (int p2 = warp; p2 < G; p2 += kCT / 32) {
                     if (p2 == (int)rank || bytes == 0) continue;
                     const uint32_t bar = mapa_u32(tc::smem_u32(&full_bar[nxt]), (uint32_t)p2);
-                    bulk_to_peer(mapa_u32(tc::smem_u32(Bop(nxt, 0) + (size_t)rank * NBM * 64), (uint32_t)p2), Stg(par, 0),
-                                 bytes, bar);
-                    if (SPLIT)
-                        bulk_to_peer(mapa_u32(tc::smem_u32(Bop(nxt, 1) + (size_t)rank * NBM * 64), (uint32_t)p2),
-                                     Stg(par, 1), bytes, bar);
+#pragma unroll
+                    for (int k = 0; k < NP; ++k)
+                        bulk_to_peer(mapa_u32(tc::smem_u32(Bop(nxt, k) + (size_t)rank * NBM * 64), (uint32_t)p2),
+                                     Stg(par, k), bytes, bar);
                 }
                 bulk_commit();
             }
-            cstamp(a, false, dir, rank, s, 4, 4);
-            if (tma_pre && threadIdx.x == kTileIssuer && s + 1 < T && !failed) {   // the tile has been read
+            cstamp(a, false, dir, srank, s, 4, 4);
+            if (tma_pre && threadIdx.x == kTileIssuer && s + 1 < Tg && !failed) {   // the tile has been read
                 issue_pre(s + 1, false);
                 last_tile = s + 1;
             }
-            if (s + 1 < T && sender && !failed) bulk_wait_read_all_but_one();   // step s - 1's staging
+            if (s + 1 < Tg && sender && !failed) bulk_wait_read_all_but_one();   // step s - 1's staging
         } else {
             cluster_wait();        // every peer's product of this step is done with its operand
             // h_t into every peer's operand of the next step (row j, columns u0 + q8*4 ..)
-            if (s + 1 < T) {
+            if (s + 1 < Tg) {
 #pragma unroll
                 for (int it = 0; it < 4; ++it) {
                     const int j = jq + it * 32;
                     if (j >= n) continue;
                     const uint32_t o = sw_off4(j, u0 + q8 * 4, NBM);
-                    for (int p2 = 0; p2 < G; ++p2) {
-                        *reinterpret_cast<uint2*>(cl.map_shared_rank(Bop(0, 0) + o, p2)) = xh[it];
-                        if (SPLIT) *reinterpret_cast<uint2*>(cl.map_shared_rank(Bop(0, 1) + o, p2)) = xl[it];
-                    }
+                    for (int p2 = 0; p2 < G; ++p2)
+#pragma unroll
+                        for (int k = 0; k < NP; ++k)
+                            *reinterpret_cast<uint2*>(cl.map_shared_rank(Bop(0, k) + o, p2)) = xp[it][k];
                 }
             }
             fence_proxy_async_cluster();
@@ -759,10 +797,10 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
         if (!BULK) {
 #pragma unroll
             for (int it = 0; it < 2; ++it)
-                if (jq + it * 32 < n) store_outputs(jq + it * 32, og_[it], oc_[it], oh_[it], xh[it]);
+                if (jq + it * 32 < n) store_outputs(jq + it * 32, og_[it], oc_[it], oh_[it], xp[it][0]);
         }
         pre_ok_prev = pre_ok;
-        cstamp(a, false, dir, rank, s, 3, 3);
+        cstamp(a, false, dir, srank, s, 3, 3);
     }
     // after a timeout the last tile issued may not have been waited for: no load may still be
     // writing this CTA's shared memory when it exits (bounded wait)
@@ -771,7 +809,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
     if (BULK) {
         if (lane == 0 && warp < G) bulk_wait_all();   // no copy of this CTA is still in flight
         cl.sync();                              // nor one into it: every CTA has passed its last wait
-    } else {
+    } else if (Tg > 0) {
         cluster_wait();            // the last step's arrival
     }
     tc::tc_fence_before_sync();
@@ -794,14 +832,14 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
 // P_c that belongs to CTA c' (its 32 units) into c''s inbox.  At the next step
 // each CTA adds the G partials of its units in CTA order.  db and dpeep are
 // summed afterwards by lstm_param_sums_kernel.
-// Shared memory (RecArgs offsets): off_contrib = B (gate errors, hi then
-// lo), off_acc = inbox, off_state = dc carry, off_sums = mbarriers, TMEM
-// slot, failure flag, off_peep = peepholes, off_tab = tables; BULK also
-// off_h = staging of the outgoing partials [G][NBM][32]; with a.tma_pre
-// off_red = operand tiles [7][NBM][32] (gates i f z o, c_t, c_{t-1}, dy).
-// Tensor memory: accumulators (tile m, chain ch) at columns
-// (m * chains + ch) * NBM; R^T tile m from column tm_acol + 64m (hi) and
-// tm_acol + 64 MT + 64m (lo).
+// Shared memory (RecArgs offsets): off_contrib = B (gate errors, NP pieces),
+// off_acc = inbox, off_state = dc carry, off_sums = mbarriers, TMEM slot,
+// failure flag, the group's step count, off_peep = peepholes, off_tab =
+// tables; BULK also off_h = staging of the outgoing partials [G][NBM][32];
+// with a.tma_pre off_red = operand tiles [7][NBM][32] (gates i f z o, c_t,
+// c_{t-1}, dy).  Tensor memory: accumulators (tile m, chain ch) at columns
+// (m * chains + ch) * NBM; piece k of R^T tile m from column
+// tm_acol + 64 MT k + 64 m.  Sequence groups as in the forward kernel.
 //
 // Exchanges of the partials:
 //  * BULK: the inbox is double-buffered per step parity ([2][G][NBM][32]);
@@ -816,7 +854,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
 // issued after the barrier that follows the cell (every thread has read them).
 //  * otherwise: one inbox written with plain DSMEM stores between the two
 //    halves of a split cluster barrier.
-template <bool SPLIT, bool BULK>
+template <int NP, bool BULK>
 __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
                                                                      const __grid_constant__ CUtensorMap map_ga,
                                                                      const __grid_constant__ CUtensorMap map_c,
@@ -827,27 +865,31 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
     cg::cluster_group cl = cg::this_cluster();
     const int G = a.G;
     const int rank = (int)cl.block_rank();
-    const int dir = blockIdx.x / G;
+    const int ng = a.ngroups;
+    const int dir = (int)(blockIdx.x / G) / ng, grp = (int)(blockIdx.x / G) % ng;
+    const int S = a.grp_rows, j0 = grp * S;           // this cluster's sorted slots [j0, j0 + S)
+    const int srank = grp == 0 ? rank : -1;           // the phase stamps come from group 0
     const int H = a.H, T = a.T, NBM = a.JC;
     const int MT = (H + kCM - 1) / kCM;              // 128-unit tiles of the partial product
     const int u0 = rank * kCU;
     const int ndH = a.ndir * H, nd4H = a.ndir * 4 * H;
     const int nch = a.tm_chains;                     // chains per tile; issuers = MT * nch
-    uint8_t* Bhi = base + a.off_contrib;             // [2 k-blocks][NBM][128 B]
-    uint8_t* Blo = Bhi + (size_t)2 * NBM * 128;
+    uint8_t* Bb = base + a.off_contrib;              // [NP][2 k-blocks][NBM][128 B]
+    const size_t bsz = (size_t)2 * NBM * 128;        // bytes of one B piece
     float* inbox = reinterpret_cast<float*>(base + a.off_acc);       // [BULK ? 2 : 1][G][NBM][32]
     float* stage = reinterpret_cast<float*>(base + a.off_h);         // BULK: [G][NBM][32]
     float* tiles = reinterpret_cast<float*>(base + a.off_red);       // BULK + tma_pre: [7][NBM][32]
-    float* dcc = reinterpret_cast<float*>(base + a.off_state);       // [B][32]
+    float* dcc = reinterpret_cast<float*>(base + a.off_state);       // [S][32]
     uint64_t* mma_bar = reinterpret_cast<uint64_t*>(base + a.off_sums);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_bar + 1);
     int* s_fail = reinterpret_cast<int*>(tmem_slot + 1);
     uint64_t* full_bar = mma_bar + 2;                                // BULK: [2] inbox arrival per parity
     uint64_t* opnd_bar = mma_bar + 4;                                // operand tiles' arrival
+    int* s_tg = reinterpret_cast<int*>(mma_bar + 6);                 // the group's step count
     float* peep_s = reinterpret_cast<float*>(base + a.off_peep);
-    int* s_bs = reinterpret_cast<int*>(base + a.off_tab);
-    int* s_off = s_bs + T;
-    int* s_len = s_off + T + 1;
+    int* s_bs = reinterpret_cast<int*>(base + a.off_tab);            // [T] the group's active rows
+    int* s_off = s_bs + T;                                           // [T+1] the group's first row
+    int* s_len = s_off + T + 1;                                      // [S] lengths of the group's slots
     const uint32_t tcols = (uint32_t)a.Umax;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool tma_opnd = a.tma_pre != 0;
@@ -855,10 +897,11 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
         return inbox + (((size_t)(BULK ? parity : 0) * G + src) * NBM + j) * kCU;
     };
     auto tile = [&](int k, int j) -> float* { return tiles + ((size_t)k * NBM + j) * kCU; };
+    int Tg = 0;
     // rows of the partials of step s2 - 1 that step s2 reads: its rows with a step after them
     // (in recurrence order); the cell reads no others
     auto step_rows = [&](int s2) -> int {
-        const int tp = dir == 0 ? T - s2 : s2 - 1, tn = dir == 0 ? T - 1 - s2 : s2;
+        const int tp = dir == 0 ? Tg - s2 : s2 - 1, tn = dir == 0 ? Tg - 1 - s2 : s2;
         return min(s_bs[tp], s_bs[tn]);
     };
     // bytes a CTA receives for step s2: those rows from every other CTA (its own it writes itself)
@@ -866,16 +909,23 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
         return (uint32_t)(G - 1) * (uint32_t)step_rows(s2) * (uint32_t)(kCU * 4);
     };
 
-    for (int i = threadIdx.x; i < (SPLIT ? 2 : 1) * 2 * NBM * 128 / 16; i += kCT)
-        reinterpret_cast<uint4*>(Bhi)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < NP * bsz / 16; i += kCT) reinterpret_cast<uint4*>(Bb)[i] = make_uint4(0, 0, 0, 0);
     for (int i = threadIdx.x; i < (BULK ? 2 : 1) * G * NBM * kCU; i += kCT) inbox[i] = 0.f;
-    for (int i = threadIdx.x; i < T; i += kCT) s_bs[i] = a.bs[i];
-    for (int i = threadIdx.x; i <= T; i += kCT) s_off[i] = a.off[i];
-    for (int i = threadIdx.x; i < a.B; i += kCT) s_len[i] = a.slot_len[i];
+    if (threadIdx.x == 0) *s_tg = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < T; i += kCT) {
+        const int n = min(max(a.bs[i] - j0, 0), S);
+        s_bs[i] = n;
+        if (n > 0 && (i + 1 == T || a.bs[i + 1] <= j0)) *s_tg = i + 1;
+    }
+    for (int i = threadIdx.x; i <= T; i += kCT) s_off[i] = a.off[i] + j0;
+    for (int i = threadIdx.x; i < S; i += kCT) s_len[i] = j0 + i < a.B ? a.slot_len[j0 + i] : 0;
     for (int i = threadIdx.x; i < 3 * kCU; i += kCT) {
         const int q = i / kCU, uu = i - q * kCU;
         peep_s[i] = a.peep[(size_t)dir * 3 * H + q * H + u0 + uu];
     }
+    __syncthreads();
+    Tg = *s_tg;
     if (threadIdx.x == 0) {
         tc::mbar_init(mma_bar, (uint32_t)(MT * nch));
         *s_fail = 0;
@@ -886,7 +936,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
         if (tma_opnd) tc::mbar_init(opnd_bar, 1);
         tc::fence_mbar_init();
         // the inbox of step 1 (parity 1) is armed before the cluster barrier below
-        if (BULK && T > 1) tc::mbar_arrive_expect_tx(&full_bar[1], step_bytes(1));
+        if (BULK && Tg > 1) tc::mbar_arrive_expect_tx(&full_bar[1], step_bytes(1));
     }
     if (threadIdx.x < 32) {
         tc::tmem_alloc(tmem_slot, tcols);
@@ -897,7 +947,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
     __syncthreads();
     tc::tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t a_hi = tmem + (uint32_t)a.tm_acol, a_lo = a_hi + (uint32_t)(64 * MT);
+    const uint32_t a0 = tmem + (uint32_t)a.tm_acol, ap = (uint32_t)(64 * MT);
     // R^T slice -> tensor memory: tile m, lane l = unit 128m + l (zero past H); column 64m + c
     // holds this CTA's gate rows r = 2c, 2c + 1 (r = 32g + uu); warps q and q + 4 share the
     // lanes 32q.. and take alternate gates
@@ -911,14 +961,15 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
 #pragma unroll
                 for (int uu = 0; uu < 32; ++uu) {
                     const size_t src = (size_t)dir * 4 * H * H + (size_t)(g * H + u0 + uu) * H + up;
-                    v[uu] = up < H ? (SPLIT ? __ldg(reinterpret_cast<const float*>(a.R) + src)
-                                            : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.R)[src]))
+                    v[uu] = up < H ? (NP > 1 ? __ldg(reinterpret_cast<const float*>(a.R) + src)
+                                             : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.R)[src]))
                                    : 0.f;
                 }
-                uint32_t hi[16], lo[16];
-                split32<SPLIT>(v, hi, lo);
-                tc::tmem_st_32x32b_x16(a_hi + lanes + (uint32_t)(64 * m + 16 * g), hi);
-                if (SPLIT) tc::tmem_st_32x32b_x16(a_lo + lanes + (uint32_t)(64 * m + 16 * g), lo);
+                uint32_t pc[NP][16];
+                split32<NP>(v, pc);
+#pragma unroll
+                for (int k = 0; k < NP; ++k)
+                    tc::tmem_st_32x32b_x16(a0 + (uint32_t)k * ap + lanes + (uint32_t)(64 * m + 16 * g), pc[k]);
             }
         }
         tc::tmem_wait_st();
@@ -929,9 +980,9 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
     // tma_opnd: the seven operand tiles of step s2 (NBM rows each; rows past the packed rows read
     // 0), one thread, completing on opnd_bar
     auto issue_opnd = [&](int s2) {
-        const int t2 = dir == 0 ? T - 1 - s2 : s2;
+        const int t2 = dir == 0 ? Tg - 1 - s2 : s2;
         const int y0 = s_off[t2];
-        const int yp = dir == 0 ? (t2 >= 1 ? s_off[t2 - 1] : 0) : (t2 + 1 < T ? s_off[t2 + 1] : 0);
+        const int yp = dir == 0 ? (t2 >= 1 ? s_off[t2 - 1] : 0) : (t2 + 1 < Tg ? s_off[t2 + 1] : 0);
         tc::mbar_arrive_expect_tx(opnd_bar, (uint32_t)(7 * NBM * kCU * 4));
 #pragma unroll
         for (int g = 0; g < 4; ++g) tc::tma_load_2d(tile(g, 0), &map_ga, opnd_bar, dir * 4 * H + g * H + u0, y0);
@@ -940,7 +991,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
         tc::tma_load_2d(tile(6, 0), &map_dy, opnd_bar, dir * H + u0, y0);
     };
     int last_tile = -1;                   // tile issuer: the last step whose tiles were issued
-    if (tma_opnd && threadIdx.x == kTileIssuer) { issue_opnd(0); last_tile = 0; }
+    if (tma_opnd && threadIdx.x == kTileIssuer && Tg > 0) { issue_opnd(0); last_tile = 0; }
     cl.sync();
 
     const int jq = threadIdx.x >> 3, q8 = threadIdx.x & 7;          // cell item: row jq (+32k), units q8*4..+4
@@ -950,11 +1001,17 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
     for (int q = 0; q < 3; ++q)
 #pragma unroll
         for (int e = 0; e < 4; ++e) pk[q][e] = peep_s[q * kCU + q8 * 4 + e];
+    // c0 of slot j's units u0 + q8*4 .. +4 (the state before its first step; zero without one)
+    auto init_c = [&](int j) -> float4 {
+        return a.c0 ? __ldg(reinterpret_cast<const float4*>(a.c0 + ((size_t)dir * a.B + a.perm[j0 + j]) * H + u0 +
+                                                            q8 * 4))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
     // own operands (gates, c_t, c_{t-1}, dy) of row jq of a step, loaded one step ahead
     // (without operand tiles)
     float nx[7][4];
     auto load_own = [&](int s2) {
-        const int t2 = dir == 0 ? T - 1 - s2 : s2;
+        const int t2 = dir == 0 ? Tg - 1 - s2 : s2;
         const int n2 = s_bs[t2];
         if (jq >= n2) return;
         const int row = s_off[t2] + jq;
@@ -969,28 +1026,29 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
         const float4 d0 = __ldg(reinterpret_cast<const float4*>(a.dy + yo));
         nx[4][0] = c0.x; nx[4][1] = c0.y; nx[4][2] = c0.z; nx[4][3] = c0.w;
         nx[6][0] = d0.x; nx[6][1] = d0.y; nx[6][2] = d0.z; nx[6][3] = d0.w;
-        const int np2 = dir == 0 ? (t2 >= 1 ? n2 : 0) : (t2 + 1 < T ? s_bs[t2 + 1] : 0);
+        const int np2 = dir == 0 ? (t2 >= 1 ? n2 : 0) : (t2 + 1 < Tg ? s_bs[t2 + 1] : 0);
         if (jq < np2) {
             const int pb2 = dir == 0 ? s_off[t2 - 1] : s_off[t2 + 1];
             const float4 p0 = __ldg(reinterpret_cast<const float4*>(a.cbuf + (size_t)(pb2 + jq) * ndH + dir * H + u0 + q8 * 4));
             nx[5][0] = p0.x; nx[5][1] = p0.y; nx[5][2] = p0.z; nx[5][3] = p0.w;
         } else {
-            nx[5][0] = nx[5][1] = nx[5][2] = nx[5][3] = 0.f;
+            const float4 p0 = init_c(jq);
+            nx[5][0] = p0.x; nx[5][1] = p0.y; nx[5][2] = p0.z; nx[5][3] = p0.w;
         }
     };
-    if (!tma_opnd) load_own(0);
+    if (!tma_opnd && Tg > 0) load_own(0);
     bool failed = false;                  // CTA-uniform: a bounded wait ran out
     bool step_ok = true;                  // this thread's wait of the last product
-    for (int s = 0; s < T; ++s) {
-        const int t = dir == 0 ? T - 1 - s : s;
+    for (int s = 0; s < Tg; ++s) {
+        const int t = dir == 0 ? Tg - 1 - s : s;
         const int n = s_bs[t];
         const int rowbase = s_off[t];
-        const int n_next = dir == 0 ? (t + 1 < T ? s_bs[t + 1] : 0) : (t >= 1 ? n : 0);
-        const int prev_base = dir == 0 ? (t >= 1 ? s_off[t - 1] : 0) : (t + 1 < T ? s_off[t + 1] : 0);
-        const int n_prev = dir == 0 ? (t >= 1 ? n : 0) : (t + 1 < T ? s_bs[t + 1] : 0);
+        const int n_next = dir == 0 ? (t + 1 < Tg ? s_bs[t + 1] : 0) : (t >= 1 ? n : 0);
+        const int prev_base = dir == 0 ? (t >= 1 ? s_off[t - 1] : 0) : (t + 1 < Tg ? s_off[t + 1] : 0);
+        const int n_prev = dir == 0 ? (t >= 1 ? n : 0) : (t + 1 < Tg ? s_bs[t + 1] : 0);
         const int NBs = (n + 15) & ~15;
         const int par = BULK ? (s & 1) : 0;
-        cstamp(a, true, dir, rank, s, 0, 0);
+        cstamp(a, true, dir, srank, s, 0, 0);
         bool arrived = true;              // this step's inbox and operand tiles arrived
         if (BULK && s > 0 && !failed)
             arrived = tc::mbar_wait(&full_bar[par], (uint32_t)(((s - 1) >> 1) & 1), a.wait_limit_ns);
@@ -999,7 +1057,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
             record_failure(a.status, LSTM_ERR_TIMEOUT, 0x60000u | (unsigned)s);
             *s_fail = 1 + s;
         }
-        cstamp(a, true, dir, rank, s, 1, 1);
+        cstamp(a, true, dir, srank, s, 1, 1);
         for (int it = 0; it * 32 < n; ++it) {
             const int j = jq + it * 32;
             if (j >= n) continue;
@@ -1018,8 +1076,8 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
                 const float4 d0 = *reinterpret_cast<const float4*>(tile(6, j) + uub);
                 cv[0] = c0.x; cv[1] = c0.y; cv[2] = c0.z; cv[3] = c0.w;
                 dyv[0] = d0.x; dyv[1] = d0.y; dyv[2] = d0.z; dyv[3] = d0.w;
-                const bool hp = j < n_prev;
-                cpv[0] = hp ? p0.x : 0.f; cpv[1] = hp ? p0.y : 0.f; cpv[2] = hp ? p0.z : 0.f; cpv[3] = hp ? p0.w : 0.f;
+                const float4 pc = j < n_prev ? p0 : init_c(j);
+                cpv[0] = pc.x; cpv[1] = pc.y; cpv[2] = pc.z; cpv[3] = pc.w;
             } else if (it == 0) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -1037,18 +1095,16 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
                 cv[0] = c0.x; cv[1] = c0.y; cv[2] = c0.z; cv[3] = c0.w;
                 const float4 d0 = __ldg(reinterpret_cast<const float4*>(a.dy + yo));
                 dyv[0] = d0.x; dyv[1] = d0.y; dyv[2] = d0.z; dyv[3] = d0.w;
-                if (j < n_prev) {
-                    const float4 p0 = __ldg(reinterpret_cast<const float4*>(
-                        a.cbuf + (size_t)(prev_base + j) * ndH + dir * H + u0 + uub));
-                    cpv[0] = p0.x; cpv[1] = p0.y; cpv[2] = p0.z; cpv[3] = p0.w;
-                } else {
-                    cpv[0] = cpv[1] = cpv[2] = cpv[3] = 0.f;
-                }
+                const float4 p0 = j < n_prev ? __ldg(reinterpret_cast<const float4*>(
+                                                   a.cbuf + (size_t)(prev_base + j) * ndH + dir * H + u0 + uub))
+                                             : init_c(j);
+                cpv[0] = p0.x; cpv[1] = p0.y; cpv[2] = p0.z; cpv[3] = p0.w;
             }
             const bool has_next = j < n_next;
             const bool real = !a.padded || t < s_len[j];
             // the G partial sums of R^T da of the step after, added in CTA order, and the carry
             float dhr[4] = {0.f, 0.f, 0.f, 0.f}, car[4] = {0.f, 0.f, 0.f, 0.f};
+            const size_t so = ((size_t)dir * a.B + a.perm[j0 + j]) * H + u0 + uub;   // caller-order state
             if (has_next) {
                 for (int c2 = 0; c2 < G; ++c2) {
                     const float4 x = *reinterpret_cast<const float4*>(inbox_at(par, c2, j) + uub);
@@ -1056,6 +1112,16 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
                 }
                 const float4 x = *reinterpret_cast<const float4*>(dcc + j * kCU + uub);
                 car[0] = x.x; car[1] = x.y; car[2] = x.z; car[3] = x.w;
+            } else {
+                // the sequence's last step: the final state's own errors from outside
+                if (a.dh_n) {
+                    const float4 x = __ldg(reinterpret_cast<const float4*>(a.dh_n + so));
+                    dhr[0] = x.x; dhr[1] = x.y; dhr[2] = x.z; dhr[3] = x.w;
+                }
+                if (a.dc_n) {
+                    const float4 x = __ldg(reinterpret_cast<const float4*>(a.dc_n + so));
+                    car[0] = x.x; car[1] = x.y; car[2] = x.z; car[3] = x.w;
+                }
             }
             float da[4][4], cout[4];
 #pragma unroll
@@ -1077,17 +1143,19 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
                 cout[e] = carry_out;
             }
             *reinterpret_cast<float4*>(dcc + j * kCU + uub) = make_float4(cout[0], cout[1], cout[2], cout[3]);
+            if (j >= n_prev && a.dc0)                    // the sequence's first step: dL/dc0
+                *reinterpret_cast<float4*>(a.dc0 + so) = make_float4(cout[0], cout[1], cout[2], cout[3]);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 *reinterpret_cast<float4*>(gr + g * H) = make_float4(da[g][0], da[g][1], da[g][2], da[g][3]);
-                uint2 hi, lo;
-                split4(da[g], hi, lo, SPLIT);
+                uint2 pc[NP];
+                split4<NP>(da[g], pc);
                 const uint32_t o = sw_off4(j, g * kCU + uub, NBM);
-                *reinterpret_cast<uint2*>(Bhi + o) = hi;
-                if (SPLIT) *reinterpret_cast<uint2*>(Blo + o) = lo;
+#pragma unroll
+                for (int k = 0; k < NP; ++k) *reinterpret_cast<uint2*>(Bb + (size_t)k * bsz + o) = pc[k];
             }
         }
-        if (BULK) cstamp(a, true, dir, rank, s, 4, 4);   // (BULK: stamp 4 = cell done)
+        if (BULK) cstamp(a, true, dir, srank, s, 4, 4);   // (BULK: stamp 4 = cell done)
         if (!BULK) cluster_arrive_relaxed();   // this CTA has read its inbox: peers may overwrite it
         // the previous step's staging must have been read by its copies before this step's read-out
         if (BULK && lane == 0 && warp < G) bulk_wait_read_all();
@@ -1098,41 +1166,40 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
         // status word marks the results as invalid)
         if (__syncthreads_or(!step_ok || !arrived)) failed = true;
         // the operand tiles and this parity's inbox have been read
-        if (tma_opnd && threadIdx.x == kTileIssuer && s + 1 < T && !failed) {
+        if (tma_opnd && threadIdx.x == kTileIssuer && s + 1 < Tg && !failed) {
             issue_opnd(s + 1);
             last_tile = s + 1;
         }
         // BULK: re-arm this parity for step s + 2 before this CTA's partials of step s go out
-        if (BULK && threadIdx.x == 0 && !failed && s + 2 < T)
+        if (BULK && threadIdx.x == 0 && !failed && s + 2 < Tg)
             tc::mbar_arrive_expect_tx(&full_bar[par], step_bytes(s + 2));
-        cstamp(a, true, dir, rank, s, 2, 2);
-        if (s + 1 < T) {
+        cstamp(a, true, dir, srank, s, 2, 2);
+        if (s + 1 < Tg) {
             // P[u'][j] = sum over this CTA's gate rows r of R[r][u'] da[j][r]: warp w issues tile
             // m = w / chains, chain ch = w % chains (k-steps ch, ch + chains, ... of the 8)
             if (lane == 0 && warp < MT * nch && !failed) {
                 tc::tc_fence_after_sync();
                 const int m = warp / nch, ch = warp - m * nch;
                 const uint32_t idesc = tc::idesc_bf16_f32(kCM, NBs);
-                const uint64_t dbh = tc::sdesc_sw128(tc::smem_u32(Bhi)), dbl = tc::sdesc_sw128(tc::smem_u32(Blo));
-                const uint32_t dm = tmem + (uint32_t)(warp * NBM), ahm = a_hi + (uint32_t)(64 * m),
-                               alm = a_lo + (uint32_t)(64 * m);
-                if (nch == 4) issue_chain_fixed<4, 8, 4, SPLIT>(dm, ahm, alm, dbh, dbl, bstep, ch, idesc);
-                else if (nch == 2) issue_chain_fixed<2, 8, 4, SPLIT>(dm, ahm, alm, dbh, dbl, bstep, ch, idesc);
-                else issue_chain_fixed<1, 8, 4, SPLIT>(dm, ahm, alm, dbh, dbl, bstep, ch, idesc);
-                if (!(s == 0 && dir == 0 && rank == a.debug_skip_cta)) tc::mma_commit(mma_bar);   // test hook
+                const uint64_t db0 = tc::sdesc_sw128(tc::smem_u32(Bb)), bp = (uint64_t)(bsz >> 4);
+                const uint32_t dm = tmem + (uint32_t)(warp * NBM), am = a0 + (uint32_t)(64 * m);
+                if (nch == 4) issue_chain_fixed<4, 8, 4, NP>(dm, am, ap, db0, bp, bstep, ch, idesc);
+                else if (nch == 2) issue_chain_fixed<2, 8, 4, NP>(dm, am, ap, db0, bp, bstep, ch, idesc);
+                else issue_chain_fixed<1, 8, 4, NP>(dm, am, ap, db0, bp, bstep, ch, idesc);
+                if (!(s == 0 && dir == 0 && grp == 0 && rank == a.debug_skip_cta)) tc::mma_commit(mma_bar);   // test hook
             }
             if (warp < MT * nch) __syncwarp();
-            cstamp(a, true, dir, rank, s, 6, 6);
+            cstamp(a, true, dir, srank, s, 6, 6);
             step_ok = failed ? true : tc::mbar_wait(mma_bar, (uint32_t)(s & 1), a.wait_limit_ns);
             if (!step_ok) {
                 record_failure(a.status, LSTM_ERR_TIMEOUT, 0x50000u | (unsigned)s);
                 *s_fail = 1 + s;
             }
             tc::tc_fence_after_sync();
-            cstamp(a, true, dir, rank, s, 5, 7);
+            cstamp(a, true, dir, srank, s, 5, 7);
         }
         if (BULK) {
-            if (s + 1 < T && !failed) {
+            if (s + 1 < Tg && !failed) {
                 // read-out into the staging, per owner: tile m, lane quarter q -> owner 4m + q,
                 // units 32q + lane of the tile, rows [0, NBs)
                 for (int pq = warp; pq < MT * 4; pq += kCT / 32) {
@@ -1154,7 +1221,7 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
             fence_proxy_async_cta();
             __syncthreads();
             // lane 0 of warp w sends to owners w, w + 8 (copies issued by one warp's lanes serialise)
-            if (s + 1 < T && !failed && lane == 0 && warp < G) {
+            if (s + 1 < Tg && !failed && lane == 0 && warp < G) {
                 const uint32_t nxt = (uint32_t)(par ^ 1);
                 const uint32_t bytes = (uint32_t)step_rows(s + 1) * (uint32_t)(kCU * 4);
                 for (int o = warp; o < G; o += kCT / 32) {
@@ -1165,11 +1232,11 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
                 }
                 bulk_commit();
             }
-            if (!tma_opnd && s + 1 < T) load_own(s + 1);   // the next step's own operands
-            cstamp(a, true, dir, rank, s, 3, 3);
+            if (!tma_opnd && s + 1 < Tg) load_own(s + 1);   // the next step's own operands
+            cstamp(a, true, dir, srank, s, 3, 3);
         } else {
             cluster_wait();        // every peer has read its inbox of this step
-            if (s + 1 < T && !failed) {
+            if (s + 1 < Tg && !failed) {
                 // tile m, lane quarter q: units u' = 128m + 32q + lane, owned by CTA 4m + q
                 for (int pq = warp; pq < MT * 4; pq += kCT / 32) {
                     const int m = pq >> 2, q = pq & 3;
@@ -1188,12 +1255,12 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
                 }
                 tc::tc_fence_before_sync();
             }
-            cstamp(a, true, dir, rank, s, 3, 3);
+            cstamp(a, true, dir, srank, s, 3, 3);
             fence_proxy_async_cluster();
             cluster_arrive();      // release: this CTA's partial sums are in their owners' inboxes
-            if (!tma_opnd && s + 1 < T) load_own(s + 1);   // the next step's own operands, in flight across the barrier
+            if (!tma_opnd && s + 1 < Tg) load_own(s + 1);   // the next step's own operands, in flight across the barrier
             cluster_wait();
-            cstamp(a, true, dir, rank, s, 4, 4);
+            cstamp(a, true, dir, srank, s, 4, 4);
         }
     }
     // after a timeout the last tiles issued may not have been waited for (bounded wait)
@@ -1323,11 +1390,30 @@ static int max_active_rows(const Plan& p)
     return bmax;
 }
 
+// Sequence groups: the sorted slots are cut into ng contiguous groups of S slots, one cluster
+// per (direction, group).  S is the smallest multiple of 8 (at least 8) for which every
+// cluster has an SM of its own, or the plan's forced size; one group when S covers the batch.
+// False when a group would need more than 128 rows (the cell's row items).
+static bool choose_groups(const Plan& p, int G, int ndir, int* S_out, int* ng_out)
+{
+    int S;
+    if (p.forced_group_rows > 0) {
+        S = p.forced_group_rows;
+    } else {
+        const int maxg = std::max(1, p.num_sms / (G * ndir));
+        S = std::max(8, (ceil_div(p.B, maxg) + 7) / 8 * 8);
+    }
+    if (S >= p.B) S = p.B;
+    if (S > 128) return false;
+    *S_out = S;
+    *ng_out = ceil_div(p.B, S);
+    return true;
+}
+
 static const void* fwd_kernel(bool bf16, bool bulk)
 {
-    if (bulk) return bf16 ? (const void*)lstm_rec_fwd_cluster_kernel<false, true>
-                          : (const void*)lstm_rec_fwd_cluster_kernel<true, true>;
-    return bf16 ? (const void*)lstm_rec_fwd_cluster_kernel<false, false> : (const void*)lstm_rec_fwd_cluster_kernel<true, false>;
+    if (bulk) return bf16 ? (const void*)lstm_rec_fwd_cluster_kernel<1, true> : (const void*)lstm_rec_fwd_cluster_kernel<3, true>;
+    return bf16 ? (const void*)lstm_rec_fwd_cluster_kernel<1, false> : (const void*)lstm_rec_fwd_cluster_kernel<3, false>;
 }
 
 bool rec_cluster_fwd_configure(const Plan& p, int H, int ndir, bool bf16, RecConfig* out, RecArgs* lay)
@@ -1336,12 +1422,13 @@ bool rec_cluster_fwd_configure(const Plan& p, int H, int ndir, bool bf16, RecCon
     if (H % kCU != 0) return false;
     const int G = H / kCU;
     if (G > 16 || G * ndir > p.num_sms) return false;
-    const int NBM = std::max(16, (max_active_rows(p) + 15) & ~15);
-    if (NBM > 128) return false;                   // cell items: 4 rows of 32 per thread
-    const bool split = !bf16;
+    int S = 0, ng = 1;
+    if (!choose_groups(p, G, ndir, &S, &ng)) return false;
+    const int NBM = std::max(16, (std::min(S, max_active_rows(p)) + 15) & ~15);
+    const int np = bf16 ? 1 : 3;                   // bf16 pieces of each operand
     const int KB = (H + 63) / 64;
     const int nks = (H + 15) / 16;
-    const int acols = (H / 2) * (split ? 2 : 1);   // R slice in TMEM, two bf16 per column
+    const int acols = (H / 2) * np;                // R slice in TMEM, two bf16 per column and piece
     int nch = 4;
     while (nch > 1 && (nch > nks || nch * NBM + acols > 512)) nch >>= 1;
     if (nch * NBM + acols > 512) return false;
@@ -1352,16 +1439,16 @@ bool rec_cluster_fwd_configure(const Plan& p, int H, int ndir, bool bf16, RecCon
     for (int oi = 0; oi < 4; ++oi) {
         const int bulk = order[oi][0], pre = order[oi][1];
         if (p.forced_variant >= 0 && p.forced_variant != (bulk | pre << 1)) continue;
-        const size_t bbytes = bulk ? 2 * (split ? 2 : 1) * (size_t)G * NBM * 64 : (split ? 2 : 1) * (size_t)KB * NBM * 128;
+        const size_t bbytes = bulk ? 2 * (size_t)np * G * NBM * 64 : (size_t)np * KB * NBM * 128;
         size_t off = 0;
         const size_t o_b = off; off = al(off + bbytes, 1024);
-        const size_t o_stage = off; if (bulk) off = al(off + 4 * (size_t)NBM * 64, 1024);
+        const size_t o_stage = off; if (bulk) off = al(off + 2 * (size_t)np * NBM * 64, 1024);
         const size_t o_pre = off; if (pre) off = al(off + 4 * (size_t)NBM * kCU * 4, 1024);
         const size_t o_acc = off; off = al(off + (size_t)NBM * kCM * 4, 16);
-        const size_t o_cst = off; off = al(off + (size_t)p.B * kCU * 4, 16);
+        const size_t o_cst = off; off = al(off + (size_t)S * kCU * 4, 16);
         const size_t o_bar = off; off = al(off + 64, 16);
         const size_t o_peep = off; off = al(off + 3 * kCU * 4, 16);
-        const size_t o_tab = off; off = al(off + (size_t)(2 * p.T + 1 + p.B) * 4, 16);
+        const size_t o_tab = off; off = al(off + (size_t)(2 * p.T + 1 + S) * 4, 16);
         size_t smem = off + 1024 + 64;            // 1024 for the base alignment, 64 static
         smem = tmem_safe_smem(p, smem, cols);
         if (smem == 0) return false;
@@ -1369,6 +1456,7 @@ bool rec_cluster_fwd_configure(const Plan& p, int H, int ndir, bool bf16, RecCon
         RecConfig c;
         c.G = G; c.Umax = (int)cols; c.JC = NBM; c.smem = smem; c.cluster = 1;
         c.chains = nch; c.acol = (int)cols - acols; c.bulk = bulk; c.tma_pre = pre;
+        c.grp_rows = S; c.ngroups = ng;
         *out = c;
         lay->off_contrib = (int)o_b; lay->off_h = (int)o_stage; lay->off_red = (int)o_pre; lay->off_acc = (int)o_acc;
         lay->off_state = (int)o_cst; lay->off_sums = (int)o_bar; lay->off_peep = (int)o_peep;
@@ -1378,6 +1466,7 @@ bool rec_cluster_fwd_configure(const Plan& p, int H, int ndir, bool bf16, RecCon
     return false;
 }
 
+// One cluster of c.G CTAs per (direction, sequence group).
 static lstm_status cluster_launch(const RecConfig& c, const void* fn, void** args, int ndir, cudaStream_t s)
 {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem) != cudaSuccess)
@@ -1386,7 +1475,7 @@ static lstm_status cluster_launch(const RecConfig& c, const void* fn, void** arg
         return LSTM_ERR_UNSUPPORTED;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    cfg.gridDim = dim3(c.G * ndir);
+    cfg.gridDim = dim3(c.G * ndir * c.ngroups);
     cfg.blockDim = dim3(kCT);
     cfg.dynamicSmemBytes = c.smem;
     cfg.stream = s;
@@ -1404,6 +1493,7 @@ static lstm_status cluster_launch(const RecConfig& c, const void* fn, void** arg
 lstm_status rec_cluster_fwd_launch(const Plan& p, const RecConfig& c, RecArgs a, cudaStream_t s)
 {
     a.G = c.G; a.Umax = c.Umax; a.JC = c.JC; a.tm_chains = c.chains; a.tm_acol = c.acol;
+    a.grp_rows = c.grp_rows; a.ngroups = c.ngroups;
     a.trace = p.d_trace; a.trace_steps = p.trace_steps;
     const void* fn = fwd_kernel(a.bf16 != 0, c.bulk != 0);
     // the pre-activation tiles' map: ga as [rows][ndir*4H] fp32, boxes of 32 units x NBM rows
@@ -1420,9 +1510,8 @@ lstm_status rec_cluster_fwd_launch(const Plan& p, const RecConfig& c, RecArgs a,
 
 static const void* bwd_kernel(bool bf16, bool bulk)
 {
-    if (bulk) return bf16 ? (const void*)lstm_rec_bwd_cluster_kernel<false, true>
-                          : (const void*)lstm_rec_bwd_cluster_kernel<true, true>;
-    return bf16 ? (const void*)lstm_rec_bwd_cluster_kernel<false, false> : (const void*)lstm_rec_bwd_cluster_kernel<true, false>;
+    if (bulk) return bf16 ? (const void*)lstm_rec_bwd_cluster_kernel<1, true> : (const void*)lstm_rec_bwd_cluster_kernel<3, true>;
+    return bf16 ? (const void*)lstm_rec_bwd_cluster_kernel<1, false> : (const void*)lstm_rec_bwd_cluster_kernel<3, false>;
 }
 
 bool rec_cluster_bwd_configure(const Plan& p, int H, int ndir, bool bf16, RecConfig* out, RecArgs* lay)
@@ -1431,11 +1520,12 @@ bool rec_cluster_bwd_configure(const Plan& p, int H, int ndir, bool bf16, RecCon
     if (H % kCU != 0) return false;
     const int G = H / kCU;
     if (G > 16 || G * ndir > p.num_sms) return false;
-    const int NBM = std::max(16, (max_active_rows(p) + 15) & ~15);
-    if (NBM > 128) return false;
+    int S = 0, ng = 1;
+    if (!choose_groups(p, G, ndir, &S, &ng)) return false;
+    const int NBM = std::max(16, (std::min(S, max_active_rows(p)) + 15) & ~15);
     const int MT = (H + kCM - 1) / kCM;
-    const bool split = !bf16;
-    const int acols = MT * 64 * (split ? 2 : 1);   // R^T tiles in TMEM: 128 gate rows = 64 columns
+    const int np = bf16 ? 1 : 3;                   // bf16 pieces of each operand
+    const int acols = MT * 64 * np;                // R^T tiles in TMEM: 128 gate rows = 64 columns per piece
     int nch = 4;
     while (nch > 1 && (MT * nch > 4 || MT * nch * NBM + acols > 512)) nch >>= 1;
     if (MT * nch * NBM + acols > 512 || MT * nch > kCT / 32) return false;
@@ -1448,14 +1538,14 @@ bool rec_cluster_bwd_configure(const Plan& p, int H, int ndir, bool bf16, RecCon
         if (oi == 3 && p.forced_variant < 0) break;   // the bulk exchange without tiles only on request
         if (p.forced_variant >= 0 && p.forced_variant != (bulk | tiles << 1)) continue;
         size_t off = 0;
-        const size_t o_b = off; off = al(off + (split ? 2 : 1) * (size_t)2 * NBM * 128, 1024);
+        const size_t o_b = off; off = al(off + (size_t)np * 2 * NBM * 128, 1024);
         const size_t o_in = off; off = al(off + (bulk ? 2 : 1) * (size_t)G * NBM * kCU * 4, 1024);
         const size_t o_stage = off; if (bulk) off = al(off + (size_t)G * NBM * kCU * 4, 1024);
         const size_t o_tiles = off; if (tiles) off = al(off + 7 * (size_t)NBM * kCU * 4, 1024);
-        const size_t o_dcc = off; off = al(off + (size_t)p.B * kCU * 4, 16);
+        const size_t o_dcc = off; off = al(off + (size_t)S * kCU * 4, 16);
         const size_t o_bar = off; off = al(off + 64, 16);
         const size_t o_peep = off; off = al(off + 3 * kCU * 4, 16);
-        const size_t o_tab = off; off = al(off + (size_t)(2 * p.T + 1 + p.B) * 4, 16);
+        const size_t o_tab = off; off = al(off + (size_t)(2 * p.T + 1 + S) * 4, 16);
         size_t smem = off + 1024 + 64;
         smem = tmem_safe_smem(p, smem, cols);
         if (smem == 0) return false;
@@ -1463,6 +1553,7 @@ bool rec_cluster_bwd_configure(const Plan& p, int H, int ndir, bool bf16, RecCon
         RecConfig c;
         c.G = G; c.Umax = (int)cols; c.JC = NBM; c.smem = smem; c.cluster = 1;
         c.chains = nch; c.acol = (int)cols - acols; c.bulk = bulk; c.tma_pre = tiles;
+        c.grp_rows = S; c.ngroups = ng;
         *out = c;
         lay->off_contrib = (int)o_b; lay->off_acc = (int)o_in; lay->off_h = (int)o_stage; lay->off_red = (int)o_tiles;
         lay->off_state = (int)o_dcc; lay->off_sums = (int)o_bar; lay->off_peep = (int)o_peep; lay->off_tab = (int)o_tab;
@@ -1476,6 +1567,7 @@ size_t rec_cluster_bwd_sum_floats(int H, int ndir) { return (size_t)kSumChunks *
 lstm_status rec_cluster_bwd_launch(const Plan& p, const RecConfig& c, RecArgs a, float* sum_scratch, cudaStream_t s)
 {
     a.G = c.G; a.Umax = c.Umax; a.JC = c.JC; a.tm_chains = c.chains; a.tm_acol = c.acol;
+    a.grp_rows = c.grp_rows; a.ngroups = c.ngroups;
     a.trace = p.d_trace; a.trace_steps = p.trace_steps;
     const void* fn = bwd_kernel(a.bf16 != 0, c.bulk != 0);
     // operand tiles: ga as [rows][ndir*4H], c and dy as [rows][ndir*H] fp32, boxes of 32 x NBM

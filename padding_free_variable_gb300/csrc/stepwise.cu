@@ -29,10 +29,10 @@ __global__ void step_cell_fwd_kernel(StepArgs a, int s)
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;
     const int j = idx / H, u = idx - j * H;
     const int ndH = a.ndir * H, nd4H = a.ndir * 4 * H;
-    if (s == 0 && j < a.B && a.slot_len[j] == 0 && a.h_n) {      // empty sequences end in the zero state
+    if (s == 0 && j < a.B && a.slot_len[j] == 0 && a.h_n) {      // empty sequences end in their initial state
         const size_t o = ((size_t)dir * a.B + a.perm[j]) * H + u;
-        a.h_n[o] = 0.f;
-        if (a.c_n) a.c_n[o] = 0.f;
+        a.h_n[o] = a.h0 ? a.h0[o] : 0.f;
+        if (a.c_n) a.c_n[o] = a.c0 ? a.c0[o] : 0.f;
     }
     const int t = dir == 0 ? s : T - 1 - s;
     const int n = a.bs[t];
@@ -56,14 +56,17 @@ __global__ void step_cell_fwd_kernel(StepArgs a, int s)
     float av[4];
 #pragma unroll
     for (int g = 0; g < 4; ++g) av[g] = pre[g * H] + r[g];
-    const float cp = has_prev ? a.cbuf[(size_t)prow * ndH + dir * H + u] : 0.f;
+    const size_t so = ((size_t)dir * a.B + a.perm[j]) * H + u;     // caller-order state
+    const float cp = has_prev ? a.cbuf[(size_t)prow * ndH + dir * H + u] : (a.c0 ? a.c0[so] : 0.f);
     const float* pp = a.peep + (size_t)dir * 3 * H + u;
     const float ig = sigm(av[0] + pp[0] * cp);
     const float fg = sigm(av[1] + pp[H] * cp);
     const float zg = tanhf(av[2]);
-    const float c = fg * cp + ig * zg;
+    float c = fg * cp + ig * zg;
     const float og = sigm(av[3] + pp[2 * H] * c);
-    const float h = og * tanhf(c);
+    float h = og * tanhf(c);
+    const int len = a.slot_len[j];
+    if (a.padded && t >= len) { c = 0.f; h = 0.f; }     // a padding frame: computed, then masked
     float* gw = a.ga + (size_t)row * nd4H + (size_t)dir * 4 * H + u;
     gw[0] = ig; gw[H] = fg; gw[2 * H] = zg; gw[3 * H] = og;
     const size_t yo = (size_t)row * ndH + dir * H + u;
@@ -71,7 +74,6 @@ __global__ void step_cell_fwd_kernel(StepArgs a, int s)
     a.y[yo] = h;
     if (a.y_lo) a.y_lo[yo] = __float2bfloat16_rn(h);
     if (a.hb16) a.hb16[((size_t)dir * a.B + j) * H + u] = __float2bfloat16_rn(h);
-    const int len = a.slot_len[j];
     if (a.h_n && ((dir == 0 && t == len - 1) || (dir == 1 && t == 0))) {
         const size_t o = ((size_t)dir * a.B + a.perm[j]) * H + u;
         a.h_n[o] = h;
@@ -100,24 +102,32 @@ __global__ void step_cell_bwd_kernel(StepArgs a, int s)
     const float ig = gw[0], fg = gw[H], zg = gw[2 * H], og = gw[3 * H];
     const size_t yo = (size_t)row * ndH + dir * H + u;
     const float c = a.cbuf[yo];
-    const float cp = has_prev ? a.cbuf[(size_t)prow * ndH + dir * H + u] : 0.f;
+    const size_t st = ((size_t)dir * a.B + a.perm[j]) * H + u;     // caller-order state
+    const float cp = has_prev ? a.cbuf[(size_t)prow * ndH + dir * H + u] : (a.c0 ? a.c0[st] : 0.f);
     const size_t so = ((size_t)dir * a.B + j) * H + u;
     float dhr = 0.f;
     if (has_next) {
         const float* dr = a.dh_rec + ((size_t)dir * a.dh_splits * a.B + j) * H + u;
         for (int z = 0; z < a.dh_splits; ++z) dhr += dr[(size_t)z * a.B * H];
+    } else if (a.dh_n) {
+        dhr = a.dh_n[st];                          // the sequence's last step: the final state's error
     }
     const float dh = a.dy[yo] + dhr;
-    const float carry = has_next ? a.dcc[so] : 0.f;
+    const float carry = has_next ? a.dcc[so] : (a.dc_n ? a.dc_n[st] : 0.f);
     const float* pp = a.peep + (size_t)dir * 3 * H + u;
-    const float tc = tanhf(c);
-    const float dao = dh * tc * og * (1.f - og);
-    const float dc = dh * og * (1.f - tc * tc) + dao * pp[2 * H] + carry;
-    const float dai = dc * zg * ig * (1.f - ig);
-    const float daf = dc * cp * fg * (1.f - fg);
-    const float daz = dc * ig * (1.f - zg * zg);
+    float dai = 0.f, daf = 0.f, daz = 0.f, dao = 0.f, carry_out = 0.f;
+    if (!a.padded || t < a.slot_len[j]) {           // a padding frame passes no gradient
+        const float tc = tanhf(c);
+        dao = dh * tc * og * (1.f - og);
+        const float dc = dh * og * (1.f - tc * tc) + dao * pp[2 * H] + carry;
+        dai = dc * zg * ig * (1.f - ig);
+        daf = dc * cp * fg * (1.f - fg);
+        daz = dc * ig * (1.f - zg * zg);
+        carry_out = dc * fg + dai * pp[0] + daf * pp[H];
+        if (!has_prev && a.dc0) a.dc0[st] = carry_out;   // the sequence's first step
+    }
     gw[0] = dai; gw[H] = daf; gw[2 * H] = daz; gw[3 * H] = dao;
-    a.dcc[so] = dc * fg + dai * pp[0] + daf * pp[H];
+    a.dcc[so] = carry_out;
     if (a.dab16) {
         __nv_bfloat16* db = a.dab16 + ((size_t)dir * a.B + j) * 4 * H + u;
         db[0] = __float2bfloat16_rn(dai); db[H] = __float2bfloat16_rn(daf);

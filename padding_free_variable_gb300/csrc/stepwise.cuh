@@ -27,6 +27,14 @@ struct StepArgs {
     __nv_bfloat16* hb16;      // optional, forward: [ndir][B][H] bf16 h of the step's rows (next product's A)
     __nv_bfloat16* dab16;     // optional, backward: [ndir][B][4H] bf16 gate errors of the step's rows
     int rh_splits, dh_splits; // K slices of the per-step products (1 without split)
+    int padded;               // the padded comparator's plan: frames t >= length are masked
+    // initial states and final-state errors, [ndir][B][H] caller order (NULL = zero / not wanted);
+    // R h0 is folded into the first step's pre-activations beforehand
+    const float* h0;
+    const float* c0;
+    const float* dh_n;
+    const float* dc_n;
+    float* dc0;
 };
 
 // Cell of step s (forward, or BPTT in backward order) for both directions.

@@ -84,6 +84,17 @@ class Plan:
                 "product": ("cuda_cores", "mma_sync", "tcgen05")[m.value],
                 "exchange": "bulk" if v.value & 1 else "barrier", "tma_tiles": bool(v.value & 2)}
 
+    def recurrent_groups(self, backward: bool = False) -> tuple:
+        """(sequence groups, sorted slots per group) of the last forward (or backward) recurrent launch."""
+        g, r = ctypes.c_int32(), ctypes.c_int32()
+        check(_lib.load().lstm_plan_recurrent_groups(self.handle, int(bool(backward)), ctypes.byref(g),
+                                                     ctypes.byref(r)), "lstm_plan_recurrent_groups")
+        return g.value, r.value
+
+    def debug_sequence_groups(self, slots: int):
+        """Force the cluster kernels' slots per sequence group (0 = automatic)."""
+        check(_lib.load().lstm_debug_sequence_groups(self.handle, int(slots)), "lstm_debug_sequence_groups")
+
     def trace_steps(self, buffer, steps: int):
         """Phase stamps into `buffer` (int64 device tensor of 2*ndir*steps*8), or off with steps=0."""
         check(_lib.load().lstm_debug_trace_steps(self.handle, _ptr(buffer), int(steps)), "lstm_debug_trace_steps")
@@ -129,6 +140,20 @@ class Plan:
             self.close()
         except Exception:
             pass
+
+
+def device_layers(layers, bf16: bool, device="cuda") -> list:
+    """Per-layer parameter dicts (numpy W, R, b, peep in the header's layout) as device tensors:
+    W and R in the layer's operand type (bf16 or fp32), b and peep fp32."""
+    wdt = torch.bfloat16 if bf16 else torch.float32
+    out = []
+    for lay in layers:
+        out.append({"W": torch.from_numpy(np.ascontiguousarray(lay["W"])).to(device=device, dtype=wdt).contiguous(),
+                    "R": torch.from_numpy(np.ascontiguousarray(lay["R"])).to(device=device, dtype=wdt).contiguous(),
+                    "b": torch.from_numpy(np.ascontiguousarray(lay["b"])).to(device=device, dtype=torch.float32),
+                    "peep": torch.from_numpy(np.ascontiguousarray(lay["peep"])).to(device=device,
+                                                                                   dtype=torch.float32)})
+    return out
 
 
 def layer_shape(input_size, hidden_size, num_directions, bf16: bool) -> LayerShape:

@@ -1,25 +1,33 @@
 """Shared helpers of the GPU parity tests: run a workload through the C ABI
 and through the oracle, and compare.
 
-Error metric.  The required bars are a maximum relative error of 1e-4 (fp32
-path) and 2e-2 (bf16-operand path); the pages define neither term.  Reading:
-the relative error of an output tensor is its largest absolute deviation
-relative to its largest magnitude,
+Error metrics.  The required bars are a maximum relative error of 1e-4 (fp32
+path) and 2e-2 (bf16-operand path); the pages define neither term.  Two
+readings are computed for every output tensor:
 
-    err = max_i |g_i - r_i| / max_i |r_i| .
+    normwise     err = max_i |g_i - r_i| / max_i |r_i|
+    element-wise err = max_i |g_i - r_i| / max(|r_i|, 1e-3 max_j |r_j|)
 
-An element-by-element ratio is ill-posed here: gradients are sums of many
-signed terms and have entries near zero by cancellation, and the bf16 path's
-own defined arithmetic (h and the gate errors rounded to bf16 before each
-product) already moves such entries by more than 100% of their value while
-moving no entry by more than ~3e-3 of the tensor's scale (measured on the
-oracle alone, with and without that rounding).  The element-wise ratio with
-a floor of 1e-3 of the tensor's scale is still computed and recorded as a
-diagnostic (``elementwise``).
+The fp32 path is gated on BOTH: the normwise error at 1e-4, and the
+element-wise error (floor 1e-3 of the tensor's scale) at TOL_F32_ELEMENTWISE.
+That second bar is set from what plain fp32 arithmetic reaches on these
+cases: the CUDA-core engine (FFMA products, fp32 accumulation) measured up
+to 1.0e-3 element-wise against the fp64 oracle on the same inputs (workload
+2's dpeep; workload 4's dW 9.2e-4; the small cases 1.5e-4 to 5.0e-4), so
+no fp32 implementation meets 1e-4 element-wise on every entry near the
+floor.  2e-3 is twice that worst case, and 2-9x below what the products
+reached when each term kept only 2^-17 of its value (a two-piece bf16
+split: 3.5e-3 to 1.7e-2 on workloads 2 and 4).
 
-For the bf16 path a second, tighter comparison runs against the oracle in
-its bf16-product mode (the same roundings as the kernels), so that a wrong
-kernel cannot hide inside the 2e-2 allowance for rounding.
+The bf16 path is gated normwise only.  Its own defined arithmetic (h and the
+gate errors rounded to bf16 before each product) moves gradient entries near
+zero by more than 100% of their value while moving no entry by more than
+~3e-3 of the tensor's scale (measured on the oracle alone, with and without
+that rounding), so an element-wise ratio would reject every correct bf16
+implementation; it is still recorded (``elementwise``).  A second, tighter
+comparison runs against the oracle in its bf16-product mode (the same
+roundings as the kernels), so that a wrong kernel cannot hide inside the
+2e-2 allowance for rounding.
 """
 from __future__ import annotations
 
@@ -29,6 +37,7 @@ import os
 import numpy as np
 
 TOL_F32 = 1e-4
+TOL_F32_ELEMENTWISE = 2e-3
 TOL_BF16 = 2e-2
 # bf16 path vs the oracle doing the same roundings: what remains is fp32
 # accumulation order and the rare operand that rounds to the other bf16
@@ -60,20 +69,12 @@ def elementwise_err(got, ref, floor=1e-3) -> float:
 
 
 def device_layers(w, device="cuda"):
-    import torch
-    bf16 = w.spec.dtype == "bf16"
-    wdt = torch.bfloat16 if bf16 else torch.float32
-    out = []
-    for lay in w.layers:
-        out.append({"W": torch.from_numpy(lay["W"]).to(device=device, dtype=wdt).contiguous(),
-                    "R": torch.from_numpy(lay["R"]).to(device=device, dtype=wdt).contiguous(),
-                    "b": torch.from_numpy(lay["b"]).to(device=device, dtype=torch.float32).contiguous(),
-                    "peep": torch.from_numpy(lay["peep"]).to(device=device, dtype=torch.float32).contiguous()})
-    return out
+    from padding_free_variable_gb300 import ops
+    return ops.device_layers(w.layers, w.spec.dtype == "bf16", device)
 
 
 def run_gpu(w, padded: bool = False, device="cuda", ctas: int = 0, engine: int = 0, stepwise: bool = False,
-            variant: int = -1):
+            variant: int = -1, group_slots: int = 0):
     """pack -> all layers forward -> all layers backward -> unpack, through the C ABI."""
     import torch
     from padding_free_variable_gb300 import ops
@@ -83,6 +84,8 @@ def run_gpu(w, padded: bool = False, device="cuda", ctas: int = 0, engine: int =
         plan.set_ctas_per_direction(ctas)
     if variant >= 0:
         plan.debug_cluster_variant(variant)
+    if group_slots:
+        plan.debug_sequence_groups(group_slots)
     if engine:
         plan.set_gemm_engine(engine)
     stack = ops.PackedLSTMStack(plan, device_layers(w, device), w.spec.input_size, w.spec.hidden_size,
@@ -136,11 +139,18 @@ def record(label, kind, errs, elem):
             f.write(json.dumps({"case": label, "against": kind, "max_rel": errs, "elementwise_1e-3": elem}) + "\n")
 
 
-def compare_all(gpu, ref, tol, grads=True, label="", against="oracle"):
+def compare_all(gpu, ref, tol, grads=True, label="", against="oracle", elem_tol=None):
+    """Normwise gate at `tol`; element-wise gate at `elem_tol` (default: TOL_F32_ELEMENTWISE
+    for the fp32 bar, none for the bf16 bars)."""
+    if elem_tol is None and tol == TOL_F32:
+        elem_tol = TOL_F32_ELEMENTWISE
     pairs = _pairs(gpu, ref, grads)
     errs = {k: rel_err(g, r) for k, g, r in pairs}
     elem = {k: elementwise_err(g, r) for k, g, r in pairs}
     record(label, against, errs, elem)
     bad = {k: v for k, v in errs.items() if not v <= tol}
     assert not bad, f"{label} vs {against} over tolerance {tol}: {bad} (all: {errs})"
+    if elem_tol is not None:
+        bad = {k: v for k, v in elem.items() if not v <= elem_tol}
+        assert not bad, f"{label} vs {against} element-wise over {elem_tol}: {bad} (all: {elem})"
     return errs

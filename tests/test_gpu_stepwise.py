@@ -57,3 +57,27 @@ def test_wide_bf16_layers_run_per_step_tensor_core_products():
     compare_all(gpu, run_oracle(w), TOL_BF16, label="wide bf16 per-step")
     compare_all(gpu, run_oracle(w, bf16_products=True), TOL_BF16_EMULATED, label="wide bf16 per-step",
                 against="oracle-bf16-products")
+
+
+def test_wide_bf16_padded_plan_runs_the_same_per_step_kernels():
+    """The zero-padded comparator of a layer wider than a cluster (H > 512) runs the same
+    per-step tcgen05 products and masked cell kernels as the packed run, and gives the
+    per-sequence results ("On batching variable size inputs...", Sec. 2: padding to the
+    longest sequence of the batch)."""
+    w = synthetic.custom(2, 2, 24, 520, [7, 1, 12, 0, 12, 3], seed=78, dtype="bf16", weight_range=0.1)
+    gpu = run_gpu(w, padded=True)
+    for backward in (False, True):
+        cfg = gpu["plan"].recurrent_config(backward)
+        assert cfg["kernel"] == "step_launches" and cfg["product"] == "tcgen05", cfg
+    compare_all(gpu, run_oracle(w), TOL_BF16, label="wide bf16 padded")
+    packed = run_gpu(w)
+    for k in ("y", "dx", "h_n", "c_n"):
+        assert np.abs(gpu[k] - packed[k]).max() <= 1e-6 * max(1.0, np.abs(packed[k]).max()), k
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_stepwise_padded_plan_matches_oracle(dtype):
+    w = synthetic.custom(2, 2, 16, 64, [9, 0, 4, 21, 21, 2], seed=19, dtype=dtype,
+                         weight_range=0.1 if dtype == "bf16" else 0.3)
+    gpu = run_gpu(w, padded=True, stepwise=True)
+    compare_all(gpu, run_oracle(w), TOL_BF16 if dtype == "bf16" else TOL_F32, label=f"stepwise padded {dtype}")

@@ -379,3 +379,161 @@ def test_bf16_rounding_of_generator_is_representable():
     assert synthetic.round_bf16(np.array([1 + 2 ** -8], np.float32))[0] == 1.0
     assert synthetic.round_bf16(np.array([1 + 3 * 2 ** -8], np.float32))[0] == 1 + 2 ** -6
     assert math.isclose(float(synthetic.round_bf16(np.array([0.1], np.float32))[0]), 0.10009765625)
+
+
+# --------------------------------------------------------------------------- bf16-product rounding
+
+def _nearest_bf16_by_definition(v: float) -> float:
+    """The bfloat16 nearest to fp32(v), ties to the neighbour with an even last mantissa bit,
+    found by comparing distances to the two bf16 neighbours that bracket it (exact in fp64)."""
+    f = np.float32(v)
+    if not np.isfinite(f):
+        return float(f)
+    bits = int(np.array([f], np.float32).view(np.uint32)[0])
+    lo_bits = bits & 0xFFFF0000                     # bf16 neighbour toward zero (same sign)
+    hi_bits = lo_bits + 0x10000                     # next bf16 away from zero
+    lo = float(np.array([lo_bits], np.uint32).view(np.float32)[0])
+    hi = float(np.array([hi_bits & 0xFFFFFFFF], np.uint32).view(np.float32)[0])
+    dlo, dhi = abs(float(f) - lo), abs(hi - float(f))
+    if dlo < dhi:
+        return lo
+    if dhi < dlo:
+        return hi
+    return lo if ((lo_bits >> 16) & 1) == 0 else hi
+
+
+def test_oracle_bf16_rounding_nearest_ties_to_even():
+    """The oracle's bf16-product mode rounds like the kernels' cvt.rn.bf16: fp32 first, then the
+    nearest bf16 with ties to even; Inf and NaN pass through."""
+    one = 1.0
+    # exact ties: 1 + 2^-8 lies halfway between 1 and 1 + 2^-7 (even: 1); 1 + 3*2^-8 halfway
+    # between 1 + 2^-7 and 1 + 2^-6 (even: 1 + 2^-6); the same below zero
+    assert oracle.round_bf16(one + 2.0 ** -8) == one
+    assert oracle.round_bf16(one + 3 * 2.0 ** -8) == one + 2.0 ** -6
+    assert oracle.round_bf16(-(one + 2.0 ** -8)) == -one
+    assert oracle.round_bf16(one + 2.0 ** -8 + 2.0 ** -20) == one + 2.0 ** -7    # just past the tie
+    assert oracle.round_bf16(0.0) == 0.0 and math.copysign(1.0, oracle.round_bf16(-0.0)) == -1.0
+    assert oracle.round_bf16(float("inf")) == float("inf")
+    assert oracle.round_bf16(float("-inf")) == float("-inf")
+    assert math.isnan(oracle.round_bf16(float("nan")))
+    rng = np.random.default_rng(2024)
+    vals = np.concatenate([rng.standard_normal(4000) * 10.0 ** rng.integers(-30, 30, 4000),
+                           rng.uniform(-1, 1, 2000)])
+    for v in vals:
+        r = oracle.round_bf16(float(v))
+        assert r == _nearest_bf16_by_definition(float(v)), v
+        assert r == float(synthetic.round_bf16(np.array([v]))[0]), v
+
+
+# --------------------------------------------------------------------------- initial states
+
+def _state_inputs(rng, nl, ndir, B, H, scale=0.5):
+    return [rng.uniform(-scale, scale, (nl, ndir, B, H)) for _ in range(4)]     # h0, c0, dh_n, dc_n
+
+
+@pytest.mark.parametrize("ndir,nl", [(1, 1), (2, 1), (2, 2)])
+def test_initial_states_match_torch_lstm(ndir, nl):
+    """torch.nn.LSTM given (h0, c0), no peepholes, the loss reading y, h_n and c_n: outputs,
+    final states and the gradients of x, every weight, h0 and c0 through autograd."""
+    torch = pytest.importorskip("torch")
+    from torch.nn.utils.rnn import pack_sequence, pad_packed_sequence
+    rng = np.random.default_rng(300 + 10 * ndir + nl)
+    H, D0 = 5, 3
+    lengths = np.array([4, 7, 1, 3, 7])
+    B = len(lengths)
+    layers = [rand_layer(rng, ndir, D0 if l == 0 else ndir * H, H, peep=False) for l in range(nl)]
+    x = rng.standard_normal((lengths.sum(), D0))
+    G = rng.standard_normal((lengths.sum(), ndir * H))
+    h0, c0, Gh, Gc = _state_inputs(rng, nl, ndir, B, H)
+    out = oracle.lstm_stack(lengths, x, layers, ndir, H, G=G, h0=h0, c0=c0, dh_n=Gh, dc_n=Gc)
+
+    mod = torch.nn.LSTM(D0, H, num_layers=nl, bidirectional=(ndir == 2)).double()
+    with torch.no_grad():
+        for l, lay in enumerate(layers):
+            for d in range(ndir):
+                sfx = f"_l{l}" + ("_reverse" if d else "")
+                getattr(mod, "weight_ih" + sfx).copy_(torch.from_numpy(lay["W"][d]))
+                getattr(mod, "weight_hh" + sfx).copy_(torch.from_numpy(lay["R"][d]))
+                getattr(mod, "bias_ih" + sfx).copy_(torch.from_numpy(lay["b"][d]))
+                getattr(mod, "bias_hh" + sfx).zero_()
+    st = concat_offsets(lengths)
+    seqs = [torch.tensor(x[st[i]:st[i + 1]], dtype=torch.float64, requires_grad=True) for i in range(B)]
+    th0 = torch.tensor(h0.reshape(nl * ndir, B, H), requires_grad=True)
+    tc0 = torch.tensor(c0.reshape(nl * ndir, B, H), requires_grad=True)
+    y, (h_n, c_n) = mod(pack_sequence(seqs, enforce_sorted=False), (th0, tc0))
+    ypad, _ = pad_packed_sequence(y, batch_first=True)
+    ycat = torch.cat([ypad[i, :lengths[i]] for i in range(B)])
+    loss = (ycat * torch.from_numpy(G)).sum() + (h_n * torch.from_numpy(Gh.reshape(nl * ndir, B, H))).sum() \
+        + (c_n * torch.from_numpy(Gc.reshape(nl * ndir, B, H))).sum()
+    loss.backward()
+    tol = dict(rtol=1e-11, atol=1e-13)
+    np.testing.assert_allclose(out["y"], ycat.detach().numpy(), **tol)
+    np.testing.assert_allclose(out["h_n"], h_n.detach().numpy().reshape(nl, ndir, B, H), **tol)
+    np.testing.assert_allclose(out["c_n"], c_n.detach().numpy().reshape(nl, ndir, B, H), **tol)
+    np.testing.assert_allclose(out["dx"], torch.cat([s.grad for s in seqs]).numpy(), **tol)
+    np.testing.assert_allclose(out["dh0"], th0.grad.numpy().reshape(nl, ndir, B, H), **tol)
+    np.testing.assert_allclose(out["dc0"], tc0.grad.numpy().reshape(nl, ndir, B, H), **tol)
+    for l in range(nl):
+        for k, tk in (("W", "weight_ih"), ("R", "weight_hh"), ("b", "bias_ih")):
+            ref = np.stack([getattr(mod, f"{tk}_l{l}" + ("_reverse" if d else "")).grad.numpy()
+                            for d in range(ndir)])
+            np.testing.assert_allclose(out["grads"][l][k], ref, err_msg=f"layer {l} d{k}", **tol)
+
+
+@pytest.mark.parametrize("ndir,nl", [(1, 1), (2, 2)])
+def test_initial_state_gradients_match_central_differences(ndir, nl):
+    """With peepholes (which read c0 at the first step): dh0, dc0 and every parameter
+    gradient against central differences of L = <y, G> + <h_n, Gh> + <c_n, Gc>."""
+    rng = np.random.default_rng(400 + 10 * ndir + nl)
+    H, D0 = 4, 3
+    lengths = np.array([1, 2, 5, 0])
+    B = len(lengths)
+    layers = [rand_layer(rng, ndir, D0 if l == 0 else ndir * H, H, a=0.6) for l in range(nl)]
+    x = rng.standard_normal((lengths.sum(), D0))
+    G = rng.standard_normal((lengths.sum(), ndir * H))
+    h0, c0, Gh, Gc = _state_inputs(rng, nl, ndir, B, H, scale=0.8)
+    out = oracle.lstm_stack(lengths, x, layers, ndir, H, G=G, h0=h0, c0=c0, dh_n=Gh, dc_n=Gc)
+
+    def loss():
+        r = oracle.lstm_stack(lengths, x, layers, ndir, H, h0=h0, c0=c0)
+        return float((r["y"] * G).sum() + (r["h_n"] * Gh).sum() + (r["c_n"] * Gc).sum())
+
+    eps = 1e-6
+
+    def check(arr, grad, name):
+        flat, gflat = arr.reshape(-1), grad.reshape(-1)
+        for i in range(flat.size):
+            keep = flat[i]
+            flat[i] = keep + eps
+            lp = loss()
+            flat[i] = keep - eps
+            lm = loss()
+            flat[i] = keep
+            fd = (lp - lm) / (2 * eps)
+            assert abs(fd - gflat[i]) <= 1e-7 * max(1.0, abs(fd)), (name, i, fd, gflat[i])
+
+    check(h0, out["dh0"], "h0")
+    check(c0, out["dc0"], "c0")
+    check(x, out["dx"], "x")
+    for l in range(nl):
+        for k in ("W", "R", "b", "peep"):
+            check(layers[l][k], out["grads"][l][k], f"layer{l}.{k}")
+    # an empty sequence consumes nothing: its final state is its initial state
+    np.testing.assert_array_equal(out["h_n"][:, :, 3], h0[:, :, 3])
+    np.testing.assert_array_equal(out["dc0"][:, :, 3], Gc[:, :, 3])
+
+
+def test_passing_the_final_state_on_equals_one_longer_sequence():
+    """RETURNN paper, Sec. 3.2 (one RNN's final state as another's initial state): running
+    frames [0, L1) and then [L1, L) from the first part's final state gives the outputs and
+    final state of running all L frames at once (forward direction)."""
+    rng = np.random.default_rng(17)
+    H, D = 6, 4
+    lay = rand_layer(rng, 1, D, H)
+    x = rng.standard_normal((11, D))
+    whole = oracle.lstm_stack(np.array([11]), x, [lay], 1, H)
+    a = oracle.lstm_stack(np.array([4]), x[:4], [lay], 1, H)
+    b = oracle.lstm_stack(np.array([7]), x[4:], [lay], 1, H, h0=a["h_n"], c0=a["c_n"])
+    np.testing.assert_allclose(np.concatenate([a["y"], b["y"]]), whole["y"], rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(b["h_n"], whole["h_n"], rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(b["c_n"], whole["c_n"], rtol=1e-14, atol=1e-15)
