@@ -169,24 +169,33 @@ SMEM_BYTES_PER_CLK = 128      # shared-memory bandwidth of one SM, bytes per clo
 GEMM_KINDS = ("input_gemm", "gemm_dx", "gemm_dw", "gemm_dr")
 
 
-def rec_smem_bytes(kind, spec, rows, T, ctas):
+def group_steps(lengths, slots):
+    """Steps of each sequence group: the longest length among its sorted slots."""
+    srt = np.sort(np.asarray(lengths))[::-1]
+    slots = max(1, int(slots))
+    return [int(srt[g]) for g in range(0, len(srt), slots)]
+
+
+def rec_smem_bytes(kind, spec, rows, T, ctas, steps_per_cluster=None):
     """Algorithmic on-chip bytes of one recurrent pass over all layers.
 
-    Per step and direction: every element of R_dir read once from on-chip storage
-    (4H*H elements at the weight precision) plus the step's vector operand staged
-    into each of the direction's CTAs (bs[t] rows of H values: h_{t-1} forward, the
-    partial sums of R^T*dA backward).  Summed over steps: T*|R_dir| + ctas*N*H*b_h.
+    Per step of each cluster (one per direction and sequence group): every element of
+    R_dir read once from on-chip storage (4H*H elements at the weight precision) plus the
+    step's vector operand staged into each of the cluster's CTAs (its rows of H values:
+    h_{t-1} forward, the partial sums of R^T*dA backward).  Summed over the clusters' steps:
+    sum_g T_g * |R_dir| + ctas * N * H * b_h per direction (one group: T * |R_dir| + ...).
     """
     H, nd = spec.hidden_size, spec.num_directions
     e = 2 if spec.dtype == "bf16" else 4
-    return float(spec.num_layers * nd * (T * 4 * H * H * e + ctas * rows * H * e))
+    steps = float(sum(steps_per_cluster)) if steps_per_cluster else float(T)
+    return float(spec.num_layers * nd * (steps * 4 * H * H * e + ctas * rows * H * e))
 
 
-def roofline_of(kind, ms_per_step, calls_per_step, spec, rows, T, D0, peaks, rec_cfg):
+def roofline_of(kind, ms_per_step, calls_per_step, spec, rows, T, D0, peaks, rec_cfg, lengths=None):
     """Roofline entry of one kernel kind from its per-step time.
 
-    rec_fwd/rec_bwd: shared-memory bandwidth of the SMs holding R (152 SMs x 128 B/clk at
-    the maximum SM clock, scaled to the CTAs in use).  GEMMs with bf16 operands (tcgen05):
+    rec_fwd/rec_bwd: shared-memory bandwidth of the SMs holding R (128 B/clk per SM at the
+    maximum SM clock, over every CTA of every cluster in use: ctas x directions x groups).  GEMMs with bf16 operands (tcgen05):
     the sustained measured bf16 peak, or HBM when the bytes take longer.  The rest:
     HBM (measured copy bandwidth) or CUDA-core FP32 (derived) whichever bounds it.
     """
@@ -204,17 +213,34 @@ def roofline_of(kind, ms_per_step, calls_per_step, spec, rows, T, D0, peaks, rec
                 "per_launch": {"flops": fl / per, "ms": ms_per_step / per}}
     if kind in ("rec_fwd", "rec_bwd") and rec_cfg and rec_cfg.get("ctas_per_direction"):
         ctas = rec_cfg["ctas_per_direction"]
-        sb = rec_smem_bytes(kind, spec, rows, T, ctas)
-        sms = ctas * spec.num_directions
+        groups = int(rec_cfg.get("groups") or 1)
+        gsteps = group_steps(lengths, rec_cfg.get("slots_per_group") or len(lengths)) \
+            if (lengths is not None and groups > 1) else None
+        sb = rec_smem_bytes(kind, spec, rows, T, ctas, gsteps)
+        sms = ctas * spec.num_directions * groups
         peak = sms * SMEM_BYTES_PER_CLK * clk * 1e6 / 1e9                     # GB/s
         ach = sb / sec / 1e9 if sec > 0 else 0.0
         tensor_peak = float(peaks["bf16_tflops_sustained"]) * (1.0 if spec.dtype == "bf16" else 1.1 / 2.25)
-        return {"kernel": kind, "bound": "smem", "achieved": round(ach, 1), "peak": round(peak, 1), "unit": "GB/s",
-                "frac": round(ach / peak, 4), "recurrent_kernel": rec_cfg,
-                "peak_source": f"derived: {sms} SMs x {SMEM_BYTES_PER_CLK} B/clk x {clk:.0f} MHz",
-                "tensor_view": {"achieved_tflops": round(fl / sec / 1e12, 3) if sec > 0 else 0.0,
-                                "peak_tflops": round(tensor_peak, 1)},
-                "per_launch": {"smem_bytes": sb / per, "flops": fl / per, "ms": ms_per_step / per}}
+        out = {"kernel": kind, "bound": "smem", "achieved": round(ach, 1), "peak": round(peak, 1), "unit": "GB/s",
+               "frac": round(ach / peak, 4), "recurrent_kernel": rec_cfg,
+               "peak_source": f"derived: {sms} SMs x {SMEM_BYTES_PER_CLK} B/clk x {clk:.0f} MHz",
+               "tensor_view": {"achieved_tflops": round(fl / sec / 1e12, 3) if sec > 0 else 0.0,
+                               "peak_tflops": round(tensor_peak, 1)},
+               "per_launch": {"smem_bytes": sb / per, "flops": fl / per, "ms": ms_per_step / per}}
+        if gsteps:
+            # the cluster of the longest sequences sets the kernel's time: its own bytes over its
+            # own SMs (the other groups finish earlier and leave their SMs idle)
+            H, nd = spec.hidden_size, spec.num_directions
+            e = 2 if spec.dtype == "bf16" else 4
+            srt = np.sort(np.asarray(lengths))[::-1]
+            rows0 = int(srt[:int(rec_cfg["slots_per_group"])].sum())     # frames of group 0's slots
+            b0 = float(spec.num_layers * (gsteps[0] * 4 * H * H * e + ctas * rows0 * H * e))
+            p0 = ctas * SMEM_BYTES_PER_CLK * clk * 1e6 / 1e9
+            a0 = b0 / sec / 1e9 if sec > 0 else 0.0
+            out["critical_cluster"] = {"steps": gsteps[0], "rows": rows0, "achieved": round(a0, 1),
+                                       "peak": round(p0, 1), "frac": round(a0 / p0, 4),
+                                       "group_steps": gsteps}
+        return out
     hbm_peak = float(peaks["hbm_gbs"])                                        # GB/s
     t_hbm = by / (hbm_peak * 1e9)
     if kind in GEMM_KINDS and spec.dtype == "bf16":
@@ -533,10 +559,13 @@ def main():
     plan.enable_timing(False)
     kernels = {}
     rec_cfg = {"rec_fwd": plan.recurrent_config(False), "rec_bwd": plan.recurrent_config(True)}
+    for k, bwd in (("rec_fwd", False), ("rec_bwd", True)):
+        g, sl = plan.recurrent_groups(bwd)
+        rec_cfg[k].update({"groups": g, "slots_per_group": sl})
     for kind, (ms, calls) in tim.items():
         if calls:
             r = roofline_of(kind, ms / traced, calls / traced, spec, plan.rows, T, spec.input_size, peaks,
-                            rec_cfg.get(kind))
+                            rec_cfg.get(kind), lengths=w.lengths)
             r["ms_per_step"] = round(ms / traced, 4)
             kernels[kind] = r
     dom = max(kernels.values(), key=lambda r: r["ms_per_step"])

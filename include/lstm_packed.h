@@ -155,6 +155,63 @@ lstm_status lstm_plan_compute_host(const int32_t* lengths_host, int32_t B, int32
                                    int32_t* slot_len, int32_t* row_src, int32_t* prev_fwd,
                                    int32_t* prev_rev);
 
+/*
+ * Segment plan (RETURNN paper, Sec. 4: sequences are cut into possibly
+ * overlapping segments of constant length, each trained as a sequence of its
+ * own, which trades context for far less padding).  Sequence b of lengths_host
+ * yields segments starting at frames 0, step, 2*step, ... of min(chunk,
+ * L_b - start) frames, up to the first segment that reaches the sequence's
+ * end; an empty sequence yields one empty segment.  1 <= step <= chunk.
+ * The plan's sequences ("caller order") are the segments in that order
+ * (sequence-major): h_n, c_n and states are per segment.  lstm_pack reads the
+ * caller's concatenated frames of the ORIGINAL sequences (frames overlapped by
+ * two segments are read by both); lstm_unpack writes each original frame once,
+ * from the segment that owns it (a segment owns its frames up to the next
+ * segment's start, the last one to the sequence's end).  lstm_plan_info
+ * reports the segments as the batch and sum(L_b) as the frames.
+ */
+lstm_status lstm_plan_create_segments(const int32_t* lengths_host, int32_t B, int32_t chunk,
+                                      int32_t step, lstm_plan** out);
+
+/* Host-only listing of the same segments (no device, no allocation):
+ * *num_segments receives their count; with capacity >= that count the arrays
+ * (any may be NULL) receive each segment's sequence, start frame and length.
+ * LSTM_ERR_INVALID_ARG when the arrays are too short. */
+lstm_status lstm_segments_host(const int32_t* lengths_host, int32_t B, int32_t chunk, int32_t step,
+                               int32_t* num_segments, int32_t* seg_seq, int32_t* seg_start,
+                               int32_t* seg_len, int32_t capacity);
+
+/*
+ * Window plan for truncated back-propagation through time ("Single Stream
+ * Parallelization...", Sec. 4, BPTT(h; h'): the network steps h' frames at a
+ * time, and the errors of those frames are back-propagated through them only).
+ * The plan covers frames [start, start + width) of every sequence (fewer, or
+ * none, near and past its end) with all B sequences in the caller's order, so
+ * lstm_fwd_state started from the previous window's h_n / c_n continues each
+ * sequence exactly, and lstm_bwd_state truncates its errors at the window's
+ * start.  lstm_pack reads and lstm_unpack writes the caller's full
+ * concatenated tensors (sum(L_b) rows): only the window's frames are touched.
+ */
+lstm_status lstm_plan_create_window(const int32_t* lengths_host, int32_t B, int32_t start, int32_t width,
+                                    lstm_plan** out);
+
+/*
+ * Dynamic (frame-budget) batch formation ("On batching variable size
+ * inputs...", Sec. 2: a dynamic batch size is a total length of the batch's
+ * sequences rather than a number of sequences, so that batches of short
+ * sequences hold more of them).  Sequences are taken in the given order (the
+ * caller's batching strategy -- random, sorted or bucketed -- fixes that
+ * order); each joins the current batch while the batch stays within `budget`,
+ * else it starts the next batch.  budget_kind 0 counts packed frames (sum of
+ * the batch's lengths: what the packed kernels compute); 1 counts padded
+ * frames (sequences x longest length: the page's definition).  A sequence that
+ * alone exceeds the budget forms a batch of its own (cut it first with
+ * lstm_plan_create_segments to bound it).  Writes batch_of[i] (batches
+ * numbered from 0 in order) and *num_batches.  Host only.
+ */
+lstm_status lstm_form_batches(const int32_t* lengths_host, int32_t n, int64_t budget, int32_t budget_kind,
+                              int32_t* batch_of, int32_t* num_batches);
+
 /* Free the plan and its device tables.  NULL is accepted. */
 lstm_status lstm_plan_destroy(lstm_plan* plan);
 
@@ -241,6 +298,67 @@ lstm_status lstm_bwd(const lstm_plan* plan, const lstm_layer_shape* shape,
                      const float* y_packed, void* workspace, const float* dy_packed,
                      float* dx_packed, const lstm_layer_grads* grads, void* scratch,
                      void* stream);
+
+/*
+ * Initial states and final-state errors of one layer (RETURNN paper, Sec. 3.2:
+ * the final state of one recurrent network passed on as the initial state of
+ * another).  Every array is [ndir][B][H] fp32 in caller order (direction d,
+ * sequence b at [d][b]), device memory, 16-byte aligned; any pointer may be
+ * NULL, meaning zero (inputs) or not wanted (outputs).
+ *   h0, c0      the state a direction starts from: the forward direction's
+ *               state before frame 0, the reverse direction's before frame
+ *               L-1 (it consumes x_L .. x_1).  They enter the first step as
+ *               h_{t-1} and c_{t-1}: a = W x + R h0 + b, and c0 in the forget
+ *               gate and the input and forget peepholes.
+ *   dh_n, dc_n  (backward inputs) dL/dh_n and dL/dc_n from outside the layer,
+ *               for a loss that reads the final states as well as y.
+ *   dh0, dc0    (backward outputs) dL/dh0 and dL/dc0.
+ * A sequence of length 0 consumes nothing: h_n = h0, c_n = c0, dh0 = dh_n,
+ * dc0 = dc_n.  Padded plans (lstm_plan_create_padded) take no state: a call
+ * with any non-NULL state pointer on one returns LSTM_ERR_UNSUPPORTED.
+ */
+typedef struct {
+    const float* h0;
+    const float* c0;
+} lstm_state;
+
+typedef struct {
+    const float* dh_n;
+    const float* dc_n;
+    float* dh0;
+    float* dc0;
+} lstm_state_grads;
+
+/* Bytes of the scratch lstm_fwd_state / lstm_bwd_state need (the product
+ * R h0 over the batch, and the first steps' gate errors): [ndir][B][4H] fp32.
+ * Needed when h0 is given (forward) or h0 or dh0 is (backward).  0 on a bad
+ * argument. */
+size_t lstm_state_scratch_bytes(const lstm_plan* plan, const lstm_layer_shape* shape);
+
+/*
+ * lstm_fwd starting from the initial states in `state` (NULL = both zero):
+ * same arguments, results and errors as lstm_fwd, plus `state_scratch`
+ * (lstm_state_scratch_bytes, caller-owned, 16-byte aligned; NULL allowed when
+ * h0 is NULL).  h_n / c_n are the states after each sequence's last frame.
+ */
+lstm_status lstm_fwd_state(const lstm_plan* plan, const lstm_layer_shape* shape,
+                           const lstm_layer_params* params, const lstm_state* state,
+                           const void* x_packed, float* y_packed, void* y_lo, float* h_n,
+                           float* c_n, void* workspace, void* state_scratch, void* stream);
+
+/*
+ * lstm_bwd of a layer run by lstm_fwd_state with the same `state`: the loss
+ * is L = sum <y, dy> + <h_n, dh_n> + <c_n, dc_n>.  Same arguments, results
+ * and errors as lstm_bwd (the weight gradients include the first steps'
+ * terms through h0 and c0), plus `state_grads` (NULL = no final-state errors,
+ * no initial-state gradients) and `state_scratch` as for lstm_fwd_state.
+ */
+lstm_status lstm_bwd_state(const lstm_plan* plan, const lstm_layer_shape* shape,
+                           const lstm_layer_params* params, const lstm_state* state,
+                           const void* x_packed, const float* y_packed, void* workspace,
+                           const float* dy_packed, float* dx_packed, const lstm_layer_grads* grads,
+                           const lstm_state_grads* state_grads, void* scratch, void* state_scratch,
+                           void* stream);
 
 /*
  * lstm_bwd without device allocation.  (The pages have no counterpart: this
@@ -352,9 +470,11 @@ int64_t lstm_plan_launch_count(const lstm_plan* plan);
 /* Launch configuration of the last recurrent kernel run through this plan:
  * `pass` 0 = forward (lstm_fwd), 1 = backward (lstm_bwd / lstm_bwd_noalloc).
  * kind: 0 none yet, 1 grid-wide persistent kernel with flag barriers,
- *       2 one thread-block cluster per direction, 3 per-step launches of a
- *       tcgen05 product over the whole GPU and a cell kernel (bf16 layers
- *       whose R does not fit one cluster, H > 512);
+ *       2 one thread-block cluster per direction and sequence group, 3 per-step
+ *       launches of a tcgen05 product over the whole GPU and a cell kernel,
+ *       4 the persistent kernel of bf16 layers whose R does not fit one cluster
+ *       (H > 512): R or R^T resident in the shared memory of H/16 CTAs per
+ *       direction, tcgen05 products, a grid barrier per step;
  * ctas_per_direction: CTAs that hold one direction's recurrent weights;
  * product: 0 CUDA cores, 1 warp-level mma.sync, 2 tcgen05 with TMEM accumulators;
  * variant (cluster kernels): bit 0 = operands exchanged by bulk copies into
@@ -375,6 +495,13 @@ lstm_status lstm_plan_recurrent_config(const lstm_plan* plan, int32_t pass, int3
  * LSTM_ERR_INVALID_ARG for a NULL plan or a pass other than 0 or 1. */
 lstm_status lstm_plan_recurrent_groups(const lstm_plan* plan, int32_t pass, int32_t* groups,
                                        int32_t* slots_per_group);
+
+/* Test hook for bf16 layers wider than one cluster (H > 512): -1 = automatic
+ * (the persistent kernel with R resident across H/16 CTAs per direction where
+ * it applies -- H a multiple of 64 up to 1024, at most 256 sequences -- else
+ * per-step launches), 0 = per-step launches, 1 = the persistent kernel where it
+ * applies.  LSTM_ERR_INVALID_ARG outside -1..1. */
+lstm_status lstm_debug_wide_recurrence(lstm_plan* plan, int32_t mode);
 
 /* Test hook: slots per sequence group of the cluster recurrent kernels (0 =
  * automatic: the smallest multiple of 8 that gives every cluster an SM of its

@@ -30,7 +30,9 @@ EXPORTED = (
     "lstm_plan_launch_count", "lstm_debug_trace_steps", "lstm_bwd_noalloc",
     "lstm_plan_set_gemm_engine", "lstm_debug_input_projection", "lstm_plan_recurrent_config",
     "lstm_stepwise_scratch_bytes", "lstm_fwd_stepwise", "lstm_bwd_stepwise", "lstm_debug_cluster_variant",
-    "lstm_plan_recurrent_groups", "lstm_debug_sequence_groups",
+    "lstm_plan_recurrent_groups", "lstm_debug_sequence_groups", "lstm_state_scratch_bytes", "lstm_fwd_state",
+    "lstm_bwd_state", "lstm_plan_create_segments", "lstm_segments_host", "lstm_plan_create_window",
+    "lstm_form_batches", "lstm_debug_wide_recurrence",
 )
 
 KERNEL_KINDS = ("pack", "unpack", "input_gemm", "rec_fwd", "rec_bwd", "gemm_dx", "gemm_dw", "gemm_dr", "convert")
@@ -49,6 +51,15 @@ class LayerParams(ctypes.Structure):
 class LayerGrads(ctypes.Structure):
     _fields_ = [("dW", ctypes.c_void_p), ("dR", ctypes.c_void_p), ("db", ctypes.c_void_p),
                 ("dpeep", ctypes.c_void_p)]
+
+
+class State(ctypes.Structure):
+    _fields_ = [("h0", ctypes.c_void_p), ("c0", ctypes.c_void_p)]
+
+
+class StateGrads(ctypes.Structure):
+    _fields_ = [("dh_n", ctypes.c_void_p), ("dc_n", ctypes.c_void_p), ("dh0", ctypes.c_void_p),
+                ("dc0", ctypes.c_void_p)]
 
 
 class LSTMError(RuntimeError):
@@ -90,7 +101,18 @@ def _declare(lib):
         "lstm_plan_launch_count": (i64, [vp]),
         "lstm_plan_recurrent_config": (c, [vp, i32, pi32, pi32, pi32, pi32]),
         "lstm_plan_recurrent_groups": (c, [vp, i32, pi32, pi32]),
+        "lstm_state_scratch_bytes": (sz, [vp, ctypes.POINTER(LayerShape)]),
+        "lstm_plan_create_segments": (c, [pi32, i32, i32, i32, ctypes.POINTER(vp)]),
+        "lstm_segments_host": (c, [pi32, i32, i32, i32, pi32, pi32, pi32, pi32, i32]),
+        "lstm_plan_create_window": (c, [pi32, i32, i32, i32, ctypes.POINTER(vp)]),
+        "lstm_form_batches": (c, [pi32, i32, i64, i32, pi32, pi32]),
+        "lstm_fwd_state": (c, [vp, ctypes.POINTER(LayerShape), ctypes.POINTER(LayerParams), ctypes.POINTER(State),
+                               vp, vp, vp, vp, vp, vp, vp, vp]),
+        "lstm_bwd_state": (c, [vp, ctypes.POINTER(LayerShape), ctypes.POINTER(LayerParams), ctypes.POINTER(State),
+                               vp, vp, vp, vp, vp, ctypes.POINTER(LayerGrads), ctypes.POINTER(StateGrads), vp, vp,
+                               vp]),
         "lstm_debug_sequence_groups": (c, [vp, i32]),
+        "lstm_debug_wide_recurrence": (c, [vp, i32]),
         "lstm_stepwise_scratch_bytes": (ctypes.c_size_t, [vp, ctypes.POINTER(LayerShape)]),
         "lstm_fwd_stepwise": (c, [vp, ctypes.POINTER(LayerShape), ctypes.POINTER(LayerParams), vp, vp, vp, vp, vp,
                                   vp, vp, vp]),

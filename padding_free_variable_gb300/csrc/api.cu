@@ -13,6 +13,7 @@
 #include "common.cuh"
 #include "gemm.cuh"
 #include "recurrent.cuh"
+#include "state.cuh"
 #include "stepwise.cuh"
 
 namespace lstm {
@@ -20,6 +21,19 @@ namespace lstm {
 namespace {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Initial states and final-state errors of one call (all [ndir][B][H] caller order; null =
+// zero / not wanted) and the scratch their products use.
+struct StateIO {
+    const float* h0 = nullptr;
+    const float* c0 = nullptr;
+    const float* dh_n = nullptr;
+    const float* dc_n = nullptr;
+    float* dh0 = nullptr;
+    float* dc0 = nullptr;
+    float* scratch = nullptr;
+    bool any() const { return h0 || c0 || dh_n || dc_n || dh0 || dc0; }
+};
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
@@ -68,10 +82,11 @@ Layout workspace_layout(const Plan& p, const lstm_layer_shape& s)
     const size_t ns = kSplitSegments;
     l.ws_off = l.xs_off + (f32_split_shape(s) ? align256(rows * ns * D * 2) : 0);
     l.rh_off = l.ws_off + (f32_split_shape(s) ? align256(nd * 4 * H * ns * D * 2) : 0);
-    // wide bf16 layers: a step's R h_{t-1} [ndir][B][4H] fp32 and bf16 h [ndir][B][H]
+    // wide bf16 layers: a step's R h_{t-1} [ndir][B][4H] fp32 and bf16 h [ndir][2][B][H] (the per-step
+    // products use parity 0; the persistent kernel exchanges h through both)
     const size_t B = (size_t)p.B;
     l.hb_off = l.rh_off + (wide_bf16(s) ? align256(nd * (size_t)step_splits(p, s, false) * B * 4 * H * 4) : 0);
-    l.total = l.hb_off + (wide_bf16(s) ? align256(nd * B * H * 2) : 0);
+    l.total = l.hb_off + (wide_bf16(s) ? align256(2 * nd * B * H * 2) : 0);
     return l;
 }
 
@@ -320,7 +335,7 @@ StepScratch step_scratch(const Plan& p, const lstm_layer_shape& s)
     q.dcc = off; off += align256(nd * B * H * sizeof(float));
     if (s.dtype == LSTM_BF16) {
         q.hb = off; off += align256(nd * B * H * 2);
-        q.dab = off; off += align256(nd * B * 4 * H * 2);
+        q.dab = off; off += align256(2 * nd * B * 4 * H * 2);      // [ndir][2][B][4H]: both parities (persistent kernel)
         q.rt = off; off += align256(nd * H * 4 * H * 2);
     }
     q.total = off;
@@ -360,12 +375,13 @@ bool step_tc(const Plan& p, const lstm_layer_shape& s)
 // cores from y), then one cell launch for both directions.
 lstm_status stepwise_fwd_core(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm, float* y,
                               void* y_lo, float* h_n, float* c_n, float* ga, float* cbuf, float* rh,
-                              __nv_bfloat16* hb16, cudaStream_t cs)
+                              __nv_bfloat16* hb16, cudaStream_t cs, const StateIO& sio = StateIO())
 {
     const int H = s.hidden_size, nd = s.num_directions, ndH = nd * H;
     const bool bf16 = s.dtype == LSTM_BF16;
     const size_t esz = bf16 ? 2 : 4;
     StepArgs a = step_args(p, s, prm, ga, cbuf);
+    a.h0 = sio.h0; a.c0 = sio.c0;
     a.rh = rh; a.hb16 = hb16;
     a.y = y; a.y_lo = (__nv_bfloat16*)y_lo; a.h_n = h_n; a.c_n = c_n;
     lstm_status st = LSTM_OK;
@@ -424,7 +440,8 @@ lstm_status stepwise_fwd_core(const Plan& p, const lstm_layer_shape& s, const ls
 lstm_status stepwise_bwd_core(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm,
                               const void* x_packed, const float* y_packed, float* ga, float* cbuf,
                               const float* dy_packed, float* dx_packed, const lstm_layer_grads& grads, void* scratch,
-                              float* dh_rec, float* dcc, __nv_bfloat16* dab16, __nv_bfloat16* rt16, cudaStream_t cs)
+                              float* dh_rec, float* dcc, __nv_bfloat16* dab16, __nv_bfloat16* rt16, cudaStream_t cs,
+                              const StateIO& sio = StateIO())
 {
     const int H = s.hidden_size, nd = s.num_directions;
     const bool bf16 = s.dtype == LSTM_BF16;
@@ -432,6 +449,7 @@ lstm_status stepwise_bwd_core(const Plan& p, const lstm_layer_shape& s, const ls
     const size_t esz = bf16 ? 2 : 4;
     StepArgs a = step_args(p, s, prm, ga, cbuf);
     a.dy = dy_packed; a.dh_rec = dh_rec; a.dcc = dcc; a.dab16 = dab16;
+    a.c0 = sio.c0; a.dh_n = sio.dh_n; a.dc_n = sio.dc_n; a.dc0 = sio.dc0;
     lstm_status st = LSTM_OK;
     if (rt16)   // R_d^T [H][4H] bf16: the B operand (K-major) of the per-step R^T da products
         for (int d = 0; d < nd && st == LSTM_OK; ++d)
@@ -478,12 +496,38 @@ lstm_status stepwise_bwd_core(const Plan& p, const lstm_layer_shape& s, const ls
         }
     }
     if (st == LSTM_OK) {
-        st = param_sums_launch(p, ga, cbuf, H, nd, grads.db, grads.dpeep, (float*)scratch, cs);
+        st = param_sums_launch(p, ga, cbuf, H, nd, grads.db, grads.dpeep, (float*)scratch, cs, sio.c0);
         launches += 2;
     }
     trace_end(p, K_REC_BWD, cs, launches);
     if (st != LSTM_OK) return st;
     return bwd_products(p, s, prm, x_packed, y_packed, ga, dx_packed, grads, scratch, cs);
+}
+
+WideArgs wide_args(const Plan& p, const lstm_layer_shape& s, const lstm_layer_params& prm, float* ga, float* cbuf,
+                   const StateIO& sio)
+{
+    WideArgs w;
+    memset(&w, 0, sizeof(w));
+    w.T = p.T; w.B = p.B; w.H = s.hidden_size; w.ndir = s.num_directions;
+    w.padded = p.padded ? 1 : 0;
+    w.bs = p.d_bs; w.off = p.d_off; w.len = p.d_len; w.perm = p.d_perm;
+    w.ga = ga; w.peep = prm.peep; w.cbuf = cbuf;
+    w.h0 = sio.h0; w.c0 = sio.c0; w.dh_n = sio.dh_n; w.dc_n = sio.dc_n; w.dc0 = sio.dc0;
+    w.status = p.d_status; w.wait_limit_ns = p.wait_limit_ns;
+    return w;
+}
+
+// Argument checks of the state pointers (16-byte aligned: the kernels read them as float4).
+lstm_status check_state(const Plan& p, const StateIO& sio, bool need_scratch)
+{
+    if (!sio.any()) return LSTM_OK;
+    if (p.padded) return LSTM_ERR_UNSUPPORTED;   // the padded comparator runs from the zero state
+    for (const void* q : {(const void*)sio.h0, (const void*)sio.c0, (const void*)sio.dh_n, (const void*)sio.dc_n,
+                          (const void*)sio.dh0, (const void*)sio.dc0})
+        if (q && !aligned16(q)) return LSTM_ERR_INVALID_ARG;
+    if (need_scratch && (!sio.scratch || !aligned16(sio.scratch))) return LSTM_ERR_INVALID_ARG;
+    return LSTM_OK;
 }
 
 lstm_status check_params(const lstm_layer_params* prm)
@@ -492,6 +536,188 @@ lstm_status check_params(const lstm_layer_params* prm)
     if (!aligned16(prm->W) || !aligned16(prm->R) || !aligned16(prm->b) || !aligned16(prm->peep))
         return LSTM_ERR_INVALID_ARG;
     return LSTM_OK;
+}
+
+lstm_status fwd_impl(const lstm_plan* plan, const lstm_layer_shape* shape,
+                            const lstm_layer_params* params, const void* x_packed, float* y_packed,
+                            void* y_lo, float* h_n, float* c_n, void* workspace, const StateIO& sio, void* stream)
+{
+    if (!plan) return LSTM_ERR_INVALID_ARG;
+    lstm_status st = check_shape(shape);
+    if (st != LSTM_OK) return st;
+    if ((st = check_params(params)) != LSTM_OK) return st;
+    const Plan& p = plan->p;
+    const lstm_layer_shape& s = *shape;
+    const int H = s.hidden_size, nd = s.num_directions;
+    const bool bf16 = s.dtype == LSTM_BF16;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if ((h_n && !aligned16(h_n)) || (c_n && !aligned16(c_n))) return LSTM_ERR_INVALID_ARG;
+    if ((st = check_state(p, sio, sio.h0 != nullptr && p.rows > 0)) != LSTM_OK) return st;
+    if (p.rows == 0) {      // every sequence is empty: its final state is its initial state
+        const size_t bytes = sizeof(float) * nd * p.B * H;
+        if (h_n) LSTM_CUDA_TRY(sio.h0 ? cudaMemcpyAsync(h_n, sio.h0, bytes, cudaMemcpyDeviceToDevice, cs)
+                                      : cudaMemsetAsync(h_n, 0, bytes, cs));
+        if (c_n) LSTM_CUDA_TRY(sio.c0 ? cudaMemcpyAsync(c_n, sio.c0, bytes, cudaMemcpyDeviceToDevice, cs)
+                                      : cudaMemsetAsync(c_n, 0, bytes, cs));
+        return LSTM_OK;
+    }
+    if (!x_packed || !y_packed || !workspace) return LSTM_ERR_INVALID_ARG;
+    if (!aligned16(x_packed) || !aligned16(y_packed) || !aligned16(workspace) || (y_lo && !aligned16(y_lo)))
+        return LSTM_ERR_INVALID_ARG;
+    const Layout L = workspace_layout(p, s);
+    float* ga = (float*)((char*)workspace + L.ga_off);
+    float* cbuf = (float*)((char*)workspace + L.c_off);
+
+    if (wide_step_path(p, s)) {
+        if ((st = input_projection(p, s, *params, x_packed, ga, (char*)workspace + L.xs_off, cs)) != LSTM_OK)
+            return st;
+        if ((st = state_fold_input(p, H, nd, bf16, params->R, sio.h0, ga, sio.scratch, cs)) != LSTM_OK) return st;
+        if (p.wide_mode != 0 && rec_wide_supported(p, H, nd, bf16)) {
+            WideArgs w = wide_args(p, s, *params, ga, cbuf, sio);
+            w.y = y_packed; w.y_lo = (__nv_bfloat16*)y_lo; w.h_n = h_n; w.c_n = c_n;
+            w.xbuf = (__nv_bfloat16*)((char*)workspace + L.hb_off);
+            p.last_rec_kind[0] = 4; p.last_rec_ctas[0] = H / 16; p.last_rec_mma[0] = 2; p.last_rec_variant[0] = 0;
+            p.last_rec_groups[0] = 1; p.last_rec_grp_rows[0] = p.B;
+            // a launch the device cannot co-schedule falls back to per-step launches (nothing ran)
+            if ((st = rec_wide_fwd_launch(p, w, params->R, cs)) != LSTM_ERR_UNSUPPORTED) return st;
+        }
+        p.last_rec_kind[0] = 3; p.last_rec_ctas[0] = 0; p.last_rec_mma[0] = 2; p.last_rec_variant[0] = 0;
+        p.last_rec_groups[0] = 1; p.last_rec_grp_rows[0] = p.B;
+        return stepwise_fwd_core(p, s, *params, y_packed, y_lo, h_n, c_n, ga, cbuf,
+                                 (float*)((char*)workspace + L.rh_off), (__nv_bfloat16*)((char*)workspace + L.hb_off),
+                                 cs, sio);
+    }
+    RecConfig rc, rcc;
+    RecArgs cl_layout;
+    memset(&cl_layout, 0, sizeof(cl_layout));
+    const bool cluster = rec_cluster_fwd_configure(p, H, nd, bf16, &rcc, &cl_layout);
+    if (!cluster && (st = rec_configure(p, H, nd, bf16, false, p.forced_ctas, &rc)) != LSTM_OK) return st;
+
+    if ((st = input_projection(p, s, *params, x_packed, ga, (char*)workspace + L.xs_off, cs)) != LSTM_OK) return st;
+    if ((st = state_fold_input(p, H, nd, bf16, params->R, sio.h0, ga, sio.scratch, cs)) != LSTM_OK) return st;
+
+    RecArgs a = base_args(p, s, *params, ga, cbuf);
+    a.y = y_packed; a.y_lo = (__nv_bfloat16*)y_lo; a.h_n = h_n; a.c_n = c_n;
+    a.h0 = sio.h0; a.c0 = sio.c0;
+    if (cluster) {
+        a.off_h = cl_layout.off_h; a.off_red = cl_layout.off_red; a.off_contrib = cl_layout.off_contrib;
+        a.off_acc = cl_layout.off_acc; a.off_state = cl_layout.off_state; a.off_sums = cl_layout.off_sums;
+        a.off_peep = cl_layout.off_peep; a.off_tab = cl_layout.off_tab;
+        p.last_rec_kind[0] = 2; p.last_rec_ctas[0] = rcc.G; p.last_rec_mma[0] = 2;
+        p.last_rec_variant[0] = (rcc.bulk ? 1 : 0) | (rcc.tma_pre ? 2 : 0);
+        p.last_rec_groups[0] = rcc.ngroups; p.last_rec_grp_rows[0] = rcc.grp_rows;
+        return rec_cluster_fwd_launch(p, rcc, a, cs);
+    }
+    p.last_rec_kind[0] = 1; p.last_rec_ctas[0] = rc.G; p.last_rec_mma[0] = rc.mma;
+    p.last_rec_groups[0] = 1; p.last_rec_grp_rows[0] = p.B;
+    return rec_launch(p, rc, a, false, cs);
+}
+
+lstm_status bwd_impl(const lstm_plan* plan, const lstm_layer_shape* shape,
+                            const lstm_layer_params* params, const void* x_packed, const float* y_packed,
+                            void* workspace, const float* dy_packed, float* dx_packed,
+                            const lstm_layer_grads* grads, void* scratch, const StateIO& sio, void* stream)
+{
+    if (!plan) return LSTM_ERR_INVALID_ARG;
+    lstm_status st = check_shape(shape);
+    if (st != LSTM_OK) return st;
+    if ((st = check_params(params)) != LSTM_OK) return st;
+    if (!grads || !grads->dW || !grads->dR || !grads->db || !grads->dpeep) return LSTM_ERR_INVALID_ARG;
+    if (!aligned16(grads->dW) || !aligned16(grads->dR) || !aligned16(grads->db) || !aligned16(grads->dpeep))
+        return LSTM_ERR_INVALID_ARG;
+    const Plan& p = plan->p;
+    const lstm_layer_shape& s = *shape;
+    const int H = s.hidden_size, nd = s.num_directions, D = s.input_size;
+    const bool bf16 = s.dtype == LSTM_BF16;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if ((st = check_state(p, sio, (sio.h0 || sio.dh0) && p.rows > 0)) != LSTM_OK) return st;
+    if (p.rows == 0) {
+        LSTM_CUDA_TRY(cudaMemsetAsync(grads->dW, 0, sizeof(float) * nd * 4 * H * D, cs));
+        LSTM_CUDA_TRY(cudaMemsetAsync(grads->dR, 0, sizeof(float) * nd * 4 * H * H, cs));
+        LSTM_CUDA_TRY(cudaMemsetAsync(grads->db, 0, sizeof(float) * nd * 4 * H, cs));
+        LSTM_CUDA_TRY(cudaMemsetAsync(grads->dpeep, 0, sizeof(float) * nd * 3 * H, cs));
+        // every sequence is empty: the final-state errors are the initial-state errors
+        const size_t bytes = sizeof(float) * nd * p.B * H;
+        if (sio.dh0) LSTM_CUDA_TRY(sio.dh_n ? cudaMemcpyAsync(sio.dh0, sio.dh_n, bytes, cudaMemcpyDeviceToDevice, cs)
+                                            : cudaMemsetAsync(sio.dh0, 0, bytes, cs));
+        if (sio.dc0) LSTM_CUDA_TRY(sio.dc_n ? cudaMemcpyAsync(sio.dc0, sio.dc_n, bytes, cudaMemcpyDeviceToDevice, cs)
+                                            : cudaMemsetAsync(sio.dc0, 0, bytes, cs));
+        return LSTM_OK;
+    }
+    if (!x_packed || !y_packed || !workspace || !dy_packed) return LSTM_ERR_INVALID_ARG;
+    if (!aligned16(x_packed) || !aligned16(y_packed) || !aligned16(workspace) || !aligned16(dy_packed) ||
+        (dx_packed && !aligned16(dx_packed)))
+        return LSTM_ERR_INVALID_ARG;
+    const size_t need_scratch = scratch_floats(p, s);
+    if (need_scratch > 0 && (!scratch || !aligned16(scratch))) return LSTM_ERR_INVALID_ARG;
+    const Layout L = workspace_layout(p, s);
+    float* ga = (float*)((char*)workspace + L.ga_off);
+    float* cbuf = (float*)((char*)workspace + L.c_off);
+
+    if (wide_step_path(p, s)) {
+        const StepScratch q = step_scratch(p, s);
+        char* sc = (char*)scratch;
+        if (p.wide_mode != 0 && rec_wide_supported(p, H, nd, bf16)) {
+            // R^T [ndir][H][4H] bf16: the resident B operand of each CTA's R^T da product
+            __nv_bfloat16* rt16 = (__nv_bfloat16*)(sc + q.rt);
+            for (int d = 0; d < nd; ++d)
+                if ((st = transpose_to_bf16_split(p, (const char*)params->R + (size_t)d * 4 * H * H * 2, true, H, 0,
+                                                  nullptr, 4 * H, 4 * H, H, 0, rt16 + (size_t)d * H * 4 * H, 4 * H, 0,
+                                                  nullptr, 0, 0, cs)) != LSTM_OK)
+                    return st;
+            WideArgs w = wide_args(p, s, *params, ga, cbuf, sio);
+            w.dy = dy_packed;
+            w.xbuf = (__nv_bfloat16*)(sc + q.dab);
+            p.last_rec_kind[1] = 4; p.last_rec_ctas[1] = H / 16; p.last_rec_mma[1] = 2; p.last_rec_variant[1] = 0;
+            p.last_rec_groups[1] = 1; p.last_rec_grp_rows[1] = p.B;
+            st = rec_wide_bwd_launch(p, w, rt16, (float*)scratch, grads->db, grads->dpeep, cs);
+            if (st == LSTM_OK) {
+                if ((st = bwd_products(p, s, *params, x_packed, y_packed, ga, dx_packed, *grads, scratch, cs)) != LSTM_OK)
+                    return st;
+                return sio.any() ? state_backward(p, H, nd, bf16, params->R, ga, sio.h0, sio.dh_n, sio.dc_n, sio.dh0,
+                                                  sio.dc0, grads->dR, sio.scratch, cs)
+                                 : LSTM_OK;
+            }
+            if (st != LSTM_ERR_UNSUPPORTED) return st;   // not co-schedulable: per-step launches below
+        }
+        p.last_rec_kind[1] = 3; p.last_rec_ctas[1] = 0; p.last_rec_mma[1] = 2; p.last_rec_variant[1] = 0;
+        p.last_rec_groups[1] = 1; p.last_rec_grp_rows[1] = p.B;
+        if ((st = stepwise_bwd_core(p, s, *params, x_packed, y_packed, ga, cbuf, dy_packed, dx_packed, *grads, scratch,
+                                    (float*)(sc + q.dh), (float*)(sc + q.dcc), (__nv_bfloat16*)(sc + q.dab),
+                                    (__nv_bfloat16*)(sc + q.rt), cs, sio)) != LSTM_OK)
+            return st;
+        return sio.any() ? state_backward(p, H, nd, bf16, params->R, ga, sio.h0, sio.dh_n, sio.dc_n, sio.dh0, sio.dc0,
+                                          grads->dR, sio.scratch, cs)
+                         : LSTM_OK;
+    }
+    RecConfig rc, rcc;
+    RecArgs cl_layout;
+    memset(&cl_layout, 0, sizeof(cl_layout));
+    const bool cluster = rec_cluster_bwd_configure(p, H, nd, bf16, &rcc, &cl_layout);
+    if (!cluster && (st = rec_configure(p, H, nd, bf16, true, p.forced_ctas, &rc)) != LSTM_OK) return st;
+    RecArgs a = base_args(p, s, *params, ga, cbuf);
+    a.y = const_cast<float*>(y_packed); a.dy = dy_packed; a.db = grads->db; a.dpeep = grads->dpeep;
+    a.part = (float*)scratch;
+    a.c0 = sio.c0; a.dh_n = sio.dh_n; a.dc_n = sio.dc_n; a.dc0 = sio.dc0;
+    if (cluster) {
+        a.off_h = cl_layout.off_h; a.off_red = cl_layout.off_red; a.off_contrib = cl_layout.off_contrib;
+        a.off_acc = cl_layout.off_acc; a.off_state = cl_layout.off_state; a.off_sums = cl_layout.off_sums;
+        a.off_peep = cl_layout.off_peep; a.off_tab = cl_layout.off_tab;
+        p.last_rec_kind[1] = 2; p.last_rec_ctas[1] = rcc.G; p.last_rec_mma[1] = 2;
+        p.last_rec_variant[1] = (rcc.bulk ? 1 : 0) | (rcc.tma_pre ? 2 : 0);
+        p.last_rec_groups[1] = rcc.ngroups; p.last_rec_grp_rows[1] = rcc.grp_rows;
+        if ((st = rec_cluster_bwd_launch(p, rcc, a, (float*)scratch, cs)) != LSTM_OK) return st;
+    } else {
+        p.last_rec_kind[1] = 1; p.last_rec_ctas[1] = rc.G; p.last_rec_mma[1] = rc.mma; p.last_rec_variant[1] = 0;
+        p.last_rec_groups[1] = 1; p.last_rec_grp_rows[1] = p.B;
+        if ((st = rec_launch(p, rc, a, true, cs)) != LSTM_OK) return st;
+    }
+
+    if ((st = bwd_products(p, s, *params, x_packed, y_packed, ga, dx_packed, *grads, scratch, cs)) != LSTM_OK)
+        return st;
+    return sio.any() ? state_backward(p, H, nd, bf16, params->R, ga, sio.h0, sio.dh_n, sio.dc_n, sio.dh0, sio.dc0,
+                                      grads->dR, sio.scratch, cs)
+                     : LSTM_OK;
 }
 
 }  // namespace
@@ -518,59 +744,7 @@ lstm_status lstm_fwd(const lstm_plan* plan, const lstm_layer_shape* shape,
                      const lstm_layer_params* params, const void* x_packed, float* y_packed,
                      void* y_lo, float* h_n, float* c_n, void* workspace, void* stream)
 {
-    if (!plan) return LSTM_ERR_INVALID_ARG;
-    lstm_status st = check_shape(shape);
-    if (st != LSTM_OK) return st;
-    if ((st = check_params(params)) != LSTM_OK) return st;
-    const Plan& p = plan->p;
-    const lstm_layer_shape& s = *shape;
-    const int H = s.hidden_size, nd = s.num_directions;
-    const bool bf16 = s.dtype == LSTM_BF16;
-    cudaStream_t cs = (cudaStream_t)stream;
-    if ((h_n && !aligned16(h_n)) || (c_n && !aligned16(c_n))) return LSTM_ERR_INVALID_ARG;
-    if (p.rows == 0) {
-        if (h_n) LSTM_CUDA_TRY(cudaMemsetAsync(h_n, 0, sizeof(float) * nd * p.B * H, cs));
-        if (c_n) LSTM_CUDA_TRY(cudaMemsetAsync(c_n, 0, sizeof(float) * nd * p.B * H, cs));
-        return LSTM_OK;
-    }
-    if (!x_packed || !y_packed || !workspace) return LSTM_ERR_INVALID_ARG;
-    if (!aligned16(x_packed) || !aligned16(y_packed) || !aligned16(workspace) || (y_lo && !aligned16(y_lo)))
-        return LSTM_ERR_INVALID_ARG;
-    const Layout L = workspace_layout(p, s);
-    float* ga = (float*)((char*)workspace + L.ga_off);
-    float* cbuf = (float*)((char*)workspace + L.c_off);
-
-    if (wide_step_path(p, s)) {
-        if ((st = input_projection(p, s, *params, x_packed, ga, (char*)workspace + L.xs_off, cs)) != LSTM_OK)
-            return st;
-        p.last_rec_kind[0] = 3; p.last_rec_ctas[0] = 0; p.last_rec_mma[0] = 2; p.last_rec_variant[0] = 0;
-        p.last_rec_groups[0] = 1; p.last_rec_grp_rows[0] = p.B;
-        return stepwise_fwd_core(p, s, *params, y_packed, y_lo, h_n, c_n, ga, cbuf,
-                                 (float*)((char*)workspace + L.rh_off), (__nv_bfloat16*)((char*)workspace + L.hb_off),
-                                 cs);
-    }
-    RecConfig rc, rcc;
-    RecArgs cl_layout;
-    memset(&cl_layout, 0, sizeof(cl_layout));
-    const bool cluster = rec_cluster_fwd_configure(p, H, nd, bf16, &rcc, &cl_layout);
-    if (!cluster && (st = rec_configure(p, H, nd, bf16, false, p.forced_ctas, &rc)) != LSTM_OK) return st;
-
-    if ((st = input_projection(p, s, *params, x_packed, ga, (char*)workspace + L.xs_off, cs)) != LSTM_OK) return st;
-
-    RecArgs a = base_args(p, s, *params, ga, cbuf);
-    a.y = y_packed; a.y_lo = (__nv_bfloat16*)y_lo; a.h_n = h_n; a.c_n = c_n;
-    if (cluster) {
-        a.off_h = cl_layout.off_h; a.off_red = cl_layout.off_red; a.off_contrib = cl_layout.off_contrib;
-        a.off_acc = cl_layout.off_acc; a.off_state = cl_layout.off_state; a.off_sums = cl_layout.off_sums;
-        a.off_peep = cl_layout.off_peep; a.off_tab = cl_layout.off_tab;
-        p.last_rec_kind[0] = 2; p.last_rec_ctas[0] = rcc.G; p.last_rec_mma[0] = 2;
-        p.last_rec_variant[0] = (rcc.bulk ? 1 : 0) | (rcc.tma_pre ? 2 : 0);
-        p.last_rec_groups[0] = rcc.ngroups; p.last_rec_grp_rows[0] = rcc.grp_rows;
-        return rec_cluster_fwd_launch(p, rcc, a, cs);
-    }
-    p.last_rec_kind[0] = 1; p.last_rec_ctas[0] = rc.G; p.last_rec_mma[0] = rc.mma;
-    p.last_rec_groups[0] = 1; p.last_rec_grp_rows[0] = p.B;
-    return rec_launch(p, rc, a, false, cs);
+    return fwd_impl(plan, shape, params, x_packed, y_packed, y_lo, h_n, c_n, workspace, StateIO(), stream);
 }
 
 lstm_status lstm_bwd(const lstm_plan* plan, const lstm_layer_shape* shape,
@@ -578,67 +752,41 @@ lstm_status lstm_bwd(const lstm_plan* plan, const lstm_layer_shape* shape,
                      void* workspace, const float* dy_packed, float* dx_packed,
                      const lstm_layer_grads* grads, void* scratch, void* stream)
 {
-    if (!plan) return LSTM_ERR_INVALID_ARG;
-    lstm_status st = check_shape(shape);
-    if (st != LSTM_OK) return st;
-    if ((st = check_params(params)) != LSTM_OK) return st;
-    if (!grads || !grads->dW || !grads->dR || !grads->db || !grads->dpeep) return LSTM_ERR_INVALID_ARG;
-    if (!aligned16(grads->dW) || !aligned16(grads->dR) || !aligned16(grads->db) || !aligned16(grads->dpeep))
-        return LSTM_ERR_INVALID_ARG;
-    const Plan& p = plan->p;
-    const lstm_layer_shape& s = *shape;
-    const int H = s.hidden_size, nd = s.num_directions, D = s.input_size;
-    const bool bf16 = s.dtype == LSTM_BF16;
-    cudaStream_t cs = (cudaStream_t)stream;
-    if (p.rows == 0) {
-        LSTM_CUDA_TRY(cudaMemsetAsync(grads->dW, 0, sizeof(float) * nd * 4 * H * D, cs));
-        LSTM_CUDA_TRY(cudaMemsetAsync(grads->dR, 0, sizeof(float) * nd * 4 * H * H, cs));
-        LSTM_CUDA_TRY(cudaMemsetAsync(grads->db, 0, sizeof(float) * nd * 4 * H, cs));
-        LSTM_CUDA_TRY(cudaMemsetAsync(grads->dpeep, 0, sizeof(float) * nd * 3 * H, cs));
-        return LSTM_OK;
-    }
-    if (!x_packed || !y_packed || !workspace || !dy_packed) return LSTM_ERR_INVALID_ARG;
-    if (!aligned16(x_packed) || !aligned16(y_packed) || !aligned16(workspace) || !aligned16(dy_packed) ||
-        (dx_packed && !aligned16(dx_packed)))
-        return LSTM_ERR_INVALID_ARG;
-    const size_t need_scratch = scratch_floats(p, s);
-    if (need_scratch > 0 && (!scratch || !aligned16(scratch))) return LSTM_ERR_INVALID_ARG;
-    const Layout L = workspace_layout(p, s);
-    float* ga = (float*)((char*)workspace + L.ga_off);
-    float* cbuf = (float*)((char*)workspace + L.c_off);
+    return bwd_impl(plan, shape, params, x_packed, y_packed, workspace, dy_packed, dx_packed, grads, scratch,
+                    StateIO(), stream);
+}
 
-    if (wide_step_path(p, s)) {
-        const StepScratch q = step_scratch(p, s);
-        char* sc = (char*)scratch;
-        p.last_rec_kind[1] = 3; p.last_rec_ctas[1] = 0; p.last_rec_mma[1] = 2; p.last_rec_variant[1] = 0;
-        p.last_rec_groups[1] = 1; p.last_rec_grp_rows[1] = p.B;
-        return stepwise_bwd_core(p, s, *params, x_packed, y_packed, ga, cbuf, dy_packed, dx_packed, *grads, scratch,
-                                 (float*)(sc + q.dh), (float*)(sc + q.dcc), (__nv_bfloat16*)(sc + q.dab),
-                                 (__nv_bfloat16*)(sc + q.rt), cs);
-    }
-    RecConfig rc, rcc;
-    RecArgs cl_layout;
-    memset(&cl_layout, 0, sizeof(cl_layout));
-    const bool cluster = rec_cluster_bwd_configure(p, H, nd, bf16, &rcc, &cl_layout);
-    if (!cluster && (st = rec_configure(p, H, nd, bf16, true, p.forced_ctas, &rc)) != LSTM_OK) return st;
-    RecArgs a = base_args(p, s, *params, ga, cbuf);
-    a.y = const_cast<float*>(y_packed); a.dy = dy_packed; a.db = grads->db; a.dpeep = grads->dpeep;
-    a.part = (float*)scratch;
-    if (cluster) {
-        a.off_h = cl_layout.off_h; a.off_red = cl_layout.off_red; a.off_contrib = cl_layout.off_contrib;
-        a.off_acc = cl_layout.off_acc; a.off_state = cl_layout.off_state; a.off_sums = cl_layout.off_sums;
-        a.off_peep = cl_layout.off_peep; a.off_tab = cl_layout.off_tab;
-        p.last_rec_kind[1] = 2; p.last_rec_ctas[1] = rcc.G; p.last_rec_mma[1] = 2;
-        p.last_rec_variant[1] = (rcc.bulk ? 1 : 0) | (rcc.tma_pre ? 2 : 0);
-        p.last_rec_groups[1] = rcc.ngroups; p.last_rec_grp_rows[1] = rcc.grp_rows;
-        if ((st = rec_cluster_bwd_launch(p, rcc, a, (float*)scratch, cs)) != LSTM_OK) return st;
-    } else {
-        p.last_rec_kind[1] = 1; p.last_rec_ctas[1] = rc.G; p.last_rec_mma[1] = rc.mma; p.last_rec_variant[1] = 0;
-        p.last_rec_groups[1] = 1; p.last_rec_grp_rows[1] = p.B;
-        if ((st = rec_launch(p, rc, a, true, cs)) != LSTM_OK) return st;
-    }
+size_t lstm_state_scratch_bytes(const lstm_plan* plan, const lstm_layer_shape* shape)
+{
+    if (!plan || check_shape(shape) != LSTM_OK) return 0;
+    return align256(std::max<size_t>(1, state_scratch_floats(plan->p, shape->hidden_size, shape->num_directions)) *
+                    sizeof(float));
+}
 
-    return bwd_products(p, s, *params, x_packed, y_packed, ga, dx_packed, *grads, scratch, cs);
+lstm_status lstm_fwd_state(const lstm_plan* plan, const lstm_layer_shape* shape, const lstm_layer_params* params,
+                           const lstm_state* state, const void* x_packed, float* y_packed, void* y_lo, float* h_n,
+                           float* c_n, void* workspace, void* state_scratch, void* stream)
+{
+    StateIO sio;
+    if (state) { sio.h0 = state->h0; sio.c0 = state->c0; }
+    sio.scratch = (float*)state_scratch;
+    return fwd_impl(plan, shape, params, x_packed, y_packed, y_lo, h_n, c_n, workspace, sio, stream);
+}
+
+lstm_status lstm_bwd_state(const lstm_plan* plan, const lstm_layer_shape* shape, const lstm_layer_params* params,
+                           const lstm_state* state, const void* x_packed, const float* y_packed, void* workspace,
+                           const float* dy_packed, float* dx_packed, const lstm_layer_grads* grads,
+                           const lstm_state_grads* state_grads, void* scratch, void* state_scratch, void* stream)
+{
+    StateIO sio;
+    if (state) { sio.h0 = state->h0; sio.c0 = state->c0; }
+    if (state_grads) {
+        sio.dh_n = state_grads->dh_n; sio.dc_n = state_grads->dc_n;
+        sio.dh0 = state_grads->dh0; sio.dc0 = state_grads->dc0;
+    }
+    sio.scratch = (float*)state_scratch;
+    return bwd_impl(plan, shape, params, x_packed, y_packed, workspace, dy_packed, dx_packed, grads, scratch, sio,
+                    stream);
 }
 
 size_t lstm_stepwise_scratch_bytes(const lstm_plan* plan, const lstm_layer_shape* shape)

@@ -46,6 +46,8 @@ struct Plan {
     int32_t forced_ctas = 0;        // 0 = automatic
     int32_t forced_variant = -1;    // cluster kernels: -1 automatic, else bit 0 bulk exchange, bit 1 TMA tiles
     int32_t forced_group_rows = 0;  // cluster kernels: sorted slots per sequence group (0 = automatic)
+    int32_t wide_mode = -1;         // bf16 layers wider than a cluster: -1 automatic, 0 per-step launches,
+                                    // 1 the persistent kernel where it applies
     int32_t gemm_engine = 0;        // 0 = tensor cores for bf16 operands, 1 = CUDA cores
     int device = 0;
     int num_sms = 0;
@@ -64,6 +66,7 @@ struct Plan {
     int32_t* d_prev_fwd = nullptr;  // [rows] row holding h_{t-1} for the forward direction (-1 none)
     int32_t* d_prev_rev = nullptr;  // [rows] row holding the reverse direction's previous state
     int32_t* d_row_slot = nullptr;  // [rows] sorted slot j of packed row (row off[t] + j)
+    int32_t* d_row_dst = nullptr;   // segment / window plans: [rows] caller frame unpack writes (-1 none)
     unsigned* d_flags = nullptr;    // [2 * kMaxCtasPerDir] step counters
     DeviceStatus* d_status = nullptr;
     Tracer* tracer = nullptr;       // owned; mutable through const plans

@@ -24,6 +24,7 @@ struct GemmDesc {
     const float* bias = nullptr;
     int round_bf16 = 0;       // round fp32 operands to bf16 before multiplying
     int k_splits = 1;
+    int accumulate = 0;       // C += result instead of C = result (taken unsplit)
     float* partial = nullptr;
 };
 
@@ -81,6 +82,11 @@ lstm_status gemm_tc_pair(const Plan& p, int kind, const TcOperands& o0, int M0, 
 // TMA-addressable (16-byte aligned base, pitch and box row).
 bool make_map_f32(CUtensorMap* map, const float* ptr, int64_t rows, int64_t cols, int64_t ld, int box_cols,
                   int box_rows);
+
+// TMA map of a row-major bf16 matrix [rows][cols] (row pitch ld elements) in boxes of 64
+// columns x box_rows rows with the 128-byte swizzle (the K-major operand layout of
+// tc::sdesc_sw128); out-of-range elements read 0.
+bool make_map_bf16_sw128(CUtensorMap* map, const void* ptr, int rows, int cols, int64_t ld, int box_rows);
 
 // The same with a padded row range (rows in [rows, rows_pad) written as 0)
 // and an fp32 split into three bf16 pieces v0 + v1 + v2 written as six K

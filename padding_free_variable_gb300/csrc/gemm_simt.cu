@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(GemmDesc d, int k_ch
             if (gn >= d.N) continue;
             float v = acc[i][j];
             if (!split && d.bias) v += __ldg(d.bias + gn);
+            if (!split && d.accumulate) v += out[(int64_t)gm * ldo + gn];
             out[(int64_t)gm * ldo + gn] = v;
         }
     }
@@ -179,7 +180,7 @@ cudaError_t splitk_reduce(const float* partial, int splits, int M, int N, float*
 
 int gemm_choose_splits(const GemmDesc& d, int num_sms)
 {
-    if (d.k_splits <= 1) return 1;
+    if (d.k_splits <= 1 || d.accumulate) return 1;
     const int tiles = ((d.N + BN - 1) / BN) * ((d.M + BM - 1) / BM);
     int splits = (2 * num_sms + tiles - 1) / tiles;
     const int max_by_k = (d.K + 255) / 256;
@@ -208,6 +209,7 @@ lstm_status gemm_simt_run(const GemmDesc& d, int num_sms, cudaStream_t s)
 {
     const int splits = gemm_choose_splits(d, num_sms);
     if (d.K <= 0) {
+        if (d.accumulate) return LSTM_OK;             // C += 0
         // empty reduction: C = bias (or 0)
         GemmDesc z = d;
         z.k_splits = 1;

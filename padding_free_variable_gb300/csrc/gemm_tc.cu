@@ -457,6 +457,11 @@ bool make_map(CUtensorMap* map, const void* ptr, int rows, int cols, int64_t ld,
 
 }  // namespace
 
+bool make_map_bf16_sw128(CUtensorMap* map, const void* ptr, int rows, int cols, int64_t ld, int box_rows)
+{
+    return ((uintptr_t)ptr & 15u) == 0 && (ld * 2) % 16 == 0 && make_map(map, ptr, rows, cols, ld, box_rows);
+}
+
 bool make_map_f32(CUtensorMap* map, const float* ptr, int64_t rows, int64_t cols, int64_t ld, int box_cols,
                   int box_rows)
 {

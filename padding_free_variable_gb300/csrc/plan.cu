@@ -51,8 +51,11 @@ lstm_status launch_pack(const Plan& p, const void* src, int width, int elem_byte
     const int64_t cap = (int64_t)p.num_sms * 8;
     if (blocks > cap) blocks = cap;
     trace_begin(p, unpack ? K_UNPACK : K_PACK, s);
-    pack_rows_kernel<<<(unsigned)blocks, threads, 0, s>>>((const uint4*)src, (uint4*)dst,
-                                                          p.d_row_src, p.rows, vecs, unpack ? 1 : 0);
+    // segment and window plans unpack through their own map (frames that several segments
+    // read are written back by the one segment that owns them)
+    const int32_t* map = unpack && p.d_row_dst ? p.d_row_dst : p.d_row_src;
+    pack_rows_kernel<<<(unsigned)blocks, threads, 0, s>>>((const uint4*)src, (uint4*)dst, map, p.rows, vecs,
+                                                          unpack ? 1 : 0);
     trace_end(p, unpack ? K_UNPACK : K_PACK, s, 1);
     return cudaGetLastError() == cudaSuccess ? LSTM_OK : LSTM_ERR_CUDA;
 }
@@ -113,6 +116,7 @@ static void free_plan(Plan& p)
     free(p.h_bs); free(p.h_off); free(p.h_perm); free(p.h_len); free(p.h_cstart);
     cudaFree(p.d_bs); cudaFree(p.d_off); cudaFree(p.d_perm); cudaFree(p.d_len);
     cudaFree(p.d_row_src); cudaFree(p.d_prev_fwd); cudaFree(p.d_prev_rev); cudaFree(p.d_row_slot);
+    cudaFree(p.d_row_dst);
     cudaFree(p.d_flags); cudaFree(p.d_status);
     p = Plan();
 }
@@ -181,7 +185,17 @@ static lstm_status compute_tables(const int32_t* lengths, int32_t B, bool padded
     return LSTM_OK;
 }
 
-static lstm_status create_plan(const int32_t* lengths, int32_t B, bool padded, lstm_plan** out)
+// Frame map of a plan whose units are pieces of the caller's sequences (segments, windows):
+// unit u covers caller frames src_start[u] .. + length - 1; unpack writes back only its first
+// own_len[u] frames; the caller's tensors have `frames` rows.
+struct FrameMap {
+    const int32_t* src_start = nullptr;
+    const int32_t* own_len = nullptr;
+    int64_t frames = 0;
+};
+
+static lstm_status create_plan(const int32_t* lengths, int32_t B, bool padded, lstm_plan** out,
+                               const FrameMap* fm = nullptr)
 {
     if (!out) return LSTM_ERR_INVALID_ARG;
     *out = nullptr;
@@ -190,6 +204,7 @@ static lstm_status create_plan(const int32_t* lengths, int32_t B, bool padded, l
     lstm_status st = compute_tables(lengths, B, padded, &T, &rows, &frames, nullptr, nullptr, nullptr,
                                     nullptr, nullptr, nullptr, nullptr, nullptr);
     if (st != LSTM_OK) return st;
+    if (fm) frames = fm->frames;
 
     lstm_plan* hp = new lstm_plan();
     Plan& p = hp->p;
@@ -206,15 +221,26 @@ static lstm_status create_plan(const int32_t* lengths, int32_t B, bool padded, l
     p.h_perm = (int32_t*)malloc(sizeof(int32_t) * B);
     p.h_len = (int32_t*)malloc(sizeof(int32_t) * B);
     p.h_cstart = (int32_t*)malloc(sizeof(int32_t) * (B + 1));
-    std::vector<int32_t> row_src(rows), prev_fwd(rows), prev_rev(rows);
+    std::vector<int32_t> row_src(rows), prev_fwd(rows), prev_rev(rows), row_dst;
     compute_tables(lengths, B, padded, nullptr, nullptr, nullptr, p.h_bs, p.h_off, p.h_perm, p.h_len,
                    p.h_cstart, row_src.data(), prev_fwd.data(), prev_rev.data());
+    if (fm) {   // rows read (and write back) the caller's frames through the frame map
+        row_dst.resize(rows);
+        for (int t = 0; t < T; ++t)
+            for (int j = 0; j < p.h_bs[t]; ++j) {
+                const int64_t r = (int64_t)p.h_off[t] + j;
+                const int u = p.h_perm[j];
+                row_src[r] = fm->src_start[u] + t;
+                row_dst[r] = t < fm->own_len[u] ? fm->src_start[u] + t : -1;
+            }
+    }
     cudaError_t e = cudaSuccess;
     if (e == cudaSuccess) e = upload(&p.d_bs, p.h_bs, (size_t)T);
     if (e == cudaSuccess) e = upload(&p.d_off, p.h_off, (size_t)T + 1);
     if (e == cudaSuccess) e = upload(&p.d_perm, p.h_perm, (size_t)B);
     if (e == cudaSuccess) e = upload(&p.d_len, p.h_len, (size_t)B);
     if (e == cudaSuccess) e = upload(&p.d_row_src, row_src.data(), (size_t)rows);
+    if (e == cudaSuccess && fm) e = upload(&p.d_row_dst, row_dst.data(), (size_t)rows);
     if (e == cudaSuccess) e = upload(&p.d_prev_fwd, prev_fwd.data(), (size_t)rows);
     if (e == cudaSuccess) e = upload(&p.d_prev_rev, prev_rev.data(), (size_t)rows);
     {   // sorted slot of each packed row (row off[t] + j holds slot j)
@@ -236,6 +262,35 @@ static lstm_status create_plan(const int32_t* lengths, int32_t B, bool padded, l
     return LSTM_OK;
 }
 
+// Segments of RETURNN-style chunking (RETURNN paper, Sec. 4: sequences cut into possibly
+// overlapping segments of constant length, each then trained as a sequence of its own):
+// sequence b yields segments starting at 0, step, 2 step, ... of min(chunk, L_b - start)
+// frames, up to the first segment that reaches the sequence's end; an empty sequence yields
+// one empty segment.  Segment u owns (unpacks) its frames up to the next segment's start.
+static lstm_status make_segments(const int32_t* lengths, int32_t B, int32_t chunk, int32_t step,
+                                 std::vector<int32_t>* seq, std::vector<int32_t>* start, std::vector<int32_t>* len,
+                                 std::vector<int32_t>* own, int64_t* frames)
+{
+    if (!lengths || B < 1 || chunk < 1 || step < 1 || step > chunk) return LSTM_ERR_INVALID_ARG;
+    int64_t f = 0;
+    for (int32_t b = 0; b < B; ++b) {
+        if (lengths[b] < 0) return LSTM_ERR_INVALID_ARG;
+        const int32_t L = lengths[b];
+        for (int32_t s0 = 0;; s0 += step) {
+            const int32_t e = std::min(s0 + chunk, L);
+            seq->push_back(b);
+            start->push_back(s0);
+            len->push_back(std::max(0, e - s0));
+            own->push_back(e == L ? std::max(0, e - s0) : step);
+            if (e >= L) break;
+        }
+        f += L;
+    }
+    if (f > INT32_MAX || seq->size() > (size_t)INT32_MAX) return LSTM_ERR_INVALID_ARG;
+    *frames = f;
+    return LSTM_OK;
+}
+
 }  // namespace lstm
 
 using lstm::Plan;
@@ -250,6 +305,80 @@ lstm_status lstm_plan_create(const int32_t* lengths_host, int32_t B, lstm_plan**
 lstm_status lstm_plan_create_padded(const int32_t* lengths_host, int32_t B, lstm_plan** out)
 {
     return lstm::create_plan(lengths_host, B, true, out);
+}
+
+lstm_status lstm_segments_host(const int32_t* lengths_host, int32_t B, int32_t chunk, int32_t step,
+                               int32_t* num_segments, int32_t* seg_seq, int32_t* seg_start, int32_t* seg_len,
+                               int32_t capacity)
+{
+    std::vector<int32_t> seq, start, len, own;
+    int64_t frames = 0;
+    const lstm_status st = lstm::make_segments(lengths_host, B, chunk, step, &seq, &start, &len, &own, &frames);
+    if (st != LSTM_OK) return st;
+    const int32_t n = (int32_t)seq.size();
+    if (num_segments) *num_segments = n;
+    if (!seg_seq && !seg_start && !seg_len) return LSTM_OK;
+    if (capacity < n) return LSTM_ERR_INVALID_ARG;
+    for (int32_t u = 0; u < n; ++u) {
+        if (seg_seq) seg_seq[u] = seq[u];
+        if (seg_start) seg_start[u] = start[u];
+        if (seg_len) seg_len[u] = len[u];
+    }
+    return LSTM_OK;
+}
+
+lstm_status lstm_plan_create_segments(const int32_t* lengths_host, int32_t B, int32_t chunk, int32_t step,
+                                      lstm_plan** out)
+{
+    std::vector<int32_t> seq, start, len, own;
+    int64_t frames = 0;
+    lstm_status st = lstm::make_segments(lengths_host, B, chunk, step, &seq, &start, &len, &own, &frames);
+    if (st != LSTM_OK) return st;
+    std::vector<int32_t> cst(B + 1, 0), src(seq.size());
+    for (int32_t b = 0; b < B; ++b) cst[b + 1] = cst[b] + lengths_host[b];
+    for (size_t u = 0; u < seq.size(); ++u) src[u] = cst[seq[u]] + start[u];
+    lstm::FrameMap fm;
+    fm.src_start = src.data(); fm.own_len = own.data(); fm.frames = frames;
+    return lstm::create_plan(len.data(), (int32_t)len.size(), false, out, &fm);
+}
+
+lstm_status lstm_plan_create_window(const int32_t* lengths_host, int32_t B, int32_t start, int32_t width,
+                                    lstm_plan** out)
+{
+    if (!lengths_host || B < 1 || start < 0 || width < 1) return LSTM_ERR_INVALID_ARG;
+    std::vector<int32_t> len(B), src(B);
+    int64_t frames = 0;
+    for (int32_t b = 0; b < B; ++b) {
+        if (lengths_host[b] < 0) return LSTM_ERR_INVALID_ARG;
+        len[b] = std::max(0, std::min(lengths_host[b] - start, width));
+        src[b] = (int32_t)frames + std::min(start, lengths_host[b]);
+        frames += lengths_host[b];
+    }
+    if (frames > INT32_MAX) return LSTM_ERR_INVALID_ARG;
+    lstm::FrameMap fm;
+    fm.src_start = src.data(); fm.own_len = len.data(); fm.frames = frames;
+    return lstm::create_plan(len.data(), B, false, out, &fm);
+}
+
+lstm_status lstm_form_batches(const int32_t* lengths_host, int32_t n, int64_t budget, int32_t budget_kind,
+                              int32_t* batch_of, int32_t* num_batches)
+{
+    if (n < 0 || (n > 0 && (!lengths_host || !batch_of)) || budget < 1 || (budget_kind != 0 && budget_kind != 1))
+        return LSTM_ERR_INVALID_ARG;
+    int32_t b = 0, count = 0, longest = 0;
+    int64_t sum = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t L = lengths_host[i];
+        if (L < 0) return LSTM_ERR_INVALID_ARG;
+        const int64_t size = budget_kind == 0 ? sum + L : (int64_t)(count + 1) * std::max(longest, L);
+        if (count > 0 && size > budget) { ++b; count = 0; sum = 0; longest = 0; }
+        batch_of[i] = b;
+        ++count;
+        sum += L;
+        longest = std::max(longest, L);
+    }
+    if (num_batches) *num_batches = n > 0 ? b + 1 : 0;
+    return LSTM_OK;
 }
 
 lstm_status lstm_plan_dims(const int32_t* lengths_host, int32_t B, int32_t padded, int32_t* steps,
@@ -348,6 +477,13 @@ lstm_status lstm_plan_recurrent_groups(const lstm_plan* plan, int32_t pass, int3
     if (!plan || pass < 0 || pass > 1) return LSTM_ERR_INVALID_ARG;
     if (groups) *groups = plan->p.last_rec_groups[pass];
     if (slots_per_group) *slots_per_group = plan->p.last_rec_grp_rows[pass];
+    return LSTM_OK;
+}
+
+lstm_status lstm_debug_wide_recurrence(lstm_plan* plan, int32_t mode)
+{
+    if (!plan || mode < -1 || mode > 1) return LSTM_ERR_INVALID_ARG;
+    plan->p.wide_mode = mode;
     return LSTM_OK;
 }
 

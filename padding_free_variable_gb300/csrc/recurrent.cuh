@@ -84,6 +84,43 @@ size_t rec_cluster_bwd_sum_floats(int H, int ndir);
 lstm_status rec_cluster_bwd_launch(const Plan& p, const RecConfig& c, RecArgs a, float* sum_scratch,
                                    cudaStream_t s);
 
+// Persistent kernels of bf16 layers wider than a cluster (recurrent_wide.cu): H/16 CTAs per
+// direction, each holding its slice of R (forward) or R^T (backward) in shared memory; the
+// previous step's operand (bf16 h, or bf16 gate errors) is exchanged through a double-
+// buffered global array read back with TMA; a bounded grid barrier per step.
+struct WideArgs {
+    int T, B, H, ndir, NC;                 // NC: CTAs per direction (set by the launchers)
+    int padded;
+    const int32_t* bs;
+    const int32_t* off;
+    const int32_t* len;
+    const int32_t* perm;
+    float* ga;                             // [rows][ndir*4H] pre-activations -> gates -> gate errors
+    const float* peep;
+    float* y;                              // forward
+    __nv_bfloat16* y_lo;                   // forward, optional
+    float* cbuf;
+    float* h_n;                            // forward, optional
+    float* c_n;
+    const float* dy;                       // backward
+    const float* h0;                       // initial states and final-state errors (optional)
+    const float* c0;
+    const float* dh_n;
+    const float* dc_n;
+    float* dc0;
+    __nv_bfloat16* xbuf;                   // forward [ndir][2][B][H], backward [ndir][2][B][4H] bf16
+    unsigned* ctr;                         // [ndir] step counters (set by the launchers)
+    DeviceStatus* status;
+    unsigned long long wait_limit_ns;
+};
+
+bool rec_wide_supported(const Plan& p, int H, int ndir, bool bf16);
+size_t rec_wide_xbuf_bytes(const Plan& p, int H, int ndir, bool bwd);
+lstm_status rec_wide_fwd_launch(const Plan& p, WideArgs a, const void* R, cudaStream_t s);
+// RT: R^T as [ndir][H][4H] bf16.  Runs the db / dpeep sums after the kernel.
+lstm_status rec_wide_bwd_launch(const Plan& p, WideArgs a, const void* RT, float* sum_scratch, float* db,
+                                float* dpeep, cudaStream_t s);
+
 // Floats of the backward kernel's partial-product exchange buffer.
 size_t rec_bwd_part_floats(const Plan& p, int H, int ndir, bool bf16, int forced_G);
 
@@ -91,6 +128,6 @@ size_t rec_bwd_part_floats(const Plan& p, int H, int ndir, bool bf16, int forced
 // a fixed row-chunk order (bitwise repeatable); sum_scratch holds
 // rec_cluster_bwd_sum_floats(H, ndir) floats.
 lstm_status param_sums_launch(const Plan& p, const float* ga, const float* cbuf, int H, int ndir, float* db,
-                              float* dpeep, float* sum_scratch, cudaStream_t s);
+                              float* dpeep, float* sum_scratch, cudaStream_t s, const float* c0 = nullptr);
 
 }  // namespace lstm

@@ -1283,9 +1283,12 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
 // db and dpeep from the gate errors: column (direction, quantity q, unit u),
 // q = 0..3 -> sum of da_q, 4 -> da_i c_{t-1}, 5 -> da_f c_{t-1}, 6 -> da_o c_t;
 // each thread sums its column over one chunk of rows in row order, and the
-// chunks are then added in chunk order (bitwise repeatable).
+// chunks are then added in chunk order (bitwise repeatable).  c_{t-1} of a
+// sequence's first step is its initial state c0 (zero when c0 is null).
 __global__ void lstm_param_sums_kernel(const float* __restrict__ ga, const float* __restrict__ cbuf,
                                        const int32_t* __restrict__ prev_fwd, const int32_t* __restrict__ prev_rev,
+                                       const float* __restrict__ c0, const int32_t* __restrict__ row_slot,
+                                       const int32_t* __restrict__ perm, int B,
                                        int rows, int H, int ndir, int chunk, float* __restrict__ partial)
 {
     const int ncols = ndir * 7 * H;
@@ -1302,7 +1305,9 @@ __global__ void lstm_param_sums_kernel(const float* __restrict__ ga, const float
         if (q < 4) s += v;
         else if (q < 6) {
             const int pr = __ldg(prev + r);
-            s += pr >= 0 ? v * __ldg(cbuf + (size_t)pr * ndH + d * H + u) : 0.f;
+            const float cp = pr >= 0 ? __ldg(cbuf + (size_t)pr * ndH + d * H + u)
+                           : c0 ? __ldg(c0 + ((size_t)d * B + __ldg(perm + __ldg(row_slot + r))) * H + u) : 0.f;
+            s += v * cp;
         } else {
             s += v * __ldg(cbuf + (size_t)r * ndH + d * H + u);
         }
@@ -1584,7 +1589,7 @@ lstm_status rec_cluster_bwd_launch(const Plan& p, const RecConfig& c, RecArgs a,
     lstm_status st = cluster_launch(c, fn, args, a.ndir, s);
     int launched = st == LSTM_OK ? 1 : 0;
     if (st == LSTM_OK) {
-        st = param_sums_launch(p, a.ga, a.cbuf, a.H, a.ndir, a.db, a.dpeep, sum_scratch, s);
+        st = param_sums_launch(p, a.ga, a.cbuf, a.H, a.ndir, a.db, a.dpeep, sum_scratch, s, a.c0);
         if (st == LSTM_OK) launched += 2;
     }
     trace_end(p, K_REC_BWD, s, launched);
@@ -1592,13 +1597,13 @@ lstm_status rec_cluster_bwd_launch(const Plan& p, const RecConfig& c, RecArgs a,
 }
 
 lstm_status param_sums_launch(const Plan& p, const float* ga, const float* cbuf, int H, int ndir, float* db,
-                              float* dpeep, float* sum_scratch, cudaStream_t s)
+                              float* dpeep, float* sum_scratch, cudaStream_t s, const float* c0)
 {
     const int ncols = ndir * 7 * H;
     const int rows = (int)p.rows;
     const int chunk = (rows + kSumChunks - 1) / kSumChunks;
     lstm_param_sums_kernel<<<dim3((ncols + 255) / 256, kSumChunks), 256, 0, s>>>(
-        ga, cbuf, p.d_prev_fwd, p.d_prev_rev, rows, H, ndir, chunk, sum_scratch);
+        ga, cbuf, p.d_prev_fwd, p.d_prev_rev, c0, p.d_row_slot, p.d_perm, p.B, rows, H, ndir, chunk, sum_scratch);
     lstm_param_sums_combine<<<(ncols + 255) / 256, 256, 0, s>>>(sum_scratch, kSumChunks, H, ndir, db, dpeep);
     return cudaGetLastError() == cudaSuccess ? LSTM_OK : LSTM_ERR_UNSUPPORTED;
 }

@@ -1,0 +1,612 @@
+// recurrent_wide.cu -- persistent recurrent kernels for bf16 layers wider than a
+// thread-block cluster (512 < H <= 1024).
+//
+// "Single Stream Parallelization of Generalized LSTM-Like RNNs on a GPU",
+// Sec. 3: once the non-recurrent part is done for all frames, only the
+// recurrent node remains sequential.  For H = 1024 one direction's R is 8 MB
+// of bf16, more than one cluster holds, so one launch spreads it over H/16
+// CTAs per direction (64 for H = 1024, both directions on 128 SMs):
+//
+//  * CTA c owns units [16c, 16c + 16) and their 64 gate rows.  Its slice of R
+//    (forward: 64 gate rows x H) or of R^T (backward: 16 units x 4H) is loaded
+//    once by TMA into shared memory (128 KB) and stays there: it is the MMA's
+//    B operand (N = 64, resp. 16) for every step.
+//  * Every step the whole previous operand -- h_{t-1} forward, the previous
+//    step's gate errors backward, bf16, one row per active sequence -- sits in
+//    a double-buffered global array that L2 holds; each CTA streams it in
+//    128-row x 64-column TMA tiles through a 4-stage ring into tcgen05.mma
+//    (M = 128 rows of the batch per tile, fp32 accumulator in tensor memory).
+//  * The cell runs on the accumulator rows: thread r of a 128-thread half
+//    reads row r of its tile from tensor memory (all four gates of the CTA's
+//    16 units), adds the step's input projection and runs the forward cell
+//    (or its BPTT); it keeps its row's cell state (forward) or cell-state
+//    error (backward) in registers from step to step, and writes its 16 new
+//    values of the operand for the next step.
+//  * Steps of a direction are separated by a grid barrier: each CTA adds 1 to
+//    the direction's counter (release) after its writes; a CTA starts step s
+//    once the counter reaches s times the CTAs per direction (acquire; the wait
+//    is bounded and a timeout is recorded in the plan's status word).
+// One cooperative launch runs every step of both directions.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "common.cuh"
+#include "gemm.cuh"
+#include "recurrent.cuh"
+#include "tc_ptx.cuh"
+
+namespace lstm {
+
+namespace {
+
+constexpr int kWU = 16;                          // units per CTA
+constexpr int kWT = 256;                         // threads: rows 0..127 and 128..255 of the batch
+constexpr int kWStages = 4;                      // operand ring stages
+constexpr uint32_t kWTile = 128 * 64 * 2;        // one operand tile: 128 rows x 64 bf16
+constexpr unsigned long long kWTeardownNs = 1000000000ull;
+
+__device__ __forceinline__ float sigm_w(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float tanh_w(float x)
+{
+    const float e = __expf(2.0f * fminf(fmaxf(x, -40.0f), 40.0f));
+    return 1.0f - __fdividef(2.0f, e + 1.0f);
+}
+
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Every CTA of the direction has published step `target` (bounded wait by thread 0; the
+// outcome is the same for every thread of the CTA).
+__device__ __forceinline__ bool grid_wait(const unsigned* ctr, unsigned target, const WideArgs& a, unsigned where)
+{
+    int fail = 0;
+    if (threadIdx.x == 0) {
+        const unsigned long long t0 = global_timer_ns();
+        unsigned spins = 0;
+        while ((int)(ld_acquire_gpu(ctr) - target) < 0) {
+            if ((++spins & 63u) == 0) {
+                if (failure_recorded(a.status)) { fail = 1; break; }
+                if (global_timer_ns() - t0 > a.wait_limit_ns) {
+                    record_failure(a.status, LSTM_ERR_TIMEOUT, where);
+                    fail = 1;
+                    break;
+                }
+            }
+        }
+    }
+    return __syncthreads_or(fail) == 0;
+}
+
+// Shared memory of both kernels: the resident weight slice (KBW blocks of rowsW x 128 B),
+// the operand ring, barriers.
+struct WideSmem {
+    uint8_t* w;
+    uint8_t* ring;
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* mma_bar;
+    uint64_t* w_bar;
+    uint32_t* tmem_slot;
+    int* counters;          // [0] loads issued, [1] tiles consumed (teardown after a timeout)
+    float* peep;            // [3][16]
+};
+
+__device__ __forceinline__ WideSmem wide_smem(int KBW, int rowsW)
+{
+    extern __shared__ unsigned char smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    WideSmem m;
+    m.w = base;
+    m.ring = base + (size_t)KBW * rowsW * 128;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(m.ring + (size_t)kWStages * kWTile);
+    m.full = bars;
+    m.empty = bars + kWStages;
+    m.mma_bar = bars + 2 * kWStages;
+    m.w_bar = m.mma_bar + 1;
+    m.tmem_slot = reinterpret_cast<uint32_t*>(m.w_bar + 1);
+    m.counters = reinterpret_cast<int*>(m.tmem_slot + 2);
+    m.peep = reinterpret_cast<float*>(m.counters + 2);
+    return m;
+}
+
+size_t wide_smem_bytes(int KBW, int rowsW)
+{
+    return 1024 + (size_t)KBW * rowsW * 128 + (size_t)kWStages * kWTile + (2 * kWStages + 2) * 8 + 16 + 3 * kWU * 4;
+}
+
+// One step's product: D[tile m][rows][N] = sum over the KB blocks of A (the operand tiles,
+// streamed from rows ybase + 128 m) times the resident weight slice (B, N rows per block).
+// Thread 0 issues the TMA tiles, thread 32 the MMAs; it_prod / it_cons carry the ring
+// position across steps (each only in its own thread).
+__device__ __forceinline__ bool wide_product(const WideSmem& m, const CUtensorMap* mapA, int ybase, int MT, int KB,
+                                             int N, uint32_t tmem, const WideArgs& a, uint32_t& it_prod,
+                                             uint32_t& it_cons, bool& w_ready, unsigned where)
+{
+    bool ok = true;
+    if (threadIdx.x == 0) {
+        fence_async_global();
+        for (int t = 0; t < MT && ok; ++t)
+            for (int kb = 0; kb < KB; ++kb, ++it_prod) {
+                const int st = (int)(it_prod % kWStages);
+                if (it_prod >= (uint32_t)kWStages &&
+                    !tc::mbar_wait(&m.empty[st], ((it_prod / kWStages) - 1) & 1, a.wait_limit_ns)) {
+                    record_failure(a.status, LSTM_ERR_TIMEOUT, where | 0x1000u);
+                    ok = false;
+                    break;
+                }
+                tc::mbar_arrive_expect_tx(&m.full[st], kWTile);
+                tc::tma_load_2d(m.ring + (size_t)st * kWTile, mapA, &m.full[st], kb * 64, ybase + t * 128);
+                m.counters[0] = (int)it_prod + 1;
+            }
+    } else if (threadIdx.x == 32) {
+        if (!w_ready) {
+            if (!tc::mbar_wait(m.w_bar, 0, a.wait_limit_ns)) {
+                record_failure(a.status, LSTM_ERR_TIMEOUT, where | 0x2000u);
+                ok = false;
+            }
+            w_ready = true;
+        }
+        const uint32_t idesc = tc::idesc_bf16_f32(128, N);
+        const uint32_t wbytes = (uint32_t)N * 128;               // one block of the weight slice
+        for (int t = 0; t < MT && ok; ++t)
+            for (int kb = 0; kb < KB; ++kb, ++it_cons) {
+                const int st = (int)(it_cons % kWStages);
+                if (!tc::mbar_wait(&m.full[st], (it_cons / kWStages) & 1, a.wait_limit_ns)) {
+                    record_failure(a.status, LSTM_ERR_TIMEOUT, where | 0x3000u);
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after_sync();
+                const uint32_t a0 = tc::smem_u32(m.ring + (size_t)st * kWTile);
+                const uint32_t b0 = tc::smem_u32(m.w + (size_t)kb * wbytes);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    tc::mma_bf16_ss(tmem + (uint32_t)(t * N), tc::sdesc_sw128(a0 + kk * 32), tc::sdesc_sw128(b0 + kk * 32),
+                                    idesc, (kb | kk) != 0 ? 1u : 0u);
+                tc::mma_commit(&m.empty[st]);
+                m.counters[1] = (int)it_cons + 1;
+            }
+        tc::mma_commit(m.mma_bar);
+    }
+    return ok;
+}
+
+// After a timeout: no TMA tile may still be landing in this CTA's shared memory and no MMA
+// may still be using tensor memory when the CTA leaves (bounded waits).
+__device__ __forceinline__ void wide_teardown(const WideSmem& m, uint32_t it_prod, uint32_t mma_phase)
+{
+    if (threadIdx.x == 0) {
+        for (uint32_t it = (uint32_t)max(0, m.counters[1]); it < it_prod; ++it)
+            tc::mbar_wait(&m.full[it % kWStages], (it / kWStages) & 1, kWTeardownNs);
+        tc::mbar_wait(m.mma_bar, (mma_phase - 1) & 1, kWTeardownNs);
+        tc::mbar_wait(m.w_bar, 0, kWTeardownNs);
+    }
+}
+
+}  // namespace
+
+// Forward.  Operand array a.xbuf: [ndir][2][B][H] bf16, step s reads parity s & 1 and
+// writes parity (s + 1) & 1.  Tensor maps: mapW = R as [ndir*4H][H] (boxes 16 rows x 64),
+// mapA = a.xbuf as [ndir*2*B][H] (boxes 128 rows x 64).
+__global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, const __grid_constant__ CUtensorMap mapW,
+                                                                  const __grid_constant__ CUtensorMap mapA)
+{
+    const int H = a.H, T = a.T, B = a.B, NC = a.NC;
+    const int KB = H / 64;
+    const int dir = blockIdx.x / NC, cta = blockIdx.x - dir * NC, u0 = cta * kWU;
+    const int nd4H = a.ndir * 4 * H, ndH = a.ndir * H;
+    const WideSmem m = wide_smem(KB, 64);
+    const int warp = threadIdx.x >> 5;
+    const int tile = threadIdx.x >> 7, j = threadIdx.x;      // this thread's row of the batch
+    unsigned* ctr = a.ctr + dir;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kWStages; ++s) {
+            tc::mbar_init(&m.full[s], 1);
+            tc::mbar_init(&m.empty[s], 1);
+        }
+        tc::mbar_init(m.mma_bar, 1);
+        tc::mbar_init(m.w_bar, 1);
+        m.counters[0] = m.counters[1] = 0;
+        tc::fence_mbar_init();
+        // the CTA's 64 gate rows of R (gate g, units u0..u0+15 -> slice rows 16 g ..), K-blocks of 64
+        tc::mbar_arrive_expect_tx(m.w_bar, (uint32_t)KB * 64 * 128);
+        for (int kb = 0; kb < KB; ++kb)
+            for (int g = 0; g < 4; ++g)
+                tc::tma_load_2d(m.w + (size_t)kb * 8192 + g * 2048, &mapW, m.w_bar, kb * 64, dir * 4 * H + g * H + u0);
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(m.tmem_slot, 128);
+        tc::tmem_relinquish();
+    }
+    for (int i = threadIdx.x; i < 3 * kWU; i += kWT) m.peep[i] = a.peep[(size_t)dir * 3 * H + (i / kWU) * H + u0 + i % kWU];
+    // empty sequences end in their initial state
+    if (a.h_n && j < B && a.len[j] == 0)
+        for (int k = 0; k < kWU; ++k) {
+            const size_t o = ((size_t)dir * B + a.perm[j]) * H + u0 + k;
+            a.h_n[o] = a.h0 ? a.h0[o] : 0.f;
+            if (a.c_n) a.c_n[o] = a.c0 ? a.c0[o] : 0.f;
+        }
+    tc::tc_fence_before_sync();
+    __syncthreads();
+    tc::tc_fence_after_sync();
+    const uint32_t tmem = *m.tmem_slot;
+
+    float creg[kWU];                                  // c of this thread's row, step to step
+#pragma unroll
+    for (int k = 0; k < kWU; ++k) creg[k] = 0.f;
+    uint32_t it_prod = 0, it_cons = 0, mma_phase = 0;
+    bool w_ready = false, failed = false;
+    for (int s = 0; s < T && !failed; ++s) {
+        const int t = dir == 0 ? s : T - 1 - s;
+        const int n = a.bs[t];
+        const int n_prev = dir == 0 ? (t >= 1 ? n : 0) : (t + 1 < T ? a.bs[t + 1] : 0);
+        const int row = a.off[t] + j;
+        // this row's input projection (own data: loaded before the wait)
+        float pre[4][kWU];
+        if (j < n) {
+            const float* gr = a.ga + (size_t)row * nd4H + (size_t)dir * 4 * H + u0;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+#pragma unroll
+                for (int q = 0; q < kWU / 4; ++q) {
+                    const float4 x = *reinterpret_cast<const float4*>(gr + g * H + 4 * q);
+                    pre[g][4 * q] = x.x; pre[g][4 * q + 1] = x.y; pre[g][4 * q + 2] = x.z; pre[g][4 * q + 3] = x.w;
+                }
+        }
+        if (s > 0 && !grid_wait(ctr, (unsigned)(NC * s), a, 0x90000u | (unsigned)s)) { failed = true; break; }
+        const int MT = (n_prev + 127) / 128;
+        if (MT > 0) {
+            bool ok = wide_product(m, &mapA, (dir * 2 + (s & 1)) * B, MT, KB, 64, tmem, a, it_prod, it_cons, w_ready,
+                                   0xA0000u | (unsigned)(s & 0xfff));
+            ++mma_phase;
+            ok = tc::mbar_wait(m.mma_bar, (mma_phase - 1) & 1, a.wait_limit_ns) && ok;
+            if (__syncthreads_or(!ok)) {
+                record_failure(a.status, LSTM_ERR_TIMEOUT, 0xB0000u | (unsigned)s);
+                failed = true;
+                break;
+            }
+            tc::tc_fence_after_sync();
+        }
+        // R h_{t-1} of this row: tensor-memory lane = row within the tile (warp-uniform loads)
+        float acc[4][kWU];
+        if (tile < MT) {
+            uint32_t r[4][16];
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+                tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(tile * 64 + g * 16), r[g]);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+#pragma unroll
+                for (int k = 0; k < kWU; ++k) acc[g][k] = j < n_prev ? __uint_as_float(r[g][k]) : 0.f;
+        } else {
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+#pragma unroll
+                for (int k = 0; k < kWU; ++k) acc[g][k] = 0.f;
+        }
+        if (j < n) {
+            const int len = a.len[j];
+            const size_t so = ((size_t)dir * B + a.perm[j]) * H + u0;          // caller-order state
+            float hv[kWU], cv[kWU], gv[4][kWU];
+#pragma unroll
+            for (int k = 0; k < kWU; ++k) {
+                const float cp = j < n_prev ? creg[k] : (a.c0 ? __ldg(a.c0 + so + k) : 0.f);
+                const float ig = sigm_w(pre[0][k] + acc[0][k] + m.peep[k] * cp);
+                const float fg = sigm_w(pre[1][k] + acc[1][k] + m.peep[kWU + k] * cp);
+                const float zg = tanh_w(pre[2][k] + acc[2][k]);
+                float c = fg * cp + ig * zg;
+                const float og = sigm_w(pre[3][k] + acc[3][k] + m.peep[2 * kWU + k] * c);
+                float h = og * tanh_w(c);
+                if (a.padded && t >= len) { c = 0.f; h = 0.f; }
+                gv[0][k] = ig; gv[1][k] = fg; gv[2][k] = zg; gv[3][k] = og;
+                cv[k] = c; hv[k] = h; creg[k] = c;
+            }
+            float* gw = a.ga + (size_t)row * nd4H + (size_t)dir * 4 * H + u0;
+            const size_t yo = (size_t)row * ndH + (size_t)dir * H + u0;
+#pragma unroll
+            for (int q = 0; q < kWU / 4; ++q) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    *reinterpret_cast<float4*>(gw + g * H + 4 * q) =
+                        make_float4(gv[g][4 * q], gv[g][4 * q + 1], gv[g][4 * q + 2], gv[g][4 * q + 3]);
+                *reinterpret_cast<float4*>(a.cbuf + yo + 4 * q) = make_float4(cv[4 * q], cv[4 * q + 1], cv[4 * q + 2], cv[4 * q + 3]);
+                *reinterpret_cast<float4*>(a.y + yo + 4 * q) = make_float4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
+            }
+            uint32_t hb[kWU / 2];
+#pragma unroll
+            for (int e = 0; e < kWU / 2; ++e) {
+                const __nv_bfloat162 p2 = __floats2bfloat162_rn(hv[2 * e], hv[2 * e + 1]);
+                hb[e] = *reinterpret_cast<const uint32_t*>(&p2);
+            }
+            if (a.y_lo) {
+                uint4* yl = reinterpret_cast<uint4*>(a.y_lo + yo);
+                yl[0] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+                yl[1] = make_uint4(hb[4], hb[5], hb[6], hb[7]);
+            }
+            if (s + 1 < T) {         // h_t for the next step's product
+                uint4* xb = reinterpret_cast<uint4*>(a.xbuf + (((size_t)dir * 2 + ((s + 1) & 1)) * B + j) * H + u0);
+                xb[0] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+                xb[1] = make_uint4(hb[4], hb[5], hb[6], hb[7]);
+            }
+            if (a.h_n && ((dir == 0 && t == len - 1) || (dir == 1 && t == 0 && len > 0)))
+#pragma unroll
+                for (int k = 0; k < kWU; ++k) {
+                    a.h_n[so + k] = hv[k];
+                    if (a.c_n) a.c_n[so + k] = cv[k];
+                }
+        }
+        fence_async_global();       // this thread's h_t is read by the peers' TMA tiles
+        tc::tc_fence_before_sync();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            red_release_add(ctr, 1u);
+        }
+    }
+    if (failed) wide_teardown(m, it_prod, mma_phase);
+    // the weight slice's loads have landed even when no step needed a product (bounded)
+    if (threadIdx.x == 0) tc::mbar_wait(m.w_bar, 0, kWTeardownNs);
+    tc::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::tc_fence_after_sync();
+        tc::tmem_dealloc(tmem, 128);
+    }
+}
+
+// BPTT.  Operand array a.xbuf: [ndir][2][B][4H] bf16 gate errors (step s reads parity s & 1,
+// the errors of the previous BPTT step; writes parity (s + 1) & 1).  mapW = R^T as
+// [ndir*H][4H] (boxes 16 rows x 64), mapA = a.xbuf as [ndir*2*B][4H] (boxes 128 rows x 64).
+__global__ void __launch_bounds__(kWT, 1) lstm_rec_bwd_wide_kernel(WideArgs a, const __grid_constant__ CUtensorMap mapW,
+                                                                  const __grid_constant__ CUtensorMap mapA)
+{
+    const int H = a.H, T = a.T, B = a.B, NC = a.NC;
+    const int KB = 4 * H / 64;
+    const int dir = blockIdx.x / NC, cta = blockIdx.x - dir * NC, u0 = cta * kWU;
+    const int nd4H = a.ndir * 4 * H, ndH = a.ndir * H;
+    const WideSmem m = wide_smem(KB, kWU);
+    const int warp = threadIdx.x >> 5;
+    const int tile = threadIdx.x >> 7, j = threadIdx.x;
+    unsigned* ctr = a.ctr + dir;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kWStages; ++s) {
+            tc::mbar_init(&m.full[s], 1);
+            tc::mbar_init(&m.empty[s], 1);
+        }
+        tc::mbar_init(m.mma_bar, 1);
+        tc::mbar_init(m.w_bar, 1);
+        m.counters[0] = m.counters[1] = 0;
+        tc::fence_mbar_init();
+        // R^T rows of the CTA's 16 units over all 4H gate rows, K-blocks of 64 (2 KB each)
+        tc::mbar_arrive_expect_tx(m.w_bar, (uint32_t)KB * kWU * 128);
+        for (int kb = 0; kb < KB; ++kb)
+            tc::tma_load_2d(m.w + (size_t)kb * kWU * 128, &mapW, m.w_bar, kb * 64, dir * H + u0);
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(m.tmem_slot, 32);
+        tc::tmem_relinquish();
+    }
+    for (int i = threadIdx.x; i < 3 * kWU; i += kWT) m.peep[i] = a.peep[(size_t)dir * 3 * H + (i / kWU) * H + u0 + i % kWU];
+    tc::tc_fence_before_sync();
+    __syncthreads();
+    tc::tc_fence_after_sync();
+    const uint32_t tmem = *m.tmem_slot;
+
+    float dcc[kWU];                                   // the cell-state error carried to the step before
+#pragma unroll
+    for (int k = 0; k < kWU; ++k) dcc[k] = 0.f;
+    uint32_t it_prod = 0, it_cons = 0, mma_phase = 0;
+    bool w_ready = false, failed = false;
+    for (int s = 0; s < T && !failed; ++s) {
+        const int t = dir == 0 ? T - 1 - s : s;
+        const int n = a.bs[t];
+        const int n_next = dir == 0 ? (t + 1 < T ? a.bs[t + 1] : 0) : (t >= 1 ? n : 0);
+        const int n_prev = dir == 0 ? (t >= 1 ? n : 0) : (t + 1 < T ? a.bs[t + 1] : 0);
+        const int prev_base = dir == 0 ? (t >= 1 ? a.off[t - 1] : 0) : (t + 1 < T ? a.off[t + 1] : 0);
+        const int row = a.off[t] + j;
+        // own operands of the row (before the wait): gates, c_t, c_{t-1}, dy
+        float gv[4][kWU], cv[kWU], cp[kWU], dyv[kWU];
+        const size_t so = j < B ? ((size_t)dir * B + a.perm[j]) * H + u0 : 0;   // caller-order state
+        if (j < n) {
+            const float* gr = a.ga + (size_t)row * nd4H + (size_t)dir * 4 * H + u0;
+            const size_t yo = (size_t)row * ndH + (size_t)dir * H + u0;
+            const size_t po = (size_t)(prev_base + j) * ndH + (size_t)dir * H + u0;
+#pragma unroll
+            for (int q = 0; q < kWU / 4; ++q) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const float4 x = *reinterpret_cast<const float4*>(gr + g * H + 4 * q);
+                    gv[g][4 * q] = x.x; gv[g][4 * q + 1] = x.y; gv[g][4 * q + 2] = x.z; gv[g][4 * q + 3] = x.w;
+                }
+                const float4 c4 = __ldg(reinterpret_cast<const float4*>(a.cbuf + yo + 4 * q));
+                const float4 d4 = __ldg(reinterpret_cast<const float4*>(a.dy + yo + 4 * q));
+                const float4 p4 = j < n_prev ? __ldg(reinterpret_cast<const float4*>(a.cbuf + po + 4 * q))
+                                  : a.c0 ? __ldg(reinterpret_cast<const float4*>(a.c0 + so + 4 * q))
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                cv[4 * q] = c4.x; cv[4 * q + 1] = c4.y; cv[4 * q + 2] = c4.z; cv[4 * q + 3] = c4.w;
+                dyv[4 * q] = d4.x; dyv[4 * q + 1] = d4.y; dyv[4 * q + 2] = d4.z; dyv[4 * q + 3] = d4.w;
+                cp[4 * q] = p4.x; cp[4 * q + 1] = p4.y; cp[4 * q + 2] = p4.z; cp[4 * q + 3] = p4.w;
+            }
+        }
+        if (s > 0 && !grid_wait(ctr, (unsigned)(NC * s), a, 0xC0000u | (unsigned)s)) { failed = true; break; }
+        // R^T da of the step after this one (recurrence order), for the rows that have one
+        const int MT = (n_next + 127) / 128;
+        if (MT > 0) {
+            bool ok = wide_product(m, &mapA, (dir * 2 + (s & 1)) * B, MT, KB, kWU, tmem, a, it_prod, it_cons, w_ready,
+                                   0xD0000u | (unsigned)(s & 0xfff));
+            ++mma_phase;
+            ok = tc::mbar_wait(m.mma_bar, (mma_phase - 1) & 1, a.wait_limit_ns) && ok;
+            if (__syncthreads_or(!ok)) {
+                record_failure(a.status, LSTM_ERR_TIMEOUT, 0xE0000u | (unsigned)s);
+                failed = true;
+                break;
+            }
+            tc::tc_fence_after_sync();
+        }
+        float dhr[kWU];
+        if (tile < MT) {
+            uint32_t r[16];
+            tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(tile * kWU), r);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < kWU; ++k) dhr[k] = j < n_next ? __uint_as_float(r[k]) : 0.f;
+        } else {
+#pragma unroll
+            for (int k = 0; k < kWU; ++k) dhr[k] = 0.f;
+        }
+        if (j < n) {
+            const bool has_next = j < n_next;
+            const bool real = !a.padded || t < a.len[j];
+            float da[4][kWU];
+#pragma unroll
+            for (int k = 0; k < kWU; ++k) {
+                float dai = 0.f, daf = 0.f, daz = 0.f, dao = 0.f, carry_out = 0.f;
+                if (real) {
+                    // the sequence's last step: the final state's own errors from outside
+                    const float dh = dyv[k] + (has_next ? dhr[k] : (a.dh_n ? __ldg(a.dh_n + so + k) : 0.f));
+                    const float carry = has_next ? dcc[k] : (a.dc_n ? __ldg(a.dc_n + so + k) : 0.f);
+                    const float ig = gv[0][k], fg = gv[1][k], zg = gv[2][k], og = gv[3][k];
+                    const float tcv = tanh_w(cv[k]);
+                    dao = dh * tcv * og * (1.f - og);
+                    const float dc = dh * og * (1.f - tcv * tcv) + dao * m.peep[2 * kWU + k] + carry;
+                    dai = dc * zg * ig * (1.f - ig);
+                    daf = dc * cp[k] * fg * (1.f - fg);
+                    daz = dc * ig * (1.f - zg * zg);
+                    carry_out = dc * fg + dai * m.peep[k] + daf * m.peep[kWU + k];
+                    if (j >= n_prev && a.dc0) a.dc0[so + k] = carry_out;       // the sequence's first step
+                }
+                da[0][k] = dai; da[1][k] = daf; da[2][k] = daz; da[3][k] = dao;
+                dcc[k] = carry_out;
+            }
+            float* gw = a.ga + (size_t)row * nd4H + (size_t)dir * 4 * H + u0;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+#pragma unroll
+                for (int q = 0; q < kWU / 4; ++q)
+                    *reinterpret_cast<float4*>(gw + g * H + 4 * q) =
+                        make_float4(da[g][4 * q], da[g][4 * q + 1], da[g][4 * q + 2], da[g][4 * q + 3]);
+                if (s + 1 < T) {     // bf16 gate errors for the next step's product
+                    uint32_t w8[kWU / 2];
+#pragma unroll
+                    for (int e = 0; e < kWU / 2; ++e) {
+                        const __nv_bfloat162 p2 = __floats2bfloat162_rn(da[g][2 * e], da[g][2 * e + 1]);
+                        w8[e] = *reinterpret_cast<const uint32_t*>(&p2);
+                    }
+                    uint4* xb = reinterpret_cast<uint4*>(
+                        a.xbuf + (((size_t)dir * 2 + ((s + 1) & 1)) * B + j) * 4 * H + (size_t)g * H + u0);
+                    xb[0] = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+                    xb[1] = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+                }
+            }
+        }
+        fence_async_global();
+        tc::tc_fence_before_sync();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            red_release_add(ctr, 1u);
+        }
+    }
+    if (failed) wide_teardown(m, it_prod, mma_phase);
+    if (threadIdx.x == 0) tc::mbar_wait(m.w_bar, 0, kWTeardownNs);
+    tc::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::tc_fence_after_sync();
+        tc::tmem_dealloc(tmem, 32);
+    }
+}
+
+// ------------------------------------------------------------------------- configuration
+
+bool rec_wide_supported(const Plan& p, int H, int ndir, bool bf16)
+{
+    if (!bf16 || p.gemm_engine != 0 || p.forced_ctas != 0) return false;
+    if (H % 64 != 0 || H > 1024 || p.B > 256 || p.B < 1) return false;
+    const int grid = ndir * H / kWU;
+    if (grid > p.num_sms) return false;
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p.device) != cudaSuccess) return false;
+    const size_t smem = wide_smem_bytes(H / 64, 64);
+    return smem <= (size_t)optin && wide_smem_bytes(4 * H / 64, kWU) <= (size_t)optin;
+}
+
+size_t rec_wide_xbuf_bytes(const Plan& p, int H, int ndir, bool bwd)
+{
+    return (size_t)ndir * 2 * p.B * (bwd ? 4 * H : H) * 2;
+}
+
+static lstm_status wide_launch(const Plan& p, const void* fn, WideArgs& a, const CUtensorMap& mapW,
+                               const CUtensorMap& mapA, size_t smem, cudaStream_t s)
+{
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+        cudaGetLastError();
+        return LSTM_ERR_UNSUPPORTED;
+    }
+    const int grid = a.ndir * a.NC;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kWT, smem) != cudaSuccess || per_sm < 1 ||
+        per_sm * p.num_sms < grid) {
+        cudaGetLastError();
+        return LSTM_ERR_UNSUPPORTED;
+    }
+    if (cudaMemsetAsync(a.ctr, 0, sizeof(unsigned) * 2, s) != cudaSuccess) return LSTM_ERR_CUDA;
+    CUtensorMap mw = mapW, ma = mapA;
+    void* args[] = {&a, &mw, &ma};
+    const cudaError_t e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kWT), args, smem, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return e == cudaErrorCooperativeLaunchTooLarge ? LSTM_ERR_UNSUPPORTED : LSTM_ERR_CUDA;
+    }
+    return LSTM_OK;
+}
+
+lstm_status rec_wide_fwd_launch(const Plan& p, WideArgs a, const void* R, cudaStream_t s)
+{
+    a.NC = a.H / kWU;
+    a.ctr = p.d_flags;
+    CUtensorMap mapW, mapA;
+    memset(&mapW, 0, sizeof(mapW));
+    memset(&mapA, 0, sizeof(mapA));
+    if (!make_map_bf16_sw128(&mapW, R, a.ndir * 4 * a.H, a.H, a.H, kWU) ||
+        !make_map_bf16_sw128(&mapA, a.xbuf, a.ndir * 2 * a.B, a.H, a.H, 128))
+        return LSTM_ERR_UNSUPPORTED;
+    trace_begin(p, K_REC_FWD, s);
+    const lstm_status st = wide_launch(p, (const void*)lstm_rec_fwd_wide_kernel, a, mapW, mapA,
+                                       wide_smem_bytes(a.H / 64, 64), s);
+    trace_end(p, K_REC_FWD, s, st == LSTM_OK ? 1 : 0);
+    return st;
+}
+
+lstm_status rec_wide_bwd_launch(const Plan& p, WideArgs a, const void* RT, float* sum_scratch, float* db,
+                                float* dpeep, cudaStream_t s)
+{
+    a.NC = a.H / kWU;
+    a.ctr = p.d_flags;
+    CUtensorMap mapW, mapA;
+    memset(&mapW, 0, sizeof(mapW));
+    memset(&mapA, 0, sizeof(mapA));
+    if (!make_map_bf16_sw128(&mapW, RT, a.ndir * a.H, 4 * a.H, 4 * a.H, kWU) ||
+        !make_map_bf16_sw128(&mapA, a.xbuf, a.ndir * 2 * a.B, 4 * a.H, 4 * a.H, 128))
+        return LSTM_ERR_UNSUPPORTED;
+    trace_begin(p, K_REC_BWD, s);
+    lstm_status st = wide_launch(p, (const void*)lstm_rec_bwd_wide_kernel, a, mapW, mapA,
+                                 wide_smem_bytes(4 * a.H / 64, kWU), s);
+    int launched = st == LSTM_OK ? 1 : 0;
+    if (st == LSTM_OK) {
+        st = param_sums_launch(p, a.ga, a.cbuf, a.H, a.ndir, db, dpeep, sum_scratch, s, a.c0);
+        if (st == LSTM_OK) launched += 2;
+    }
+    trace_end(p, K_REC_BWD, s, launched);
+    return st;
+}
+
+}  // namespace lstm

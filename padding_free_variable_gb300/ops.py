@@ -11,7 +11,7 @@ import numpy as np
 import torch
 
 from . import _lib
-from ._lib import LayerGrads, LayerParams, LayerShape, check
+from ._lib import LayerGrads, LayerParams, LayerShape, State, StateGrads, check
 
 
 def _ptr(t) -> ctypes.c_void_p:
@@ -24,17 +24,26 @@ def _stream(stream=None) -> ctypes.c_void_p:
 
 
 class Plan:
-    """Packing plan of one batch of sequence lengths (optionally the padded layout)."""
+    """Packing plan of one batch of sequence lengths: packed (default), the padded layout,
+    a segment plan (``segments=(chunk, step)``: lstm_plan_create_segments) or a window plan
+    (``window=(start, width)``: lstm_plan_create_window)."""
 
-    def __init__(self, lengths, padded: bool = False):
+    def __init__(self, lengths, padded: bool = False, segments=None, window=None):
         lib = _lib.load()
         lens = np.ascontiguousarray(np.asarray(lengths, dtype=np.int32))
         self.lengths = lens
         self.padded = padded
         h = ctypes.c_void_p()
-        fn = lib.lstm_plan_create_padded if padded else lib.lstm_plan_create
-        check(fn(lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), int(lens.size), ctypes.byref(h)),
-              "lstm_plan_create")
+        lp = lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        if segments is not None:
+            check(lib.lstm_plan_create_segments(lp, int(lens.size), int(segments[0]), int(segments[1]),
+                                                ctypes.byref(h)), "lstm_plan_create_segments")
+        elif window is not None:
+            check(lib.lstm_plan_create_window(lp, int(lens.size), int(window[0]), int(window[1]), ctypes.byref(h)),
+                  "lstm_plan_create_window")
+        else:
+            fn = lib.lstm_plan_create_padded if padded else lib.lstm_plan_create
+            check(fn(lp, int(lens.size), ctypes.byref(h)), "lstm_plan_create")
         self.handle = h
         rows, frames = ctypes.c_int64(), ctypes.c_int64()
         steps, batch = ctypes.c_int32(), ctypes.c_int32()
@@ -80,7 +89,8 @@ class Plan:
         check(_lib.load().lstm_plan_recurrent_config(self.handle, int(bool(backward)), ctypes.byref(k),
                                                      ctypes.byref(g), ctypes.byref(m), ctypes.byref(v)),
               "lstm_plan_recurrent_config")
-        return {"kernel": ("none", "grid", "cluster", "step_launches")[k.value], "ctas_per_direction": g.value,
+        return {"kernel": ("none", "grid", "cluster", "step_launches", "persistent_wide")[k.value],
+                "ctas_per_direction": g.value,
                 "product": ("cuda_cores", "mma_sync", "tcgen05")[m.value],
                 "exchange": "bulk" if v.value & 1 else "barrier", "tma_tiles": bool(v.value & 2)}
 
@@ -90,6 +100,10 @@ class Plan:
         check(_lib.load().lstm_plan_recurrent_groups(self.handle, int(bool(backward)), ctypes.byref(g),
                                                      ctypes.byref(r)), "lstm_plan_recurrent_groups")
         return g.value, r.value
+
+    def debug_wide_recurrence(self, mode: int):
+        """bf16 layers with H > 512: -1 automatic, 0 per-step launches, 1 the persistent kernel."""
+        check(_lib.load().lstm_debug_wide_recurrence(self.handle, int(mode)), "lstm_debug_wide_recurrence")
 
     def debug_sequence_groups(self, slots: int):
         """Force the cluster kernels' slots per sequence group (0 = automatic)."""
@@ -140,6 +154,33 @@ class Plan:
             self.close()
         except Exception:
             pass
+
+
+def segments_host(lengths, chunk: int, step: int):
+    """(sequence, start, length) arrays of lstm_plan_create_segments' segments (host only)."""
+    lib = _lib.load()
+    lens = np.ascontiguousarray(np.asarray(lengths, dtype=np.int32))
+    lp = lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    n = ctypes.c_int32()
+    check(lib.lstm_segments_host(lp, int(lens.size), int(chunk), int(step), ctypes.byref(n), None, None, None, 0),
+          "lstm_segments_host")
+    out = [np.zeros(n.value, np.int32) for _ in range(3)]
+    ptrs = [o.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) for o in out]
+    check(lib.lstm_segments_host(lp, int(lens.size), int(chunk), int(step), ctypes.byref(n), *ptrs, n.value),
+          "lstm_segments_host")
+    return tuple(out)
+
+
+def form_batches(lengths, budget: int, padded_budget: bool = False) -> np.ndarray:
+    """Batch index of each sequence under a frame budget (lstm_form_batches; host only)."""
+    lib = _lib.load()
+    lens = np.ascontiguousarray(np.asarray(lengths, dtype=np.int32))
+    out = np.zeros(lens.size, np.int32)
+    nb = ctypes.c_int32()
+    check(lib.lstm_form_batches(lens.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), int(lens.size), int(budget),
+                                1 if padded_budget else 0, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                ctypes.byref(nb)), "lstm_form_batches")
+    return out
 
 
 def device_layers(layers, bf16: bool, device="cuda") -> list:
@@ -197,6 +238,31 @@ def layer_backward(plan: Plan, shape: LayerShape, layer: dict, x_packed, y_packe
           "lstm_bwd")
 
 
+def state_scratch_bytes(plan: Plan, shape: LayerShape) -> int:
+    return int(_lib.load().lstm_state_scratch_bytes(plan.handle, ctypes.byref(shape)))
+
+
+def layer_forward_state(plan: Plan, shape: LayerShape, layer: dict, h0, c0, x_packed, y_packed, y_lo, h_n, c_n,
+                        workspace, state_scratch, stream=None):
+    """lstm_fwd_state: the layer starting from h0 / c0 ([ndir][B][H] fp32 device tensors or None)."""
+    st = State(0 if h0 is None else h0.data_ptr(), 0 if c0 is None else c0.data_ptr())
+    check(_lib.load().lstm_fwd_state(plan.handle, ctypes.byref(shape), ctypes.byref(_params(layer)), ctypes.byref(st),
+                                     _ptr(x_packed), _ptr(y_packed), _ptr(y_lo), _ptr(h_n), _ptr(c_n),
+                                     _ptr(workspace), _ptr(state_scratch), _stream(stream)), "lstm_fwd_state")
+
+
+def layer_backward_state(plan: Plan, shape: LayerShape, layer: dict, h0, c0, x_packed, y_packed, workspace, dy_packed,
+                         dx_packed, grads: dict, dh_n, dc_n, dh0, dc0, scratch, state_scratch, stream=None):
+    """lstm_bwd_state: also takes dL/dh_n, dL/dc_n and returns dL/dh0, dL/dc0 (any may be None)."""
+    st = State(0 if h0 is None else h0.data_ptr(), 0 if c0 is None else c0.data_ptr())
+    sg = StateGrads(*[0 if t is None else t.data_ptr() for t in (dh_n, dc_n, dh0, dc0)])
+    g = LayerGrads(grads["W"].data_ptr(), grads["R"].data_ptr(), grads["b"].data_ptr(), grads["peep"].data_ptr())
+    check(_lib.load().lstm_bwd_state(plan.handle, ctypes.byref(shape), ctypes.byref(_params(layer)), ctypes.byref(st),
+                                     _ptr(x_packed), _ptr(y_packed), _ptr(workspace), _ptr(dy_packed),
+                                     _ptr(dx_packed), ctypes.byref(g), ctypes.byref(sg), _ptr(scratch),
+                                     _ptr(state_scratch), _stream(stream)), "lstm_bwd_state")
+
+
 def stepwise_scratch_bytes(plan: Plan, shape: LayerShape) -> int:
     return int(_lib.load().lstm_stepwise_scratch_bytes(plan.handle, ctypes.byref(shape)))
 
@@ -248,6 +314,11 @@ class PackedLSTMStack:
                    for s in self.shapes]
         need = max((stepwise_scratch_bytes if self.stepwise else scratch_bytes)(plan, s) for s in self.shapes)
         self.scratch = torch.empty(max(1, need), dtype=torch.uint8, device=dev)
+        # initial states / final-state errors ([layers][ndir][B][H] fp32, caller order) when set;
+        # dh0 / dc0 are filled by backward_packed then
+        self.h0 = self.c0 = self.dh_n = self.dc_n = None
+        self.dh0 = self.dc0 = None
+        self.state_scratch = None
         self.dy_packed = torch.empty((rows, nd * H), dtype=torch.float32, device=dev)
         self.dx = [torch.empty((rows, s.input_size), dtype=torch.float32, device=dev) for s in self.shapes]
         self.grads = [{"W": torch.empty(tuple(lay["W"].shape), dtype=torch.float32, device=dev),
@@ -256,12 +327,31 @@ class PackedLSTMStack:
                        "peep": torch.empty(tuple(lay["peep"].shape), dtype=torch.float32, device=dev)}
                       for lay in layers]
 
+    def set_states(self, h0=None, c0=None, dh_n=None, dc_n=None):
+        """Initial states and final-state errors of every layer ([layers][ndir][B][H] fp32 device tensors,
+        caller order; None = zero).  Afterwards forward_packed / backward_packed run through
+        lstm_fwd_state / lstm_bwd_state, and backward_packed fills self.dh0 / self.dc0."""
+        self.h0, self.c0, self.dh_n, self.dc_n = h0, c0, dh_n, dc_n
+        dev = self.y[0].device
+        shape = (len(self.layers), self.nd, self.plan.batch, self.H)
+        self.dh0 = torch.empty(shape, dtype=torch.float32, device=dev)
+        self.dc0 = torch.empty(shape, dtype=torch.float32, device=dev)
+        need = max(state_scratch_bytes(self.plan, s) for s in self.shapes)
+        self.state_scratch = torch.empty(max(1, need), dtype=torch.uint8, device=dev)
+
+    def _st(self, t, l):
+        return None if t is None else t[l]
+
     def layer_input(self, l):
         return self.x_packed if l == 0 else (self.y_lo[l - 1] if self.bf16 else self.y[l - 1])
 
     def forward_packed(self, stream=None):
         for l, lay in enumerate(self.layers):
-            if self.stepwise:
+            if self.state_scratch is not None:
+                layer_forward_state(self.plan, self.shapes[l], lay, self._st(self.h0, l), self._st(self.c0, l),
+                                    self.layer_input(l), self.y[l], self.y_lo[l], self.h_n[l], self.c_n[l],
+                                    self.ws[l], self.state_scratch, stream)
+            elif self.stepwise:
                 layer_forward_stepwise(self.plan, self.shapes[l], lay, self.layer_input(l), self.y[l],
                                        self.y_lo[l], self.h_n[l], self.c_n[l], self.ws[l], self.scratch, stream)
             else:
@@ -273,8 +363,14 @@ class PackedLSTMStack:
         dy = self.dy_packed
         back = layer_backward_stepwise if self.stepwise else layer_backward
         for l in range(len(self.layers) - 1, -1, -1):
-            back(self.plan, self.shapes[l], self.layers[l], self.layer_input(l), self.y[l],
-                 self.ws[l], dy, self.dx[l], self.grads[l], self.scratch, stream)
+            if self.state_scratch is not None:
+                layer_backward_state(self.plan, self.shapes[l], self.layers[l], self._st(self.h0, l),
+                                     self._st(self.c0, l), self.layer_input(l), self.y[l], self.ws[l], dy, self.dx[l],
+                                     self.grads[l], self._st(self.dh_n, l), self._st(self.dc_n, l), self.dh0[l],
+                                     self.dc0[l], self.scratch, self.state_scratch, stream)
+            else:
+                back(self.plan, self.shapes[l], self.layers[l], self.layer_input(l), self.y[l],
+                     self.ws[l], dy, self.dx[l], self.grads[l], self.scratch, stream)
             dy = self.dx[l]
         return self.dx[0]
 
@@ -285,3 +381,50 @@ class PackedLSTMStack:
         self.forward_packed(stream)
         self.backward_packed(stream)
         return self.plan.unpack(self.y[-1], stream=stream), self.plan.unpack(self.dx[0], stream=stream)
+
+
+class TruncatedBPTT:
+    """Truncated back-propagation through time over windows of `window` frames ("Single Stream
+    Parallelization...", Sec. 4, BPTT(h; h') with h = h'): window k of every sequence runs
+    lstm_fwd_state from window k-1's final states (carry=True; the forward direction only -- the
+    reverse direction cannot see the frames after its window and starts each window from zero)
+    and lstm_bwd_state with the window's own errors, so no error crosses a window boundary.
+    Each window is one window plan (lstm_plan_create_window) over the caller's full tensors.
+    carry=False gives RETURNN-style independent chunks (every window from the zero state)."""
+
+    def __init__(self, lengths, layers: list, input_size: int, hidden_size: int, num_directions: int,
+                 bf16: bool, window: int, device="cuda", carry: bool = True):
+        lens = np.asarray(lengths, dtype=np.int32)
+        T = int(lens.max()) if lens.size else 0
+        self.window, self.carry = int(window), bool(carry)
+        self.frames = int(lens.sum())
+        self.plans = [Plan(lens, window=(k * self.window, self.window)) for k in range(max(1, -(-T // self.window)))]
+        self.stacks = [PackedLSTMStack(p, layers, input_size, hidden_size, num_directions, bf16, device)
+                       for p in self.plans]
+        for st in self.stacks:
+            st.set_states()
+        self.nd, self.H, self.D0 = int(num_directions), int(hidden_size), int(input_size)
+
+    def step(self, x_cat, G_cat, stream=None):
+        """All windows in order; returns (y_cat, dx_cat, per-window gradients).  y and dx are the
+        caller's full tensors (every frame written by its window); window k's weight gradients
+        are those of its own frames' errors (one mini-batch of BPTT(h'; h'))."""
+        dev = x_cat.device
+        y_cat = torch.zeros((self.frames, self.nd * self.H), dtype=torch.float32, device=dev)
+        dx_cat = torch.zeros((self.frames, self.D0), dtype=torch.float32, device=dev)
+        grads = []
+        h = c = None
+        for plan, st in zip(self.plans, self.stacks):
+            st.h0, st.c0 = (h, c) if self.carry else (None, None)
+            plan.pack(x_cat, st.x_packed, stream)
+            plan.pack(G_cat, st.dy_packed, stream)
+            st.forward_packed(stream)
+            st.backward_packed(stream)
+            plan.unpack(st.y[-1], y_cat, stream)
+            plan.unpack(st.dx[0], dx_cat, stream)
+            grads.append([{k: v.clone() for k, v in g.items()} for g in st.grads])
+            h, c = st.h_n.clone(), st.c_n.clone()
+            if self.nd == 2:               # the reverse direction restarts every window from zero
+                h[:, 1].zero_()
+                c[:, 1].zero_()
+        return y_cat, dx_cat, grads

@@ -74,8 +74,10 @@ def device_layers(w, device="cuda"):
 
 
 def run_gpu(w, padded: bool = False, device="cuda", ctas: int = 0, engine: int = 0, stepwise: bool = False,
-            variant: int = -1, group_slots: int = 0):
-    """pack -> all layers forward -> all layers backward -> unpack, through the C ABI."""
+            variant: int = -1, group_slots: int = 0, states=None):
+    """pack -> all layers forward -> all layers backward -> unpack, through the C ABI.
+    states: optional dict of numpy h0, c0, dh_n, dc_n [layers][ndir][B][H] (lstm_fwd_state /
+    lstm_bwd_state); the result then holds dh0 and dc0 too."""
     import torch
     from padding_free_variable_gb300 import ops
     bf16 = w.spec.dtype == "bf16"
@@ -90,6 +92,10 @@ def run_gpu(w, padded: bool = False, device="cuda", ctas: int = 0, engine: int =
         plan.set_gemm_engine(engine)
     stack = ops.PackedLSTMStack(plan, device_layers(w, device), w.spec.input_size, w.spec.hidden_size,
                                 w.spec.num_directions, bf16, device, stepwise=stepwise)
+    if states is not None:
+        dev = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(device))
+               for k, v in states.items()}
+        stack.set_states(dev.get("h0"), dev.get("c0"), dev.get("dh_n"), dev.get("dc_n"))
     x = torch.from_numpy(w.x).to(device=device, dtype=torch.bfloat16 if bf16 else torch.float32)
     G = torch.from_numpy(w.G).to(device)
     y_cat, dx_cat = stack.step(x, G)
@@ -100,11 +106,15 @@ def run_gpu(w, padded: bool = False, device="cuda", ctas: int = 0, engine: int =
            "h_n": stack.h_n.cpu().numpy(), "c_n": stack.c_n.cpu().numpy(),
            "grads": [{k: v.cpu().numpy() for k, v in g.items()} for g in stack.grads],
            "plan": plan, "stack": stack}
+    if states is not None:
+        res["dh0"] = stack.dh0.cpu().numpy()
+        res["dc0"] = stack.dc0.cpu().numpy()
     return res
 
 
-def run_oracle(w, seqs=None, nthreads=None, bf16_products=False):
-    """The oracle on the whole workload, or on the sequences `seqs` only."""
+def run_oracle(w, seqs=None, nthreads=None, bf16_products=False, states=None):
+    """The oracle on the whole workload, or on the sequences `seqs` only (optionally from
+    initial states, with final-state errors: a dict of h0, c0, dh_n, dc_n)."""
     import oracle
     nthreads = nthreads or os.cpu_count() or 1
     lengths, x, G = w.lengths, w.x, w.G
@@ -113,8 +123,10 @@ def run_oracle(w, seqs=None, nthreads=None, bf16_products=False):
         lengths = w.lengths[seqs]
         x = np.concatenate([w.x[st[s]:st[s + 1]] for s in seqs])
         G = np.concatenate([w.G[st[s]:st[s + 1]] for s in seqs])
+    st = states or {}
     return oracle.lstm_stack(lengths, x, w.layers, w.spec.num_directions, w.spec.hidden_size, G=G,
-                             nthreads=nthreads, bf16_products=bf16_products)
+                             nthreads=nthreads, bf16_products=bf16_products, h0=st.get("h0"), c0=st.get("c0"),
+                             dh_n=st.get("dh_n"), dc_n=st.get("dc_n"))
 
 
 def select_rows(w, seqs, arr):
@@ -129,6 +141,9 @@ def _pairs(gpu, ref, grads):
         for l, (g, r) in enumerate(zip(gpu["grads"], ref["grads"])):
             for k in ("W", "R", "b", "peep"):
                 out.append((f"L{l}.d{k}", g[k], r[k]))
+        for k in ("dh0", "dc0"):
+            if k in gpu:
+                out.append((k, gpu[k], ref[k]))
     return out
 
 
