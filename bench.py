@@ -454,6 +454,9 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", type=int, default=3)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="diagnostic: the workload with only this many sequences (same distributions); "
+                         "0 = the workload as defined")
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--no-comparators", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -464,7 +467,7 @@ def main():
     args.warmup = max(3, args.warmup)
 
     from padding_free_variable_gb300 import synthetic
-    w = synthetic.workload(args.workload)
+    w = synthetic.workload(args.workload, batch=args.batch or None)
     spec = w.spec
     N, T, B = w.N, w.T, len(w.lengths)
     config = {"workload": spec.name, "sequences": B, "frames_per_step": N, "max_length": T,

@@ -497,10 +497,14 @@ lstm_status lstm_plan_recurrent_groups(const lstm_plan* plan, int32_t pass, int3
                                        int32_t* slots_per_group);
 
 /* Test hook for bf16 layers wider than one cluster (H > 512): -1 = automatic
- * (the persistent kernel with R resident across H/16 CTAs per direction where
- * it applies -- H a multiple of 64 up to 1024, at most 256 sequences -- else
- * per-step launches), 0 = per-step launches, 1 = the persistent kernel where it
- * applies.  LSTM_ERR_INVALID_ARG outside -1..1. */
+ * (forward: the persistent kernel with R resident across H/16 CTAs per
+ * direction where it applies -- H a multiple of 64 up to 1024, at most 256
+ * sequences -- else per-step launches; backward: per-step launches), 0 =
+ * per-step launches both ways, 1 = the persistent kernels both ways where they
+ * apply, 2 = the same without thread-block clusters (every CTA reads each
+ * operand tile from L2 itself instead of sharing it by multicast).
+ * lstm_plan_recurrent_config reports the persistent kernels' cluster size in
+ * `variant`.  LSTM_ERR_INVALID_ARG outside -1..2. */
 lstm_status lstm_debug_wide_recurrence(lstm_plan* plan, int32_t mode);
 
 /* Test hook: slots per sequence group of the cluster recurrent kernels (0 =
@@ -518,8 +522,9 @@ lstm_status lstm_debug_sequence_groups(lstm_plan* plan, int32_t slots);
  * buffer is the caller's; steps = 0 turns the stamps off. */
 lstm_status lstm_debug_trace_steps(lstm_plan* plan, int64_t* device_buffer, int32_t steps);
 
-/* Test hook (-1 = off).  Grid recurrent kernels: CTA `cta` never announces
- * its steps, so the others' barrier waits run out.  Cluster recurrent
+/* Test hook (-1 = off).  Grid recurrent kernels, and the persistent kernels of
+ * layers wider than a cluster: CTA `cta` (of direction 0) never announces its
+ * (first) step, so the others' barrier waits run out.  Cluster recurrent
  * kernels: CTA `cta` of the first direction's cluster withholds the
  * completion signal of its first tensor-core product, so its own bounded wait
  * runs out (and, with the bulk exchange, its peers' waits for its operand).

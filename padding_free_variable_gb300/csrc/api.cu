@@ -515,6 +515,7 @@ WideArgs wide_args(const Plan& p, const lstm_layer_shape& s, const lstm_layer_pa
     w.ga = ga; w.peep = prm.peep; w.cbuf = cbuf;
     w.h0 = sio.h0; w.c0 = sio.c0; w.dh_n = sio.dh_n; w.dc_n = sio.dc_n; w.dc0 = sio.dc0;
     w.status = p.d_status; w.wait_limit_ns = p.wait_limit_ns;
+    w.debug_skip_cta = p.debug_skip_cta;
     return w;
 }
 
@@ -657,7 +658,10 @@ lstm_status bwd_impl(const lstm_plan* plan, const lstm_layer_shape* shape,
     if (wide_step_path(p, s)) {
         const StepScratch q = step_scratch(p, s);
         char* sc = (char*)scratch;
-        if (p.wide_mode != 0 && rec_wide_supported(p, H, nd, bf16)) {
+        // the persistent backward streams every step's gate errors into all H/16 CTAs: it runs
+        // only on request (wide_mode 1); by default the per-step products (GEMM tiles with far
+        // more operand reuse) are faster
+        if (p.wide_mode >= 1 && rec_wide_supported(p, H, nd, bf16)) {
             // R^T [ndir][H][4H] bf16: the resident B operand of each CTA's R^T da product
             __nv_bfloat16* rt16 = (__nv_bfloat16*)(sc + q.rt);
             for (int d = 0; d < nd; ++d)

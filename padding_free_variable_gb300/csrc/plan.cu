@@ -482,7 +482,7 @@ lstm_status lstm_plan_recurrent_groups(const lstm_plan* plan, int32_t pass, int3
 
 lstm_status lstm_debug_wide_recurrence(lstm_plan* plan, int32_t mode)
 {
-    if (!plan || mode < -1 || mode > 1) return LSTM_ERR_INVALID_ARG;
+    if (!plan || mode < -1 || mode > 2) return LSTM_ERR_INVALID_ARG;
     plan->p.wide_mode = mode;
     return LSTM_OK;
 }

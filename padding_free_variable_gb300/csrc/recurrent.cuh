@@ -112,6 +112,9 @@ struct WideArgs {
     unsigned* ctr;                         // [ndir] step counters (set by the launchers)
     DeviceStatus* status;
     unsigned long long wait_limit_ns;
+    long long* trace;                      // optional phase stamps of CTA 0 of each direction (as RecArgs)
+    int trace_steps;
+    int debug_skip_cta;                    // test hook: this CTA of direction 0 never publishes step 0 (-1 off)
 };
 
 bool rec_wide_supported(const Plan& p, int H, int ndir, bool bf16);

@@ -16,6 +16,11 @@
 //    a double-buffered global array that L2 holds; each CTA streams it in
 //    128-row x 64-column TMA tiles through a 4-stage ring into tcgen05.mma
 //    (M = 128 rows of the batch per tile, fp32 accumulator in tensor memory).
+//    Every CTA of a direction needs the same tiles, so CTAs are grouped in
+//    clusters of CS (4 when the device co-schedules them): each tile is read
+//    from L2 once per cluster and multicast into all CS CTAs, and each CTA's
+//    MMA completion frees the ring stage in all of them (multicast commit), so
+//    L2 serves a quarter of the bytes.
 //  * The cell runs on the accumulator rows: thread r of a 128-thread half
 //    reads row r of its tile from tensor memory (all four gates of the CTA's
 //    16 units), adds the step's input projection and runs the forward cell
@@ -27,6 +32,7 @@
 //    once the counter reaches s times the CTAs per direction (acquire; the wait
 //    is bounded and a timeout is recorded in the plan's status word).
 // One cooperative launch runs every step of both directions.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -82,6 +88,14 @@ __device__ __forceinline__ bool grid_wait(const unsigned* ctr, unsigned target, 
     return __syncthreads_or(fail) == 0;
 }
 
+// Phase stamps of CTA 0 of each direction, in the recurrent kernels' slots [kernel][dir][step][8]:
+// 0 step start, 1 after the grid barrier, 5 product in tensor memory, 3 cell done, 4 published.
+__device__ __forceinline__ void wstamp(const WideArgs& a, bool bwd, int dir, int cta, int s, int k)
+{
+    if (threadIdx.x == 0 && a.trace && cta == 0 && s < a.trace_steps)
+        a.trace[(((size_t)(bwd ? 1 : 0) * a.ndir + dir) * a.trace_steps + s) * 8 + k] = clock64();
+}
+
 // Shared memory of both kernels: the resident weight slice (KBW blocks of rowsW x 128 B),
 // the operand ring, barriers.
 struct WideSmem {
@@ -121,18 +135,23 @@ size_t wide_smem_bytes(int KBW, int rowsW)
 
 // One step's product: D[tile m][rows][N] = sum over the KB blocks of A (the operand tiles,
 // streamed from rows ybase + 128 m) times the resident weight slice (B, N rows per block).
-// Thread 0 issues the TMA tiles, thread 32 the MMAs; it_prod / it_cons carry the ring
-// position across steps (each only in its own thread).
+// Thread 0 arms the ring and issues its share of the TMA tiles (with CS > 1: tile i by
+// cluster rank i mod CS, multicast to the whole cluster), thread 32 issues the MMAs and frees
+// each stage in every CTA of the cluster; it_prod / it_cons carry the ring position across
+// steps (each only in its own thread).
+template <int CS>
 __device__ __forceinline__ bool wide_product(const WideSmem& m, const CUtensorMap* mapA, int ybase, int MT, int KB,
                                              int N, uint32_t tmem, const WideArgs& a, uint32_t& it_prod,
-                                             uint32_t& it_cons, bool& w_ready, unsigned where)
+                                             uint32_t& it_cons, bool& w_ready, unsigned where, int crank)
 {
     bool ok = true;
+    constexpr uint16_t kMask = (uint16_t)((1u << CS) - 1u);
     if (threadIdx.x == 0) {
         fence_async_global();
         for (int t = 0; t < MT && ok; ++t)
             for (int kb = 0; kb < KB; ++kb, ++it_prod) {
                 const int st = (int)(it_prod % kWStages);
+                // the stage's previous tile has been consumed by every CTA of the cluster
                 if (it_prod >= (uint32_t)kWStages &&
                     !tc::mbar_wait(&m.empty[st], ((it_prod / kWStages) - 1) & 1, a.wait_limit_ns)) {
                     record_failure(a.status, LSTM_ERR_TIMEOUT, where | 0x1000u);
@@ -140,7 +159,11 @@ __device__ __forceinline__ bool wide_product(const WideSmem& m, const CUtensorMa
                     break;
                 }
                 tc::mbar_arrive_expect_tx(&m.full[st], kWTile);
-                tc::tma_load_2d(m.ring + (size_t)st * kWTile, mapA, &m.full[st], kb * 64, ybase + t * 128);
+                if (CS == 1)
+                    tc::tma_load_2d(m.ring + (size_t)st * kWTile, mapA, &m.full[st], kb * 64, ybase + t * 128);
+                else if ((t * KB + kb) % CS == crank)
+                    tc::tma_load_2d_multicast(m.ring + (size_t)st * kWTile, mapA, &m.full[st], kb * 64, ybase + t * 128,
+                                              kMask);
                 m.counters[0] = (int)it_prod + 1;
             }
     } else if (threadIdx.x == 32) {
@@ -168,23 +191,47 @@ __device__ __forceinline__ bool wide_product(const WideSmem& m, const CUtensorMa
                 for (int kk = 0; kk < 4; ++kk)
                     tc::mma_bf16_ss(tmem + (uint32_t)(t * N), tc::sdesc_sw128(a0 + kk * 32), tc::sdesc_sw128(b0 + kk * 32),
                                     idesc, (kb | kk) != 0 ? 1u : 0u);
-                tc::mma_commit(&m.empty[st]);
+                if (CS == 1) tc::mma_commit(&m.empty[st]);
+                else tc::mma_commit_multicast(&m.empty[st], kMask);
                 m.counters[1] = (int)it_cons + 1;
             }
         tc::mma_commit(m.mma_bar);
     }
+    // the other lanes of the issuing warps wait here instead of polling while lane 0 works
+    // (measured: polling lanes of the same warp slowed the issue loops ~3x)
+    if (threadIdx.x < 64) __syncwarp();
     return ok;
 }
 
-// After a timeout: no TMA tile may still be landing in this CTA's shared memory and no MMA
-// may still be using tensor memory when the CTA leaves (bounded waits).
-__device__ __forceinline__ void wide_teardown(const WideSmem& m, uint32_t it_prod, uint32_t mma_phase)
+// Before a CTA leaves: no TMA tile may still be landing in its shared memory, no MMA may
+// still use its tensor memory, and (clusters) no peer's stage-release may still be on its way
+// to its barriers -- every wait bounded.  A clean run waits only for the peers' releases of
+// the ring's last uses; after a timeout the CTA also waits for the tiles it armed and then
+// gives any multicast tile already issued by a peer a millisecond to land.
+template <int CS>
+__device__ __forceinline__ void wide_finish(const WideSmem& m, uint32_t it_prod, uint32_t mma_phase, bool failed)
 {
     if (threadIdx.x == 0) {
-        for (uint32_t it = (uint32_t)max(0, m.counters[1]); it < it_prod; ++it)
-            tc::mbar_wait(&m.full[it % kWStages], (it / kWStages) & 1, kWTeardownNs);
-        tc::mbar_wait(m.mma_bar, (mma_phase - 1) & 1, kWTeardownNs);
+        if (failed) {
+            for (uint32_t it = (uint32_t)max(0, m.counters[1]); it < it_prod; ++it)
+                tc::mbar_wait(&m.full[it % kWStages], (it / kWStages) & 1, kWTeardownNs);
+            tc::mbar_wait(m.mma_bar, (mma_phase - 1) & 1, kWTeardownNs);
+        }
         tc::mbar_wait(m.w_bar, 0, kWTeardownNs);
+        if (CS > 1) {
+            // each stage's last use released by every CTA of the cluster
+            for (uint32_t it = it_prod > (uint32_t)kWStages ? it_prod - kWStages : 0u; it < it_prod; ++it)
+                tc::mbar_wait(&m.empty[it % kWStages], (it / kWStages) & 1, failed ? 1000000ull : kWTeardownNs);
+            if (failed) {
+                const unsigned long long t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 1000000ull) {
+                }
+            }
+        }
+    }
+    if (CS > 1) {
+        __syncthreads();
+        cooperative_groups::this_cluster().sync();      // no peer still sends into this CTA
     }
 }
 
@@ -193,6 +240,7 @@ __device__ __forceinline__ void wide_teardown(const WideSmem& m, uint32_t it_pro
 // Forward.  Operand array a.xbuf: [ndir][2][B][H] bf16, step s reads parity s & 1 and
 // writes parity (s + 1) & 1.  Tensor maps: mapW = R as [ndir*4H][H] (boxes 16 rows x 64),
 // mapA = a.xbuf as [ndir*2*B][H] (boxes 128 rows x 64).
+template <int CS>
 __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, const __grid_constant__ CUtensorMap mapW,
                                                                   const __grid_constant__ CUtensorMap mapA)
 {
@@ -202,13 +250,14 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, c
     const int nd4H = a.ndir * 4 * H, ndH = a.ndir * H;
     const WideSmem m = wide_smem(KB, 64);
     const int warp = threadIdx.x >> 5;
+    const int crank = CS > 1 ? (int)cooperative_groups::this_cluster().block_rank() : 0;
     const int tile = threadIdx.x >> 7, j = threadIdx.x;      // this thread's row of the batch
     unsigned* ctr = a.ctr + dir;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kWStages; ++s) {
             tc::mbar_init(&m.full[s], 1);
-            tc::mbar_init(&m.empty[s], 1);
+            tc::mbar_init(&m.empty[s], CS);          // one release from each CTA of the cluster
         }
         tc::mbar_init(m.mma_bar, 1);
         tc::mbar_init(m.w_bar, 1);
@@ -235,6 +284,7 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, c
     tc::tc_fence_before_sync();
     __syncthreads();
     tc::tc_fence_after_sync();
+    if (CS > 1) cooperative_groups::this_cluster().sync();   // every peer's barriers exist before any multicast
     const uint32_t tmem = *m.tmem_slot;
 
     float creg[kWU];                                  // c of this thread's row, step to step
@@ -247,6 +297,7 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, c
         const int n = a.bs[t];
         const int n_prev = dir == 0 ? (t >= 1 ? n : 0) : (t + 1 < T ? a.bs[t + 1] : 0);
         const int row = a.off[t] + j;
+        wstamp(a, false, dir, cta, s, 0);
         // this row's input projection (own data: loaded before the wait)
         float pre[4][kWU];
         if (j < n) {
@@ -259,13 +310,23 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, c
                     pre[g][4 * q] = x.x; pre[g][4 * q + 1] = x.y; pre[g][4 * q + 2] = x.z; pre[g][4 * q + 3] = x.w;
                 }
         }
+        if (s + 1 < T) {           // the next step's pre-activations of this row into L2
+            const int t2 = dir == 0 ? s + 1 : T - 2 - s;
+            if (j < a.bs[t2]) {
+                const float* g2 = a.ga + (size_t)(a.off[t2] + j) * nd4H + (size_t)dir * 4 * H + u0;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) asm volatile("prefetch.global.L2 [%0];" ::"l"(g2 + g * H));
+            }
+        }
         if (s > 0 && !grid_wait(ctr, (unsigned)(NC * s), a, 0x90000u | (unsigned)s)) { failed = true; break; }
+        wstamp(a, false, dir, cta, s, 1);
         const int MT = (n_prev + 127) / 128;
         if (MT > 0) {
-            bool ok = wide_product(m, &mapA, (dir * 2 + (s & 1)) * B, MT, KB, 64, tmem, a, it_prod, it_cons, w_ready,
-                                   0xA0000u | (unsigned)(s & 0xfff));
+            bool ok = wide_product<CS>(m, &mapA, (dir * 2 + (s & 1)) * B, MT, KB, 64, tmem, a, it_prod, it_cons,
+                                       w_ready, 0xA0000u | (unsigned)(s & 0xfff), crank);
             ++mma_phase;
-            ok = tc::mbar_wait(m.mma_bar, (mma_phase - 1) & 1, a.wait_limit_ns) && ok;
+            // one thread polls the product's completion; the others wait at the barrier below
+            if (threadIdx.x == 0) ok = tc::mbar_wait(m.mma_bar, (mma_phase - 1) & 1, a.wait_limit_ns) && ok;
             if (__syncthreads_or(!ok)) {
                 record_failure(a.status, LSTM_ERR_TIMEOUT, 0xB0000u | (unsigned)s);
                 failed = true;
@@ -273,6 +334,7 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, c
             }
             tc::tc_fence_after_sync();
         }
+        wstamp(a, false, dir, cta, s, 5);
         // R h_{t-1} of this row: tensor-memory lane = row within the tile (warp-uniform loads)
         float acc[4][kWU];
         if (tile < MT) {
@@ -291,10 +353,12 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, c
 #pragma unroll
                 for (int k = 0; k < kWU; ++k) acc[g][k] = 0.f;
         }
+        // the cell; h_t goes to the exchange buffer first and is published at once, the layer's
+        // own outputs (gates, c, y) are stored after the publish, off the peers' critical path
+        float hv[kWU], cv[kWU], gv[4][kWU];
+        const int len = j < B ? a.len[j] : 0;
+        const size_t so = j < B ? ((size_t)dir * B + a.perm[j]) * H + u0 : 0;          // caller-order state
         if (j < n) {
-            const int len = a.len[j];
-            const size_t so = ((size_t)dir * B + a.perm[j]) * H + u0;          // caller-order state
-            float hv[kWU], cv[kWU], gv[4][kWU];
 #pragma unroll
             for (int k = 0; k < kWU; ++k) {
                 const float cp = j < n_prev ? creg[k] : (a.c0 ? __ldg(a.c0 + so + k) : 0.f);
@@ -308,6 +372,28 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, c
                 gv[0][k] = ig; gv[1][k] = fg; gv[2][k] = zg; gv[3][k] = og;
                 cv[k] = c; hv[k] = h; creg[k] = c;
             }
+        }
+        uint32_t hb[kWU / 2];
+#pragma unroll
+        for (int e = 0; e < kWU / 2; ++e) {
+            const __nv_bfloat162 p2 = __floats2bfloat162_rn(j < n ? hv[2 * e] : 0.f, j < n ? hv[2 * e + 1] : 0.f);
+            hb[e] = *reinterpret_cast<const uint32_t*>(&p2);
+        }
+        if (j < n && s + 1 < T) {    // h_t for the next step's product
+            uint4* xb = reinterpret_cast<uint4*>(a.xbuf + (((size_t)dir * 2 + ((s + 1) & 1)) * B + j) * H + u0);
+            xb[0] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+            xb[1] = make_uint4(hb[4], hb[5], hb[6], hb[7]);
+        }
+        fence_async_global();       // this thread's h_t is read by the peers' TMA tiles
+        tc::tc_fence_before_sync();
+        __syncthreads();
+        wstamp(a, false, dir, cta, s, 3);
+        if (threadIdx.x == 0 && !(s == 0 && dir == 0 && cta == a.debug_skip_cta)) {   // (test hook)
+            __threadfence();
+            red_release_add(ctr, 1u);
+        }
+        wstamp(a, false, dir, cta, s, 4);
+        if (j < n) {
             float* gw = a.ga + (size_t)row * nd4H + (size_t)dir * 4 * H + u0;
             const size_t yo = (size_t)row * ndH + (size_t)dir * H + u0;
 #pragma unroll
@@ -319,21 +405,10 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, c
                 *reinterpret_cast<float4*>(a.cbuf + yo + 4 * q) = make_float4(cv[4 * q], cv[4 * q + 1], cv[4 * q + 2], cv[4 * q + 3]);
                 *reinterpret_cast<float4*>(a.y + yo + 4 * q) = make_float4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
             }
-            uint32_t hb[kWU / 2];
-#pragma unroll
-            for (int e = 0; e < kWU / 2; ++e) {
-                const __nv_bfloat162 p2 = __floats2bfloat162_rn(hv[2 * e], hv[2 * e + 1]);
-                hb[e] = *reinterpret_cast<const uint32_t*>(&p2);
-            }
             if (a.y_lo) {
                 uint4* yl = reinterpret_cast<uint4*>(a.y_lo + yo);
                 yl[0] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
                 yl[1] = make_uint4(hb[4], hb[5], hb[6], hb[7]);
-            }
-            if (s + 1 < T) {         // h_t for the next step's product
-                uint4* xb = reinterpret_cast<uint4*>(a.xbuf + (((size_t)dir * 2 + ((s + 1) & 1)) * B + j) * H + u0);
-                xb[0] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
-                xb[1] = make_uint4(hb[4], hb[5], hb[6], hb[7]);
             }
             if (a.h_n && ((dir == 0 && t == len - 1) || (dir == 1 && t == 0 && len > 0)))
 #pragma unroll
@@ -342,17 +417,8 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, c
                     if (a.c_n) a.c_n[so + k] = cv[k];
                 }
         }
-        fence_async_global();       // this thread's h_t is read by the peers' TMA tiles
-        tc::tc_fence_before_sync();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            __threadfence();
-            red_release_add(ctr, 1u);
-        }
     }
-    if (failed) wide_teardown(m, it_prod, mma_phase);
-    // the weight slice's loads have landed even when no step needed a product (bounded)
-    if (threadIdx.x == 0) tc::mbar_wait(m.w_bar, 0, kWTeardownNs);
+    wide_finish<CS>(m, it_prod, mma_phase, failed);
     tc::tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) {
@@ -364,6 +430,7 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, c
 // BPTT.  Operand array a.xbuf: [ndir][2][B][4H] bf16 gate errors (step s reads parity s & 1,
 // the errors of the previous BPTT step; writes parity (s + 1) & 1).  mapW = R^T as
 // [ndir*H][4H] (boxes 16 rows x 64), mapA = a.xbuf as [ndir*2*B][4H] (boxes 128 rows x 64).
+template <int CS>
 __global__ void __launch_bounds__(kWT, 1) lstm_rec_bwd_wide_kernel(WideArgs a, const __grid_constant__ CUtensorMap mapW,
                                                                   const __grid_constant__ CUtensorMap mapA)
 {
@@ -373,13 +440,14 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_bwd_wide_kernel(WideArgs a, c
     const int nd4H = a.ndir * 4 * H, ndH = a.ndir * H;
     const WideSmem m = wide_smem(KB, kWU);
     const int warp = threadIdx.x >> 5;
+    const int crank = CS > 1 ? (int)cooperative_groups::this_cluster().block_rank() : 0;
     const int tile = threadIdx.x >> 7, j = threadIdx.x;
     unsigned* ctr = a.ctr + dir;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kWStages; ++s) {
             tc::mbar_init(&m.full[s], 1);
-            tc::mbar_init(&m.empty[s], 1);
+            tc::mbar_init(&m.empty[s], CS);          // one release from each CTA of the cluster
         }
         tc::mbar_init(m.mma_bar, 1);
         tc::mbar_init(m.w_bar, 1);
@@ -398,6 +466,7 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_bwd_wide_kernel(WideArgs a, c
     tc::tc_fence_before_sync();
     __syncthreads();
     tc::tc_fence_after_sync();
+    if (CS > 1) cooperative_groups::this_cluster().sync();   // every peer's barriers exist before any multicast
     const uint32_t tmem = *m.tmem_slot;
 
     float dcc[kWU];                                   // the cell-state error carried to the step before
@@ -412,6 +481,7 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_bwd_wide_kernel(WideArgs a, c
         const int n_prev = dir == 0 ? (t >= 1 ? n : 0) : (t + 1 < T ? a.bs[t + 1] : 0);
         const int prev_base = dir == 0 ? (t >= 1 ? a.off[t - 1] : 0) : (t + 1 < T ? a.off[t + 1] : 0);
         const int row = a.off[t] + j;
+        wstamp(a, true, dir, cta, s, 0);
         // own operands of the row (before the wait): gates, c_t, c_{t-1}, dy
         float gv[4][kWU], cv[kWU], cp[kWU], dyv[kWU];
         const size_t so = j < B ? ((size_t)dir * B + a.perm[j]) * H + u0 : 0;   // caller-order state
@@ -436,14 +506,26 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_bwd_wide_kernel(WideArgs a, c
                 cp[4 * q] = p4.x; cp[4 * q + 1] = p4.y; cp[4 * q + 2] = p4.z; cp[4 * q + 3] = p4.w;
             }
         }
+        if (s + 1 < T) {           // the next step's gates, c and dy of this row into L2
+            const int t2 = dir == 0 ? T - 2 - s : s + 1;
+            if (j < a.bs[t2]) {
+                const int r2 = a.off[t2] + j;
+                const float* g2 = a.ga + (size_t)r2 * nd4H + (size_t)dir * 4 * H + u0;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) asm volatile("prefetch.global.L2 [%0];" ::"l"(g2 + g * H));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(a.cbuf + (size_t)r2 * ndH + (size_t)dir * H + u0));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(a.dy + (size_t)r2 * ndH + (size_t)dir * H + u0));
+            }
+        }
         if (s > 0 && !grid_wait(ctr, (unsigned)(NC * s), a, 0xC0000u | (unsigned)s)) { failed = true; break; }
+        wstamp(a, true, dir, cta, s, 1);
         // R^T da of the step after this one (recurrence order), for the rows that have one
         const int MT = (n_next + 127) / 128;
         if (MT > 0) {
-            bool ok = wide_product(m, &mapA, (dir * 2 + (s & 1)) * B, MT, KB, kWU, tmem, a, it_prod, it_cons, w_ready,
-                                   0xD0000u | (unsigned)(s & 0xfff));
+            bool ok = wide_product<CS>(m, &mapA, (dir * 2 + (s & 1)) * B, MT, KB, kWU, tmem, a, it_prod, it_cons,
+                                       w_ready, 0xD0000u | (unsigned)(s & 0xfff), crank);
             ++mma_phase;
-            ok = tc::mbar_wait(m.mma_bar, (mma_phase - 1) & 1, a.wait_limit_ns) && ok;
+            if (threadIdx.x == 0) ok = tc::mbar_wait(m.mma_bar, (mma_phase - 1) & 1, a.wait_limit_ns) && ok;
             if (__syncthreads_or(!ok)) {
                 record_failure(a.status, LSTM_ERR_TIMEOUT, 0xE0000u | (unsigned)s);
                 failed = true;
@@ -451,6 +533,7 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_bwd_wide_kernel(WideArgs a, c
             }
             tc::tc_fence_after_sync();
         }
+        wstamp(a, true, dir, cta, s, 5);
         float dhr[kWU];
         if (tile < MT) {
             uint32_t r[16];
@@ -462,10 +545,12 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_bwd_wide_kernel(WideArgs a, c
 #pragma unroll
             for (int k = 0; k < kWU; ++k) dhr[k] = 0.f;
         }
+        // the cell; the bf16 gate errors go to the exchange buffer and are published first, the
+        // fp32 gate errors (for the weight gradients) are stored after the publish
+        float da[4][kWU];
         if (j < n) {
             const bool has_next = j < n_next;
             const bool real = !a.padded || t < a.len[j];
-            float da[4][kWU];
 #pragma unroll
             for (int k = 0; k < kWU; ++k) {
                 float dai = 0.f, daf = 0.f, daz = 0.f, dao = 0.f, carry_out = 0.f;
@@ -481,19 +566,13 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_bwd_wide_kernel(WideArgs a, c
                     daf = dc * cp[k] * fg * (1.f - fg);
                     daz = dc * ig * (1.f - zg * zg);
                     carry_out = dc * fg + dai * m.peep[k] + daf * m.peep[kWU + k];
-                    if (j >= n_prev && a.dc0) a.dc0[so + k] = carry_out;       // the sequence's first step
                 }
                 da[0][k] = dai; da[1][k] = daf; da[2][k] = daz; da[3][k] = dao;
                 dcc[k] = carry_out;
             }
-            float* gw = a.ga + (size_t)row * nd4H + (size_t)dir * 4 * H + u0;
+            if (s + 1 < T) {         // bf16 gate errors for the next step's product
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-#pragma unroll
-                for (int q = 0; q < kWU / 4; ++q)
-                    *reinterpret_cast<float4*>(gw + g * H + 4 * q) =
-                        make_float4(da[g][4 * q], da[g][4 * q + 1], da[g][4 * q + 2], da[g][4 * q + 3]);
-                if (s + 1 < T) {     // bf16 gate errors for the next step's product
+                for (int g = 0; g < 4; ++g) {
                     uint32_t w8[kWU / 2];
 #pragma unroll
                     for (int e = 0; e < kWU / 2; ++e) {
@@ -510,13 +589,26 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_bwd_wide_kernel(WideArgs a, c
         fence_async_global();
         tc::tc_fence_before_sync();
         __syncthreads();
-        if (threadIdx.x == 0) {
+        wstamp(a, true, dir, cta, s, 3);
+        if (threadIdx.x == 0 && !(s == 0 && dir == 0 && cta == a.debug_skip_cta)) {   // (test hook)
             __threadfence();
             red_release_add(ctr, 1u);
         }
+        wstamp(a, true, dir, cta, s, 4);
+        if (j < n) {
+            float* gw = a.ga + (size_t)row * nd4H + (size_t)dir * 4 * H + u0;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+#pragma unroll
+                for (int q = 0; q < kWU / 4; ++q)
+                    *reinterpret_cast<float4*>(gw + g * H + 4 * q) =
+                        make_float4(da[g][4 * q], da[g][4 * q + 1], da[g][4 * q + 2], da[g][4 * q + 3]);
+            if (j >= n_prev && a.dc0 && (!a.padded || t < a.len[j]))     // the sequence's first step: dL/dc0
+#pragma unroll
+                for (int k = 0; k < kWU; ++k) a.dc0[so + k] = dcc[k];
+        }
     }
-    if (failed) wide_teardown(m, it_prod, mma_phase);
-    if (threadIdx.x == 0) tc::mbar_wait(m.w_bar, 0, kWTeardownNs);
+    wide_finish<CS>(m, it_prod, mma_phase, failed);
     tc::tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) {
@@ -544,28 +636,60 @@ size_t rec_wide_xbuf_bytes(const Plan& p, int H, int ndir, bool bwd)
     return (size_t)ndir * 2 * p.B * (bwd ? 4 * H : H) * 2;
 }
 
-static lstm_status wide_launch(const Plan& p, const void* fn, WideArgs& a, const CUtensorMap& mapW,
-                               const CUtensorMap& mapA, size_t smem, cudaStream_t s)
+constexpr int kWCluster = 4;     // CTAs sharing each operand tile by multicast
+
+// One cooperative launch of `fn1` (no clusters) or `fn4` (clusters of kWCluster sharing the
+// operand tiles): the clustered form when the plan allows it and the device co-schedules all
+// of its clusters, else the plain one.  *cs receives the cluster size used.
+static lstm_status wide_launch(const Plan& p, const void* fn1, const void* fn4, WideArgs& a, const CUtensorMap& mapW,
+                               const CUtensorMap& mapA, size_t smem, cudaStream_t s, int* cs)
 {
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    const int grid = a.ndir * a.NC;
+    CUtensorMap mw = mapW, ma = mapA;
+    void* args[] = {&a, &mw, &ma};
+    if (cudaMemsetAsync(a.ctr, 0, sizeof(unsigned) * 2, s) != cudaSuccess) return LSTM_ERR_CUDA;
+    if (p.wide_mode != 2 && a.NC % kWCluster == 0 &&
+        cudaFuncSetAttribute(fn4, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[2];
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kWT);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kWCluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeCooperative;
+        attr[1].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;                       // the occupancy query takes the cluster shape only
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, fn4, &cfg) == cudaSuccess && clusters * kWCluster >= grid) {
+            cfg.numAttrs = 2;
+            if (cudaLaunchKernelExC(&cfg, fn4, args) == cudaSuccess) {
+                *cs = kWCluster;
+                return LSTM_OK;
+            }
+        }
+        cudaGetLastError();                      // fall back to the plain launch below
+    }
+    if (cudaFuncSetAttribute(fn1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
         cudaGetLastError();
         return LSTM_ERR_UNSUPPORTED;
     }
-    const int grid = a.ndir * a.NC;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kWT, smem) != cudaSuccess || per_sm < 1 ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn1, kWT, smem) != cudaSuccess || per_sm < 1 ||
         per_sm * p.num_sms < grid) {
         cudaGetLastError();
         return LSTM_ERR_UNSUPPORTED;
     }
-    if (cudaMemsetAsync(a.ctr, 0, sizeof(unsigned) * 2, s) != cudaSuccess) return LSTM_ERR_CUDA;
-    CUtensorMap mw = mapW, ma = mapA;
-    void* args[] = {&a, &mw, &ma};
-    const cudaError_t e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kWT), args, smem, s);
+    const cudaError_t e = cudaLaunchCooperativeKernel(fn1, dim3(grid), dim3(kWT), args, smem, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return e == cudaErrorCooperativeLaunchTooLarge ? LSTM_ERR_UNSUPPORTED : LSTM_ERR_CUDA;
     }
+    *cs = 1;
     return LSTM_OK;
 }
 
@@ -573,6 +697,7 @@ lstm_status rec_wide_fwd_launch(const Plan& p, WideArgs a, const void* R, cudaSt
 {
     a.NC = a.H / kWU;
     a.ctr = p.d_flags;
+    a.trace = p.d_trace; a.trace_steps = p.trace_steps;
     CUtensorMap mapW, mapA;
     memset(&mapW, 0, sizeof(mapW));
     memset(&mapA, 0, sizeof(mapA));
@@ -580,9 +705,12 @@ lstm_status rec_wide_fwd_launch(const Plan& p, WideArgs a, const void* R, cudaSt
         !make_map_bf16_sw128(&mapA, a.xbuf, a.ndir * 2 * a.B, a.H, a.H, 128))
         return LSTM_ERR_UNSUPPORTED;
     trace_begin(p, K_REC_FWD, s);
-    const lstm_status st = wide_launch(p, (const void*)lstm_rec_fwd_wide_kernel, a, mapW, mapA,
-                                       wide_smem_bytes(a.H / 64, 64), s);
+    int cs = 0;
+    const lstm_status st = wide_launch(p, (const void*)lstm_rec_fwd_wide_kernel<1>,
+                                       (const void*)lstm_rec_fwd_wide_kernel<kWCluster>, a, mapW, mapA,
+                                       wide_smem_bytes(a.H / 64, 64), s, &cs);
     trace_end(p, K_REC_FWD, s, st == LSTM_OK ? 1 : 0);
+    p.last_rec_variant[0] = cs;
     return st;
 }
 
@@ -591,6 +719,7 @@ lstm_status rec_wide_bwd_launch(const Plan& p, WideArgs a, const void* RT, float
 {
     a.NC = a.H / kWU;
     a.ctr = p.d_flags;
+    a.trace = p.d_trace; a.trace_steps = p.trace_steps;
     CUtensorMap mapW, mapA;
     memset(&mapW, 0, sizeof(mapW));
     memset(&mapA, 0, sizeof(mapA));
@@ -598,8 +727,10 @@ lstm_status rec_wide_bwd_launch(const Plan& p, WideArgs a, const void* RT, float
         !make_map_bf16_sw128(&mapA, a.xbuf, a.ndir * 2 * a.B, 4 * a.H, 4 * a.H, 128))
         return LSTM_ERR_UNSUPPORTED;
     trace_begin(p, K_REC_BWD, s);
-    lstm_status st = wide_launch(p, (const void*)lstm_rec_bwd_wide_kernel, a, mapW, mapA,
-                                 wide_smem_bytes(4 * a.H / 64, kWU), s);
+    int cs = 0;
+    lstm_status st = wide_launch(p, (const void*)lstm_rec_bwd_wide_kernel<1>, (const void*)lstm_rec_bwd_wide_kernel<kWCluster>,
+                                 a, mapW, mapA, wide_smem_bytes(4 * a.H / 64, kWU), s, &cs);
+    p.last_rec_variant[1] = cs;
     int launched = st == LSTM_OK ? 1 : 0;
     if (st == LSTM_OK) {
         st = param_sums_launch(p, a.ga, a.cbuf, a.H, a.ndir, db, dpeep, sum_scratch, s, a.c0);

@@ -73,6 +73,18 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// The same load multicast to the CTAs of `mask` in this thread's cluster: the box lands at
+// the same shared-memory offset in each, completing on the mbarrier at the same offset.
+__device__ __forceinline__ void tma_load_2d_multicast(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                                      int y, uint16_t mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;"
+        ::"r"(smem_u32(smem_dst)), "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask)
+        : "memory");
+}
+
 // 2-D tiled store of one box from shared memory (bulk-group completion, this thread's
 // group).  Parts of the box outside the tensor are not written.  x as for the load.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src, int x, int y)
@@ -189,6 +201,16 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
+}
+
+// Arrive on the mbarrier at `bar`'s offset in every CTA of `mask` (this cluster) once every
+// MMA issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        ::"r"(smem_u32(bar)), "h"(mask)
+        : "memory");
 }
 
 // 32 lanes x 32 bits, 16 consecutive columns: thread i gets lane (base+i).

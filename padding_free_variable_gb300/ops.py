@@ -89,10 +89,13 @@ class Plan:
         check(_lib.load().lstm_plan_recurrent_config(self.handle, int(bool(backward)), ctypes.byref(k),
                                                      ctypes.byref(g), ctypes.byref(m), ctypes.byref(v)),
               "lstm_plan_recurrent_config")
-        return {"kernel": ("none", "grid", "cluster", "step_launches", "persistent_wide")[k.value],
-                "ctas_per_direction": g.value,
-                "product": ("cuda_cores", "mma_sync", "tcgen05")[m.value],
-                "exchange": "bulk" if v.value & 1 else "barrier", "tma_tiles": bool(v.value & 2)}
+        kind = ("none", "grid", "cluster", "step_launches", "persistent_wide")[k.value]
+        out = {"kernel": kind, "ctas_per_direction": g.value, "product": ("cuda_cores", "mma_sync", "tcgen05")[m.value]}
+        if kind == "persistent_wide":
+            out["cluster_size"] = v.value            # CTAs sharing each operand tile by multicast
+        else:
+            out.update({"exchange": "bulk" if v.value & 1 else "barrier", "tma_tiles": bool(v.value & 2)})
+        return out
 
     def recurrent_groups(self, backward: bool = False) -> tuple:
         """(sequence groups, sorted slots per group) of the last forward (or backward) recurrent launch."""

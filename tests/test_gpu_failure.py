@@ -88,3 +88,45 @@ def test_cluster_kernels_timeout_is_reported_and_context_survives(variant):
     y, dx = stack.step(x, G)
     assert plan.poll() == _lib.LSTM_OK
     assert torch.equal(y, y_ref) and torch.equal(dx, dx_ref)
+
+
+@pytest.mark.parametrize("mode", [1, 2], ids=["clusters", "no-clusters"])
+def test_wide_persistent_kernels_timeout_is_reported_and_context_survives(mode):
+    """The persistent kernels of layers wider than a cluster wait at a grid barrier every step.
+    With the test hook one CTA never announces its first step: the other CTAs' bounded waits
+    run out, every CTA leaves through its bounded teardown (with clusters: after its peers'
+    stage releases and the final cluster barrier), LSTM_ERR_TIMEOUT is reported, and a clean
+    rerun in the same context gives the reference results bit for bit (forward and backward)."""
+    from padding_free_variable_gb300 import _lib, ops, synthetic
+    from gpu_harness import device_layers
+    w = synthetic.custom(2, 1, 16, 576, [9, 4, 13, 7, 11], seed=4, dtype="bf16", weight_range=0.05)
+    layers = device_layers(w)
+
+    def fresh():
+        plan = ops.Plan(w.lengths)
+        plan.debug_wide_recurrence(mode)
+        return plan, ops.PackedLSTMStack(plan, layers, 16, 576, 2, True)
+
+    x = torch.from_numpy(w.x).cuda().to(torch.bfloat16)
+    G = torch.from_numpy(w.G).cuda()
+    ref_plan, ref_stack = fresh()
+    y_ref, dx_ref = (t.clone() for t in ref_stack.step(x, G))
+    assert ref_plan.poll() == _lib.LSTM_OK
+    assert ref_plan.recurrent_config(False)["kernel"] == "persistent_wide"
+    plan, stack = fresh()
+    plan.set_wait_limit(50_000_000)          # 50 ms
+    plan.pack(x, stack.x_packed)
+    plan.pack(G, stack.dy_packed)
+    plan.debug_skip_arrival(3)
+    stack.forward_packed()
+    assert plan.poll() == _lib.LSTM_ERR_TIMEOUT
+    plan.debug_skip_arrival(-1)
+    stack.forward_packed()
+    assert plan.poll() == _lib.LSTM_OK
+    plan.debug_skip_arrival(3)
+    stack.backward_packed()
+    assert plan.poll() == _lib.LSTM_ERR_TIMEOUT
+    plan.debug_skip_arrival(-1)
+    y, dx = stack.step(x, G)
+    assert plan.poll() == _lib.LSTM_OK
+    assert torch.equal(y, y_ref) and torch.equal(dx, dx_ref)

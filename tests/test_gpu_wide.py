@@ -52,14 +52,23 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("mode", [1, 2], ids=["clusters", "no-clusters"])
 @pytest.mark.parametrize("case", CASES, ids=[f"nd{c[0]}-L{c[1]}-H{c[3]}-B{len(c[4])}" for c in CASES])
-def test_persistent_wide_matches_oracle(case):
+def test_persistent_wide_matches_oracle(case, mode):
+    """Both forms of the launch: clusters of 4 CTAs sharing each operand tile by multicast
+    (mode 1), and every CTA loading every tile itself (mode 2)."""
     nd, nl, D, H, lengths = case
     w = synthetic.custom(nd, nl, D, H, lengths, seed=13 + H, dtype="bf16", weight_range=0.05)
-    gpu = _run(w, 1)
+    gpu = _run(w, mode)
     for backward in (False, True):
         cfg = gpu["plan"].recurrent_config(backward)
         assert cfg["kernel"] == "persistent_wide" and cfg["ctas_per_direction"] == H // 16, cfg
+    if mode == 2:
+        assert gpu["plan"].recurrent_config(False)["cluster_size"] == 1
+    auto = _run(w, -1)           # the automatic choice: persistent forward, per-step backward
+    assert auto["plan"].recurrent_config(False)["kernel"] == "persistent_wide"
+    assert auto["plan"].recurrent_config(True)["kernel"] == "step_launches"
+    compare_all(auto, run_oracle(w), TOL_BF16, label=f"wide automatic {case}")
     compare_all(gpu, run_oracle(w), TOL_BF16, label=f"wide persistent {case}")
     compare_all(gpu, run_oracle(w, bf16_products=True), TOL_BF16_EMULATED, label=f"wide persistent {case}",
                 against="oracle-bf16-products")
@@ -81,10 +90,11 @@ def test_persistent_wide_padded_and_states():
     compare_all(gpu, run_oracle(w, states=st), TOL_BF16, label="wide persistent states")
 
 
-def test_persistent_wide_bitwise_repeatable():
+@pytest.mark.parametrize("mode", [1, 2], ids=["clusters", "no-clusters"])
+def test_persistent_wide_bitwise_repeatable(mode):
     w = synthetic.custom(2, 1, 32, 1024, list(np.random.default_rng(9).integers(1, 20, 30)), seed=2,
                          dtype="bf16", weight_range=0.05)
-    a, b = _run(w, 1), _run(w, 1)
+    a, b = _run(w, mode), _run(w, mode)
     for k in ("y", "dx", "h_n", "c_n"):
         assert np.array_equal(a[k], b[k]), k
     for ga, gb in zip(a["grads"], b["grads"]):
