@@ -403,13 +403,18 @@ const char* lstm_status_string(lstm_status status);
  * CTA owns ceil(H / ctas) units; the count is capped at the SMs available. */
 lstm_status lstm_plan_set_ctas_per_direction(lstm_plan* plan, int32_t ctas);
 
-/* Engine of the matrix products.  0 (default): tensor cores -- the bf16
- * input projection on tcgen05 (TMA-fed, fp32 accumulation in tensor memory)
- * and the recurrent kernels' per-step products on warp-level MMA wherever a
- * CTA's R fragments fit in registers (fp32 operands as three tf32 products,
- * about 22 bits per product; bf16 as one product).  1: CUDA-core FFMA for
- * every product (a comparator).  The fp32 path's other products use CUDA
- * cores under both settings. */
+/* Engine of the matrix products.  0 (default): tensor cores.  The input
+ * projection and the backward's dX, dW and dR run on the tcgen05 GEMM
+ * (TMA-fed, fp32 accumulation in tensor memory); fp32 operands are split
+ * into three bf16 pieces and the six piece products above 2^-24 of the
+ * leading one are accumulated, over K slices of at most 1024 whose partial
+ * sums are added on CUDA cores, so the products keep fp32 accuracy.  The
+ * recurrent products run on tcgen05 in the cluster kernels (fp32 as the
+ * same three pieces) and in the persistent kernels and per-step launches of
+ * bf16 layers wider than a cluster, and on warp-level mma.sync in the grid
+ * kernels that cover the remaining shapes (fp32 as three tf32 products).  1: CUDA-core FFMA for
+ * every product, a comparator: the GEMMs on CUDA cores and the recurrence
+ * in the grid kernels.  LSTM_ERR_INVALID_ARG outside 0..1. */
 lstm_status lstm_plan_set_gemm_engine(lstm_plan* plan, int32_t engine);
 
 /* Test hook: only the forward input projection of lstm_fwd,
@@ -497,15 +502,27 @@ lstm_status lstm_plan_recurrent_groups(const lstm_plan* plan, int32_t pass, int3
                                        int32_t* slots_per_group);
 
 /* Test hook for bf16 layers wider than one cluster (H > 512): -1 = automatic
- * (forward: the persistent kernel with R resident across H/16 CTAs per
- * direction where it applies -- H a multiple of 64 up to 1024, at most 256
- * sequences -- else per-step launches; backward: per-step launches), 0 =
- * per-step launches both ways, 1 = the persistent kernels both ways where they
- * apply, 2 = the same without thread-block clusters (every CTA reads each
- * operand tile from L2 itself instead of sharing it by multicast).
+ * (the persistent kernels with R, resp. R^T, resident across H/16 CTAs per
+ * direction where they apply -- H a multiple of 64 up to 1024, at most 256
+ * sequences -- the backward only in its form with clusters of four CTAs that
+ * split the gate errors between them; else per-step launches), 0 = per-step
+ * launches both ways, 1 = the persistent kernels both ways where they apply
+ * (either form), 2 = the persistent kernels without thread-block clusters
+ * (forward: every CTA reads each operand tile from L2 itself instead of
+ * sharing it by multicast; backward: every CTA streams all 4H gate errors).
  * lstm_plan_recurrent_config reports the persistent kernels' cluster size in
  * `variant`.  LSTM_ERR_INVALID_ARG outside -1..2. */
 lstm_status lstm_debug_wide_recurrence(lstm_plan* plan, int32_t mode);
+
+/* Tuning hook of the persistent kernels of layers wider than a cluster: caps
+ * the depth of the operand ring each CTA streams the step's operand tiles
+ * through (`max_stages` >= 2; 0 = no cap, as many 16 KB stages as the shared
+ * memory beside the resident weights holds, at most 8; -1 = leave the cap as
+ * it is), and reports the depths the last forward and backward persistent
+ * launches used (0 when none ran).  Results do not depend on the depth.
+ * Either output pointer may be NULL.  LSTM_ERR_INVALID_ARG for a NULL plan or
+ * max_stages outside -1, 0, 2..64. */
+lstm_status lstm_debug_wide_stages(lstm_plan* plan, int32_t max_stages, int32_t* used_fwd, int32_t* used_bwd);
 
 /* Test hook: slots per sequence group of the cluster recurrent kernels (0 =
  * automatic: the smallest multiple of 8 that gives every cluster an SM of its

@@ -32,7 +32,7 @@ EXPORTED = (
     "lstm_stepwise_scratch_bytes", "lstm_fwd_stepwise", "lstm_bwd_stepwise", "lstm_debug_cluster_variant",
     "lstm_plan_recurrent_groups", "lstm_debug_sequence_groups", "lstm_state_scratch_bytes", "lstm_fwd_state",
     "lstm_bwd_state", "lstm_plan_create_segments", "lstm_segments_host", "lstm_plan_create_window",
-    "lstm_form_batches", "lstm_debug_wide_recurrence",
+    "lstm_form_batches", "lstm_debug_wide_recurrence", "lstm_debug_wide_stages",
 )
 
 KERNEL_KINDS = ("pack", "unpack", "input_gemm", "rec_fwd", "rec_bwd", "gemm_dx", "gemm_dw", "gemm_dr", "convert")
@@ -113,6 +113,7 @@ def _declare(lib):
                                vp]),
         "lstm_debug_sequence_groups": (c, [vp, i32]),
         "lstm_debug_wide_recurrence": (c, [vp, i32]),
+        "lstm_debug_wide_stages": (c, [vp, i32, pi32, pi32]),
         "lstm_stepwise_scratch_bytes": (ctypes.c_size_t, [vp, ctypes.POINTER(LayerShape)]),
         "lstm_fwd_stepwise": (c, [vp, ctypes.POINTER(LayerShape), ctypes.POINTER(LayerParams), vp, vp, vp, vp, vp,
                                   vp, vp, vp]),

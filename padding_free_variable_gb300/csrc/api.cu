@@ -658,10 +658,9 @@ lstm_status bwd_impl(const lstm_plan* plan, const lstm_layer_shape* shape,
     if (wide_step_path(p, s)) {
         const StepScratch q = step_scratch(p, s);
         char* sc = (char*)scratch;
-        // the persistent backward streams every step's gate errors into all H/16 CTAs: it runs
-        // only on request (wide_mode 1); by default the per-step products (GEMM tiles with far
-        // more operand reuse) are faster
-        if (p.wide_mode >= 1 && rec_wide_supported(p, H, nd, bf16)) {
+        // the persistent backward (automatic: only its K-split cluster form; when that cannot
+        // be launched, the per-step launches below)
+        if (p.wide_mode != 0 && rec_wide_supported(p, H, nd, bf16)) {
             // R^T [ndir][H][4H] bf16: the resident B operand of each CTA's R^T da product
             __nv_bfloat16* rt16 = (__nv_bfloat16*)(sc + q.rt);
             for (int d = 0; d < nd; ++d)

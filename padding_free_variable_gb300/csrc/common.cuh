@@ -48,6 +48,7 @@ struct Plan {
     int32_t forced_group_rows = 0;  // cluster kernels: sorted slots per sequence group (0 = automatic)
     int32_t wide_mode = -1;         // bf16 layers wider than a cluster: -1 automatic, 0 per-step launches,
                                     // 1 the persistent kernel where it applies
+    int32_t wide_stages = 0;        // persistent wide kernels: cap on the operand-ring depth (0 = none)
     int32_t gemm_engine = 0;        // 0 = tensor cores for bf16 operands, 1 = CUDA cores
     int device = 0;
     int num_sms = 0;
@@ -79,6 +80,7 @@ struct Plan {
     mutable int32_t last_rec_variant[2] = {0, 0}; // cluster kernels: bit 0 bulk exchange, bit 1 TMA tiles
     mutable int32_t last_rec_groups[2] = {0, 0};  // cluster kernels: sequence groups
     mutable int32_t last_rec_grp_rows[2] = {0, 0}; // cluster kernels: sorted slots per group
+    mutable int32_t last_rec_stages[2] = {0, 0};   // persistent wide kernels: operand-ring depth
 };
 
 // Bracket a launch sequence of `kind`; `kernels` = launches it issued.  A

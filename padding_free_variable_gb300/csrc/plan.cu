@@ -487,6 +487,15 @@ lstm_status lstm_debug_wide_recurrence(lstm_plan* plan, int32_t mode)
     return LSTM_OK;
 }
 
+lstm_status lstm_debug_wide_stages(lstm_plan* plan, int32_t max_stages, int32_t* used_fwd, int32_t* used_bwd)
+{
+    if (!plan || max_stages < -1 || max_stages == 1 || max_stages > 64) return LSTM_ERR_INVALID_ARG;
+    if (max_stages >= 0) plan->p.wide_stages = max_stages;
+    if (used_fwd) *used_fwd = plan->p.last_rec_stages[0];
+    if (used_bwd) *used_bwd = plan->p.last_rec_stages[1];
+    return LSTM_OK;
+}
+
 lstm_status lstm_debug_sequence_groups(lstm_plan* plan, int32_t slots)
 {
     if (!plan || slots < 0 || slots > 128) return LSTM_ERR_INVALID_ARG;

@@ -90,6 +90,7 @@ lstm_status rec_cluster_bwd_launch(const Plan& p, const RecConfig& c, RecArgs a,
 // buffered global array read back with TMA; a bounded grid barrier per step.
 struct WideArgs {
     int T, B, H, ndir, NC;                 // NC: CTAs per direction (set by the launchers)
+    int stages;                            // operand-ring depth (set by the launchers)
     int padded;
     const int32_t* bs;
     const int32_t* off;

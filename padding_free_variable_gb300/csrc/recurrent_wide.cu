@@ -7,30 +7,35 @@
 // of bf16, more than one cluster holds, so one launch spreads it over H/16
 // CTAs per direction (64 for H = 1024, both directions on 128 SMs):
 //
-//  * CTA c owns units [16c, 16c + 16) and their 64 gate rows.  Its slice of R
-//    (forward: 64 gate rows x H) or of R^T (backward: 16 units x 4H) is loaded
-//    once by TMA into shared memory (128 KB) and stays there: it is the MMA's
-//    B operand (N = 64, resp. 16) for every step.
+//  * CTA c owns units [16c, 16c + 16).  Forward: its 64 gate rows of R (64 x H)
+//    are loaded once by TMA into shared memory (128 KB) and stay there as the
+//    MMA's B operand (N = 64) for every step.
 //  * Every step the whole previous operand -- h_{t-1} forward, the previous
 //    step's gate errors backward, bf16, one row per active sequence -- sits in
-//    a double-buffered global array that L2 holds; each CTA streams it in
-//    128-row x 64-column TMA tiles through a 4-stage ring into tcgen05.mma
-//    (M = 128 rows of the batch per tile, fp32 accumulator in tensor memory).
-//    Every CTA of a direction needs the same tiles, so CTAs are grouped in
-//    clusters of CS (4 when the device co-schedules them): each tile is read
+//    a double-buffered global array that L2 holds; a CTA streams the part it
+//    needs in 128-row x 64-column TMA tiles through a ring of up to 4 stages
+//    into tcgen05.mma (M = 128 rows of the batch per tile, fp32 accumulator in
+//    tensor memory).  Forward, every CTA needs all of h_{t-1}: CTAs are grouped
+//    in clusters of CS (4 when the device co-schedules them), each tile is read
 //    from L2 once per cluster and multicast into all CS CTAs, and each CTA's
-//    MMA completion frees the ring stage in all of them (multicast commit), so
-//    L2 serves a quarter of the bytes.
+//    MMA completion frees the ring stage in all of them (multicast commit).
+//  * Backward, R^T da needs all 4H gate errors for every unit.  In clusters of
+//    four CTAs, CTA r takes only gate r's H errors against R^T rows of the
+//    cluster's 64 units (64 x H resident, N = 64), so it streams a quarter of
+//    the operand; the 16-column pieces of the partial products are exchanged
+//    through distributed shared memory and added by the units' owners in a
+//    fixed order.  Without clusters each CTA takes all 4H errors against its
+//    own 16 units' R^T rows (16 x 4H, N = 16).
 //  * The cell runs on the accumulator rows: thread r of a 128-thread half
 //    reads row r of its tile from tensor memory (all four gates of the CTA's
-//    16 units), adds the step's input projection and runs the forward cell
-//    (or its BPTT); it keeps its row's cell state (forward) or cell-state
+//    16 units) and runs the forward cell (or its BPTT) after adding the step's
+//    input projection; it keeps its row's cell state (forward) or cell-state
 //    error (backward) in registers from step to step, and writes its 16 new
 //    values of the operand for the next step.
 //  * Steps of a direction are separated by a grid barrier: each CTA adds 1 to
-//    the direction's counter (release) after its writes; a CTA starts step s
-//    once the counter reaches s times the CTAs per direction (acquire; the wait
-//    is bounded and a timeout is recorded in the plan's status word).
+//    the direction's counter (release) after its operand writes; a CTA starts
+//    step s once the counter reaches s times the CTAs per direction (acquire;
+//    the wait is bounded and a timeout is recorded in the plan's status word).
 // One cooperative launch runs every step of both directions.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
@@ -49,7 +54,8 @@ namespace {
 
 constexpr int kWU = 16;                          // units per CTA
 constexpr int kWT = 256;                         // threads: rows 0..127 and 128..255 of the batch
-constexpr int kWStages = 4;                      // operand ring stages
+constexpr int kWMaxStages = 4;                   // operand ring stages at most (measured: 6 stages ran
+                                                 // ~5% slower than 4 on H = 1024)
 constexpr uint32_t kWTile = 128 * 64 * 2;        // one operand tile: 128 rows x 64 bf16
 constexpr unsigned long long kWTeardownNs = 1000000000ull;
 
@@ -65,6 +71,36 @@ __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v)
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ void fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// Distributed shared memory: a peer's address, a store into it, a release arrival on a peer's
+// mbarrier, and the acquiring wait that pairs with it.
+__device__ __forceinline__ uint32_t mapa_w(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f4(uint32_t addr, float x, float y, float z, float w)
+{
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(x), "f"(y), "f"(z), "f"(w)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(tc::smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 
 // Every CTA of the direction has published step `target` (bounded wait by thread 0; the
 // outcome is the same for every thread of the CTA).
@@ -97,74 +133,94 @@ __device__ __forceinline__ void wstamp(const WideArgs& a, bool bwd, int dir, int
 }
 
 // Shared memory of both kernels: the resident weight slice (KBW blocks of rowsW x 128 B),
-// the operand ring, barriers.
+// the operand ring (`stages` tiles), the partial-product inbox of the split backward, barriers.
 struct WideSmem {
     uint8_t* w;
     uint8_t* ring;
+    float* inbox;           // split backward: [3 senders][B rows][16] fp32 (16-byte chunks swizzled)
     uint64_t* full;
     uint64_t* empty;
     uint64_t* mma_bar;
     uint64_t* w_bar;
+    uint64_t* inbox_bar;    // split backward: one arrival from each of the three peers per step
     uint32_t* tmem_slot;
     int* counters;          // [0] loads issued, [1] tiles consumed (teardown after a timeout)
     float* peep;            // [3][16]
+    int stages;
 };
 
-__device__ __forceinline__ WideSmem wide_smem(int KBW, int rowsW)
+__device__ __forceinline__ WideSmem wide_smem(int KBW, int rowsW, int stages, size_t inbox_bytes)
 {
     extern __shared__ unsigned char smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     WideSmem m;
+    m.stages = stages;
     m.w = base;
     m.ring = base + (size_t)KBW * rowsW * 128;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(m.ring + (size_t)kWStages * kWTile);
+    m.inbox = reinterpret_cast<float*>(m.ring + (size_t)stages * kWTile);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(m.inbox) + inbox_bytes);
     m.full = bars;
-    m.empty = bars + kWStages;
-    m.mma_bar = bars + 2 * kWStages;
+    m.empty = bars + stages;
+    m.mma_bar = bars + 2 * stages;
     m.w_bar = m.mma_bar + 1;
-    m.tmem_slot = reinterpret_cast<uint32_t*>(m.w_bar + 1);
+    m.inbox_bar = m.mma_bar + 2;
+    m.tmem_slot = reinterpret_cast<uint32_t*>(m.mma_bar + 3);
     m.counters = reinterpret_cast<int*>(m.tmem_slot + 2);
     m.peep = reinterpret_cast<float*>(m.counters + 2);
     return m;
 }
 
-size_t wide_smem_bytes(int KBW, int rowsW)
+size_t wide_smem_bytes(int KBW, int rowsW, int stages, size_t inbox_bytes)
 {
-    return 1024 + (size_t)KBW * rowsW * 128 + (size_t)kWStages * kWTile + (2 * kWStages + 2) * 8 + 16 + 3 * kWU * 4;
+    return 1024 + (size_t)KBW * rowsW * 128 + (size_t)stages * kWTile + inbox_bytes + (2 * stages + 3) * 8 + 16 +
+           3 * kWU * 4;
 }
 
-// One step's product: D[tile m][rows][N] = sum over the KB blocks of A (the operand tiles,
-// streamed from rows ybase + 128 m) times the resident weight slice (B, N rows per block).
+// Position in the operand ring: tiles issued (or consumed) so far, and the stage and lap
+// parity of the next one, advanced without division.
+struct RingPos {
+    uint32_t it = 0;
+    int st = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void advance(int stages)
+    {
+        ++it;
+        if (++st == stages) { st = 0; ph ^= 1u; }
+    }
+};
+
+// One step's product: D[tile m][rows][N] = sum over the KB blocks of A (the operand tiles of
+// columns x0 + 64 kb, streamed from rows ybase + 128 m) times the resident weight slice (B, N
+// rows per block).
 // Thread 0 arms the ring and issues its share of the TMA tiles (with CS > 1: tile i by
 // cluster rank i mod CS, multicast to the whole cluster), thread 32 issues the MMAs and frees
-// each stage in every CTA of the cluster; it_prod / it_cons carry the ring position across
+// each stage in every CTA of the cluster; prod / cons carry the ring position across
 // steps (each only in its own thread).
 template <int CS>
-__device__ __forceinline__ bool wide_product(const WideSmem& m, const CUtensorMap* mapA, int ybase, int MT, int KB,
-                                             int N, uint32_t tmem, const WideArgs& a, uint32_t& it_prod,
-                                             uint32_t& it_cons, bool& w_ready, unsigned where, int crank)
+__device__ __forceinline__ bool wide_product(const WideSmem& m, const CUtensorMap* mapA, int x0, int ybase, int MT,
+                                             int KB, int N, uint32_t tmem, const WideArgs& a, RingPos& prod,
+                                             RingPos& cons, bool& w_ready, unsigned where, int crank)
 {
     bool ok = true;
     constexpr uint16_t kMask = (uint16_t)((1u << CS) - 1u);
     if (threadIdx.x == 0) {
         fence_async_global();
         for (int t = 0; t < MT && ok; ++t)
-            for (int kb = 0; kb < KB; ++kb, ++it_prod) {
-                const int st = (int)(it_prod % kWStages);
+            for (int kb = 0; kb < KB; ++kb, prod.advance(m.stages)) {
+                const int st = prod.st;
                 // the stage's previous tile has been consumed by every CTA of the cluster
-                if (it_prod >= (uint32_t)kWStages &&
-                    !tc::mbar_wait(&m.empty[st], ((it_prod / kWStages) - 1) & 1, a.wait_limit_ns)) {
+                if (prod.it >= (uint32_t)m.stages && !tc::mbar_wait(&m.empty[st], prod.ph ^ 1u, a.wait_limit_ns)) {
                     record_failure(a.status, LSTM_ERR_TIMEOUT, where | 0x1000u);
                     ok = false;
                     break;
                 }
                 tc::mbar_arrive_expect_tx(&m.full[st], kWTile);
                 if (CS == 1)
-                    tc::tma_load_2d(m.ring + (size_t)st * kWTile, mapA, &m.full[st], kb * 64, ybase + t * 128);
+                    tc::tma_load_2d(m.ring + (size_t)st * kWTile, mapA, &m.full[st], x0 + kb * 64, ybase + t * 128);
                 else if ((t * KB + kb) % CS == crank)
-                    tc::tma_load_2d_multicast(m.ring + (size_t)st * kWTile, mapA, &m.full[st], kb * 64, ybase + t * 128,
-                                              kMask);
-                m.counters[0] = (int)it_prod + 1;
+                    tc::tma_load_2d_multicast(m.ring + (size_t)st * kWTile, mapA, &m.full[st], x0 + kb * 64,
+                                              ybase + t * 128, kMask);
+                m.counters[0] = (int)prod.it + 1;
             }
     } else if (threadIdx.x == 32) {
         if (!w_ready) {
@@ -177,9 +233,9 @@ __device__ __forceinline__ bool wide_product(const WideSmem& m, const CUtensorMa
         const uint32_t idesc = tc::idesc_bf16_f32(128, N);
         const uint32_t wbytes = (uint32_t)N * 128;               // one block of the weight slice
         for (int t = 0; t < MT && ok; ++t)
-            for (int kb = 0; kb < KB; ++kb, ++it_cons) {
-                const int st = (int)(it_cons % kWStages);
-                if (!tc::mbar_wait(&m.full[st], (it_cons / kWStages) & 1, a.wait_limit_ns)) {
+            for (int kb = 0; kb < KB; ++kb, cons.advance(m.stages)) {
+                const int st = cons.st;
+                if (!tc::mbar_wait(&m.full[st], cons.ph, a.wait_limit_ns)) {
                     record_failure(a.status, LSTM_ERR_TIMEOUT, where | 0x3000u);
                     ok = false;
                     break;
@@ -193,7 +249,7 @@ __device__ __forceinline__ bool wide_product(const WideSmem& m, const CUtensorMa
                                     idesc, (kb | kk) != 0 ? 1u : 0u);
                 if (CS == 1) tc::mma_commit(&m.empty[st]);
                 else tc::mma_commit_multicast(&m.empty[st], kMask);
-                m.counters[1] = (int)it_cons + 1;
+                m.counters[1] = (int)cons.it + 1;
             }
         tc::mma_commit(m.mma_bar);
     }
@@ -204,24 +260,26 @@ __device__ __forceinline__ bool wide_product(const WideSmem& m, const CUtensorMa
 }
 
 // Before a CTA leaves: no TMA tile may still be landing in its shared memory, no MMA may
-// still use its tensor memory, and (clusters) no peer's stage-release may still be on its way
-// to its barriers -- every wait bounded.  A clean run waits only for the peers' releases of
-// the ring's last uses; after a timeout the CTA also waits for the tiles it armed and then
-// gives any multicast tile already issued by a peer a millisecond to land.
-template <int CS>
+// still use its tensor memory, and (clusters) no peer's stage-release or partial product may
+// still be on its way to it -- every wait bounded.  A clean run waits only for the peers'
+// releases of the ring's last uses; after a timeout the CTA also waits for the tiles it armed
+// and then gives any multicast tile already issued by a peer a millisecond to land.
+// MC: CTAs sharing each operand tile (multicast); CL: the launch has clusters.
+template <int MC, bool CL>
 __device__ __forceinline__ void wide_finish(const WideSmem& m, uint32_t it_prod, uint32_t mma_phase, bool failed)
 {
     if (threadIdx.x == 0) {
+        const uint32_t ns = (uint32_t)m.stages;
         if (failed) {
             for (uint32_t it = (uint32_t)max(0, m.counters[1]); it < it_prod; ++it)
-                tc::mbar_wait(&m.full[it % kWStages], (it / kWStages) & 1, kWTeardownNs);
+                tc::mbar_wait(&m.full[it % ns], (it / ns) & 1, kWTeardownNs);
             tc::mbar_wait(m.mma_bar, (mma_phase - 1) & 1, kWTeardownNs);
         }
         tc::mbar_wait(m.w_bar, 0, kWTeardownNs);
-        if (CS > 1) {
+        if (MC > 1) {
             // each stage's last use released by every CTA of the cluster
-            for (uint32_t it = it_prod > (uint32_t)kWStages ? it_prod - kWStages : 0u; it < it_prod; ++it)
-                tc::mbar_wait(&m.empty[it % kWStages], (it / kWStages) & 1, failed ? 1000000ull : kWTeardownNs);
+            for (uint32_t it = it_prod > ns ? it_prod - ns : 0u; it < it_prod; ++it)
+                tc::mbar_wait(&m.empty[it % ns], (it / ns) & 1, failed ? 1000000ull : kWTeardownNs);
             if (failed) {
                 const unsigned long long t0 = global_timer_ns();
                 while (global_timer_ns() - t0 < 1000000ull) {
@@ -229,7 +287,7 @@ __device__ __forceinline__ void wide_finish(const WideSmem& m, uint32_t it_prod,
             }
         }
     }
-    if (CS > 1) {
+    if (CL) {
         __syncthreads();
         cooperative_groups::this_cluster().sync();      // no peer still sends into this CTA
     }
@@ -248,14 +306,14 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, c
     const int KB = H / 64;
     const int dir = blockIdx.x / NC, cta = blockIdx.x - dir * NC, u0 = cta * kWU;
     const int nd4H = a.ndir * 4 * H, ndH = a.ndir * H;
-    const WideSmem m = wide_smem(KB, 64);
+    const WideSmem m = wide_smem(KB, 64, a.stages, 0);
     const int warp = threadIdx.x >> 5;
     const int crank = CS > 1 ? (int)cooperative_groups::this_cluster().block_rank() : 0;
     const int tile = threadIdx.x >> 7, j = threadIdx.x;      // this thread's row of the batch
     unsigned* ctr = a.ctr + dir;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kWStages; ++s) {
+        for (int s = 0; s < a.stages; ++s) {
             tc::mbar_init(&m.full[s], 1);
             tc::mbar_init(&m.empty[s], CS);          // one release from each CTA of the cluster
         }
@@ -290,7 +348,8 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, c
     float creg[kWU];                                  // c of this thread's row, step to step
 #pragma unroll
     for (int k = 0; k < kWU; ++k) creg[k] = 0.f;
-    uint32_t it_prod = 0, it_cons = 0, mma_phase = 0;
+    RingPos prod, cons;
+    uint32_t mma_phase = 0;
     bool w_ready = false, failed = false;
     for (int s = 0; s < T && !failed; ++s) {
         const int t = dir == 0 ? s : T - 1 - s;
@@ -322,7 +381,7 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, c
         wstamp(a, false, dir, cta, s, 1);
         const int MT = (n_prev + 127) / 128;
         if (MT > 0) {
-            bool ok = wide_product<CS>(m, &mapA, (dir * 2 + (s & 1)) * B, MT, KB, 64, tmem, a, it_prod, it_cons,
+            bool ok = wide_product<CS>(m, &mapA, 0, (dir * 2 + (s & 1)) * B, MT, KB, 64, tmem, a, prod, cons,
                                        w_ready, 0xA0000u | (unsigned)(s & 0xfff), crank);
             ++mma_phase;
             // one thread polls the product's completion; the others wait at the barrier below
@@ -335,23 +394,18 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, c
             tc::tc_fence_after_sync();
         }
         wstamp(a, false, dir, cta, s, 5);
-        // R h_{t-1} of this row: tensor-memory lane = row within the tile (warp-uniform loads)
-        float acc[4][kWU];
-        if (tile < MT) {
-            uint32_t r[4][16];
+        // R h_{t-1} of this row (tensor-memory lane = row within the tile, warp-uniform loads),
+        // added into the pre-activations one gate at a time
+        if (tile < MT) {                  // (warp-uniform: the loads are warp-collective)
 #pragma unroll
-            for (int g = 0; g < 4; ++g)
-                tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(tile * 64 + g * 16), r[g]);
-            tc::tmem_wait_ld();
+            for (int g = 0; g < 4; ++g) {
+                uint32_t r[16];
+                tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(tile * 64 + g * 16), r);
+                tc::tmem_wait_ld();
+                if (j < n_prev)
 #pragma unroll
-            for (int g = 0; g < 4; ++g)
-#pragma unroll
-                for (int k = 0; k < kWU; ++k) acc[g][k] = j < n_prev ? __uint_as_float(r[g][k]) : 0.f;
-        } else {
-#pragma unroll
-            for (int g = 0; g < 4; ++g)
-#pragma unroll
-                for (int k = 0; k < kWU; ++k) acc[g][k] = 0.f;
+                    for (int k = 0; k < kWU; ++k) pre[g][k] += __uint_as_float(r[k]);
+            }
         }
         // the cell; h_t goes to the exchange buffer first and is published at once, the layer's
         // own outputs (gates, c, y) are stored after the publish, off the peers' critical path
@@ -362,11 +416,11 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, c
 #pragma unroll
             for (int k = 0; k < kWU; ++k) {
                 const float cp = j < n_prev ? creg[k] : (a.c0 ? __ldg(a.c0 + so + k) : 0.f);
-                const float ig = sigm_w(pre[0][k] + acc[0][k] + m.peep[k] * cp);
-                const float fg = sigm_w(pre[1][k] + acc[1][k] + m.peep[kWU + k] * cp);
-                const float zg = tanh_w(pre[2][k] + acc[2][k]);
+                const float ig = sigm_w(pre[0][k] + m.peep[k] * cp);
+                const float fg = sigm_w(pre[1][k] + m.peep[kWU + k] * cp);
+                const float zg = tanh_w(pre[2][k]);
                 float c = fg * cp + ig * zg;
-                const float og = sigm_w(pre[3][k] + acc[3][k] + m.peep[2 * kWU + k] * c);
+                const float og = sigm_w(pre[3][k] + m.peep[2 * kWU + k] * c);
                 float h = og * tanh_w(c);
                 if (a.padded && t >= len) { c = 0.f; h = 0.f; }
                 gv[0][k] = ig; gv[1][k] = fg; gv[2][k] = zg; gv[3][k] = og;
@@ -388,10 +442,9 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, c
         tc::tc_fence_before_sync();
         __syncthreads();
         wstamp(a, false, dir, cta, s, 3);
-        if (threadIdx.x == 0 && !(s == 0 && dir == 0 && cta == a.debug_skip_cta)) {   // (test hook)
-            __threadfence();
+        // the release add is cumulative over the CTA's writes ordered before it by the barrier
+        if (threadIdx.x == 0 && !(s == 0 && dir == 0 && cta == a.debug_skip_cta))   // (test hook)
             red_release_add(ctr, 1u);
-        }
         wstamp(a, false, dir, cta, s, 4);
         if (j < n) {
             float* gw = a.ga + (size_t)row * nd4H + (size_t)dir * 4 * H + u0;
@@ -418,7 +471,7 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, c
                 }
         }
     }
-    wide_finish<CS>(m, it_prod, mma_phase, failed);
+    wide_finish<CS, (CS > 1)>(m, prod.it, mma_phase, failed);
     tc::tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) {
@@ -430,49 +483,77 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_fwd_wide_kernel(WideArgs a, c
 // BPTT.  Operand array a.xbuf: [ndir][2][B][4H] bf16 gate errors (step s reads parity s & 1,
 // the errors of the previous BPTT step; writes parity (s + 1) & 1).  mapW = R^T as
 // [ndir*H][4H] (boxes 16 rows x 64), mapA = a.xbuf as [ndir*2*B][4H] (boxes 128 rows x 64).
-template <int CS>
+//  KS = false: CTA c multiplies all 4H gate errors of each row by the R^T rows of its own 16
+//    units (N = 16, K = 4H): every CTA streams the whole operand.
+//  KS = true (clusters of four consecutive CTAs): CTA r of a cluster takes only gate r's H
+//    errors (K = H) against the R^T rows of the cluster's 64 units (N = 64), a quarter of the
+//    operand.  Of its partial product it keeps the 16 columns of its own units and stores the
+//    other three 16-column pieces into their owners' inboxes (distributed shared memory); each
+//    owner adds to its own partial those of ranks r+1, r+2, r+3 (mod 4), in that order, so the
+//    sum does not depend on timing.  A peer writes into an inbox only after the grid barrier that follows the owner's
+//    reading of it, so one inbox per CTA suffices.
+template <bool KS>
 __global__ void __launch_bounds__(kWT, 1) lstm_rec_bwd_wide_kernel(WideArgs a, const __grid_constant__ CUtensorMap mapW,
                                                                   const __grid_constant__ CUtensorMap mapA)
 {
+    constexpr int NU = KS ? 4 * kWU : kWU;            // product columns (units)
+    constexpr uint32_t kTmemCols = 2 * NU < 32 ? 32 : 2 * NU;
     const int H = a.H, T = a.T, B = a.B, NC = a.NC;
-    const int KB = 4 * H / 64;
+    const int KB = (KS ? H : 4 * H) / 64;
     const int dir = blockIdx.x / NC, cta = blockIdx.x - dir * NC, u0 = cta * kWU;
     const int nd4H = a.ndir * 4 * H, ndH = a.ndir * H;
-    const WideSmem m = wide_smem(KB, kWU);
+    const int crank = KS ? (int)cooperative_groups::this_cluster().block_rank() : 0;
+    const int U0 = u0 - crank * kWU;                  // first unit of the product's columns
+    const int x0 = crank * H;                         // first gate-error column of its K range
+    const WideSmem m = wide_smem(KB, NU, a.stages, KS ? (size_t)3 * B * kWU * 4 : 0);
     const int warp = threadIdx.x >> 5;
-    const int crank = CS > 1 ? (int)cooperative_groups::this_cluster().block_rank() : 0;
     const int tile = threadIdx.x >> 7, j = threadIdx.x;
     unsigned* ctr = a.ctr + dir;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kWStages; ++s) {
+        for (int s = 0; s < a.stages; ++s) {
             tc::mbar_init(&m.full[s], 1);
-            tc::mbar_init(&m.empty[s], CS);          // one release from each CTA of the cluster
+            tc::mbar_init(&m.empty[s], 1);
         }
         tc::mbar_init(m.mma_bar, 1);
         tc::mbar_init(m.w_bar, 1);
+        tc::mbar_init(m.inbox_bar, 3);
         m.counters[0] = m.counters[1] = 0;
         tc::fence_mbar_init();
-        // R^T rows of the CTA's 16 units over all 4H gate rows, K-blocks of 64 (2 KB each)
-        tc::mbar_arrive_expect_tx(m.w_bar, (uint32_t)KB * kWU * 128);
+        // R^T rows of the product's units over its K range, K-blocks of 64 (NU x 128 B each)
+        tc::mbar_arrive_expect_tx(m.w_bar, (uint32_t)KB * NU * 128);
         for (int kb = 0; kb < KB; ++kb)
-            tc::tma_load_2d(m.w + (size_t)kb * kWU * 128, &mapW, m.w_bar, kb * 64, dir * H + u0);
+            for (int i = 0; i < NU / kWU; ++i)
+                tc::tma_load_2d(m.w + (size_t)kb * NU * 128 + i * kWU * 128, &mapW, m.w_bar, x0 + kb * 64,
+                                dir * H + U0 + i * kWU);
     }
     if (warp == 0) {
-        tc::tmem_alloc(m.tmem_slot, 32);
+        tc::tmem_alloc(m.tmem_slot, kTmemCols);
         tc::tmem_relinquish();
     }
     for (int i = threadIdx.x; i < 3 * kWU; i += kWT) m.peep[i] = a.peep[(size_t)dir * 3 * H + (i / kWU) * H + u0 + i % kWU];
     tc::tc_fence_before_sync();
     __syncthreads();
     tc::tc_fence_after_sync();
-    if (CS > 1) cooperative_groups::this_cluster().sync();   // every peer's barriers exist before any multicast
+    if (KS) cooperative_groups::this_cluster().sync();   // every peer's inbox barrier exists before any arrival
     const uint32_t tmem = *m.tmem_slot;
+    // this thread's row in each peer's inbox (the slot a peer keeps for this CTA), 16-byte
+    // chunks swizzled by row so that a warp's accesses spread over all banks
+    uint32_t inbox_peer[4] = {0u, 0u, 0u, 0u};
+    if (KS)
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            if (c != crank) {
+                const int slot = ((crank - c + 4) & 3) - 1;
+                inbox_peer[c] = mapa_w(tc::smem_u32(m.inbox + ((size_t)slot * B + (j < B ? j : 0)) * kWU), (uint32_t)c);
+            }
+    const int swz = (j >> 1) & 3;
 
     float dcc[kWU];                                   // the cell-state error carried to the step before
 #pragma unroll
     for (int k = 0; k < kWU; ++k) dcc[k] = 0.f;
-    uint32_t it_prod = 0, it_cons = 0, mma_phase = 0;
+    RingPos prod, cons;
+    uint32_t mma_phase = 0, inbox_phase = 0;
     bool w_ready = false, failed = false;
     for (int s = 0; s < T && !failed; ++s) {
         const int t = dir == 0 ? T - 1 - s : s;
@@ -522,8 +603,8 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_bwd_wide_kernel(WideArgs a, c
         // R^T da of the step after this one (recurrence order), for the rows that have one
         const int MT = (n_next + 127) / 128;
         if (MT > 0) {
-            bool ok = wide_product<CS>(m, &mapA, (dir * 2 + (s & 1)) * B, MT, KB, kWU, tmem, a, it_prod, it_cons,
-                                       w_ready, 0xD0000u | (unsigned)(s & 0xfff), crank);
+            bool ok = wide_product<1>(m, &mapA, x0, (dir * 2 + (s & 1)) * B, MT, KB, NU, tmem, a, prod, cons,
+                                      w_ready, 0xD0000u | (unsigned)(s & 0xfff), 0);
             ++mma_phase;
             if (threadIdx.x == 0) ok = tc::mbar_wait(m.mma_bar, (mma_phase - 1) & 1, a.wait_limit_ns) && ok;
             if (__syncthreads_or(!ok)) {
@@ -535,16 +616,77 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_bwd_wide_kernel(WideArgs a, c
         }
         wstamp(a, true, dir, cta, s, 5);
         float dhr[kWU];
-        if (tile < MT) {
-            uint32_t r[16];
-            tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(tile * kWU), r);
-            tc::tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < kWU; ++k) dhr[k] = j < n_next ? __uint_as_float(r[k]) : 0.f;
-        } else {
+        for (int k = 0; k < kWU; ++k) dhr[k] = 0.f;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        if (!KS) {
+            if (tile < MT) {
+                uint32_t r[16];
+                tc::tmem_ld_32x32b_x16(tmem + lane_base + (uint32_t)(tile * kWU), r);
+                tc::tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < kWU; ++k) dhr[k] = 0.f;
+                for (int k = 0; k < kWU; ++k) dhr[k] = j < n_next ? __uint_as_float(r[k]) : 0.f;
+            }
+        } else if (MT > 0) {
+            // keep the own 16 columns, send the other three pieces to their owners
+            if (tile < MT) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[16];
+                    tc::tmem_ld_32x32b_x16(tmem + lane_base + (uint32_t)(tile * NU + c * kWU), r);
+                    tc::tmem_wait_ld();
+                    if (c == crank) {
+#pragma unroll
+                        for (int k = 0; k < kWU; ++k) dhr[k] = __uint_as_float(r[k]);
+                    } else if (j < n_next) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            st_cluster_f4(inbox_peer[c] + (uint32_t)((q ^ swz) * 16), __uint_as_float(r[4 * q]),
+                                          __uint_as_float(r[4 * q + 1]), __uint_as_float(r[4 * q + 2]),
+                                          __uint_as_float(r[4 * q + 3]));
+                    }
+                }
+            }
+            fence_acq_rel_cluster();
+            __syncthreads();
+            if (threadIdx.x == 0)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (c != crank) mbar_arrive_remote(mapa_w(tc::smem_u32(m.inbox_bar), (uint32_t)c));
+            // the three peers' pieces of this CTA's columns (every thread waits, bounded)
+            int fail = 0;
+            {
+                const uint32_t par = inbox_phase & 1;
+                if (!mbar_try_wait_cluster(m.inbox_bar, par)) {
+                    const unsigned long long t0 = global_timer_ns();
+                    while (!mbar_try_wait_cluster(m.inbox_bar, par))
+                        if (global_timer_ns() - t0 > a.wait_limit_ns || failure_recorded(a.status)) { fail = 1; break; }
+                }
+            }
+            ++inbox_phase;
+            if (__syncthreads_or(fail)) {
+                record_failure(a.status, LSTM_ERR_TIMEOUT, 0xF0000u | (unsigned)s);
+                failed = true;
+                break;
+            }
+            // own partial first, then the peers' in rank order after this CTA's (a fixed order
+            // per unit: bitwise repeatable)
+            if (j < n_next) {
+#pragma unroll
+                for (int slot = 0; slot < 3; ++slot) {
+                    const float4* src = reinterpret_cast<const float4*>(m.inbox + ((size_t)slot * B + j) * kWU);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 v = src[q ^ swz];
+                        dhr[4 * q] += v.x; dhr[4 * q + 1] += v.y; dhr[4 * q + 2] += v.z; dhr[4 * q + 3] += v.w;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < kWU; ++k) dhr[k] = 0.f;
+            }
         }
+        wstamp(a, true, dir, cta, s, 2);
         // the cell; the bf16 gate errors go to the exchange buffer and are published first, the
         // fp32 gate errors (for the weight gradients) are stored after the publish
         float da[4][kWU];
@@ -590,10 +732,8 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_bwd_wide_kernel(WideArgs a, c
         tc::tc_fence_before_sync();
         __syncthreads();
         wstamp(a, true, dir, cta, s, 3);
-        if (threadIdx.x == 0 && !(s == 0 && dir == 0 && cta == a.debug_skip_cta)) {   // (test hook)
-            __threadfence();
+        if (threadIdx.x == 0 && !(s == 0 && dir == 0 && cta == a.debug_skip_cta))   // (test hook)
             red_release_add(ctr, 1u);
-        }
         wstamp(a, true, dir, cta, s, 4);
         if (j < n) {
             float* gw = a.ga + (size_t)row * nd4H + (size_t)dir * 4 * H + u0;
@@ -608,16 +748,39 @@ __global__ void __launch_bounds__(kWT, 1) lstm_rec_bwd_wide_kernel(WideArgs a, c
                 for (int k = 0; k < kWU; ++k) a.dc0[so + k] = dcc[k];
         }
     }
-    wide_finish<CS>(m, it_prod, mma_phase, failed);
+    wide_finish<1, KS>(m, prod.it, mma_phase, failed);
     tc::tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) {
         tc::tc_fence_after_sync();
-        tc::tmem_dealloc(tmem, 32);
+        tc::tmem_dealloc(tmem, kTmemCols);
     }
 }
 
 // ------------------------------------------------------------------------- configuration
+
+constexpr int kWCluster = 4;     // forward: CTAs sharing each operand tile; backward: the K split
+
+static int optin_smem(const Plan& p)
+{
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p.device) != cudaSuccess) return 0;
+    return optin;
+}
+
+// Ring stages that fit beside a weight slice of KBW x rowsW x 128 B and an inbox: as many as
+// fit, at most kWMaxStages and at most the plan's cap; 0 when fewer than two fit.
+static int wide_stages(const Plan& p, int KBW, int rowsW, size_t inbox)
+{
+    const size_t optin = (size_t)optin_smem(p);
+    int st = 0;
+    for (int n = 2; n <= kWMaxStages; ++n)
+        if (wide_smem_bytes(KBW, rowsW, n, inbox) <= optin) st = n;
+    if (p.wide_stages > 0 && p.wide_stages < st) st = p.wide_stages;
+    return st;
+}
+
+static size_t bwd_inbox_bytes(const Plan& p) { return (size_t)3 * p.B * kWU * 4; }
 
 bool rec_wide_supported(const Plan& p, int H, int ndir, bool bf16)
 {
@@ -625,10 +788,7 @@ bool rec_wide_supported(const Plan& p, int H, int ndir, bool bf16)
     if (H % 64 != 0 || H > 1024 || p.B > 256 || p.B < 1) return false;
     const int grid = ndir * H / kWU;
     if (grid > p.num_sms) return false;
-    int optin = 0;
-    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, p.device) != cudaSuccess) return false;
-    const size_t smem = wide_smem_bytes(H / 64, 64);
-    return smem <= (size_t)optin && wide_smem_bytes(4 * H / 64, kWU) <= (size_t)optin;
+    return wide_stages(p, H / 64, 64, 0) > 0 && wide_stages(p, 4 * H / 64, kWU, 0) > 0;
 }
 
 size_t rec_wide_xbuf_bytes(const Plan& p, int H, int ndir, bool bwd)
@@ -636,25 +796,30 @@ size_t rec_wide_xbuf_bytes(const Plan& p, int H, int ndir, bool bwd)
     return (size_t)ndir * 2 * p.B * (bwd ? 4 * H : H) * 2;
 }
 
-constexpr int kWCluster = 4;     // CTAs sharing each operand tile by multicast
+// One kernel form: its entry, shared memory and ring depth.
+struct WideForm {
+    const void* fn;
+    size_t smem;
+    int stages;
+};
 
-// One cooperative launch of `fn1` (no clusters) or `fn4` (clusters of kWCluster sharing the
-// operand tiles): the clustered form when the plan allows it and the device co-schedules all
-// of its clusters, else the plain one.  *cs receives the cluster size used.
-static lstm_status wide_launch(const Plan& p, const void* fn1, const void* fn4, WideArgs& a, const CUtensorMap& mapW,
-                               const CUtensorMap& mapA, size_t smem, cudaStream_t s, int* cs)
+// One cooperative launch: the clustered form `f4` (clusters of kWCluster) when the plan allows
+// it, it fits and the device co-schedules all of its clusters, else the plain form `f1` (when
+// `plain` allows it; LSTM_ERR_UNSUPPORTED otherwise).  *cs receives the cluster size used.
+static lstm_status wide_launch(const Plan& p, const WideForm& f1, const WideForm& f4, bool plain, WideArgs& a,
+                               const CUtensorMap& mapW, const CUtensorMap& mapA, cudaStream_t s, int* cs)
 {
     const int grid = a.ndir * a.NC;
     CUtensorMap mw = mapW, ma = mapA;
     void* args[] = {&a, &mw, &ma};
     if (cudaMemsetAsync(a.ctr, 0, sizeof(unsigned) * 2, s) != cudaSuccess) return LSTM_ERR_CUDA;
-    if (p.wide_mode != 2 && a.NC % kWCluster == 0 &&
-        cudaFuncSetAttribute(fn4, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess) {
+    if (p.wide_mode != 2 && a.NC % kWCluster == 0 && f4.stages > 0 &&
+        cudaFuncSetAttribute(f4.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)f4.smem) == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[2];
         cfg.gridDim = dim3(grid);
         cfg.blockDim = dim3(kWT);
-        cfg.dynamicSmemBytes = smem;
+        cfg.dynamicSmemBytes = f4.smem;
         cfg.stream = s;
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = kWCluster;
@@ -665,26 +830,29 @@ static lstm_status wide_launch(const Plan& p, const void* fn1, const void* fn4, 
         cfg.attrs = attr;
         cfg.numAttrs = 1;                       // the occupancy query takes the cluster shape only
         int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, fn4, &cfg) == cudaSuccess && clusters * kWCluster >= grid) {
+        if (cudaOccupancyMaxActiveClusters(&clusters, f4.fn, &cfg) == cudaSuccess && clusters * kWCluster >= grid) {
             cfg.numAttrs = 2;
-            if (cudaLaunchKernelExC(&cfg, fn4, args) == cudaSuccess) {
+            a.stages = f4.stages;
+            if (cudaLaunchKernelExC(&cfg, f4.fn, args) == cudaSuccess) {
                 *cs = kWCluster;
                 return LSTM_OK;
             }
         }
         cudaGetLastError();                      // fall back to the plain launch below
     }
-    if (cudaFuncSetAttribute(fn1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    if (!plain || f1.stages <= 0 ||
+        cudaFuncSetAttribute(f1.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)f1.smem) != cudaSuccess) {
         cudaGetLastError();
         return LSTM_ERR_UNSUPPORTED;
     }
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn1, kWT, smem) != cudaSuccess || per_sm < 1 ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, f1.fn, kWT, f1.smem) != cudaSuccess || per_sm < 1 ||
         per_sm * p.num_sms < grid) {
         cudaGetLastError();
         return LSTM_ERR_UNSUPPORTED;
     }
-    const cudaError_t e = cudaLaunchCooperativeKernel(fn1, dim3(grid), dim3(kWT), args, smem, s);
+    a.stages = f1.stages;
+    const cudaError_t e = cudaLaunchCooperativeKernel(f1.fn, dim3(grid), dim3(kWT), args, f1.smem, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return e == cudaErrorCooperativeLaunchTooLarge ? LSTM_ERR_UNSUPPORTED : LSTM_ERR_CUDA;
@@ -704,13 +872,15 @@ lstm_status rec_wide_fwd_launch(const Plan& p, WideArgs a, const void* R, cudaSt
     if (!make_map_bf16_sw128(&mapW, R, a.ndir * 4 * a.H, a.H, a.H, kWU) ||
         !make_map_bf16_sw128(&mapA, a.xbuf, a.ndir * 2 * a.B, a.H, a.H, 128))
         return LSTM_ERR_UNSUPPORTED;
+    const int KB = a.H / 64, ns = wide_stages(p, KB, 64, 0);
+    const WideForm f1 = {(const void*)lstm_rec_fwd_wide_kernel<1>, wide_smem_bytes(KB, 64, ns, 0), ns};
+    const WideForm f4 = {(const void*)lstm_rec_fwd_wide_kernel<kWCluster>, f1.smem, ns};
     trace_begin(p, K_REC_FWD, s);
     int cs = 0;
-    const lstm_status st = wide_launch(p, (const void*)lstm_rec_fwd_wide_kernel<1>,
-                                       (const void*)lstm_rec_fwd_wide_kernel<kWCluster>, a, mapW, mapA,
-                                       wide_smem_bytes(a.H / 64, 64), s, &cs);
+    const lstm_status st = wide_launch(p, f1, f4, true, a, mapW, mapA, s, &cs);
     trace_end(p, K_REC_FWD, s, st == LSTM_OK ? 1 : 0);
     p.last_rec_variant[0] = cs;
+    p.last_rec_stages[0] = st == LSTM_OK ? a.stages : 0;
     return st;
 }
 
@@ -726,11 +896,17 @@ lstm_status rec_wide_bwd_launch(const Plan& p, WideArgs a, const void* RT, float
     if (!make_map_bf16_sw128(&mapW, RT, a.ndir * a.H, 4 * a.H, 4 * a.H, kWU) ||
         !make_map_bf16_sw128(&mapA, a.xbuf, a.ndir * 2 * a.B, 4 * a.H, 4 * a.H, 128))
         return LSTM_ERR_UNSUPPORTED;
+    const int KB1 = 4 * a.H / 64, KB4 = a.H / 64;
+    const size_t inbox = bwd_inbox_bytes(p);
+    const int ns1 = wide_stages(p, KB1, kWU, 0), ns4 = wide_stages(p, KB4, 4 * kWU, inbox);
+    const WideForm f1 = {(const void*)lstm_rec_bwd_wide_kernel<false>, wide_smem_bytes(KB1, kWU, ns1, 0), ns1};
+    const WideForm f4 = {(const void*)lstm_rec_bwd_wide_kernel<true>, wide_smem_bytes(KB4, 4 * kWU, ns4, inbox), ns4};
     trace_begin(p, K_REC_BWD, s);
     int cs = 0;
-    lstm_status st = wide_launch(p, (const void*)lstm_rec_bwd_wide_kernel<1>, (const void*)lstm_rec_bwd_wide_kernel<kWCluster>,
-                                 a, mapW, mapA, wide_smem_bytes(4 * a.H / 64, kWU), s, &cs);
+    // automatic choice: only the split form (the plain one is slower than per-step launches)
+    lstm_status st = wide_launch(p, f1, f4, p.wide_mode >= 1, a, mapW, mapA, s, &cs);
     p.last_rec_variant[1] = cs;
+    p.last_rec_stages[1] = st == LSTM_OK ? a.stages : 0;
     int launched = st == LSTM_OK ? 1 : 0;
     if (st == LSTM_OK) {
         st = param_sums_launch(p, a.ga, a.cbuf, a.H, a.ndir, db, dpeep, sum_scratch, s, a.c0);

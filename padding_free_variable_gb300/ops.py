@@ -108,6 +108,14 @@ class Plan:
         """bf16 layers with H > 512: -1 automatic, 0 per-step launches, 1 the persistent kernel."""
         check(_lib.load().lstm_debug_wide_recurrence(self.handle, int(mode)), "lstm_debug_wide_recurrence")
 
+    def debug_wide_stages(self, max_stages: int = -1) -> tuple:
+        """Cap the persistent wide kernels' operand-ring depth (0 none, -1 unchanged); returns the
+        depths (forward, backward) the last persistent launches used."""
+        f, b = ctypes.c_int32(), ctypes.c_int32()
+        check(_lib.load().lstm_debug_wide_stages(self.handle, int(max_stages), ctypes.byref(f), ctypes.byref(b)),
+              "lstm_debug_wide_stages")
+        return f.value, b.value
+
     def debug_sequence_groups(self, slots: int):
         """Force the cluster kernels' slots per sequence group (0 = automatic)."""
         check(_lib.load().lstm_debug_sequence_groups(self.handle, int(slots)), "lstm_debug_sequence_groups")

@@ -1,7 +1,9 @@
 """The persistent recurrent kernels of bf16 layers wider than one cluster (H > 512): R (and
 R^T) resident in the shared memory of H/16 CTAs per direction, the previous step's operand
-streamed back with TMA, tcgen05 products, a grid barrier per step.  Against the oracle, and
-against the per-step-launch path on the same inputs."""
+streamed back with TMA, tcgen05 products, a grid barrier per step; the backward either splits
+the gate errors over clusters of four CTAs (partial products exchanged through distributed
+shared memory) or streams all of them into every CTA.  Against the oracle, and against the
+per-step-launch path on the same inputs."""
 import numpy as np
 import pytest
 
@@ -26,6 +28,8 @@ def _run(w, mode, **kw):
     from padding_free_variable_gb300 import ops
     plan = ops.Plan(w.lengths, padded=kw.get("padded", False))
     plan.debug_wide_recurrence(mode)
+    if kw.get("stages"):
+        plan.debug_wide_stages(kw["stages"])
     bf16 = True
     stack = ops.PackedLSTMStack(plan, device_layers(w), w.spec.input_size, w.spec.hidden_size,
                                 w.spec.num_directions, bf16)
@@ -55,19 +59,20 @@ CASES = [
 @pytest.mark.parametrize("mode", [1, 2], ids=["clusters", "no-clusters"])
 @pytest.mark.parametrize("case", CASES, ids=[f"nd{c[0]}-L{c[1]}-H{c[3]}-B{len(c[4])}" for c in CASES])
 def test_persistent_wide_matches_oracle(case, mode):
-    """Both forms of the launch: clusters of 4 CTAs sharing each operand tile by multicast
-    (mode 1), and every CTA loading every tile itself (mode 2)."""
+    """Both forms of the launch: clusters of 4 CTAs (forward: sharing each operand tile by
+    multicast; backward: splitting the gate errors four ways), mode 1, and no clusters (every
+    CTA loads every tile it needs itself), mode 2."""
     nd, nl, D, H, lengths = case
     w = synthetic.custom(nd, nl, D, H, lengths, seed=13 + H, dtype="bf16", weight_range=0.05)
     gpu = _run(w, mode)
     for backward in (False, True):
         cfg = gpu["plan"].recurrent_config(backward)
         assert cfg["kernel"] == "persistent_wide" and cfg["ctas_per_direction"] == H // 16, cfg
-    if mode == 2:
-        assert gpu["plan"].recurrent_config(False)["cluster_size"] == 1
-    auto = _run(w, -1)           # the automatic choice: persistent forward, per-step backward
-    assert auto["plan"].recurrent_config(False)["kernel"] == "persistent_wide"
-    assert auto["plan"].recurrent_config(True)["kernel"] == "step_launches"
+        assert cfg["cluster_size"] == (4 if mode == 1 else 1), cfg
+    auto = _run(w, -1)           # the automatic choice: both persistent, the backward split
+    for backward in (False, True):
+        assert auto["plan"].recurrent_config(backward)["kernel"] == "persistent_wide"
+    assert auto["plan"].recurrent_config(True)["cluster_size"] == 4
     compare_all(auto, run_oracle(w), TOL_BF16, label=f"wide automatic {case}")
     compare_all(gpu, run_oracle(w), TOL_BF16, label=f"wide persistent {case}")
     compare_all(gpu, run_oracle(w, bf16_products=True), TOL_BF16_EMULATED, label=f"wide persistent {case}",
@@ -98,5 +103,30 @@ def test_persistent_wide_bitwise_repeatable(mode):
     for k in ("y", "dx", "h_n", "c_n"):
         assert np.array_equal(a[k], b[k]), k
     for ga, gb in zip(a["grads"], b["grads"]):
+        for k in ga:
+            assert np.array_equal(ga[k], gb[k]), k
+
+
+def test_split_backward_against_unsplit_and_ring_depth():
+    """The forward is the same arithmetic with or without multicast: bitwise equal.  The
+    K-split backward (clusters) and the unsplit one (no clusters) add the same partial products
+    in different orders, and the bf16 rounding of the gate errors passed between steps can
+    amplify that: equal within the bf16 path's bar.  The operand ring's depth does not change
+    any result bit (the product's accumulation order is fixed)."""
+    w = synthetic.custom(2, 1, 32, 1024, list(np.random.default_rng(4).integers(1, 40, 160)), seed=7,
+                         dtype="bf16", weight_range=0.05)
+    split, unsplit = _run(w, 1), _run(w, 2)
+    for k in ("y", "h_n", "c_n"):
+        assert np.array_equal(split[k], unsplit[k]), k
+    assert rel_err(split["dx"], unsplit["dx"]) <= 5e-3, rel_err(split["dx"], unsplit["dx"])
+    for gs, gu in zip(split["grads"], unsplit["grads"]):
+        for k in gs:
+            assert rel_err(gs[k], gu[k]) <= 5e-3, (k, rel_err(gs[k], gu[k]))
+    shallow = _run(w, 1, stages=2)
+    assert shallow["plan"].debug_wide_stages(-1) == (2, 2)
+    assert split["plan"].debug_wide_stages(-1)[0] >= 3
+    for k in ("y", "dx", "h_n", "c_n"):
+        assert np.array_equal(split[k], shallow[k]), k
+    for ga, gb in zip(split["grads"], shallow["grads"]):
         for k in ga:
             assert np.array_equal(ga[k], gb[k]), k
