@@ -375,6 +375,241 @@ def reference_arm(args, w, config):
     return 0
 
 
+# --------------------------------------------------------------------------- 2-D (MDLSTM) workloads
+
+MD_METRIC = "non-padded pixels/sec MDLSTM layer fwd+bwd, 4 scan directions (1 GB300); % of CUDA-core roofline"
+MD_UNIT = "pixels/s"
+
+
+def md_kind_work(kind: str, N: int, nd: int, D: int, H: int) -> float:
+    """Algorithmic flops of one call of an MDLSTM phase (every pixel, every direction).
+
+    md_fwd: per cell the two recurrent products U1 h1 + U2 h2 (2 x 2 x 5H x H flops) and the
+    cell (about 25 flops a unit); md_bwd: U1^T da + U2^T da of the successors (20 H^2) and the
+    cell's backward (about 40 a unit); md_input: x W^T + b (2 N D 5H per direction);
+    md_grads: dx and dW (2 N 5H D each per direction), dU1 and dU2 (2 N 5H H each per
+    direction), db and the peephole sums (2 x 11H per cell)."""
+    cells = N * nd
+    if kind == "md_fwd":
+        return cells * (20.0 * H * H + 25.0 * H)
+    if kind == "md_bwd":
+        return cells * (20.0 * H * H + 40.0 * H)
+    if kind == "md_input":
+        return 2.0 * N * D * nd * 5 * H
+    if kind == "md_grads":
+        return 2 * 2.0 * N * nd * 5 * H * D + 2 * 2.0 * cells * 5 * H * H + 22.0 * cells * H
+    return 0.0
+
+
+def md_cpu_sample(w, seconds: float, nthreads: int):
+    """Images (in order) forming about `seconds` of oracle work, by pixel count."""
+    import oracle
+    oracle.build()
+    probe = max(1, min(4, w.heights.size))
+    pix_off = np.concatenate([[0], np.cumsum(w.heights.astype(np.int64) * w.widths)])
+    t0 = time.perf_counter()
+    run_md_oracle(w, list(range(probe)), pix_off)
+    per_pixel = (time.perf_counter() - t0) / max(1, int(pix_off[probe]))
+    budget = int(seconds / max(per_pixel, 1e-9))
+    pick, tot = [], 0
+    for i in range(w.heights.size):
+        npx = int(pix_off[i + 1] - pix_off[i])
+        if pick and tot + npx > budget:
+            break
+        pick.append(i)
+        tot += npx
+    return pick, tot, pix_off
+
+
+def run_md_oracle(w, pick, pix_off):
+    import oracle
+    rows = np.concatenate([np.arange(pix_off[i], pix_off[i + 1]) for i in pick]) if pick else np.zeros(0, int)
+    t0 = time.perf_counter()
+    oracle.md_layer(w.heights[pick], w.widths[pick], w.x[rows], w.layer, w.G[rows])
+    return time.perf_counter() - t0
+
+
+def md_main(args):
+    from padding_free_variable_gb300 import synthetic
+    name = args.workload[3:]
+    w = synthetic.md_workload(name, batch=args.batch or None)
+    nd, D, H = w.num_directions, w.input_size, w.hidden_size
+    N, B = w.N, int(w.heights.size)
+    config = {"workload": w.name, "images": B, "pixels_per_step": N, "input_size": D, "hidden_size": H,
+              "directions": nd, "dtype": "f32", "heights": f"uniform int [{w.heights.min()}, {w.heights.max()}]",
+              "widths": f"uniform int [{w.widths.min()}, {w.widths.max()}]",
+              "schedule": "diagonal (every image from step 0; the canvas schedule is a comparator)",
+              "l2": "flushed (512 MiB write) before every timed step", "parallelism": "single GPU"}
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        nthreads = os.cpu_count() or 1
+        per_step = max(0.5, 150.0 / max(1, args.steps + args.warmup))
+        pick, px, pix_off = md_cpu_sample(w, per_step, nthreads)
+        for _ in range(args.warmup):
+            run_md_oracle(w, pick, pix_off)
+        times = [run_md_oracle(w, pick, pix_off) for _ in range(args.steps)]
+        value = px * args.steps / sum(times)
+        out = {"metric": MD_METRIC, "value": round(value, 2), "unit": MD_UNIT, "n_gpus": args.gpus,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * sum(times) / args.steps, 3),
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+               "data": "synthetic", "impl": "reference", "config": dict(config, sample_pixels_per_step=px),
+               "cpu_baseline": {"value": round(value, 2), "unit": MD_UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"{len(pick)} of {B} images ({px} pixels) per step, single thread"},
+               "e2e": {"value": round(value, 2), "unit": MD_UNIT, "h2d_bytes_per_step": 0,
+                       "d2h_bytes_per_step": 0}}
+        print(json.dumps(out))
+        return 0
+
+    import torch
+    torch.cuda.set_device(local_rank)
+    from padding_free_variable_gb300 import build as native, ops
+    native.build()
+    plan = ops.MdPlan(w.heights, w.widths, 0, nd, 1)
+    layer = ops.MdLayer(plan, w.layer, D, H)
+    x_dev = torch.from_numpy(w.x).cuda()
+    G_dev = torch.from_numpy(w.G).cuda()
+    y_dev = torch.empty((N, nd * H), device="cuda")
+    dx_dev = torch.empty((N, D), device="cuda")
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(lay=layer, xx=x_dev, gg=G_dev, yy=y_dev, dd=dx_dev):
+        lay.forward(xx, yy)
+        lay.backward(xx, gg, dd)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if plan.poll() != 0:
+        raise RuntimeError("device status set during warm-up")
+    sampler = ClockSampler(gpu_index(local_rank))
+    sampler.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    launches0 = plan.launch_count()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    launches = plan.launch_count() - launches0
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if plan.poll() != 0:
+        raise RuntimeError("device status set during the timed region")
+    value = N * args.steps / (total_ms / 1e3)
+
+    # per-phase times (a separate traced pass) and their rooflines
+    peaks = load_peaks()
+    clk = float(peaks.get("sm_max_mhz", 2070.0))
+    alu_peak = NUM_SMS * FP32_LANES_PER_SM * 2 * clk * 1e6 / 1e12
+    plan.enable_timing(True)
+    traced = max(3, min(10, args.steps))
+    for _ in range(traced):
+        flush.fill_(0.0)
+        step()
+    tim = plan.read_timing()
+    plan.enable_timing(False)
+    kernels = {}
+    for kind, (ms, calls) in tim.items():
+        if not calls:
+            continue
+        per_ms = ms / calls
+        fl = md_kind_work(kind, N, nd, D, H)
+        ach = fl / (per_ms / 1e3) / 1e12
+        kernels[kind] = {"kernel": kind, "bound": "alu", "achieved": round(ach, 3), "peak": round(alu_peak, 1),
+                         "unit": "TFLOP/s", "frac": round(ach / alu_peak, 4),
+                         "peak_source": f"derived: {NUM_SMS} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {clk:.0f} MHz",
+                         "per_launch": {"flops": fl, "ms": round(per_ms, 4)}, "ms_per_step": round(ms / traced, 4)}
+    dom = max(kernels.values(), key=lambda r: r["ms_per_step"])
+    roof = {k: dom[k] for k in ("bound", "achieved", "peak", "unit", "frac", "kernel", "peak_source")}
+    roof["traffic"] = recorded_traffic(dom["kernel"], w.name)
+    walk = {"steps": plan.steps, "cells_per_step": round(N * nd / max(1, plan.steps), 1)}
+    if "md_fwd" in kernels:
+        walk["us_per_step_fwd"] = round(1e3 * kernels["md_fwd"]["per_launch"]["ms"] / max(1, plan.steps), 3)
+    if "md_bwd" in kernels:
+        walk["us_per_step_bwd"] = round(1e3 * kernels["md_bwd"]["per_launch"]["ms"] / max(1, plan.steps), 3)
+
+    # end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    x_host = torch.from_numpy(w.x).pin_memory()
+    G_host = torch.from_numpy(w.G).pin_memory()
+    y_host = torch.empty((N, nd * H), dtype=torch.float32).pin_memory()
+    dx_host = torch.empty((N, D), dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    for i in range(e2e_steps):
+        flush.fill_(float(i))
+        es[i].record(stream)
+        x_dev.copy_(x_host, non_blocking=True)
+        G_dev.copy_(G_host, non_blocking=True)
+        step()
+        y_host.copy_(y_dev, non_blocking=True)
+        dx_host.copy_(dx_dev, non_blocking=True)
+        ee[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in zip(es, ee))
+    e2e = {"value": round(N * e2e_steps / (e2e_ms / 1e3), 2), "unit": MD_UNIT,
+           "h2d_bytes_per_step": int(4 * (x_host.numel() + G_host.numel())),
+           "d2h_bytes_per_step": int(4 * (y_host.numel() + dx_host.numel()))}
+
+    comparators = {}
+    if not args.no_comparators:
+        csteps = max(3, min(10, args.steps))
+        # the same cells on the page's canvas: a cell runs at its skewed canvas column
+        cplan = ops.MdPlan(w.heights, w.widths, 0, nd, 0)
+        clayer = ops.MdLayer(cplan, w.layer, D, H)
+        cms = _time_steps(lambda: step(lay=clayer), csteps, flush, stream)
+        comparators["canvas_schedule"] = {
+            "pixels_per_s": round(N / (cms / 1e3), 2), "ms_per_step": round(cms, 3), "steps": cplan.steps,
+            "canvas": {"height": cplan.canvas[0], "width": cplan.canvas[1], "rows": cplan.rows,
+                       "fill": round(N / max(1, cplan.canvas[0] * cplan.canvas[1]), 4),
+                       "skewed_fill": round(N / max(1, cplan.canvas[0] * (cplan.canvas[1] + cplan.canvas[0] - 1)),
+                                            4)}}
+        del clayer, cplan
+        # the page's batch padding: every image padded to the batch's largest height and width
+        # (the same kernels over B x hmax x wmax pixels; the work is what is compared)
+        hm, wm = int(w.heights.max()), int(w.widths.max())
+        Np = B * hm * wm
+        pplan = ops.MdPlan(np.full(B, hm), np.full(B, wm), 0, nd, 0)
+        player = ops.MdLayer(pplan, w.layer, D, H)
+        xp = torch.zeros((Np, D), device="cuda")
+        gp = torch.zeros((Np, nd * H), device="cuda")
+        yp = torch.empty((Np, nd * H), device="cuda")
+        dxp = torch.empty((Np, D), device="cuda")
+        pms = _time_steps(lambda: step(lay=player, xx=xp, gg=gp, yy=yp, dd=dxp), csteps, flush, stream)
+        comparators["batch_padded"] = {"pixels_per_s": round(N / (pms / 1e3), 2), "ms_per_step": round(pms, 3),
+                                       "computed_pixels": Np, "waste_fraction": round((Np - N) / Np, 4),
+                                       "zero_padding_rate": round((Np - N) / N, 4)}
+        del player, pplan, xp, gp, yp, dxp
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        pick, px, pix_off = md_cpu_sample(w, 15.0, 1)
+        dt = run_md_oracle(w, pick, pix_off)
+        cpu = {"value": round(px / dt, 2), "unit": MD_UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{len(pick)} of {B} images ({px} pixels), fwd+backward of the layer in all "
+                         f"{nd} directions, fp64, single thread, {dt:.1f} s"}
+
+    out = {"metric": MD_METRIC, "value": round(value, 2), "unit": MD_UNIT, "n_gpus": 1, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
+           "clocks": clocks, "e2e": e2e, "gpu_launches": int(launches), "roofline": roof, "cpu_baseline": cpu,
+           "kernels": kernels, "wavefront": walk, "comparators": comparators,
+           "wall_s_timed_region": round(wall, 3),
+           "step_ms": {"min": round(min(step_ms), 4), "median": round(statistics.median(step_ms), 4),
+                       "max": round(max(step_ms), 4)}}
+    print(json.dumps(out))
+    return 0
+
+
 # --------------------------------------------------------------------------- GPU arm
 
 def _time_steps(fn, steps, flush, stream):
@@ -453,7 +688,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=3)
+    ap.add_argument("--workload", default="3",
+                    help="1..5: the 1-D LSTM workloads; md-words / md-lines: one 2-D MDLSTM layer over "
+                         "example-packed images")
     ap.add_argument("--batch", type=int, default=0,
                     help="diagnostic: the workload with only this many sequences (same distributions); "
                          "0 = the workload as defined")
@@ -465,6 +702,9 @@ def main():
                          "bit 1 TMA tiles); -1 = the library's own choice")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if str(args.workload).startswith("md-"):
+        return md_main(args)
+    args.workload = int(args.workload)
 
     from padding_free_variable_gb300 import synthetic
     w = synthetic.workload(args.workload, batch=args.batch or None)

@@ -557,6 +557,137 @@ lstm_status lstm_debug_skip_arrival(lstm_plan* plan, int32_t cta);
  * reach every variant at small sizes.  LSTM_ERR_INVALID_ARG outside -1..3. */
 lstm_status lstm_debug_cluster_variant(lstm_plan* plan, int32_t variant);
 
+/* ======================================================================
+ * 2-D example-packing for MDLSTM layers ("No Padding Please: Efficient
+ * Neural Handwriting Recognition", Sec. III-V, App. A-B).  fp32 throughout.
+ *
+ * Examples are images of h x w pixels with D features each, given in caller
+ * order: pixels of example 0 row by row, then example 1, ... (N pixels).  The
+ * plan places them on a canvas with the page's packing algorithm (App. B,
+ * Algorithm 1): bucket by height (descending), fill rows greedily with the
+ * widest example that still fits beside the row's examples and one separator
+ * pixel (ties: lower index; an empty row takes the widest example left even
+ * if it is wider than the row; a bucket's last row closes when the bucket runs
+ * out), stack the rows with one separator row between them.  The row width
+ * is the caller's, or the widest example when 0.
+ *
+ * A layer scans the image from num_directions corners (direction d flips x
+ * when d & 1 and y when d & 2; Sec. III's 4-directional layer stacks all
+ * four).  Cell of a direction at scan position (ys, xs): predecessor 1 is
+ * (ys - 1, xs), predecessor 2 is (ys, xs - 1), absent outside the example
+ * (the mask of Sec. V: zero state input).  With gates a_g = W_g x + U1_g h1
+ * + U2_g h2 + b_g, g in (i, f1, f2, z, o):
+ *   i = sig(a_i + p_i1 S1 + p_i2 S2), f1 = sig(a_f1 + p_f1 S1),
+ *   f2 = sig(a_f2 + p_f2 S2), z = tanh(a_z), o = sig(a_o + p_o1 S1 + p_o2 S2),
+ *   c = f1 S1 + f2 S2 + i z, h = o tanh(c)
+ * (App. A: five products per hidden state, three per memory state; Sec. III:
+ * the output gate reads the previous states).  Output y[N][ndir*H], the
+ * direction d in columns [dH, dH + H).
+ *
+ * Schedule (Sec. IV-A, input skewing): the cells of one skewed column depend
+ * only on the previous column and run as one parallel step.  schedule 0 =
+ * the canvas's skewed columns (height + width - 1 steps); 1 = every example
+ * from step 0 along its own anti-diagonals (longest h + w - 1 steps).  The
+ * results do not depend on the schedule; separator and padding cells are
+ * never computed under either.
+ * ====================================================================== */
+
+typedef struct lstm_md_plan lstm_md_plan;
+
+typedef struct {
+    int32_t input_size;      /* D */
+    int32_t hidden_size;     /* H, 1..128 */
+    int32_t num_directions;  /* must equal the plan's */
+} lstm_md_shape;
+
+/* Device pointers, fp32, 16-byte aligned: W[ndir][5H][D], U1[ndir][5H][H]
+ * (predecessor 1), U2[ndir][5H][H], b[ndir][5H], peep[ndir][6][H] in the order
+ * p_i1, p_i2, p_f1, p_f2, p_o1, p_o2; gate blocks of 5H in the order i, f1,
+ * f2, z, o. */
+typedef struct {
+    const float* W;
+    const float* U1;
+    const float* U2;
+    const float* b;
+    const float* peep;
+} lstm_md_params;
+
+/* Gradients in the same layouts (overwritten; any pointer may be NULL). */
+typedef struct {
+    float* W;
+    float* U1;
+    float* U2;
+    float* b;
+    float* peep;
+} lstm_md_grads;
+
+/* Pack n examples (heights[i] x widths[i], either may be 0) and build the
+ * schedule's tables on the current device.  row_width >= 0 (0 = widest),
+ * num_directions 1..4, schedule 0 or 1.  Host and device memory are owned by
+ * the plan.  LSTM_ERR_INVALID_ARG for bad arguments, LSTM_ERR_UNSUPPORTED when
+ * ndir x N reaches 2^31 cells, LSTM_ERR_CUDA when the device tables cannot be
+ * made. */
+lstm_status lstm_md_plan_create(const int32_t* heights, const int32_t* widths, int32_t n, int32_t row_width,
+                                int32_t num_directions, int32_t schedule, lstm_md_plan** out);
+void lstm_md_plan_destroy(lstm_md_plan* plan);
+
+/* The same packing and schedule on the host only (no device work), for
+ * checking: info = {steps, canvas height, canvas width, packed rows}; y0, x0
+ * [n] = each example's top-left canvas pixel (-1 without pixels); step_off
+ * [ndir][steps + 1] = first cell of each step (cells are numbered direction by
+ * direction, step by step, examples in packing order, then by scan row); per
+ * cell [ndir * N]: src = its pixel (caller order), pred1 / pred2 = its
+ * predecessor cells, succ1 / succ2 = the cells it is predecessor 1 / 2 of (-1
+ * none).  Any output pointer may be NULL. */
+lstm_status lstm_md_plan_compute_host(const int32_t* heights, const int32_t* widths, int32_t n, int32_t row_width,
+                                      int32_t num_directions, int32_t schedule, int32_t* info, int32_t* y0,
+                                      int32_t* x0, int64_t* step_off, int32_t* src, int32_t* pred1, int32_t* pred2,
+                                      int32_t* succ1, int32_t* succ2);
+
+lstm_status lstm_md_plan_info(const lstm_md_plan* plan, int64_t* pixels, int32_t* steps, int32_t* canvas_height,
+                              int32_t* canvas_width, int32_t* rows);
+lstm_status lstm_md_plan_placement(const lstm_md_plan* plan, int32_t* y0, int32_t* x0);
+/* step_off[ndir][steps + 1], as lstm_md_plan_compute_host. */
+lstm_status lstm_md_plan_step_cells(const lstm_md_plan* plan, int64_t* step_off);
+/* Bound on each grid-barrier wait of the layer kernels (default 2 s). */
+lstm_status lstm_md_plan_set_wait_limit(lstm_md_plan* plan, uint64_t ns);
+/* Synchronise the stream, then return and clear the plan's device status word
+ * (LSTM_OK or LSTM_ERR_TIMEOUT). */
+lstm_status lstm_md_status_poll(lstm_md_plan* plan, void* stream);
+/* Test hook (-1 = off): CTA `cta` of the layer kernels never arrives at the
+ * first grid barrier, so every CTA's bounded wait runs out; the launch
+ * returns and LSTM_ERR_TIMEOUT is reported without a GPU fault. */
+lstm_status lstm_md_debug_skip_arrival(lstm_md_plan* plan, int32_t cta);
+/* Kernels launched through this plan; -1 for a NULL plan. */
+int64_t lstm_md_plan_launch_count(const lstm_md_plan* plan);
+/* Optional CUDA-event timing of the layer's phases (diagnostics; enabling
+ * clears the totals): read_timing fills ms[4] and calls[4] in the order input
+ * projection (GEMM and weight transpose), forward walk, backward walk,
+ * gradient products and sums.  Either output may be NULL; reading waits for
+ * the recorded events. */
+lstm_status lstm_md_plan_enable_timing(lstm_md_plan* plan, int32_t enable);
+lstm_status lstm_md_plan_read_timing(lstm_md_plan* plan, double* ms, int64_t* calls);
+
+/* Device bytes the caller provides: the workspace (kept from lstm_md_fwd to
+ * lstm_md_bwd) and the backward scratch.  0 for an invalid shape. */
+size_t lstm_md_workspace_bytes(const lstm_md_plan* plan, const lstm_md_shape* shape);
+size_t lstm_md_scratch_bytes(const lstm_md_plan* plan, const lstm_md_shape* shape);
+
+/* Forward of one layer: x[N][D] (caller order) -> y[N][ndir*H]; stream-ordered
+ * on `stream`.  The workspace keeps the cells' h, c and gates for the
+ * backward pass.  A barrier wait that runs out is reported by
+ * lstm_md_status_poll. */
+lstm_status lstm_md_fwd(const lstm_md_plan* plan, const lstm_md_shape* shape, const lstm_md_params* params,
+                        const float* x, float* y, void* workspace, void* stream);
+
+/* Backward of the last lstm_md_fwd on this workspace (it is consumed: a
+ * second backward needs a new forward): dy[N][ndir*H] = dL/dy; writes dx[N][D]
+ * (NULL: skipped) and the parameter gradients (bitwise repeatable: every sum
+ * runs in a fixed order). */
+lstm_status lstm_md_bwd(const lstm_md_plan* plan, const lstm_md_shape* shape, const lstm_md_params* params,
+                        const float* x, void* workspace, const float* dy, float* dx, const lstm_md_grads* grads,
+                        void* scratch, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

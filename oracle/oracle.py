@@ -15,6 +15,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "lstm_oracle.c")
+_SRCS = (_SRC, os.path.join(_HERE, "mdlstm_oracle.c"))
 _LIB = os.path.join(_HERE, "liblstm_oracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -22,10 +23,10 @@ _lib = None
 
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (plain C, OpenMP over sequences, no fast-math)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    if force or not os.path.exists(_LIB) or any(os.path.getmtime(_LIB) < os.path.getmtime(f) for f in _SRCS):
         tmp = _LIB + f".tmp{os.getpid()}"
         cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
-               "-o", tmp, _SRC, "-lm"]
+               "-o", tmp, *_SRCS, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
     return _LIB
@@ -57,6 +58,15 @@ def _load():
             lib.oracle_round_bf16.argtypes = [ctypes.c_double]
             lib.oracle_layer_param_count.restype = ctypes.c_long
             lib.oracle_layer_param_count.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+            ip = ctypes.POINTER(ctypes.c_int)
+            lib.oracle_md_param_count.restype = ctypes.c_long
+            lib.oracle_md_param_count.argtypes = [ctypes.c_int, ctypes.c_int]
+            lib.oracle_md_layer.restype = ctypes.c_int
+            lib.oracle_md_layer.argtypes = [ctypes.c_int, ip, ip, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            dp, dp, dp, dp, dp, dp]
+            lib.oracle_md_forward.restype = None
+            lib.oracle_md_forward.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, dp, dp, dp, dp, dp]
             _lib = lib
     return _lib
 

@@ -33,9 +33,14 @@ EXPORTED = (
     "lstm_plan_recurrent_groups", "lstm_debug_sequence_groups", "lstm_state_scratch_bytes", "lstm_fwd_state",
     "lstm_bwd_state", "lstm_plan_create_segments", "lstm_segments_host", "lstm_plan_create_window",
     "lstm_form_batches", "lstm_debug_wide_recurrence", "lstm_debug_wide_stages",
+    "lstm_md_plan_create", "lstm_md_plan_compute_host", "lstm_md_plan_destroy", "lstm_md_plan_info",
+    "lstm_md_plan_placement", "lstm_md_plan_step_cells", "lstm_md_plan_set_wait_limit", "lstm_md_status_poll",
+    "lstm_md_plan_launch_count", "lstm_md_workspace_bytes", "lstm_md_scratch_bytes", "lstm_md_fwd", "lstm_md_bwd",
+    "lstm_md_plan_enable_timing", "lstm_md_plan_read_timing", "lstm_md_debug_skip_arrival",
 )
 
 KERNEL_KINDS = ("pack", "unpack", "input_gemm", "rec_fwd", "rec_bwd", "gemm_dx", "gemm_dw", "gemm_dr", "convert")
+MD_KINDS = ("md_input", "md_fwd", "md_bwd", "md_grads")
 
 
 class LayerShape(ctypes.Structure):
@@ -60,6 +65,21 @@ class State(ctypes.Structure):
 class StateGrads(ctypes.Structure):
     _fields_ = [("dh_n", ctypes.c_void_p), ("dc_n", ctypes.c_void_p), ("dh0", ctypes.c_void_p),
                 ("dc0", ctypes.c_void_p)]
+
+
+class MdShape(ctypes.Structure):
+    _fields_ = [("input_size", ctypes.c_int32), ("hidden_size", ctypes.c_int32),
+                ("num_directions", ctypes.c_int32)]
+
+
+class MdParams(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("U1", ctypes.c_void_p), ("U2", ctypes.c_void_p), ("b", ctypes.c_void_p),
+                ("peep", ctypes.c_void_p)]
+
+
+class MdGrads(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("U1", ctypes.c_void_p), ("U2", ctypes.c_void_p), ("b", ctypes.c_void_p),
+                ("peep", ctypes.c_void_p)]
 
 
 class LSTMError(RuntimeError):
@@ -114,6 +134,24 @@ def _declare(lib):
         "lstm_debug_sequence_groups": (c, [vp, i32]),
         "lstm_debug_wide_recurrence": (c, [vp, i32]),
         "lstm_debug_wide_stages": (c, [vp, i32, pi32, pi32]),
+        "lstm_md_plan_create": (c, [pi32, pi32, i32, i32, i32, i32, ctypes.POINTER(vp)]),
+        "lstm_md_plan_compute_host": (c, [pi32, pi32, i32, i32, i32, i32, pi32, pi32, pi32,
+                                          ctypes.POINTER(ctypes.c_int64), pi32, pi32, pi32, pi32, pi32]),
+        "lstm_md_plan_destroy": (None, [vp]),
+        "lstm_md_plan_info": (c, [vp, ctypes.POINTER(ctypes.c_int64), pi32, pi32, pi32, pi32]),
+        "lstm_md_plan_placement": (c, [vp, pi32, pi32]),
+        "lstm_md_plan_step_cells": (c, [vp, ctypes.POINTER(ctypes.c_int64)]),
+        "lstm_md_plan_set_wait_limit": (c, [vp, u64]),
+        "lstm_md_status_poll": (c, [vp, vp]),
+        "lstm_md_plan_launch_count": (i64, [vp]),
+        "lstm_md_plan_enable_timing": (c, [vp, i32]),
+        "lstm_md_debug_skip_arrival": (c, [vp, i32]),
+        "lstm_md_plan_read_timing": (c, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]),
+        "lstm_md_workspace_bytes": (sz, [vp, ctypes.POINTER(MdShape)]),
+        "lstm_md_scratch_bytes": (sz, [vp, ctypes.POINTER(MdShape)]),
+        "lstm_md_fwd": (c, [vp, ctypes.POINTER(MdShape), ctypes.POINTER(MdParams), vp, vp, vp, vp]),
+        "lstm_md_bwd": (c, [vp, ctypes.POINTER(MdShape), ctypes.POINTER(MdParams), vp, vp, vp, vp,
+                            ctypes.POINTER(MdGrads), vp, vp]),
         "lstm_stepwise_scratch_bytes": (ctypes.c_size_t, [vp, ctypes.POINTER(LayerShape)]),
         "lstm_fwd_stepwise": (c, [vp, ctypes.POINTER(LayerShape), ctypes.POINTER(LayerParams), vp, vp, vp, vp, vp,
                                   vp, vp, vp]),

@@ -88,6 +88,10 @@ struct Plan {
 // another kind's bracket).
 void trace_begin(const Plan& p, int kind, cudaStream_t s);
 void trace_end(const Plan& p, int kind, cudaStream_t s, int kernels);
+// The same on a tracer of its own (the 2-D plan's); flush = wait for and add up the pending records.
+void tracer_begin(Tracer* t, int kind, cudaStream_t s);
+void tracer_end(Tracer* t, int kind, cudaStream_t s, int kernels);
+void tracer_flush(Tracer* t);
 
 // ---------------------------------------------------------------- helpers
 

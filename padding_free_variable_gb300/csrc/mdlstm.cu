@@ -1,0 +1,636 @@
+// mdlstm.cu -- one 2-D MDLSTM layer over example-packed images (fp32).
+//
+// "No Padding Please: Efficient Neural Handwriting Recognition":
+//  * Sec. III / App. A: a cell of the 2-D grid takes the pixel input and the
+//    hidden and memory states of its two predecessors (the previous row and
+//    the previous column in its scan order); five input blocks (input gate,
+//    two forget gates, input node, output gate) each sum W x + U1 h1 + U2 h2
+//    + b; each predecessor state enters the input gate, its own forget gate
+//    and the output gate (the output gate reads the previous states, the
+//    page's variant):
+//        i = sig(a_i + p_i1 S1 + p_i2 S2)   f1 = sig(a_f1 + p_f1 S1)
+//        f2 = sig(a_f2 + p_f2 S2)           z = tanh(a_z)
+//        o = sig(a_o + p_o1 S1 + p_o2 S2)   c = f1 S1 + f2 S2 + i z
+//        h = o tanh(c)
+//    A predecessor outside the example gives h = S = 0 (Sec. V's mask).
+//  * Sec. IV-A: along a skewed column (an anti-diagonal of the image) the
+//    cells depend only on the previous column: one parallel step.
+//  * Sec. V: the examples are packed so that one launch covers them all.
+//
+// Layout: the plan stores the cells of every scan direction in wavefront
+// order with their predecessor and successor cells (md_plan.cu).  A layer is
+//  1. the input projection of every pixel for all directions, one CUDA-core
+//     GEMM: gx[N][ndir*5H] = x W^T + b;
+//  2. one cooperative launch over all SMs that walks the steps: a warp per
+//     cell, a lane per unit (up to 4 units a lane); the recurrent products
+//     U1 h1 + U2 h2 read h1, h2 from L2 and U^T from shared memory (when the
+//     layer's weights fit) and the cell writes h, c, the gates and y; a
+//     bounded grid barrier separates the steps;
+//  3. backward: the same walk in reverse; a cell's h error is its dy plus
+//     U1^T da of the cell that takes it as predecessor 1 plus U2^T da of the
+//     one that takes it as predecessor 2, and its state error is what those
+//     successors left for it; the gate errors overwrite the gates in place;
+//  4. dx and dW from the pixel-order gate errors, dU1 and dU2 from the
+//     cell-order gate errors against the predecessors' h (CUDA-core GEMMs,
+//     deterministic K splits), db and the six peephole sums in fixed order.
+#include <cstring>
+
+#include "gemm.cuh"
+#include "md_plan.cuh"
+
+namespace lstm {
+
+namespace {
+
+constexpr int kMdThreads = 256;
+constexpr int kMdMaxH = 128;                  // 4 units a lane
+constexpr size_t kMdSmemCap = 200 * 1024;     // resident recurrent weights up to this size
+constexpr int kMdMaxSplits = 1024;            // K splits allowed to the gradient reductions (K = pixels)
+
+__device__ __forceinline__ float sg_md(float v) { return __fdividef(1.0f, 1.0f + __expf(-v)); }
+__device__ __forceinline__ float th_md(float v)
+{
+    const float e = __expf(2.0f * fminf(fmaxf(v, -40.0f), 40.0f));
+    return 1.0f - __fdividef(2.0f, e + 1.0f);
+}
+
+__device__ __forceinline__ void red_release_add_md(unsigned* p, unsigned v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+struct MdArgs {
+    int H, ndir, steps;
+    int64_t N;
+    const int64_t* step_off;     // [ndir][steps+1]
+    const int32_t* src;
+    const int32_t* pred1;
+    const int32_t* pred2;
+    const int32_t* succ1;
+    const int32_t* succ2;
+    const float* U;              // forward: U^T [ndir][2][H][5H]; backward: U [ndir][2][5H][H]
+    const float* peep;           // [ndir][6][H]
+    const float* gx;             // [N][ndir*5H]
+    float* h;                    // [cells][H]
+    float* c;                    // [cells][H]
+    float* act;                  // [cells][5H] gates, then gate errors
+    float* y;                    // [N][ndir*H]
+    const float* dy;             // [N][ndir*H]
+    float* dap;                  // [N][ndir*5H] gate errors in pixel order
+    float* ds1;                  // [cells][H] state error a cell leaves for its predecessor 1
+    float* ds2;
+    unsigned* ctr;
+    DeviceStatus* status;
+    unsigned long long wait_limit_ns;
+    int debug_skip_cta;          // test hook (-1 off): this CTA skips its first arrival
+};
+
+// Every CTA has finished step `done` (steps counted from 1): bounded wait by thread 0.
+__device__ __forceinline__ bool md_barrier(const MdArgs& a, unsigned done, unsigned where)
+{
+    __syncthreads();
+    int fail = 0;
+    if (threadIdx.x == 0) {
+        if (!(done == 1 && (int)blockIdx.x == a.debug_skip_cta)) red_release_add_md(a.ctr, 1u);
+        const unsigned target = done * gridDim.x;
+        const unsigned long long t0 = global_timer_ns();
+        unsigned spins = 0;
+        while ((int)(ld_acquire_gpu(a.ctr) - target) < 0) {
+            if ((++spins & 63u) == 0) {
+                if (failure_recorded(a.status)) { fail = 1; break; }
+                if (global_timer_ns() - t0 > a.wait_limit_ns) {
+                    record_failure(a.status, LSTM_ERR_TIMEOUT, where);
+                    fail = 1;
+                    break;
+                }
+            }
+        }
+    }
+    return __syncthreads_or(fail) == 0;
+}
+
+// the item-th cell of step k over all directions: its direction and index
+__device__ __forceinline__ bool md_item(const MdArgs& a, int k, int64_t item, int& d, int64_t& p)
+{
+    for (d = 0; d < a.ndir; ++d) {
+        const int64_t* so = a.step_off + (size_t)d * (a.steps + 1);
+        const int64_t n = so[k + 1] - so[k];
+        if (item < n) { p = so[k] + item; return true; }
+        item -= n;
+    }
+    return false;
+}
+
+__device__ __forceinline__ int64_t md_step_cells(const MdArgs& a, int k)
+{
+    int64_t n = 0;
+    for (int d = 0; d < a.ndir; ++d) {
+        const int64_t* so = a.step_off + (size_t)d * (a.steps + 1);
+        n += so[k + 1] - so[k];
+    }
+    return n;
+}
+
+// Forward walk.  NU = units per lane (ceil(H / 32)); SM = U^T resident in shared memory.
+template <int NU, bool SM>
+__global__ void __launch_bounds__(kMdThreads) md_fwd_kernel(MdArgs a)
+{
+    extern __shared__ float md_smem[];
+    const int H = a.H, H5 = 5 * H;
+    const int lane = threadIdx.x & 31;
+    const float* UT = a.U;
+    if (SM) {
+        const int64_t nw = (int64_t)a.ndir * 2 * H * H5;
+        for (int64_t i = threadIdx.x; i < nw; i += blockDim.x) md_smem[i] = a.U[i];
+        __syncthreads();
+        UT = md_smem;
+    }
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    for (int k = 0; k < a.steps; ++k) {
+        const int64_t total = md_step_cells(a, k);
+        for (int64_t item = gw; item < total; item += warps) {
+            int d;
+            int64_t p;
+            md_item(a, k, item, d, p);
+            const int q1 = a.pred1[p], q2 = a.pred2[p];
+            const int64_t px = a.src[p];
+            float h1[NU], h2[NU], s1[NU], s2[NU], acc[5][NU];
+#pragma unroll
+            for (int j = 0; j < NU; ++j) {
+                const int u = lane + 32 * j;
+                const bool ok = u < H;
+                h1[j] = ok && q1 >= 0 ? __ldcg(a.h + (size_t)q1 * H + u) : 0.f;
+                s1[j] = ok && q1 >= 0 ? __ldcg(a.c + (size_t)q1 * H + u) : 0.f;
+                h2[j] = ok && q2 >= 0 ? __ldcg(a.h + (size_t)q2 * H + u) : 0.f;
+                s2[j] = ok && q2 >= 0 ? __ldcg(a.c + (size_t)q2 * H + u) : 0.f;
+#pragma unroll
+                for (int g = 0; g < 5; ++g)
+                    acc[g][j] = ok ? __ldg(a.gx + (size_t)px * a.ndir * H5 + (size_t)d * H5 + g * H + u) : 0.f;
+            }
+            // U1 h1 + U2 h2: h1[kk], h2[kk] broadcast from the lane that holds them
+            const float* U1t = UT + (size_t)d * 2 * H * H5;
+            const float* U2t = U1t + (size_t)H * H5;
+            if (q1 >= 0 || q2 >= 0) {
+#pragma unroll
+                for (int jj = 0; jj < NU; ++jj)
+                    for (int l = 0; l < 32; ++l) {
+                        const int kk = 32 * jj + l;
+                        if (kk >= H) break;
+                        const float x1 = __shfl_sync(0xffffffffu, h1[jj], l);
+                        const float x2 = __shfl_sync(0xffffffffu, h2[jj], l);
+                        const float* r1 = U1t + (size_t)kk * H5;
+                        const float* r2 = U2t + (size_t)kk * H5;
+#pragma unroll
+                        for (int j = 0; j < NU; ++j) {
+                            const int u = lane + 32 * j;
+                            if (u < H)
+#pragma unroll
+                                for (int g = 0; g < 5; ++g)
+                                    acc[g][j] = fmaf(r1[g * H + u], x1, fmaf(r2[g * H + u], x2, acc[g][j]));
+                        }
+                    }
+            }
+            const float* pp = a.peep + (size_t)d * 6 * H;
+#pragma unroll
+            for (int j = 0; j < NU; ++j) {
+                const int u = lane + 32 * j;
+                if (u >= H) continue;
+                const float ig = sg_md(acc[0][j] + __ldg(pp + u) * s1[j] + __ldg(pp + H + u) * s2[j]);
+                const float f1 = sg_md(acc[1][j] + __ldg(pp + 2 * H + u) * s1[j]);
+                const float f2 = sg_md(acc[2][j] + __ldg(pp + 3 * H + u) * s2[j]);
+                const float zg = th_md(acc[3][j]);
+                const float og = sg_md(acc[4][j] + __ldg(pp + 4 * H + u) * s1[j] + __ldg(pp + 5 * H + u) * s2[j]);
+                const float cv = f1 * s1[j] + f2 * s2[j] + ig * zg;
+                const float hv = og * th_md(cv);
+                a.h[(size_t)p * H + u] = hv;
+                a.c[(size_t)p * H + u] = cv;
+                float* ar = a.act + (size_t)p * H5;
+                ar[u] = ig; ar[H + u] = f1; ar[2 * H + u] = f2; ar[3 * H + u] = zg; ar[4 * H + u] = og;
+                a.y[(size_t)px * a.ndir * H + (size_t)d * H + u] = hv;
+            }
+        }
+        if (k + 1 < a.steps && !md_barrier(a, (unsigned)(k + 1), 0xA00000u | (unsigned)k)) return;
+    }
+}
+
+// Backward walk (steps in reverse).  SM = U resident in shared memory.
+template <int NU, bool SM>
+__global__ void __launch_bounds__(kMdThreads) md_bwd_kernel(MdArgs a)
+{
+    extern __shared__ float md_smem[];
+    const int H = a.H, H5 = 5 * H;
+    constexpr int NR = (5 * 32 * NU + 31) / 32;      // 5H / 32 rounded up, per lane
+    const int lane = threadIdx.x & 31;
+    const float* Uw = a.U;
+    if (SM) {
+        const int64_t nw = (int64_t)a.ndir * 2 * H5 * H;
+        for (int64_t i = threadIdx.x; i < nw; i += blockDim.x) md_smem[i] = a.U[i];
+        __syncthreads();
+        Uw = md_smem;
+    }
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    unsigned done = 0;
+    for (int k = a.steps - 1; k >= 0; --k) {
+        const int64_t total = md_step_cells(a, k);
+        for (int64_t item = gw; item < total; item += warps) {
+            int d;
+            int64_t p;
+            md_item(a, k, item, d, p);
+            const int r1 = a.succ1[p], r2 = a.succ2[p];
+            const int q1 = a.pred1[p], q2 = a.pred2[p];
+            const int64_t px = a.src[p];
+            float e[NU], dsin[NU];
+#pragma unroll
+            for (int j = 0; j < NU; ++j) {
+                const int u = lane + 32 * j;
+                const bool ok = u < H;
+                e[j] = ok ? __ldg(a.dy + (size_t)px * a.ndir * H + (size_t)d * H + u) : 0.f;
+                dsin[j] = (ok && r1 >= 0 ? __ldcg(a.ds1 + (size_t)r1 * H + u) : 0.f) +
+                          (ok && r2 >= 0 ? __ldcg(a.ds2 + (size_t)r2 * H + u) : 0.f);
+            }
+            // U1^T da(successor 1) + U2^T da(successor 2): the successors' gate errors are
+            // spread over the lanes (element 32 m + lane in slot m) and broadcast one by one
+            const float* U1 = Uw + (size_t)d * 2 * H5 * H;
+            const float* U2 = U1 + (size_t)H5 * H;
+            if (r1 >= 0 || r2 >= 0) {
+                float g1[NR], g2[NR];
+#pragma unroll
+                for (int m = 0; m < NR; ++m) {
+                    const int r = 32 * m + lane;
+                    g1[m] = r < H5 && r1 >= 0 ? __ldcg(a.act + (size_t)r1 * H5 + r) : 0.f;
+                    g2[m] = r < H5 && r2 >= 0 ? __ldcg(a.act + (size_t)r2 * H5 + r) : 0.f;
+                }
+#pragma unroll
+                for (int m = 0; m < NR; ++m)
+                    for (int l = 0; l < 32; ++l) {
+                        const int r = 32 * m + l;
+                        if (r >= H5) break;
+                        const float x1 = __shfl_sync(0xffffffffu, g1[m], l);
+                        const float x2 = __shfl_sync(0xffffffffu, g2[m], l);
+#pragma unroll
+                        for (int j = 0; j < NU; ++j) {
+                            const int u = lane + 32 * j;
+                            if (u < H) e[j] = fmaf(U1[(size_t)r * H + u], x1, fmaf(U2[(size_t)r * H + u], x2, e[j]));
+                        }
+                    }
+            }
+            // every lane has read the successors' errors before any lane of another warp can
+            // change them: they were final at the previous barrier, and this cell writes only
+            // its own row
+            const float* pp = a.peep + (size_t)d * 6 * H;
+            float* ar = a.act + (size_t)p * H5;
+#pragma unroll
+            for (int j = 0; j < NU; ++j) {
+                const int u = lane + 32 * j;
+                if (u >= H) continue;
+                const float S1 = q1 >= 0 ? __ldcg(a.c + (size_t)q1 * H + u) : 0.f;
+                const float S2 = q2 >= 0 ? __ldcg(a.c + (size_t)q2 * H + u) : 0.f;
+                const float ig = ar[u], f1 = ar[H + u], f2 = ar[2 * H + u], zg = ar[3 * H + u], og = ar[4 * H + u];
+                const float cv = __ldcg(a.c + (size_t)p * H + u);
+                const float tc = th_md(cv);
+                const float dao = e[j] * tc * og * (1.f - og);
+                const float dc = e[j] * og * (1.f - tc * tc) + dsin[j];
+                const float dai = dc * zg * ig * (1.f - ig);
+                const float daf1 = dc * S1 * f1 * (1.f - f1);
+                const float daf2 = dc * S2 * f2 * (1.f - f2);
+                const float daz = dc * ig * (1.f - zg * zg);
+                a.ds1[(size_t)p * H + u] = dc * f1 + __ldg(pp + u) * dai + __ldg(pp + 2 * H + u) * daf1 +
+                                           __ldg(pp + 4 * H + u) * dao;
+                a.ds2[(size_t)p * H + u] = dc * f2 + __ldg(pp + H + u) * dai + __ldg(pp + 3 * H + u) * daf2 +
+                                           __ldg(pp + 5 * H + u) * dao;
+                ar[u] = dai; ar[H + u] = daf1; ar[2 * H + u] = daf2; ar[3 * H + u] = daz; ar[4 * H + u] = dao;
+                float* dp = a.dap + (size_t)px * a.ndir * H5 + (size_t)d * H5;
+                dp[u] = dai; dp[H + u] = daf1; dp[2 * H + u] = daf2; dp[3 * H + u] = daz; dp[4 * H + u] = dao;
+            }
+        }
+        ++done;
+        if (k > 0 && !md_barrier(a, done, 0xB00000u | (unsigned)k)) return;
+    }
+}
+
+// U [ndir][2][5H][H] -> U^T [ndir][2][H][5H]
+__global__ void md_transpose_kernel(const float* __restrict__ U1, const float* __restrict__ U2, float* __restrict__ UT,
+                                    float* __restrict__ Ucat, int ndir, int H)
+{
+    const int H5 = 5 * H;
+    const int64_t n = (int64_t)ndir * 2 * H5 * H;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t per = (int64_t)H5 * H;
+        const int d = (int)(i / (2 * per));
+        const int w = (int)((i / per) & 1);
+        const int64_t r = i % per;                   // element of U_w[d]: row r / H, column r % H
+        const int row = (int)(r / H), col = (int)(r % H);
+        const float v = (w == 0 ? U1 : U2)[(size_t)d * per + r];
+        Ucat[i] = v;
+        UT[(size_t)d * 2 * per + (size_t)w * per + (size_t)col * H5 + row] = v;
+    }
+}
+
+// db and the peephole sums of one direction: column j < 5H -> sum of da_j; 5H + 6q + .. ->
+// peephole q of unit u: q = 0 i1 (da_i S1), 1 i2 (da_i S2), 2 f1 (da_f1 S1), 3 f2 (da_f2 S2),
+// 4 o1 (da_o S1), 5 o2 (da_o S2).  Each thread sums one column over one chunk of the
+// direction's cells in cell order; the chunks are added in chunk order (bitwise repeatable).
+__global__ void md_param_sums_kernel(const float* __restrict__ act, const float* __restrict__ c,
+                                     const int32_t* __restrict__ pred1, const int32_t* __restrict__ pred2, int H,
+                                     int64_t N, int ndir, int64_t chunk, float* __restrict__ partial)
+{
+    const int ncol = 11 * H;
+    const int col = blockIdx.x * blockDim.x + threadIdx.x;
+    const int d = blockIdx.z;
+    if (col >= ncol || d >= ndir) return;
+    const int64_t lo = (int64_t)blockIdx.y * chunk, hi = min(N, lo + chunk);
+    const int H5 = 5 * H;
+    float s = 0.f;
+    const int64_t base = (int64_t)d * N;
+    if (col < H5) {
+        for (int64_t i = lo; i < hi; ++i) s += act[(size_t)(base + i) * H5 + col];
+    } else {
+        const int q = (col - H5) / H, u = (col - H5) % H;
+        const int gate = q < 2 ? 0 : q == 2 ? 1 : q == 3 ? 2 : 4;     // i, i, f1, f2, o, o
+        const bool first = (q & 1) == 0;                               // S1 (else S2)
+        for (int64_t i = lo; i < hi; ++i) {
+            const int pr = first ? pred1[base + i] : pred2[base + i];
+            if (pr >= 0) s += act[(size_t)(base + i) * H5 + gate * H + u] * c[(size_t)pr * H + u];
+        }
+    }
+    partial[((size_t)d * gridDim.y + blockIdx.y) * ncol + col] = s;
+}
+
+__global__ void md_param_sums_combine(const float* __restrict__ partial, int chunks, int H, int ndir,
+                                      float* __restrict__ db, float* __restrict__ dpeep)
+{
+    const int ncol = 11 * H, H5 = 5 * H;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= ndir * ncol) return;
+    const int d = i / ncol, col = i % ncol;
+    float s = 0.f;
+    for (int k = 0; k < chunks; ++k) s += partial[((size_t)d * chunks + k) * ncol + col];
+    if (col < H5) {
+        if (db) db[(size_t)d * H5 + col] = s;
+    } else if (dpeep) {
+        dpeep[(size_t)d * 6 * H + (col - H5)] = s;
+    }
+}
+
+// ---------------------------------------------------------------- workspace layout
+
+struct MdLayout {
+    size_t gx, h, c, act, ut, ucat, total;          // byte offsets (workspace)
+    size_t ds1, ds2, part, sums, stotal;            // byte offsets (scratch)
+    int chunks = 1;
+};
+
+size_t al256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+MdLayout md_layout(const MdPlan& p, int D, int H)
+{
+    MdLayout L;
+    const size_t N = (size_t)p.pixels, cells = (size_t)p.cells, nd = (size_t)p.ndir, H5 = 5 * (size_t)H;
+    size_t o = 0;
+    L.gx = o; o = al256(o + 4 * N * nd * H5);
+    L.h = o; o = al256(o + 4 * cells * H);
+    L.c = o; o = al256(o + 4 * cells * H);
+    L.act = o; o = al256(o + 4 * cells * H5);
+    L.ut = o; o = al256(o + 4 * nd * 2 * H5 * H);
+    L.ucat = o; o = al256(o + 4 * nd * 2 * H5 * H);
+    L.total = o;
+    // scratch: ds1, ds2, GEMM partials (the largest of the products), parameter-sum partials
+    o = 0;
+    L.ds1 = o; o = al256(o + 4 * cells * H);
+    L.ds2 = o; o = al256(o + 4 * cells * H);
+    GemmDesc dw;
+    dw.M = (int)(nd * H5); dw.N = D; dw.K = (int)N; dw.k_splits = kMdMaxSplits;
+    GemmDesc du;
+    du.M = (int)H5; du.N = H; du.K = (int)N; du.k_splits = kMdMaxSplits;
+    const size_t part = std::max(gemm_partial_floats(dw, p.num_sms), gemm_partial_floats(du, p.num_sms));
+    L.part = o; o = al256(o + 4 * part);
+    const int64_t chunk = 2048;
+    L.chunks = (int)std::max<int64_t>(1, (p.pixels + chunk - 1) / chunk);
+    L.sums = o; o = al256(o + 4 * nd * (size_t)L.chunks * 11 * H);
+    L.stotal = o;
+    return L;
+}
+
+bool md_shape_ok(const MdPlan& p, const lstm_md_shape* s)
+{
+    return s && s->hidden_size >= 1 && s->hidden_size <= kMdMaxH && s->input_size >= 1 &&
+           s->num_directions == p.ndir;
+}
+
+bool al16(const void* q) { return ((uintptr_t)q & 15) == 0; }
+
+template <bool FWD>
+lstm_status md_launch(const MdPlan& p, MdArgs& a, cudaStream_t s)
+{
+    const int H = a.H;
+    const int NU = (H + 31) / 32;
+    const size_t wbytes = (size_t)p.ndir * 2 * 5 * H * H * 4;
+    const bool sm = wbytes <= kMdSmemCap;
+    const void* fn = nullptr;
+#define MD_PICK(nu)                                                                                  \
+    if (NU == nu) fn = FWD ? (sm ? (const void*)md_fwd_kernel<nu, true> : (const void*)md_fwd_kernel<nu, false>) \
+                           : (sm ? (const void*)md_bwd_kernel<nu, true> : (const void*)md_bwd_kernel<nu, false>);
+    MD_PICK(1) MD_PICK(2) MD_PICK(3) MD_PICK(4)
+#undef MD_PICK
+    if (!fn) return LSTM_ERR_UNSUPPORTED;
+    const size_t smem = sm ? wbytes : 0;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+        cudaGetLastError();
+        return LSTM_ERR_UNSUPPORTED;
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kMdThreads, smem) != cudaSuccess || per_sm < 1) {
+        cudaGetLastError();
+        return LSTM_ERR_UNSUPPORTED;
+    }
+    const int grid = p.num_sms * std::min(per_sm, 2);
+    if (cudaMemsetAsync(a.ctr, 0, sizeof(unsigned), s) != cudaSuccess) return LSTM_ERR_CUDA;
+    void* args[] = {&a};
+    tracer_begin(p.tracer, FWD ? MD_FWD : MD_BWD, s);
+    const cudaError_t e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kMdThreads), args, smem, s);
+    tracer_end(p.tracer, FWD ? MD_FWD : MD_BWD, s, e == cudaSuccess ? 1 : 0);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return LSTM_ERR_CUDA;
+    }
+    return LSTM_OK;
+}
+
+MdArgs md_args(const MdPlan& p, int H)
+{
+    MdArgs a;
+    memset(&a, 0, sizeof(a));
+    a.H = H; a.ndir = p.ndir; a.steps = p.steps; a.N = p.pixels;
+    a.step_off = p.d_step_off; a.src = p.d_src;
+    a.pred1 = p.d_pred1; a.pred2 = p.d_pred2; a.succ1 = p.d_succ1; a.succ2 = p.d_succ2;
+    a.ctr = p.d_ctr; a.status = p.d_status; a.wait_limit_ns = p.wait_limit_ns;
+    a.debug_skip_cta = p.debug_skip_cta;
+    return a;
+}
+
+// dx = dA W, dW = dA^T x (pixel order, all directions at once); dU1, dU2 per direction; db and
+// the peephole sums.  *launched counts the kernels.
+lstm_status md_grads(const MdPlan& p, int D, int H, const lstm_md_params* prm, const float* x, const float* dap,
+                          const float* h, const float* c, const float* act, float* dx, const lstm_md_grads* grads,
+                          float* part, float* sums, int chunks, cudaStream_t s, int* launched)
+{
+    const int nd = p.ndir, H5 = 5 * H;
+    lstm_status st = LSTM_OK;
+    if (dx) {
+        lstm::GemmDesc g;
+        g.M = (int)p.pixels; g.N = D; g.K = nd * H5;
+        g.A = dap; g.sam = nd * H5; g.sak = 1;
+        g.B = prm->W; g.sbk = D; g.sbn = 1;
+        g.C = dx; g.ldc = D;
+        g.partial = part;
+        if ((st = gemm_simt_run(g, p.num_sms, s)) != LSTM_OK) return st;
+        *launched += 1;
+    }
+    if (grads->W) {
+        lstm::GemmDesc g;
+        g.M = nd * H5; g.N = D; g.K = (int)p.pixels;
+        g.A = dap; g.sam = 1; g.sak = nd * H5;
+        g.B = x; g.sbk = D; g.sbn = 1;
+        g.C = grads->W; g.ldc = D;
+        g.k_splits = kMdMaxSplits;                       // the cap; the launcher picks the count
+        g.k_splits = gemm_choose_splits(g, p.num_sms);
+        g.partial = part;
+        if ((st = gemm_simt_run(g, p.num_sms, s)) != LSTM_OK) return st;
+        *launched += g.k_splits > 1 ? 2 : 1;
+    }
+    // dU1 / dU2 of each direction: its cells' gate errors against the predecessors' h
+    for (int d = 0; d < nd; ++d)
+        for (int w = 0; w < 2; ++w) {
+            float* dst = w == 0 ? grads->U1 : grads->U2;
+            if (!dst) continue;
+            lstm::GemmDesc g;
+            g.M = H5; g.N = H; g.K = (int)p.pixels;
+            g.A = act + (size_t)d * p.pixels * H5; g.sam = 1; g.sak = H5;
+            g.B = h; g.sbk = H; g.sbn = 1;
+            g.b_rows = (w == 0 ? p.d_pred1 : p.d_pred2) + (size_t)d * p.pixels;
+            g.C = dst + (size_t)d * H5 * H; g.ldc = H;
+            g.k_splits = kMdMaxSplits;                   // the cap; the launcher picks the count
+            g.k_splits = gemm_choose_splits(g, p.num_sms);
+            g.partial = part;
+            if ((st = gemm_simt_run(g, p.num_sms, s)) != LSTM_OK) return st;
+            *launched += g.k_splits > 1 ? 2 : 1;
+        }
+    if (grads->b || grads->peep) {
+        const int ncol = 11 * H;
+        const int64_t chunk = (p.pixels + chunks - 1) / chunks;
+        dim3 grid((ncol + 127) / 128, chunks, nd);
+        md_param_sums_kernel<<<grid, 128, 0, s>>>(act, c, p.d_pred1, p.d_pred2, H, p.pixels, nd, chunk, sums);
+        md_param_sums_combine<<<(nd * ncol + 255) / 256, 256, 0, s>>>(sums, chunks, H, nd, grads->b, grads->peep);
+        if (cudaGetLastError() != cudaSuccess) return LSTM_ERR_CUDA;
+        *launched += 2;
+    }
+    return LSTM_OK;
+}
+
+}  // namespace
+
+}  // namespace lstm
+
+using lstm::MdLayout;
+using lstm::MdPlan;
+
+extern "C" {
+
+size_t lstm_md_workspace_bytes(const lstm_md_plan* plan, const lstm_md_shape* shape)
+{
+    if (!plan || !lstm::md_shape_ok(plan->p, shape)) return 0;
+    return lstm::md_layout(plan->p, shape->input_size, shape->hidden_size).total;
+}
+
+size_t lstm_md_scratch_bytes(const lstm_md_plan* plan, const lstm_md_shape* shape)
+{
+    if (!plan || !lstm::md_shape_ok(plan->p, shape)) return 0;
+    return lstm::md_layout(plan->p, shape->input_size, shape->hidden_size).stotal;
+}
+
+lstm_status lstm_md_fwd(const lstm_md_plan* plan, const lstm_md_shape* shape, const lstm_md_params* prm,
+                        const float* x, float* y, void* workspace, void* stream)
+{
+    if (!plan || !prm) return LSTM_ERR_INVALID_ARG;
+    const MdPlan& p = plan->p;
+    if (!lstm::md_shape_ok(p, shape)) return LSTM_ERR_INVALID_ARG;
+    if (!p.d_src) return LSTM_ERR_UNSUPPORTED;                  // a host-only plan
+    if (p.pixels == 0) return LSTM_OK;
+    if (!x || !y || !workspace || !prm->W || !prm->U1 || !prm->U2 || !prm->b || !prm->peep) return LSTM_ERR_INVALID_ARG;
+    if (!lstm::al16(workspace)) return LSTM_ERR_INVALID_ARG;
+    const int D = shape->input_size, H = shape->hidden_size, nd = p.ndir, H5 = 5 * H;
+    cudaStream_t s = (cudaStream_t)stream;
+    const MdLayout L = lstm::md_layout(p, D, H);
+    char* ws = (char*)workspace;
+    float* gx = (float*)(ws + L.gx);
+    // 1. gx = x W^T + b for every pixel and direction
+    lstm::GemmDesc g;
+    g.M = (int)p.pixels; g.N = nd * H5; g.K = D;
+    g.A = x; g.sam = D; g.sak = 1;
+    g.B = prm->W; g.sbk = 1; g.sbn = D;
+    g.C = gx; g.ldc = nd * H5; g.bias = prm->b;
+    lstm::tracer_begin(p.tracer, lstm::MD_INPUT, s);
+    lstm_status st = lstm::gemm_simt_run(g, p.num_sms, s);
+    // 2. U^T (forward operand) and U (backward operand, kept in the workspace)
+    if (st == LSTM_OK) {
+        lstm::md_transpose_kernel<<<64, 256, 0, s>>>(prm->U1, prm->U2, (float*)(ws + L.ut), (float*)(ws + L.ucat),
+                                                     nd, H);
+        if (cudaGetLastError() != cudaSuccess) st = LSTM_ERR_CUDA;
+    }
+    lstm::tracer_end(p.tracer, lstm::MD_INPUT, s, st == LSTM_OK ? 2 : 0);
+    if (st != LSTM_OK) return st;
+    lstm::MdArgs a = lstm::md_args(p, H);
+    a.U = (const float*)(ws + L.ut);
+    a.peep = prm->peep;
+    a.gx = gx;
+    a.h = (float*)(ws + L.h); a.c = (float*)(ws + L.c); a.act = (float*)(ws + L.act);
+    a.y = y;
+    return lstm::md_launch<true>(p, a, s);
+}
+
+lstm_status lstm_md_bwd(const lstm_md_plan* plan, const lstm_md_shape* shape, const lstm_md_params* prm,
+                        const float* x, void* workspace, const float* dy, float* dx, const lstm_md_grads* grads,
+                        void* scratch, void* stream)
+{
+    if (!plan || !prm || !grads) return LSTM_ERR_INVALID_ARG;
+    const MdPlan& p = plan->p;
+    if (!lstm::md_shape_ok(p, shape)) return LSTM_ERR_INVALID_ARG;
+    if (!p.d_src) return LSTM_ERR_UNSUPPORTED;
+    const int D = shape->input_size, H = shape->hidden_size, nd = p.ndir, H5 = 5 * H;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (p.pixels == 0) {      // no pixel: every gradient is zero
+        const size_t pc[5] = {(size_t)nd * H5 * D, (size_t)nd * H5 * H, (size_t)nd * H5 * H, (size_t)nd * H5,
+                              (size_t)nd * 6 * H};
+        float* dst[5] = {grads->W, grads->U1, grads->U2, grads->b, grads->peep};
+        for (int i = 0; i < 5; ++i)
+            if (dst[i] && cudaMemsetAsync(dst[i], 0, sizeof(float) * pc[i], s) != cudaSuccess) return LSTM_ERR_CUDA;
+        return LSTM_OK;
+    }
+    if (!x || !dy || !workspace || !scratch || !prm->W || !prm->peep) return LSTM_ERR_INVALID_ARG;
+    if (!lstm::al16(workspace) || !lstm::al16(scratch)) return LSTM_ERR_INVALID_ARG;
+    const MdLayout L = lstm::md_layout(p, D, H);
+    char* ws = (char*)workspace;
+    char* sc = (char*)scratch;
+    float* dap = (float*)(ws + L.gx);             // the pre-activations' region, no longer needed
+    float* h = (float*)(ws + L.h);
+    float* c = (float*)(ws + L.c);
+    float* act = (float*)(ws + L.act);
+    float* part = (float*)(sc + L.part);
+    lstm::MdArgs a = lstm::md_args(p, H);
+    a.U = (const float*)(ws + L.ucat);
+    a.peep = prm->peep;
+    a.h = h; a.c = c; a.act = act; a.dy = dy; a.dap = dap;
+    a.ds1 = (float*)(sc + L.ds1); a.ds2 = (float*)(sc + L.ds2);
+    lstm_status st = lstm::md_launch<false>(p, a, s);
+    if (st != LSTM_OK) return st;
+    lstm::tracer_begin(p.tracer, lstm::MD_GRADS, s);
+    int launched = 0;
+    st = lstm::md_grads(p, D, H, prm, x, dap, h, c, act, dx, grads, part, (float*)(sc + L.sums), L.chunks, s,
+                        &launched);
+    lstm::tracer_end(p.tracer, lstm::MD_GRADS, s, launched);
+    return st;
+}
+
+}  // extern "C"

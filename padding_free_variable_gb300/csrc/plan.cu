@@ -60,9 +60,8 @@ lstm_status launch_pack(const Plan& p, const void* src, int width, int elem_byte
     return cudaGetLastError() == cudaSuccess ? LSTM_OK : LSTM_ERR_CUDA;
 }
 
-void trace_begin(const Plan& p, int kind, cudaStream_t s)
+void tracer_begin(Tracer* t, int kind, cudaStream_t s)
 {
-    Tracer* t = p.tracer;
     if (!t || !t->enabled || kind < 0) return;     // kind < 0: counted, not timed (inside another kind)
     if (t->npending == t->cap) {
         int ncap = t->cap ? 2 * t->cap : 64;
@@ -79,9 +78,8 @@ void trace_begin(const Plan& p, int kind, cudaStream_t s)
     ++t->npending;
 }
 
-void trace_end(const Plan& p, int kind, cudaStream_t s, int kernels)
+void tracer_end(Tracer* t, int kind, cudaStream_t s, int kernels)
 {
-    Tracer* t = p.tracer;
     if (!t) return;
     t->launches += kernels;
     if (!t->enabled || t->npending == 0 || kind < 0) return;
@@ -89,7 +87,11 @@ void trace_end(const Plan& p, int kind, cudaStream_t s, int kernels)
     if (r.kind == kind) cudaEventRecord(r.b, s);
 }
 
-static void tracer_flush(Tracer* t)
+void trace_begin(const Plan& p, int kind, cudaStream_t s) { tracer_begin(p.tracer, kind, s); }
+
+void trace_end(const Plan& p, int kind, cudaStream_t s, int kernels) { tracer_end(p.tracer, kind, s, kernels); }
+
+void tracer_flush(Tracer* t)
 {
     for (int i = 0; i < t->npending; ++i) {
         Tracer::Rec& r = t->pending[i];

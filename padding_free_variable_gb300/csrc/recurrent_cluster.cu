@@ -54,7 +54,7 @@ namespace {
 constexpr int kCU = 32;        // units per CTA
 constexpr int kCM = 128;       // gate rows per CTA (MMA M)
 constexpr int kCT = 256;       // threads
-constexpr int kSumChunks = 64; // row chunks of the db / dpeep sums
+constexpr int kSumChunks = 128; // row chunks of the db / dpeep sums
 // bound on the teardown wait for a product still in flight after a timeout
 // (an MMA takes microseconds; TMEM is freed only after it has completed)
 constexpr unsigned long long kTeardownWaitNs = 1000000000ull;
@@ -1281,8 +1281,9 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
 }
 
 // db and dpeep from the gate errors: column (direction, quantity q, unit u),
-// q = 0..3 -> sum of da_q, 4 -> da_i c_{t-1}, 5 -> da_f c_{t-1}, 6 -> da_o c_t;
-// each thread sums its column over one chunk of rows in row order, and the
+// q = 0..3 -> sum of da_q, 4 -> da_i c_{t-1}, 5 -> da_f c_{t-1}, 6 -> da_o c_t.
+// Thread (direction, unit) takes all seven columns of its unit over one chunk of
+// rows, in row order, so each row's gate errors and states are read once; the
 // chunks are then added in chunk order (bitwise repeatable).  c_{t-1} of a
 // sequence's first step is its initial state c0 (zero when c0 is null).
 __global__ void lstm_param_sums_kernel(const float* __restrict__ ga, const float* __restrict__ cbuf,
@@ -1291,28 +1292,27 @@ __global__ void lstm_param_sums_kernel(const float* __restrict__ ga, const float
                                        const int32_t* __restrict__ perm, int B,
                                        int rows, int H, int ndir, int chunk, float* __restrict__ partial)
 {
-    const int ncols = ndir * 7 * H;
-    const int col = blockIdx.x * blockDim.x + threadIdx.x;
-    if (col >= ncols) return;
-    const int d = col / (7 * H), rem = col - d * 7 * H, q = rem / H, u = rem - q * H;
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= ndir * H) return;
+    const int d = t / H, u = t - d * H;
     const int r0 = blockIdx.y * chunk, r1 = min(rows, r0 + chunk);
     const int nd4H = ndir * 4 * H, ndH = ndir * H;
     const int32_t* prev = d == 0 ? prev_fwd : prev_rev;
-    const int gq = q < 4 ? q : (q == 4 ? 0 : (q == 5 ? 1 : 3));
-    float s = 0.f;
+    float s[7] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
     for (int r = r0; r < r1; ++r) {
-        const float v = __ldg(ga + (size_t)r * nd4H + d * 4 * H + gq * H + u);
-        if (q < 4) s += v;
-        else if (q < 6) {
-            const int pr = __ldg(prev + r);
-            const float cp = pr >= 0 ? __ldg(cbuf + (size_t)pr * ndH + d * H + u)
-                           : c0 ? __ldg(c0 + ((size_t)d * B + __ldg(perm + __ldg(row_slot + r))) * H + u) : 0.f;
-            s += v * cp;
-        } else {
-            s += v * __ldg(cbuf + (size_t)r * ndH + d * H + u);
-        }
+        const float* g = ga + (size_t)r * nd4H + (size_t)d * 4 * H + u;
+        const float ai = __ldg(g), af = __ldg(g + H), az = __ldg(g + 2 * H), ao = __ldg(g + 3 * H);
+        const int pr = __ldg(prev + r);
+        const float cp = pr >= 0 ? __ldg(cbuf + (size_t)pr * ndH + d * H + u)
+                       : c0 ? __ldg(c0 + ((size_t)d * B + __ldg(perm + __ldg(row_slot + r))) * H + u) : 0.f;
+        const float ct = __ldg(cbuf + (size_t)r * ndH + d * H + u);
+        s[0] += ai; s[1] += af; s[2] += az; s[3] += ao;
+        s[4] += ai * cp; s[5] += af * cp; s[6] += ao * ct;
     }
-    partial[(size_t)blockIdx.y * ncols + col] = s;
+    float* out = partial + (size_t)blockIdx.y * ndir * 7 * H + (size_t)d * 7 * H + u;
+#pragma unroll
+    for (int q = 0; q < 7; ++q) out[(size_t)q * H] = s[q];
 }
 
 __global__ void lstm_param_sums_combine(const float* __restrict__ partial, int chunks, int H, int ndir,
@@ -1602,7 +1602,7 @@ lstm_status param_sums_launch(const Plan& p, const float* ga, const float* cbuf,
     const int ncols = ndir * 7 * H;
     const int rows = (int)p.rows;
     const int chunk = (rows + kSumChunks - 1) / kSumChunks;
-    lstm_param_sums_kernel<<<dim3((ncols + 255) / 256, kSumChunks), 256, 0, s>>>(
+    lstm_param_sums_kernel<<<dim3((ndir * H + 127) / 128, kSumChunks), 128, 0, s>>>(
         ga, cbuf, p.d_prev_fwd, p.d_prev_rev, c0, p.d_row_slot, p.d_perm, p.B, rows, H, ndir, chunk, sum_scratch);
     lstm_param_sums_combine<<<(ncols + 255) / 256, 256, 0, s>>>(sum_scratch, kSumChunks, H, ndir, db, dpeep);
     return cudaGetLastError() == cudaSuccess ? LSTM_OK : LSTM_ERR_UNSUPPORTED;

@@ -439,3 +439,153 @@ class TruncatedBPTT:
                 h[:, 1].zero_()
                 c[:, 1].zero_()
         return y_cat, dx_cat, grads
+
+
+# --------------------------------------------------------------------------- 2-D (MDLSTM) layers
+
+def md_compute_host(heights, widths, row_width: int = 0, num_directions: int = 1, schedule: int = 0) -> dict:
+    """The 2-D packing and schedule computed on the host (lstm_md_plan_compute_host)."""
+    lib = _lib.load()
+    hs = np.ascontiguousarray(np.asarray(heights, dtype=np.int32))
+    ws = np.ascontiguousarray(np.asarray(widths, dtype=np.int32))
+    n = int(hs.size)
+    N = int((hs.astype(np.int64) * ws).sum())
+    cells = N * int(num_directions)
+    pi = ctypes.POINTER(ctypes.c_int32)
+    info = np.zeros(4, dtype=np.int32)
+    y0 = np.zeros(max(n, 1), dtype=np.int32)
+    x0 = np.zeros(max(n, 1), dtype=np.int32)
+    # the step count is only known afterwards: ask for it first
+    check(lib.lstm_md_plan_compute_host(hs.ctypes.data_as(pi), ws.ctypes.data_as(pi), n, int(row_width),
+                                        int(num_directions), int(schedule), info.ctypes.data_as(pi), None, None,
+                                        None, None, None, None, None, None), "lstm_md_plan_compute_host")
+    steps = int(info[0])
+    step_off = np.zeros(num_directions * (steps + 1), dtype=np.int64)
+    t = {k: np.zeros(max(cells, 1), dtype=np.int32) for k in ("src", "pred1", "pred2", "succ1", "succ2")}
+    check(lib.lstm_md_plan_compute_host(hs.ctypes.data_as(pi), ws.ctypes.data_as(pi), n, int(row_width),
+                                        int(num_directions), int(schedule), info.ctypes.data_as(pi),
+                                        y0.ctypes.data_as(pi), x0.ctypes.data_as(pi),
+                                        step_off.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                        *[t[k].ctypes.data_as(pi) for k in ("src", "pred1", "pred2", "succ1",
+                                                                            "succ2")]),
+          "lstm_md_plan_compute_host")
+    out = {"steps": steps, "height": int(info[1]), "width": int(info[2]), "rows": int(info[3]),
+           "y0": y0[:n], "x0": x0[:n], "step_off": step_off.reshape(num_directions, steps + 1)}
+    out.update({k: v[:cells] for k, v in t.items()})
+    return out
+
+
+class MdPlan:
+    """Example-packing plan of a list of images for one MDLSTM layer's scan directions.
+    schedule 1 (default): every image from step 0 along its own anti-diagonals; 0: the
+    page's canvas, a cell at its skewed canvas column (same results, more steps)."""
+
+    def __init__(self, heights, widths, row_width: int = 0, num_directions: int = 4, schedule: int = 1):
+        lib = _lib.load()
+        self.heights = np.ascontiguousarray(np.asarray(heights, dtype=np.int32))
+        self.widths = np.ascontiguousarray(np.asarray(widths, dtype=np.int32))
+        self.num_directions = int(num_directions)
+        h = ctypes.c_void_p()
+        pi = ctypes.POINTER(ctypes.c_int32)
+        check(lib.lstm_md_plan_create(self.heights.ctypes.data_as(pi), self.widths.ctypes.data_as(pi),
+                                      int(self.heights.size), int(row_width), self.num_directions, int(schedule),
+                                      ctypes.byref(h)), "lstm_md_plan_create")
+        self.handle = h
+        px, st, ch, cw, rows = (ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32(),
+                                ctypes.c_int32())
+        check(lib.lstm_md_plan_info(h, ctypes.byref(px), ctypes.byref(st), ctypes.byref(ch), ctypes.byref(cw),
+                                    ctypes.byref(rows)), "lstm_md_plan_info")
+        self.pixels, self.steps = px.value, st.value
+        self.canvas = (ch.value, cw.value)
+        self.rows = rows.value
+
+    def placement(self):
+        n = int(self.heights.size)
+        y0 = np.zeros(max(n, 1), dtype=np.int32)
+        x0 = np.zeros(max(n, 1), dtype=np.int32)
+        pi = ctypes.POINTER(ctypes.c_int32)
+        check(_lib.load().lstm_md_plan_placement(self.handle, y0.ctypes.data_as(pi), x0.ctypes.data_as(pi)),
+              "lstm_md_plan_placement")
+        return y0[:n], x0[:n]
+
+    def step_cells(self) -> np.ndarray:
+        so = np.zeros(self.num_directions * (self.steps + 1), dtype=np.int64)
+        check(_lib.load().lstm_md_plan_step_cells(self.handle, so.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))),
+              "lstm_md_plan_step_cells")
+        return so.reshape(self.num_directions, self.steps + 1)
+
+    def set_wait_limit(self, ns: int):
+        check(_lib.load().lstm_md_plan_set_wait_limit(self.handle, int(ns)), "lstm_md_plan_set_wait_limit")
+
+    def poll(self, stream=None) -> int:
+        return int(_lib.load().lstm_md_status_poll(self.handle, _stream(stream)))
+
+    def debug_skip_arrival(self, cta: int):
+        check(_lib.load().lstm_md_debug_skip_arrival(self.handle, int(cta)), "lstm_md_debug_skip_arrival")
+
+    def launch_count(self) -> int:
+        return int(_lib.load().lstm_md_plan_launch_count(self.handle))
+
+    def enable_timing(self, on: bool = True):
+        check(_lib.load().lstm_md_plan_enable_timing(self.handle, 1 if on else 0), "lstm_md_plan_enable_timing")
+
+    def read_timing(self) -> dict:
+        ms = (ctypes.c_double * 4)()
+        calls = (ctypes.c_int64 * 4)()
+        check(_lib.load().lstm_md_plan_read_timing(self.handle, ms, calls), "lstm_md_plan_read_timing")
+        return {k: (ms[i], calls[i]) for i, k in enumerate(_lib.MD_KINDS)}
+
+    def close(self):
+        if getattr(self, "handle", None):
+            _lib.load().lstm_md_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class MdLayer:
+    """One MDLSTM layer (fp32) over an MdPlan: device weights, workspace and scratch.
+    layer: W[ndir,5H,D], U1/U2[ndir,5H,H], b[ndir,5H], peep[ndir,6,H] (torch, cuda)."""
+
+    def __init__(self, plan: MdPlan, layer: dict, input_size: int, hidden_size: int, device="cuda"):
+        lib = _lib.load()
+        self.plan = plan
+        self.layer = {k: torch.as_tensor(v, dtype=torch.float32, device=device).contiguous() for k, v in layer.items()}
+        self.shape = _lib.MdShape(int(input_size), int(hidden_size), plan.num_directions)
+        ws = lib.lstm_md_workspace_bytes(plan.handle, ctypes.byref(self.shape))
+        sc = lib.lstm_md_scratch_bytes(plan.handle, ctypes.byref(self.shape))
+        if ws == 0 and plan.pixels > 0:
+            raise ValueError("unsupported MDLSTM layer shape")
+        self.workspace = torch.empty(max(int(ws), 16), dtype=torch.uint8, device=device)
+        self.scratch = torch.empty(max(int(sc), 16), dtype=torch.uint8, device=device)
+        self.grads = {k: torch.empty_like(v) for k, v in self.layer.items()}
+
+    def _params(self):
+        L = self.layer
+        return _lib.MdParams(L["W"].data_ptr(), L["U1"].data_ptr(), L["U2"].data_ptr(), L["b"].data_ptr(),
+                             L["peep"].data_ptr())
+
+    def forward(self, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        nd, H = self.plan.num_directions, self.shape.hidden_size
+        if y is None:
+            y = torch.empty((self.plan.pixels, nd * H), dtype=torch.float32, device=x.device)
+        prm = self._params()
+        check(_lib.load().lstm_md_fwd(self.plan.handle, ctypes.byref(self.shape), ctypes.byref(prm), _ptr(x),
+                                      _ptr(y), _ptr(self.workspace), _stream(stream)), "lstm_md_fwd")
+        return y
+
+    def backward(self, x: torch.Tensor, dy: torch.Tensor, dx: torch.Tensor | None = None, stream=None):
+        if dx is None:
+            dx = torch.empty_like(x)
+        prm = self._params()
+        g = self.grads
+        gr = _lib.MdGrads(g["W"].data_ptr(), g["U1"].data_ptr(), g["U2"].data_ptr(), g["b"].data_ptr(),
+                          g["peep"].data_ptr())
+        check(_lib.load().lstm_md_bwd(self.plan.handle, ctypes.byref(self.shape), ctypes.byref(prm), _ptr(x),
+                                      _ptr(self.workspace), _ptr(dy), _ptr(dx), ctypes.byref(gr), _ptr(self.scratch),
+                                      _stream(stream)), "lstm_md_bwd")
+        return dx

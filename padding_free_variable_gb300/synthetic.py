@@ -170,3 +170,104 @@ def custom(num_directions: int, num_layers: int, input_size: int, hidden_size: i
                         len(lengths), ("fixed", tuple(int(v) for v in lengths)), x_dist,
                         weight_range, forget_bias)
     return make_workload(spec, seed)
+
+
+# --------------------------------------------------------------------------- 2-D (MDLSTM) workloads
+#
+# "No Padding Please", Sec. VII: word strips (IAM words, batch 200 with packing)
+# and line strips (IAM lines, batch 12 with packing) feed MDLSTM layers of 2 to 100
+# units after block-strided convolutions.  The page gives no image-size
+# distribution; these stand-ins draw heights and widths uniformly in ranges of the
+# feature maps such strips give after the model's first 4x down-sampling, one
+# MDLSTM layer with its four scan directions.
+#
+#   name    images  height   width     D   H
+#   words   200     [8, 24]  [8, 96]   16  32
+#   lines   12      [12, 20] [200, 600] 16 32
+#
+# Draw order from ``numpy.random.default_rng(seed)``: heights, widths, x, then per
+# direction (W, U1, U2, b, peep), then G; the named workloads then add a forget bias of -1
+# to both forget gates' biases.  Layouts: W[ndir, 5H, D], U1/U2[ndir, 5H, H],
+# b[ndir, 5H], peep[ndir, 6, H] (p_i1, p_i2, p_f1, p_f2, p_o1, p_o2), gate blocks in
+# the order (i, f1, f2, z, o); x[N, D] and G[N, ndir*H] in caller order (images back to
+# back, each row by row).
+
+
+@dataclasses.dataclass(frozen=True)
+class MdSpec:
+    name: str
+    num_directions: int
+    input_size: int
+    hidden_size: int
+    batch: int
+    heights: tuple          # ("uniform", lo, hi)
+    widths: tuple
+    x_dist: str
+    weight_range: float
+    forget_bias: float = -1.0
+
+
+# forget bias -1 on both forget gates: f1 + f2 stays near 0.5 instead of 1, the regime in which
+# the 2-D state does not grow along the scan (Sec. III: with the two forget gates summing to
+# more than one the state norm grows, the instability the page's stable cells address)
+MD_WORKLOADS = {
+    "words": MdSpec("md-4x32-d16-words-b200", 4, 16, 32, 200, ("uniform", 8, 24), ("uniform", 8, 96),
+                    "uniform01", 0.1),
+    "lines": MdSpec("md-4x32-d16-lines-b12", 4, 16, 32, 12, ("uniform", 12, 20), ("uniform", 200, 600),
+                    "uniform01", 0.1),
+}
+
+
+@dataclasses.dataclass
+class MdWorkload:
+    name: str
+    heights: np.ndarray
+    widths: np.ndarray
+    x: np.ndarray
+    layer: dict
+    G: np.ndarray
+    num_directions: int
+    input_size: int
+    hidden_size: int
+
+    @property
+    def N(self) -> int:
+        return int((self.heights.astype(np.int64) * self.widths).sum())
+
+
+def md_custom(num_directions: int, input_size: int, hidden_size: int, heights, widths, seed: int,
+              weight_range: float = 0.1, x_dist: str = "normal", name: str = "md-custom",
+              forget_bias: float = 0.0) -> MdWorkload:
+    rng = np.random.default_rng(seed)
+    hs = np.asarray(heights, dtype=np.int32)
+    ws = np.asarray(widths, dtype=np.int32)
+    return _md_draw(rng, name, num_directions, input_size, hidden_size, hs, ws, weight_range, x_dist, forget_bias)
+
+
+def _md_draw(rng, name, nd, D, H, hs, ws, wr, x_dist, forget_bias=0.0) -> MdWorkload:
+    N = int((hs.astype(np.int64) * ws).sum())
+    if x_dist == "uniform01":
+        x = rng.uniform(0.0, 1.0, (N, D))
+    else:
+        x = rng.standard_normal((N, D))
+    keys = ("W", "U1", "U2", "b", "peep")
+    shapes = {"W": (5 * H, D), "U1": (5 * H, H), "U2": (5 * H, H), "b": (5 * H,), "peep": (6, H)}
+    per = {k: [] for k in keys}
+    for _ in range(nd):
+        for k in keys:
+            per[k].append(rng.uniform(-wr, wr, shapes[k]))
+    layer = {k: np.stack(v) for k, v in per.items()}
+    layer["b"][:, H:3 * H] += forget_bias              # the two forget gates' blocks
+    layer = {k: v.astype(np.float32) for k, v in layer.items()}
+    G = rng.standard_normal((N, nd * H))
+    return MdWorkload(name, hs, ws, x.astype(np.float32), layer, G.astype(np.float32), nd, D, H)
+
+
+def md_workload(name: str = "words", seed: int | None = None, batch: int | None = None) -> MdWorkload:
+    spec = MD_WORKLOADS[name]
+    rng = np.random.default_rng(4242 if seed is None else seed)
+    n = spec.batch if batch is None else int(batch)
+    hs = rng.integers(spec.heights[1], spec.heights[2] + 1, n).astype(np.int32)
+    ws = rng.integers(spec.widths[1], spec.widths[2] + 1, n).astype(np.int32)
+    return _md_draw(rng, spec.name, spec.num_directions, spec.input_size, spec.hidden_size, hs, ws,
+                    spec.weight_range, spec.x_dist, spec.forget_bias)

@@ -130,3 +130,39 @@ def test_wide_persistent_kernels_timeout_is_reported_and_context_survives(mode):
     y, dx = stack.step(x, G)
     assert plan.poll() == _lib.LSTM_OK
     assert torch.equal(y, y_ref) and torch.equal(dx, dx_ref)
+
+
+def test_md_layer_timeout_is_reported_and_context_survives():
+    """The 2-D MDLSTM walk waits at a grid barrier between steps.  With the test hook one CTA
+    never arrives at the first barrier: every CTA's bounded wait runs out, LSTM_ERR_TIMEOUT is
+    reported for the forward and the backward walk, and a clean rerun in the same context
+    gives the reference results bit for bit."""
+    from padding_free_variable_gb300 import _lib, ops, synthetic
+    w = synthetic.md_custom(4, 8, 16, [5, 9, 3, 7], [11, 4, 8, 6], seed=4, weight_range=0.3)
+
+    def fresh():
+        plan = ops.MdPlan(w.heights, w.widths, 0, 4, 0)
+        return plan, ops.MdLayer(plan, w.layer, 8, 16)
+
+    x = torch.from_numpy(w.x).cuda()
+    G = torch.from_numpy(w.G).cuda()
+    ref_plan, ref = fresh()
+    y_ref = ref.forward(x).clone()
+    dx_ref = ref.backward(x, G).clone()
+    assert ref_plan.poll() == _lib.LSTM_OK
+    plan, layer = fresh()
+    plan.set_wait_limit(50_000_000)          # 50 ms
+    plan.debug_skip_arrival(3)
+    layer.forward(x)
+    assert plan.poll() == _lib.LSTM_ERR_TIMEOUT
+    plan.debug_skip_arrival(-1)
+    layer.forward(x)
+    assert plan.poll() == _lib.LSTM_OK
+    plan.debug_skip_arrival(3)
+    layer.backward(x, G)
+    assert plan.poll() == _lib.LSTM_ERR_TIMEOUT
+    plan.debug_skip_arrival(-1)
+    y = layer.forward(x)
+    dx = layer.backward(x, G)
+    assert plan.poll() == _lib.LSTM_OK
+    assert torch.equal(y, y_ref) and torch.equal(dx, dx_ref)
