@@ -30,9 +30,10 @@
 //     U1^T da of the cell that takes it as predecessor 1 plus U2^T da of the
 //     one that takes it as predecessor 2, and its state error is what those
 //     successors left for it; the gate errors overwrite the gates in place;
-//  4. dx and dW from the pixel-order gate errors, dU1 and dU2 from the
-//     cell-order gate errors against the predecessors' h (CUDA-core GEMMs,
-//     deterministic K splits), db and the six peephole sums in fixed order.
+//  4. dx = dA W from the pixel-order gate errors (CUDA-core GEMM); dW, dU1,
+//     dU2, db and the six peephole sums in one pass over each direction's
+//     cells (outer products of the gate errors with [x | h1 | h2 | 1], chunk
+//     partials added in chunk order: bitwise repeatable).
 #include <cstring>
 
 #include "gemm.cuh"
@@ -45,7 +46,6 @@ namespace {
 constexpr int kMdThreads = 256;
 constexpr int kMdMaxH = 128;                  // 4 units a lane
 constexpr size_t kMdSmemCap = 200 * 1024;     // resident recurrent weights up to this size
-constexpr int kMdMaxSplits = 1024;            // K splits allowed to the gradient reductions (K = pixels)
 
 __device__ __forceinline__ float sg_md(float v) { return __fdividef(1.0f, 1.0f + __expf(-v)); }
 __device__ __forceinline__ float th_md(float v)
@@ -131,9 +131,38 @@ __device__ __forceinline__ int64_t md_step_cells(const MdArgs& a, int k)
     return n;
 }
 
+// One cell's own operands, loaded before the barrier that precedes its step: its direction,
+// index, predecessors, pixel and input projection (none of them depends on the step before).
+template <int NU>
+struct MdCell {
+    int d = 0, q1 = -1, q2 = -1;
+    int64_t p = -1, px = 0;
+    float g[5][NU];
+};
+
+template <int NU>
+__device__ __forceinline__ void md_fetch(const MdArgs& a, int k, int64_t item, int lane, MdCell<NU>& m)
+{
+    const int H = a.H, H5 = 5 * H;
+    m.p = -1;
+    if (k >= a.steps || !md_item(a, k, item, m.d, m.p)) return;
+    m.q1 = a.pred1[m.p];
+    m.q2 = a.pred2[m.p];
+    m.px = a.src[m.p];
+    const float* gr = a.gx + (size_t)m.px * a.ndir * H5 + (size_t)m.d * H5;
+#pragma unroll
+    for (int j = 0; j < NU; ++j) {
+        const int u = lane + 32 * j;
+#pragma unroll
+        for (int g = 0; g < 5; ++g) m.g[g][j] = u < H ? __ldg(gr + g * H + u) : 0.f;
+    }
+}
+
 // Forward walk.  NU = units per lane (ceil(H / 32)); SM = U^T resident in shared memory.
+// Each warp's first cell of the next step is fetched before the barrier; the rest of a
+// step's cells fetch their operands in turn.
 template <int NU, bool SM>
-__global__ void __launch_bounds__(kMdThreads) md_fwd_kernel(MdArgs a)
+__global__ void __launch_bounds__(kMdThreads, 1) md_fwd_kernel(MdArgs a)
 {
     extern __shared__ float md_smem[];
     const int H = a.H, H5 = 5 * H;
@@ -147,15 +176,17 @@ __global__ void __launch_bounds__(kMdThreads) md_fwd_kernel(MdArgs a)
     }
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    MdCell<NU> nxt;
+    md_fetch<NU>(a, 0, gw, lane, nxt);
     for (int k = 0; k < a.steps; ++k) {
         const int64_t total = md_step_cells(a, k);
         for (int64_t item = gw; item < total; item += warps) {
-            int d;
-            int64_t p;
-            md_item(a, k, item, d, p);
-            const int q1 = a.pred1[p], q2 = a.pred2[p];
-            const int64_t px = a.src[p];
-            float h1[NU], h2[NU], s1[NU], s2[NU], acc[5][NU];
+            MdCell<NU> m;
+            if (item == gw) m = nxt;
+            else md_fetch<NU>(a, k, item, lane, m);
+            const int d = m.d, q1 = m.q1, q2 = m.q2;
+            const int64_t p = m.p, px = m.px;
+            float h1[NU], h2[NU], s1[NU], s2[NU], acc1[5][NU], acc2[5][NU];
 #pragma unroll
             for (int j = 0; j < NU; ++j) {
                 const int u = lane + 32 * j;
@@ -165,29 +196,36 @@ __global__ void __launch_bounds__(kMdThreads) md_fwd_kernel(MdArgs a)
                 h2[j] = ok && q2 >= 0 ? __ldcg(a.h + (size_t)q2 * H + u) : 0.f;
                 s2[j] = ok && q2 >= 0 ? __ldcg(a.c + (size_t)q2 * H + u) : 0.f;
 #pragma unroll
-                for (int g = 0; g < 5; ++g)
-                    acc[g][j] = ok ? __ldg(a.gx + (size_t)px * a.ndir * H5 + (size_t)d * H5 + g * H + u) : 0.f;
+                for (int g = 0; g < 5; ++g) {
+                    acc1[g][j] = m.g[g][j];
+                    acc2[g][j] = 0.f;
+                }
             }
-            // U1 h1 + U2 h2: h1[kk], h2[kk] broadcast from the lane that holds them
+            // U1 h1 and U2 h2 in separate accumulators (two short dependency chains); h1[kk],
+            // h2[kk] broadcast from the lane that holds them
             const float* U1t = UT + (size_t)d * 2 * H * H5;
             const float* U2t = U1t + (size_t)H * H5;
             if (q1 >= 0 || q2 >= 0) {
 #pragma unroll
                 for (int jj = 0; jj < NU; ++jj)
+#pragma unroll
                     for (int l = 0; l < 32; ++l) {
                         const int kk = 32 * jj + l;
-                        if (kk >= H) break;
-                        const float x1 = __shfl_sync(0xffffffffu, h1[jj], l);
-                        const float x2 = __shfl_sync(0xffffffffu, h2[jj], l);
-                        const float* r1 = U1t + (size_t)kk * H5;
-                        const float* r2 = U2t + (size_t)kk * H5;
+                        if (kk < H) {                       // (uniform across the warp)
+                            const float x1 = __shfl_sync(0xffffffffu, h1[jj], l);
+                            const float x2 = __shfl_sync(0xffffffffu, h2[jj], l);
+                            const float* r1 = U1t + (size_t)kk * H5;
+                            const float* r2 = U2t + (size_t)kk * H5;
 #pragma unroll
-                        for (int j = 0; j < NU; ++j) {
-                            const int u = lane + 32 * j;
-                            if (u < H)
+                            for (int j = 0; j < NU; ++j) {
+                                const int u = lane + 32 * j;
+                                if (u < H)
 #pragma unroll
-                                for (int g = 0; g < 5; ++g)
-                                    acc[g][j] = fmaf(r1[g * H + u], x1, fmaf(r2[g * H + u], x2, acc[g][j]));
+                                    for (int g = 0; g < 5; ++g) {
+                                        acc1[g][j] = fmaf(r1[g * H + u], x1, acc1[g][j]);
+                                        acc2[g][j] = fmaf(r2[g * H + u], x2, acc2[g][j]);
+                                    }
+                            }
                         }
                     }
             }
@@ -196,11 +234,14 @@ __global__ void __launch_bounds__(kMdThreads) md_fwd_kernel(MdArgs a)
             for (int j = 0; j < NU; ++j) {
                 const int u = lane + 32 * j;
                 if (u >= H) continue;
-                const float ig = sg_md(acc[0][j] + __ldg(pp + u) * s1[j] + __ldg(pp + H + u) * s2[j]);
-                const float f1 = sg_md(acc[1][j] + __ldg(pp + 2 * H + u) * s1[j]);
-                const float f2 = sg_md(acc[2][j] + __ldg(pp + 3 * H + u) * s2[j]);
-                const float zg = th_md(acc[3][j]);
-                const float og = sg_md(acc[4][j] + __ldg(pp + 4 * H + u) * s1[j] + __ldg(pp + 5 * H + u) * s2[j]);
+                float acc[5];
+#pragma unroll
+                for (int g = 0; g < 5; ++g) acc[g] = acc1[g][j] + acc2[g][j];
+                const float ig = sg_md(acc[0] + __ldg(pp + u) * s1[j] + __ldg(pp + H + u) * s2[j]);
+                const float f1 = sg_md(acc[1] + __ldg(pp + 2 * H + u) * s1[j]);
+                const float f2 = sg_md(acc[2] + __ldg(pp + 3 * H + u) * s2[j]);
+                const float zg = th_md(acc[3]);
+                const float og = sg_md(acc[4] + __ldg(pp + 4 * H + u) * s1[j] + __ldg(pp + 5 * H + u) * s2[j]);
                 const float cv = f1 * s1[j] + f2 * s2[j] + ig * zg;
                 const float hv = og * th_md(cv);
                 a.h[(size_t)p * H + u] = hv;
@@ -210,13 +251,14 @@ __global__ void __launch_bounds__(kMdThreads) md_fwd_kernel(MdArgs a)
                 a.y[(size_t)px * a.ndir * H + (size_t)d * H + u] = hv;
             }
         }
+        md_fetch<NU>(a, k + 1, gw, lane, nxt);            // the next step's first cell, before the barrier
         if (k + 1 < a.steps && !md_barrier(a, (unsigned)(k + 1), 0xA00000u | (unsigned)k)) return;
     }
 }
 
 // Backward walk (steps in reverse).  SM = U resident in shared memory.
 template <int NU, bool SM>
-__global__ void __launch_bounds__(kMdThreads) md_bwd_kernel(MdArgs a)
+__global__ void __launch_bounds__(kMdThreads, 1) md_bwd_kernel(MdArgs a)
 {
     extern __shared__ float md_smem[];
     const int H = a.H, H5 = 5 * H;
@@ -266,7 +308,7 @@ __global__ void __launch_bounds__(kMdThreads) md_bwd_kernel(MdArgs a)
                 for (int m = 0; m < NR; ++m)
                     for (int l = 0; l < 32; ++l) {
                         const int r = 32 * m + l;
-                        if (r >= H5) break;
+                        if (r >= H5) break;                 // (uniform across the warp)
                         const float x1 = __shfl_sync(0xffffffffu, g1[m], l);
                         const float x2 = __shfl_sync(0xffffffffu, g2[m], l);
 #pragma unroll
@@ -328,57 +370,165 @@ __global__ void md_transpose_kernel(const float* __restrict__ U1, const float* _
     }
 }
 
-// db and the peephole sums of one direction: column j < 5H -> sum of da_j; 5H + 6q + .. ->
-// peephole q of unit u: q = 0 i1 (da_i S1), 1 i2 (da_i S2), 2 f1 (da_f1 S1), 3 f2 (da_f2 S2),
-// 4 o1 (da_o S1), 5 o2 (da_o S2).  Each thread sums one column over one chunk of the
-// direction's cells in cell order; the chunks are added in chunk order (bitwise repeatable).
-__global__ void md_param_sums_kernel(const float* __restrict__ act, const float* __restrict__ c,
-                                     const int32_t* __restrict__ pred1, const int32_t* __restrict__ pred2, int H,
-                                     int64_t N, int ndir, int64_t chunk, float* __restrict__ partial)
+// Weight gradients of one direction in one pass over its cells.  Cell p contributes the outer
+// product of its gate errors da[p][5H] with its operand row v[p] = [x(pixel) | h(pred 1) |
+// h(pred 2) | 1] (D + 2H + 1 columns: dW, dU1, dU2, db), and the six peephole products
+// da_g S_d (element-wise).  A CTA takes one chunk of kMdWgCells cells, stages kMdWgTile of them
+// at a time in shared memory (gathered rows) and accumulates a register block of RB x CB
+// outputs per thread (a 16 x 16 thread grid over an output tile of 16 RB rows x 16 CB
+// columns; larger shapes walk several output tiles); every output sums its cells in cell
+// order, and the chunks are added in chunk order by md_wgrad_combine (bitwise repeatable).
+constexpr int kMdWgTile = 32;
+constexpr int kMdWgCells = 1024;
+constexpr int kMdWgRB = 10, kMdWgCB = 6;
+
+__global__ void __launch_bounds__(256) md_wgrad_kernel(const float* __restrict__ act, const float* __restrict__ h,
+                                                        const float* __restrict__ c, const float* __restrict__ x,
+                                                        const int32_t* __restrict__ src,
+                                                        const int32_t* __restrict__ pred1,
+                                                        const int32_t* __restrict__ pred2, int D, int H, int64_t N,
+                                                        float* __restrict__ partial)
 {
-    const int ncol = 11 * H;
-    const int col = blockIdx.x * blockDim.x + threadIdx.x;
-    const int d = blockIdx.z;
-    if (col >= ncol || d >= ndir) return;
-    const int64_t lo = (int64_t)blockIdx.y * chunk, hi = min(N, lo + chunk);
-    const int H5 = 5 * H;
-    float s = 0.f;
+    extern __shared__ float wg_smem[];
+    const int H5 = 5 * H, L = D + 2 * H + 1, nout = H5 * L + 6 * H;
+    const int d = blockIdx.y;
+    const int64_t lo = (int64_t)blockIdx.x * kMdWgCells, hi = min(N, lo + kMdWgCells);
     const int64_t base = (int64_t)d * N;
-    if (col < H5) {
-        for (int64_t i = lo; i < hi; ++i) s += act[(size_t)(base + i) * H5 + col];
-    } else {
-        const int q = (col - H5) / H, u = (col - H5) % H;
-        const int gate = q < 2 ? 0 : q == 2 ? 1 : q == 3 ? 2 : 4;     // i, i, f1, f2, o, o
-        const bool first = (q & 1) == 0;                               // S1 (else S2)
-        for (int64_t i = lo; i < hi; ++i) {
-            const int pr = first ? pred1[base + i] : pred2[base + i];
-            if (pr >= 0) s += act[(size_t)(base + i) * H5 + gate * H + u] * c[(size_t)pr * H + u];
+    float* sda = wg_smem;                                   // [tile][5H]
+    float* sv = sda + kMdWgTile * H5;                       // [tile][L]
+    float* ss1 = sv + kMdWgTile * L;                        // [tile][H]
+    float* ss2 = ss1 + kMdWgTile * H;
+    const int t = threadIdx.x, ty = t >> 4, tx = t & 15;
+    float* out = partial + ((size_t)d * gridDim.x + blockIdx.x) * nout;
+    const int rt_n = (H5 + 16 * kMdWgRB - 1) / (16 * kMdWgRB), ct_n = (L + 16 * kMdWgCB - 1) / (16 * kMdWgCB);
+    for (int ot = 0; ot < rt_n * ct_n; ++ot) {
+        const int r0 = (ot / ct_n) * 16 * kMdWgRB, c0 = (ot % ct_n) * 16 * kMdWgCB;
+        const bool peep_pass = ot == 0;
+        float acc[kMdWgRB][kMdWgCB];
+#pragma unroll
+        for (int i = 0; i < kMdWgRB; ++i)
+#pragma unroll
+            for (int j = 0; j < kMdWgCB; ++j) acc[i][j] = 0.f;
+        float pacc[3] = {0.f, 0.f, 0.f};                   // peephole sums: items t, t + 256, t + 512
+        for (int64_t p0 = lo; p0 < hi; p0 += kMdWgTile) {
+            const int nt = (int)min((int64_t)kMdWgTile, hi - p0);
+            __syncthreads();                                // the previous tile has been read
+            for (int i = t; i < kMdWgTile * H5; i += 256) {
+                const int k = i / H5, r = i - k * H5;
+                sda[i] = k < nt ? act[(size_t)(base + p0 + k) * H5 + r] : 0.f;
+            }
+            for (int i = t; i < kMdWgTile * L; i += 256) {
+                const int k = i / L, col = i - k * L;
+                float v = 0.f;
+                if (k < nt) {
+                    const int64_t p = base + p0 + k;
+                    if (col < D) {
+                        v = x[(size_t)src[p] * D + col];
+                    } else if (col < D + H) {
+                        const int q = pred1[p];
+                        v = q >= 0 ? h[(size_t)q * H + col - D] : 0.f;
+                    } else if (col < D + 2 * H) {
+                        const int q = pred2[p];
+                        v = q >= 0 ? h[(size_t)q * H + col - D - H] : 0.f;
+                    } else {
+                        v = 1.f;
+                    }
+                }
+                sv[i] = v;
+            }
+            if (peep_pass)
+                for (int i = t; i < kMdWgTile * H; i += 256) {
+                    const int k = i / H, u = i - k * H;
+                    float a1 = 0.f, a2 = 0.f;
+                    if (k < nt) {
+                        const int64_t p = base + p0 + k;
+                        const int q1 = pred1[p], q2 = pred2[p];
+                        a1 = q1 >= 0 ? c[(size_t)q1 * H + u] : 0.f;
+                        a2 = q2 >= 0 ? c[(size_t)q2 * H + u] : 0.f;
+                    }
+                    ss1[i] = a1;
+                    ss2[i] = a2;
+                }
+            __syncthreads();
+            for (int k = 0; k < nt; ++k) {
+                float a[kMdWgRB], v[kMdWgCB];
+#pragma unroll
+                for (int i = 0; i < kMdWgRB; ++i) {
+                    const int r = r0 + ty + 16 * i;
+                    a[i] = r < H5 ? sda[k * H5 + r] : 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < kMdWgCB; ++j) {
+                    const int col = c0 + tx + 16 * j;
+                    v[j] = col < L ? sv[k * L + col] : 0.f;
+                }
+#pragma unroll
+                for (int i = 0; i < kMdWgRB; ++i)
+#pragma unroll
+                    for (int j = 0; j < kMdWgCB; ++j) acc[i][j] = fmaf(a[i], v[j], acc[i][j]);
+            }
+            if (peep_pass)
+#pragma unroll
+                for (int m = 0; m < 3; ++m) {
+                    const int it = t + 256 * m;            // peephole q = it / H of unit it % H
+                    if (it < 6 * H) {
+                        const int q = it / H, u = it - q * H;
+                        const int gate = q < 2 ? 0 : q == 2 ? 1 : q == 3 ? 2 : 4;   // i, i, f1, f2, o, o
+                        const float* S = (q & 1) == 0 ? ss1 : ss2;
+                        for (int k = 0; k < nt; ++k) pacc[m] = fmaf(sda[k * H5 + gate * H + u], S[k * H + u], pacc[m]);
+                    }
+                }
         }
+#pragma unroll
+        for (int i = 0; i < kMdWgRB; ++i)
+#pragma unroll
+            for (int j = 0; j < kMdWgCB; ++j) {
+                const int r = r0 + ty + 16 * i, col = c0 + tx + 16 * j;
+                if (r < H5 && col < L) out[(size_t)r * L + col] = acc[i][j];
+            }
+        if (peep_pass)
+#pragma unroll
+            for (int m = 0; m < 3; ++m) {
+                const int it = t + 256 * m;
+                if (it < 6 * H) out[(size_t)H5 * L + it] = pacc[m];
+            }
     }
-    partial[((size_t)d * gridDim.y + blockIdx.y) * ncol + col] = s;
 }
 
-__global__ void md_param_sums_combine(const float* __restrict__ partial, int chunks, int H, int ndir,
-                                      float* __restrict__ db, float* __restrict__ dpeep)
+// Chunks added in order; the columns scattered to dW, dU1, dU2, db and the peepholes.
+__global__ void md_wgrad_combine(const float* __restrict__ partial, int chunks, int D, int H, int ndir,
+                                 float* __restrict__ dW, float* __restrict__ dU1, float* __restrict__ dU2,
+                                 float* __restrict__ db, float* __restrict__ dpeep)
 {
-    const int ncol = 11 * H, H5 = 5 * H;
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= ndir * ncol) return;
-    const int d = i / ncol, col = i % ncol;
+    const int H5 = 5 * H, L = D + 2 * H + 1, nout = H5 * L + 6 * H;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)ndir * nout) return;
+    const int d = (int)(i / nout), e = (int)(i - (int64_t)d * nout);
     float s = 0.f;
-    for (int k = 0; k < chunks; ++k) s += partial[((size_t)d * chunks + k) * ncol + col];
-    if (col < H5) {
-        if (db) db[(size_t)d * H5 + col] = s;
-    } else if (dpeep) {
-        dpeep[(size_t)d * 6 * H + (col - H5)] = s;
+    for (int k = 0; k < chunks; ++k) s += partial[((size_t)d * chunks + k) * nout + e];
+    if (e >= H5 * L) {
+        if (dpeep) dpeep[(size_t)d * 6 * H + (e - H5 * L)] = s;
+        return;
+    }
+    const int r = e / L, col = e - r * L;
+    if (col < D) {
+        if (dW) dW[((size_t)d * H5 + r) * D + col] = s;
+    } else if (col < D + H) {
+        if (dU1) dU1[((size_t)d * H5 + r) * H + col - D] = s;
+    } else if (col < D + 2 * H) {
+        if (dU2) dU2[((size_t)d * H5 + r) * H + col - D - H] = s;
+    } else if (db) {
+        db[(size_t)d * H5 + r] = s;
     }
 }
+
+size_t md_wgrad_smem(int D, int H) { return sizeof(float) * kMdWgTile * (5 * H + (D + 2 * H + 1) + 2 * H); }
 
 // ---------------------------------------------------------------- workspace layout
 
 struct MdLayout {
     size_t gx, h, c, act, ut, ucat, total;          // byte offsets (workspace)
-    size_t ds1, ds2, part, sums, stotal;            // byte offsets (scratch)
+    size_t ds1, ds2, part, stotal;                  // byte offsets (scratch)
     int chunks = 1;
 };
 
@@ -396,19 +546,12 @@ MdLayout md_layout(const MdPlan& p, int D, int H)
     L.ut = o; o = al256(o + 4 * nd * 2 * H5 * H);
     L.ucat = o; o = al256(o + 4 * nd * 2 * H5 * H);
     L.total = o;
-    // scratch: ds1, ds2, GEMM partials (the largest of the products), parameter-sum partials
+    // scratch: ds1, ds2, the weight gradients' chunk partials
     o = 0;
     L.ds1 = o; o = al256(o + 4 * cells * H);
     L.ds2 = o; o = al256(o + 4 * cells * H);
-    GemmDesc dw;
-    dw.M = (int)(nd * H5); dw.N = D; dw.K = (int)N; dw.k_splits = kMdMaxSplits;
-    GemmDesc du;
-    du.M = (int)H5; du.N = H; du.K = (int)N; du.k_splits = kMdMaxSplits;
-    const size_t part = std::max(gemm_partial_floats(dw, p.num_sms), gemm_partial_floats(du, p.num_sms));
-    L.part = o; o = al256(o + 4 * part);
-    const int64_t chunk = 2048;
-    L.chunks = (int)std::max<int64_t>(1, (p.pixels + chunk - 1) / chunk);
-    L.sums = o; o = al256(o + 4 * nd * (size_t)L.chunks * 11 * H);
+    L.chunks = (int)std::max<int64_t>(1, (p.pixels + kMdWgCells - 1) / kMdWgCells);
+    L.part = o; o = al256(o + 4 * nd * (size_t)L.chunks * ((size_t)H5 * (D + 2 * H + 1) + 6 * H));
     L.stotal = o;
     return L;
 }
@@ -473,56 +616,32 @@ MdArgs md_args(const MdPlan& p, int H)
 // dx = dA W, dW = dA^T x (pixel order, all directions at once); dU1, dU2 per direction; db and
 // the peephole sums.  *launched counts the kernels.
 lstm_status md_grads(const MdPlan& p, int D, int H, const lstm_md_params* prm, const float* x, const float* dap,
-                          const float* h, const float* c, const float* act, float* dx, const lstm_md_grads* grads,
-                          float* part, float* sums, int chunks, cudaStream_t s, int* launched)
+                     const float* h, const float* c, const float* act, float* dx, const lstm_md_grads* grads,
+                     float* part, int chunks, cudaStream_t s, int* launched)
 {
     const int nd = p.ndir, H5 = 5 * H;
     lstm_status st = LSTM_OK;
     if (dx) {
-        lstm::GemmDesc g;
+        GemmDesc g;
         g.M = (int)p.pixels; g.N = D; g.K = nd * H5;
         g.A = dap; g.sam = nd * H5; g.sak = 1;
         g.B = prm->W; g.sbk = D; g.sbn = 1;
         g.C = dx; g.ldc = D;
-        g.partial = part;
         if ((st = gemm_simt_run(g, p.num_sms, s)) != LSTM_OK) return st;
         *launched += 1;
     }
-    if (grads->W) {
-        lstm::GemmDesc g;
-        g.M = nd * H5; g.N = D; g.K = (int)p.pixels;
-        g.A = dap; g.sam = 1; g.sak = nd * H5;
-        g.B = x; g.sbk = D; g.sbn = 1;
-        g.C = grads->W; g.ldc = D;
-        g.k_splits = kMdMaxSplits;                       // the cap; the launcher picks the count
-        g.k_splits = gemm_choose_splits(g, p.num_sms);
-        g.partial = part;
-        if ((st = gemm_simt_run(g, p.num_sms, s)) != LSTM_OK) return st;
-        *launched += g.k_splits > 1 ? 2 : 1;
-    }
-    // dU1 / dU2 of each direction: its cells' gate errors against the predecessors' h
-    for (int d = 0; d < nd; ++d)
-        for (int w = 0; w < 2; ++w) {
-            float* dst = w == 0 ? grads->U1 : grads->U2;
-            if (!dst) continue;
-            lstm::GemmDesc g;
-            g.M = H5; g.N = H; g.K = (int)p.pixels;
-            g.A = act + (size_t)d * p.pixels * H5; g.sam = 1; g.sak = H5;
-            g.B = h; g.sbk = H; g.sbn = 1;
-            g.b_rows = (w == 0 ? p.d_pred1 : p.d_pred2) + (size_t)d * p.pixels;
-            g.C = dst + (size_t)d * H5 * H; g.ldc = H;
-            g.k_splits = kMdMaxSplits;                   // the cap; the launcher picks the count
-            g.k_splits = gemm_choose_splits(g, p.num_sms);
-            g.partial = part;
-            if ((st = gemm_simt_run(g, p.num_sms, s)) != LSTM_OK) return st;
-            *launched += g.k_splits > 1 ? 2 : 1;
+    if (grads->W || grads->U1 || grads->U2 || grads->b || grads->peep) {
+        const size_t smem = md_wgrad_smem(D, H);
+        if (cudaFuncSetAttribute(md_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return LSTM_ERR_UNSUPPORTED;
         }
-    if (grads->b || grads->peep) {
-        const int ncol = 11 * H;
-        const int64_t chunk = (p.pixels + chunks - 1) / chunks;
-        dim3 grid((ncol + 127) / 128, chunks, nd);
-        md_param_sums_kernel<<<grid, 128, 0, s>>>(act, c, p.d_pred1, p.d_pred2, H, p.pixels, nd, chunk, sums);
-        md_param_sums_combine<<<(nd * ncol + 255) / 256, 256, 0, s>>>(sums, chunks, H, nd, grads->b, grads->peep);
+        md_wgrad_kernel<<<dim3(chunks, nd), 256, smem, s>>>(act, h, c, x, p.d_src, p.d_pred1, p.d_pred2, D, H,
+                                                             p.pixels, part);
+        const int64_t nout = (int64_t)nd * (H5 * (D + 2 * H + 1) + 6 * H);
+        md_wgrad_combine<<<(unsigned)((nout + 255) / 256), 256, 0, s>>>(part, chunks, D, H, nd, grads->W, grads->U1,
+                                                                         grads->U2, grads->b, grads->peep);
         if (cudaGetLastError() != cudaSuccess) return LSTM_ERR_CUDA;
         *launched += 2;
     }
@@ -627,8 +746,7 @@ lstm_status lstm_md_bwd(const lstm_md_plan* plan, const lstm_md_shape* shape, co
     if (st != LSTM_OK) return st;
     lstm::tracer_begin(p.tracer, lstm::MD_GRADS, s);
     int launched = 0;
-    st = lstm::md_grads(p, D, H, prm, x, dap, h, c, act, dx, grads, part, (float*)(sc + L.sums), L.chunks, s,
-                        &launched);
+    st = lstm::md_grads(p, D, H, prm, x, dap, h, c, act, dx, grads, part, L.chunks, s, &launched);
     lstm::tracer_end(p.tracer, lstm::MD_GRADS, s, launched);
     return st;
 }

@@ -237,7 +237,7 @@ class MdWorkload:
 
 def md_custom(num_directions: int, input_size: int, hidden_size: int, heights, widths, seed: int,
               weight_range: float = 0.1, x_dist: str = "normal", name: str = "md-custom",
-              forget_bias: float = 0.0) -> MdWorkload:
+              forget_bias: float = -1.0) -> MdWorkload:
     rng = np.random.default_rng(seed)
     hs = np.asarray(heights, dtype=np.int32)
     ws = np.asarray(widths, dtype=np.int32)

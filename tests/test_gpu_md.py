@@ -72,17 +72,16 @@ def test_md_layer_matches_oracle(case, schedule):
 
 
 def test_schedules_compute_the_same_cells():
-    """Canvas and diagonal schedules run every cell from the same predecessors: y, dx and dW
-    (sums over pixels in pixel order) are bitwise equal; the sums over cells in cell order
-    (dU, db, dpeep) are taken in another order and agree to rounding."""
+    """Canvas and diagonal schedules run every cell from the same predecessors: y and dx (a
+    product over pixels in pixel order) are bitwise equal; the weight gradients sum over the
+    cells in cell order, which the schedule changes, and agree to rounding."""
     w = synthetic.md_custom(4, 16, 32, list(np.random.default_rng(7).integers(1, 14, 24)),
                             list(np.random.default_rng(8).integers(1, 40, 24)), seed=9, weight_range=0.3)
     a, b = run_md(w, 0), run_md(w, 1)
     assert a["plan"].steps > b["plan"].steps
     for k in ("y", "dx"):
         assert np.array_equal(a[k], b[k]), k
-    assert np.array_equal(a["grads"]["W"], b["grads"]["W"])
-    for k in ("U1", "U2", "b", "peep"):
+    for k in ("W", "U1", "U2", "b", "peep"):
         assert rel_err(a["grads"][k], b["grads"][k]) <= 1e-5, k
 
 
@@ -109,7 +108,7 @@ def test_md_workload_full_size_sampled(name):
     rows = np.concatenate([np.arange(pix_off[i], pix_off[i + 1]) for i in pick])
     G = np.zeros_like(w.G)
     G[rows] = w.G[rows]
-    gpu = run_md(w, 0, G=G)
+    gpu = run_md(w, 1, G=G)
     ref = oracle.md_layer(w.heights[pick], w.widths[pick], w.x[rows], w.layer, w.G[rows])
     sub = {"y": gpu["y"][rows], "dx": gpu["dx"][rows], "grads": gpu["grads"]}
     compare(sub, ref, f"md workload {name}")
