@@ -30,7 +30,8 @@
 //     U1^T da of the cell that takes it as predecessor 1 plus U2^T da of the
 //     one that takes it as predecessor 2, and its state error is what those
 //     successors left for it; the gate errors overwrite the gates in place;
-//  4. dx = dA W from the pixel-order gate errors (CUDA-core GEMM); dW, dU1,
+//  4. dx = dA W from the pixel-order gate errors (one thread a pixel, W in
+//     shared memory); dW, dU1,
 //     dU2, db and the six peephole sums in one pass over each direction's
 //     cells (outer products of the gate errors with [x | h1 | h2 | 1], chunk
 //     partials added in chunk order: bitwise repeatable).
@@ -398,6 +399,7 @@ __global__ void __launch_bounds__(256) md_wgrad_kernel(const float* __restrict__
     float* sv = sda + kMdWgTile * H5;                       // [tile][L]
     float* ss1 = sv + kMdWgTile * L;                        // [tile][H]
     float* ss2 = ss1 + kMdWgTile * H;
+    int* sidx = reinterpret_cast<int*>(ss2 + kMdWgTile * H);   // [3][tile]: pixel, pred 1, pred 2
     const int t = threadIdx.x, ty = t >> 4, tx = t & 15;
     float* out = partial + ((size_t)d * gridDim.x + blockIdx.x) * nout;
     const int rt_n = (H5 + 16 * kMdWgRB - 1) / (16 * kMdWgRB), ct_n = (L + 16 * kMdWgCB - 1) / (16 * kMdWgCB);
@@ -413,42 +415,33 @@ __global__ void __launch_bounds__(256) md_wgrad_kernel(const float* __restrict__
         for (int64_t p0 = lo; p0 < hi; p0 += kMdWgTile) {
             const int nt = (int)min((int64_t)kMdWgTile, hi - p0);
             __syncthreads();                                // the previous tile has been read
-            for (int i = t; i < kMdWgTile * H5; i += 256) {
-                const int k = i / H5, r = i - k * H5;
-                sda[i] = k < nt ? act[(size_t)(base + p0 + k) * H5 + r] : 0.f;
+            if (t < kMdWgTile) {                            // the tile's cells: pixel and predecessors
+                const bool live = t < nt;
+                const int64_t p = base + p0 + t;
+                sidx[t] = live ? src[p] : -1;
+                sidx[kMdWgTile + t] = live ? pred1[p] : -1;
+                sidx[2 * kMdWgTile + t] = live ? pred2[p] : -1;
             }
-            for (int i = t; i < kMdWgTile * L; i += 256) {
-                const int k = i / L, col = i - k * L;
-                float v = 0.f;
-                if (k < nt) {
-                    const int64_t p = base + p0 + k;
-                    if (col < D) {
-                        v = x[(size_t)src[p] * D + col];
-                    } else if (col < D + H) {
-                        const int q = pred1[p];
-                        v = q >= 0 ? h[(size_t)q * H + col - D] : 0.f;
-                    } else if (col < D + 2 * H) {
-                        const int q = pred2[p];
-                        v = q >= 0 ? h[(size_t)q * H + col - D - H] : 0.f;
-                    } else {
-                        v = 1.f;
+            __syncthreads();
+            // warp w gathers rows w, w + 8, ...: each row's columns by consecutive lanes
+            for (int k = t >> 5; k < kMdWgTile; k += 8) {
+                const int lane = t & 31;
+                const bool live = k < nt;
+                const int64_t p = base + p0 + k;
+                const int px = sidx[k], q1 = sidx[kMdWgTile + k], q2 = sidx[2 * kMdWgTile + k];
+                for (int r = lane; r < H5; r += 32) sda[k * H5 + r] = live ? act[(size_t)p * H5 + r] : 0.f;
+                float* vr = sv + k * L;
+                for (int col = lane; col < D; col += 32) vr[col] = live ? x[(size_t)px * D + col] : 0.f;
+                for (int u = lane; u < H; u += 32) {
+                    vr[D + u] = live && q1 >= 0 ? h[(size_t)q1 * H + u] : 0.f;
+                    vr[D + H + u] = live && q2 >= 0 ? h[(size_t)q2 * H + u] : 0.f;
+                    if (peep_pass) {
+                        ss1[k * H + u] = live && q1 >= 0 ? c[(size_t)q1 * H + u] : 0.f;
+                        ss2[k * H + u] = live && q2 >= 0 ? c[(size_t)q2 * H + u] : 0.f;
                     }
                 }
-                sv[i] = v;
+                if (lane == 0) vr[D + 2 * H] = live ? 1.f : 0.f;
             }
-            if (peep_pass)
-                for (int i = t; i < kMdWgTile * H; i += 256) {
-                    const int k = i / H, u = i - k * H;
-                    float a1 = 0.f, a2 = 0.f;
-                    if (k < nt) {
-                        const int64_t p = base + p0 + k;
-                        const int q1 = pred1[p], q2 = pred2[p];
-                        a1 = q1 >= 0 ? c[(size_t)q1 * H + u] : 0.f;
-                        a2 = q2 >= 0 ? c[(size_t)q2 * H + u] : 0.f;
-                    }
-                    ss1[i] = a1;
-                    ss2[i] = a2;
-                }
             __syncthreads();
             for (int k = 0; k < nt; ++k) {
                 float a[kMdWgRB], v[kMdWgCB];
@@ -522,7 +515,41 @@ __global__ void md_wgrad_combine(const float* __restrict__ partial, int chunks, 
     }
 }
 
-size_t md_wgrad_smem(int D, int H) { return sizeof(float) * kMdWgTile * (5 * H + (D + 2 * H + 1) + 2 * H); }
+size_t md_wgrad_smem(int D, int H)
+{
+    return sizeof(float) * kMdWgTile * (5 * H + (D + 2 * H + 1) + 2 * H) + sizeof(int) * 3 * kMdWgTile;
+}
+
+// dx[p][k] = sum over the ndir*5H gate errors of pixel p of dA[p][r] W[r][k]: one thread per
+// pixel with its D outputs in registers, W (all directions) staged in shared memory.
+template <int DK>
+__global__ void __launch_bounds__(128) md_dx_kernel(const float* __restrict__ dap, const float* __restrict__ W, int R,
+                                                     int D, int64_t N, float* __restrict__ dx)
+{
+    extern __shared__ float dx_smem[];
+    for (int i = threadIdx.x; i < R * D; i += blockDim.x) dx_smem[i] = W[i];
+    __syncthreads();
+    const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (p >= N) return;
+    float acc[DK];
+#pragma unroll
+    for (int k = 0; k < DK; ++k) acc[k] = 0.f;
+    const float4* row = reinterpret_cast<const float4*>(dap + (size_t)p * R);
+    for (int r4 = 0; r4 < R / 4; ++r4) {
+        const float4 a4 = __ldg(row + r4);
+        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float* wr = dx_smem + (size_t)(4 * r4 + e) * D;
+#pragma unroll
+            for (int k = 0; k < DK; ++k)
+                if (k < D) acc[k] = fmaf(av[e], wr[k], acc[k]);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < DK; ++k)
+        if (k < D) dx[(size_t)p * D + k] = acc[k];
+}
 
 // ---------------------------------------------------------------- workspace layout
 
@@ -622,12 +649,26 @@ lstm_status md_grads(const MdPlan& p, int D, int H, const lstm_md_params* prm, c
     const int nd = p.ndir, H5 = 5 * H;
     lstm_status st = LSTM_OK;
     if (dx) {
-        GemmDesc g;
-        g.M = (int)p.pixels; g.N = D; g.K = nd * H5;
-        g.A = dap; g.sam = nd * H5; g.sak = 1;
-        g.B = prm->W; g.sbk = D; g.sbn = 1;
-        g.C = dx; g.ldc = D;
-        if ((st = gemm_simt_run(g, p.num_sms, s)) != LSTM_OK) return st;
+        const int R = nd * H5;                         // a multiple of 4 (5H per direction, ndir 1..4: 5H*ndir)
+        const size_t wsm = sizeof(float) * (size_t)R * D;
+        const void* fn = D <= 16 ? (const void*)md_dx_kernel<16> : D <= 32 ? (const void*)md_dx_kernel<32>
+                       : D <= 64 ? (const void*)md_dx_kernel<64> : nullptr;
+        if (fn && R % 4 == 0 && wsm <= 200 * 1024 &&
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsm) == cudaSuccess) {
+            const unsigned blocks = (unsigned)((p.pixels + 127) / 128);
+            if (D <= 16) md_dx_kernel<16><<<blocks, 128, wsm, s>>>(dap, prm->W, R, D, p.pixels, dx);
+            else if (D <= 32) md_dx_kernel<32><<<blocks, 128, wsm, s>>>(dap, prm->W, R, D, p.pixels, dx);
+            else md_dx_kernel<64><<<blocks, 128, wsm, s>>>(dap, prm->W, R, D, p.pixels, dx);
+            if (cudaGetLastError() != cudaSuccess) return LSTM_ERR_CUDA;
+        } else {                                       // wide inputs: the CUDA-core GEMM
+            cudaGetLastError();
+            GemmDesc g;
+            g.M = (int)p.pixels; g.N = D; g.K = R;
+            g.A = dap; g.sam = R; g.sak = 1;
+            g.B = prm->W; g.sbk = D; g.sbn = 1;
+            g.C = dx; g.ldc = D;
+            if ((st = gemm_simt_run(g, p.num_sms, s)) != LSTM_OK) return st;
+        }
         *launched += 1;
     }
     if (grads->W || grads->U1 || grads->U2 || grads->b || grads->peep) {
