@@ -272,6 +272,8 @@ def roofline_of(kind, ms_per_step, calls_per_step, spec, rows, T, D0, peaks, rec
 KERNEL_SOURCES = {
     "rec_fwd": ("recurrent_cluster.cu", "recurrent.cu", "recurrent.cuh", "tc_ptx.cuh", "common.cuh"),
     "rec_bwd": ("recurrent_cluster.cu", "recurrent.cu", "recurrent.cuh", "tc_ptx.cuh", "common.cuh"),
+    "md_fwd": ("mdlstm.cu", "md_plan.cuh", "common.cuh"),
+    "md_bwd": ("mdlstm.cu", "md_plan.cuh", "common.cuh"),
 }
 
 
@@ -293,7 +295,7 @@ def recorded_traffic(kind: str, workload: str):
             rec = json.load(f)
     except Exception:
         return None
-    ent = rec.get(kind)
+    ent = rec.get(f"{kind}@{workload}")
     if not ent or ent.get("source_digest") != source_digest(kind) or ent.get("workload") != workload:
         return None
     return ent.get("dram_bytes_per_launch")

@@ -69,13 +69,23 @@ def test_gemm_work_and_bound_by_hand():
 
 
 def test_recorded_traffic_is_keyed_to_sources_and_workload(tmp_path, monkeypatch):
-    rec = {"rec_fwd": {"workload": "w", "dram_bytes_per_launch": 123, "source_digest": bench.source_digest("rec_fwd")}}
+    rec = {"rec_fwd@w": {"workload": "w", "dram_bytes_per_launch": 123, "source_digest": bench.source_digest("rec_fwd")}}
     (tmp_path / "profiles").mkdir()
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setattr(bench, "source_digest", lambda kind="": rec["rec_fwd"]["source_digest"])
+    monkeypatch.setattr(bench, "source_digest", lambda kind="": rec["rec_fwd@w"]["source_digest"])
     assert bench.recorded_traffic("rec_fwd", "w") == 123
     assert bench.recorded_traffic("rec_fwd", "other") is None          # another workload
     assert bench.recorded_traffic("rec_bwd", "w") is None              # nothing recorded
     monkeypatch.setattr(bench, "source_digest", lambda kind="": "changed")
     assert bench.recorded_traffic("rec_fwd", "w") is None              # the kernels changed since
+
+
+def test_md_work_counts():
+    """The 2-D phases' algorithmic flops: per cell 20 H^2 + 25 H forward (two recurrent products
+    and the cell), 20 H^2 + 40 H backward; the input projection 10 D H per pixel and direction."""
+    N, nd, D, H = 1000, 4, 16, 32
+    assert bench.md_kind_work("md_fwd", N, nd, D, H) == N * nd * (20 * H * H + 25 * H)
+    assert bench.md_kind_work("md_bwd", N, nd, D, H) == N * nd * (20 * H * H + 40 * H)
+    assert bench.md_kind_work("md_input", N, nd, D, H) == 2 * N * D * nd * 5 * H
+    assert bench.md_kind_work("nothing", N, nd, D, H) == 0.0
