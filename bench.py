@@ -270,8 +270,10 @@ def roofline_of(kind, ms_per_step, calls_per_step, spec, rows, T, D0, peaks, rec
 # the sources that define each kernel kind's device code (a recorded ncu capture stays valid
 # while these files are unchanged)
 KERNEL_SOURCES = {
-    "rec_fwd": ("recurrent_cluster.cu", "recurrent.cu", "recurrent.cuh", "tc_ptx.cuh", "common.cuh"),
-    "rec_bwd": ("recurrent_cluster.cu", "recurrent.cu", "recurrent.cuh", "tc_ptx.cuh", "common.cuh"),
+    "rec_fwd": ("recurrent_cluster.cu", "recurrent_cluster.cuh", "recurrent.cu", "recurrent.cuh", "tc_ptx.cuh",
+                "common.cuh"),
+    "rec_bwd": ("recurrent_cluster_bwd.cu", "recurrent_cluster.cuh", "recurrent.cu", "recurrent.cuh", "tc_ptx.cuh",
+                "common.cuh"),
     "md_fwd": ("mdlstm.cu", "md_plan.cuh", "common.cuh"),
     "md_bwd": ("mdlstm.cu", "md_plan.cuh", "common.cuh"),
 }

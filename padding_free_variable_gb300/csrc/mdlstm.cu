@@ -216,8 +216,8 @@ __device__ __forceinline__ void md_fwd_cell(const MdArgs& a, const float* UT, in
     if (m.q1 >= 0 || m.q2 >= 0) {
 #pragma unroll
         for (int jj = 0; jj < NU; ++jj)
-#pragma unroll
-            for (int l = 0; l < 32; ++l) {
+#pragma unroll(NU == 1 ? 32 : 4)
+            for (int l = 0; l < 32; ++l) {          // (full unroll for one unit a lane: compile time)
                 const int kk = 32 * jj + l;
                 if (kk < H) {                               // (uniform across the warp)
                     const float x1 = __shfl_sync(0xffffffffu, m.h1[jj], l);
