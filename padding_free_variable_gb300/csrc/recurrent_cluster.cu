@@ -515,7 +515,7 @@ static const void* fwd_kernel_u(bool bf16, bool bulk)
 }
 static const void* fwd_kernel(bool bf16, bool bulk, int group_rows)
 {
-    return cell_units(group_rows) == 2 ? fwd_kernel_u<2>(bf16, bulk) : fwd_kernel_u<4>(bf16, bulk);
+    return cell_units(group_rows, false) == 2 ? fwd_kernel_u<2>(bf16, bulk) : fwd_kernel_u<4>(bf16, bulk);
 }
 
 bool rec_cluster_fwd_configure(const Plan& p, int H, int ndir, bool bf16, RecConfig* out, RecArgs* lay)

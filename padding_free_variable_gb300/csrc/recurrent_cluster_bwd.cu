@@ -501,7 +501,7 @@ static const void* bwd_kernel_u(bool bf16, bool bulk)
 }
 static const void* bwd_kernel(bool bf16, bool bulk, int group_rows)
 {
-    return cell_units(group_rows) == 2 ? bwd_kernel_u<2>(bf16, bulk) : bwd_kernel_u<4>(bf16, bulk);
+    return cell_units(group_rows, true) == 2 ? bwd_kernel_u<2>(bf16, bulk) : bwd_kernel_u<4>(bf16, bulk);
 }
 
 bool rec_cluster_bwd_configure(const Plan& p, int H, int ndir, bool bf16, RecConfig* out, RecArgs* lay)
