@@ -212,7 +212,14 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
     __syncthreads();
     tc::tc_fence_after_sync();
     // tma_pre: the four gate tiles of step s2 (rows from off[t2], NBM of them; rows past the
-    // packed rows read 0), one thread, completing on pre_bar
+    // packed rows read 0), one thread, completing on pre_bar.  The tiles of step s2 + kTileAhead
+    // are brought into L2 at the same time, so that each load finds its rows there
+    auto prefetch_pre = [&](int s2) {
+        if (s2 >= Tg) return;
+        const int t2 = dir == 0 ? s2 : Tg - 1 - s2;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) tc::tma_prefetch_2d(&pre_map, dir * 4 * H + g * H + u0, s_off[t2]);
+    };
     auto issue_pre = [&](int s2, bool fence) {
         const int t2 = dir == 0 ? s2 : Tg - 1 - s2;
         if (fence) fence_proxy_async_cta();
@@ -220,9 +227,14 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_fwd_cluster_kernel(RecArgs a,
 #pragma unroll
         for (int g = 0; g < 4; ++g)
             tc::tma_load_2d(pre_tile + (size_t)g * NBM * kCU, &pre_map, pre_bar, dir * 4 * H + g * H + u0, s_off[t2]);
+        prefetch_pre(s2 + kTileAhead);
     };
     int last_tile = -1;                   // tile issuer: the last step whose tile was issued
-    if (tma_pre && threadIdx.x == kTileIssuer && Tg > 0) { issue_pre(0, true); last_tile = 0; }
+    if (tma_pre && threadIdx.x == kTileIssuer && Tg > 0) {
+        for (int s2 = 1; s2 < kTileAhead; ++s2) prefetch_pre(s2);
+        issue_pre(0, true);
+        last_tile = 0;
+    }
     cl.sync();     // every CTA of the cluster is resident before any remote write
 
     // cell item: row jq (+ RPP k), units uq .. uq + U: U units a thread, 32 / U threads a row

@@ -364,7 +364,11 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
         if (BULK) {
             if (s + 1 < Tg && !failed) {
                 // read-out into the staging, per owner: tile m, lane quarter q -> owner 4m + q,
-                // units 32q + lane of the tile, rows [0, NBs)
+                // units 32q + lane of the tile, rows [0, NBs).  The warp that wrote an owner's
+                // partial copies it to that owner at once (lane 0; warp w serves owners w, w + 8),
+                // so no CTA barrier stands between a partial and its copy
+                const uint32_t nxt = (uint32_t)(par ^ 1);
+                const uint32_t bytes = (uint32_t)step_rows(s + 1) * (uint32_t)(kCU * 4);
                 for (int pq = warp; pq < MT * 4; pq += kCT / 32) {
                     const int m = pq >> 2, q = pq & 3;
                     const int owner = 4 * m + q;
@@ -378,23 +382,19 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
 #pragma unroll
                         for (int e = 0; e < 16; ++e) dst[(size_t)(c0 + e) * kCU + lane] = v[e];
                     }
+                    if (owner != (int)rank && bytes != 0) {
+                        fence_proxy_async_cta();      // this lane's stores, visible to the copy
+                        __syncwarp();
+                        if (lane == 0)
+                            bulk_to_peer(mapa_u32(tc::smem_u32(inbox_at(nxt, rank, 0)), (uint32_t)owner),
+                                         stage + (size_t)owner * NBM * kCU, bytes,
+                                         mapa_u32(tc::smem_u32(&full_bar[nxt]), (uint32_t)owner));
+                    }
                 }
+                if (lane == 0 && warp < G) bulk_commit();
             }
             tc::tc_fence_before_sync();
-            fence_proxy_async_cta();
-            __syncthreads();
-            // lane 0 of warp w sends to owners w, w + 8 (copies issued by one warp's lanes serialise)
-            if (s + 1 < Tg && !failed && lane == 0 && warp < G) {
-                const uint32_t nxt = (uint32_t)(par ^ 1);
-                const uint32_t bytes = (uint32_t)step_rows(s + 1) * (uint32_t)(kCU * 4);
-                for (int o = warp; o < G; o += kCT / 32) {
-                    if (o == (int)rank || bytes == 0) continue;
-                    const uint32_t bar = mapa_u32(tc::smem_u32(&full_bar[nxt]), (uint32_t)o);
-                    bulk_to_peer(mapa_u32(tc::smem_u32(inbox_at(nxt, rank, 0)), (uint32_t)o),
-                                 stage + (size_t)o * NBM * kCU, bytes, bar);
-                }
-                bulk_commit();
-            }
+            __syncthreads();      // this CTA's own partial (in its next inbox) is visible to every thread
             if (!tma_opnd && s + 1 < Tg) load_own(s + 1);   // the next step's own operands
             cstamp(a, true, dir, srank, s, 3, 3);
         } else {

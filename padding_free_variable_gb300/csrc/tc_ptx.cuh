@@ -114,6 +114,14 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
 
+// Bring one box of a 2-D tensor into L2 ahead of its load (no shared memory, no barrier;
+// parts outside the tensor are skipped).  x as for the load.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- TMEM
 
 // One full warp: allocate `ncols` (power of two >= 32) columns; address to *dst.
