@@ -369,19 +369,11 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
                 // so no CTA barrier stands between a partial and its copy
                 const uint32_t nxt = (uint32_t)(par ^ 1);
                 const uint32_t bytes = (uint32_t)step_rows(s + 1) * (uint32_t)(kCU * 4);
-                for (int pq = warp; pq < MT * 4; pq += kCT / 32) {
-                    const int m = pq >> 2, q = pq & 3;
-                    const int owner = 4 * m + q;
-                    if (owner >= G) continue;
-                    // this CTA's own units go straight into its next inbox
-                    float* dst = owner == (int)rank ? inbox_at(par ^ 1, rank, 0) : stage + (size_t)owner * NBM * kCU;
-                    for (int c0 = 0; c0 < NBs; c0 += 16) {
-                        float v[16];
-                        tmem_sum_chains(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(m * nch * NBM + c0),
-                                        (uint32_t)NBM, nch, v);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) dst[(size_t)(c0 + e) * kCU + lane] = v[e];
-                    }
+                // this CTA's own units go straight into its next inbox
+                auto dst_of = [&](int owner) -> float* {
+                    return owner == (int)rank ? inbox_at(par ^ 1, rank, 0) : stage + (size_t)owner * NBM * kCU;
+                };
+                auto send = [&](int owner) {
                     if (owner != (int)rank && bytes != 0) {
                         fence_proxy_async_cta();      // this lane's stores, visible to the copy
                         __syncwarp();
@@ -389,6 +381,50 @@ __global__ void __launch_bounds__(kCT, 1) lstm_rec_bwd_cluster_kernel(RecArgs a,
                             bulk_to_peer(mapa_u32(tc::smem_u32(inbox_at(nxt, rank, 0)), (uint32_t)owner),
                                          stage + (size_t)owner * NBM * kCU, bytes,
                                          mapa_u32(tc::smem_u32(&full_bar[nxt]), (uint32_t)owner));
+                    }
+                };
+                const int o0 = warp, o1 = warp + kCT / 32;     // at most two owners a warp
+                const bool h0 = o0 < MT * 4 && o0 < G, h1 = o1 < MT * 4 && o1 < G;
+                if (NBs == 16 && MT * 4 <= 2 * (kCT / 32) && ((int)h0 + (int)h1) * nch <= 2) {
+                    // one column block and at most two accumulator loads a warp (two owners of one
+                    // chain, or one owner of two chains): all loads in flight together
+                    const uint32_t t0 = tmem + ((uint32_t)((o0 & 3) * 32) << 16) + (uint32_t)((o0 >> 2) * nch * NBM);
+                    const uint32_t t1 = tmem + ((uint32_t)((o1 & 3) * 32) << 16) + (uint32_t)((o1 >> 2) * nch * NBM);
+                    uint32_t r0[16], r1[16];
+                    if (h0) tc::tmem_ld_32x32b_x16(t0, r0);
+                    if (h1) tc::tmem_ld_32x32b_x16(t1, r1);
+                    else if (h0 && nch == 2) tc::tmem_ld_32x32b_x16(t0 + (uint32_t)NBM, r1);   // o0's second chain
+                    tc::tmem_wait_ld();
+                    if (h0) {
+                        float* dst = dst_of(o0);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            float v = __uint_as_float(r0[e]);
+                            if (nch == 2) v += __uint_as_float(r1[e]);
+                            dst[(size_t)e * kCU + lane] = v;
+                        }
+                        send(o0);
+                    }
+                    if (h1) {
+                        float* dst = dst_of(o1);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) dst[(size_t)e * kCU + lane] = __uint_as_float(r1[e]);
+                        send(o1);
+                    }
+                } else {
+                    for (int pq = warp; pq < MT * 4; pq += kCT / 32) {
+                        const int m = pq >> 2, q = pq & 3;
+                        const int owner = 4 * m + q;
+                        if (owner >= G) continue;
+                        float* dst = dst_of(owner);
+                        for (int c0 = 0; c0 < NBs; c0 += 16) {
+                            float v[16];
+                            tmem_sum_chains(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(m * nch * NBM + c0),
+                                            (uint32_t)NBM, nch, v);
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) dst[(size_t)(c0 + e) * kCU + lane] = v[e];
+                        }
+                        send(owner);
                     }
                 }
                 if (lane == 0 && warp < G) bulk_commit();
