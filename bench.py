@@ -279,13 +279,38 @@ KERNEL_SOURCES = {
 }
 
 
+def code_only(text: str) -> str:
+    """C/CUDA source without its comments and with whitespace runs collapsed: what the
+    compiler sees, so that editing a comment does not retire a measurement."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":                                   # string or character literal, kept whole
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_digest(kind: str = "") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "padding_free_variable_gb300", "csrc")
     files = KERNEL_SOURCES.get(kind) or tuple(sorted(os.listdir(csrc)))
     for f in sorted(files):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update((f + "\0" + code_only(fh.read()) + "\0").encode())
     return h.hexdigest()[:16]
 
 

@@ -28,7 +28,9 @@ namespace lstm {
 //    the TMEM read-out lands in a staging buffer laid out per owner, and one
 //    cp.async.bulk per owner copies it into the owner's inbox, completing on
 //    the owner's mbarrier of that parity (re-armed before the CTA's own copies
-//    go out, as in the forward kernel).  A source can only write parity
+//    go out, as in the forward kernel).  Warp w reads out owners w and w + 8
+//    and issues their copies itself, each right after its own stores, so no
+//    CTA barrier delays a copy.  A source can only write parity
 //    (s & 1) again for step s + 2 after it received this CTA's partials of
 //    step s + 1, which are formed after this CTA's cell of step s has read the
 //    inbox.

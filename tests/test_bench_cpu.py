@@ -81,6 +81,17 @@ def test_recorded_traffic_is_keyed_to_sources_and_workload(tmp_path, monkeypatch
     assert bench.recorded_traffic("rec_fwd", "w") is None              # the kernels changed since
 
 
+def test_source_digest_sees_code_not_comments():
+    """The digest that keys a traffic record follows what the compiler sees: a comment or a
+    whitespace change keeps it, a changed token (also inside a string literal) moves it."""
+    base = 'int f(int a) { return a + 1; }  // adds one\nconst char* s = "x // y";\n'
+    same = '/* header */\nint f(int a)\n{\n    return a + 1;   // one more\n}\nconst char* s = "x // y";\n'
+    assert bench.code_only(base) == bench.code_only(same)
+    assert bench.code_only(base) != bench.code_only(base.replace("a + 1", "a + 2"))
+    assert bench.code_only(base) != bench.code_only(base.replace('"x // y"', '"x // z"'))
+    assert "adds" not in bench.code_only(base) and "x // y" in bench.code_only(base)
+
+
 def test_md_work_counts():
     """The 2-D phases' algorithmic flops: per cell 20 H^2 + 25 H forward (two recurrent products
     and the cell), 20 H^2 + 40 H backward; the input projection 10 D H per pixel and direction."""
