@@ -29,8 +29,10 @@ constexpr unsigned long long kTeardownWaitNs = 1000000000ull;
 // the thread that issues the TMA operand tiles: lane 0 of the last warp, which never issues
 // MMAs (at most 4 issuing warps), so the tile loads do not delay the next product
 constexpr int kTileIssuer = kCT - 32;
-// steps between the L2 prefetch of a step's operand tiles and their load into shared memory
-// (the load itself is issued one step ahead; the rows mostly come from HBM)
+// forward: steps between the L2 prefetch of a step's gate tiles and their load into shared
+// memory (the load itself is issued one step ahead; the rows mostly come from HBM).  The
+// backward issues its tiles two microseconds before their use and takes no prefetch
+// (measured slower with one)
 constexpr int kTileAhead = 3;
 
 __device__ __forceinline__ float sigm_c(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
